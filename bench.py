@@ -1,0 +1,565 @@
+#!/usr/bin/env python3
+"""Benchmark of the hybrid-attention forward (CSA + HCA + sliding window) on B300.
+
+One step = one pass of the whole forward over one batch: for the default
+workload (Pro-shaped 1M-token hybrid decode, batch 4) that is, per sequence,
+a CSA layer (compress the completed block of the KV streams and of the
+indexer keys, lightning-indexer scores over 262,144 entries, top-1024, sparse
+MQA attention, sliding-window merge) and an HCA layer (compress, dense MQA
+attention over 8,192 entries, sliding-window merge).
+
+Prints ONE JSON line.  `value` is decode queries/s (or prefill tokens/s)
+with inputs resident in HBM; `e2e` is the same metric through the public
+API with the step's fresh inputs copied from pinned host memory and the
+outputs read back inside the timed region.
+
+Timing: W warm-up steps, then exactly K steps captured as one CUDA graph and
+replayed once between CUDA events; inputs rotate over enough copies that one
+pass over them touches at least 4x the L2 size.  Per-stage CUDA events inside
+the same graph give each stage's average duration.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "pro_1m_hybrid_decode"
+METRIC = "hybrid-attn decode queries/s & prefill tok/s at 1M ctx; % HBM/TC roofline"
+
+
+# ---------------------------------------------------------------- peaks
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+# -------------------------------------------------------- algorithmic bytes
+
+
+def stage_model(w):
+    """Algorithmic bytes / flops per stage per step (the minimum traffic the
+    stage's definition needs: each input read once, each output written once)."""
+    B, c, H = w.batch, w.c, w.n_h
+    bf = 2 if w.dtype.itemsize == 2 else 4
+    m = {}
+    if w.kind in ("hybrid_decode", "csa_decode"):
+        N = w.n_csa
+        m["csa_compress"] = dict(bytes=B * (4 * 2 * w.m * (c + w.c_I) * bf + c * bf + w.c_I + 4), flops=0)
+        m["csa_index_topk"] = dict(bytes=B * (N * (w.c_I + 4) + w.n_ih * (w.c_I + 8) + w.k * 4),
+                                   flops=B * N * w.n_ih * w.c_I * 2, flop_dtype="fp8")
+        m["csa_attend"] = dict(bytes=B * (w.k * (c * bf + 4) + H * c * bf + H * (c + 1) * 4),
+                               flops=B * w.k * H * c * 4, flop_dtype="bf16")
+        m["csa_swa_merge"] = dict(bytes=B * (w.n_win * c * bf + H * c * bf + H * (c + 1) * 4 + H * c * bf),
+                                  flops=B * w.n_win * H * c * 4, flop_dtype="bf16")
+    if w.kind in ("hybrid_decode", "hca_decode"):
+        Nh = w.n_hca
+        m["hca_compress"] = dict(bytes=B * (2 * w.m_hca * c * bf + c * bf), flops=0)
+        m["hca_attend"] = dict(bytes=B * (Nh * c * bf + H * c * bf + H * (c + 1) * 4), flops=B * Nh * H * c * 4,
+                               flop_dtype="bf16")
+        m["hca_swa_merge"] = dict(bytes=B * (w.n_win * c * bf + H * c * bf + H * (c + 1) * 4 + H * c * bf),
+                                  flops=B * w.n_win * H * c * 4, flop_dtype="bf16")
+    if w.kind == "csa_prefill":
+        n, N = w.n_ctx, w.n_csa
+        pairs = sum(min(N, (t + 1) // w.m) for t in range(n))  # visible (query, entry) pairs
+        sel = sum(min(w.k, (t + 1) // w.m) for t in range(n))
+        win = sum(min(w.n_win, t + 1) for t in range(n))
+        m["csa_compress"] = dict(bytes=n * 4 * (c + w.c_I) * bf + N * (c * bf + w.c_I + 4), flops=0)
+        m["csa_index_topk"] = dict(bytes=n * w.n_ih * (w.c_I + 8) + N * (w.c_I + 4) + n * w.k * 4,
+                                   flops=pairs * w.n_ih * w.c_I * 2, flop_dtype="fp8")
+        m["csa_attend"] = dict(bytes=n * H * c * (bf + 4) + N * c * bf + n * w.k * 4,
+                               flops=sel * H * c * 4, flop_dtype="bf16")
+        m["csa_swa_merge"] = dict(bytes=n * (c * bf + H * c * (bf + 4 + bf)), flops=win * H * c * 4,
+                                  flop_dtype="bf16")
+    return m
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the GPU is busy."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        return time.time()
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if not (t0 <= ts <= t1):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# -------------------------------------------------------------- our arm
+
+
+def run_ours(args, w):
+    import torch
+
+    from sparse_attention_gated_b300 import pipeline, workloads
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20
+
+    model = stage_model(w)
+    step_bytes = sum(v["bytes"] for v in model.values())
+    # each rank processes its own sequences (independent decode streams): different seeds
+    wr = workloads.scaled(w, seed=w.seed + 7919 * rank)
+    copies = max(1, min(16, math.ceil(4 * l2 / max(step_bytes, 1))))
+    if w.kind == "csa_prefill":
+        copies = 1  # 17 GB per copy; one step streams >> L2
+    steps = []
+    for r in range(copies):
+        x = workloads.make_inputs(workloads.scaled(wr, seed=wr.seed + 104729 * r), dev)
+        steps.append(pipeline.HybridStep(w, x))
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.Stream(device=dev)
+    stages = list(model.keys())
+
+    def run_step(st, ev=None):
+        # one forward step; ev: dict stage -> (start, end) events recorded around each stage
+        def rec(name, which):
+            if ev is not None:
+                ev[name][which].record(stream)
+
+        if st.has_csa:
+            rec("csa_compress", 0)
+            _csa_parts(st, stream, rec)
+        if st.has_hca:
+            rec("hca_compress", 0)
+            _hca_parts(st, stream, rec)
+
+    # warm-up (eager), also the first-call setup of every kernel
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            run_step(steps[i % copies])
+    stream.synchronize()
+
+    # the K timed steps as one graph, with per-stage events
+    events = [{s: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for s in stages}
+              for _ in range(args.steps)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(args.steps):
+                run_step(steps[i % copies], events[i])
+    # warm the graph (and the clocks) for about a second
+    sampler = ClockSampler(local)
+    t_busy0 = time.time()
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    t_graph = time.time() - t_busy0
+    reps = max(1, int(1.0 / max(t_graph, 1e-3)))
+    with torch.cuda.stream(stream):
+        for _ in range(min(reps, 200)):
+            g.replay()
+    stream.synchronize()
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_timed0 = time.time()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        g.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    t_timed1 = time.time()
+    clocks = sampler.stop(t_busy0, t_timed1)
+    ms_total = start.elapsed_time(end)
+    if dist is not None:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    stage_ms = {s: statistics.mean(events[i][s][0].elapsed_time(events[i][s][1]) for i in range(args.steps))
+                for s in stages}
+
+    units = w.batch if w.decode else w.n_ctx
+    value = units * world / (ms_step / 1e3)
+
+    # -------- e2e through the public API: fresh inputs from pinned host memory
+    e2e = run_e2e(args, w, steps[0], stream, units, world, dist)
+
+    # -------- roofline of the dominant stage
+    peaks, peak_kind = measured_peaks()
+    dom = max(stage_ms, key=lambda s: stage_ms[s])
+    dm = model[dom]
+    if dm["flops"] > 0 and dm.get("flop_dtype") in ("bf16", "fp8") and \
+            dm["flops"] / max(dm["bytes"], 1) > _ridge(peaks, dm.get("flop_dtype")):
+        peak = peaks["bf16_tflops_sustained"] * (2 if dm["flop_dtype"] == "fp8" else 1)
+        achieved = dm["flops"] / (stage_ms[dom] / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": None}
+    else:
+        peak = peaks["hbm_gbs"]
+        achieved = dm["bytes"] / (stage_ms[dom] / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": None}
+    roof["kernel"] = dom
+    roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
+
+    step_roof_s = max(step_bytes / (peaks["hbm_gbs"] * 1e9), 0.0)
+    out = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "queries/s" if w.decode else "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16+fp8" if w.dtype != __import__("torch").float32 else "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "context": w.n_ctx, "n_h": w.n_h, "c": w.c,
+                   "m": w.m, "m_hca": w.m_hca, "top_k": w.k, "n_ih": w.n_ih, "c_I": w.c_I, "n_win": w.n_win,
+                   "l2_defeat": f"inputs rotate over {copies} copies (>= 4x L2 per pass)" if copies > 1 else
+                   "one step streams several times the L2 size", "graph": "K steps captured as one CUDA graph"},
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": _launches_per_step(w) * args.steps,
+        "roofline": roof,
+        "stages_ms": stage_ms,
+        "step_hbm_roofline_frac": step_roof_s / (ms_step / 1e3),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, steps[0])
+    if dist is not None:
+        dist.destroy_process_group()
+    return out if rank == 0 else None
+
+
+def _ridge(peaks, dt):
+    tf = peaks["bf16_tflops_sustained"] * (2 if dt == "fp8" else 1)
+    return tf * 1e12 / (peaks["hbm_gbs"] * 1e9)
+
+
+def _csa_parts(st, stream, rec):
+    """The CSA layer's ABI calls with stage events between them (same calls as HybridStep.run_csa)."""
+    from sparse_attention_gated_b300 import ops
+
+    w, x, b = st.w, st.x, st.buf
+    kc, kI, kIs = st._csa_tensors()
+    s = st.dev_status
+    if w.decode:
+        N = w.n_csa
+        ops.hyb_compress(x["ca"], x["za"], x["bias"], w.m, cb=x["cb"], zb=x["zb"], overlap=True, first_block=N - 2,
+                         out=kc, out_row0=N - 1, dev_status=s, stream=stream)
+        ops.hyb_compress(x["kIa"], x["zIa"], x["biasI"], w.m, cb=x["kIb"], zb=x["zIb"], overlap=True,
+                         first_block=N - 2, out=kI, out_scale=kIs, out_row0=N - 1, dev_status=s, stream=stream)
+    else:
+        ops.hyb_compress(x["ca"], x["za"], x["bias"], w.m, cb=x["cb"], zb=x["zb"], overlap=True, out=kc,
+                         dev_status=s, stream=stream)
+        ops.hyb_compress(x["kIa"], x["zIa"], x["biasI"], w.m, cb=x["kIb"], zb=x["zIb"], overlap=True, out=kI,
+                         out_scale=kIs, dev_status=s, stream=stream)
+    rec("csa_compress", 1)
+    rec("csa_index_topk", 0)
+    ops.csa_index_topk(x["qI"], x["w"], kI, m=w.m, k=w.k, q_pos0=w.q_pos0, qI_scale=x.get("qI_scale"), kI_scale=kIs,
+                       idx=b["idx"], workspace=st.ws["index"], dev_status=s, stream=stream)
+    rec("csa_index_topk", 1)
+    rec("csa_attend", 0)
+    ops.csa_attend(x["q"], kc, kc, b["idx"], scale=w.scale, o=b["o"], lse=b["lse"], workspace=st.ws["csa"],
+                   dev_status=s, stream=stream)
+    rec("csa_attend", 1)
+    rec("csa_swa_merge", 0)
+    kv_pos0 = w.n_ctx - w.n_win if w.decode else 0
+    ops.swa_merge(x["q"], x["kv"], x["kv"], kv_pos0=kv_pos0, q_pos0=w.q_pos0, n_win=w.n_win, scale=w.scale,
+                  o_in=b["o"], lse_in=b["lse"], out=b["out"], dev_status=s, stream=stream)
+    rec("csa_swa_merge", 1)
+
+
+def _hca_parts(st, stream, rec):
+    from sparse_attention_gated_b300 import ops
+
+    w, x, b = st.w, st.x, st.buf
+    s = st.dev_status
+    kc = st._hca_cache()
+    q = x["q_h"] if w.kind == "hybrid_decode" else x["q"]
+    kv = x["kv_h"] if w.kind == "hybrid_decode" else x["kv"]
+    Nh = w.n_hca
+    ops.hyb_compress(x["ch"], x["zh"], x["bias_h"], w.m_hca, first_block=Nh - 1, out=kc, out_row0=Nh - 1,
+                     dev_status=s, stream=stream)
+    rec("hca_compress", 1)
+    rec("hca_attend", 0)
+    ops.hca_attend(q, kc, kc, m=w.m_hca, q_pos0=w.q_pos0, scale=w.scale, o=b["o_h"], lse=b["lse_h"],
+                   workspace=st.ws["hca"], dev_status=s, stream=stream)
+    rec("hca_attend", 1)
+    rec("hca_swa_merge", 0)
+    ops.swa_merge(q, kv, kv, kv_pos0=w.n_ctx - w.n_win, q_pos0=w.q_pos0, n_win=w.n_win, scale=w.scale,
+                  o_in=b["o_h"], lse_in=b["lse_h"], out=b["out_h"], dev_status=s, stream=stream)
+    rec("hca_swa_merge", 1)
+
+
+def _launches_per_step(w):
+    n = 0
+    if w.kind in ("hybrid_decode", "csa_decode", "csa_prefill"):
+        n += 2 + 2 + 2 + 1  # compress x2, index scores + top-k, attend (+ combine), window merge
+    if w.kind in ("hybrid_decode", "hca_decode"):
+        n += 1 + 2 + 1
+    return n
+
+
+def run_e2e(args, w, st, stream, units, world, dist):
+    """Same metric through the public API (HybridStep.run), with every step's
+    fresh inputs copied from pinned host memory and the outputs copied back."""
+    import torch
+
+    keys = st.step_input_keys()
+    host_in = {k: st.x[k].detach().cpu().pin_memory() for k in keys}
+    outs = st.output_keys()
+    host_out = {k: torch.empty(st.buf[k].shape, dtype=st.buf[k].dtype, pin_memory=True) for k in outs}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def one():
+        for k in keys:
+            st.x[k].copy_(host_in[k], non_blocking=True)
+        st.run(stream)
+        for k in outs:
+            host_out[k].copy_(st.buf[k], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            one()
+    stream.synchronize()
+    n = args.steps
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(n):
+                one()
+        g.replay()
+    stream.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        s0.record(stream)
+        g.replay()
+        s1.record(stream)
+    torch.cuda.synchronize()
+    ms = s0.elapsed_time(s1)
+    if dist is not None:
+        t = torch.tensor([ms], device=stream.device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": units * world / (ms / n / 1e3), "unit": "queries/s" if w.decode else "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / n,
+            "graph": "copies + step captured as one CUDA graph"}
+
+
+# ------------------------------------------------------------ CPU oracle
+
+
+def oracle_query(w, x, b):
+    """The float64 oracle's chain for query b of a decode workload (the
+    CPU-baseline unit of work).  x holds CPU tensors."""
+    import oracle
+
+    t = w.n_ctx - 1
+    sl = slice(b, b + 1)
+    if w.kind in ("hybrid_decode", "csa_decode"):
+        N = w.n_csa
+        oracle.compress(x["ca"][sl], x["za"][sl], x["bias"], w.m, cb=x["cb"][sl], zb=x["zb"][sl], overlap=True,
+                        first_block=N - 2)
+        kIn = oracle.compress(x["kIa"][sl], x["zIa"][sl], x["biasI"], w.m, cb=x["kIb"][sl], zb=x["zIb"][sl],
+                              overlap=True, first_block=N - 2)
+        oracle.quantise_fp8_rows(kIn.astype("float32"))
+        s = oracle.index_scores(x["qI"][sl], x["w"][sl], x["kI"][sl], m=w.m, q_pos0=t, qI_scale=x["qI_scale"][sl],
+                                kI_scale=x["kI_scale"][sl])
+        idx = oracle.topk(s, [[N]], w.k)
+        o, l = oracle.csa_attend(x["q"][sl], x["kc"][sl], x["kc"][sl], idx, w.scale)
+        oracle.swa_merge(x["q"][sl], x["kv"][sl], x["kv"][sl], w.n_ctx - w.n_win, t, w.n_win, w.scale, o, l)
+    if w.kind in ("hybrid_decode", "hca_decode"):
+        sfx = "_h" if w.kind == "hybrid_decode" else ""
+        kc = x["kc" + sfx][sl]
+        oracle.compress(x["ch"][sl], x["zh"][sl], x["bias_h"], w.m_hca, first_block=w.n_hca - 1)
+        o, l = oracle.hca_attend(x["q" + sfx][sl], kc, kc, m=w.m_hca, q_pos0=t, scale=w.scale)
+        oracle.swa_merge(x["q" + sfx][sl], x["kv" + sfx][sl], x["kv" + sfx][sl], w.n_ctx - w.n_win, t, w.n_win,
+                         w.scale, o, l)
+
+
+def oracle_prefill_rows(w, x, rows):
+    """Oracle chain of a prefill workload for the given query rows (plus the
+    full compression of the chunk).  Returns the seconds spent on the rows."""
+    import numpy as np
+
+    import oracle
+
+    ent = oracle.compress(x["ca"], x["za"], x["bias"], w.m, cb=x["cb"], zb=x["zb"], overlap=True)
+    kIf = oracle.compress(x["kIa"], x["zIa"], x["biasI"], w.m, cb=x["kIb"], zb=x["zIb"], overlap=True)
+    codes, scales = oracle.quantise_fp8_rows(kIf.astype(np.float32))
+    e = oracle.round_bf16_bits(ent)
+    t0 = time.perf_counter()
+    for j in rows:
+        js = slice(j, j + 1)
+        s = oracle.index_scores(x["qI"][:, js], x["w"][:, js], codes, m=w.m, q_pos0=j, qI_scale=x["qI_scale"][:, js],
+                                kI_scale=scales)
+        idx = oracle.topk(s, [[oracle.visible(j, w.m)]], w.k)
+        o, l = oracle.csa_attend(x["q"][:, js], e, e, idx, w.scale)
+        oracle.swa_merge(x["q"][:, js], x["kv"], x["kv"], 0, j, w.n_win, w.scale, o, l)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, st=None, budget_s=25.0):
+    """The oracle, as it stands, on one host core, on a bounded sample."""
+    import torch
+
+    from sparse_attention_gated_b300 import workloads
+
+    if st is not None:
+        x = {k: v.detach().cpu() for k, v in st.x.items()}
+    else:
+        x = workloads.make_inputs(w, "cpu")
+    if w.decode:
+        done, t0 = 0, time.perf_counter()
+        while done < w.batch and (done == 0 or time.perf_counter() - t0 < budget_s):
+            oracle_query(w, x, done)
+            done += 1
+        dt = time.perf_counter() - t0
+        return {"value": done / dt, "unit": "queries/s", "cores": 1, "kind": "oracle",
+                "sample": f"{done} of the {w.batch} decode queries of one step, whole (float64, one thread)",
+                "host_nproc": os.cpu_count()}
+    rows = sorted(set([w.n_ctx - 1] + [int(r) for r in torch.linspace(0, w.n_ctx - 1, 16).tolist()]))
+    dt = oracle_prefill_rows(w, x, rows)
+    # extrapolate per-token time linearly in the attended work of each row
+    def cost(j):
+        return min(w.k, (j + 1) // w.m) + min(w.n_win, j + 1) + (j + 1) // w.m * 0.05
+    sample_cost = sum(cost(j) for j in rows)
+    total_cost = sum(cost(j) for j in range(w.n_ctx))
+    est = dt * total_cost / sample_cost
+    return {"value": w.n_ctx / est, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{len(rows)} evenly spaced query rows of the chunk (float64, one thread), extrapolated to "
+                      f"all {w.n_ctx} rows by their attended work", "host_nproc": os.cpu_count()}
+
+
+def run_reference(args, w):
+    """The reference arm: the CPU oracle as it stands, on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    from sparse_attention_gated_b300 import workloads
+
+    x = {k: v for k, v in workloads.make_inputs(w, "cpu").items()}
+    budget = 150.0
+    if w.decode:
+        for i in range(min(args.warmup, 1)):
+            oracle_query(w, x, i % w.batch)
+        t0 = time.perf_counter()
+        done = 0
+        while done < args.steps and (done == 0 or time.perf_counter() - t0 < budget):
+            oracle_query(w, x, done % w.batch)
+            done += 1
+        dt = time.perf_counter() - t0
+        value = done / dt
+        sample = (f"{done} decode queries (one sequence per step: a CSA layer and an HCA layer, whole), "
+                  f"float64 oracle on one core; {args.steps} steps were asked, capped at {budget:.0f} s")
+        unit = "queries/s"
+        ms = dt / done * 1e3
+    else:
+        rows = sorted(set([w.n_ctx - 1] + [int(r) for r in range(0, w.n_ctx, w.n_ctx // 8)]))
+        dt = oracle_prefill_rows(w, x, rows)
+        cb = cpu_baseline(w)
+        value, unit, done, ms = cb["value"], "tokens/s", 1, w.n_ctx / cb["value"] * 1e3
+        sample = cb["sample"]
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": 1, "steps": done,
+            "warmup": min(args.warmup, 1), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "context": w.n_ctx},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    from sparse_attention_gated_b300 import workloads
+
+    w = workloads.WORKLOADS[args.workload]
+    out = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+    if out is not None:
+        print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,298 @@
+/*
+ * hyb.h -- C ABI of the B300 (sm_103a) hybrid-attention library: the
+ * DeepSeek-V4 CSA / HCA / sliding-window attention forward.
+ *
+ * Sources (web pages on DeepSeek-V4, cited by title and section):
+ *   [HA]  "DeepSeek-V4 hybrid attention: CSA, HCA, mHC, MoE" (trishampatil.com):
+ *         V.1 compression with overlap, V.2 lightning indexer, V.3 core
+ *         attention, VI heavily compressed attention.
+ *   [DV4] "DeepSeek-V4: Anatomy of an Open-Source Frontier Model"
+ *         (modernaiengineering.com): "One query in a CSA layer" steps 1-5.
+ *   [KE]  "DeepSeek-V4 Architecture From Kernels" (shivasnotes.com):
+ *         section 6 (the CSA attention contract: caller-owned buffers,
+ *         explicit sizes and scale, an int index array), section 9
+ *         (heterogeneous KV cache: tails, exact recent window).
+ *   [MA]  "Mastering DeepSeek-V4 Architecture, Course 1" (mailtotanvir.github.io):
+ *         model configurations table (m = 4, m' = 128, top-k, c = 512, c_I = 128).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - All tensor pointers are DEVICE pointers, row-major, innermost dimension
+ *    last, densely packed unless a stride field says otherwise.  The caller
+ *    allocates and frees all of them; the library keeps no pointer after the
+ *    call returns and allocates no device memory.
+ *  - Each call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and never synchronises the device.
+ *  - Scratch memory: `workspace` must hold hyb_<call>_workspace_size(args)
+ *    bytes (256-byte aligned device memory), or may be NULL when that size is
+ *    0.  The workspace's contents need not be initialised.
+ *  - Query positions: query j of every batch element sits at absolute token
+ *    position t = q_pos0 + j (queries are consecutive positions).
+ *  - Visibility ([HA] V.2: only earlier blocks are scored; [KE] section 9): a compressed
+ *    entry s built with compression factor m is visible to position t iff its
+ *    last token is <= t, i.e. s < floor((t+1)/m).  Unfinished tails are covered
+ *    by the sliding window.
+ *  - Validation is host-side and happens before any launch; an invalid
+ *    argument returns an error status and launches nothing.  Values that live
+ *    in device memory (index lists) are range-checked by the kernels: a bad
+ *    value is skipped and reported through the optional `dev_status` word
+ *    (bits HYB_DEV_*), which the kernels only ever OR into.
+ *  - Errors: HYB_ERR_INVALID_ARG (null pointer, bad size, misaligned pointer,
+ *    inconsistent dtypes), HYB_ERR_UNSUPPORTED (a valid shape for which no
+ *    kernel is compiled), HYB_ERR_WORKSPACE (workspace missing or too small),
+ *    HYB_ERR_CUDA (a launch failed; hyb_last_error() holds the CUDA message).
+ *    hyb_last_error() returns a thread-local description of the last failure.
+ */
+#ifndef HYB_H_
+#define HYB_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define HYB_API __attribute__((visibility("default")))
+#else
+#define HYB_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum hyb_status {
+  HYB_OK = 0,
+  HYB_ERR_INVALID_ARG = 1,
+  HYB_ERR_UNSUPPORTED = 2,
+  HYB_ERR_WORKSPACE = 3,
+  HYB_ERR_CUDA = 4,
+  HYB_ERR_TIMEOUT = 5
+} hyb_status;
+
+typedef enum hyb_dtype {
+  HYB_F32 = 0,   /* IEEE binary32 */
+  HYB_BF16 = 1,  /* bfloat16 (upper half of binary32) */
+  HYB_E4M3 = 2   /* OCP FP8 e4m3 (bias 7, max 448, no inf), one float32 scale per row */
+} hyb_dtype;
+
+/* bits OR-ed into *dev_status by the kernels */
+#define HYB_DEV_BAD_INDEX 0x1 /* an index list held a value outside [-1, n_entries) */
+#define HYB_DEV_TIMEOUT 0x2   /* a bounded device-side wait gave up */
+
+/* ------------------------------------------------------------------------
+ * hyb_compress -- softmax-gated compressor ([HA] V.1 for CSA, [HA] VI for HCA;
+ * [KE] section 6: a softmax over each block followed by a weighted sum).
+ *
+ * Pools each block of m consecutive token rows into one entry.  For entry i
+ * and channel ch the gate is a softmax over the rows of its window of the
+ * logits Z[row][ch] + bias[position][ch], and the entry is the gate-weighted
+ * sum of C[row][ch]:
+ *   overlap = 1 (CSA): window = stream b over block i-1 (positions 0..m-1)
+ *                      followed by stream a over block i (positions m..2m-1);
+ *                      one softmax over all 2m logits.  Block 0 has no block
+ *                      -1: its stream-b logits are -inf.
+ *   overlap = 0 (HCA): window = the m rows of block i (positions 0..m-1).
+ *
+ * Inputs ca, za (and cb, zb when overlap) are [batch][n_rows][c] of in_dtype
+ * (F32 or BF16); cb/zb must be NULL when overlap = 0.  bias is float32
+ * [overlap ? 2m : m][c].  Row r of the inputs is absolute token
+ * first_block*m + r; n_rows need not be a multiple of m (a trailing partial
+ * block is a tail and produces nothing).
+ *
+ * Output: entries for the complete blocks, except that with overlap and
+ * first_block > 0 the first block only serves as the previous block of the
+ * next one (this is the decode-append form: pass the last 2m rows and
+ * first_block = (t+1)/m - 2 to produce entry (t+1)/m - 1).  The count is
+ * hyb_compress_out_count().  Output j is written at out + (b*out_batch_stride
+ * + j)*c elements (out_batch_stride >= count; 0 means "= count"), of
+ * out_dtype: F32, BF16 (round to nearest even) or E4M3 (per-entry scale
+ * written to out_scale[b*out_batch_stride + j]: scale = amax/448 over the
+ * entry's c channels, or 1 when amax = 0; code = nearest-even e4m3 of
+ * value/scale, saturated to +-448; both divisions IEEE-rounded float32).
+ * Arithmetic: float32 softmax and accumulation.
+ * ------------------------------------------------------------------------ */
+typedef struct hyb_compress_args {
+  const void* ca;
+  const void* cb;
+  const void* za;
+  const void* zb;
+  const float* bias;
+  void* out;
+  float* out_scale;
+  int64_t batch;
+  int64_t n_rows;
+  int64_t c;
+  int64_t m;
+  int64_t first_block;
+  int64_t out_batch_stride;
+  int32_t overlap;
+  int32_t in_dtype;  /* hyb_dtype */
+  int32_t out_dtype; /* hyb_dtype */
+  int32_t* dev_status;
+} hyb_compress_args;
+
+HYB_API int64_t hyb_compress_out_count(int64_t n_rows, int64_t m, int32_t overlap, int64_t first_block);
+HYB_API size_t hyb_compress_workspace_size(const hyb_compress_args* a);
+HYB_API hyb_status hyb_compress(const hyb_compress_args* a, void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * csa_index_topk -- lightning indexer scores and top-k selection
+ * ([HA] V.2: I[t,s] = sum_h w[t,h] * ReLU(q_I[t,h] . K_I[s]); keep the top-k;
+ * [DV4] steps 2-3; the indexer runs at reduced precision).
+ *
+ * qI [batch][n_q][n_ih][c_I] and kI [batch][kv_stride][c_I] are both F32 or
+ * both E4M3 (dtype).  With E4M3 the decoded codes are multiplied by
+ * qI_scale [batch][n_q][n_ih] and kI_scale [batch][kv_stride] (float32);
+ * with F32 both scale pointers must be NULL.  w [batch][n_q][n_ih] float32.
+ * Entries 0..n_entries-1 exist; query j (position t = q_pos0 + j) scores only
+ * the visible ones, s < floor((t+1)/m), and floor((q_pos0+n_q)/m) must not
+ * exceed n_entries.
+ *
+ * Output idx [batch][n_q][k] int32: the min(k, visible) entries ranked first
+ * by (score descending, entry index ascending), written in ascending entry
+ * order and padded with -1.  Optional scores [batch][n_q][k] float32 receive
+ * the selected entries' scores in the same order (-inf for padding).
+ * Arithmetic: E4M3 products accumulated in float32 (tensor cores on
+ * sm_103a), float32 ReLU and head reduction; the ranking compares the float32
+ * scores exactly.
+ * ------------------------------------------------------------------------ */
+typedef struct hyb_index_args {
+  const void* qI;
+  const float* qI_scale;
+  const float* w;
+  const void* kI;
+  const float* kI_scale;
+  int32_t* idx;
+  float* scores;
+  int64_t batch;
+  int64_t n_q;
+  int64_t n_entries;
+  int64_t kv_stride; /* entries between batch elements of kI / kI_scale; 0 means n_entries */
+  int64_t n_ih;
+  int64_t c_I;
+  int64_t m;
+  int64_t k;
+  int64_t q_pos0;
+  int32_t dtype; /* hyb_dtype: HYB_F32 or HYB_E4M3 */
+  int32_t* dev_status;
+} hyb_index_args;
+
+HYB_API size_t csa_index_topk_workspace_size(const hyb_index_args* a);
+HYB_API hyb_status csa_index_topk(const hyb_index_args* a, void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * csa_attend -- CSA core attention over the selected entries ([HA] V.3, MQA:
+ * every head shares one compressed K and V; [KE] section 6 contract).
+ *
+ * For every head h of query (b, j):  p = softmax over the listed entries of
+ * scale * q[b][j][h] . kc[b][s];  o[b][j][h] = sum p * vc[b][s];
+ * lse[b][j][h] = natural log of the softmax denominator of the scaled scores.
+ * idx [batch][n_q][k] int32 lists the entries; -1 entries are padding.  An
+ * empty list gives o = 0 and lse = -inf.  q [batch][n_q][n_h][c]; kc, vc
+ * [batch][kv_stride][c] (vc may equal kc: in the method key = value = the
+ * compressed entries).  o float32 [batch][n_q][n_h][c], lse float32
+ * [batch][n_q][n_h].  dtype F32 or BF16 (q, kc, vc); float32 accumulation.
+ * ------------------------------------------------------------------------ */
+typedef struct hyb_csa_attend_args {
+  const void* q;
+  const void* kc;
+  const void* vc;
+  const int32_t* idx;
+  float* o;
+  float* lse;
+  int64_t batch;
+  int64_t n_q;
+  int64_t n_h;
+  int64_t c;
+  int64_t n_entries;
+  int64_t kv_stride; /* rows between batch elements of kc / vc; 0 means n_entries */
+  int64_t k;
+  float scale;
+  int32_t dtype; /* hyb_dtype */
+  int32_t* dev_status;
+} hyb_csa_attend_args;
+
+HYB_API size_t csa_attend_workspace_size(const hyb_csa_attend_args* a);
+HYB_API hyb_status csa_attend(const hyb_csa_attend_args* a, void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * hca_attend -- HCA core attention, dense over every visible entry ([HA] VI).
+ *
+ * Like csa_attend, with the entry list of query j being 0 .. V-1,
+ * V = floor((q_pos0 + j + 1)/m) (compression factor m of the HCA entries);
+ * floor((q_pos0 + n_q)/m) must not exceed n_entries.
+ * ------------------------------------------------------------------------ */
+typedef struct hyb_hca_attend_args {
+  const void* q;
+  const void* kc;
+  const void* vc;
+  float* o;
+  float* lse;
+  int64_t batch;
+  int64_t n_q;
+  int64_t n_h;
+  int64_t c;
+  int64_t n_entries;
+  int64_t kv_stride;
+  int64_t m;
+  int64_t q_pos0;
+  float scale;
+  int32_t dtype;
+  int32_t* dev_status;
+} hyb_hca_attend_args;
+
+HYB_API size_t hca_attend_workspace_size(const hyb_hca_attend_args* a);
+HYB_API hyb_status hca_attend(const hyb_hca_attend_args* a, void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * swa_merge -- sliding-window branch merged by log-sum-exp ([DV4] steps 4-5:
+ * the last n_win uncompressed tokens and the compressed entries are attended
+ * as one set; [KE] section 9: the most recent 128 tokens stay uncompressed).
+ *
+ * Query j at position t attends the raw rows at absolute positions
+ * max(0, t-n_win+1) .. t, read from kw / vw [batch][n_kv][c] whose row 0 is
+ * absolute position kv_pos0 (every needed row must lie inside the buffer).
+ * The window result (o_w, lse_w) is merged with the compressed-branch result
+ * (o_in float32 [batch][n_q][n_h][c], lse_in float32 [batch][n_q][n_h]):
+ *   L = logaddexp(lse_in, lse_w);  out = e^(lse_in-L) o_in + e^(lse_w-L) o_w,
+ * which equals one softmax over the union of both key sets.  o_in and lse_in
+ * may both be NULL (no compressed branch).  out [batch][n_q][n_h][c] of
+ * out_dtype (F32 or BF16); lse_out (optional, float32) receives L.
+ * dtype (q, kw, vw): F32 or BF16.
+ * ------------------------------------------------------------------------ */
+typedef struct hyb_swa_args {
+  const void* q;
+  const void* kw;
+  const void* vw;
+  const float* o_in;
+  const float* lse_in;
+  void* out;
+  float* lse_out;
+  int64_t batch;
+  int64_t n_q;
+  int64_t n_h;
+  int64_t c;
+  int64_t n_kv;
+  int64_t kv_pos0;
+  int64_t q_pos0;
+  int64_t n_win;
+  float scale;
+  int32_t dtype;
+  int32_t out_dtype;
+  int32_t* dev_status;
+} hyb_swa_args;
+
+HYB_API size_t swa_merge_workspace_size(const hyb_swa_args* a);
+HYB_API hyb_status swa_merge(const hyb_swa_args* a, void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ misc */
+HYB_API const char* hyb_status_string(hyb_status s);
+HYB_API const char* hyb_last_error(void);
+/* Library version and the SM architecture the kernels were built for (1030 = sm_103a). */
+HYB_API int32_t hyb_version(void);
+HYB_API int32_t hyb_built_arch(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HYB_H_ */

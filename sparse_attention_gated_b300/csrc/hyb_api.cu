@@ -1,0 +1,299 @@
+// hyb_api.cu -- the C ABI declared in include/hyb.h: host-side argument
+// validation (before any launch), workspace sizing, dispatch to the kernels
+// and error reporting.  No device memory is allocated here.
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "kernels.cuh"
+
+#ifndef HYB_BUILT_ARCH
+#define HYB_BUILT_ARCH 1030
+#endif
+
+namespace {
+
+thread_local std::string g_last_error = "";
+
+hyb_status fail(hyb_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+hyb_status ok() {
+  g_last_error.clear();
+  return HYB_OK;
+}
+
+hyb_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return ok();
+  return fail(HYB_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return a <= 1 || (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t elem_size(int32_t dt) { return dt == HYB_F32 ? 4 : dt == HYB_BF16 ? 2 : 1; }
+
+// alignment a warp-lane vector access needs: V = c/32 elements, capped at 16 bytes
+size_t lane_align(int64_t c, int32_t dt) {
+  size_t bytes = (size_t)(c / 32) * elem_size(dt);
+  return bytes >= 16 ? 16 : bytes;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int64_t n_vis_max(int64_t q_pos0, int64_t n_q, int64_t m, int64_t n_entries) {
+  if (n_q <= 0) return 0;
+  int64_t v = hyb::visible_entries(q_pos0 + n_q - 1, m);
+  return v < n_entries ? v : n_entries;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t hyb_version(void) { return 1; }
+int32_t hyb_built_arch(void) { return HYB_BUILT_ARCH; }
+
+const char* hyb_status_string(hyb_status s) {
+  switch (s) {
+    case HYB_OK: return "HYB_OK";
+    case HYB_ERR_INVALID_ARG: return "HYB_ERR_INVALID_ARG";
+    case HYB_ERR_UNSUPPORTED: return "HYB_ERR_UNSUPPORTED";
+    case HYB_ERR_WORKSPACE: return "HYB_ERR_WORKSPACE";
+    case HYB_ERR_CUDA: return "HYB_ERR_CUDA";
+    case HYB_ERR_TIMEOUT: return "HYB_ERR_TIMEOUT";
+  }
+  return "HYB_ERR_UNKNOWN";
+}
+
+const char* hyb_last_error(void) { return g_last_error.c_str(); }
+
+// ---------------------------------------------------------------- compress
+
+int64_t hyb_compress_out_count(int64_t n_rows, int64_t m, int32_t overlap, int64_t first_block) {
+  if (m <= 0 || n_rows < 0) return 0;
+  const int64_t blocks = n_rows / m;
+  const int64_t skip = (overlap && first_block > 0) ? 1 : 0;
+  return blocks > skip ? blocks - skip : 0;
+}
+
+size_t hyb_compress_workspace_size(const hyb_compress_args*) { return 0; }
+
+static hyb_status validate_compress(const hyb_compress_args* a, int64_t* n_out) {
+  if (!a) return fail(HYB_ERR_INVALID_ARG, "hyb_compress: args is NULL");
+  if (a->batch < 0 || a->n_rows < 0 || a->m < 1 || a->first_block < 0 || a->out_batch_stride < 0)
+    return fail(HYB_ERR_INVALID_ARG, "hyb_compress: negative size or m < 1");
+  if (a->overlap != 0 && a->overlap != 1) return fail(HYB_ERR_INVALID_ARG, "hyb_compress: overlap must be 0 or 1");
+  if (a->in_dtype != HYB_F32 && a->in_dtype != HYB_BF16)
+    return fail(HYB_ERR_INVALID_ARG, "hyb_compress: in_dtype must be F32 or BF16");
+  if (a->out_dtype != HYB_F32 && a->out_dtype != HYB_BF16 && a->out_dtype != HYB_E4M3)
+    return fail(HYB_ERR_INVALID_ARG, "hyb_compress: bad out_dtype");
+  if (a->c < 1) return fail(HYB_ERR_INVALID_ARG, "hyb_compress: c < 1");
+  if (!hyb::compress_shape_supported(a->c))
+    return fail(HYB_ERR_UNSUPPORTED, "hyb_compress: c = %lld not compiled (32, 64, 128, 256, 512)", (long long)a->c);
+  *n_out = hyb_compress_out_count(a->n_rows, a->m, a->overlap, a->first_block);
+  if (a->out_batch_stride != 0 && a->out_batch_stride < *n_out)
+    return fail(HYB_ERR_INVALID_ARG, "hyb_compress: out_batch_stride %lld < entries %lld",
+                (long long)a->out_batch_stride, (long long)*n_out);
+  if (!a->overlap && (a->cb || a->zb)) return fail(HYB_ERR_INVALID_ARG, "hyb_compress: cb/zb must be NULL without overlap");
+  if (*n_out == 0 || a->batch == 0) return ok();
+  if (!a->ca || !a->za || !a->bias || !a->out) return fail(HYB_ERR_INVALID_ARG, "hyb_compress: NULL ca/za/bias/out");
+  if (a->overlap && (!a->cb || !a->zb)) return fail(HYB_ERR_INVALID_ARG, "hyb_compress: overlap needs cb and zb");
+  if ((a->out_dtype == HYB_E4M3) != (a->out_scale != nullptr))
+    return fail(HYB_ERR_INVALID_ARG, "hyb_compress: out_scale is required for E4M3 output and only then");
+  const size_t ai = lane_align(a->c, a->in_dtype);
+  if (!aligned(a->ca, ai) || !aligned(a->za, ai) || (a->overlap && (!aligned(a->cb, ai) || !aligned(a->zb, ai))) ||
+      !aligned(a->bias, lane_align(a->c, HYB_F32)) || !aligned(a->out, lane_align(a->c, a->out_dtype)) ||
+      !aligned(a->out_scale, 4))
+    return fail(HYB_ERR_INVALID_ARG, "hyb_compress: misaligned pointer");
+  return ok();
+}
+
+hyb_status hyb_compress(const hyb_compress_args* a, void*, size_t, void* stream) {
+  int64_t n_out = 0;
+  hyb_status st = validate_compress(a, &n_out);
+  if (st != HYB_OK || n_out == 0 || a->batch == 0) return st;
+  return cuda_status(hyb::launch_compress(a, n_out, static_cast<cudaStream_t>(stream)), "hyb_compress launch");
+}
+
+// ---------------------------------------------------------------- index + top-k
+
+static size_t index_scores_bytes(const hyb_index_args* a) {
+  const int64_t nv = n_vis_max(a->q_pos0, a->n_q, a->m, a->n_entries);
+  return round_up((size_t)(a->batch * a->n_q) * (size_t)nv * sizeof(float), 256);
+}
+
+size_t csa_index_topk_workspace_size(const hyb_index_args* a) {
+  if (!a || a->batch <= 0 || a->n_q <= 0 || a->m < 1) return 0;
+  const int64_t nv = n_vis_max(a->q_pos0, a->n_q, a->m, a->n_entries);
+  return index_scores_bytes(a) + round_up(hyb::topk_workspace_bytes(a, nv), 256);
+}
+
+static hyb_status validate_index(const hyb_index_args* a) {
+  if (!a) return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: args is NULL");
+  if (a->batch < 0 || a->n_q < 0 || a->n_entries < 0 || a->kv_stride < 0 || a->q_pos0 < 0 || a->m < 1)
+    return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: negative size or m < 1");
+  if (a->dtype != HYB_F32 && a->dtype != HYB_E4M3)
+    return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: dtype must be F32 or E4M3");
+  if (a->k < 1 || a->n_ih < 1 || a->c_I < 1) return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: k, n_ih, c_I must be >= 1");
+  if (a->k > 2048) return fail(HYB_ERR_UNSUPPORTED, "csa_index_topk: k = %lld > 2048", (long long)a->k);
+  if (!hyb::index_cc_shape_supported(a->n_ih, a->c_I))
+    return fail(HYB_ERR_UNSUPPORTED, "csa_index_topk: n_ih = %lld / c_I = %lld not supported", (long long)a->n_ih,
+                (long long)a->c_I);
+  if (a->kv_stride != 0 && a->kv_stride < a->n_entries)
+    return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: kv_stride < n_entries");
+  if (a->n_q > 0 && hyb::visible_entries(a->q_pos0 + a->n_q - 1, a->m) > a->n_entries)
+    return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: the last query sees %lld entries but only %lld exist",
+                (long long)hyb::visible_entries(a->q_pos0 + a->n_q - 1, a->m), (long long)a->n_entries);
+  if (a->batch == 0 || a->n_q == 0) return ok();
+  if (!a->qI || !a->w || !a->idx) return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: NULL qI/w/idx");
+  if (a->n_entries > 0 && !a->kI) return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: NULL kI");
+  const bool fp8 = a->dtype == HYB_E4M3;
+  if (fp8 && (!a->qI_scale || (a->n_entries > 0 && !a->kI_scale)))
+    return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: E4M3 needs qI_scale and kI_scale");
+  if (!fp8 && (a->qI_scale || a->kI_scale))
+    return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: scales must be NULL for F32");
+  if (!aligned(a->kI, 16) || !aligned(a->qI, 4) || !aligned(a->w, 4) || !aligned(a->idx, 4) || !aligned(a->scores, 4))
+    return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: misaligned pointer (kI needs 16 bytes)");
+  return ok();
+}
+
+hyb_status csa_index_topk(const hyb_index_args* a, void* workspace, size_t ws_bytes, void* stream) {
+  hyb_status st = validate_index(a);
+  if (st != HYB_OK || a->batch == 0 || a->n_q == 0) return st;
+  const size_t need = csa_index_topk_workspace_size(a);
+  if (need > 0 && (!workspace || ws_bytes < need))
+    return fail(HYB_ERR_WORKSPACE, "csa_index_topk: workspace of %zu bytes needed, %zu given", need, ws_bytes);
+  if (!aligned(workspace, 256)) return fail(HYB_ERR_WORKSPACE, "csa_index_topk: workspace must be 256-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t nv = n_vis_max(a->q_pos0, a->n_q, a->m, a->n_entries);
+  float* scores = static_cast<float*>(workspace);
+  cudaError_t e = hyb::launch_index_scores_cc(a, scores, nv, nv, s);
+  if (e != cudaSuccess) return cuda_status(e, "csa_index_topk: index-score launch");
+  void* topk_ws = static_cast<char*>(workspace) + index_scores_bytes(a);
+  return cuda_status(hyb::launch_topk(a, scores, nv, topk_ws, s), "csa_index_topk: top-k launch");
+}
+
+// ---------------------------------------------------------------- attention
+
+static hyb::AttendJob csa_job(const hyb_csa_attend_args* a) {
+  hyb::AttendJob j{};
+  j.mode = 0, j.q = a->q, j.k = a->kc, j.v = a->vc, j.idx = a->idx, j.o = a->o, j.lse = a->lse;
+  j.batch = a->batch, j.n_q = a->n_q, j.n_h = a->n_h, j.c = a->c, j.n_entries = a->n_entries;
+  j.kv_stride = a->kv_stride > 0 ? a->kv_stride : a->n_entries;
+  j.list_len = a->k, j.scale = a->scale, j.dtype = a->dtype, j.dev_status = a->dev_status;
+  return j;
+}
+
+static hyb::AttendJob hca_job(const hyb_hca_attend_args* a) {
+  hyb::AttendJob j{};
+  j.mode = 1, j.q = a->q, j.k = a->kc, j.v = a->vc, j.o = a->o, j.lse = a->lse;
+  j.batch = a->batch, j.n_q = a->n_q, j.n_h = a->n_h, j.c = a->c, j.n_entries = a->n_entries;
+  j.kv_stride = a->kv_stride > 0 ? a->kv_stride : a->n_entries;
+  j.m = a->m, j.q_pos0 = a->q_pos0, j.scale = a->scale, j.dtype = a->dtype, j.dev_status = a->dev_status;
+  return j;
+}
+
+static hyb::AttendJob swa_job(const hyb_swa_args* a) {
+  hyb::AttendJob j{};
+  j.mode = 2, j.q = a->q, j.k = a->kw, j.v = a->vw, j.o_in = a->o_in, j.lse_in = a->lse_in, j.out = a->out;
+  j.out_bf16 = a->out_dtype == HYB_BF16, j.lse = a->lse_out;
+  j.batch = a->batch, j.n_q = a->n_q, j.n_h = a->n_h, j.c = a->c, j.n_entries = a->n_kv, j.kv_stride = a->n_kv;
+  j.kv_pos0 = a->kv_pos0, j.q_pos0 = a->q_pos0, j.n_win = a->n_win;
+  j.scale = a->scale, j.dtype = a->dtype, j.dev_status = a->dev_status;
+  return j;
+}
+
+static hyb_status validate_attend_common(const char* name, int64_t batch, int64_t n_q, int64_t n_h, int64_t c,
+                                         int32_t dtype, const void* q, const void* k, const void* v) {
+  if (batch < 0 || n_q < 0 || n_h < 0 || c < 1) return fail(HYB_ERR_INVALID_ARG, "%s: negative size or c < 1", name);
+  if (dtype != HYB_F32 && dtype != HYB_BF16) return fail(HYB_ERR_INVALID_ARG, "%s: dtype must be F32 or BF16", name);
+  if (!hyb::attend_cc_shape_supported(c, n_h))
+    return fail(HYB_ERR_UNSUPPORTED, "%s: c = %lld not compiled (32, 64, 128, 256, 512)", name, (long long)c);
+  if (batch == 0 || n_q == 0 || n_h == 0) return ok();
+  if (!q || !k || !v) return fail(HYB_ERR_INVALID_ARG, "%s: NULL q/k/v", name);
+  const size_t al = lane_align(c, dtype);
+  if (!aligned(q, al) || !aligned(k, al) || !aligned(v, al)) return fail(HYB_ERR_INVALID_ARG, "%s: misaligned q/k/v", name);
+  return ok();
+}
+
+static hyb_status run_attend(const char* name, const hyb::AttendJob& j, void* workspace, size_t ws_bytes, void* stream) {
+  const size_t need = hyb::attend_cc_workspace_bytes(j);
+  if (need > 0 && (!workspace || ws_bytes < need))
+    return fail(HYB_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", name, need, ws_bytes);
+  if (!aligned(workspace, 256)) return fail(HYB_ERR_WORKSPACE, "%s: workspace must be 256-byte aligned", name);
+  return cuda_status(hyb::launch_attend_cc(j, workspace, static_cast<cudaStream_t>(stream)), name);
+}
+
+size_t csa_attend_workspace_size(const hyb_csa_attend_args* a) {
+  if (!a || a->batch <= 0 || a->n_q <= 0 || a->n_h <= 0) return 0;
+  return hyb::attend_cc_workspace_bytes(csa_job(a));
+}
+
+hyb_status csa_attend(const hyb_csa_attend_args* a, void* workspace, size_t ws_bytes, void* stream) {
+  if (!a) return fail(HYB_ERR_INVALID_ARG, "csa_attend: args is NULL");
+  hyb_status st = validate_attend_common("csa_attend", a->batch, a->n_q, a->n_h, a->c, a->dtype, a->q, a->kc, a->vc);
+  if (st != HYB_OK) return st;
+  if (a->k < 0 || a->n_entries < 0 || a->kv_stride < 0) return fail(HYB_ERR_INVALID_ARG, "csa_attend: negative size");
+  if (a->kv_stride != 0 && a->kv_stride < a->n_entries) return fail(HYB_ERR_INVALID_ARG, "csa_attend: kv_stride < n_entries");
+  if (a->batch == 0 || a->n_q == 0 || a->n_h == 0) return ok();
+  if (!a->o || !a->lse || (a->k > 0 && !a->idx)) return fail(HYB_ERR_INVALID_ARG, "csa_attend: NULL o/lse/idx");
+  if (!aligned(a->o, lane_align(a->c, HYB_F32)) || !aligned(a->idx, 4) || !aligned(a->lse, 4))
+    return fail(HYB_ERR_INVALID_ARG, "csa_attend: misaligned o/lse/idx");
+  return run_attend("csa_attend", csa_job(a), workspace, ws_bytes, stream);
+}
+
+size_t hca_attend_workspace_size(const hyb_hca_attend_args* a) {
+  if (!a || a->batch <= 0 || a->n_q <= 0 || a->n_h <= 0 || a->m < 1) return 0;
+  return hyb::attend_cc_workspace_bytes(hca_job(a));
+}
+
+hyb_status hca_attend(const hyb_hca_attend_args* a, void* workspace, size_t ws_bytes, void* stream) {
+  if (!a) return fail(HYB_ERR_INVALID_ARG, "hca_attend: args is NULL");
+  hyb_status st = validate_attend_common("hca_attend", a->batch, a->n_q, a->n_h, a->c, a->dtype, a->q, a->kc, a->vc);
+  if (st != HYB_OK) return st;
+  if (a->m < 1 || a->q_pos0 < 0 || a->n_entries < 0 || a->kv_stride < 0)
+    return fail(HYB_ERR_INVALID_ARG, "hca_attend: m < 1 or negative size");
+  if (a->kv_stride != 0 && a->kv_stride < a->n_entries) return fail(HYB_ERR_INVALID_ARG, "hca_attend: kv_stride < n_entries");
+  if (a->n_q > 0 && hyb::visible_entries(a->q_pos0 + a->n_q - 1, a->m) > a->n_entries)
+    return fail(HYB_ERR_INVALID_ARG, "hca_attend: the last query sees %lld entries but only %lld exist",
+                (long long)hyb::visible_entries(a->q_pos0 + a->n_q - 1, a->m), (long long)a->n_entries);
+  if (a->batch == 0 || a->n_q == 0 || a->n_h == 0) return ok();
+  if (!a->o || !a->lse) return fail(HYB_ERR_INVALID_ARG, "hca_attend: NULL o/lse");
+  if (!aligned(a->o, lane_align(a->c, HYB_F32)) || !aligned(a->lse, 4))
+    return fail(HYB_ERR_INVALID_ARG, "hca_attend: misaligned o/lse");
+  return run_attend("hca_attend", hca_job(a), workspace, ws_bytes, stream);
+}
+
+size_t swa_merge_workspace_size(const hyb_swa_args*) { return 0; }
+
+hyb_status swa_merge(const hyb_swa_args* a, void* workspace, size_t ws_bytes, void* stream) {
+  if (!a) return fail(HYB_ERR_INVALID_ARG, "swa_merge: args is NULL");
+  hyb_status st = validate_attend_common("swa_merge", a->batch, a->n_q, a->n_h, a->c, a->dtype, a->q, a->kw, a->vw);
+  if (st != HYB_OK) return st;
+  if (a->n_win < 1 || a->q_pos0 < 0 || a->kv_pos0 < 0 || a->n_kv < 0)
+    return fail(HYB_ERR_INVALID_ARG, "swa_merge: n_win < 1 or negative position");
+  if (a->out_dtype != HYB_F32 && a->out_dtype != HYB_BF16)
+    return fail(HYB_ERR_INVALID_ARG, "swa_merge: out_dtype must be F32 or BF16");
+  if ((a->o_in == nullptr) != (a->lse_in == nullptr))
+    return fail(HYB_ERR_INVALID_ARG, "swa_merge: o_in and lse_in must both be given or both be NULL");
+  if (a->batch == 0 || a->n_q == 0 || a->n_h == 0) return ok();
+  const int64_t lo = a->q_pos0 - a->n_win + 1 > 0 ? a->q_pos0 - a->n_win + 1 : 0;
+  const int64_t hi = a->q_pos0 + a->n_q - 1;
+  if (lo < a->kv_pos0 || hi >= a->kv_pos0 + a->n_kv)
+    return fail(HYB_ERR_INVALID_ARG, "swa_merge: window rows %lld..%lld are not all inside the buffer %lld..%lld",
+                (long long)lo, (long long)hi, (long long)a->kv_pos0, (long long)(a->kv_pos0 + a->n_kv - 1));
+  if (!a->out) return fail(HYB_ERR_INVALID_ARG, "swa_merge: NULL out");
+  if (!aligned(a->out, lane_align(a->c, a->out_dtype)) || !aligned(a->o_in, lane_align(a->c, HYB_F32)) ||
+      !aligned(a->lse_in, 4) || !aligned(a->lse_out, 4))
+    return fail(HYB_ERR_INVALID_ARG, "swa_merge: misaligned out/o_in/lse");
+  return run_attend("swa_merge", swa_job(a), workspace, ws_bytes, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,46 @@
+// kernels.cuh -- launchers of the hybrid-attention kernels (internal to the
+// library; the public boundary is include/hyb.h).  Arguments have already
+// been validated by the C-ABI layer when these are called.
+#pragma once
+
+#include "common.cuh"
+
+namespace hyb {
+
+// compress.cu
+bool compress_shape_supported(int64_t c);
+cudaError_t launch_compress(const hyb_compress_args* a, int64_t n_out, cudaStream_t s);
+
+// indexer.cu (CUDA-core scores, any supported dtype)
+bool index_cc_shape_supported(int64_t n_ih, int64_t c_I);
+cudaError_t launch_index_scores_cc(const hyb_index_args* a, float* scores, int64_t score_stride, int64_t n_vis_max,
+                                   cudaStream_t s);
+
+// topk.cu
+size_t topk_workspace_bytes(const hyb_index_args* a, int64_t n_vis_max);
+cudaError_t launch_topk(const hyb_index_args* a, const float* scores, int64_t score_stride, void* ws, cudaStream_t s);
+
+// attend_cc.cu (CUDA-core attention for all three entry sources)
+struct AttendJob {
+  int mode;  // 0 = CSA index list, 1 = HCA visible range, 2 = sliding window + merge
+  const void* q;
+  const void* k;
+  const void* v;
+  const int32_t* idx;
+  float* o;
+  float* lse;
+  const float* o_in;
+  const float* lse_in;
+  void* out;
+  int out_bf16;
+  int64_t batch, n_q, n_h, c, n_entries, kv_stride, list_len, m, q_pos0, kv_pos0, n_win;
+  float scale;
+  int dtype;
+  int32_t* dev_status;
+};
+bool attend_cc_shape_supported(int64_t c, int64_t n_h);
+int attend_cc_splits(const AttendJob& j);
+size_t attend_cc_workspace_bytes(const AttendJob& j);
+cudaError_t launch_attend_cc(const AttendJob& j, void* ws, cudaStream_t s);
+
+}  // namespace hyb

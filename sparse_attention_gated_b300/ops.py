@@ -1,0 +1,226 @@
+"""Torch-facing binding of the C ABI: same names as include/hyb.h.
+
+Each function checks that the tensors it is given are CUDA, dense and of a
+dtype the ABI accepts, allocates outputs / workspace with torch when the
+caller does not pass them, fills the argument struct and calls the library on
+the current (or given) CUDA stream.  No arithmetic of the method happens here:
+every step runs in the library's CUDA kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from . import _abi
+
+_DT = {torch.float32: _abi.HYB_F32, torch.bfloat16: _abi.HYB_BF16, torch.float8_e4m3fn: _abi.HYB_E4M3}
+_TORCH_OF = {v: k for k, v in _DT.items()}
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to the hybrid-attention library must be CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the hybrid-attention library must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype(t):
+    try:
+        return _DT[t.dtype]
+    except KeyError:
+        raise ValueError(f"unsupported dtype {t.dtype}") from None
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _workspace(nbytes, workspace, device):
+    if nbytes == 0:
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError(f"workspace holds {workspace.numel() * workspace.element_size()} bytes, {nbytes} needed")
+    return _ptr(workspace), workspace.numel() * workspace.element_size()
+
+
+# ------------------------------------------------------------------ compress
+
+
+def compress_out_count(n_rows: int, m: int, overlap: bool, first_block: int = 0) -> int:
+    return int(_abi.load().hyb_compress_out_count(n_rows, m, int(bool(overlap)), first_block))
+
+
+def compress_args(ca, za, bias, m, cb=None, zb=None, overlap=False, first_block=0, out=None, out_scale=None,
+                  out_batch_stride=0, out_dtype=None, dev_status=None, out_row0=0):
+    """Argument struct of hyb_compress.  With out_row0 > 0 the entries are written
+    from row out_row0 of out ([B][rows][c]) on, and the batch stride is out's row count."""
+    B, n, c = ca.shape
+    a = _abi.CompressArgs()
+    a.ca, a.cb, a.za, a.zb, a.bias = _ptr(ca), _ptr(cb), _ptr(za), _ptr(zb), _ptr(bias)
+    a.out, a.out_scale = _ptr(out), _ptr(out_scale)
+    if out is not None and out_row0:
+        a.out = ctypes.c_void_p(out.data_ptr() + out_row0 * c * out.element_size())
+        if out_scale is not None:
+            a.out_scale = ctypes.c_void_p(out_scale.data_ptr() + out_row0 * out_scale.element_size())
+        out_batch_stride = out.shape[1]
+    a.batch, a.n_rows, a.c, a.m, a.first_block = B, n, c, m, first_block
+    a.out_batch_stride = out_batch_stride
+    a.overlap = int(bool(overlap))
+    a.in_dtype = _dtype(ca)
+    a.out_dtype = _dtype(out) if out is not None else _DT[out_dtype]
+    a.dev_status = _ptr(dev_status)
+    return a
+
+
+def hyb_compress(ca, za, bias, m: int, *, cb=None, zb=None, overlap: bool = False, first_block: int = 0,
+                 out=None, out_scale=None, out_dtype=None, out_batch_stride: int = 0, out_row0: int = 0,
+                 dev_status=None, stream=None):
+    """Softmax-gated compressor.  Returns (out, out_scale or None).
+
+    out_row0 writes the entries into rows out_row0.. of an existing [B][rows][c]
+    buffer (a cache slot in decode)."""
+    B, n, c = ca.shape
+    n_out = compress_out_count(n, m, overlap, first_block)
+    if out is None:
+        dt = out_dtype if out_dtype is not None else ca.dtype
+        out = torch.empty((B, n_out, c), dtype=dt, device=ca.device)
+        if dt == torch.float8_e4m3fn and out_scale is None:
+            out_scale = torch.empty((B, n_out), dtype=torch.float32, device=ca.device)
+    if out_row0 and (out_row0 + n_out > out.shape[1]):
+        raise ValueError("out_row0 + entries exceeds the rows of out")
+    a = compress_args(ca, za, bias, m, cb, zb, overlap, first_block, out, out_scale, out_batch_stride, None,
+                      dev_status, out_row0)
+    lib = _abi.load()
+    _abi.check(lib.hyb_compress(ctypes.byref(a), None, 0, _stream(stream)), "hyb_compress")
+    return out, out_scale
+
+
+# ------------------------------------------------------------- index + top-k
+
+
+def index_args(qI, w, kI, m, k, q_pos0, qI_scale=None, kI_scale=None, idx=None, scores=None, n_entries=None,
+               dev_status=None):
+    B, n_q, n_ih, c_I = qI.shape
+    a = _abi.IndexArgs()
+    a.qI, a.qI_scale, a.w, a.kI, a.kI_scale = _ptr(qI), _ptr(qI_scale), _ptr(w), _ptr(kI), _ptr(kI_scale)
+    a.idx, a.scores = _ptr(idx), _ptr(scores)
+    a.batch, a.n_q, a.n_ih, a.c_I, a.m, a.k, a.q_pos0 = B, n_q, n_ih, c_I, m, k, q_pos0
+    a.n_entries = kI.shape[1] if n_entries is None else n_entries
+    a.kv_stride = kI.shape[1]
+    a.dtype = _dtype(qI)
+    a.dev_status = _ptr(dev_status)
+    return a
+
+
+def csa_index_topk_workspace_size(a) -> int:
+    return int(_abi.load().csa_index_topk_workspace_size(ctypes.byref(a)))
+
+
+def csa_index_topk(qI, w, kI, *, m: int, k: int, q_pos0: int, qI_scale=None, kI_scale=None, n_entries=None,
+                   idx=None, scores=None, want_scores: bool = False, workspace=None, dev_status=None, stream=None):
+    """Lightning-indexer scores + top-k.  Returns idx (and the selected scores when asked)."""
+    B, n_q = qI.shape[:2]
+    if idx is None:
+        idx = torch.empty((B, n_q, k), dtype=torch.int32, device=qI.device)
+    if scores is None and want_scores:
+        scores = torch.empty((B, n_q, k), dtype=torch.float32, device=qI.device)
+    a = index_args(qI, w, kI, m, k, q_pos0, qI_scale, kI_scale, idx, scores, n_entries, dev_status)
+    ws, nbytes = _workspace(csa_index_topk_workspace_size(a), workspace, qI.device)
+    _abi.check(_abi.load().csa_index_topk(ctypes.byref(a), ws, nbytes, _stream(stream)), "csa_index_topk")
+    return (idx, scores) if want_scores else idx
+
+
+# ---------------------------------------------------------------- attention
+
+
+def csa_attend_args(q, kc, vc, idx, scale, o, lse, n_entries=None, dev_status=None):
+    B, n_q, n_h, c = q.shape
+    a = _abi.CsaAttendArgs()
+    a.q, a.kc, a.vc, a.idx, a.o, a.lse = _ptr(q), _ptr(kc), _ptr(vc), _ptr(idx), _ptr(o), _ptr(lse)
+    a.batch, a.n_q, a.n_h, a.c = B, n_q, n_h, c
+    a.n_entries = kc.shape[1] if n_entries is None else n_entries
+    a.kv_stride = kc.shape[1]
+    a.k = idx.shape[-1]
+    a.scale = scale
+    a.dtype = _dtype(q)
+    a.dev_status = _ptr(dev_status)
+    return a
+
+
+def csa_attend(q, kc, vc, idx, *, scale: float | None = None, n_entries=None, o=None, lse=None, workspace=None,
+               dev_status=None, stream=None):
+    """CSA core attention over the selected entries.  Returns (o, lse)."""
+    B, n_q, n_h, c = q.shape
+    scale = 1.0 / math.sqrt(c) if scale is None else scale
+    o = torch.empty((B, n_q, n_h, c), dtype=torch.float32, device=q.device) if o is None else o
+    lse = torch.empty((B, n_q, n_h), dtype=torch.float32, device=q.device) if lse is None else lse
+    a = csa_attend_args(q, kc, vc, idx, scale, o, lse, n_entries, dev_status)
+    lib = _abi.load()
+    ws, nbytes = _workspace(int(lib.csa_attend_workspace_size(ctypes.byref(a))), workspace, q.device)
+    _abi.check(lib.csa_attend(ctypes.byref(a), ws, nbytes, _stream(stream)), "csa_attend")
+    return o, lse
+
+
+def hca_attend_args(q, kc, vc, m, q_pos0, scale, o, lse, n_entries=None, dev_status=None):
+    B, n_q, n_h, c = q.shape
+    a = _abi.HcaAttendArgs()
+    a.q, a.kc, a.vc, a.o, a.lse = _ptr(q), _ptr(kc), _ptr(vc), _ptr(o), _ptr(lse)
+    a.batch, a.n_q, a.n_h, a.c = B, n_q, n_h, c
+    a.n_entries = kc.shape[1] if n_entries is None else n_entries
+    a.kv_stride = kc.shape[1]
+    a.m, a.q_pos0, a.scale = m, q_pos0, scale
+    a.dtype = _dtype(q)
+    a.dev_status = _ptr(dev_status)
+    return a
+
+
+def hca_attend(q, kc, vc, *, m: int, q_pos0: int, scale: float | None = None, n_entries=None, o=None, lse=None,
+               workspace=None, dev_status=None, stream=None):
+    """HCA core attention over every visible entry.  Returns (o, lse)."""
+    B, n_q, n_h, c = q.shape
+    scale = 1.0 / math.sqrt(c) if scale is None else scale
+    o = torch.empty((B, n_q, n_h, c), dtype=torch.float32, device=q.device) if o is None else o
+    lse = torch.empty((B, n_q, n_h), dtype=torch.float32, device=q.device) if lse is None else lse
+    a = hca_attend_args(q, kc, vc, m, q_pos0, scale, o, lse, n_entries, dev_status)
+    lib = _abi.load()
+    ws, nbytes = _workspace(int(lib.hca_attend_workspace_size(ctypes.byref(a))), workspace, q.device)
+    _abi.check(lib.hca_attend(ctypes.byref(a), ws, nbytes, _stream(stream)), "hca_attend")
+    return o, lse
+
+
+def swa_args(q, kw, vw, kv_pos0, q_pos0, n_win, scale, o_in, lse_in, out, lse_out, dev_status=None):
+    B, n_q, n_h, c = q.shape
+    a = _abi.SwaArgs()
+    a.q, a.kw, a.vw, a.o_in, a.lse_in, a.out, a.lse_out = (_ptr(q), _ptr(kw), _ptr(vw), _ptr(o_in), _ptr(lse_in),
+                                                           _ptr(out), _ptr(lse_out))
+    a.batch, a.n_q, a.n_h, a.c = B, n_q, n_h, c
+    a.n_kv, a.kv_pos0, a.q_pos0, a.n_win, a.scale = kw.shape[1], kv_pos0, q_pos0, n_win, scale
+    a.dtype = _dtype(q)
+    a.out_dtype = _dtype(out)
+    a.dev_status = _ptr(dev_status)
+    return a
+
+
+def swa_merge(q, kw, vw, *, kv_pos0: int, q_pos0: int, n_win: int, scale: float | None = None, o_in=None,
+              lse_in=None, out=None, out_dtype=None, lse_out=None, want_lse: bool = False, workspace=None,
+              dev_status=None, stream=None):
+    """Sliding-window branch merged with (o_in, lse_in) by log-sum-exp.  Returns out (and lse when asked)."""
+    B, n_q, n_h, c = q.shape
+    scale = 1.0 / math.sqrt(c) if scale is None else scale
+    if out is None:
+        out = torch.empty((B, n_q, n_h, c), dtype=out_dtype or q.dtype, device=q.device)
+    if lse_out is None and want_lse:
+        lse_out = torch.empty((B, n_q, n_h), dtype=torch.float32, device=q.device)
+    a = swa_args(q, kw, vw, kv_pos0, q_pos0, n_win, scale, o_in, lse_in, out, lse_out, dev_status)
+    lib = _abi.load()
+    ws, nbytes = _workspace(int(lib.swa_merge_workspace_size(ctypes.byref(a))), workspace, q.device)
+    _abi.check(lib.swa_merge(ctypes.byref(a), ws, nbytes, _stream(stream)), "swa_merge")
+    return (out, lse_out) if want_lse else out

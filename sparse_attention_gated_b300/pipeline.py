@@ -1,0 +1,145 @@
+"""One forward step of a hybrid-attention workload, every stage a library call.
+
+``HybridStep`` owns the output buffers and workspaces of a workload (allocated
+once, with torch) and runs the stages of the forward in order on one stream:
+
+  CSA layer  ("DeepSeek-V4: Anatomy..." (modernaiengineering.com), "One query
+             in a CSA layer", steps 1-5): compress the completed block(s) of
+             both the KV streams and the indexer keys, score + select top-k,
+             attend the selected entries, merge the sliding window.
+  HCA layer  ("DeepSeek-V4 hybrid attention" (trishampatil.com) section VI):
+             compress the completed block(s), attend every visible entry,
+             merge the sliding window.
+
+Decode workloads keep the compressed caches resident (state) and write the
+entry of the block that completes at this step into its cache slot; the
+query is the last context token.  Prefill / forward workloads compress the
+whole chunk and treat every position as a query.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import ops
+from .workloads import Workload
+
+
+class HybridStep:
+    def __init__(self, w: Workload, inputs: dict):
+        self.w = w
+        self.x = inputs
+        dev = inputs["q" if "q" in inputs else "q_h"].device
+        self.device = dev
+        B, c, n_h = w.batch, w.c, w.n_h
+        n_q = w.n_q
+        self.buf = {}
+        kinds_csa = w.kind in ("forward", "csa_prefill", "csa_decode", "hybrid_decode")
+        kinds_hca = w.kind in ("forward", "hca_decode", "hybrid_decode")
+        self.has_csa, self.has_hca = kinds_csa, kinds_hca
+        f32 = torch.float32
+        if kinds_csa:
+            if not w.decode:
+                N = w.n_csa
+                self.buf["entries"] = torch.empty((B, N, c), dtype=w.dtype, device=dev)
+                self.buf["kI"] = torch.empty((B, N, w.c_I), dtype=w.idx_dtype, device=dev)
+                if w.idx_dtype != f32:
+                    self.buf["kI_scale"] = torch.empty((B, N), dtype=f32, device=dev)
+            self.buf["idx"] = torch.empty((B, n_q, w.k), dtype=torch.int32, device=dev)
+            self.buf["o"] = torch.empty((B, n_q, n_h, c), dtype=f32, device=dev)
+            self.buf["lse"] = torch.empty((B, n_q, n_h), dtype=f32, device=dev)
+            self.buf["out"] = torch.empty((B, n_q, n_h, c), dtype=w.dtype, device=dev)
+        if kinds_hca:
+            if not w.decode:
+                self.buf["entries_h"] = torch.empty((B, w.n_hca, c), dtype=w.dtype, device=dev)
+            self.buf["o_h"] = torch.empty((B, n_q, n_h, c), dtype=f32, device=dev)
+            self.buf["lse_h"] = torch.empty((B, n_q, n_h), dtype=f32, device=dev)
+            self.buf["out_h"] = torch.empty((B, n_q, n_h, c), dtype=w.dtype, device=dev)
+        self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.ws = {}
+        self._size_workspaces()
+
+    # ------------------------------------------------------------ helpers
+    def _csa_tensors(self):
+        x, b = self.x, self.buf
+        if self.w.decode:
+            return x["kc"], x["kI"], x.get("kI_scale")
+        return b["entries"], b["kI"], b.get("kI_scale")
+
+    def _hca_cache(self):
+        return self.x["kc_h"] if self.w.kind == "hybrid_decode" else (
+            self.x["kc"] if self.w.kind == "hca_decode" else self.buf["entries_h"])
+
+    def _size_workspaces(self):
+        w, x, b = self.w, self.x, self.buf
+        if self.has_csa:
+            kc, kI, kIs = self._csa_tensors()
+            a = ops.index_args(x["qI"], x["w"], kI, w.m, w.k, w.q_pos0, x.get("qI_scale"), kIs, b["idx"], None)
+            n = ops.csa_index_topk_workspace_size(a)
+            self.ws["index"] = torch.empty(max(n, 1), dtype=torch.uint8, device=self.device)
+            a = ops.csa_attend_args(x["q"], kc, kc, b["idx"], w.scale, b["o"], b["lse"])
+            n = int(ops._abi.load().csa_attend_workspace_size(a))
+            self.ws["csa"] = torch.empty(max(n, 1), dtype=torch.uint8, device=self.device)
+        if self.has_hca:
+            kc = self._hca_cache()
+            q = x["q_h"] if w.kind == "hybrid_decode" else x["q"]
+            a = ops.hca_attend_args(q, kc, kc, w.m_hca, w.q_pos0, w.scale, b["o_h"], b["lse_h"])
+            n = int(ops._abi.load().hca_attend_workspace_size(a))
+            self.ws["hca"] = torch.empty(max(n, 1), dtype=torch.uint8, device=self.device)
+
+    # ------------------------------------------------------------ stages
+    def run_csa(self, stream=None):
+        w, x, b = self.w, self.x, self.buf
+        kc, kI, kIs = self._csa_tensors()
+        st = self.dev_status
+        if w.decode:
+            N = w.n_csa
+            # the block ending at the query completes entry N-1: pass blocks N-2 and N-1
+            ops.hyb_compress(x["ca"], x["za"], x["bias"], w.m, cb=x["cb"], zb=x["zb"], overlap=True,
+                             first_block=N - 2, out=kc, out_row0=N - 1, dev_status=st, stream=stream)
+            ops.hyb_compress(x["kIa"], x["zIa"], x["biasI"], w.m, cb=x["kIb"], zb=x["zIb"], overlap=True,
+                             first_block=N - 2, out=kI, out_scale=kIs, out_row0=N - 1, dev_status=st, stream=stream)
+        else:
+            ops.hyb_compress(x["ca"], x["za"], x["bias"], w.m, cb=x["cb"], zb=x["zb"], overlap=True, out=kc,
+                             dev_status=st, stream=stream)
+            ops.hyb_compress(x["kIa"], x["zIa"], x["biasI"], w.m, cb=x["kIb"], zb=x["zIb"], overlap=True, out=kI,
+                             out_scale=kIs, dev_status=st, stream=stream)
+        ops.csa_index_topk(x["qI"], x["w"], kI, m=w.m, k=w.k, q_pos0=w.q_pos0, qI_scale=x.get("qI_scale"),
+                           kI_scale=kIs, idx=b["idx"], workspace=self.ws["index"], dev_status=st, stream=stream)
+        ops.csa_attend(x["q"], kc, kc, b["idx"], scale=w.scale, o=b["o"], lse=b["lse"], workspace=self.ws["csa"],
+                       dev_status=st, stream=stream)
+        kv_pos0 = w.n_ctx - w.n_win if w.decode else 0
+        ops.swa_merge(x["q"], x["kv"], x["kv"], kv_pos0=kv_pos0, q_pos0=w.q_pos0, n_win=w.n_win, scale=w.scale,
+                      o_in=b["o"], lse_in=b["lse"], out=b["out"], dev_status=st, stream=stream)
+
+    def run_hca(self, stream=None):
+        w, x, b = self.w, self.x, self.buf
+        st = self.dev_status
+        kc = self._hca_cache()
+        q = x["q_h"] if w.kind == "hybrid_decode" else x["q"]
+        kv = x["kv_h"] if w.kind == "hybrid_decode" else x["kv"]
+        if w.decode:
+            Nh = w.n_hca
+            ops.hyb_compress(x["ch"], x["zh"], x["bias_h"], w.m_hca, first_block=Nh - 1, out=kc, out_row0=Nh - 1,
+                             dev_status=st, stream=stream)
+        else:
+            ops.hyb_compress(x["ch"], x["zh"], x["bias_h"], w.m_hca, out=kc, dev_status=st, stream=stream)
+        ops.hca_attend(q, kc, kc, m=w.m_hca, q_pos0=w.q_pos0, scale=w.scale, o=b["o_h"], lse=b["lse_h"],
+                       workspace=self.ws["hca"], dev_status=st, stream=stream)
+        kv_pos0 = w.n_ctx - w.n_win if w.decode else 0
+        ops.swa_merge(q, kv, kv, kv_pos0=kv_pos0, q_pos0=w.q_pos0, n_win=w.n_win, scale=w.scale, o_in=b["o_h"],
+                      lse_in=b["lse_h"], out=b["out_h"], dev_status=st, stream=stream)
+
+    def run(self, stream=None):
+        if self.has_csa:
+            self.run_csa(stream)
+        if self.has_hca:
+            self.run_hca(stream)
+
+    # ------------------------------------------------------------ e2e view
+    def step_input_keys(self):
+        """Inputs that arrive fresh every step (the rest is resident state: caches)."""
+        keys = [k for k in self.x if k not in ("kc", "kI", "kI_scale", "kc_h", "bias", "biasI", "bias_h")]
+        return keys
+
+    def output_keys(self):
+        return [k for k in ("out", "out_h") if k in self.buf]

@@ -1,0 +1,58 @@
+"""Shared helpers of the parity tests: tolerance checks and the top-k rule."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+# tolerances on attention outputs (max-abs), per the parity bar of the build
+TOL_F32 = 1e-4
+TOL_BF16 = 2e-2
+TOPK_GAP = 1e-3  # relative oracle score gap below which several top-k sets count as correct
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16 or t.dtype == torch.float8_e4m3fn:
+        t = t.to(torch.float64)
+    return t.numpy()
+
+
+def max_abs(a, b) -> float:
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    both_inf = np.isinf(a) & np.isinf(b) & (np.sign(a) == np.sign(b))
+    d = np.abs(np.where(both_inf, 0.0, a - b))
+    return float(np.nanmax(d)) if d.size else 0.0
+
+
+def check_topk_row(gpu_idx: np.ndarray, ref_scores: np.ndarray, visible: int, k: int, gap: float = TOPK_GAP):
+    """Top-k parity for one query row.
+
+    gpu_idx: the GPU's k indices (ascending, -1 padded).  ref_scores: the
+    oracle's float64 scores of the visible entries.  The selected set must equal
+    the oracle's where the oracle's k-th / (k+1)-th gap exceeds `gap` relative;
+    otherwise the selected minimum must be >= the excluded maximum - gap*|max|.
+    Returns "exact" or "relaxed" for reporting; raises AssertionError on failure.
+    """
+    take = min(k, visible)
+    sel = gpu_idx[:take]
+    assert (gpu_idx[take:] == -1).all(), "padding must be -1"
+    assert np.all(np.diff(sel) > 0), "indices must be strictly ascending"
+    assert sel.min() >= 0 and sel.max() < visible, "index outside the visible entries"
+    if take == visible:
+        assert np.array_equal(sel, np.arange(visible))
+        return "exact"
+    s = ref_scores[:visible]
+    order = np.lexsort((np.arange(visible), -s))  # score desc, index asc
+    ref_set = np.sort(order[:take])
+    kth, nxt = s[order[take - 1]], s[order[take]]
+    scale = max(abs(kth), abs(nxt), 1e-30)
+    if (kth - nxt) > gap * scale:
+        assert np.array_equal(sel, ref_set), "top-k set differs from the oracle's with a clear score gap"
+        return "exact"
+    mask = np.zeros(visible, dtype=bool)
+    mask[sel] = True
+    excl_max = s[~mask].max()
+    sel_min = s[mask].min()
+    assert sel_min >= excl_max - gap * max(abs(excl_max), 1e-30), "selected set violates the relaxed top-k rule"
+    return "relaxed"

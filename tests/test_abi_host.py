@@ -1,0 +1,125 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every symbol include/hyb.h declares, and rejects invalid arguments before any
+launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_attention_gated_b300 import _abi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "hyb.h")).read()
+    return set(re.findall(r"HYB_API\s+[\w\s\*]+?\b(\w+)\s*\(", text))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_abi.LIB_PATH):
+        from sparse_attention_gated_b300 import build
+
+        build.build()
+    return _abi.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared_functions()
+    assert len(declared) >= 15
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(_abi.SIGNATURES) == declared
+
+
+def test_library_reports_its_build(lib):
+    assert lib.hyb_version() >= 1
+    assert lib.hyb_built_arch() == 1030
+    assert lib.hyb_status_string(0) == b"HYB_OK"
+
+
+def test_out_count_matches_the_append_rule(lib):
+    assert lib.hyb_compress_out_count(16, 4, 1, 0) == 4
+    assert lib.hyb_compress_out_count(8, 4, 1, 5) == 1
+    assert lib.hyb_compress_out_count(8, 4, 1, 0) == 2
+    assert lib.hyb_compress_out_count(255, 4, 0, 0) == 63
+    assert lib.hyb_compress_out_count(3, 4, 1, 0) == 0
+
+
+FAKE = 1 << 20  # a well-aligned non-null address; validation fails before anything is launched
+
+
+def _compress_args(**kw):
+    a = _abi.CompressArgs()
+    a.ca = a.za = a.bias = a.out = FAKE
+    a.cb = a.zb = FAKE
+    a.batch, a.n_rows, a.c, a.m, a.overlap = 1, 16, 64, 4, 1
+    a.in_dtype, a.out_dtype = _abi.HYB_F32, _abi.HYB_F32
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("change,status", [
+    (dict(ca=None), 1), (dict(m=0), 1), (dict(overlap=2), 1), (dict(in_dtype=_abi.HYB_E4M3), 1),
+    (dict(c=48), 2), (dict(out_dtype=_abi.HYB_E4M3), 1), (dict(ca=FAKE + 4), 1), (dict(zb=None), 1),
+    (dict(out_batch_stride=2), 1), (dict(batch=-1), 1),
+])
+def test_compress_rejects_invalid_arguments(lib, change, status):
+    a = _compress_args(**change)
+    assert lib.hyb_compress(ctypes.byref(a), None, 0, None) == status
+    assert lib.hyb_last_error()
+
+
+def test_compress_with_nothing_to_do_launches_nothing(lib):
+    a = _compress_args(n_rows=3)
+    assert lib.hyb_compress(ctypes.byref(a), None, 0, None) == 0
+
+
+def _index_args(**kw):
+    a = _abi.IndexArgs()
+    a.qI = a.w = a.kI = a.idx = FAKE
+    a.batch, a.n_q, a.n_entries, a.n_ih, a.c_I, a.m, a.k, a.q_pos0 = 1, 4, 100, 4, 32, 4, 16, 0
+    a.dtype = _abi.HYB_F32
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("change,status", [
+    (dict(qI=None), 1), (dict(k=0), 1), (dict(k=4096), 2), (dict(dtype=_abi.HYB_BF16), 1),
+    (dict(q_pos0=1000), 1), (dict(c_I=24), 2), (dict(dtype=_abi.HYB_E4M3), 1), (dict(qI_scale=FAKE), 1),
+    (dict(kI=FAKE + 8), 1), (dict(kv_stride=50), 1),
+])
+def test_index_rejects_invalid_arguments(lib, change, status):
+    a = _index_args(**change)
+    assert lib.csa_index_topk(ctypes.byref(a), FAKE, 1 << 30, None) == status
+
+
+def test_index_requires_a_workspace(lib):
+    a = _index_args()
+    assert lib.csa_index_topk_workspace_size(ctypes.byref(a)) > 0
+    assert lib.csa_index_topk(ctypes.byref(a), None, 0, None) == 3
+
+
+def test_attend_and_merge_reject_invalid_arguments(lib):
+    a = _abi.CsaAttendArgs()
+    a.q = a.kc = a.vc = a.idx = a.o = a.lse = FAKE
+    a.batch, a.n_q, a.n_h, a.c, a.n_entries, a.k, a.scale, a.dtype = 1, 2, 4, 64, 10, 4, 0.1, _abi.HYB_E4M3
+    assert lib.csa_attend(ctypes.byref(a), None, 0, None) == 1
+    a.dtype = _abi.HYB_F32
+    a.c = 96
+    assert lib.csa_attend(ctypes.byref(a), None, 0, None) == 2
+    h = _abi.HcaAttendArgs()
+    h.q = h.kc = h.vc = h.o = h.lse = FAKE
+    h.batch, h.n_q, h.n_h, h.c, h.n_entries, h.m, h.q_pos0, h.dtype = 1, 1, 4, 64, 3, 16, 100, _abi.HYB_F32
+    assert lib.hca_attend(ctypes.byref(h), None, 0, None) == 1  # position 100 sees 6 entries, only 3 exist
+    s = _abi.SwaArgs()
+    s.q = s.kw = s.vw = s.out = FAKE
+    s.batch, s.n_q, s.n_h, s.c, s.n_kv, s.kv_pos0, s.q_pos0, s.n_win = 1, 1, 4, 64, 16, 100, 200, 16
+    s.dtype = s.out_dtype = _abi.HYB_F32
+    assert lib.swa_merge(ctypes.byref(s), None, 0, None) == 1  # window rows outside the buffer
+    s.kv_pos0, s.o_in = 185, FAKE
+    assert lib.swa_merge(ctypes.byref(s), None, 0, None) == 1  # o_in without lse_in

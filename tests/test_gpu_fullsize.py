@@ -1,0 +1,122 @@
+"""Full-size parity: the benchmark workloads run through HybridStep at their
+full sizes, in the launch configuration the benchmark times, checked against
+the oracle on sampled query rows (stage by stage: each oracle stage is fed the
+tensors the GPU stored for the previous one).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.helpers import TOL_BF16, check_topk_row, max_abs, to_np
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from sparse_attention_gated_b300 import pipeline, workloads
+
+DEV = "cuda"
+
+
+def _run(name):
+    w = workloads.WORKLOADS[name]
+    x = workloads.make_inputs(w, DEV)
+    cache_before = {k: x[k].clone() for k in ("kc", "kI", "kI_scale", "kc_h") if k in x}
+    step = pipeline.HybridStep(w, x)
+    step.run()
+    torch.cuda.synchronize()
+    assert step.dev_status.item() == 0
+    return w, x, step, cache_before
+
+
+def _bf16_close(got, ref):
+    return max_abs(got, ref) <= 2.0 ** -7 * max(np.abs(ref).max(), 1e-3)
+
+
+def _check_decode_csa(w, x, step, before, b):
+    sl = slice(b, b + 1)
+    cpu = lambda k: x[k][sl].cpu()
+    N = w.n_csa
+    t = w.n_ctx - 1
+    # compress: the entry of the block ending at t lands in slot N-1, nothing else changes
+    ref = oracle.compress(cpu("ca"), cpu("za"), x["bias"].cpu(), w.m, cb=cpu("cb"), zb=cpu("zb"), overlap=True,
+                          first_block=N - 2)
+    assert _bf16_close(to_np(x["kc"][b, N - 1]), ref[0, 0])
+    assert torch.equal(x["kc"][b, : N - 1], before["kc"][b, : N - 1])
+    refk = oracle.compress(cpu("kIa"), cpu("zIa"), x["biasI"].cpu(), w.m, cb=cpu("kIb"), zb=cpu("zIb"), overlap=True,
+                           first_block=N - 2)[0, 0]
+    dec = to_np(x["kI"][b, N - 1]) * x["kI_scale"][b, N - 1].item()
+    assert np.all(np.abs(dec - refk) <= np.abs(refk) * 2.0 ** -3 + x["kI_scale"][b, N - 1].item() * 2.0 ** -9)
+    # index + top-k over all N entries (the GPU's cache, including the new slot)
+    s = oracle.index_scores(cpu("qI"), cpu("w"), cpu("kI"), m=w.m, q_pos0=t, qI_scale=cpu("qI_scale"),
+                            kI_scale=cpu("kI_scale"))
+    gidx = step.buf["idx"][sl].cpu().numpy()
+    check_topk_row(gidx[0, 0], s[0, 0], N, w.k)
+    # attention with the GPU's selection, then the window merge
+    kc = cpu("kc")
+    o, l = oracle.csa_attend(cpu("q"), kc, kc, gidx, w.scale)
+    assert max_abs(to_np(step.buf["o"][sl]), o) <= TOL_BF16
+    assert max_abs(to_np(step.buf["lse"][sl]), l) <= TOL_BF16
+    out, _ = oracle.swa_merge(cpu("q"), cpu("kv"), cpu("kv"), w.n_ctx - w.n_win, t, w.n_win, w.scale, o, l)
+    assert max_abs(to_np(step.buf["out"][sl]), out) <= TOL_BF16
+
+
+def _check_decode_hca(w, x, step, before, b, sfx):
+    sl = slice(b, b + 1)
+    cpu = lambda k: x[k][sl].cpu()
+    Nh = w.n_hca
+    t = w.n_ctx - 1
+    kc_key = "kc" + sfx
+    ref = oracle.compress(cpu("ch"), cpu("zh"), x["bias_h"].cpu(), w.m_hca, first_block=Nh - 1)
+    assert _bf16_close(to_np(x[kc_key][b, Nh - 1]), ref[0, 0])
+    assert torch.equal(x[kc_key][b, : Nh - 1], before[kc_key][b, : Nh - 1])
+    kc = cpu(kc_key)
+    q = cpu("q" + sfx)
+    o, l = oracle.hca_attend(q, kc, kc, m=w.m_hca, q_pos0=t, scale=w.scale)
+    assert max_abs(to_np(step.buf["o_h"][sl]), o) <= TOL_BF16
+    out, _ = oracle.swa_merge(q, cpu("kv" + sfx), cpu("kv" + sfx), w.n_ctx - w.n_win, t, w.n_win, w.scale, o, l)
+    assert max_abs(to_np(step.buf["out_h"][sl]), out) <= TOL_BF16
+
+
+def test_flash_csa_decode_full_size():
+    w, x, step, before = _run("flash_csa_decode")
+    for b in (0, w.batch - 1):
+        _check_decode_csa(w, x, step, before, b)
+
+
+def test_flash_hca_decode_full_size():
+    w, x, step, before = _run("flash_hca_decode")
+    for b in (0, w.batch - 1):
+        _check_decode_hca(w, x, step, before, b, "")
+
+
+def test_pro_1m_hybrid_decode_full_size():
+    w, x, step, before = _run("pro_1m_hybrid_decode")
+    for b in (0, w.batch - 1):
+        _check_decode_csa(w, x, step, before, b)
+        _check_decode_hca(w, x, step, before, b, "_h")
+
+
+def test_pro_csa_prefill_full_size_sampled_rows():
+    w, x, step, _ = _run("pro_csa_prefill")
+    cpu = {k: v.cpu() for k, v in x.items()}
+    ent = oracle.compress(cpu["ca"], cpu["za"], cpu["bias"], w.m, cb=cpu["cb"], zb=cpu["zb"], overlap=True)
+    assert _bf16_close(to_np(step.buf["entries"]), ent)
+    refk = oracle.compress(cpu["kIa"], cpu["zIa"], cpu["biasI"], w.m, cb=cpu["kIb"], zb=cpu["zIb"], overlap=True)
+    sc = step.buf["kI_scale"].cpu().numpy()[..., None]
+    dec = to_np(step.buf["kI"]) * sc
+    assert np.all(np.abs(dec - refk) <= np.abs(refk) * 2.0 ** -3 + sc * 2.0 ** -9)
+    kI, kIs = step.buf["kI"].cpu(), step.buf["kI_scale"].cpu()
+    e = step.buf["entries"].cpu()
+    gidx = step.buf["idx"].cpu().numpy()
+    for j in (0, 2, 3, 4, 127, 128, 4095, 4096, 16383, 32767):
+        js = slice(j, j + 1)
+        s = oracle.index_scores(cpu["qI"][:, js], cpu["w"][:, js], kI, m=w.m, q_pos0=j,
+                                qI_scale=cpu["qI_scale"][:, js], kI_scale=kIs)
+        check_topk_row(gidx[0, j], s[0, 0], oracle.visible(j, w.m), w.k)
+        o, l = oracle.csa_attend(cpu["q"][:, js], e, e, gidx[:, js], w.scale)
+        assert max_abs(to_np(step.buf["o"][:, js]), o) <= TOL_BF16
+        out, _ = oracle.swa_merge(cpu["q"][:, js], cpu["kv"], cpu["kv"], 0, j, w.n_win, w.scale, o, l)
+        assert max_abs(to_np(step.buf["out"][:, js]), out) <= TOL_BF16
