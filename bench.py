@@ -203,8 +203,9 @@ def run_ours(args, w):
     stream.synchronize()
 
     # the K timed steps as one graph, with per-stage events
-    events = [{s: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for s in stages}
-              for _ in range(args.steps)]
+    # external event records: real timestamps taken by each replay of the graph
+    ev = lambda: torch.cuda.Event(enable_timing=True, external=True)
+    events = [{s: (ev(), ev()) for s in stages} for _ in range(args.steps)]
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(g, stream=stream):

@@ -174,7 +174,8 @@ hyb_status csa_index_topk(const hyb_index_args* a, void* workspace, size_t ws_by
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t nv = n_vis_max(a->q_pos0, a->n_q, a->m, a->n_entries);
   float* scores = static_cast<float*>(workspace);
-  cudaError_t e = hyb::launch_index_scores_cc(a, scores, nv, nv, s);
+  cudaError_t e = hyb::index_tc_shape_supported(a) ? hyb::launch_index_scores_tc(a, scores, nv, nv, s)
+                                                   : hyb::launch_index_scores_cc(a, scores, nv, nv, s);
   if (e != cudaSuccess) return cuda_status(e, "csa_index_topk: index-score launch");
   void* topk_ws = static_cast<char*>(workspace) + index_scores_bytes(a);
   return cuda_status(hyb::launch_topk(a, scores, nv, topk_ws, s), "csa_index_topk: top-k launch");

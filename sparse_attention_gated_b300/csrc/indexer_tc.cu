@@ -1,0 +1,350 @@
+// indexer_tc.cu -- lightning-indexer scores on the 5th-generation tensor cores
+// ("DeepSeek-V4 hybrid attention" (trishampatil.com) section V.2; the indexer
+// runs in FP8, "DeepSeek-V4: Anatomy..." (modernaiengineering.com) step 2):
+//
+//   I[t,s] = sum_h w[t,h] * ReLU( (qs[t,h] q8[t,h]) . (ks[s] k8[s]) )
+//
+// Per tile of 128 entries the FP8 products Q8 K8^T are one tcgen05.mma
+// (kind::f8f6f4, M = 128 entries, N = NQ queries x 64 heads, K = c_I = 128 in
+// four K=32 steps) accumulating in TMEM in float32.  The epilogue warps read
+// the accumulator rows (one entry per thread), apply the scales, ReLU and the
+// head weights, and write one float32 score per (query, entry).
+//
+// Roles (one CTA, persistent over work units = (query group, chunk of entry tiles)):
+//   warp 0      TMA producer: key tiles (16 KiB, 128-byte swizzle) + their
+//               scales into a ring of stages; the query group's FP8 rows.
+//   warp 1      TMEM allocator and MMA issuer (one elected thread).
+//   warps 2..   epilogue (TMEM -> registers -> scores).
+// Key stages are released by tcgen05.commit when their MMAs complete; TMEM
+// accumulators are double/quad-buffered so the epilogue of tile i overlaps
+// the loads and MMAs of tiles i+1...  Every wait is bounded (about 1 s): on
+// expiry the kernel raises HYB_DEV_TIMEOUT in dev_status, drains its own
+// copies in flight, frees TMEM and returns.
+#include "kernels.cuh"
+#include "tc_common.cuh"
+
+namespace hyb {
+
+template <int NQ>
+struct IdxTc {
+  static constexpr int kTileE = 128;
+  static constexpr int kHeads = 64;
+  static constexpr int kN = NQ * kHeads;
+  static constexpr int kStages = NQ == 1 ? 5 : 4;
+  static constexpr int kAcc = NQ == 1 ? 4 : 2;
+  static constexpr int kTmemCols = kAcc * kN;  // 256 or 512
+  static constexpr int kEpiWarps = NQ == 1 ? 4 : 8;
+  static constexpr int kThreads = (2 + kEpiWarps) * 32;
+  static constexpr int kScaleRing = kStages + kAcc;
+  static constexpr int kKeyBytes = kTileE * 128;
+  static constexpr int kScaleBytes = kTileE * 4;
+  static constexpr int kQBytes = kN * 128;
+  static constexpr int kOffKeys = 0;
+  static constexpr int kOffQ = kOffKeys + kStages * kKeyBytes;
+  static constexpr int kOffScales = kOffQ + 2 * kQBytes;
+  static constexpr int kOffW = kOffScales + kScaleRing * kScaleBytes;  // 3 x float[NQ*64]: w*qs, w, qs
+  static constexpr int kOffBar = kOffW + 3 * kN * 4;
+  static constexpr int kNumBars = 2 * kStages + 4 + 2 * kAcc + 2 * kScaleRing + 1;
+  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 64 + 1024;  // + flags + alignment slack
+};
+
+struct IdxTcParams {
+  const float* w;
+  const float* qI_scale;
+  float* scores;
+  int64_t score_stride;
+  int64_t n_q, n_entries, kv_stride, m, q_pos0;
+  int64_t groups_per_b, tiles_per_unit, units_per_group, n_units;
+  int32_t* dev_status;
+};
+
+struct IdxUnit {
+  int64_t b, j0, nq, tile_begin, tile_end;
+};
+
+template <int NQ>
+__device__ __forceinline__ IdxUnit idx_unit(const IdxTcParams& p, int64_t u) {
+  IdxUnit U;
+  const int64_t g = u / p.units_per_group, chunk = u % p.units_per_group;
+  U.b = g / p.groups_per_b;
+  U.j0 = (g % p.groups_per_b) * NQ;
+  U.nq = p.n_q - U.j0 < NQ ? p.n_q - U.j0 : NQ;
+  int64_t vis = visible_entries(p.q_pos0 + U.j0 + U.nq - 1, p.m);
+  if (vis > p.n_entries) vis = p.n_entries;
+  const int64_t tiles = (vis + 127) / 128;
+  U.tile_begin = chunk * p.tiles_per_unit;
+  U.tile_end = U.tile_begin + p.tiles_per_unit < tiles ? U.tile_begin + p.tiles_per_unit : tiles;
+  return U;
+}
+
+template <int NQ>
+__global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
+    index_tc_kernel(const __grid_constant__ CUtensorMap tm_keys, const __grid_constant__ CUtensorMap tm_scales,
+                    const __grid_constant__ CUtensorMap tm_q, IdxTcParams p) {
+  using C = IdxTc<NQ>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* keys = smem + C::kOffKeys;
+  uint8_t* qbuf = smem + C::kOffQ;
+  float* scales = reinterpret_cast<float*>(smem + C::kOffScales);
+  float* w_c = reinterpret_cast<float*>(smem + C::kOffW);  // w*qs
+  float* w_w = w_c + C::kN;                                 // w
+  float* w_q = w_w + C::kN;                                 // qs
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* full = bars;
+  uint64_t* empty = full + C::kStages;
+  uint64_t* q_full = empty + C::kStages;
+  uint64_t* q_empty = q_full + 2;
+  uint64_t* acc_full = q_empty + 2;
+  uint64_t* acc_empty = acc_full + C::kAcc;
+  uint64_t* sc_full = acc_empty + C::kAcc;
+  uint64_t* sc_empty = sc_full + C::kScaleRing;
+  uint64_t* done_bar = sc_empty + C::kScaleRing;
+  volatile int* s_abort = reinterpret_cast<volatile int*>(bars + C::kNumBars);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + C::kNumBars) + 1;
+  int* s_allpos = reinterpret_cast<int*>(bars + C::kNumBars) + 2;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kStages; ++i) tc::mbar_init(&full[i], 1), tc::mbar_init(&empty[i], 1);
+    for (int i = 0; i < 2; ++i) tc::mbar_init(&q_full[i], 1), tc::mbar_init(&q_empty[i], 1);
+    for (int i = 0; i < C::kAcc; ++i) tc::mbar_init(&acc_full[i], 1), tc::mbar_init(&acc_empty[i], C::kEpiWarps);
+    for (int i = 0; i < C::kScaleRing; ++i) tc::mbar_init(&sc_full[i], 1), tc::mbar_init(&sc_empty[i], C::kEpiWarps);
+    tc::mbar_init(done_bar, 1);
+    *s_abort = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 1) tc::tmem_alloc(s_tmem, C::kTmemCols);
+  if (warp == 0 && lane == 0) {
+    tc::prefetch_tmap(&tm_keys);
+    tc::prefetch_tmap(&tm_scales);
+    tc::prefetch_tmap(&tm_q);
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (tc::elect_one()) {
+      int stage = 0;
+      uint32_t sphase = 0;
+      int64_t q_count = 0, seq = 0, issued = 0;
+      bool ok = true;
+      for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+        const IdxUnit U = idx_unit<NQ>(p, u);
+        if (U.tile_begin >= U.tile_end) continue;
+        const int qb = (int)(q_count & 1);
+        if (!(ok = tc::mbar_wait(&q_empty[qb], (uint32_t)((q_count >> 1) & 1) ^ 1u, s_abort))) break;
+        tc::mbar_arrive_expect_tx(&q_full[qb], C::kQBytes);
+        tc::tma_load_2d(qbuf + qb * C::kQBytes, &tm_q, &q_full[qb], 0, (int32_t)((U.b * p.n_q + U.j0) * C::kHeads));
+        ++q_count;
+        for (int64_t t = U.tile_begin; t < U.tile_end; ++t, ++seq) {
+          const int r = (int)(seq % C::kScaleRing);
+          if (!(ok = tc::mbar_wait(&sc_empty[r], (uint32_t)((seq / C::kScaleRing) & 1) ^ 1u, s_abort))) break;
+          tc::mbar_arrive_expect_tx(&sc_full[r], C::kScaleBytes);
+          tc::tma_load_2d(scales + r * C::kTileE, &tm_scales, &sc_full[r], (int32_t)(t * C::kTileE), (int32_t)U.b);
+          if (!(ok = tc::mbar_wait(&empty[stage], sphase ^ 1u, s_abort))) break;
+          tc::mbar_arrive_expect_tx(&full[stage], C::kKeyBytes);
+          tc::tma_load_2d(keys + stage * C::kKeyBytes, &tm_keys, &full[stage], 0,
+                          (int32_t)(U.b * p.kv_stride + t * C::kTileE));
+          ++issued;
+          if (++stage == C::kStages) stage = 0, sphase ^= 1u;
+        }
+      }
+      if (!ok) {
+        // drain this thread's copies in flight before the CTA can exit
+        for (int64_t i = issued > C::kStages ? issued - C::kStages : 0; i < issued; ++i)
+          tc::mbar_wait_drain(&full[i % C::kStages], (uint32_t)((i / C::kStages) & 1));
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (tc::elect_one()) {
+      constexpr uint32_t idesc = tc::make_idesc(0, 0, 0, 0, 128, C::kN);
+      int stage = 0, acc = 0;
+      uint32_t sphase = 0, aphase = 0;
+      int64_t q_count = 0;
+      bool ok = true;
+      for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+        const IdxUnit U = idx_unit<NQ>(p, u);
+        if (U.tile_begin >= U.tile_end) continue;
+        const int qb = (int)(q_count & 1);
+        if (!(ok = tc::mbar_wait(&q_full[qb], (uint32_t)((q_count >> 1) & 1), s_abort))) break;
+        const uint32_t b_base = tc::smem_u32(qbuf + qb * C::kQBytes);
+        for (int64_t t = U.tile_begin; t < U.tile_end; ++t) {
+          if (!(ok = tc::mbar_wait(&acc_empty[acc], aphase ^ 1u, s_abort))) break;
+          if (!(ok = tc::mbar_wait(&full[stage], sphase, s_abort))) break;
+          tc::tc_fence_after();
+          const uint32_t a_base = tc::smem_u32(keys + stage * C::kKeyBytes);
+          const uint32_t d = tmem_base + (uint32_t)(acc * C::kN);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            tc::mma_f8f6f4(d, tc::desc_kmajor_sw128(a_base + 32 * k), tc::desc_kmajor_sw128(b_base + 32 * k), idesc,
+                           k > 0 ? 1u : 0u);
+          tc::mma_commit(&empty[stage]);
+          tc::mma_commit(&acc_full[acc]);
+          if (++stage == C::kStages) stage = 0, sphase ^= 1u;
+          if (++acc == C::kAcc) acc = 0, aphase ^= 1u;
+        }
+        if (!ok) break;
+        tc::mma_commit(&q_empty[qb]);
+        ++q_count;
+      }
+      // every MMA issued above has completed once done_bar flips
+      tc::mma_commit(done_bar);
+      tc::mbar_wait_drain(done_bar, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int et = threadIdx.x - 64;  // 0 .. kEpiWarps*32-1
+    const int quad = warp & 3;        // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) / 4;  // which queries this warp handles (NQ = 4: two each)
+    constexpr int kQPerWarp = NQ == 1 ? 1 : 2;
+    int acc = 0;
+    uint32_t aphase = 0;
+    int64_t seq = 0;
+    bool ok = true;
+    for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+      const IdxUnit U = idx_unit<NQ>(p, u);
+      if (U.tile_begin >= U.tile_end) continue;
+      tc::named_barrier(1, C::kEpiWarps * 32);
+      if (et == 0) *s_allpos = 1;
+      tc::named_barrier(1, C::kEpiWarps * 32);
+      for (int i = et; i < C::kN; i += C::kEpiWarps * 32) {
+        const int jq = i / C::kHeads, h = i % C::kHeads;
+        float wv = 0.f, qs = 1.f;
+        if (jq < U.nq) {
+          const int64_t off = ((U.b * p.n_q) + U.j0 + jq) * C::kHeads + h;
+          wv = p.w[off];
+          qs = p.qI_scale[off];
+        }
+        w_c[i] = wv * qs;
+        w_w[i] = wv;
+        w_q[i] = qs;
+        if (!(qs > 0.f)) *s_allpos = 0;
+      }
+      tc::named_barrier(1, C::kEpiWarps * 32);
+      const bool allpos = *s_allpos != 0;
+      for (int64_t t = U.tile_begin; t < U.tile_end; ++t, ++seq) {
+        const int r = (int)(seq % C::kScaleRing);
+        if (!(ok = tc::mbar_wait(&acc_full[acc], aphase, s_abort))) break;
+        if (!(ok = tc::mbar_wait(&sc_full[r], (uint32_t)((seq / C::kScaleRing) & 1), s_abort))) break;
+        tc::tc_fence_after();
+        const int row = quad * 32 + lane;
+        const int64_t s = t * C::kTileE + row;
+        const float ks = scales[r * C::kTileE + row];
+        float score[kQPerWarp];
+#pragma unroll
+        for (int qi = 0; qi < kQPerWarp; ++qi) {
+          const int q = NQ == 1 ? 0 : 2 * half + qi;
+          const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * C::kN + q * C::kHeads);
+          float v0[32], v1[32];
+          tc::tmem_ld32(taddr, v0);
+          tc::tmem_ld32(taddr + 32, v1);
+          tc::tmem_ld_wait();
+          const float* wc = w_c + q * C::kHeads;
+          float sum = 0.f;
+          if (allpos && ks > 0.f) {
+#pragma unroll
+            for (int h = 0; h < 32; ++h) sum = fmaf(wc[h], fmaxf(v0[h], 0.f), sum);
+#pragma unroll
+            for (int h = 0; h < 32; ++h) sum = fmaf(wc[32 + h], fmaxf(v1[h], 0.f), sum);
+            sum *= ks;
+          } else {
+            const float* ww = w_w + q * C::kHeads;
+            const float* wq = w_q + q * C::kHeads;
+#pragma unroll
+            for (int h = 0; h < 32; ++h) sum = fmaf(ww[h], fmaxf(v0[h] * (wq[h] * ks), 0.f), sum);
+#pragma unroll
+            for (int h = 0; h < 32; ++h) sum = fmaf(ww[32 + h], fmaxf(v1[h] * (wq[32 + h] * ks), 0.f), sum);
+          }
+          score[qi] = sum;
+        }
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          tc::mbar_arrive(&acc_empty[acc]);
+          tc::mbar_arrive(&sc_empty[r]);
+        }
+#pragma unroll
+        for (int qi = 0; qi < kQPerWarp; ++qi) {
+          const int q = NQ == 1 ? 0 : 2 * half + qi;
+          if (q >= U.nq) continue;
+          const int64_t j = U.j0 + q;
+          int64_t vis = visible_entries(p.q_pos0 + j, p.m);
+          if (vis > p.n_entries) vis = p.n_entries;
+          if (s < vis) p.scores[(U.b * p.n_q + j) * p.score_stride + s] = score[qi];
+        }
+        if (++acc == C::kAcc) acc = 0, aphase ^= 1u;
+      }
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *s_abort) flag_status(p.dev_status, HYB_DEV_TIMEOUT);
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------- host
+
+bool index_tc_shape_supported(const hyb_index_args* a) {
+  if (a->dtype != HYB_E4M3 || a->c_I != 128 || a->n_ih != 64) return false;
+  const int64_t kvs = a->kv_stride > 0 ? a->kv_stride : a->n_entries;
+  if (kvs % 4 != 0 || kvs < 1) return false;  // scale rows must start on 16-byte boundaries
+  const uintptr_t al = reinterpret_cast<uintptr_t>(a->kI) | reinterpret_cast<uintptr_t>(a->kI_scale) |
+                       reinterpret_cast<uintptr_t>(a->qI);
+  if (al % 16 != 0) return false;
+  if (a->batch * kvs >= (int64_t(1) << 31) || a->batch * a->n_q * 64 >= (int64_t(1) << 31)) return false;
+  return true;
+}
+
+template <int NQ>
+static cudaError_t launch_nq(const hyb_index_args* a, float* scores, int64_t score_stride, int64_t n_vis_max,
+                             cudaStream_t s) {
+  using C = IdxTc<NQ>;
+  const int64_t kvs = a->kv_stride > 0 ? a->kv_stride : a->n_entries;
+  CUtensorMap tm_keys, tm_scales, tm_q;
+  if (!encode_tmap_2d(&tm_keys, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->kI, 128, (uint64_t)(a->batch * kvs), 128, 128,
+                      C::kTileE, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap_2d(&tm_scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a->kI_scale, (uint64_t)kvs, (uint64_t)a->batch,
+                      (uint64_t)kvs * 4, C::kTileE, 1, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_tmap_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->qI, 128, (uint64_t)(a->batch * a->n_q * 64), 128, 128,
+                      (uint32_t)C::kN, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  IdxTcParams p;
+  p.w = a->w, p.qI_scale = a->qI_scale, p.scores = scores, p.score_stride = score_stride;
+  p.n_q = a->n_q, p.n_entries = a->n_entries, p.kv_stride = kvs, p.m = a->m, p.q_pos0 = a->q_pos0;
+  p.groups_per_b = (a->n_q + NQ - 1) / NQ;
+  const int64_t groups = p.groups_per_b * a->batch;
+  const int64_t tiles_max = (n_vis_max + 127) / 128;
+  const int ctas_per_sm = C::kSmemBytes <= 113 * 1024 ? 2 : 1;
+  const int64_t slots = (int64_t)kNumSMs * ctas_per_sm;
+  int64_t tpu = (groups * tiles_max + 2 * slots - 1) / (2 * slots);
+  tpu = tpu < 1 ? 1 : (tpu > tiles_max ? tiles_max : tpu);
+  p.tiles_per_unit = tpu;
+  p.units_per_group = (tiles_max + tpu - 1) / tpu;
+  p.n_units = groups * p.units_per_group;
+  p.dev_status = a->dev_status;
+  if (p.n_units == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(index_tc_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = p.n_units < slots ? p.n_units : slots;
+  index_tc_kernel<NQ><<<(unsigned)grid, C::kThreads, C::kSmemBytes, s>>>(tm_keys, tm_scales, tm_q, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_index_scores_tc(const hyb_index_args* a, float* scores, int64_t score_stride, int64_t n_vis_max,
+                                   cudaStream_t s) {
+  if (n_vis_max == 0 || a->n_q == 0 || a->batch == 0) return cudaSuccess;
+  if (a->n_q >= 8) return launch_nq<4>(a, scores, score_stride, n_vis_max, s);
+  return launch_nq<1>(a, scores, score_stride, n_vis_max, s);
+}
+
+}  // namespace hyb

@@ -16,6 +16,11 @@ bool index_cc_shape_supported(int64_t n_ih, int64_t c_I);
 cudaError_t launch_index_scores_cc(const hyb_index_args* a, float* scores, int64_t score_stride, int64_t n_vis_max,
                                    cudaStream_t s);
 
+// indexer_tc.cu (tcgen05 FP8 scores: E4M3, c_I = 128, 64 indexer heads)
+bool index_tc_shape_supported(const hyb_index_args* a);
+cudaError_t launch_index_scores_tc(const hyb_index_args* a, float* scores, int64_t score_stride, int64_t n_vis_max,
+                                   cudaStream_t s);
+
 // topk.cu
 size_t topk_workspace_bytes(const hyb_index_args* a, int64_t n_vis_max);
 cudaError_t launch_topk(const hyb_index_args* a, const float* scores, int64_t score_stride, void* ws, cudaStream_t s);

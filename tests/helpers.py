@@ -37,6 +37,8 @@ def check_topk_row(gpu_idx: np.ndarray, ref_scores: np.ndarray, visible: int, k:
     take = min(k, visible)
     sel = gpu_idx[:take]
     assert (gpu_idx[take:] == -1).all(), "padding must be -1"
+    if take == 0:
+        return "exact"
     assert np.all(np.diff(sel) > 0), "indices must be strictly ascending"
     assert sel.min() >= 0 and sel.max() < visible, "index outside the visible entries"
     if take == visible:
