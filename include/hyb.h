@@ -77,6 +77,9 @@ typedef enum hyb_dtype {
 /* bits OR-ed into *dev_status by the kernels */
 #define HYB_DEV_BAD_INDEX 0x1 /* an index list held a value outside [-1, n_entries) */
 #define HYB_DEV_TIMEOUT 0x2   /* a bounded device-side wait gave up */
+/* bits 8-15 of *dev_status: with HYB_DEV_TIMEOUT, a nonzero kernel-internal
+   identifier of the wait that gave up (diagnostic only) */
+#define HYB_DEV_WAIT_SITE(status) (((status) >> 8) & 0xFF)
 
 /* ------------------------------------------------------------------------
  * hyb_compress -- softmax-gated compressor ([HA] V.1 for CSA, [HA] VI for HCA;

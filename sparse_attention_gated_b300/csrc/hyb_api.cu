@@ -152,6 +152,9 @@ static hyb_status validate_index(const hyb_index_args* a) {
     return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: the last query sees %lld entries but only %lld exist",
                 (long long)hyb::visible_entries(a->q_pos0 + a->n_q - 1, a->m), (long long)a->n_entries);
   if (a->batch == 0 || a->n_q == 0) return ok();
+  if (!hyb::topk_shape_supported(a, n_vis_max(a->q_pos0, a->n_q, a->m, a->n_entries)))
+    return fail(HYB_ERR_UNSUPPORTED, "csa_index_topk: %lld visible entries with k = %lld exceed the top-k plan",
+                (long long)n_vis_max(a->q_pos0, a->n_q, a->m, a->n_entries), (long long)a->k);
   if (!a->qI || !a->w || !a->idx) return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: NULL qI/w/idx");
   if (a->n_entries > 0 && !a->kI) return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: NULL kI");
   const bool fp8 = a->dtype == HYB_E4M3;
@@ -224,17 +227,25 @@ static hyb_status validate_attend_common(const char* name, int64_t batch, int64_
   return ok();
 }
 
+// Attention dispatch: the tensor-core kernel for its shapes (bf16, c = 512,
+// heads a multiple of 64), the CUDA-core kernel otherwise.
+static size_t attend_workspace(const hyb::AttendJob& j) {
+  return hyb::attend_tc_supported(j) ? hyb::attend_tc_workspace_bytes(j) : hyb::attend_cc_workspace_bytes(j);
+}
+
 static hyb_status run_attend(const char* name, const hyb::AttendJob& j, void* workspace, size_t ws_bytes, void* stream) {
-  const size_t need = hyb::attend_cc_workspace_bytes(j);
+  const size_t need = attend_workspace(j);
   if (need > 0 && (!workspace || ws_bytes < need))
     return fail(HYB_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", name, need, ws_bytes);
   if (!aligned(workspace, 256)) return fail(HYB_ERR_WORKSPACE, "%s: workspace must be 256-byte aligned", name);
-  return cuda_status(hyb::launch_attend_cc(j, workspace, static_cast<cudaStream_t>(stream)), name);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (hyb::attend_tc_supported(j)) return cuda_status(hyb::launch_attend_tc(j, workspace, s), name);
+  return cuda_status(hyb::launch_attend_cc(j, workspace, s), name);
 }
 
 size_t csa_attend_workspace_size(const hyb_csa_attend_args* a) {
   if (!a || a->batch <= 0 || a->n_q <= 0 || a->n_h <= 0) return 0;
-  return hyb::attend_cc_workspace_bytes(csa_job(a));
+  return attend_workspace(csa_job(a));
 }
 
 hyb_status csa_attend(const hyb_csa_attend_args* a, void* workspace, size_t ws_bytes, void* stream) {
@@ -252,7 +263,7 @@ hyb_status csa_attend(const hyb_csa_attend_args* a, void* workspace, size_t ws_b
 
 size_t hca_attend_workspace_size(const hyb_hca_attend_args* a) {
   if (!a || a->batch <= 0 || a->n_q <= 0 || a->n_h <= 0 || a->m < 1) return 0;
-  return hyb::attend_cc_workspace_bytes(hca_job(a));
+  return attend_workspace(hca_job(a));
 }
 
 hyb_status hca_attend(const hyb_hca_attend_args* a, void* workspace, size_t ws_bytes, void* stream) {

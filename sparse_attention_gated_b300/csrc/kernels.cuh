@@ -23,6 +23,7 @@ cudaError_t launch_index_scores_tc(const hyb_index_args* a, float* scores, int64
 
 // topk.cu
 size_t topk_workspace_bytes(const hyb_index_args* a, int64_t n_vis_max);
+bool topk_shape_supported(const hyb_index_args* a, int64_t n_vis_max);
 cudaError_t launch_topk(const hyb_index_args* a, const float* scores, int64_t score_stride, void* ws, cudaStream_t s);
 
 // attend_cc.cu (CUDA-core attention for all three entry sources)
@@ -44,6 +45,12 @@ struct AttendJob {
   int32_t* dev_status;
 };
 bool attend_cc_shape_supported(int64_t c, int64_t n_h);
+
+// attend_tc.cu (tcgen05 MQA attention: bf16, c = 512, heads in groups of 64)
+bool attend_tc_supported(const AttendJob& j);
+int attend_tc_splits(const AttendJob& j);
+size_t attend_tc_workspace_bytes(const AttendJob& j);
+cudaError_t launch_attend_tc(const AttendJob& j, void* ws, cudaStream_t s);
 int attend_cc_splits(const AttendJob& j);
 size_t attend_cc_workspace_bytes(const AttendJob& j);
 cudaError_t launch_attend_cc(const AttendJob& j, void* ws, cudaStream_t s);

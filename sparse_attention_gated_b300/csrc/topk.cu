@@ -3,84 +3,125 @@
 // blocks are kept; "DeepSeek-V4: Anatomy..." (modernaiengineering.com) worked
 // example: fewer than k entries are kept when fewer exist).
 //
-// One CTA of 1024 threads per query row.  Exact radix select on the
-// order-preserving uint32 image of the float32 scores, 8 bits per pass from
-// the top: after four passes the threshold key T (the k-th largest) and the
-// number of ties to keep are known.  The kept set is every entry with key > T
-// plus the lowest-indexed entries with key == T, i.e. ranking by
-// (score descending, index ascending).  It is written in ascending index
-// order (a bitonic sort in shared memory) and padded with -1.
-// Rows that fit (<= kStageCap scores) are staged once in shared memory;
-// longer rows (decode over 10^5 entries) are re-read from L2 on each pass.
+// Ranking: (score descending, entry index ascending), compared exactly on the
+// order-preserving uint32 image ("key") of the float32 scores.  The kept set
+// is every entry with key > T plus the lowest-indexed entries with key == T,
+// where T is the k-th largest key; it is written in ascending index order and
+// padded with -1.
+//
+// Building blocks (CTAs of 1024 threads):
+//   radix_select     exact k-th key of a list, 8 bits per pass from the top;
+//                    histogram atomics are aggregated per warp (match.any), so
+//                    lists whose keys share their top bits do not serialise.
+//   collect_ordered  one pass in list order that writes the kept positions to
+//                    their final (ascending) slots: a block scan of the
+//                    (key > T, key == T) flags gives each kept element's slot,
+//                    so no sort is needed.
+// Plans:
+//   one stage   (rows of at most kStageCap visible entries): one CTA per row
+//               stages the keys in shared memory, selects and collects.
+//   three kernels (longer rows, e.g. 262,144 entries at 1M context):
+//     hist    CTA (chunk, row): 12-bit histogram of its chunk, added into the
+//             row's global histogram.
+//     filter  CTA (chunk, row): from the row histogram, the bin b* that holds
+//             the k-th largest key; the chunk's entries above b* (all kept)
+//             and inside b* (candidates) are written, in index order, to the
+//             chunk's own regions.
+//     final   CTA per row: selects the k - (#above) best candidates exactly,
+//             then merges them with the entries above b* (both lists are
+//             ascending) into the output.
 #include "kernels.cuh"
 
 namespace hyb {
 
 constexpr int kTopkThreads = 1024;
-constexpr int64_t kStageCap = 16384;
+constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int64_t kStageCap = 16384;  // one-stage plan: keys staged in shared memory
+constexpr int64_t kCandCap = 12288;   // final kernel: candidates staged in shared memory
+constexpr int kHistBits = 12;
+constexpr int kHistBins = 1 << kHistBits;
+constexpr int kMaxChunks = 64;
 
 struct TopkParams {
   const float* scores;
   int64_t score_stride;
   int32_t* idx;
   float* out_scores;
-  int64_t n_q, n_entries, m, k, q_pos0, kp;
+  int64_t n_q, n_entries, m, k, q_pos0;
+  // three-kernel plan
+  int64_t chunk;
+  int n_chunks;
+  uint32_t* ghist;      // [rows][kHistBins]
+  int32_t* def_idx;     // [rows][n_chunks][chunk]: entries above the threshold bin
+  uint32_t* cand_key;   // [rows][n_chunks][chunk]: entries in the threshold bin
+  int32_t* cand_idx;
+  int32_t* counts;      // [rows][n_chunks][2]: (#above, #candidates) of each chunk
 };
 
-template <bool STAGED>
-__device__ __forceinline__ uint32_t row_key(const uint32_t* keys_s, const float* sc, int64_t s) {
-  if constexpr (STAGED)
-    return keys_s[s];
-  else
-    return float_order_key(__ldg(sc + s));
-}
-
-// append to the selection; never writes past its kp slots
-__device__ __forceinline__ void push_sel(int32_t* sel, int* n, int64_t kp, int32_t s) {
-  const int pos = atomicAdd(n, 1);
-  if (pos < kp) sel[pos] = s;
-}
-
-template <bool STAGED>
-__global__ void __launch_bounds__(kTopkThreads) topk_radix_kernel(TopkParams p) {
-  extern __shared__ uint32_t dyn[];
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t warp_tot[32];
-  __shared__ uint32_t s_prefix, s_mask, s_desired, s_chunk_eq;
-  __shared__ int s_nsel;
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t row = blockIdx.x;
+__device__ __forceinline__ int64_t row_visible(const TopkParams& p, int64_t row) {
   const int64_t j = row % p.n_q;
-  int64_t vis = visible_entries(p.q_pos0 + j, p.m);
-  if (vis > p.n_entries) vis = p.n_entries;
-  const float* sc = p.scores + row * p.score_stride;
-  int32_t* out = p.idx + row * p.k;
-  float* out_sc = p.out_scores ? p.out_scores + row * p.k : nullptr;
+  const int64_t v = visible_entries(p.q_pos0 + j, p.m);
+  return v < p.n_entries ? v : p.n_entries;
+}
 
-  if (vis <= p.k) {  // everything visible is kept, already in ascending order
-    for (int64_t i = tid; i < p.k; i += kTopkThreads) {
-      out[i] = i < vis ? (int32_t)i : -1;
-      if (out_sc) out_sc[i] = i < vis ? sc[i] : -INFINITY;
-    }
-    return;
-  }
+struct BlockShared {
+  uint32_t hist[256];
+  uint32_t warp_tot[kTopkWarps];
+  uint32_t total;
+  uint32_t prefix, mask, desired;
+};
 
-  uint32_t* keys_s = dyn;                                                  // [vis] when STAGED
-  int32_t* sel = reinterpret_cast<int32_t*>(dyn + (STAGED ? kStageCap : 0));  // [kp]
-  if constexpr (STAGED) {
-    for (int64_t s = tid; s < vis; s += kTopkThreads) keys_s[s] = float_order_key(__ldg(sc + s));
-  }
-  if (tid == 0) s_prefix = 0, s_mask = 0, s_desired = (uint32_t)p.k, s_nsel = 0;
+// Exclusive block-wide prefix of two flags packed as (a | b << 16) in thread
+// order; returns (a_before, b_before) of this thread and the block totals.
+__device__ __forceinline__ void block_scan2(bool fa, bool fb, BlockShared& S, uint32_t& a_before, uint32_t& b_before,
+                                            uint32_t& a_tot, uint32_t& b_tot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t ba = __ballot_sync(0xffffffffu, fa), bb = __ballot_sync(0xffffffffu, fb);
+  const uint32_t lt = (1u << lane) - 1u;
+  if (lane == 0) S.warp_tot[warp] = (uint32_t)__popc(ba) | ((uint32_t)__popc(bb) << 16);
   __syncthreads();
+  if (warp == 0) {
+    const uint32_t v = S.warp_tot[lane];
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    S.warp_tot[lane] = incl - v;
+    if (lane == 31) S.total = incl;
+  }
+  __syncthreads();
+  const uint32_t base = S.warp_tot[warp];
+  a_before = (base & 0xFFFFu) + (uint32_t)__popc(ba & lt);
+  b_before = (base >> 16) + (uint32_t)__popc(bb & lt);
+  a_tot = S.total & 0xFFFFu;
+  b_tot = S.total >> 16;
+  __syncthreads();
+}
 
+__device__ __forceinline__ void hist_add(uint32_t* hist, bool take, uint32_t digit) {
+  const uint32_t active = __ballot_sync(0xffffffffu, take);
+  if (take) {
+    const uint32_t peers = __match_any_sync(active, digit);
+    if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(peers));
+  }
+}
+
+// The `take`-th largest key T of keyfn(0..L) and how many elements equal to T
+// are kept (the lowest positions).  Requires 1 <= take <= L.
+template <typename KeyFn>
+__device__ void radix_select(KeyFn keyfn, int64_t L, int64_t take, BlockShared& S, uint32_t& T, uint32_t& ties) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) S.prefix = 0, S.mask = 0, S.desired = (uint32_t)take;
   for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
+    for (int i = tid; i < 256; i += kTopkThreads) S.hist[i] = 0;
     __syncthreads();
-    const uint32_t prefix = s_prefix, mask = s_mask;
-    for (int64_t s = tid; s < vis; s += kTopkThreads) {
-      const uint32_t key = row_key<STAGED>(keys_s, sc, s);
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    const uint32_t prefix = S.prefix, mask = S.mask;
+    for (int64_t base = 0; base < L; base += kTopkThreads) {
+      const int64_t s = base + tid;
+      const uint32_t key = s < L ? keyfn(s) : 0u;
+      hist_add(S.hist, s < L && (key & mask) == prefix, (key >> shift) & 255u);
     }
     __syncthreads();
     if (warp == 0) {
@@ -88,7 +129,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_radix_kernel(TopkParams p) 
       const int hi = 255 - 8 * lane;
       uint32_t lane_sum = 0;
 #pragma unroll
-      for (int d = 0; d < 8; ++d) lane_sum += hist[hi - d];
+      for (int d = 0; d < 8; ++d) lane_sum += S.hist[hi - d];
       uint32_t incl = lane_sum;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -96,103 +137,343 @@ __global__ void __launch_bounds__(kTopkThreads) topk_radix_kernel(TopkParams p) 
         if (lane >= o) incl += v;
       }
       const uint32_t excl = incl - lane_sum;
-      const uint32_t desired = s_desired;
+      const uint32_t desired = S.desired;
       if (excl < desired && desired <= incl) {
         uint32_t cum = excl;
         for (int d = hi; d > hi - 8; --d) {
-          if (cum + hist[d] >= desired) {
-            s_prefix = prefix | ((uint32_t)d << shift);
-            s_mask = mask | (255u << shift);
-            s_desired = desired - cum;
+          if (cum + S.hist[d] >= desired) {
+            S.prefix = prefix | ((uint32_t)d << shift);
+            S.mask = mask | (255u << shift);
+            S.desired = desired - cum;
             break;
           }
-          cum += hist[d];
+          cum += S.hist[d];
         }
       }
     }
     __syncthreads();
   }
-
-  const uint32_t T = s_prefix;
-  const uint32_t ties = s_desired;  // how many entries with key == T to keep (the lowest indices)
-  uint32_t eq_base = 0;
-  for (int64_t base = 0; base < vis; base += kTopkThreads) {
-    const int64_t s = base + tid;
-    const uint32_t key = s < vis ? row_key<STAGED>(keys_s, sc, s) : 0u;
-    const bool gt = s < vis && key > T;
-    const bool eq = s < vis && key == T;
-    if (gt) push_sel(sel, &s_nsel, p.kp, (int32_t)s);
-    const uint32_t ball = __ballot_sync(0xffffffffu, eq);
-    const uint32_t lane_rank = __popc(ball & ((1u << lane) - 1u));
-    if (lane == 0) warp_tot[warp] = __popc(ball);
-    __syncthreads();
-    if (warp == 0) {
-      const uint32_t v = warp_tot[lane];
-      uint32_t incl = v;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += u;
-      }
-      warp_tot[lane] = incl - v;  // exclusive offset of each warp
-      if (lane == 31) s_chunk_eq = incl;
-    }
-    __syncthreads();
-    if (eq && eq_base + warp_tot[warp] + lane_rank < ties) push_sel(sel, &s_nsel, p.kp, (int32_t)s);
-    eq_base += s_chunk_eq;
-    __syncthreads();
-    if (eq_base >= ties && base + kTopkThreads < vis) {
-      // all ties taken; the remaining chunks can only add entries with key > T
-      for (int64_t s2 = base + kTopkThreads + tid; s2 < vis; s2 += kTopkThreads) {
-        if (row_key<STAGED>(keys_s, sc, s2) > T) push_sel(sel, &s_nsel, p.kp, (int32_t)s2);
-      }
-      break;
-    }
-  }
-  for (int64_t i = p.k + tid; i < p.kp; i += kTopkThreads) sel[i] = INT32_MAX;
+  T = S.prefix;
+  ties = S.desired;
   __syncthreads();
+}
 
-  // bitonic sort of sel[0..kp) ascending
-  for (int64_t size = 2; size <= p.kp; size <<= 1) {
-    for (int64_t stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int64_t i = tid; i < p.kp; i += kTopkThreads) {
-        const int64_t partner = i ^ stride;
-        if (partner > i) {
-          const bool up = (i & size) == 0;
-          const int32_t a = sel[i], b = sel[partner];
-          if ((a > b) == up) sel[i] = b, sel[partner] = a;
-        }
-      }
-      __syncthreads();
-    }
-  }
-  for (int64_t i = tid; i < p.k; i += kTopkThreads) {
-    out[i] = sel[i];
-    if (out_sc) out_sc[i] = sc[sel[i]];
+// Calls emit(slot, position) for every kept position, slot = its rank in list
+// order among the kept ones (0 .. take-1).
+template <typename KeyFn, typename Emit>
+__device__ void collect_ordered(KeyFn keyfn, int64_t L, uint32_t T, uint32_t ties, BlockShared& S, Emit emit) {
+  uint32_t gt_base = 0, eq_base = 0;
+  for (int64_t base = 0; base < L; base += kTopkThreads) {
+    const int64_t s = base + threadIdx.x;
+    const uint32_t key = s < L ? keyfn(s) : 0u;
+    const bool gt = s < L && key > T;
+    const bool eq = s < L && key == T;
+    uint32_t gb, eb, gtot, etot;
+    block_scan2(gt, eq, S, gb, eb, gtot, etot);
+    gb += gt_base, eb += eq_base;
+    if (gt) emit(gb + (eb < ties ? eb : ties), s);
+    if (eq && eb < ties) emit(gb + eb, s);
+    gt_base += gtot, eq_base += etot;
   }
 }
 
-size_t topk_workspace_bytes(const hyb_index_args*, int64_t) { return 0; }
+__device__ __forceinline__ void keep_all(const TopkParams& p, int64_t row, int64_t vis) {
+  const float* sc = p.scores + row * p.score_stride;
+  int32_t* out = p.idx + row * p.k;
+  float* out_sc = p.out_scores ? p.out_scores + row * p.k : nullptr;
+  for (int64_t i = threadIdx.x; i < p.k; i += kTopkThreads) {
+    out[i] = i < vis ? (int32_t)i : -1;
+    if (out_sc) out_sc[i] = i < vis ? sc[i] : -INFINITY;
+  }
+}
 
-cudaError_t launch_topk(const hyb_index_args* a, const float* scores, int64_t score_stride, void*, cudaStream_t s) {
-  TopkParams p;
+// ------------------------------------------------------------- one stage
+__global__ void __launch_bounds__(kTopkThreads) topk_row_kernel(TopkParams p) {
+  extern __shared__ uint32_t keys_s[];  // [kStageCap]
+  __shared__ BlockShared S;
+  const int64_t row = blockIdx.x;
+  const int64_t vis = row_visible(p, row);
+  if (vis <= p.k) {
+    keep_all(p, row, vis);
+    return;
+  }
+  const float* sc = p.scores + row * p.score_stride;
+  int32_t* out = p.idx + row * p.k;
+  float* out_sc = p.out_scores ? p.out_scores + row * p.k : nullptr;
+  for (int64_t s = threadIdx.x; s < vis; s += kTopkThreads) keys_s[s] = float_order_key(__ldg(sc + s));
+  __syncthreads();
+  auto keyfn = [&](int64_t s) { return keys_s[s]; };
+  uint32_t T, ties;
+  radix_select(keyfn, vis, p.k, S, T, ties);
+  collect_ordered(keyfn, vis, T, ties, S, [&](uint32_t slot, int64_t s) {
+    out[slot] = (int32_t)s;
+    if (out_sc) out_sc[slot] = sc[s];
+  });
+}
+
+// ------------------------------------------------ three kernels: hist
+__global__ void __launch_bounds__(kTopkThreads) topk_hist_kernel(TopkParams p) {
+  __shared__ uint32_t hist[kHistBins];
+  const int64_t row = blockIdx.y;
+  const int64_t vis = row_visible(p, row);
+  if (vis <= p.k) return;
+  const int64_t s0 = (int64_t)blockIdx.x * p.chunk;
+  if (s0 >= vis) return;
+  const int64_t len = vis - s0 < p.chunk ? vis - s0 : p.chunk;
+  for (int i = threadIdx.x; i < kHistBins; i += kTopkThreads) hist[i] = 0;
+  __syncthreads();
+  const float* sc = p.scores + row * p.score_stride + s0;
+  for (int64_t base = 0; base < len; base += kTopkThreads) {
+    const int64_t s = base + threadIdx.x;
+    const uint32_t key = s < len ? float_order_key(__ldg(sc + s)) : 0u;
+    hist_add(hist, s < len, key >> (32 - kHistBits));
+  }
+  __syncthreads();
+  uint32_t* gh = p.ghist + row * kHistBins;
+  for (int i = threadIdx.x; i < kHistBins; i += kTopkThreads)
+    if (hist[i]) atomicAdd(gh + i, hist[i]);
+}
+
+// The bin holding the k-th largest key of a row, from its histogram, and the
+// number of keys in higher bins (< k).
+__device__ void threshold_bin(const uint32_t* gh, uint32_t k, BlockShared& S, uint32_t& bstar, uint32_t& above) {
+  constexpr int kPer = kHistBins / kTopkThreads;  // bins per thread, from the top
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int hi = kHistBins - 1 - kPer * tid;
+  uint32_t c[kPer], sum = 0;
+#pragma unroll
+  for (int d = 0; d < kPer; ++d) c[d] = gh[hi - d], sum += c[d];
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) S.warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t v = S.warp_tot[lane];
+    uint32_t wi = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t u = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += u;
+    }
+    S.warp_tot[lane] = wi - v;
+  }
+  __syncthreads();
+  const uint32_t excl = S.warp_tot[warp] + incl - sum;  // keys in bins above this thread's
+  if (excl < k && k <= excl + sum) {
+    uint32_t cum = excl;
+    for (int d = 0; d < kPer; ++d) {
+      if (cum + c[d] >= k) {
+        S.prefix = (uint32_t)(hi - d);
+        S.desired = cum;
+        break;
+      }
+      cum += c[d];
+    }
+  }
+  __syncthreads();
+  bstar = S.prefix;
+  above = S.desired;
+  __syncthreads();
+}
+
+// ---------------------------------------------- three kernels: filter
+__global__ void __launch_bounds__(kTopkThreads) topk_filter_kernel(TopkParams p) {
+  __shared__ BlockShared S;
+  const int64_t row = blockIdx.y;
+  const int64_t vis = row_visible(p, row);
+  if (vis <= p.k) return;
+  const int64_t s0 = (int64_t)blockIdx.x * p.chunk;
+  int32_t* cnt = p.counts + (row * p.n_chunks + blockIdx.x) * 2;
+  if (s0 >= vis) {
+    if (threadIdx.x == 0) cnt[0] = 0, cnt[1] = 0;
+    return;
+  }
+  const int64_t len = vis - s0 < p.chunk ? vis - s0 : p.chunk;
+  uint32_t bstar, above;
+  threshold_bin(p.ghist + row * kHistBins, (uint32_t)p.k, S, bstar, above);
+  const float* sc = p.scores + row * p.score_stride + s0;
+  const int64_t reg = (row * p.n_chunks + blockIdx.x) * p.chunk;
+  uint32_t nd = 0, nc = 0;
+  for (int64_t base = 0; base < len; base += kTopkThreads) {
+    const int64_t s = base + threadIdx.x;
+    const uint32_t key = s < len ? float_order_key(__ldg(sc + s)) : 0u;
+    const uint32_t bin = key >> (32 - kHistBits);
+    const bool d = s < len && bin > bstar;
+    const bool c = s < len && bin == bstar;
+    uint32_t db, cb, dt, ct;
+    block_scan2(d, c, S, db, cb, dt, ct);
+    if (d) p.def_idx[reg + nd + db] = (int32_t)(s0 + s);
+    if (c) {
+      p.cand_key[reg + nc + cb] = key;
+      p.cand_idx[reg + nc + cb] = (int32_t)(s0 + s);
+    }
+    nd += dt, nc += ct;
+  }
+  if (threadIdx.x == 0) cnt[0] = (int32_t)nd, cnt[1] = (int32_t)nc;
+}
+
+// ----------------------------------------------- three kernels: final
+__global__ void __launch_bounds__(kTopkThreads) topk_final_kernel(TopkParams p) {
+  extern __shared__ uint32_t dyn[];
+  __shared__ BlockShared S;
+  __shared__ int32_t pre_d[kMaxChunks + 1], pre_c[kMaxChunks + 1];
+  const int64_t row = blockIdx.x;
+  const int64_t vis = row_visible(p, row);
+  if (vis <= p.k) {
+    keep_all(p, row, vis);
+    return;
+  }
+  const int tid = threadIdx.x;
+  const float* sc = p.scores + row * p.score_stride;
+  int32_t* out = p.idx + row * p.k;
+  float* out_sc = p.out_scores ? p.out_scores + row * p.k : nullptr;
+  const int32_t* cnt = p.counts + row * p.n_chunks * 2;
+  if (tid == 0) {
+    int32_t a = 0, b = 0;
+    for (int c = 0; c < p.n_chunks; ++c) {
+      pre_d[c] = a, pre_c[c] = b;
+      a += cnt[2 * c], b += cnt[2 * c + 1];
+    }
+    pre_d[p.n_chunks] = a, pre_c[p.n_chunks] = b;
+  }
+  __syncthreads();
+  const int64_t n_def = pre_d[p.n_chunks], n_cand = pre_c[p.n_chunks];
+  const int64_t r = p.k - n_def;  // candidates to keep (>= 1)
+  const int64_t reg0 = row * p.n_chunks * p.chunk;
+  int32_t* A = reinterpret_cast<int32_t*>(dyn);  // [k]: entries above the threshold bin, ascending
+  int32_t* B = A + p.k;                          // [k]: kept candidates, ascending
+  uint32_t* ck = reinterpret_cast<uint32_t*>(B + p.k);  // [kCandCap] staged candidate keys
+  int32_t* ci = reinterpret_cast<int32_t*>(ck + kCandCap);
+  // gather both lists in chunk order
+  for (int c = 0; c < p.n_chunks; ++c) {
+    const int64_t reg = reg0 + (int64_t)c * p.chunk;
+    const int32_t nd = pre_d[c + 1] - pre_d[c], nc = pre_c[c + 1] - pre_c[c];
+    for (int32_t x = tid; x < nd; x += kTopkThreads) A[pre_d[c] + x] = p.def_idx[reg + x];
+    if (n_cand <= kCandCap)
+      for (int32_t x = tid; x < nc; x += kTopkThreads) {
+        ck[pre_c[c] + x] = p.cand_key[reg + x];
+        ci[pre_c[c] + x] = p.cand_idx[reg + x];
+      }
+  }
+  __syncthreads();
+  // exact selection of r among the candidates (staged, or read in place when too many)
+  auto staged = [&](int64_t x) { return ck[x]; };
+  auto chunk_of = [&](int64_t x) {
+    int lo = 0, hi = p.n_chunks - 1;  // last chunk c with pre_c[c] <= x
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre_c[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+  };
+  auto inplace = [&](int64_t x) {
+    const int c = chunk_of(x);
+    return p.cand_key[reg0 + (int64_t)c * p.chunk + (x - pre_c[c])];
+  };
+  uint32_t T, ties;
+  if (n_cand <= kCandCap) {
+    radix_select(staged, n_cand, r, S, T, ties);
+    collect_ordered(staged, n_cand, T, ties, S, [&](uint32_t slot, int64_t x) { B[slot] = ci[x]; });
+  } else {
+    radix_select(inplace, n_cand, r, S, T, ties);
+    collect_ordered(inplace, n_cand, T, ties, S, [&](uint32_t slot, int64_t x) {
+      const int c = chunk_of(x);
+      B[slot] = p.cand_idx[reg0 + (int64_t)c * p.chunk + (x - pre_c[c])];
+    });
+  }
+  __syncthreads();
+  // merge the two ascending, disjoint lists: slot = own rank + rank in the other list
+  for (int64_t x = tid; x < n_def + r; x += kTopkThreads) {
+    const bool in_a = x < n_def;
+    const int32_t v = in_a ? A[x] : B[x - n_def];
+    const int32_t* other = in_a ? B : A;
+    int64_t lo = 0, hi = in_a ? r : n_def;  // count of elements of `other` below v
+    while (lo < hi) {
+      const int64_t mid = (lo + hi) >> 1;
+      if (other[mid] < v) lo = mid + 1; else hi = mid;
+    }
+    const int64_t slot = (in_a ? x : x - n_def) + lo;
+    out[slot] = v;
+    if (out_sc) out_sc[slot] = sc[v];
+  }
+}
+
+// ------------------------------------------------------------------ host
+
+struct TopkPlan {
+  bool three;
+  int64_t chunk;
+  int n_chunks;
+};
+
+static TopkPlan plan_topk(const hyb_index_args* a, int64_t n_vis_max) {
+  TopkPlan pl{false, 0, 0};
+  if (n_vis_max <= kStageCap) return pl;
+  const int64_t rows = a->batch * a->n_q;
+  int64_t P = (2 * kNumSMs + rows - 1) / rows;
+  P = std::max<int64_t>(1, std::min<int64_t>(P, kMaxChunks));
+  int64_t chunk = (n_vis_max + P - 1) / P;
+  chunk = (chunk + 1023) / 1024 * 1024;
+  pl.three = true;
+  pl.chunk = chunk;
+  pl.n_chunks = (int)((n_vis_max + chunk - 1) / chunk);
+  return pl;
+}
+
+static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+size_t topk_workspace_bytes(const hyb_index_args* a, int64_t n_vis_max) {
+  const TopkPlan pl = plan_topk(a, n_vis_max);
+  if (!pl.three) return 0;
+  const size_t rows = (size_t)(a->batch * a->n_q);
+  const size_t region = rows * (size_t)pl.n_chunks * (size_t)pl.chunk;
+  return align256(rows * kHistBins * 4) + 3 * align256(region * 4) + align256(rows * pl.n_chunks * 8);
+}
+
+bool topk_shape_supported(const hyb_index_args* a, int64_t) { return a->k >= 1 && a->k <= 2048; }
+
+cudaError_t launch_topk(const hyb_index_args* a, const float* scores, int64_t score_stride, void* ws, cudaStream_t s) {
+  TopkParams p{};
   p.scores = scores, p.score_stride = score_stride, p.idx = a->idx, p.out_scores = a->scores;
   p.n_q = a->n_q, p.n_entries = a->n_entries, p.m = a->m, p.k = a->k, p.q_pos0 = a->q_pos0;
-  int64_t kp = 1;
-  while (kp < a->k) kp <<= 1;
-  p.kp = kp;
   const int64_t rows = a->batch * a->n_q;
   if (rows == 0) return cudaSuccess;
   const int64_t n_vis_max = std::min<int64_t>(visible_entries(a->q_pos0 + a->n_q - 1, a->m), a->n_entries);
-  if (n_vis_max <= kStageCap) {
-    const size_t smem = sizeof(uint32_t) * (size_t)kStageCap + sizeof(int32_t) * (size_t)kp;
-    cudaFuncSetAttribute(topk_radix_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    topk_radix_kernel<true><<<(unsigned)rows, kTopkThreads, smem, s>>>(p);
-  } else {
-    const size_t smem = sizeof(int32_t) * (size_t)kp;
-    cudaFuncSetAttribute(topk_radix_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    topk_radix_kernel<false><<<(unsigned)rows, kTopkThreads, smem, s>>>(p);
+  const TopkPlan pl = plan_topk(a, n_vis_max);
+  cudaError_t e;
+  if (!pl.three) {
+    const size_t smem = sizeof(uint32_t) * (size_t)kStageCap;
+    e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    topk_row_kernel<<<(unsigned)rows, kTopkThreads, smem, s>>>(p);
+    return cudaGetLastError();
   }
+  p.chunk = pl.chunk, p.n_chunks = pl.n_chunks;
+  const size_t region = (size_t)rows * pl.n_chunks * pl.chunk;
+  char* w = static_cast<char*>(ws);
+  p.ghist = reinterpret_cast<uint32_t*>(w);
+  w += align256((size_t)rows * kHistBins * 4);
+  p.def_idx = reinterpret_cast<int32_t*>(w);
+  w += align256(region * 4);
+  p.cand_key = reinterpret_cast<uint32_t*>(w);
+  w += align256(region * 4);
+  p.cand_idx = reinterpret_cast<int32_t*>(w);
+  w += align256(region * 4);
+  p.counts = reinterpret_cast<int32_t*>(w);
+  if ((e = cudaMemsetAsync(p.ghist, 0, (size_t)rows * kHistBins * 4, s)) != cudaSuccess) return e;
+  const dim3 grid((unsigned)pl.n_chunks, (unsigned)rows);
+  topk_hist_kernel<<<grid, kTopkThreads, 0, s>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  topk_filter_kernel<<<grid, kTopkThreads, 0, s>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const size_t smem = (size_t)2 * a->k * 4 + (size_t)kCandCap * 8;
+  e = cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  topk_final_kernel<<<(unsigned)rows, kTopkThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,209 @@
+"""Parity of the tensor-core attention kernel (bf16, c = 512, heads in groups
+of 64) against the float64 oracle, on the cases its design makes special:
+key = value aliasing (the method's shared compressed entry), split lists with
+a combine, ragged last tiles, whole tiles of padding, empty lists, scores that
+move the softmax reference late in the list, and the window merge.
+
+Also the two-stage top-k plan (rows longer than the shared-memory stage),
+bit-exact against the oracle's selection on integer-valued scores with ties.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import TOL_BF16, max_abs, to_np
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _gen(seed):
+    g = torch.Generator()
+    g.manual_seed(seed)
+    return g
+
+
+def _randn(g, shape, std=1.0):
+    return (torch.randn(shape, generator=g) * std).to(torch.bfloat16)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from sparse_attention_gated_b300 import ops  # noqa: F401
+
+
+def _ops():
+    from sparse_attention_gated_b300 import ops
+
+    return ops
+
+
+def _status():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+def _csa(q, kv, vv, idx, scale):
+    st = _status()
+    o, lse = _ops().csa_attend(q.to(DEV), kv.to(DEV), vv.to(DEV), idx.to(DEV), scale=scale, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0, f"device status {st.item()}"
+    return to_np(o), to_np(lse)
+
+
+@pytest.mark.parametrize("B,n_q,n_h,N,k,seed", [
+    (4, 1, 128, 20000, 1024, 1),  # decode: 8 query-head groups, splits + combine
+    (8, 1, 64, 16384, 512, 2),    # Flash decode shape
+    (1, 1, 64, 3000, 300, 3),     # many splits of one group, ragged last tile
+    (2, 37, 128, 900, 200, 4),    # several queries per call, one split each
+])
+def test_csa_attend_aliased_entries(B, n_q, n_h, N, k, seed):
+    g = _gen(seed)
+    c = 512
+    q = _randn(g, (B, n_q, n_h, c))
+    kc = _randn(g, (B, N, c), 1 / math.sqrt(c))
+    idx = torch.stack([torch.stack([torch.sort(torch.randperm(N, generator=g)[:k]).values for _ in range(n_q)])
+                       for _ in range(B)]).int()
+    scale = 1 / math.sqrt(c)
+    o, lse = _csa(q, kc, kc, idx, scale)
+    ro, rl = oracle.csa_attend(q, kc, kc, idx, scale)
+    assert max_abs(o, ro) <= TOL_BF16
+    assert max_abs(lse, rl) <= TOL_BF16
+
+
+def test_csa_attend_padding_runs_duplicates_and_empty_lists():
+    """Whole tiles of -1 (at the start, in the middle), a list that is all
+    padding, and repeated entries (a multiset: each repeat counts)."""
+    g = _gen(5)
+    B, n_q, n_h, N, k, c = 2, 3, 64, 5000, 700, 512
+    q = _randn(g, (B, n_q, n_h, c))
+    kc = _randn(g, (B, N, c), 2 / math.sqrt(c))
+    idx = torch.randint(0, N, (B, n_q, k), generator=g).int()
+    idx[0, 0, :300] = -1          # first two tiles and more: nothing
+    idx[0, 1, 128:512] = -1       # three whole tiles in the middle
+    idx[1, 2, :] = -1             # empty list
+    idx[1, 0, 10:20] = idx[1, 0, 5]  # repeats
+    scale = 1 / math.sqrt(c)
+    o, lse = _csa(q, kc, kc, idx, scale)
+    ro, rl = oracle.csa_attend(q, kc, kc, idx, scale)
+    assert max_abs(o, ro) <= TOL_BF16
+    assert max_abs(lse, rl) <= TOL_BF16
+    assert np.all(o[1, 2] == 0) and np.all(np.isneginf(lse[1, 2]))
+
+
+@pytest.mark.parametrize("order", ["rising", "spike", "falling"])
+def test_softmax_reference_moves_late_in_the_list(order):
+    """Scores that span ~60 nats and peak late (or spike mid-list) force the
+    lazy softmax reference to move after output has accumulated."""
+    g = _gen(6)
+    B, n_q, n_h, N, c = 1, 2, 64, 1500, 512
+    q = _randn(g, (B, n_q, n_h, c))
+    base = torch.randn((B, N, c), generator=g) / math.sqrt(c)
+    if order == "rising":
+        gain = torch.linspace(0.2, 12.0, N)
+    elif order == "falling":
+        gain = torch.linspace(12.0, 0.2, N)
+    else:
+        gain = torch.full((N,), 1.0)
+        gain[900:905] = 14.0
+    kc = (base * gain[None, :, None]).to(torch.bfloat16)
+    vc = _randn(g, (B, N, c), 1 / math.sqrt(c))
+    idx = torch.arange(N, dtype=torch.int32).expand(B, n_q, N).contiguous()
+    scale = 1 / math.sqrt(c) * 8
+    o, lse = _csa(q, kc, vc, idx, scale)
+    ro, rl = oracle.csa_attend(q, kc, vc, idx, scale)
+    assert max_abs(o, ro) <= TOL_BF16
+    assert np.max(np.abs(lse - rl) / np.maximum(1.0, np.abs(rl))) <= 2e-3
+
+
+@pytest.mark.parametrize("B,n_q,n_h,N,m,q_pos0", [
+    (4, 1, 128, 8192, 128, 8192 * 128 - 1),   # 1M-context HCA decode
+    (8, 1, 64, 2048, 128, 2048 * 128 - 1),    # Flash HCA decode
+    (1, 1, 64, 20000, 128, 20000 * 128 - 1),  # more tiles than SMs: splits of several tiles
+    (1, 300, 64, 80, 4, 0),                   # causal prefill: empty, short and ragged lists
+])
+def test_hca_attend_aliased_entries(B, n_q, n_h, N, m, q_pos0):
+    g = _gen(7)
+    c = 512
+    q = _randn(g, (B, n_q, n_h, c))
+    kc = _randn(g, (B, N, c), 1 / math.sqrt(c))
+    scale = 1 / math.sqrt(c)
+    st = _status()
+    o, lse = _ops().hca_attend(q.to(DEV), kc.to(DEV), kc.to(DEV), m=m, q_pos0=q_pos0, scale=scale, dev_status=st)
+    assert st.item() == 0, f"device status {st.item()}"
+    ro, rl = oracle.hca_attend(q, kc, kc, m=m, q_pos0=q_pos0, scale=scale)
+    assert max_abs(to_np(o), ro) <= TOL_BF16
+    assert max_abs(to_np(lse), rl) <= TOL_BF16
+
+
+@pytest.mark.parametrize("B,n_q,n_h,n_win,kv_pos0,n_kv,q_pos0,out_dtype", [
+    (4, 1, 128, 128, 2 ** 20 - 128, 128, 2 ** 20 - 1, torch.bfloat16),  # decode window
+    (1, 200, 128, 128, 0, 200, 0, torch.bfloat16),                      # prefill: windows cut by the start
+    (2, 3, 64, 100, 40, 300, 250, torch.float32),                       # window not a multiple of 128
+])
+def test_swa_merge_aliased_window(B, n_q, n_h, n_win, kv_pos0, n_kv, q_pos0, out_dtype):
+    g = _gen(8)
+    c = 512
+    q = _randn(g, (B, n_q, n_h, c))
+    kv = _randn(g, (B, n_kv, c), 1 / math.sqrt(c))
+    o_in = torch.randn((B, n_q, n_h, c), generator=g) * 0.05
+    lse_in = torch.randn((B, n_q, n_h), generator=g) * 2 + 5
+    lse_in[0, 0, :7] = -math.inf
+    scale = 1 / math.sqrt(c)
+    st = _status()
+    out = _ops().swa_merge(q.to(DEV), kv.to(DEV), kv.to(DEV), kv_pos0=kv_pos0, q_pos0=q_pos0, n_win=n_win,
+                           scale=scale, o_in=o_in.to(DEV), lse_in=lse_in.to(DEV), out_dtype=out_dtype, dev_status=st)
+    assert st.item() == 0, f"device status {st.item()}"
+    ro, _ = oracle.swa_merge(q, kv, kv, kv_pos0, q_pos0, n_win, scale, o_in.double().numpy(),
+                             lse_in.double().numpy())
+    assert max_abs(to_np(out), ro) <= TOL_BF16
+
+
+def test_attention_reads_no_row_outside_the_visible_set():
+    """Future entries (beyond floor((t+1)/m)) and rows past a ragged last tile
+    are NaN: the outputs must not change."""
+    g = _gen(9)
+    B, n_q, n_h, N, m, c = 1, 40, 64, 200, 4, 512
+    q = _randn(g, (B, n_q, n_h, c))
+    kc = _randn(g, (B, N, c), 1 / math.sqrt(c))
+    q_pos0 = 300  # sees 75 .. 84 entries of 200
+    scale = 1 / math.sqrt(c)
+    o, lse = _ops().hca_attend(q.to(DEV), kc.to(DEV), kc.to(DEV), m=m, q_pos0=q_pos0, scale=scale)
+    poisoned = kc.clone()
+    poisoned[:, (q_pos0 + n_q) // m:] = float("nan")
+    o2, lse2 = _ops().hca_attend(q.to(DEV), poisoned.to(DEV), poisoned.to(DEV), m=m, q_pos0=q_pos0, scale=scale)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+
+
+# ------------------------------------------------------------ two-stage top-k
+
+
+@pytest.mark.parametrize("B,n_q,N,k", [
+    (1, 3, 40000, 512),   # chunks of 864, a short last chunk
+    (2, 2, 16390, 1024),  # just past the one-stage limit: one 6-entry last chunk
+    (4, 1, 262144, 1024),  # the 1M-context decode shape
+])
+def test_two_stage_topk_is_bit_exact_with_ties(B, n_q, N, k):
+    """Small-integer indexer inputs give exactly representable scores with many
+    ties; the selection must equal the oracle's (score desc, index asc) exactly."""
+    g = _gen(10)
+    n_ih, c_I, m = 4, 16, 4
+    qI = torch.randint(-2, 3, (B, n_q, n_ih, c_I), generator=g).float()
+    kI = torch.randint(-2, 3, (B, N, c_I), generator=g).float()
+    w = torch.randint(0, 3, (B, n_q, n_ih), generator=g).float()
+    q_pos0 = m * N - n_q
+    idx, sc = _ops().csa_index_topk(qI.to(DEV), w.to(DEV), kI.to(DEV), m=m, k=k, q_pos0=q_pos0, want_scores=True)
+    ref = oracle.index_scores(qI, w, kI, m=m, q_pos0=q_pos0)
+    vis = np.array([min(oracle.visible(q_pos0 + j, m), N) for j in range(n_q)])
+    want = oracle.topk(ref, np.broadcast_to(vis, (B, n_q)), k)
+    got = idx.cpu().numpy()
+    assert np.array_equal(got, want)
+    gs = sc.cpu().numpy()
+    for b in range(B):
+        for j in range(n_q):
+            assert np.array_equal(gs[b, j], ref[b, j, want[b, j]].astype(np.float32))
