@@ -25,19 +25,21 @@
 // tile's loads and S^T overlap this tile's softmax within 227 KB of shared
 // memory (the query group alone takes 64 KB).
 //
-// Warp roles (256 threads, one CTA per SM):
+// Warp roles (384 threads, one CTA per SM):
 //   warps 0-2  producers: the query group by TMA once; entry slabs by TMA when
 //              a tile is 128 consecutive rows, otherwise (index lists, ragged
 //              last tile) gathered with 16-byte cp.async into the same
 //              swizzled layout, rows without an entry zero-filled; for the
 //              window merge, the compressed-branch output by one bulk copy.
 //   warp 3     TMEM owner and MMA issuer (one elected thread).
-//   warps 4-7  softmax and epilogue: thread e owns TMEM lane e (entry e of a
-//              tile, head-dim row e of an O^T chunk).
+//   warps 4-11 softmax and epilogue: two warps per TMEM lane quadrant, one
+//              per half of the 64 heads; thread (e, half) owns TMEM lane e
+//              (entry e of a tile, head-dim row e of an O^T chunk) for its
+//              32 heads.
 // Online softmax in base 2 with a lazy reference: the per-head reference
 // m[h] only moves when some score exceeds it by more than 2^8, which a
-// block-wide vote detects; only then are the tile maxima reduced across the
-// 128 entry lanes and the O^T accumulator rescaled.  Per-thread partial
+// vote of the softmax warps detects; only then are the tile maxima reduced
+// across the 128 entry lanes and the O^T accumulator rescaled.  Per-thread partial
 // denominators are reduced across lanes once, at the end.
 //
 // Splits of one query's list write unnormalised partials (o, m, l) that a
@@ -51,6 +53,8 @@ namespace hyb {
 
 namespace {
 
+constexpr int kProdWarps = 3, kMmaWarp = 3, kSoftWarp0 = 4, kSoftWarps = 8, kNumWarps = 12;
+constexpr int kSoftThreads = kSoftWarps * 32;
 constexpr int kHG = 64;                 // query heads per CTA (MMA N)
 constexpr int kC = 512;                 // head dim c
 constexpr int kTile = 128;              // entries per tile
@@ -61,18 +65,20 @@ constexpr int kOffQ = 0;
 constexpr int kOffKV = kOffQ + kSlabs * kQSlabBytes;
 constexpr int kOffP = kOffKV + kSlabs * kSlabBytes;
 constexpr int kOffRed = kOffP + kTile * kHG * 2;
-// float scratch: red[4][64], m[2][64], alpha[64], coef[2][64]
-constexpr int kRedFloats = 4 * 64 + 2 * 64 + 64 + 2 * 64;
-constexpr int kOffVote = kOffRed + kRedFloats * 4;
-constexpr int kOffBar = kOffVote + 8 * 4;
-constexpr int kNumBars = 1 + 2 * kSlabs + 2 + 2 + 1 + 1 + 1 + 1 + 1;
+// float scratch: red[2][64][4] (per-tile cross-quadrant exchange, double-buffered by
+// tile parity: head-major so that one 16-byte load gets a head's four quadrants) and
+// wt[8 warps][4][32] (each softmax warp's per-head table: reference, rescale factor,
+// output coefficients)
+constexpr int kRedFloats = 2 * 64 * 4 + 8 * 4 * 32 + 2 * 64;  // + ml[64] float2: (m, l) per head
+constexpr int kOffBar = kOffRed + kRedFloats * 4;
+constexpr int kNumBars = 1 + 2 * kSlabs + 2 + 2 + 1 + 1 + 2 + 1 + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;    // O^T: chunk ch at columns 64ch .. 64ch+63
 constexpr uint32_t kTmemS = 256;  // S^T: buffer b at columns 256+64b ..
 constexpr float kTau = 8.0f;      // lazy-reference threshold (log2 units): p <= 2^8
-constexpr int kProdWarps = 3, kMmaWarp = 3, kSoftWarp0 = 4, kNumWarps = 8;
+constexpr int kPrefetchAhead = 2;  // tiles whose rows are prefetched into L2 ahead of their loads
 constexpr int kThreads = kNumWarps * 32;
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -92,6 +98,7 @@ struct AtcParams {
   int out_bf16;
   int64_t n_q, n_h, n_entries, kv_stride, list_len, m, q_pos0, kv_pos0, n_win;
   int n_split, n_hg, alias;
+  int cluster;  // the n_split CTAs of a (query, head group) form one cluster and merge through DSMEM
   float scale_log2;
   int32_t* dev_status;
 };
@@ -107,9 +114,9 @@ struct AtcWork {
 template <int MODE>
 __device__ __forceinline__ AtcWork atc_work(const AtcParams& p) {
   AtcWork w;
-  const int64_t id = blockIdx.x;
-  w.hg = id % p.n_hg;
-  w.sp = (id / p.n_hg) % p.n_split;
+  const int64_t id = blockIdx.x;  // split fastest: the splits of a unit are consecutive CTAs (one cluster)
+  w.sp = id % p.n_split;
+  w.hg = (id / p.n_split) % p.n_hg;
   w.bq = id / ((int64_t)p.n_hg * p.n_split);
   w.b = w.bq / p.n_q;
   w.j = w.bq % p.n_q;
@@ -176,35 +183,24 @@ __device__ __forceinline__ int atc_gather_warp(int64_t g) {
   return MODE == 0 ? (int)(g % kProdWarps) : 0;
 }
 
-// Reduce 64 per-lane values (a: heads 0-31, b: heads 32-63) across the 32
-// lanes of a warp by recursive halving: after the five exchange steps lane l
-// holds the reduction for heads 2l and 2l+1.  62 shuffles instead of 320.
+// Reduce 32 per-lane values (one per head) across the 32 lanes of a warp by
+// recursive halving: after the five exchange steps lane l holds the reduction
+// for value l.  31 shuffles instead of 160.
 template <bool MAX>
-__device__ __forceinline__ void transpose_reduce(float (&a)[32], float (&b)[32], int lane, float& r0, float& r1) {
-  {
-    const bool up = lane & 16;
+__device__ __forceinline__ float transpose_reduce32(float (&a)[32], int lane) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float send = up ? a[i] : b[i];
-      const float keep = up ? b[i] : a[i];
-      const float got = __shfl_xor_sync(0xffffffffu, send, 16);
-      a[i] = MAX ? fmaxf(keep, got) : keep + got;
-    }
-  }
-#pragma unroll
-  for (int o = 8; o >= 1; o >>= 1) {
+  for (int o = 16; o >= 1; o >>= 1) {
     const bool up = lane & o;
 #pragma unroll
-    for (int i = 0; i < 2 * o; ++i) {
-      const float lo = a[i], hi = a[i + 2 * o];
+    for (int i = 0; i < o; ++i) {
+      const float lo = a[i], hi = a[i + o];
       const float send = up ? lo : hi;
       const float keep = up ? hi : lo;
       const float got = __shfl_xor_sync(0xffffffffu, send, o);
       a[i] = MAX ? fmaxf(keep, got) : keep + got;
     }
   }
-  r0 = a[0];
-  r1 = a[1];
+  return a[0];
 }
 
 template <int MODE>
@@ -216,11 +212,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* q_s = smem + kOffQ;
   uint8_t* kv_s = smem + kOffKV;
   uint8_t* p_s = smem + kOffP;
-  float* red = reinterpret_cast<float*>(smem + kOffRed);  // [4][64]
-  float* m_s = red + 4 * 64;                                // [2][64]
-  float* alpha_s = m_s + 2 * 64;                            // [64]
-  float* coef_s = alpha_s + 64;                             // [2][64]
-  volatile int* vote = reinterpret_cast<volatile int*>(smem + kOffVote);  // [2][4]
+  float* red = reinterpret_cast<float*>(smem + kOffRed);  // [2][64][4]
+  float* wtab = red + 2 * 64 * 4;                           // [8][4][32]
+  float2* ml_s = reinterpret_cast<float2*>(wtab + 8 * 4 * 32);  // [64] (m, l) of this CTA (cluster merge)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* q_full = bars;
   uint64_t* kv_full = q_full + 1;
@@ -229,8 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_empty = s_full + 2;
   uint64_t* p_full = s_empty + 2;
   uint64_t* o_done = p_full + 1;
-  uint64_t* sm_sync = o_done + 1;
-  uint64_t* fin = sm_sync + 1;
+  uint64_t* sm_sync = o_done + 1;  // [2]: one per head half (4 softmax warps each)
+  uint64_t* fin = sm_sync + 2;
   uint64_t* oin_full = fin + 1;
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kOffMisc);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc) + 1;
@@ -239,31 +233,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   const AtcWork W = atc_work<MODE>(p);
   const int64_t ntiles = W.te - W.tb;
 
+  // the first group's loads are issued by the thread that initialises the
+  // barriers, before the CTA-wide setup sync (overlapping the TMEM allocation)
+  const bool pre_k = MODE != 0 && ntiles > 0 && (W.tb + 1) * kTile <= W.L;
   if (threadIdx.x == 0) {
     tc::mbar_init(q_full, 1);
     for (int s = 0; s < kSlabs; ++s) tc::mbar_init(&kv_full[s], 1), tc::mbar_init(&kv_empty[s], 1);
-    for (int i = 0; i < 2; ++i) tc::mbar_init(&s_full[i], 1), tc::mbar_init(&s_empty[i], 4);
-    tc::mbar_init(p_full, 4);
+    for (int i = 0; i < 2; ++i) tc::mbar_init(&s_full[i], 1), tc::mbar_init(&s_empty[i], kSoftWarps);
+    tc::mbar_init(p_full, kSoftWarps);
     tc::mbar_init(o_done, 1);
-    tc::mbar_init(sm_sync, 128);
+    tc::mbar_init(&sm_sync[0], kSoftThreads / 2);
+    tc::mbar_init(&sm_sync[1], kSoftThreads / 2);
     tc::mbar_init(fin, 1);
     tc::mbar_init(oin_full, 1);
     *s_abort = 0;
     tc::fence_barrier_init();
+    if (ntiles > 0) {
+      tc::prefetch_tmap(&tm_q);
+      tc::mbar_arrive_expect_tx(q_full, kSlabs * kQSlabBytes);
+      const int32_t qrow = (int32_t)(W.bq * p.n_h + W.hg * kHG);
+      for (int s = 0; s < kSlabs; ++s) tc::tma_load_2d(q_s + s * kQSlabBytes, &tm_q, q_full, 64 * s, qrow);
+    }
+    if (pre_k) {
+      tc::prefetch_tmap(&tm_k);
+      for (int s = 0; s < kSlabs; ++s) {
+        tc::mbar_arrive_expect_tx(&kv_full[s], kSlabBytes);
+        tc::tma_load_2d(kv_s + s * kSlabBytes, &tm_k, &kv_full[s], 64 * s, (int32_t)(W.row0 + W.tb * kTile));
+      }
+    }
+    if (MODE != 0) tc::prefetch_tmap(&tm_v);
   }
   if (warp == kMmaWarp) tc::tmem_alloc(s_tmem, kTmemCols);
-  if (warp == 0 && lane == 0) {
-    tc::prefetch_tmap(&tm_q);
-    if (MODE != 0) {
-      tc::prefetch_tmap(&tm_k);
-      tc::prefetch_tmap(&tm_v);
-    }
-  }
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
+  bool sm_ok = false;  // softmax warps: the main loop and epilogue completed
   if (warp < kProdWarps) {
     // ================================================================ producers
     bool ok = true;
@@ -271,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int npend = 0;
     int64_t tma_u[kSlabs];  // last use count of each slot filled by TMA (for the drain on abort)
 #pragma unroll
-    for (int s = 0; s < kSlabs; ++s) tma_u[s] = -1;
+    for (int s = 0; s < kSlabs; ++s) tma_u[s] = pre_k ? 0 : -1;
     // make this warp's finished gathers visible to the MMA and signal them
     auto flush = [&]() {
       if (npend) {
@@ -283,20 +289,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         npend = 0;
       }
     };
-    if (warp == 0 && ntiles > 0) {
-      if (lane == 0) {
-        tc::mbar_arrive_expect_tx(q_full, kSlabs * kQSlabBytes);
-        const int32_t qrow = (int32_t)(W.bq * p.n_h + W.hg * kHG);
-        for (int s = 0; s < kSlabs; ++s) tc::tma_load_2d(q_s + s * kQSlabBytes, &tm_q, q_full, 64 * s, qrow);
-      }
-      __syncwarp();
-    }
     const int64_t ngroups = 2 * ntiles;
-    int64_t g = 0;  // slab sequence number
-    for (int64_t G = 0; G < ngroups && ok; ++G) {
+    // L2 prefetch of the entry rows kPrefetchAhead tiles ahead of the K group being
+    // loaded, so the loads that later fill the ring pay L2 rather than HBM latency
+    auto prefetch_tile = [&](int64_t i) {
+      if (i >= W.te) return;
+      if (MODE != 0) {
+        if (warp == 0 && lane == 0) {
+          const int64_t n = std::min<int64_t>(kTile, W.L - i * kTile);
+          tc::prefetch_l2(p.k + (W.row0 + i * kTile) * kC, (uint32_t)(n * kC * 2));
+        }
+      } else if (warp == 0) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int64_t row = atc_row<MODE>(p, W, i * kTile + lane + 32 * r, false);
+          if (row >= 0) tc::prefetch_l2(p.k + row * kC, kC * 2);
+        }
+      }
+    };
+    for (int64_t a = 1; a <= kPrefetchAhead; ++a) prefetch_tile(W.tb + a);
+    int64_t g = pre_k ? kSlabs : 0;  // slab sequence number
+    for (int64_t G = pre_k ? 1 : 0; G < ngroups && ok; ++G) {
       bool is_v;
       const int64_t li = atc_group(G, ngroups, is_v);
       const int64_t i = W.tb + li;
+      if (!is_v && li > 0) prefetch_tile(i + kPrefetchAhead);
       const bool tma_tile = MODE != 0 && (i + 1) * kTile <= W.L;
       int64_t rows[4];
       if (!tma_tile) {
@@ -445,211 +462,324 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ================================================================ softmax + epilogue
-    const int q4 = warp & 3;            // TMEM lane quadrant of this warp
-    const int e = q4 * 32 + lane;       // tile entry / O^T chunk row owned by this thread
-    const int st = threadIdx.x - kSoftWarp0 * 32;  // 0..127
+    // Warp w owns TMEM lane quadrant w % 4 (entries / head-dim rows 32(w%4) ..)
+    // and head half hh = (w - 4) / 4 (heads 32hh .. 32hh+31).  The four warps
+    // of a half exchange per-head values through shared memory and meet on
+    // their own barrier; the halves never wait on each other.
+    const int q4 = warp & 3;
+    const int hh = (warp - kSoftWarp0) >> 2;
+    const int e = q4 * 32 + lane;  // tile entry / O^T chunk row owned by this thread
+    const int h0 = hh * 32;        // first head of this thread
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    uint64_t* my_sync = &sm_sync[hh];
     uint32_t sync_phase = 0;
-    auto gsync = [&]() -> bool {
-      tc::mbar_arrive(sm_sync);
-      const bool r = tc::mbar_wait(sm_sync, sync_phase, s_abort, 9);
+    auto hsync = [&]() -> bool {
+      tc::mbar_arrive(my_sync);
+      const bool r = tc::mbar_wait(my_sync, sync_phase, s_abort, 9);
       sync_phase ^= 1u;
       return r;
     };
-    float lp[64];
+    float lp[32];  // partial denominators of this entry lane, per head
 #pragma unroll
-    for (int h = 0; h < 64; ++h) lp[h] = 0.f;
-    int mcur = 0;
-    if (st < 64) m_s[st] = -INFINITY, m_s[64 + st] = -INFINITY;
-    bool ok = gsync();
+    for (int h = 0; h < 32; ++h) lp[h] = 0.f;
+    // This warp's table, one column per head of its half; lane l owns head h0+l:
+    //   wt_m: softmax reference (log2 units), wt_a: rescale factor of the tile,
+    //   wt_cw / wt_cc: output coefficients of the accumulator / of o_in.
+    // Every warp of a half computes the same values from the same inputs.
+    float* wt_m = wtab + (warp - kSoftWarp0) * 128;
+    float* wt_a = wt_m + 32;
+    float* wt_cw = wt_m + 64;
+    float* wt_cc = wt_m + 96;
+    wt_m[lane] = -INFINITY;
+    __syncwarp();
+    bool ok = true;
 
     for (int64_t li = 0; li < ntiles && ok; ++li) {
       const int64_t i = W.tb + li;
       const int sb = (int)(li & 1);
       if (!(ok = tc::mbar_wait(&s_full[sb], (uint32_t)((li >> 1) & 1), s_abort, 8))) break;
       tc::tc_fence_after();
-      const uint32_t sS = tmem + lane_base + kTmemS + (uint32_t)(sb * kHG);
+      const uint32_t sS = tmem + lane_base + kTmemS + (uint32_t)(sb * kHG + h0);
       const bool valid = atc_row<MODE>(p, W, i * kTile + e, false) >= 0;
-      float sa[32], sb2[32];
+      float sv[32];
       auto load_scores = [&]() {
-        tc::tmem_ld32(sS, sa);
-        tc::tmem_ld32(sS + 32, sb2);
+        tc::tmem_ld32(sS, sv);
         tc::tmem_ld_wait();
 #pragma unroll
-        for (int h = 0; h < 32; ++h) {
-          sa[h] = valid ? sa[h] * p.scale_log2 : -INFINITY;
-          sb2[h] = valid ? sb2[h] * p.scale_log2 : -INFINITY;
-        }
+        for (int h = 0; h < 32; ++h) sv[h] = valid ? sv[h] * p.scale_log2 : -INFINITY;
       };
       load_scores();
-      const float* mref = m_s + mcur * 64;
-      bool exceed = false;
-#pragma unroll
-      for (int h = 0; h < 32; ++h) exceed |= (sa[h] > mref[h] + kTau) | (sb2[h] > mref[32 + h] + kTau);
-      const int any_w = __any_sync(0xffffffffu, exceed);
-      if (lane == 0) vote[sb * 4 + q4] = any_w;
-      if (!(ok = gsync())) break;
-      const bool any = (vote[sb * 4 + 0] | vote[sb * 4 + 1] | vote[sb * 4 + 2] | vote[sb * 4 + 3]) != 0;
+      // tile maximum of each head: over this warp's 32 entries (lane l gets head h0+l),
+      // then over the 4 quadrants through shared memory
+      float* redb = red + sb * 256;
+      redb[(h0 + lane) * 4 + q4] = transpose_reduce32<true>(sv, lane);
+      if (!(ok = hsync())) break;
+      // lazy reference of head h0+lane: moves only when the tile maximum exceeds it by
+      // more than 2^kTau (or there was none)
+      {
+        const float4 r4 = *reinterpret_cast<const float4*>(redb + (h0 + lane) * 4);
+        const float tmax = fmaxf(fmaxf(r4.x, r4.y), fmaxf(r4.z, r4.w));
+        const float mo = wt_m[lane];
+        const bool mv = tmax > mo + kTau || (mo == -INFINITY && tmax != -INFINITY);
+        wt_a[lane] = mv ? exp2f(mo - tmax) : 1.f;  // 0 when there was no reference
+        wt_m[lane] = mv ? tmax : mo;
+      }
+      const bool moved = __any_sync(0xffffffffu, wt_a[lane] != 1.f);
+      __syncwarp();
       bool odone = false;
-      if (any) {
-        // move the reference to the tile maximum of every head
-        float r0, r1;
-        transpose_reduce<true>(sa, sb2, lane, r0, r1);
-        red[q4 * 64 + 2 * lane] = r0;
-        red[q4 * 64 + 2 * lane + 1] = r1;
-        if (!(ok = gsync())) break;
-        if (st < 64) {
-          const float mo = mref[st];
-          const float mn = fmaxf(fmaxf(mo, fmaxf(red[st], red[64 + st])), fmaxf(red[128 + st], red[192 + st]));
-          m_s[(mcur ^ 1) * 64 + st] = mn;
-          alpha_s[st] = mn == -INFINITY ? 1.f : exp2f(mo - mn);
-        }
-        if (!(ok = gsync())) break;
-        mcur ^= 1;
+      if (moved) {
+        float al[32];
 #pragma unroll
-        for (int h = 0; h < 64; ++h) lp[h] *= alpha_s[h];
+        for (int x = 0; x < 8; ++x) {
+          const float4 a4 = *reinterpret_cast<const float4*>(wt_a + 4 * x);
+          al[4 * x] = a4.x, al[4 * x + 1] = a4.y, al[4 * x + 2] = a4.z, al[4 * x + 3] = a4.w;
+        }
+#pragma unroll
+        for (int h = 0; h < 32; ++h) lp[h] *= al[h];
         if (li > 0) {
-          // rescale O^T once the previous tile's products are complete
+          // rescale this thread's O^T lane (its heads, every chunk) once the previous products are done
           if (!(ok = tc::mbar_wait(o_done, (uint32_t)((li - 1) & 1), s_abort, 10))) break;
           odone = true;
           tc::tc_fence_after();
 #pragma unroll 1
-          for (int x = 0; x < 8; ++x) {
+          for (int ch = 0; ch < 4; ++ch) {
             float v[32];
-            const uint32_t ta = tmem + lane_base + kTmemO + (uint32_t)(x * 32);
+            const uint32_t ta = tmem + lane_base + kTmemO + (uint32_t)(ch * kHG + h0);
             tc::tmem_ld32(ta, v);
             tc::tmem_ld_wait();
-            const float* al = alpha_s + (x & 1) * 32;
 #pragma unroll
             for (int y = 0; y < 32; ++y) v[y] *= al[y];
             tc::tmem_st32(ta, v);
           }
           tc::tmem_st_wait();
         }
-        load_scores();  // the reduction consumed the registers
       }
-      // probabilities of this entry for every head, as row e of P^T (bf16)
-      const float* mr = m_s + mcur * 64;
-      uint32_t pk[32];
-#pragma unroll
-      for (int h = 0; h < 32; h += 2) {
-        const float p0 = sa[h] == -INFINITY ? 0.f : exp2f(sa[h] - mr[h]);
-        const float p1 = sa[h + 1] == -INFINITY ? 0.f : exp2f(sa[h + 1] - mr[h + 1]);
-        const float p2 = sb2[h] == -INFINITY ? 0.f : exp2f(sb2[h] - mr[32 + h]);
-        const float p3 = sb2[h + 1] == -INFINITY ? 0.f : exp2f(sb2[h + 1] - mr[33 + h]);
-        lp[h] += p0, lp[h + 1] += p1, lp[32 + h] += p2, lp[33 + h] += p3;
-        pk[h / 2] = pack_bf16x2(p0, p1);
-        pk[16 + h / 2] = pack_bf16x2(p2, p3);
-      }
+      // probabilities of this entry for this thread's heads: 64 bytes of row e of P^T (bf16)
+      load_scores();  // the reduction consumed the registers
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&s_empty[sb]);
+      uint32_t pk[16];
+      if (valid) {
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+          const float4 m4 = *reinterpret_cast<const float4*>(wt_m + 4 * x);
+          const float p0 = exp2f(sv[4 * x] - m4.x), p1 = exp2f(sv[4 * x + 1] - m4.y);
+          const float p2 = exp2f(sv[4 * x + 2] - m4.z), p3 = exp2f(sv[4 * x + 3] - m4.w);
+          lp[4 * x] += p0, lp[4 * x + 1] += p1, lp[4 * x + 2] += p2, lp[4 * x + 3] += p3;
+          pk[2 * x] = pack_bf16x2(p0, p1);
+          pk[2 * x + 1] = pack_bf16x2(p2, p3);
+        }
+      } else {
+#pragma unroll
+        for (int x = 0; x < 16; ++x) pk[x] = 0u;
+      }
       if (li > 0 && !odone) {
         if (!(ok = tc::mbar_wait(o_done, (uint32_t)((li - 1) & 1), s_abort, 11))) break;
       }
       uint8_t* prow = p_s + (e >> 3) * 1024 + (e & 7) * 128;
 #pragma unroll
-      for (int c16 = 0; c16 < 8; ++c16)
+      for (int x = 0; x < 4; ++x) {
+        const int c16 = hh * 4 + x;
         *reinterpret_cast<uint4*>(prow + ((c16 ^ (e & 7)) << 4)) =
-            make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
+            make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+      }
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(p_full);
     }
 
+    // ---------------------------------------------------------------- epilogue
+    // denominators: reduce the per-entry partial sums of every head across the 128 entry lanes
+    float* redl = red + (int)(ntiles & 1) * 256;  // the buffer the last tile did not use
     if (ok) {
-      // denominators: reduce the per-entry partial sums of every head across the 128 lanes
-      {
-        float la[32], lb[32];
-#pragma unroll
-        for (int h = 0; h < 32; ++h) la[h] = lp[h], lb[h] = lp[32 + h];
-        float r0, r1;
-        transpose_reduce<false>(la, lb, lane, r0, r1);
-        red[q4 * 64 + 2 * lane] = r0;
-        red[q4 * 64 + 2 * lane + 1] = r1;
-      }
-      ok = gsync();
+      redl[(h0 + lane) * 4 + q4] = transpose_reduce32<false>(lp, lane);
+      ok = hsync();
     }
+    // output coefficients of head h0+lane (acc multiplier cw, o_in multiplier cc), its lse
     if (ok) {
-      if (st < 64) {
-        const int64_t H = W.hg * kHG + st;
-        const float l = (red[st] + red[64 + st]) + (red[128 + st] + red[192 + st]);
-        const float mm = m_s[mcur * 64 + st];
-        const float lse2 = l > 0.f ? mm + __log2f(l) : -INFINITY;  // log2 of the denominator
-        if constexpr (MODE == 2) {
-          const float lse_w = lse2 * kLn2;
-          const float lse_c = p.lse_in ? p.lse_in[W.bq * p.n_h + H] : -INFINITY;
-          const float M = fmaxf(lse_w, lse_c);
-          float wc = 0.f, ww = 0.f, Lse = -INFINITY;
-          if (M != -INFINITY) {
-            const float ec = lse_c == -INFINITY ? 0.f : expf(lse_c - M);
-            const float ew = lse_w == -INFINITY ? 0.f : expf(lse_w - M);
-            const float den = ec + ew;
-            wc = ec / den;
-            ww = ew / (den * (l > 0.f ? l : 1.f));  // the accumulator is unnormalised
-            Lse = M + logf(den);
-          }
-          coef_s[st] = ww;
-          coef_s[64 + st] = wc;
-          if (p.lse_out) p.lse_out[W.bq * p.n_h + H] = Lse;
-        } else if (p.n_split > 1) {
-          coef_s[st] = 1.f;
-          p.part_ml[(W.bq * p.n_split + W.sp) * p.n_h + H] = make_float2(l > 0.f ? mm : -INFINITY, l);
-        } else {
-          coef_s[st] = l > 0.f ? 1.f / l : 0.f;
-          p.lse[W.bq * p.n_h + H] = lse2 * kLn2;
+      const float4 r4 = *reinterpret_cast<const float4*>(redl + (h0 + lane) * 4);
+      const float l = (r4.x + r4.y) + (r4.z + r4.w);
+      const float mm = wt_m[lane];
+      const int64_t H = W.hg * kHG + h0 + lane;
+      const float lse2 = l > 0.f ? mm + __log2f(l) : -INFINITY;  // log2 of the denominator
+      float cw, cc = 0.f;
+      if constexpr (MODE == 2) {
+        // one softmax over the union of the window and the compressed set
+        const float lse_w = lse2 * kLn2;
+        const float lse_c = p.lse_in ? p.lse_in[W.bq * p.n_h + H] : -INFINITY;
+        const float M = fmaxf(lse_w, lse_c);
+        float Lse = -INFINITY;
+        cw = 0.f;
+        if (M != -INFINITY) {
+          const float ec = lse_c == -INFINITY ? 0.f : expf(lse_c - M);
+          const float ew = lse_w == -INFINITY ? 0.f : expf(lse_w - M);
+          const float den = ec + ew;
+          cc = ec / den;
+          cw = ew / (den * (l > 0.f ? l : 1.f));  // the accumulator is unnormalised
+          Lse = M + logf(den);
         }
+        if (q4 == 0 && p.lse_out) p.lse_out[W.bq * p.n_h + H] = Lse;
+      } else if (p.n_split > 1) {
+        cw = 1.f;
+        const float2 ml = make_float2(l > 0.f ? mm : -INFINITY, l);
+        if (q4 == 0) {
+          if (p.cluster)
+            ml_s[h0 + lane] = ml;  // merged with the other splits of the cluster below
+          else
+            p.part_ml[(W.bq * p.n_split + W.sp) * p.n_h + H] = ml;
+        }
+      } else {
+        cw = l > 0.f ? 1.f / l : 0.f;
+        if (q4 == 0) p.lse[W.bq * p.n_h + H] = lse2 * kLn2;
       }
-      ok = gsync();
+      wt_cw[lane] = cw;
+      wt_cc[lane] = cc;
+      __syncwarp();
     }
     if (ok && ntiles > 0) {
       ok = tc::mbar_wait(o_done, (uint32_t)((ntiles - 1) & 1), s_abort, 12);
       tc::tc_fence_after();
     }
+    sm_ok = ok;
     if constexpr (MODE == 2) {
       if (ok && p.o_in != nullptr) ok = tc::mbar_wait(oin_full, 0, s_abort, 14);
     }
-    if (ok) {
-      // O^T (TMEM) -> global: for a fixed head the 32 lanes of a warp store 32 consecutive dims
-      float* obase;
-      if constexpr (MODE == 2)
-        obase = nullptr;
-      else
-        obase = p.n_split > 1 ? p.part_o + ((W.bq * p.n_split + W.sp) * p.n_h + W.hg * kHG) * kC
-                              : p.o + (W.bq * p.n_h + W.hg * kHG) * kC;
+    if (ok && !(MODE != 2 && p.cluster)) {
+      // O^T (TMEM) -> this half's 32 rows of [64 heads][512] in shared memory -> one bulk store.
+      // Staging: float32 in the free K/V ring (in place over the staged o_in for a float32
+      // window merge), bf16 window-merge output in the free query region.
+      const bool out_bf16 = MODE == 2 && p.out_bf16;
+      float* stage32 = reinterpret_cast<float*>(kv_s) + h0 * kC;
+      __nv_bfloat16* stage16 = reinterpret_cast<__nv_bfloat16*>(q_s) + h0 * kC;
+      const float* oin = reinterpret_cast<const float*>(kv_s) + h0 * kC;  // staged o_in (window merge)
+      const bool have_oin = MODE == 2 && p.o_in != nullptr;
 #pragma unroll 1
-      for (int x = 0; x < 8; ++x) {
-        const int ch = x >> 1, h0 = (x & 1) * 32;
-        float v[32];
+      for (int ch = 0; ch < 4; ++ch) {
+        // every load of the chunk first (stores to shared memory in between would serialise them)
+        float v[32], cw[32], oc[32];
         if (ntiles > 0) {
-          tc::tmem_ld32(tmem + lane_base + kTmemO + (uint32_t)(x * 32), v);
-          tc::tmem_ld_wait();
+          tc::tmem_ld32(tmem + lane_base + kTmemO + (uint32_t)(ch * kHG + h0), v);
         } else {
 #pragma unroll
           for (int y = 0; y < 32; ++y) v[y] = 0.f;
         }
-        const int64_t d = ch * 128 + e;
-        if constexpr (MODE == 2) {
-          const int64_t rb = (W.bq * p.n_h + W.hg * kHG + h0) * kC + d;
-          const float* oin = reinterpret_cast<const float*>(kv_s) + h0 * kC + d;  // staged o_in, [64][512]
+        const int d = ch * 128 + e;
 #pragma unroll
-          for (int y = 0; y < 32; ++y) {
-            const float wc = coef_s[64 + h0 + y];
-            const float r = coef_s[h0 + y] * v[y] + (wc != 0.f ? wc * oin[y * kC] : 0.f);
-            if (p.out_bf16)
-              static_cast<__nv_bfloat16*>(p.out)[rb + (int64_t)y * kC] = __float2bfloat16_rn(r);
-            else
-              static_cast<float*>(p.out)[rb + (int64_t)y * kC] = r;
+        for (int x = 0; x < 8; ++x) {
+          const float4 a = *reinterpret_cast<const float4*>(wt_cw + 4 * x);
+          cw[4 * x] = a.x, cw[4 * x + 1] = a.y, cw[4 * x + 2] = a.z, cw[4 * x + 3] = a.w;
+        }
+        if (have_oin) {
+#pragma unroll
+          for (int x = 0; x < 8; ++x) {
+            const float4 b = *reinterpret_cast<const float4*>(wt_cc + 4 * x);
+            oc[4 * x] = b.x, oc[4 * x + 1] = b.y, oc[4 * x + 2] = b.z, oc[4 * x + 3] = b.w;
           }
+#pragma unroll
+          for (int y = 0; y < 32; ++y) oc[y] = oc[y] != 0.f ? oc[y] * oin[y * kC + d] : 0.f;
         } else {
 #pragma unroll
-          for (int y = 0; y < 32; ++y) obase[(int64_t)(h0 + y) * kC + d] = v[y] * coef_s[h0 + y];
+          for (int y = 0; y < 32; ++y) oc[y] = 0.f;
+        }
+        if (ntiles > 0) tc::tmem_ld_wait();
+#pragma unroll
+        for (int y = 0; y < 32; ++y) {
+          const float r = fmaf(cw[y], v[y], oc[y]);
+          if (out_bf16)
+            stage16[y * kC + d] = __float2bfloat16_rn(r);
+          else
+            stage32[y * kC + d] = r;
+        }
+      }
+      tc::fence_proxy_async_smem();
+      ok = hsync();
+      if (ok && q4 == 0 && lane == 0) {
+        void* dst;
+        if constexpr (MODE == 2)
+          dst = out_bf16 ? static_cast<void*>(static_cast<__nv_bfloat16*>(p.out) + (W.bq * p.n_h + W.hg * kHG + h0) * kC)
+                         : static_cast<void*>(static_cast<float*>(p.out) + (W.bq * p.n_h + W.hg * kHG + h0) * kC);
+        else
+          dst = p.n_split > 1 ? p.part_o + ((W.bq * p.n_split + W.sp) * p.n_h + W.hg * kHG + h0) * kC
+                              : p.o + (W.bq * p.n_h + W.hg * kHG + h0) * kC;
+        const uint32_t bytes = 32 * kC * (out_bf16 ? 2 : 4);
+        const uint8_t* src = out_bf16 ? reinterpret_cast<const uint8_t*>(stage16) : reinterpret_cast<const uint8_t*>(stage32);
+        for (uint32_t off = 0; off < bytes; off += 16384)
+          tc::bulk_store(static_cast<uint8_t*>(dst) + off, src + off, 16384);
+        tc::bulk_commit();
+        tc::bulk_wait_read();
+      }
+    }
+  }
+  __syncwarp();  // every warp reaches the cluster and CTA barriers converged
+  if constexpr (MODE != 2) {
+    if (p.cluster) {
+      // Merge the splits of this (query, head group) inside the cluster.  Every thread of
+      // every CTA passes both barriers, whatever happened before (no hardware wait is left
+      // open).  Between them, rank r scatters its O (scaled by its merge weight) into the
+      // owners' K/V rings (free once every CTA's last products are done): rank j owns dims
+      // [j*D, j*D+D), D = 512/S, received as [S ranks][64 heads][D].
+      const uint32_t S = (uint32_t)p.n_split, rank = (uint32_t)W.sp;
+      const int D = kC / (int)S;
+      tc::cluster_sync();  // every CTA's (m, l) table is written, every ring is free
+      if (warp >= kSoftWarp0 && sm_ok) {
+        const int q4 = warp & 3, hh = (warp - kSoftWarp0) >> 2, e = q4 * 32 + lane, h0 = hh * 32;
+        const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+        float* wt_cw = wtab + (warp - kSoftWarp0) * 128 + 64;
+        {
+          // merge weight of head h0+lane for this rank: one pass of log-sum-exp over the ranks
+          const uint32_t ml_addr = tc::smem_u32(ml_s + h0 + lane);
+          float M = -INFINITY, L = 0.f;
+          for (uint32_t r = 0; r < S; ++r) {
+            const float2 v = tc::ld_cluster_f32x2(tc::map_to_rank(ml_addr, r));
+            if (v.x == -INFINITY) continue;
+            const float Mn = fmaxf(M, v.x);
+            L = L * exp2f(M - Mn) + v.y * exp2f(v.x - Mn);  // exp2f(-inf) = 0 on the first rank
+            M = Mn;
+          }
+          const float2 self = ml_s[h0 + lane];
+          wt_cw[lane] = (L > 0.f && self.x != -INFINITY) ? exp2f(self.x - M) / L : 0.f;
+          if (rank == 0 && q4 == 0)
+            p.lse[W.bq * p.n_h + W.hg * kHG + h0 + lane] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
+          __syncwarp();
+        }
+        const uint32_t recv0 = tc::smem_u32(kv_s);
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          float v[32], cw[32];
+          if (ntiles > 0) {
+            tc::tmem_ld32(tmem + lane_base + kTmemO + (uint32_t)(ch * kHG + h0), v);
+          } else {
+#pragma unroll
+            for (int y = 0; y < 32; ++y) v[y] = 0.f;
+          }
+#pragma unroll
+          for (int x = 0; x < 8; ++x) {
+            const float4 a = *reinterpret_cast<const float4*>(wt_cw + 4 * x);
+            cw[4 * x] = a.x, cw[4 * x + 1] = a.y, cw[4 * x + 2] = a.z, cw[4 * x + 3] = a.w;
+          }
+          if (ntiles > 0) tc::tmem_ld_wait();
+          const int d = ch * 128 + e;
+          const uint32_t j = (uint32_t)(d / D), dd = (uint32_t)(d - (int)j * D);
+          const uint32_t dst = tc::map_to_rank(recv0, j) + ((rank * 64 + (uint32_t)h0) * (uint32_t)D + dd) * 4;
+#pragma unroll
+          for (int y = 0; y < 32; ++y) tc::st_cluster_f32(dst + (uint32_t)(y * D * 4), cw[y] * v[y]);
+        }
+      }
+      tc::cluster_sync();  // every slice has arrived
+      if (warp >= kSoftWarp0 && sm_ok) {
+        const float* recv = reinterpret_cast<const float*>(kv_s);
+        float* obase = p.o + (W.bq * p.n_h + W.hg * kHG) * kC + rank * D;
+        for (int t = threadIdx.x - kSoftWarp0 * 32; t < 64 * D; t += kSoftThreads) {
+          const int h = t / D, dd = t - h * D;
+          float acc = 0.f;
+          for (uint32_t r = 0; r < S; ++r) acc += recv[(r * 64 + h) * D + dd];
+          obase[(int64_t)h * kC + dd] = acc;
         }
       }
     }
   }
-
   tc::tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0 && *s_abort) flag_status(p.dev_status, HYB_DEV_TIMEOUT | ((*s_abort & 0xFF) << 8));
@@ -707,20 +837,69 @@ bool attend_tc_supported(const AttendJob& j) {
   return true;
 }
 
-int attend_tc_splits(const AttendJob& j) {
-  if (j.mode == 2) return 1;
+namespace {
+
+struct AtcPlan {
+  int n_split;
+  bool cluster;
+};
+
+// How many clusters of S CTAs of the given mode can be resident at once (queried once per mode and size).
+int clusters_resident(int mode, int S) {
+  static int cache[3][17];  // 0 unknown, else 1 + count
+  if (S < 2 || S > 16) return 0;
+  int& c = cache[mode][S];
+  if (c == 0) {
+    const void* fn = mode == 0 ? (const void*)attend_tc_kernel<0> : (const void*)attend_tc_kernel<1>;
+    bool ok = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) == cudaSuccess;
+    if (ok && S > 8) ok = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+    int n = 0;
+    if (ok) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)S), cfg.blockDim = dim3(kThreads), cfg.dynamicSmemBytes = kSmemBytes;
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = (unsigned)S, attr.val.clusterDim.y = 1, attr.val.clusterDim.z = 1;
+      cfg.attrs = &attr, cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();  // a refused query leaves no sticky error
+    c = 1 + n;
+  }
+  return c - 1;
+}
+
+// Splits of each (query, head group) list.  Either every CTA writes a partial and a
+// combine kernel merges them, or the splits form one cluster (a power of two, so it
+// divides the 512 dims) and merge through DSMEM.  Rough cost model per list: waves of
+// ceil(tiles/S) tiles at ~4 us each, plus ~10 us for partials + combine or ~2 us for the
+// cluster merge; a cluster plan is only taken if all its clusters are resident at once.
+AtcPlan atc_plan(const AttendJob& j) {
+  if (j.mode == 2) return {1, false};
   const int64_t T = (atc_list_len_max(j) + kTile - 1) / kTile;
   const int64_t units = j.batch * j.n_q * (j.n_h / kHG);
   int64_t s = kNumSMs / std::max<int64_t>(units, 1);
   s = std::min<int64_t>(s, T);
-  s = std::min<int64_t>(s, 64);
-  return (int)std::max<int64_t>(s, 1);
+  if (s <= 1) return {1, false};
+  auto cost = [&](int64_t S, bool cluster) { return (double)((T + S - 1) / S) * 4.0 + (cluster ? 2.0 : 10.0); };
+  AtcPlan best{(int)std::min<int64_t>(s, 64), false};
+  double best_cost = cost(best.n_split, false);
+  for (int S = 2; S <= 16 && S <= T; S *= 2) {
+    if (units * S > kNumSMs || units > clusters_resident(j.mode, S)) continue;
+    const double c = cost(S, true);
+    if (c < best_cost) best_cost = c, best = {S, true};
+  }
+  return best;
 }
 
+}  // namespace
+
+int attend_tc_splits(const AttendJob& j) { return atc_plan(j).n_split; }
+
 size_t attend_tc_workspace_bytes(const AttendJob& j) {
-  const int s = attend_tc_splits(j);
-  if (s <= 1) return 0;
-  const size_t n = (size_t)(j.batch * j.n_q * s * j.n_h);
+  const AtcPlan pl = atc_plan(j);
+  if (pl.n_split <= 1 || pl.cluster) return 0;
+  const size_t n = (size_t)(j.batch * j.n_q * pl.n_split * j.n_h);
   return n * (size_t)kC * sizeof(float) + n * sizeof(float2) + 256;
 }
 
@@ -734,13 +913,15 @@ cudaError_t launch_attend_tc(const AttendJob& j, void* ws, cudaStream_t s) {
   p.o_in = j.o_in, p.lse_in = j.lse_in, p.out = j.out, p.lse_out = j.lse, p.out_bf16 = j.out_bf16;
   p.n_q = j.n_q, p.n_h = j.n_h, p.n_entries = j.n_entries, p.kv_stride = j.kv_stride, p.list_len = j.list_len;
   p.m = j.m, p.q_pos0 = j.q_pos0, p.kv_pos0 = j.kv_pos0, p.n_win = j.n_win;
-  p.n_split = attend_tc_splits(j);
+  const AtcPlan pl = atc_plan(j);
+  p.n_split = pl.n_split;
+  p.cluster = pl.cluster ? 1 : 0;
   p.n_hg = (int)(j.n_h / kHG);
   p.alias = j.k == j.v;
   p.scale_log2 = j.scale * kLog2e;
   p.dev_status = j.dev_status;
   const int64_t rows = j.batch * j.n_q;
-  if (p.n_split > 1) {
+  if (p.n_split > 1 && !p.cluster) {
     const size_t n = (size_t)(rows * p.n_split * j.n_h);
     p.part_o = static_cast<float*>(ws);
     p.part_ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + n * (size_t)kC * sizeof(float));
@@ -758,6 +939,26 @@ cudaError_t launch_attend_tc(const AttendJob& j, void* ws, cudaStream_t s) {
   const int64_t grid = rows * p.n_split * p.n_hg;
   if (grid >= (int64_t(1) << 31)) return cudaErrorInvalidConfiguration;
   cudaError_t e;
+  if (p.cluster) {
+    const void* fn = j.mode == 0 ? (const void*)attend_tc_kernel<0> : (const void*)attend_tc_kernel<1>;
+    if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)) != cudaSuccess) return e;
+    if (p.n_split > 8 &&
+        (e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
+      return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid), cfg.blockDim = dim3(kThreads), cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = (unsigned)p.n_split, attr.val.clusterDim.y = 1, attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr, cfg.numAttrs = 1;
+    if (j.mode == 0)
+      e = cudaLaunchKernelEx(&cfg, attend_tc_kernel<0>, tm_q, tm_k, tm_v, p);
+    else
+      e = cudaLaunchKernelEx(&cfg, attend_tc_kernel<1>, tm_q, tm_k, tm_v, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
   switch (j.mode) {
     case 0:
       e = cudaFuncSetAttribute(attend_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -774,7 +975,7 @@ cudaError_t launch_attend_tc(const AttendJob& j, void* ws, cudaStream_t s) {
   }
   if (e != cudaSuccess) return e;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (p.n_split > 1) {
+  if (p.n_split > 1 && !p.cluster) {
     atc_combine_kernel<<<(unsigned)(rows * j.n_h), 128, 0, s>>>(p.part_o, p.part_ml, j.o, j.lse, j.n_h, p.n_split);
     e = cudaGetLastError();
   }

@@ -107,10 +107,10 @@ static hyb_status validate_compress(const hyb_compress_args* a, int64_t* n_out) 
   if (a->overlap && (!a->cb || !a->zb)) return fail(HYB_ERR_INVALID_ARG, "hyb_compress: overlap needs cb and zb");
   if ((a->out_dtype == HYB_E4M3) != (a->out_scale != nullptr))
     return fail(HYB_ERR_INVALID_ARG, "hyb_compress: out_scale is required for E4M3 output and only then");
-  const size_t ai = lane_align(a->c, a->in_dtype);
+  // the kernel moves 4 consecutive channels per access
+  const size_t ai = 4 * elem_size(a->in_dtype);
   if (!aligned(a->ca, ai) || !aligned(a->za, ai) || (a->overlap && (!aligned(a->cb, ai) || !aligned(a->zb, ai))) ||
-      !aligned(a->bias, lane_align(a->c, HYB_F32)) || !aligned(a->out, lane_align(a->c, a->out_dtype)) ||
-      !aligned(a->out_scale, 4))
+      !aligned(a->bias, 16) || !aligned(a->out, 4 * elem_size(a->out_dtype)) || !aligned(a->out_scale, 4))
     return fail(HYB_ERR_INVALID_ARG, "hyb_compress: misaligned pointer");
   return ok();
 }
@@ -177,11 +177,15 @@ hyb_status csa_index_topk(const hyb_index_args* a, void* workspace, size_t ws_by
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t nv = n_vis_max(a->q_pos0, a->n_q, a->m, a->n_entries);
   float* scores = static_cast<float*>(workspace);
-  cudaError_t e = hyb::index_tc_shape_supported(a) ? hyb::launch_index_scores_tc(a, scores, nv, nv, s)
-                                                   : hyb::launch_index_scores_cc(a, scores, nv, nv, s);
-  if (e != cudaSuccess) return cuda_status(e, "csa_index_topk: index-score launch");
   void* topk_ws = static_cast<char*>(workspace) + index_scores_bytes(a);
-  return cuda_status(hyb::launch_topk(a, scores, nv, topk_ws, s), "csa_index_topk: top-k launch");
+  cudaError_t e;
+  uint32_t* ghist = hyb::topk_prepare_hist(a, nv, topk_ws, s, &e);
+  if (e != cudaSuccess) return cuda_status(e, "csa_index_topk: histogram reset");
+  bool hist_done = false;
+  e = hyb::index_tc_shape_supported(a) ? hyb::launch_index_scores_tc(a, scores, nv, nv, ghist, &hist_done, s)
+                                       : hyb::launch_index_scores_cc(a, scores, nv, nv, s);
+  if (e != cudaSuccess) return cuda_status(e, "csa_index_topk: index-score launch");
+  return cuda_status(hyb::launch_topk(a, scores, nv, topk_ws, hist_done, s), "csa_index_topk: top-k launch");
 }
 
 // ---------------------------------------------------------------- attention

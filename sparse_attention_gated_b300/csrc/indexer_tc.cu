@@ -43,8 +43,10 @@ struct IdxTc {
   static constexpr int kOffQ = kOffKeys + kStages * kKeyBytes;
   static constexpr int kOffScales = kOffQ + 2 * kQBytes;
   static constexpr int kOffW = kOffScales + kScaleRing * kScaleBytes;  // 3 x float[NQ*64]: w*qs, w, qs
-  static constexpr int kOffBar = kOffW + 3 * kN * 4;
-  static constexpr int kNumBars = 2 * kStages + 4 + 2 * kAcc + 2 * kScaleRing + 1;
+  static constexpr int kOffHist = kOffW + 3 * kN * 4;  // decode: row histogram of the scores' top bits
+  static constexpr int kHistBytes = NQ == 1 ? kTopkHistBins * 4 : 0;
+  static constexpr int kOffBar = kOffHist + kHistBytes;
+  static constexpr int kNumBars = 2 * kStages + 4 + 2 * kAcc + 2 * kScaleRing + 2;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 64 + 1024;  // + flags + alignment slack
 };
 
@@ -52,6 +54,7 @@ struct IdxTcParams {
   const float* w;
   const float* qI_scale;
   float* scores;
+  uint32_t* ghist;  // optional (one query per unit): [rows][kTopkHistBins] histogram of the score keys' top bits
   int64_t score_stride;
   int64_t n_q, n_entries, kv_stride, m, q_pos0;
   int64_t groups_per_b, tiles_per_unit, units_per_group, n_units;
@@ -100,6 +103,7 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
   uint64_t* sc_full = acc_empty + C::kAcc;
   uint64_t* sc_empty = sc_full + C::kScaleRing;
   uint64_t* done_bar = sc_empty + C::kScaleRing;
+  uint64_t* epi_bar = done_bar + 1;  // epilogue-group sync (bounded)
   volatile int* s_abort = reinterpret_cast<volatile int*>(bars + C::kNumBars);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + C::kNumBars) + 1;
   int* s_allpos = reinterpret_cast<int*>(bars + C::kNumBars) + 2;
@@ -112,6 +116,7 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
     for (int i = 0; i < C::kAcc; ++i) tc::mbar_init(&acc_full[i], 1), tc::mbar_init(&acc_empty[i], C::kEpiWarps);
     for (int i = 0; i < C::kScaleRing; ++i) tc::mbar_init(&sc_full[i], 1), tc::mbar_init(&sc_empty[i], C::kEpiWarps);
     tc::mbar_init(done_bar, 1);
+    tc::mbar_init(epi_bar, C::kEpiWarps * 32);
     *s_abort = 0;
     tc::fence_barrier_init();
   }
@@ -203,6 +208,31 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
     const int quad = warp & 3;        // TMEM lane quadrant this warp may access
     const int half = (warp - 2) / 4;  // which queries this warp handles (NQ = 4: two each)
     constexpr int kQPerWarp = NQ == 1 ? 1 : 2;
+    constexpr int kEpiThreads = C::kEpiWarps * 32;
+    // the epilogue warps meet on an mbarrier (bounded), never on a hardware barrier
+    uint32_t ephase = 0;
+    auto esync = [&]() -> bool {
+      tc::mbar_arrive(epi_bar);
+      const bool r = tc::mbar_wait(epi_bar, ephase, s_abort);
+      ephase ^= 1u;
+      return r;
+    };
+    // decode: 2^11-bin histogram of the score keys' top bits of the current row, added
+    // into the row's global histogram when the row changes and at the end
+    const bool do_hist = NQ == 1 && p.ghist != nullptr;
+    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + C::kOffHist);
+    int64_t hist_row = -1;
+    if (do_hist)
+      for (int i = et; i < kTopkHistBins; i += kEpiThreads) hist[i] = 0;
+    auto flush_hist = [&]() {
+      for (int i = et; i < kTopkHistBins; i += kEpiThreads) {
+        const uint32_t v = hist[i];
+        if (v) {
+          atomicAdd(p.ghist + hist_row * kTopkHistBins + i, v);
+          hist[i] = 0;
+        }
+      }
+    };
     int acc = 0;
     uint32_t aphase = 0;
     int64_t seq = 0;
@@ -210,10 +240,14 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
     for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
       const IdxUnit U = idx_unit<NQ>(p, u);
       if (U.tile_begin >= U.tile_end) continue;
-      tc::named_barrier(1, C::kEpiWarps * 32);
+      if (!(ok = esync())) break;  // everyone is done with the previous unit's tables
+      if (do_hist && U.b * p.n_q + U.j0 != hist_row) {
+        if (hist_row >= 0) flush_hist();
+        hist_row = U.b * p.n_q + U.j0;
+      }
       if (et == 0) *s_allpos = 1;
-      tc::named_barrier(1, C::kEpiWarps * 32);
-      for (int i = et; i < C::kN; i += C::kEpiWarps * 32) {
+      if (!(ok = esync())) break;
+      for (int i = et; i < C::kN; i += kEpiThreads) {
         const int jq = i / C::kHeads, h = i % C::kHeads;
         float wv = 0.f, qs = 1.f;
         if (jq < U.nq) {
@@ -226,7 +260,7 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
         w_q[i] = qs;
         if (!(qs > 0.f)) *s_allpos = 0;
       }
-      tc::named_barrier(1, C::kEpiWarps * 32);
+      if (!(ok = esync())) break;
       const bool allpos = *s_allpos != 0;
       for (int64_t t = U.tile_begin; t < U.tile_end; ++t, ++seq) {
         const int r = (int)(seq % C::kScaleRing);
@@ -272,15 +306,17 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
 #pragma unroll
         for (int qi = 0; qi < kQPerWarp; ++qi) {
           const int q = NQ == 1 ? 0 : 2 * half + qi;
-          if (q >= U.nq) continue;
           const int64_t j = U.j0 + q;
           int64_t vis = visible_entries(p.q_pos0 + j, p.m);
           if (vis > p.n_entries) vis = p.n_entries;
-          if (s < vis) p.scores[(U.b * p.n_q + j) * p.score_stride + s] = score[qi];
+          const bool keep = q < U.nq && s < vis;
+          if (keep) p.scores[(U.b * p.n_q + j) * p.score_stride + s] = score[qi];
+          if (do_hist && keep) atomicAdd(&hist[float_order_key(score[qi]) >> (32 - kTopkHistBits)], 1u);
         }
         if (++acc == C::kAcc) acc = 0, aphase ^= 1u;
       }
     }
+    if (do_hist && ok && hist_row >= 0 && esync()) flush_hist();
   }
 
   tc::tc_fence_before();
@@ -307,7 +343,7 @@ bool index_tc_shape_supported(const hyb_index_args* a) {
 
 template <int NQ>
 static cudaError_t launch_nq(const hyb_index_args* a, float* scores, int64_t score_stride, int64_t n_vis_max,
-                             cudaStream_t s) {
+                             uint32_t* ghist, cudaStream_t s) {
   using C = IdxTc<NQ>;
   const int64_t kvs = a->kv_stride > 0 ? a->kv_stride : a->n_entries;
   CUtensorMap tm_keys, tm_scales, tm_q;
@@ -320,6 +356,7 @@ static cudaError_t launch_nq(const hyb_index_args* a, float* scores, int64_t sco
     return cudaErrorInvalidValue;
   IdxTcParams p;
   p.w = a->w, p.qI_scale = a->qI_scale, p.scores = scores, p.score_stride = score_stride;
+  p.ghist = NQ == 1 ? ghist : nullptr;
   p.n_q = a->n_q, p.n_entries = a->n_entries, p.kv_stride = kvs, p.m = a->m, p.q_pos0 = a->q_pos0;
   p.groups_per_b = (a->n_q + NQ - 1) / NQ;
   const int64_t groups = p.groups_per_b * a->batch;
@@ -333,6 +370,7 @@ static cudaError_t launch_nq(const hyb_index_args* a, float* scores, int64_t sco
   p.n_units = groups * p.units_per_group;
   p.dev_status = a->dev_status;
   if (p.n_units == 0) return cudaSuccess;
+  static_assert(NQ != 1 || C::kSmemBytes <= 113 * 1024, "the decode indexer keeps two CTAs per SM");
   cudaError_t e = cudaFuncSetAttribute(index_tc_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int64_t grid = p.n_units < slots ? p.n_units : slots;
@@ -341,10 +379,12 @@ static cudaError_t launch_nq(const hyb_index_args* a, float* scores, int64_t sco
 }
 
 cudaError_t launch_index_scores_tc(const hyb_index_args* a, float* scores, int64_t score_stride, int64_t n_vis_max,
-                                   cudaStream_t s) {
+                                   uint32_t* ghist, bool* hist_done, cudaStream_t s) {
+  *hist_done = false;
   if (n_vis_max == 0 || a->n_q == 0 || a->batch == 0) return cudaSuccess;
-  if (a->n_q >= 8) return launch_nq<4>(a, scores, score_stride, n_vis_max, s);
-  return launch_nq<1>(a, scores, score_stride, n_vis_max, s);
+  if (a->n_q >= 8) return launch_nq<4>(a, scores, score_stride, n_vis_max, nullptr, s);
+  *hist_done = ghist != nullptr;
+  return launch_nq<1>(a, scores, score_stride, n_vis_max, ghist, s);
 }
 
 }  // namespace hyb

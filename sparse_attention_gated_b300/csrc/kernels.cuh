@@ -7,6 +7,10 @@
 
 namespace hyb {
 
+// top-k threshold histogram over the top bits of the order-preserving score keys
+constexpr int kTopkHistBits = 11;
+constexpr int kTopkHistBins = 1 << kTopkHistBits;
+
 // compress.cu
 bool compress_shape_supported(int64_t c);
 cudaError_t launch_compress(const hyb_compress_args* a, int64_t n_out, cudaStream_t s);
@@ -18,13 +22,17 @@ cudaError_t launch_index_scores_cc(const hyb_index_args* a, float* scores, int64
 
 // indexer_tc.cu (tcgen05 FP8 scores: E4M3, c_I = 128, 64 indexer heads)
 bool index_tc_shape_supported(const hyb_index_args* a);
+// ghist (optional): the row histograms of the top-k plan; *hist_done tells whether this launch filled them
 cudaError_t launch_index_scores_tc(const hyb_index_args* a, float* scores, int64_t score_stride, int64_t n_vis_max,
-                                   cudaStream_t s);
+                                   uint32_t* ghist, bool* hist_done, cudaStream_t s);
 
 // topk.cu
 size_t topk_workspace_bytes(const hyb_index_args* a, int64_t n_vis_max);
 bool topk_shape_supported(const hyb_index_args* a, int64_t n_vis_max);
-cudaError_t launch_topk(const hyb_index_args* a, const float* scores, int64_t score_stride, void* ws, cudaStream_t s);
+// the zeroed row histograms when the top-k plan uses them (else nullptr)
+uint32_t* topk_prepare_hist(const hyb_index_args* a, int64_t n_vis_max, void* ws, cudaStream_t s, cudaError_t* err);
+cudaError_t launch_topk(const hyb_index_args* a, const float* scores, int64_t score_stride, void* ws, bool hist_done,
+                        cudaStream_t s);
 
 // attend_cc.cu (CUDA-core attention for all three entry sources)
 struct AttendJob {

@@ -21,15 +21,18 @@
 //   one stage   (rows of at most kStageCap visible entries): one CTA per row
 //               stages the keys in shared memory, selects and collects.
 //   three kernels (longer rows, e.g. 262,144 entries at 1M context):
-//     hist    CTA (chunk, row): 12-bit histogram of its chunk, added into the
-//             row's global histogram.
+//     hist    CTA (chunk, row): 11-bit histogram of its chunk, added into the
+//             row's global histogram (the tensor-core indexer builds it in its
+//             epilogue for decode rows; then this kernel is skipped).
 //     filter  CTA (chunk, row): from the row histogram, the bin b* that holds
 //             the k-th largest key; the chunk's entries above b* (all kept)
 //             and inside b* (candidates) are written, in index order, to the
 //             chunk's own regions.
-//     final   CTA per row: selects the k - (#above) best candidates exactly,
-//             then merges them with the entries above b* (both lists are
-//             ascending) into the output.
+//             The filter also histograms the next 11 bits of the candidates.
+//     final   CTA per row: from that second histogram, the digit b2 holding
+//             the last kept candidate; candidates above it are kept, the few
+//             equal to it are selected exactly; the kept candidates are then
+//             merged with the entries above b* (both lists are ascending).
 #include "kernels.cuh"
 
 namespace hyb {
@@ -37,10 +40,12 @@ namespace hyb {
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int64_t kStageCap = 16384;  // one-stage plan: keys staged in shared memory
-constexpr int64_t kCandCap = 12288;   // final kernel: candidates staged in shared memory
-constexpr int kHistBits = 12;
-constexpr int kHistBins = 1 << kHistBits;
+constexpr int64_t kCandCap = 65536;   // final kernel: candidates tracked by a shared-memory bitmap
+constexpr int64_t kSubCap = 8192;     // final kernel: second-level candidates staged in shared memory
+constexpr int kHistBits = kTopkHistBits;
+constexpr int kHistBins = kTopkHistBins;
 constexpr int kMaxChunks = 64;
+constexpr int kPer = 8;  // keys a thread loads before using them (histogram and filter passes)
 
 struct TopkParams {
   const float* scores;
@@ -51,7 +56,8 @@ struct TopkParams {
   // three-kernel plan
   int64_t chunk;
   int n_chunks;
-  uint32_t* ghist;      // [rows][kHistBins]
+  uint32_t* ghist;      // [rows][kHistBins]: first digit (top kHistBits of the key) of every score
+  uint32_t* ghist2;     // [rows][kHistBins]: second digit of the threshold bin's candidates
   int32_t* def_idx;     // [rows][n_chunks][chunk]: entries above the threshold bin
   uint32_t* cand_key;   // [rows][n_chunks][chunk]: entries in the threshold bin
   int32_t* cand_idx;
@@ -95,6 +101,40 @@ __device__ __forceinline__ void block_scan2(bool fa, bool fb, BlockShared& S, ui
   const uint32_t base = S.warp_tot[warp];
   a_before = (base & 0xFFFFu) + (uint32_t)__popc(ba & lt);
   b_before = (base >> 16) + (uint32_t)__popc(bb & lt);
+  a_tot = S.total & 0xFFFFu;
+  b_tot = S.total >> 16;
+  __syncthreads();
+}
+
+// Exclusive block-wide prefix of two per-thread counts (each block total < 2^16)
+// in thread order; returns this thread's (a_before, b_before) and the totals.
+__device__ __forceinline__ void block_scan_counts(uint32_t a, uint32_t b, BlockShared& S, uint32_t& a_before,
+                                                  uint32_t& b_before, uint32_t& a_tot, uint32_t& b_tot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t v = a | (b << 16);
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) S.warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t w = S.warp_tot[lane];
+    uint32_t wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t u = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += u;
+    }
+    S.warp_tot[lane] = wi - w;
+    if (lane == 31) S.total = wi;
+  }
+  __syncthreads();
+  const uint32_t base = S.warp_tot[warp] + incl - v;
+  a_before = base & 0xFFFFu;
+  b_before = base >> 16;
   a_tot = S.total & 0xFFFFu;
   b_tot = S.total >> 16;
   __syncthreads();
@@ -223,12 +263,17 @@ __global__ void __launch_bounds__(kTopkThreads) topk_hist_kernel(TopkParams p) {
   for (int i = threadIdx.x; i < kHistBins; i += kTopkThreads) hist[i] = 0;
   __syncthreads();
   const float* sc = p.scores + row * p.score_stride + s0;
-  for (int64_t base = 0; base < len; base += kTopkThreads) {
-    const int64_t s = base + threadIdx.x;
-    const uint32_t key = s < len ? float_order_key(__ldg(sc + s)) : 0u;
-    hist_add(hist, s < len, key >> (32 - kHistBits));
-  }
-  __syncthreads();
+  for (int64_t base = 0; base < len; base += kPer * kTopkThreads) {
+    uint32_t key[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {  // all loads first: one round trip per kPer elements
+      const int64_t s = base + u * kTopkThreads + threadIdx.x;
+      key[u] = s < len ? float_order_key(__ldg(sc + s)) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u)
+      hist_add(hist, base + u * kTopkThreads + threadIdx.x < len, key[u] >> (32 - kHistBits));
+  }  __syncthreads();
   uint32_t* gh = p.ghist + row * kHistBins;
   for (int i = threadIdx.x; i < kHistBins; i += kTopkThreads)
     if (hist[i]) atomicAdd(gh + i, hist[i]);
@@ -293,27 +338,48 @@ __global__ void __launch_bounds__(kTopkThreads) topk_filter_kernel(TopkParams p)
     return;
   }
   const int64_t len = vis - s0 < p.chunk ? vis - s0 : p.chunk;
+  __shared__ uint32_t hist2[kHistBins];
+  for (int i = threadIdx.x; i < kHistBins; i += kTopkThreads) hist2[i] = 0;
   uint32_t bstar, above;
-  threshold_bin(p.ghist + row * kHistBins, (uint32_t)p.k, S, bstar, above);
+  threshold_bin(p.ghist + row * kHistBins, (uint32_t)p.k, S, bstar, above);  // (syncs the zeroing too)
   const float* sc = p.scores + row * p.score_stride + s0;
   const int64_t reg = (row * p.n_chunks + blockIdx.x) * p.chunk;
+  // each thread takes 4 consecutive entries, so one block scan orders 4096 of them
   uint32_t nd = 0, nc = 0;
-  for (int64_t base = 0; base < len; base += kTopkThreads) {
-    const int64_t s = base + threadIdx.x;
-    const uint32_t key = s < len ? float_order_key(__ldg(sc + s)) : 0u;
-    const uint32_t bin = key >> (32 - kHistBits);
-    const bool d = s < len && bin > bstar;
-    const bool c = s < len && bin == bstar;
+  for (int64_t base = 0; base < len; base += 4 * kTopkThreads) {
+    const int64_t s = base + 4 * threadIdx.x;
+    uint32_t key[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) key[u] = s + u < len ? float_order_key(__ldg(sc + s + u)) : 0u;
+    bool d[4], c[4];
+    uint32_t ld = 0, lc = 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t bin = key[u] >> (32 - kHistBits);
+      d[u] = s + u < len && bin > bstar;
+      c[u] = s + u < len && bin == bstar;
+      ld += d[u], lc += c[u];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) hist_add(hist2, c[u], (key[u] >> (32 - 2 * kHistBits)) & (kHistBins - 1));
     uint32_t db, cb, dt, ct;
-    block_scan2(d, c, S, db, cb, dt, ct);
-    if (d) p.def_idx[reg + nd + db] = (int32_t)(s0 + s);
-    if (c) {
-      p.cand_key[reg + nc + cb] = key;
-      p.cand_idx[reg + nc + cb] = (int32_t)(s0 + s);
+    block_scan_counts(ld, lc, S, db, cb, dt, ct);
+    uint32_t od = nd + db, oc = nc + cb;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (d[u]) p.def_idx[reg + od++] = (int32_t)(s0 + s + u);
+      if (c[u]) {
+        p.cand_key[reg + oc] = key[u];
+        p.cand_idx[reg + oc++] = (int32_t)(s0 + s + u);
+      }
     }
     nd += dt, nc += ct;
   }
   if (threadIdx.x == 0) cnt[0] = (int32_t)nd, cnt[1] = (int32_t)nc;
+  __syncthreads();
+  uint32_t* gh2 = p.ghist2 + row * kHistBins;
+  for (int i = threadIdx.x; i < kHistBins; i += kTopkThreads)
+    if (hist2[i]) atomicAdd(gh2 + i, hist2[i]);
 }
 
 // ----------------------------------------------- three kernels: final
@@ -332,13 +398,30 @@ __global__ void __launch_bounds__(kTopkThreads) topk_final_kernel(TopkParams p) 
   int32_t* out = p.idx + row * p.k;
   float* out_sc = p.out_scores ? p.out_scores + row * p.k : nullptr;
   const int32_t* cnt = p.counts + row * p.n_chunks * 2;
-  if (tid == 0) {
-    int32_t a = 0, b = 0;
-    for (int c = 0; c < p.n_chunks; ++c) {
-      pre_d[c] = a, pre_c[c] = b;
-      a += cnt[2 * c], b += cnt[2 * c + 1];
+  // prefix sums of the per-chunk counts (at most 64 chunks: two per lane of warp 0)
+  if (tid < 32) {
+    int32_t d[2], c[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int ch = h * 32 + tid;
+      d[h] = ch < p.n_chunks ? cnt[2 * ch] : 0;
+      c[h] = ch < p.n_chunks ? cnt[2 * ch + 1] : 0;
     }
-    pre_d[p.n_chunks] = a, pre_c[p.n_chunks] = b;
+    int32_t carry_d = 0, carry_c = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      int32_t id = d[h], ic = c[h];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t ud = __shfl_up_sync(0xffffffffu, id, o), uc = __shfl_up_sync(0xffffffffu, ic, o);
+        if (tid >= o) id += ud, ic += uc;
+      }
+      pre_d[h * 32 + tid + 1] = carry_d + id;
+      pre_c[h * 32 + tid + 1] = carry_c + ic;
+      carry_d += __shfl_sync(0xffffffffu, id, 31);
+      carry_c += __shfl_sync(0xffffffffu, ic, 31);
+    }
+    if (tid == 0) pre_d[0] = 0, pre_c[0] = 0;
   }
   __syncthreads();
   const int64_t n_def = pre_d[p.n_chunks], n_cand = pre_c[p.n_chunks];
@@ -346,44 +429,73 @@ __global__ void __launch_bounds__(kTopkThreads) topk_final_kernel(TopkParams p) 
   const int64_t reg0 = row * p.n_chunks * p.chunk;
   int32_t* A = reinterpret_cast<int32_t*>(dyn);  // [k]: entries above the threshold bin, ascending
   int32_t* B = A + p.k;                          // [k]: kept candidates, ascending
-  uint32_t* ck = reinterpret_cast<uint32_t*>(B + p.k);  // [kCandCap] staged candidate keys
-  int32_t* ci = reinterpret_cast<int32_t*>(ck + kCandCap);
-  // gather both lists in chunk order
-  for (int c = 0; c < p.n_chunks; ++c) {
-    const int64_t reg = reg0 + (int64_t)c * p.chunk;
-    const int32_t nd = pre_d[c + 1] - pre_d[c], nc = pre_c[c + 1] - pre_c[c];
-    for (int32_t x = tid; x < nd; x += kTopkThreads) A[pre_d[c] + x] = p.def_idx[reg + x];
-    if (n_cand <= kCandCap)
-      for (int32_t x = tid; x < nc; x += kTopkThreads) {
-        ck[pre_c[c] + x] = p.cand_key[reg + x];
-        ci[pre_c[c] + x] = p.cand_idx[reg + x];
-      }
-  }
-  __syncthreads();
-  // exact selection of r among the candidates (staged, or read in place when too many)
-  auto staged = [&](int64_t x) { return ck[x]; };
-  auto chunk_of = [&](int64_t x) {
-    int lo = 0, hi = p.n_chunks - 1;  // last chunk c with pre_c[c] <= x
+  uint32_t* sk = reinterpret_cast<uint32_t*>(B + p.k);  // [kSubCap] keys of the sub-candidates
+  int32_t* spos = reinterpret_cast<int32_t*>(sk + kSubCap);  // [kSubCap] their candidate positions
+  uint32_t* selbits = reinterpret_cast<uint32_t*>(spos + kSubCap);  // [kCandCap/32] selected sub-candidates
+  // chunk holding element x of a concatenated list: the last c with pre[c] <= x
+  auto chunk_in = [&](const int32_t* pre, int64_t x) {
+    int lo = 0, hi = p.n_chunks - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (pre_c[mid] <= x) lo = mid; else hi = mid - 1;
+      if (pre[mid] <= x) lo = mid; else hi = mid - 1;
     }
     return lo;
   };
-  auto inplace = [&](int64_t x) {
-    const int c = chunk_of(x);
-    return p.cand_key[reg0 + (int64_t)c * p.chunk + (x - pre_c[c])];
-  };
-  uint32_t T, ties;
-  if (n_cand <= kCandCap) {
-    radix_select(staged, n_cand, r, S, T, ties);
-    collect_ordered(staged, n_cand, T, ties, S, [&](uint32_t slot, int64_t x) { B[slot] = ci[x]; });
-  } else {
-    radix_select(inplace, n_cand, r, S, T, ties);
-    collect_ordered(inplace, n_cand, T, ties, S, [&](uint32_t slot, int64_t x) {
-      const int c = chunk_of(x);
-      B[slot] = p.cand_idx[reg0 + (int64_t)c * p.chunk + (x - pre_c[c])];
+  auto cand_at = [&](int64_t x) { const int c = chunk_in(pre_c, x); return reg0 + (int64_t)c * p.chunk + (x - pre_c[c]); };
+  for (int64_t x = tid; x < n_def; x += kTopkThreads) {
+    const int c = chunk_in(pre_d, x);
+    A[x] = p.def_idx[reg0 + (int64_t)c * p.chunk + (x - pre_d[c])];
+  }
+  // second-level threshold among the candidates: digit2 = the next kHistBits of the key
+  uint32_t b2, above2;
+  threshold_bin(p.ghist2 + row * kHistBins, (uint32_t)r, S, b2, above2);
+  const int64_t r2 = r - above2;  // how many of the candidates with digit2 == b2 to keep
+  auto digit2 = [&](uint32_t key) { return (key >> (32 - 2 * kHistBits)) & (uint32_t)(kHistBins - 1); };
+  // stage the sub-candidates (digit2 == b2) in candidate order
+  uint32_t n_sub = 0;
+  for (int64_t base = 0; base < n_cand; base += kTopkThreads) {
+    const int64_t x = base + tid;
+    const uint32_t key = x < n_cand ? p.cand_key[cand_at(x)] : 0u;
+    const bool sub = x < n_cand && digit2(key) == b2;
+    uint32_t sb, ub, st, ut;
+    block_scan_counts(sub, 0u, S, sb, ub, st, ut);
+    if (sub && n_sub + sb < kSubCap) sk[n_sub + sb] = key, spos[n_sub + sb] = (int32_t)x;
+    n_sub += st;
+  }
+  const bool fast = n_sub <= kSubCap && n_cand <= kCandCap;
+  if (fast) {
+    for (int64_t x = tid; x < kCandCap / 32; x += kTopkThreads) selbits[x] = 0u;
+    __syncthreads();
+    uint32_t T, ties;
+    auto subkey = [&](int64_t x) { return sk[x]; };
+    radix_select(subkey, n_sub, r2, S, T, ties);
+    collect_ordered(subkey, n_sub, T, ties, S, [&](uint32_t, int64_t x) {
+      const int32_t pos = spos[x];
+      atomicOr(&selbits[pos >> 5], 1u << (pos & 31));
     });
+    __syncthreads();
+    // kept candidates in order: digit2 above b2, or selected among the sub-candidates
+    uint32_t nb = 0;
+    for (int64_t base = 0; base < n_cand; base += kTopkThreads) {
+      const int64_t x = base + tid;
+      bool keep = false;
+      int64_t at = 0;
+      if (x < n_cand) {
+        at = cand_at(x);
+        const uint32_t d2 = digit2(p.cand_key[at]);
+        keep = d2 > b2 || (d2 == b2 && ((selbits[x >> 5] >> (x & 31)) & 1u));
+      }
+      uint32_t kb, zb, kt, zt;
+      block_scan_counts(keep, 0u, S, kb, zb, kt, zt);
+      if (keep) B[nb + kb] = p.cand_idx[at];
+      nb += kt;
+    }
+  } else {
+    // many equal keys: exact selection over all candidates, read in place
+    auto inplace = [&](int64_t x) { return p.cand_key[cand_at(x)]; };
+    uint32_t T, ties;
+    radix_select(inplace, n_cand, r, S, T, ties);
+    collect_ordered(inplace, n_cand, T, ties, S, [&](uint32_t slot, int64_t x) { B[slot] = p.cand_idx[cand_at(x)]; });
   }
   __syncthreads();
   // merge the two ascending, disjoint lists: slot = own rank + rank in the other list
@@ -431,12 +543,39 @@ size_t topk_workspace_bytes(const hyb_index_args* a, int64_t n_vis_max) {
   if (!pl.three) return 0;
   const size_t rows = (size_t)(a->batch * a->n_q);
   const size_t region = rows * (size_t)pl.n_chunks * (size_t)pl.chunk;
-  return align256(rows * kHistBins * 4) + 3 * align256(region * 4) + align256(rows * pl.n_chunks * 8);
+  return align256(rows * kHistBins * 8) + 3 * align256(region * 4) + align256(rows * pl.n_chunks * 8);
 }
 
 bool topk_shape_supported(const hyb_index_args* a, int64_t) { return a->k >= 1 && a->k <= 2048; }
 
-cudaError_t launch_topk(const hyb_index_args* a, const float* scores, int64_t score_stride, void* ws, cudaStream_t s) {
+static void topk_pointers(TopkParams& p, const TopkPlan& pl, int64_t rows, void* ws) {
+  const size_t region = (size_t)rows * pl.n_chunks * pl.chunk;
+  char* w = static_cast<char*>(ws);
+  p.ghist = reinterpret_cast<uint32_t*>(w);
+  p.ghist2 = p.ghist + rows * kHistBins;
+  w += align256((size_t)rows * kHistBins * 8);
+  p.def_idx = reinterpret_cast<int32_t*>(w);
+  w += align256(region * 4);
+  p.cand_key = reinterpret_cast<uint32_t*>(w);
+  w += align256(region * 4);
+  p.cand_idx = reinterpret_cast<int32_t*>(w);
+  w += align256(region * 4);
+  p.counts = reinterpret_cast<int32_t*>(w);
+}
+
+uint32_t* topk_prepare_hist(const hyb_index_args* a, int64_t n_vis_max, void* ws, cudaStream_t s, cudaError_t* err) {
+  *err = cudaSuccess;
+  const int64_t rows = a->batch * a->n_q;
+  const TopkPlan pl = plan_topk(a, n_vis_max);
+  if (rows == 0 || !pl.three) return nullptr;
+  TopkParams p{};
+  topk_pointers(p, pl, rows, ws);
+  *err = cudaMemsetAsync(p.ghist, 0, (size_t)rows * kHistBins * 8, s);  // both histograms
+  return p.ghist;
+}
+
+cudaError_t launch_topk(const hyb_index_args* a, const float* scores, int64_t score_stride, void* ws, bool hist_done,
+                        cudaStream_t s) {
   TopkParams p{};
   p.scores = scores, p.score_stride = score_stride, p.idx = a->idx, p.out_scores = a->scores;
   p.n_q = a->n_q, p.n_entries = a->n_entries, p.m = a->m, p.k = a->k, p.q_pos0 = a->q_pos0;
@@ -453,24 +592,15 @@ cudaError_t launch_topk(const hyb_index_args* a, const float* scores, int64_t sc
     return cudaGetLastError();
   }
   p.chunk = pl.chunk, p.n_chunks = pl.n_chunks;
-  const size_t region = (size_t)rows * pl.n_chunks * pl.chunk;
-  char* w = static_cast<char*>(ws);
-  p.ghist = reinterpret_cast<uint32_t*>(w);
-  w += align256((size_t)rows * kHistBins * 4);
-  p.def_idx = reinterpret_cast<int32_t*>(w);
-  w += align256(region * 4);
-  p.cand_key = reinterpret_cast<uint32_t*>(w);
-  w += align256(region * 4);
-  p.cand_idx = reinterpret_cast<int32_t*>(w);
-  w += align256(region * 4);
-  p.counts = reinterpret_cast<int32_t*>(w);
-  if ((e = cudaMemsetAsync(p.ghist, 0, (size_t)rows * kHistBins * 4, s)) != cudaSuccess) return e;
+  topk_pointers(p, pl, rows, ws);
   const dim3 grid((unsigned)pl.n_chunks, (unsigned)rows);
-  topk_hist_kernel<<<grid, kTopkThreads, 0, s>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (!hist_done) {  // the histograms were zeroed by topk_prepare_hist
+    topk_hist_kernel<<<grid, kTopkThreads, 0, s>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   topk_filter_kernel<<<grid, kTopkThreads, 0, s>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const size_t smem = (size_t)2 * a->k * 4 + (size_t)kCandCap * 8;
+  const size_t smem = (size_t)2 * a->k * 4 + (size_t)kSubCap * 8 + (size_t)kCandCap / 8;
   e = cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   topk_final_kernel<<<(unsigned)rows, kTopkThreads, smem, s>>>(p);
