@@ -183,6 +183,35 @@ HYB_API size_t csa_index_topk_workspace_size(const hyb_index_args* a);
 HYB_API hyb_status csa_index_topk(const hyb_index_args* a, void* workspace, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * csa_index_topk_noalloc -- csa_index_topk for callers that cannot allocate
+ * device memory.  (The method's description has no counterpart: this is a
+ * deployment variant of the same computation.)
+ *
+ * Some callers cannot call cudaMalloc or a framework allocator at the point
+ * where they run the indexer: code that owns no allocator (a plug-in inside a
+ * host engine that hands it only input and output buffers), code that runs
+ * under a fixed memory budget reserved up front, or code that must not touch
+ * the allocator while it runs.  This entry point takes the same arguments as
+ * csa_index_topk, but no workspace: its scratch is one file-scope device array
+ * of HYB_NOALLOC_SCRATCH_BYTES, part of the library's image, which every GPU
+ * that loads the library holds until the process exits.  The caller still
+ * passes all inputs and outputs.
+ *
+ *  - The first call on a device looks up the array's device address (with that
+ *    device current) and remembers it; make that first call before any stream
+ *    capture.  Later calls allocate nothing and call no allocating routine.
+ *  - Arguments needing more scratch than HYB_NOALLOC_SCRATCH_BYTES
+ *    (csa_index_topk_workspace_size(a) > HYB_NOALLOC_SCRATCH_BYTES) are
+ *    rejected with HYB_ERR_WORKSPACE before any launch.
+ *  - Every call shares the one array, which keeps the previous call's
+ *    contents; the call clears what must start at zero.  Calls whose work
+ *    overlaps on the GPU (other streams, other host threads) race on it:
+ *    serialise them on one stream.
+ * ------------------------------------------------------------------------ */
+#define HYB_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+HYB_API hyb_status csa_index_topk_noalloc(const hyb_index_args* a, void* stream);
+
+/* ------------------------------------------------------------------------
  * csa_attend -- CSA core attention over the selected entries ([HA] V.3, MQA:
  * every head shares one compressed K and V; [KE] section 6 contract).
  *

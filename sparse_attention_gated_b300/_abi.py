@@ -13,6 +13,7 @@ LIB_PATH = os.path.join(_PKG, "libhyb.so")
 
 HYB_F32, HYB_BF16, HYB_E4M3 = 0, 1, 2
 HYB_DEV_BAD_INDEX, HYB_DEV_TIMEOUT = 0x1, 0x2
+HYB_NOALLOC_SCRATCH_BYTES = 32 << 20  # include/hyb.h
 
 _p = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -59,6 +60,7 @@ SIGNATURES = {
     "hyb_compress": (ctypes.c_int, [ctypes.POINTER(CompressArgs), _p, ctypes.c_size_t, _p]),
     "csa_index_topk_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(IndexArgs)]),
     "csa_index_topk": (ctypes.c_int, [ctypes.POINTER(IndexArgs), _p, ctypes.c_size_t, _p]),
+    "csa_index_topk_noalloc": (ctypes.c_int, [ctypes.POINTER(IndexArgs), _p]),
     "csa_attend_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(CsaAttendArgs)]),
     "csa_attend": (ctypes.c_int, [ctypes.POINTER(CsaAttendArgs), _p, ctypes.c_size_t, _p]),
     "hca_attend_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(HcaAttendArgs)]),

@@ -3,6 +3,7 @@
 // and error reporting.  No device memory is allocated here.
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 #include "kernels.cuh"
@@ -186,6 +187,46 @@ hyb_status csa_index_topk(const hyb_index_args* a, void* workspace, size_t ws_by
                                        : hyb::launch_index_scores_cc(a, scores, nv, nv, s);
   if (e != cudaSuccess) return cuda_status(e, "csa_index_topk: index-score launch");
   return cuda_status(hyb::launch_topk(a, scores, nv, topk_ws, hist_done, s), "csa_index_topk: top-k launch");
+}
+
+// ----------------------------------------------- index + top-k, no allocation
+
+namespace {
+
+// The scratch of csa_index_topk_noalloc: part of the library image, held by every
+// device that loads the library.  Host code never uses its name as an address: the
+// device address comes from cudaGetSymbolAddress, once per device.
+__device__ __align__(256) uint8_t g_noalloc_scratch[HYB_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+}  // namespace
+
+hyb_status csa_index_topk_noalloc(const hyb_index_args* a, void* stream) {
+  hyb_status st = validate_index(a);
+  if (st != HYB_OK || a->batch == 0 || a->n_q == 0) return st;
+  const size_t need = csa_index_topk_workspace_size(a);
+  if (need > HYB_NOALLOC_SCRATCH_BYTES)
+    return fail(HYB_ERR_WORKSPACE, "csa_index_topk_noalloc: these sizes need %zu bytes of scratch, more than the %zu "
+                "bytes the library holds", need, (size_t)HYB_NOALLOC_SCRATCH_BYTES);
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e, "csa_index_topk_noalloc: cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(HYB_ERR_UNSUPPORTED, "csa_index_topk_noalloc: device %d", dev);
+  void* scratch;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // with device `dev` current
+      if (e != cudaSuccess) return cuda_status(e, "csa_index_topk_noalloc: cudaGetSymbolAddress");
+      g_noalloc_ptr[dev] = p;
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  return csa_index_topk(a, scratch, HYB_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 // ---------------------------------------------------------------- attention

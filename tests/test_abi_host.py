@@ -123,3 +123,18 @@ def test_attend_and_merge_reject_invalid_arguments(lib):
     assert lib.swa_merge(ctypes.byref(s), None, 0, None) == 1  # window rows outside the buffer
     s.kv_pos0, s.o_in = 185, FAKE
     assert lib.swa_merge(ctypes.byref(s), None, 0, None) == 1  # o_in without lse_in
+
+
+def test_noalloc_indexer_rejects_sizes_beyond_its_scratch(lib):
+    """The allocation-free indexer needs csa_index_topk's workspace to fit its fixed
+    scratch; larger problems are rejected on the host, before any CUDA call."""
+    a = _abi.IndexArgs()
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the call is rejected first
+    a.qI = a.qI_scale = a.w = a.kI = a.kI_scale = a.idx = fake
+    a.batch, a.n_q, a.n_entries, a.kv_stride, a.n_ih, a.c_I, a.m, a.k = 64, 1, 1 << 20, 1 << 20, 64, 128, 4, 1024
+    a.q_pos0 = 4 * (1 << 20) - 1
+    a.dtype = _abi.HYB_E4M3
+    need = lib.csa_index_topk_workspace_size(ctypes.byref(a))
+    assert need > _abi.HYB_NOALLOC_SCRATCH_BYTES
+    assert lib.csa_index_topk_noalloc(ctypes.byref(a), None) == 3  # HYB_ERR_WORKSPACE
+    assert b"scratch" in lib.hyb_last_error()
