@@ -232,6 +232,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const AtcWork W = atc_work<MODE>(p);
   const int64_t ntiles = W.te - W.tb;
+  // K = V and one tile: O^T reads the K slabs still in the ring (no V group);
+  // otherwise the V slabs are loaded again after the next tile's K (see above)
+  const bool reuse = p.alias && ntiles == 1;
+  const int64_t ngroups = reuse ? 1 : 2 * ntiles;
 
   // the first group's loads are issued by the thread that initialises the
   // barriers, before the CTA-wide setup sync (overlapping the TMEM allocation)
@@ -273,23 +277,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kProdWarps) {
     // ================================================================ producers
     bool ok = true;
-    int pend[2];
-    int npend = 0;
     int64_t tma_u[kSlabs];  // last use count of each slot filled by TMA (for the drain on abort)
 #pragma unroll
     for (int s = 0; s < kSlabs; ++s) tma_u[s] = pre_k ? 0 : -1;
-    // make this warp's finished gathers visible to the MMA and signal them
-    auto flush = [&]() {
-      if (npend) {
-        tc::cp_async_wait_all();
-        tc::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0)
-          for (int x = 0; x < npend; ++x) tc::mbar_arrive(&kv_full[pend[x]]);
-        npend = 0;
-      }
-    };
-    const int64_t ngroups = 2 * ntiles;
     // L2 prefetch of the entry rows kPrefetchAhead tiles ahead of the K group being
     // loaded, so the loads that later fill the ring pay L2 rather than HBM latency
     auto prefetch_tile = [&](int64_t i) {
@@ -323,9 +313,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
       const __nv_bfloat16* src = is_v ? p.v : p.k;
       const uint32_t par = (uint32_t)(G & 1) ^ 1u;  // wait for the release of the slot's previous use
-      // a TMA group after gathered slabs (ragged tile K, then the full tile's V) must not
-      // block on a slot while this warp still holds copies it has not signalled
-      if (tma_tile && warp == 0) flush();
       for (int s = 0; s < kSlabs; ++s, ++g) {
         uint8_t* dst = kv_s + s * kSlabBytes;
         if (tma_tile) {
@@ -344,13 +331,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else if (atc_gather_warp<MODE>(g) == warp) {
           int okl = 1;
-          if (lane == 0) okl = tc::mbar_try_wait(&kv_empty[s], par);
-          if (!__shfl_sync(0xffffffffu, okl, 0)) {
-            flush();  // never block on a slot while holding un-signalled copies
-            if (lane == 0) okl = tc::mbar_wait(&kv_empty[s], par, s_abort, 2);
-            ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
-            if (!ok) break;
-          }
+          if (lane == 0) okl = tc::mbar_wait(&kv_empty[s], par, s_abort, 2);
+          ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
+          if (!ok) break;
           const uint32_t dbase = tc::smem_u32(dst);
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
@@ -362,20 +345,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c16 = 0; c16 < 8; ++c16)
               tc::cp_async16(drow + (uint32_t)((c16 ^ (e & 7)) << 4), rsrc + c16 * 8, have ? 16u : 0u);
           }
-          tc::cp_async_commit();
-          pend[npend++] = s;
-          if (npend == 2) {
-            tc::cp_async_wait_group<1>();
-            tc::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&kv_full[pend[0]]);
-            pend[0] = pend[1];
-            npend = 1;
-          }
+          // the slab is complete once every lane's copies have landed; nobody waits here
+          tc::cp_async_arrive_on(&kv_full[s]);
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&kv_full[s]);
         }
       }
     }
-    flush();
+    tc::cp_async_wait_all();  // this thread's copies have landed before it leaves
     bool oin_issued = false;
     if constexpr (MODE == 2) {
       // the compressed-branch output of this query's heads, into the ring once the last products are done
@@ -413,7 +390,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idS = tc::make_idesc(1, 1, 0, 0, 128, kHG);  // A = K (K-major), B = Q (K-major)
       constexpr uint32_t idO = tc::make_idesc(1, 1, 1, 1, 128, kHG);  // A = V^T (MN-major), B = P^T (MN-major)
       const uint32_t q_addr = tc::smem_u32(q_s), kv_addr = tc::smem_u32(kv_s), p_addr = tc::smem_u32(p_s);
-      const int64_t ngroups = 2 * ntiles;
       for (int64_t G = 0; G < ngroups && ok; ++G) {
         bool is_v;
         const int64_t li = atc_group(G, ngroups, is_v);
@@ -424,21 +400,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t dS = tmem + kTmemS + (uint32_t)(sb * kHG);
           for (int s = 0; s < kSlabs; ++s) {
             if (!(ok = tc::mbar_wait(&kv_full[s], par, s_abort, 5))) break;
+            tc::fence_proxy_async_smem();  // gathered slabs were written through the generic proxy
             tc::tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               tc::mma_f16(dS, tc::desc_kmajor_sw128(kv_addr + s * kSlabBytes + 32 * kk),
                           tc::desc_kmajor_sw128(q_addr + s * kQSlabBytes + 32 * kk), idS, (s | kk) ? 1u : 0u);
-            tc::mma_commit(&kv_empty[s]);  // the slot is free once these products are done
+            if (!reuse) tc::mma_commit(&kv_empty[s]);  // the slot is free once these products are done
           }
           if (!ok) break;
           tc::mma_commit(&s_full[sb]);
+          if (reuse) {
+            // O^T from the same slabs (they are V too), then release them
+            if (!(ok = tc::mbar_wait(p_full, 0, s_abort, 6))) break;
+            tc::tc_fence_after();
+            for (int ch = 0; ch < 4; ++ch) {
+              const uint32_t a0 = kv_addr + (uint32_t)(2 * ch * kSlabBytes);
+#pragma unroll
+              for (int ks = 0; ks < kTile / 16; ++ks)
+                tc::mma_f16(tmem + kTmemO + (uint32_t)(ch * kHG),
+                            tc::desc_mnmajor_sw128(a0 + ks * 2048, kSlabBytes, 1024),
+                            tc::desc_mnmajor_sw128(p_addr + ks * 2048, 16, 1024), idO, ks > 0 ? 1u : 0u);
+              tc::mma_commit(&kv_empty[2 * ch]);
+              tc::mma_commit(&kv_empty[2 * ch + 1]);
+            }
+            tc::mma_commit(o_done);
+          }
         } else {
           if (!(ok = tc::mbar_wait(p_full, (uint32_t)(li & 1), s_abort, 6))) break;
           tc::tc_fence_after();
           for (int ch = 0; ch < 4; ++ch) {
             if (!(ok = tc::mbar_wait(&kv_full[2 * ch], par, s_abort, 7))) break;
             if (!(ok = tc::mbar_wait(&kv_full[2 * ch + 1], par, s_abort, 7))) break;
+            tc::fence_proxy_async_smem();
             tc::tc_fence_after();
             // V^T chunk ch: dims 128ch.. (slabs 2ch, 2ch+1: leading offset one slab), entries along K
             // in 8-row groups 1024 bytes apart; P^T has one 64-head group (leading offset unused)

@@ -44,7 +44,7 @@ struct IdxTc {
   static constexpr int kOffScales = kOffQ + 2 * kQBytes;
   static constexpr int kOffW = kOffScales + kScaleRing * kScaleBytes;  // 3 x float[NQ*64]: w*qs, w, qs
   static constexpr int kOffHist = kOffW + 3 * kN * 4;  // decode: row histogram of the scores' top bits
-  static constexpr int kHistBytes = NQ == 1 ? kTopkHistBins * 4 : 0;
+  static constexpr int kHistBytes = NQ == 1 ? kTopkHistBins * 2 : 0;  // 16-bit counters, two per word
   static constexpr int kOffBar = kOffHist + kHistBytes;
   static constexpr int kNumBars = 2 * kStages + 4 + 2 * kAcc + 2 * kScaleRing + 2;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 64 + 1024;  // + flags + alignment slack
@@ -217,18 +217,21 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
       ephase ^= 1u;
       return r;
     };
-    // decode: 2^11-bin histogram of the score keys' top bits of the current row, added
+    // decode: histogram of the score keys' top kTopkHistBits bits of the current row
+    // (16-bit counters packed two per word: a unit holds fewer than 2^16 entries), added
     // into the row's global histogram when the row changes and at the end
     const bool do_hist = NQ == 1 && p.ghist != nullptr;
     uint32_t* hist = reinterpret_cast<uint32_t*>(smem + C::kOffHist);
     int64_t hist_row = -1;
     if (do_hist)
-      for (int i = et; i < kTopkHistBins; i += kEpiThreads) hist[i] = 0;
+      for (int i = et; i < kTopkHistBins / 2; i += kEpiThreads) hist[i] = 0;
     auto flush_hist = [&]() {
-      for (int i = et; i < kTopkHistBins; i += kEpiThreads) {
+      for (int i = et; i < kTopkHistBins / 2; i += kEpiThreads) {
         const uint32_t v = hist[i];
         if (v) {
-          atomicAdd(p.ghist + hist_row * kTopkHistBins + i, v);
+          uint32_t* g = p.ghist + hist_row * kTopkHistBins + 2 * i;
+          if (v & 0xFFFFu) atomicAdd(g, v & 0xFFFFu);
+          if (v >> 16) atomicAdd(g + 1, v >> 16);
           hist[i] = 0;
         }
       }
@@ -311,7 +314,10 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
           if (vis > p.n_entries) vis = p.n_entries;
           const bool keep = q < U.nq && s < vis;
           if (keep) p.scores[(U.b * p.n_q + j) * p.score_stride + s] = score[qi];
-          if (do_hist && keep) atomicAdd(&hist[float_order_key(score[qi]) >> (32 - kTopkHistBits)], 1u);
+          if (do_hist && keep) {
+            const uint32_t bin = float_order_key(score[qi]) >> (32 - kTopkHistBits);
+            atomicAdd(&hist[bin >> 1], 1u << (16 * (bin & 1)));
+          }
         }
         if (++acc == C::kAcc) acc = 0, aphase ^= 1u;
       }
@@ -343,7 +349,7 @@ bool index_tc_shape_supported(const hyb_index_args* a) {
 
 template <int NQ>
 static cudaError_t launch_nq(const hyb_index_args* a, float* scores, int64_t score_stride, int64_t n_vis_max,
-                             uint32_t* ghist, cudaStream_t s) {
+                             uint32_t* ghist, bool* hist_done, cudaStream_t s) {
   using C = IdxTc<NQ>;
   const int64_t kvs = a->kv_stride > 0 ? a->kv_stride : a->n_entries;
   CUtensorMap tm_keys, tm_scales, tm_q;
@@ -356,7 +362,7 @@ static cudaError_t launch_nq(const hyb_index_args* a, float* scores, int64_t sco
     return cudaErrorInvalidValue;
   IdxTcParams p;
   p.w = a->w, p.qI_scale = a->qI_scale, p.scores = scores, p.score_stride = score_stride;
-  p.ghist = NQ == 1 ? ghist : nullptr;
+  p.ghist = nullptr;  // set below once the units are known
   p.n_q = a->n_q, p.n_entries = a->n_entries, p.kv_stride = kvs, p.m = a->m, p.q_pos0 = a->q_pos0;
   p.groups_per_b = (a->n_q + NQ - 1) / NQ;
   const int64_t groups = p.groups_per_b * a->batch;
@@ -368,6 +374,8 @@ static cudaError_t launch_nq(const hyb_index_args* a, float* scores, int64_t sco
   p.tiles_per_unit = tpu;
   p.units_per_group = (tiles_max + tpu - 1) / tpu;
   p.n_units = groups * p.units_per_group;
+  // fused histogram: one query per unit and fewer than 2^16 entries per unit (16-bit counters)
+  if (NQ == 1 && ghist != nullptr && p.tiles_per_unit * C::kTileE < 65536) p.ghist = ghist;
   p.dev_status = a->dev_status;
   if (p.n_units == 0) return cudaSuccess;
   static_assert(NQ != 1 || C::kSmemBytes <= 113 * 1024, "the decode indexer keeps two CTAs per SM");
@@ -375,6 +383,7 @@ static cudaError_t launch_nq(const hyb_index_args* a, float* scores, int64_t sco
   if (e != cudaSuccess) return e;
   const int64_t grid = p.n_units < slots ? p.n_units : slots;
   index_tc_kernel<NQ><<<(unsigned)grid, C::kThreads, C::kSmemBytes, s>>>(tm_keys, tm_scales, tm_q, p);
+  *hist_done = p.ghist != nullptr;
   return cudaGetLastError();
 }
 
@@ -382,9 +391,8 @@ cudaError_t launch_index_scores_tc(const hyb_index_args* a, float* scores, int64
                                    uint32_t* ghist, bool* hist_done, cudaStream_t s) {
   *hist_done = false;
   if (n_vis_max == 0 || a->n_q == 0 || a->batch == 0) return cudaSuccess;
-  if (a->n_q >= 8) return launch_nq<4>(a, scores, score_stride, n_vis_max, nullptr, s);
-  *hist_done = ghist != nullptr;
-  return launch_nq<1>(a, scores, score_stride, n_vis_max, ghist, s);
+  if (a->n_q >= 8) return launch_nq<4>(a, scores, score_stride, n_vis_max, nullptr, hist_done, s);
+  return launch_nq<1>(a, scores, score_stride, n_vis_max, ghist, hist_done, s);
 }
 
 }  // namespace hyb

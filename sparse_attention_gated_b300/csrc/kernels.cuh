@@ -8,7 +8,7 @@
 namespace hyb {
 
 // top-k threshold histogram over the top bits of the order-preserving score keys
-constexpr int kTopkHistBits = 11;
+constexpr int kTopkHistBits = 12;
 constexpr int kTopkHistBins = 1 << kTopkHistBits;
 
 // compress.cu

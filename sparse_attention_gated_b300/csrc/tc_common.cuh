@@ -213,8 +213,16 @@ __device__ __forceinline__ void cp_async_wait_group() {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Make this thread's generic-proxy writes to shared memory visible to the
-// async proxy (tensor-core operand reads) before it signals a consumer.
+// Make the mbarrier track this thread's cp.async copies issued so far: its
+// pending count rises by one now and falls when they have all landed, so the
+// phase cannot complete before them.  The thread does not wait.
+__device__ __forceinline__ void cp_async_arrive_on(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Order generic-proxy shared-memory accesses (st.shared, cp.async) with the
+// async proxy (tensor-core operand reads): the writer before it signals, or the
+// consumer after it has observed the copies' completion.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

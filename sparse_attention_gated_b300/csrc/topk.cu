@@ -21,15 +21,15 @@
 //   one stage   (rows of at most kStageCap visible entries): one CTA per row
 //               stages the keys in shared memory, selects and collects.
 //   three kernels (longer rows, e.g. 262,144 entries at 1M context):
-//     hist    CTA (chunk, row): 11-bit histogram of its chunk, added into the
+//     hist    CTA (chunk, row): 12-bit histogram of its chunk, added into the
 //             row's global histogram (the tensor-core indexer builds it in its
 //             epilogue for decode rows; then this kernel is skipped).
 //     filter  CTA (chunk, row): from the row histogram, the bin b* that holds
 //             the k-th largest key; the chunk's entries above b* (all kept)
 //             and inside b* (candidates) are written, in index order, to the
 //             chunk's own regions.
-//             The filter also histograms the next 11 bits of the candidates.
-//     final   CTA per row: from that second histogram, the digit b2 holding
+//             The filter also histograms the next 12 bits of the candidates.
+//     final   (the row's last filter CTA): from that second histogram, the digit b2 holding
 //             the last kept candidate; candidates above it are kept, the few
 //             equal to it are selected exactly; the kept candidates are then
 //             merged with the entries above b* (both lists are ascending).
@@ -42,6 +42,7 @@ constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int64_t kStageCap = 16384;  // one-stage plan: keys staged in shared memory
 constexpr int64_t kCandCap = 65536;   // final kernel: candidates tracked by a shared-memory bitmap
 constexpr int64_t kSubCap = 8192;     // final kernel: second-level candidates staged in shared memory
+constexpr int kRun = 8;               // final kernel: candidates per thread per round
 constexpr int kHistBits = kTopkHistBits;
 constexpr int kHistBins = kTopkHistBins;
 constexpr int kMaxChunks = 64;
@@ -62,6 +63,7 @@ struct TopkParams {
   uint32_t* cand_key;   // [rows][n_chunks][chunk]: entries in the threshold bin
   int32_t* cand_idx;
   int32_t* counts;      // [rows][n_chunks][2]: (#above, #candidates) of each chunk
+  uint32_t* done;       // [rows]: filter CTAs finished (the last one selects)
 };
 
 __device__ __forceinline__ int64_t row_visible(const TopkParams& p, int64_t row) {
@@ -325,69 +327,10 @@ __device__ void threshold_bin(const uint32_t* gh, uint32_t k, BlockShared& S, ui
   __syncthreads();
 }
 
-// ---------------------------------------------- three kernels: filter
-__global__ void __launch_bounds__(kTopkThreads) topk_filter_kernel(TopkParams p) {
-  __shared__ BlockShared S;
-  const int64_t row = blockIdx.y;
-  const int64_t vis = row_visible(p, row);
-  if (vis <= p.k) return;
-  const int64_t s0 = (int64_t)blockIdx.x * p.chunk;
-  int32_t* cnt = p.counts + (row * p.n_chunks + blockIdx.x) * 2;
-  if (s0 >= vis) {
-    if (threadIdx.x == 0) cnt[0] = 0, cnt[1] = 0;
-    return;
-  }
-  const int64_t len = vis - s0 < p.chunk ? vis - s0 : p.chunk;
-  __shared__ uint32_t hist2[kHistBins];
-  for (int i = threadIdx.x; i < kHistBins; i += kTopkThreads) hist2[i] = 0;
-  uint32_t bstar, above;
-  threshold_bin(p.ghist + row * kHistBins, (uint32_t)p.k, S, bstar, above);  // (syncs the zeroing too)
-  const float* sc = p.scores + row * p.score_stride + s0;
-  const int64_t reg = (row * p.n_chunks + blockIdx.x) * p.chunk;
-  // each thread takes 4 consecutive entries, so one block scan orders 4096 of them
-  uint32_t nd = 0, nc = 0;
-  for (int64_t base = 0; base < len; base += 4 * kTopkThreads) {
-    const int64_t s = base + 4 * threadIdx.x;
-    uint32_t key[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) key[u] = s + u < len ? float_order_key(__ldg(sc + s + u)) : 0u;
-    bool d[4], c[4];
-    uint32_t ld = 0, lc = 0;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const uint32_t bin = key[u] >> (32 - kHistBits);
-      d[u] = s + u < len && bin > bstar;
-      c[u] = s + u < len && bin == bstar;
-      ld += d[u], lc += c[u];
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) hist_add(hist2, c[u], (key[u] >> (32 - 2 * kHistBits)) & (kHistBins - 1));
-    uint32_t db, cb, dt, ct;
-    block_scan_counts(ld, lc, S, db, cb, dt, ct);
-    uint32_t od = nd + db, oc = nc + cb;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if (d[u]) p.def_idx[reg + od++] = (int32_t)(s0 + s + u);
-      if (c[u]) {
-        p.cand_key[reg + oc] = key[u];
-        p.cand_idx[reg + oc++] = (int32_t)(s0 + s + u);
-      }
-    }
-    nd += dt, nc += ct;
-  }
-  if (threadIdx.x == 0) cnt[0] = (int32_t)nd, cnt[1] = (int32_t)nc;
-  __syncthreads();
-  uint32_t* gh2 = p.ghist2 + row * kHistBins;
-  for (int i = threadIdx.x; i < kHistBins; i += kTopkThreads)
-    if (hist2[i]) atomicAdd(gh2 + i, hist2[i]);
-}
-
-// ----------------------------------------------- three kernels: final
-__global__ void __launch_bounds__(kTopkThreads) topk_final_kernel(TopkParams p) {
-  extern __shared__ uint32_t dyn[];
-  __shared__ BlockShared S;
+// ------------------------------------------ three kernels: final selection
+// Run by the last filter CTA of a row, once every chunk's lists and counts are final.
+__device__ void final_select(const TopkParams& p, int64_t row, uint32_t* dyn, BlockShared& S) {
   __shared__ int32_t pre_d[kMaxChunks + 1], pre_c[kMaxChunks + 1];
-  const int64_t row = blockIdx.x;
   const int64_t vis = row_visible(p, row);
   if (vis <= p.k) {
     keep_all(p, row, vis);
@@ -451,43 +394,109 @@ __global__ void __launch_bounds__(kTopkThreads) topk_final_kernel(TopkParams p) 
   threshold_bin(p.ghist2 + row * kHistBins, (uint32_t)r, S, b2, above2);
   const int64_t r2 = r - above2;  // how many of the candidates with digit2 == b2 to keep
   auto digit2 = [&](uint32_t key) { return (key >> (32 - 2 * kHistBits)) & (uint32_t)(kHistBins - 1); };
-  // stage the sub-candidates (digit2 == b2) in candidate order
+  // Passes over the candidates in rounds of kRun * kTopkThreads: in a round each thread
+  // takes a contiguous run of kRun candidates and loads them all at once (one round trip
+  // per round), and one block scan orders the round.
+  const bool fast = n_cand <= kCandCap;
+  constexpr int64_t kRound = (int64_t)kRun * kTopkThreads;
+  // global offsets of a run's candidates: chunks first (shared memory only), so that
+  // the loads that follow are all independent
+  auto run_offsets = [&](int64_t x0, int64_t x1, int64_t (&at)[kRun]) {
+    int c = x0 < n_cand ? chunk_in(pre_c, x0) : 0;
+#pragma unroll
+    for (int u = 0; u < kRun; ++u) {
+      const int64_t x = x0 + u;
+      if (x < x1) {
+        while (pre_c[c + 1] <= x) ++c;  // a run crosses chunk boundaries in order
+        at[u] = reg0 + (int64_t)c * p.chunk + (x - pre_c[c]);
+      } else {
+        at[u] = 0;
+      }
+    }
+  };
+  auto load_run = [&](int64_t base, uint32_t (&rk)[kRun], int64_t& x0, int64_t& x1) {
+    x0 = std::min<int64_t>(base + (int64_t)tid * kRun, n_cand);
+    x1 = std::min<int64_t>(x0 + kRun, n_cand);
+    int64_t at[kRun];
+    run_offsets(x0, x1, at);
+#pragma unroll
+    for (int u = 0; u < kRun; ++u) rk[u] = x0 + u < x1 ? p.cand_key[at[u]] : 0u;
+  };
   uint32_t n_sub = 0;
-  for (int64_t base = 0; base < n_cand; base += kTopkThreads) {
-    const int64_t x = base + tid;
-    const uint32_t key = x < n_cand ? p.cand_key[cand_at(x)] : 0u;
-    const bool sub = x < n_cand && digit2(key) == b2;
-    uint32_t sb, ub, st, ut;
-    block_scan_counts(sub, 0u, S, sb, ub, st, ut);
-    if (sub && n_sub + sb < kSubCap) sk[n_sub + sb] = key, spos[n_sub + sb] = (int32_t)x;
-    n_sub += st;
-  }
-  const bool fast = n_sub <= kSubCap && n_cand <= kCandCap;
   if (fast) {
+    // the sub-candidates (digit2 == b2), in candidate order
+    for (int64_t base = 0; base < n_cand; base += kRound) {
+      uint32_t rk[kRun];
+      int64_t x0, x1;
+      load_run(base, rk, x0, x1);
+      uint32_t mine = 0;
+#pragma unroll
+      for (int u = 0; u < kRun; ++u) mine += (x0 + u < x1 && digit2(rk[u]) == b2);
+      uint32_t sb, zb, st, zt;
+      block_scan_counts(mine, 0u, S, sb, zb, st, zt);
+      sb += n_sub;
+#pragma unroll
+      for (int u = 0; u < kRun; ++u)
+        if (x0 + u < x1 && digit2(rk[u]) == b2) {
+          if (sb < kSubCap) sk[sb] = rk[u], spos[sb] = (int32_t)(x0 + u);
+          ++sb;
+        }
+      n_sub += st;
+    }
+  }
+  if (fast && n_sub <= kSubCap) {
     for (int64_t x = tid; x < kCandCap / 32; x += kTopkThreads) selbits[x] = 0u;
     __syncthreads();
-    uint32_t T, ties;
-    auto subkey = [&](int64_t x) { return sk[x]; };
-    radix_select(subkey, n_sub, r2, S, T, ties);
-    collect_ordered(subkey, n_sub, T, ties, S, [&](uint32_t, int64_t x) {
+    auto mark = [&](int64_t x) {
       const int32_t pos = spos[x];
       atomicOr(&selbits[pos >> 5], 1u << (pos & 31));
-    });
+    };
+    if (r2 == n_sub) {  // every sub-candidate is kept
+      for (int64_t x = tid; x < n_sub; x += kTopkThreads) mark(x);
+    } else if (n_sub <= kTopkThreads) {
+      // few: rank each directly by (key desc, position asc); the r2 best are kept
+      if (tid < n_sub) {
+        const uint32_t kx = sk[tid];
+        int64_t rank = 0;
+        for (int64_t y = 0; y < n_sub; ++y) {
+          const uint32_t ky = sk[y];
+          rank += ky > kx || (ky == kx && y < tid);
+        }
+        if (rank < r2) mark(tid);
+      }
+    } else {
+      uint32_t T, ties;
+      auto subkey = [&](int64_t x) { return sk[x]; };
+      radix_select(subkey, n_sub, r2, S, T, ties);
+      collect_ordered(subkey, n_sub, T, ties, S, [&](uint32_t, int64_t x) { mark(x); });
+    }
     __syncthreads();
     // kept candidates in order: digit2 above b2, or selected among the sub-candidates
     uint32_t nb = 0;
-    for (int64_t base = 0; base < n_cand; base += kTopkThreads) {
-      const int64_t x = base + tid;
-      bool keep = false;
-      int64_t at = 0;
-      if (x < n_cand) {
-        at = cand_at(x);
-        const uint32_t d2 = digit2(p.cand_key[at]);
-        keep = d2 > b2 || (d2 == b2 && ((selbits[x >> 5] >> (x & 31)) & 1u));
+    for (int64_t base = 0; base < n_cand; base += kRound) {
+      uint32_t rk[kRun];
+      int64_t x0, x1;
+      load_run(base, rk, x0, x1);
+      bool keep[kRun];
+      uint32_t mine = 0;
+#pragma unroll
+      for (int u = 0; u < kRun; ++u) {
+        const int64_t x = x0 + u;
+        const uint32_t d2 = x < x1 ? digit2(rk[u]) : 0u;
+        keep[u] = x < x1 && (d2 > b2 || (d2 == b2 && ((selbits[x >> 5] >> (x & 31)) & 1u)));
+        mine += keep[u];
       }
       uint32_t kb, zb, kt, zt;
-      block_scan_counts(keep, 0u, S, kb, zb, kt, zt);
-      if (keep) B[nb + kb] = p.cand_idx[at];
+      block_scan_counts(mine, 0u, S, kb, zb, kt, zt);
+      kb += nb;
+      int64_t at[kRun];
+      run_offsets(x0, x1, at);
+      int32_t ix[kRun];
+#pragma unroll
+      for (int u = 0; u < kRun; ++u) ix[u] = keep[u] ? p.cand_idx[at[u]] : 0;
+#pragma unroll
+      for (int u = 0; u < kRun; ++u)
+        if (keep[u]) B[kb++] = ix[u];
       nb += kt;
     }
   } else {
@@ -512,6 +521,79 @@ __global__ void __launch_bounds__(kTopkThreads) topk_final_kernel(TopkParams p) 
     out[slot] = v;
     if (out_sc) out_sc[slot] = sc[v];
   }
+}
+
+// ---------------------------------------------- three kernels: filter
+__device__ void filter_chunk(const TopkParams& p, int64_t row, int64_t vis, BlockShared& S);
+
+// Every CTA filters its chunk, then counts itself done; the row's last CTA (no
+// waiting: it is simply the one that finds all others done) runs the final selection.
+__global__ void __launch_bounds__(kTopkThreads) topk_filter_kernel(TopkParams p) {
+  extern __shared__ uint32_t dyn[];
+  __shared__ BlockShared S;
+  __shared__ uint32_t s_last;
+  const int64_t row = blockIdx.y;
+  const int64_t vis = row_visible(p, row);
+  if (vis > p.k) filter_chunk(p, row, vis, S);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(p.done + row, 1u) == (uint32_t)(p.n_chunks - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  final_select(p, row, dyn, S);
+}
+
+__device__ void filter_chunk(const TopkParams& p, int64_t row, int64_t vis, BlockShared& S) {
+  const int64_t s0 = (int64_t)blockIdx.x * p.chunk;
+  int32_t* cnt = p.counts + (row * p.n_chunks + blockIdx.x) * 2;
+  if (s0 >= vis) {
+    if (threadIdx.x == 0) cnt[0] = 0, cnt[1] = 0;
+    return;
+  }
+  const int64_t len = vis - s0 < p.chunk ? vis - s0 : p.chunk;
+  __shared__ uint32_t hist2[kHistBins];  // 16 KiB
+  for (int i = threadIdx.x; i < kHistBins; i += kTopkThreads) hist2[i] = 0;
+  uint32_t bstar, above;
+  threshold_bin(p.ghist + row * kHistBins, (uint32_t)p.k, S, bstar, above);  // (syncs the zeroing too)
+  const float* sc = p.scores + row * p.score_stride + s0;
+  const int64_t reg = (row * p.n_chunks + blockIdx.x) * p.chunk;
+  // each thread takes 4 consecutive entries, so one block scan orders 4096 of them
+  uint32_t nd = 0, nc = 0;
+  for (int64_t base = 0; base < len; base += 4 * kTopkThreads) {
+    const int64_t s = base + 4 * threadIdx.x;
+    uint32_t key[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) key[u] = s + u < len ? float_order_key(__ldg(sc + s + u)) : 0u;
+    bool d[4], c[4];
+    uint32_t ld = 0, lc = 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t bin = key[u] >> (32 - kHistBits);
+      d[u] = s + u < len && bin > bstar;
+      c[u] = s + u < len && bin == bstar;
+      ld += d[u], lc += c[u];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) hist_add(hist2, c[u], (key[u] >> (32 - 2 * kHistBits)) & (kHistBins - 1));
+    uint32_t db, cb, dt, ct;
+    block_scan_counts(ld, lc, S, db, cb, dt, ct);
+    uint32_t od = nd + db, oc = nc + cb;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (d[u]) p.def_idx[reg + od++] = (int32_t)(s0 + s + u);
+      if (c[u]) {
+        p.cand_key[reg + oc] = key[u];
+        p.cand_idx[reg + oc++] = (int32_t)(s0 + s + u);
+      }
+    }
+    nd += dt, nc += ct;
+  }
+  if (threadIdx.x == 0) cnt[0] = (int32_t)nd, cnt[1] = (int32_t)nc;
+  __syncthreads();
+  uint32_t* gh2 = p.ghist2 + row * kHistBins;
+  for (int i = threadIdx.x; i < kHistBins; i += kTopkThreads)
+    if (hist2[i]) atomicAdd(gh2 + i, hist2[i]);
 }
 
 // ------------------------------------------------------------------ host
@@ -543,7 +625,7 @@ size_t topk_workspace_bytes(const hyb_index_args* a, int64_t n_vis_max) {
   if (!pl.three) return 0;
   const size_t rows = (size_t)(a->batch * a->n_q);
   const size_t region = rows * (size_t)pl.n_chunks * (size_t)pl.chunk;
-  return align256(rows * kHistBins * 8) + 3 * align256(region * 4) + align256(rows * pl.n_chunks * 8);
+  return align256(rows * kHistBins * 8 + rows * 4) + 3 * align256(region * 4) + align256(rows * pl.n_chunks * 8);
 }
 
 bool topk_shape_supported(const hyb_index_args* a, int64_t) { return a->k >= 1 && a->k <= 2048; }
@@ -553,7 +635,8 @@ static void topk_pointers(TopkParams& p, const TopkPlan& pl, int64_t rows, void*
   char* w = static_cast<char*>(ws);
   p.ghist = reinterpret_cast<uint32_t*>(w);
   p.ghist2 = p.ghist + rows * kHistBins;
-  w += align256((size_t)rows * kHistBins * 8);
+  p.done = p.ghist2 + rows * kHistBins;
+  w += align256((size_t)rows * kHistBins * 8 + (size_t)rows * 4);
   p.def_idx = reinterpret_cast<int32_t*>(w);
   w += align256(region * 4);
   p.cand_key = reinterpret_cast<uint32_t*>(w);
@@ -570,7 +653,7 @@ uint32_t* topk_prepare_hist(const hyb_index_args* a, int64_t n_vis_max, void* ws
   if (rows == 0 || !pl.three) return nullptr;
   TopkParams p{};
   topk_pointers(p, pl, rows, ws);
-  *err = cudaMemsetAsync(p.ghist, 0, (size_t)rows * kHistBins * 8, s);  // both histograms
+  *err = cudaMemsetAsync(p.ghist, 0, (size_t)rows * (kHistBins * 8 + 4), s);  // histograms and counters
   return p.ghist;
 }
 
@@ -598,12 +681,10 @@ cudaError_t launch_topk(const hyb_index_args* a, const float* scores, int64_t sc
     topk_hist_kernel<<<grid, kTopkThreads, 0, s>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  topk_filter_kernel<<<grid, kTopkThreads, 0, s>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const size_t smem = (size_t)2 * a->k * 4 + (size_t)kSubCap * 8 + (size_t)kCandCap / 8;
-  e = cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = cudaFuncSetAttribute(topk_filter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  topk_final_kernel<<<(unsigned)rows, kTopkThreads, smem, s>>>(p);
+  topk_filter_kernel<<<grid, kTopkThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
