@@ -13,10 +13,13 @@ with inputs resident in HBM; `e2e` is the same metric through the public
 API with the step's fresh inputs copied from pinned host memory and the
 outputs read back inside the timed region.
 
-Timing: W warm-up steps, then exactly K steps captured as one CUDA graph and
-replayed once between CUDA events; inputs rotate over enough copies that one
-pass over them touches at least 4x the L2 size.  Per-stage CUDA events inside
-the same graph give each stage's average duration.
+Timing: W warm-up steps, then exactly K steps captured as one CUDA graph of
+the library's launches and replayed once between CUDA events (the headline
+time); inputs rotate over enough copies that one pass over them touches at
+least 4x the L2 size.  A second graph of the same K steps with CUDA events
+around every stage, and around the indexer's scoring kernel (recorded by the
+library), gives each stage's and that kernel's average duration (the
+roofline); its own step time is reported beside the headline.
 """
 from __future__ import annotations
 
@@ -87,6 +90,22 @@ def stage_model(w):
         m["csa_swa_merge"] = dict(bytes=n * (c * bf + H * c * (bf + 4 + bf)), flops=win * H * c * 4,
                                   flop_dtype="bf16")
     return m
+
+
+def scoring_kernel_model(w):
+    """Algorithmic bytes / flops of one launch of the indexer's scoring kernel (its
+    inputs read once: the FP8 keys and scales, the queries, scales and head weights)."""
+    if w.kind not in ("hybrid_decode", "csa_decode", "csa_prefill"):
+        return None
+    n_q = 1 if w.decode else w.n_ctx
+    N = w.n_csa
+    qb = w.n_ih * (w.c_I + 8)
+    if w.decode:
+        pairs = N
+    else:
+        pairs = sum(min(N, (t + 1) // w.m) for t in range(w.n_ctx))
+    return dict(bytes=w.batch * (N * (w.c_I + 4) + n_q * qb), flops=w.batch * pairs * w.n_ih * w.c_I * 2,
+                flop_dtype="fp8")
 
 
 # ------------------------------------------------------------------ clocks
@@ -185,13 +204,14 @@ def run_ours(args, w):
 
     def run_step(st, ev=None):
         # one forward step; ev: dict stage -> (start, end) events recorded around each stage
+        # (and "index_scores" -> the events the library records around its scoring kernel)
         def rec(name, which):
             if ev is not None:
                 ev[name][which].record(stream)
 
         if st.has_csa:
             rec("csa_compress", 0)
-            _csa_parts(st, stream, rec)
+            _csa_parts(st, stream, rec, None if ev is None else ev["index_scores"])
         if st.has_hca:
             rec("hca_compress", 0)
             _hca_parts(st, stream, rec)
@@ -202,16 +222,27 @@ def run_ours(args, w):
             run_step(steps[i % copies])
     stream.synchronize()
 
-    # the K timed steps as one graph, with per-stage events
-    # external event records: real timestamps taken by each replay of the graph
+    # The K timed steps as one graph of the library's launches only (the headline
+    # time), and the same K steps as a second graph with CUDA events around every
+    # stage and around the indexer's scoring kernel (stage and kernel times).
+    # External event records: real timestamps taken by each replay of the graph.
     ev = lambda: torch.cuda.Event(enable_timing=True, external=True)
-    events = [{s: (ev(), ev()) for s in stages} for _ in range(args.steps)]
+    events = [{s: (ev(), ev()) for s in stages + ["index_scores"]} for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for e in events:  # create the events (the library records two of them itself)
+            for pair in e.values():
+                pair[0].record(stream), pair[1].record(stream)
+    stream.synchronize()
     g = torch.cuda.CUDAGraph()
+    g_ev = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(g, stream=stream):
             for i in range(args.steps):
+                run_step(steps[i % copies])
+        with torch.cuda.graph(g_ev, stream=stream):
+            for i in range(args.steps):
                 run_step(steps[i % copies], events[i])
-    # warm the graph (and the clocks) for about a second
+    # warm the graphs (and the clocks) for about a second
     sampler = ClockSampler(local)
     t_busy0 = time.time()
     with torch.cuda.stream(stream):
@@ -222,6 +253,7 @@ def run_ours(args, w):
     with torch.cuda.stream(stream):
         for _ in range(min(reps, 200)):
             g.replay()
+        g_ev.replay()
     stream.synchronize()
 
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -244,8 +276,19 @@ def run_ours(args, w):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_total = float(t.item())
     ms_step = ms_total / args.steps
+    # the evented graph, right after: per-stage and scoring-kernel times
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        s0.record(stream)
+        g_ev.replay()
+        s1.record(stream)
+    torch.cuda.synchronize()
+    ms_step_ev = s0.elapsed_time(s1) / args.steps
+    has_scoring = "csa_index_topk" in stages
+    timed = stages + (["index_scores"] if has_scoring else [])
     stage_ms = {s: statistics.mean(events[i][s][0].elapsed_time(events[i][s][1]) for i in range(args.steps))
-                for s in stages}
+                for s in timed}
+    scoring_ms = stage_ms.pop("index_scores", None)
 
     units = w.batch if w.decode else w.n_ctx
     value = units * world / (ms_step / 1e3)
@@ -253,22 +296,29 @@ def run_ours(args, w):
     # -------- e2e through the public API: fresh inputs from pinned host memory
     e2e = run_e2e(args, w, steps[0], stream, units, world, dist)
 
-    # -------- roofline of the dominant stage
+    # -------- roofline of the dominant kernel: the indexer's scoring kernel (timed by
+    # the events the library records around it) where the workload has a CSA layer,
+    # else the dominant stage (one kernel per stage)
     peaks, peak_kind = measured_peaks()
-    dom = max(stage_ms, key=lambda s: stage_ms[s])
-    dm = model[dom]
+    if has_scoring:
+        dom, dm, dom_ms = "index_tc_kernel (csa_index_topk scoring)", scoring_kernel_model(w), scoring_ms
+    else:
+        dom = max(stage_ms, key=lambda s: stage_ms[s])
+        dm, dom_ms = model[dom], stage_ms[dom]
     if dm["flops"] > 0 and dm.get("flop_dtype") in ("bf16", "fp8") and \
             dm["flops"] / max(dm["bytes"], 1) > _ridge(peaks, dm.get("flop_dtype")):
         peak = peaks["bf16_tflops_sustained"] * (2 if dm["flop_dtype"] == "fp8" else 1)
-        achieved = dm["flops"] / (stage_ms[dom] / 1e3) / 1e12
+        achieved = dm["flops"] / (dom_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": None}
     else:
         peak = peaks["hbm_gbs"]
-        achieved = dm["bytes"] / (stage_ms[dom] / 1e3) / 1e9
+        achieved = dm["bytes"] / (dom_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": None}
     roof["kernel"] = dom
+    roof["ms_per_launch"] = dom_ms
+    roof["algorithmic_bytes"] = dm["bytes"]
     roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
 
     step_roof_s = max(step_bytes / (peaks["hbm_gbs"] * 1e9), 0.0)
@@ -294,6 +344,7 @@ def run_ours(args, w):
         "gpu_launches": _launches_per_step(w) * args.steps,
         "roofline": roof,
         "stages_ms": stage_ms,
+        "ms_per_step_with_stage_events": ms_step_ev,
         "step_hbm_roofline_frac": step_roof_s / (ms_step / 1e3),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -308,8 +359,9 @@ def _ridge(peaks, dt):
     return tf * 1e12 / (peaks["hbm_gbs"] * 1e9)
 
 
-def _csa_parts(st, stream, rec):
-    """The CSA layer's ABI calls with stage events between them (same calls as HybridStep.run_csa)."""
+def _csa_parts(st, stream, rec, scoring_events=None):
+    """The CSA layer's ABI calls with stage events between them (same calls as HybridStep.run_csa);
+    scoring_events: (begin, end) events the library records around its scoring kernel."""
     from sparse_attention_gated_b300 import ops
 
     w, x, b = st.w, st.x, st.buf
@@ -329,7 +381,8 @@ def _csa_parts(st, stream, rec):
     rec("csa_compress", 1)
     rec("csa_index_topk", 0)
     ops.csa_index_topk(x["qI"], x["w"], kI, m=w.m, k=w.k, q_pos0=w.q_pos0, qI_scale=x.get("qI_scale"), kI_scale=kIs,
-                       idx=b["idx"], workspace=st.ws["index"], dev_status=s, stream=stream)
+                       idx=b["idx"], workspace=st.ws["index"], dev_status=s, stream=stream,
+                       scores_events=scoring_events)
     rec("csa_index_topk", 1)
     rec("csa_attend", 0)
     ops.csa_attend(x["q"], kc, kc, b["idx"], scale=w.scale, o=b["o"], lse=b["lse"], workspace=st.ws["csa"],
@@ -367,9 +420,9 @@ def _hca_parts(st, stream, rec):
 def _launches_per_step(w):
     n = 0
     if w.kind in ("hybrid_decode", "csa_decode", "csa_prefill"):
-        n += 2 + 2 + 2 + 1  # compress x2, index scores + top-k, attend (+ combine), window merge
+        n += 2 + 2 + 1 + 1  # compress x2, index scores + top-k, attend (splits join in-kernel), window merge
     if w.kind in ("hybrid_decode", "hca_decode"):
-        n += 1 + 2 + 1
+        n += 1 + 1 + 1
     return n
 
 
@@ -378,19 +431,17 @@ def run_e2e(args, w, st, stream, units, world, dist):
     fresh inputs copied from pinned host memory and the outputs copied back."""
     import torch
 
-    keys = st.step_input_keys()
-    host_in = {k: st.x[k].detach().cpu().pin_memory() for k in keys}
-    outs = st.output_keys()
-    host_out = {k: torch.empty(st.buf[k].shape, dtype=st.buf[k].dtype, pin_memory=True) for k in outs}
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    # the step's inputs and outputs as one contiguous buffer each: one copy each way per step
+    dev_in, dev_out = st.pack_step_io()
+    host_in = dev_in.cpu().pin_memory()
+    host_out = torch.empty(dev_out.shape, dtype=torch.uint8, pin_memory=True)
+    h2d = host_in.numel()
+    d2h = host_out.numel()
 
     def one():
-        for k in keys:
-            st.x[k].copy_(host_in[k], non_blocking=True)
+        dev_in.copy_(host_in, non_blocking=True)
         st.run(stream)
-        for k in outs:
-            host_out[k].copy_(st.buf[k], non_blocking=True)
+        host_out.copy_(dev_out, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(max(args.warmup, 3)):
@@ -418,7 +469,7 @@ def run_e2e(args, w, st, stream, units, world, dist):
         ms = float(t.item())
     return {"value": units * world / (ms / n / 1e3), "unit": "queries/s" if w.decode else "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / n,
-            "graph": "copies + step captured as one CUDA graph"}
+            "graph": "copies + step captured as one CUDA graph", "copies": "one H2D and one D2H per step (packed buffers)"}
 
 
 # ------------------------------------------------------------ CPU oracle

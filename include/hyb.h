@@ -177,6 +177,13 @@ typedef struct hyb_index_args {
   int64_t q_pos0;
   int32_t dtype; /* hyb_dtype: HYB_F32 or HYB_E4M3 */
   int32_t* dev_status;
+  /* Optional profiling events (cudaEvent_t, or NULL): recorded on the stream
+     right before and right after the scoring kernel, so that a caller can time
+     the scoring apart from the selection.  Recorded as external events
+     (cudaEventRecordExternal), so they stay in a graph captured from the
+     stream.  The library neither creates nor destroys them. */
+  void* ev_scores_begin;
+  void* ev_scores_end;
 } hyb_index_args;
 
 HYB_API size_t csa_index_topk_workspace_size(const hyb_index_args* a);

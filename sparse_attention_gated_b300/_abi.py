@@ -31,7 +31,8 @@ class CompressArgs(ctypes.Structure):
 class IndexArgs(ctypes.Structure):
     _fields_ = [("qI", _p), ("qI_scale", _p), ("w", _p), ("kI", _p), ("kI_scale", _p), ("idx", _p), ("scores", _p),
                 ("batch", _i64), ("n_q", _i64), ("n_entries", _i64), ("kv_stride", _i64), ("n_ih", _i64),
-                ("c_I", _i64), ("m", _i64), ("k", _i64), ("q_pos0", _i64), ("dtype", _i32), ("dev_status", _p)]
+                ("c_I", _i64), ("m", _i64), ("k", _i64), ("q_pos0", _i64), ("dtype", _i32), ("dev_status", _p),
+                ("ev_scores_begin", _p), ("ev_scores_end", _p)]
 
 
 class CsaAttendArgs(ctypes.Structure):

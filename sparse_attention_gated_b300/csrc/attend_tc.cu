@@ -61,6 +61,7 @@ constexpr int kTile = 128;              // entries per tile
 constexpr int kSlabs = kC / 64;         // column slabs of 64 dims (128 bytes) per row
 constexpr int kSlabBytes = kTile * 128;  // 16 KiB
 constexpr int kQSlabBytes = kHG * 128;   // 8 KiB
+constexpr int kMaxSplits = 64;         // splits of one (query, head group) list
 constexpr int kOffQ = 0;
 constexpr int kOffKV = kOffQ + kSlabs * kQSlabBytes;
 constexpr int kOffP = kOffKV + kSlabs * kSlabBytes;
@@ -69,9 +70,9 @@ constexpr int kOffRed = kOffP + kTile * kHG * 2;
 // tile parity: head-major so that one 16-byte load gets a head's four quadrants) and
 // wt[8 warps][4][32] (each softmax warp's per-head table: reference, rescale factor,
 // output coefficients)
-constexpr int kRedFloats = 2 * 64 * 4 + 8 * 4 * 32 + 2 * 64;  // + ml[64] float2: (m, l) per head
+constexpr int kRedFloats = 2 * 64 * 4 + 8 * 4 * 32;
 constexpr int kOffBar = kOffRed + kRedFloats * 4;
-constexpr int kNumBars = 1 + 2 * kSlabs + 2 + 2 + 1 + 1 + 2 + 1 + 1;
+constexpr int kNumBars = 1 + 2 * kSlabs + 2 + 2 + 1 + 1 + 2 + 1 + 1 + 1 + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 constexpr uint32_t kTmemCols = 512;
@@ -90,6 +91,7 @@ struct AtcParams {
   float* o;                 // modes 0/1, one split: [rows][n_h][c]
   float* lse;               // [rows][n_h]
   float* part_o;            // modes 0/1, several splits: [rows][n_split][n_h][c]
+  uint32_t* join_cnt;       // modes 0/1, several splits: [rows * n_hg] splits done (zeroed per launch)
   float2* part_ml;          // [rows][n_split][n_h] (reference m in log2 units, denominator)
   const float* o_in;        // mode 2
   const float* lse_in;
@@ -98,7 +100,6 @@ struct AtcParams {
   int out_bf16;
   int64_t n_q, n_h, n_entries, kv_stride, list_len, m, q_pos0, kv_pos0, n_win;
   int n_split, n_hg, alias;
-  int cluster;  // the n_split CTAs of a (query, head group) form one cluster and merge through DSMEM
   float scale_log2;
   int32_t* dev_status;
 };
@@ -114,7 +115,7 @@ struct AtcWork {
 template <int MODE>
 __device__ __forceinline__ AtcWork atc_work(const AtcParams& p) {
   AtcWork w;
-  const int64_t id = blockIdx.x;  // split fastest: the splits of a unit are consecutive CTAs (one cluster)
+  const int64_t id = blockIdx.x;  // split fastest: the splits of a unit are consecutive CTAs
   w.sp = id % p.n_split;
   w.hg = (id / p.n_split) % p.n_hg;
   w.bq = id / ((int64_t)p.n_hg * p.n_split);
@@ -133,6 +134,10 @@ __device__ __forceinline__ AtcWork atc_work(const AtcParams& p) {
   } else {
     w.L = t + 1 < p.n_win ? t + 1 : p.n_win;
     w.row0 = w.b * p.kv_stride + (t - w.L + 1 - p.kv_pos0);
+    // (split window merges divide the output dims, not the rows: every split sees the window)
+    w.tb = 0;
+    w.te = (w.L + kTile - 1) / kTile;
+    return w;
   }
   const int64_t T = (w.L + kTile - 1) / kTile;
   w.tb = w.sp * T / p.n_split;
@@ -177,10 +182,10 @@ __device__ __forceinline__ int64_t atc_group(int64_t G, int64_t ngroups, bool& i
 // in slab order, so no warp waits on a slot more than one phase ahead.  The
 // contiguous modes gather only a ragged last tile, after TMA tiles that warp 0
 // issued alone; warp 0 also gathers so that every slot's phases are waited in
-// order by one warp.
+// order by one warp.  A list shorter than a tile has no TMA tile at all.
 template <int MODE>
-__device__ __forceinline__ int atc_gather_warp(int64_t g) {
-  return MODE == 0 ? (int)(g % kProdWarps) : 0;
+__device__ __forceinline__ int atc_gather_warp(int64_t g, int64_t list_len) {
+  return (MODE == 0 || list_len < kTile) ? (int)(g % kProdWarps) : 0;
 }
 
 // Reduce 32 per-lane values (one per head) across the 32 lanes of a warp by
@@ -214,7 +219,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* p_s = smem + kOffP;
   float* red = reinterpret_cast<float*>(smem + kOffRed);  // [2][64][4]
   float* wtab = red + 2 * 64 * 4;                           // [8][4][32]
-  float2* ml_s = reinterpret_cast<float2*>(wtab + 8 * 4 * 32);  // [64] (m, l) of this CTA (cluster merge)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* q_full = bars;
   uint64_t* kv_full = q_full + 1;
@@ -226,6 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* sm_sync = o_done + 1;  // [2]: one per head half (4 softmax warps each)
   uint64_t* fin = sm_sync + 2;
   uint64_t* oin_full = fin + 1;
+  uint64_t* q_free = oin_full + 1;  // the last products that read the query are done
+  uint64_t* sm_all = q_free + 1;     // all softmax warps (the split join)
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kOffMisc);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc) + 1;
 
@@ -236,6 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // otherwise the V slabs are loaded again after the next tile's K (see above)
   const bool reuse = p.alias && ntiles == 1;
   const int64_t ngroups = reuse ? 1 : 2 * ntiles;
+  // O^T chunks (128 dims each) this CTA computes: a split window merge takes 4/n_split of them
+  const int ch0 = MODE == 2 ? (int)W.sp * (4 / p.n_split) : 0;
+  const int ch1 = MODE == 2 ? ch0 + 4 / p.n_split : 4;
 
   // the first group's loads are issued by the thread that initialises the
   // barriers, before the CTA-wide setup sync (overlapping the TMEM allocation)
@@ -250,6 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(&sm_sync[1], kSoftThreads / 2);
     tc::mbar_init(fin, 1);
     tc::mbar_init(oin_full, 1);
+    tc::mbar_init(q_free, 1);
+    tc::mbar_init(sm_all, kSoftThreads);
     *s_abort = 0;
     tc::fence_barrier_init();
     if (ntiles > 0) {
@@ -329,21 +340,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
             if (!ok) break;
           }
-        } else if (atc_gather_warp<MODE>(g) == warp) {
+        } else if (atc_gather_warp<MODE>(g, W.L) == warp) {
           int okl = 1;
           if (lane == 0) okl = tc::mbar_wait(&kv_empty[s], par, s_abort, 2);
           ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
           if (!ok) break;
+          // eight lanes per row, one 16-byte chunk each: every instruction moves four whole
+          // 128-byte row pieces (entry e = 4*i + lane/8 takes its row from lane e % 32, value e / 32)
           const uint32_t dbase = tc::smem_u32(dst);
+          const int c16 = lane & 7;
 #pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int e = lane + 32 * r;
-            const bool have = rows[r] >= 0;
-            const __nv_bfloat16* rsrc = src + (have ? rows[r] : 0) * kC + s * 64;
-            const uint32_t drow = dbase + (uint32_t)((e >> 3) * 1024 + (e & 7) * 128);
-#pragma unroll
-            for (int c16 = 0; c16 < 8; ++c16)
-              tc::cp_async16(drow + (uint32_t)((c16 ^ (e & 7)) << 4), rsrc + c16 * 8, have ? 16u : 0u);
+          for (int i = 0; i < 32; ++i) {
+            const int e = 4 * i + (lane >> 3);
+            const int32_t row = __shfl_sync(0xffffffffu, (int32_t)rows[i >> 3], (4 * i + (lane >> 3)) & 31);
+            const bool have = row >= 0;
+            const __nv_bfloat16* rsrc = src + (int64_t)(have ? row : 0) * kC + s * 64 + c16 * 8;
+            const uint32_t dchunk = dbase + (uint32_t)((e >> 3) * 1024 + (e & 7) * 128 + ((c16 ^ (e & 7)) << 4));
+            tc::cp_async16(dchunk, rsrc, have ? 16u : 0u);
           }
           // the slab is complete once every lane's copies have landed; nobody waits here
           tc::cp_async_arrive_on(&kv_full[s]);
@@ -355,8 +368,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::cp_async_wait_all();  // this thread's copies have landed before it leaves
     bool oin_issued = false;
     if constexpr (MODE == 2) {
-      // the compressed-branch output of this query's heads, into the ring once the last products are done
-      if (ok && warp == 0 && p.o_in != nullptr && ntiles > 0) {
+      if (p.n_split > 1) {
+        // this split's dims of the compressed-branch output, [64 heads][D], into the query
+        // region once the last products that read the query are done
+        if (ok && warp == 0 && p.o_in != nullptr) {
+          int okl = 1;
+          if (lane == 0) {
+            if (ntiles > 0) okl = tc::mbar_wait(q_free, 0, s_abort, 15);
+            if (okl) {
+              const int D = kC / p.n_split;
+              tc::mbar_arrive_expect_tx(oin_full, (uint32_t)(kHG * D * 4));
+              const float* src = p.o_in + (W.bq * p.n_h + W.hg * kHG) * kC + W.sp * D;
+              for (int h = 0; h < kHG; ++h)
+                tc::bulk_load(q_s + h * D * 4, src + (int64_t)h * kC, (uint32_t)(D * 4), oin_full);
+              oin_issued = true;
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
+          oin_issued = __shfl_sync(0xffffffffu, (int)oin_issued, 0) != 0;
+        }
+      } else if (ok && warp == 0 && p.o_in != nullptr && ntiles > 0) {
+        // the compressed-branch output of this query's heads, into the ring once the last products are done
         int okl = 1;
         if (lane == 0) {
           const uint32_t lastpar = (uint32_t)((ngroups - 1) & 1);
@@ -410,17 +442,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!ok) break;
           tc::mma_commit(&s_full[sb]);
+          if (li == ntiles - 1) tc::mma_commit(q_free);
           if (reuse) {
             // O^T from the same slabs (they are V too), then release them
             if (!(ok = tc::mbar_wait(p_full, 0, s_abort, 6))) break;
             tc::tc_fence_after();
             for (int ch = 0; ch < 4; ++ch) {
               const uint32_t a0 = kv_addr + (uint32_t)(2 * ch * kSlabBytes);
+              if (ch >= ch0 && ch < ch1) {
 #pragma unroll
-              for (int ks = 0; ks < kTile / 16; ++ks)
-                tc::mma_f16(tmem + kTmemO + (uint32_t)(ch * kHG),
-                            tc::desc_mnmajor_sw128(a0 + ks * 2048, kSlabBytes, 1024),
-                            tc::desc_mnmajor_sw128(p_addr + ks * 2048, 16, 1024), idO, ks > 0 ? 1u : 0u);
+                for (int ks = 0; ks < kTile / 16; ++ks)
+                  tc::mma_f16(tmem + kTmemO + (uint32_t)(ch * kHG),
+                              tc::desc_mnmajor_sw128(a0 + ks * 2048, kSlabBytes, 1024),
+                              tc::desc_mnmajor_sw128(p_addr + ks * 2048, 16, 1024), idO, ks > 0 ? 1u : 0u);
+              }
               tc::mma_commit(&kv_empty[2 * ch]);
               tc::mma_commit(&kv_empty[2 * ch + 1]);
             }
@@ -614,15 +649,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           cw = ew / (den * (l > 0.f ? l : 1.f));  // the accumulator is unnormalised
           Lse = M + logf(den);
         }
-        if (q4 == 0 && p.lse_out) p.lse_out[W.bq * p.n_h + H] = Lse;
+        if (q4 == 0 && W.sp == 0 && p.lse_out) p.lse_out[W.bq * p.n_h + H] = Lse;
       } else if (p.n_split > 1) {
         cw = 1.f;
         const float2 ml = make_float2(l > 0.f ? mm : -INFINITY, l);
         if (q4 == 0) {
-          if (p.cluster)
-            ml_s[h0 + lane] = ml;  // merged with the other splits of the cluster below
-          else
-            p.part_ml[(W.bq * p.n_split + W.sp) * p.n_h + H] = ml;
+          p.part_ml[(W.bq * p.n_split + W.sp) * p.n_h + H] = ml;
         }
       } else {
         cw = l > 0.f ? 1.f / l : 0.f;
@@ -640,7 +672,75 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (MODE == 2) {
       if (ok && p.o_in != nullptr) ok = tc::mbar_wait(oin_full, 0, s_abort, 14);
     }
-    if (ok && !(MODE != 2 && p.cluster)) {
+    if (MODE == 2 && ok && p.n_split > 1) {
+      // split window merge: this CTA's chunks, merged with the staged o_in slice
+      // [64 heads][D] (query region), stored straight from registers (lanes along dims)
+      const int D = kC / p.n_split;
+      const float* oin = reinterpret_cast<const float*>(q_s);
+      const bool have_oin = p.o_in != nullptr;
+      const int64_t orow = (W.bq * p.n_h + W.hg * kHG + h0) * kC;
+#pragma unroll 1
+      for (int ch = ch0; ch < ch1; ++ch) {
+        float v[32], cw[32], oc[32];
+        if (ntiles > 0) {
+          tc::tmem_ld32(tmem + lane_base + kTmemO + (uint32_t)(ch * kHG + h0), v);
+        } else {
+#pragma unroll
+          for (int y = 0; y < 32; ++y) v[y] = 0.f;
+        }
+        const int dl = (ch - ch0) * 128 + e;  // dim within the slice
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+          const float4 a = *reinterpret_cast<const float4*>(wt_cw + 4 * x);
+          cw[4 * x] = a.x, cw[4 * x + 1] = a.y, cw[4 * x + 2] = a.z, cw[4 * x + 3] = a.w;
+          const float4 b = *reinterpret_cast<const float4*>(wt_cc + 4 * x);
+          oc[4 * x] = b.x, oc[4 * x + 1] = b.y, oc[4 * x + 2] = b.z, oc[4 * x + 3] = b.w;
+        }
+#pragma unroll
+        for (int y = 0; y < 32; ++y) oc[y] = (have_oin && oc[y] != 0.f) ? oc[y] * oin[(h0 + y) * D + dl] : 0.f;
+        if (ntiles > 0) tc::tmem_ld_wait();
+        const int64_t o0 = orow + ch * 128 + e;
+        if (p.out_bf16) {
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + o0;
+#pragma unroll
+          for (int y = 0; y < 32; ++y) out[(int64_t)y * kC] = __float2bfloat16_rn(fmaf(cw[y], v[y], oc[y]));
+        } else {
+          float* out = static_cast<float*>(p.out) + o0;
+#pragma unroll
+          for (int y = 0; y < 32; ++y) out[(int64_t)y * kC] = fmaf(cw[y], v[y], oc[y]);
+        }
+      }
+    } else if (MODE != 2 && ok && p.n_split > 1) {
+      // split partial (unnormalised O): chunk by chunk, this half's [32 heads][128] float32
+      // piece is staged in the free ring and bulk-stored at once into the unit's
+      // chunk-major partial [4 chunks][64 heads][128]
+      float* piece0 = reinterpret_cast<float*>(kv_s) + hh * (4 * 32 * 128);
+      float* dst0 = p.part_o + ((W.bq * p.n_split + W.sp) * p.n_hg + W.hg) * (int64_t)(kHG * kC);
+#pragma unroll 1
+      for (int ch = 0; ch < 4 && ok; ++ch) {
+        float v[32];
+        if (ntiles > 0) {
+          tc::tmem_ld32(tmem + lane_base + kTmemO + (uint32_t)(ch * kHG + h0), v);
+          tc::tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int y = 0; y < 32; ++y) v[y] = 0.f;
+        }
+        float* piece = piece0 + ch * (32 * 128);
+#pragma unroll
+        for (int y = 0; y < 32; ++y) piece[y * 128 + e] = v[y];
+        tc::fence_proxy_async_smem();
+        ok = hsync();
+        if (ok && q4 == 0 && lane == 0) {
+          tc::bulk_store(dst0 + (int64_t)(ch * kHG + h0) * 128, piece, 32 * 128 * 4);
+          tc::bulk_commit();
+        }
+      }
+      if (q4 == 0 && lane == 0) {
+        tc::bulk_wait_all();  // the partial is in global memory before this split counts itself done
+        tc::fence_proxy_async_global();
+      }
+    } else if (ok) {
       // O^T (TMEM) -> this half's 32 rows of [64 heads][512] in shared memory -> one bulk store.
       // Staging: float32 in the free K/V ring (in place over the staged o_in for a float32
       // window merge), bf16 window-merge output in the free query region.
@@ -695,8 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           dst = out_bf16 ? static_cast<void*>(static_cast<__nv_bfloat16*>(p.out) + (W.bq * p.n_h + W.hg * kHG + h0) * kC)
                          : static_cast<void*>(static_cast<float*>(p.out) + (W.bq * p.n_h + W.hg * kHG + h0) * kC);
         else
-          dst = p.n_split > 1 ? p.part_o + ((W.bq * p.n_split + W.sp) * p.n_h + W.hg * kHG + h0) * kC
-                              : p.o + (W.bq * p.n_h + W.hg * kHG + h0) * kC;
+          dst = p.o + (W.bq * p.n_h + W.hg * kHG + h0) * kC;
         const uint32_t bytes = 32 * kC * (out_bf16 ? 2 : 4);
         const uint8_t* src = out_bf16 ? reinterpret_cast<const uint8_t*>(stage16) : reinterpret_cast<const uint8_t*>(stage32);
         for (uint32_t off = 0; off < bytes; off += 16384)
@@ -705,75 +804,109 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::bulk_wait_read();
       }
     }
-  }
-  __syncwarp();  // every warp reaches the cluster and CTA barriers converged
-  if constexpr (MODE != 2) {
-    if (p.cluster) {
-      // Merge the splits of this (query, head group) inside the cluster.  Every thread of
-      // every CTA passes both barriers, whatever happened before (no hardware wait is left
-      // open).  Between them, rank r scatters its O (scaled by its merge weight) into the
-      // owners' K/V rings (free once every CTA's last products are done): rank j owns dims
-      // [j*D, j*D+D), D = 512/S, received as [S ranks][64 heads][D].
-      const uint32_t S = (uint32_t)p.n_split, rank = (uint32_t)W.sp;
-      const int D = kC / (int)S;
-      tc::cluster_sync();  // every CTA's (m, l) table is written, every ring is free
-      if (warp >= kSoftWarp0 && sm_ok) {
-        const int q4 = warp & 3, hh = (warp - kSoftWarp0) >> 2, e = q4 * 32 + lane, h0 = hh * 32;
-        const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-        float* wt_cw = wtab + (warp - kSoftWarp0) * 128 + 64;
-        {
-          // merge weight of head h0+lane for this rank: one pass of log-sum-exp over the ranks
-          const uint32_t ml_addr = tc::smem_u32(ml_s + h0 + lane);
-          float M = -INFINITY, L = 0.f;
-          for (uint32_t r = 0; r < S; ++r) {
-            const float2 v = tc::ld_cluster_f32x2(tc::map_to_rank(ml_addr, r));
-            if (v.x == -INFINITY) continue;
-            const float Mn = fmaxf(M, v.x);
-            L = L * exp2f(M - Mn) + v.y * exp2f(v.x - Mn);  // exp2f(-inf) = 0 on the first rank
-            M = Mn;
+    if (MODE != 2 && p.n_split > 1) {
+      // Join the splits of this (query, head group) through L2: once every split has
+      // counted itself done, split sp merges items [sp*N/S, (sp+1)*N/S) of the unit's
+      // N = 64 heads x 128 float4 quads from the S partials (all CTAs of a launch with
+      // splits are resident at once: at most one per SM).  Every wait is bounded.
+      const int S = p.n_split;
+      const int ts = (int)threadIdx.x - kSoftWarp0 * 32;
+      uint32_t jphase = 0;
+      auto all_sync = [&]() -> bool {
+        tc::mbar_arrive(sm_all);
+        const bool r = tc::mbar_wait(sm_all, jphase, s_abort, 17);
+        jphase ^= 1u;
+        return r;
+      };
+      ok = ok && all_sync();
+      if (ok && ts == 0) {
+        uint32_t* cnt = p.join_cnt + W.bq * p.n_hg + W.hg;
+        __threadfence();
+        atomicAdd(cnt, 1u);
+        const long long t0 = clock64();
+        while (tc::ld_acquire_gpu_u32(cnt) < (uint32_t)S) {
+          if (clock64() - t0 > tc::kWaitLimitCycles) {
+            *s_abort = 18;
+            break;
           }
-          const float2 self = ml_s[h0 + lane];
-          wt_cw[lane] = (L > 0.f && self.x != -INFINITY) ? exp2f(self.x - M) / L : 0.f;
-          if (rank == 0 && q4 == 0)
-            p.lse[W.bq * p.n_h + W.hg * kHG + h0 + lane] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
-          __syncwarp();
         }
-        const uint32_t recv0 = tc::smem_u32(kv_s);
-#pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-          float v[32], cw[32];
-          if (ntiles > 0) {
-            tc::tmem_ld32(tmem + lane_base + kTmemO + (uint32_t)(ch * kHG + h0), v);
-          } else {
-#pragma unroll
-            for (int y = 0; y < 32; ++y) v[y] = 0.f;
-          }
-#pragma unroll
-          for (int x = 0; x < 8; ++x) {
-            const float4 a = *reinterpret_cast<const float4*>(wt_cw + 4 * x);
-            cw[4 * x] = a.x, cw[4 * x + 1] = a.y, cw[4 * x + 2] = a.z, cw[4 * x + 3] = a.w;
-          }
-          if (ntiles > 0) tc::tmem_ld_wait();
-          const int d = ch * 128 + e;
-          const uint32_t j = (uint32_t)(d / D), dd = (uint32_t)(d - (int)j * D);
-          const uint32_t dst = tc::map_to_rank(recv0, j) + ((rank * 64 + (uint32_t)h0) * (uint32_t)D + dd) * 4;
-#pragma unroll
-          for (int y = 0; y < 32; ++y) tc::st_cluster_f32(dst + (uint32_t)(y * D * 4), cw[y] * v[y]);
-        }
+        __threadfence();
       }
-      tc::cluster_sync();  // every slice has arrived
-      if (warp >= kSoftWarp0 && sm_ok) {
-        const float* recv = reinterpret_cast<const float*>(kv_s);
-        float* obase = p.o + (W.bq * p.n_h + W.hg * kHG) * kC + rank * D;
-        for (int t = threadIdx.x - kSoftWarp0 * 32; t < 64 * D; t += kSoftThreads) {
-          const int h = t / D, dd = t - h * D;
-          float acc = 0.f;
-          for (uint32_t r = 0; r < S; ++r) acc += recv[(r * 64 + h) * D + dd];
-          obase[(int64_t)h * kC + dd] = acc;
+      ok = ok && all_sync() && *s_abort == 0;
+      if (ok) {
+        constexpr int kQuads = kC / 4;
+        const int n_items = kHG * kQuads;
+        const int i0 = (int)((int64_t)W.sp * n_items / S), i1 = (int)((int64_t)(W.sp + 1) * n_items / S);
+        const int h_lo = i0 / kQuads, nh = (i1 - 1) / kQuads - h_lo + 1;  // heads of this CTA's items
+        float2* t_ml = reinterpret_cast<float2*>(red);  // [nh][S] (m, l) of every split
+        float* t_w = red + 512;                          // [nh][S] merge weights (1/L included)
+        const float2* ml_b = p.part_ml + W.bq * S * p.n_h + W.hg * kHG;
+        for (int t = ts; t < nh * S; t += kSoftThreads) {
+          const int hl = t / S, s2 = t - hl * S;
+          t_ml[t] = __ldcg(&ml_b[(int64_t)s2 * p.n_h + h_lo + hl]);
+        }
+        ok = all_sync();
+        if (ok) {
+          for (int t = ts; t < nh * S; t += kSoftThreads) {
+            const int hl = t / S;
+            float M = -INFINITY;
+            for (int s2 = 0; s2 < S; ++s2) M = fmaxf(M, t_ml[hl * S + s2].x);
+            float L = 0.f;
+            if (M != -INFINITY)
+              for (int s2 = 0; s2 < S; ++s2) {
+                const float2 ml = t_ml[hl * S + s2];
+                if (ml.x != -INFINITY) L = fmaf(ml.y, exp2f(ml.x - M), L);
+              }
+            const float2 mine = t_ml[t];
+            t_w[t] = (L > 0.f && mine.x != -INFINITY) ? exp2f(mine.x - M) / L : 0.f;
+            const int h = h_lo + hl;
+            if (t - hl * S == 0 && h * kQuads >= i0)  // this CTA holds the head's first quad
+              p.lse[W.bq * p.n_h + W.hg * kHG + h] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
+          }
+          ok = all_sync();
+        }
+        if (ok) {
+          // every thread: up to 4 items (float4 quads) at once, all splits' loads in flight
+          const float* po_b = p.part_o + (W.bq * S * p.n_hg + W.hg) * (int64_t)(kHG * kC);
+          const int64_t split_stride = (int64_t)p.n_hg * kHG * kC;
+          float* o_b = p.o + (W.bq * p.n_h + W.hg * kHG) * kC;
+          for (int base = i0 + ts; base < i1; base += 4 * kSoftThreads) {
+            float4 acc[4];
+            int off[4], wi[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int it = base + k * kSoftThreads;
+              const int h = it / kQuads, d = (it - h * kQuads) * 4;
+              off[k] = ((d >> 7) * kHG + h) * 128 + (d & 127);  // chunk-major partial
+              wi[k] = (h - h_lo) * S;
+              acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll 4
+            for (int s2 = 0; s2 < S; ++s2) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                if (base + k * kSoftThreads < i1) {
+                  const float4 v = __ldcg(reinterpret_cast<const float4*>(po_b + s2 * split_stride + off[k]));
+                  const float w = t_w[wi[k] + s2];
+                  acc[k].x = fmaf(w, v.x, acc[k].x), acc[k].y = fmaf(w, v.y, acc[k].y);
+                  acc[k].z = fmaf(w, v.z, acc[k].z), acc[k].w = fmaf(w, v.w, acc[k].w);
+                }
+              }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int it = base + k * kSoftThreads;
+              if (it < i1) {
+                const int h = it / kQuads, d = (it - h * kQuads) * 4;
+                *reinterpret_cast<float4*>(o_b + (int64_t)h * kC + d) = acc[k];
+              }
+            }
+          }
         }
       }
     }
   }
+  __syncwarp();  // every warp reaches the CTA barrier converged
   tc::tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0 && *s_abort) flag_status(p.dev_status, HYB_DEV_TIMEOUT | ((*s_abort & 0xFF) << 8));
@@ -781,37 +914,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
-}
-
-// Merge the split partials of every (query, head): one CTA of 128 threads per
-// (query, head), four dims per thread.
-__global__ void __launch_bounds__(128) atc_combine_kernel(const float* __restrict__ part_o,
-                                                          const float2* __restrict__ part_ml, float* o, float* lse,
-                                                          int64_t n_h, int n_split) {
-  const int64_t bq = blockIdx.x / n_h, h = blockIdx.x % n_h;
-  const int d = threadIdx.x * 4;
-  float M = -INFINITY;
-  for (int sp = 0; sp < n_split; ++sp) M = fmaxf(M, part_ml[(bq * n_split + sp) * n_h + h].x);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float l = 0.f;
-  if (M != -INFINITY) {
-#pragma unroll 8
-    for (int sp = 0; sp < n_split; ++sp) {
-      const int64_t pi = (bq * n_split + sp) * n_h + h;
-      const float2 ml = part_ml[pi];
-      const float wgt = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-      l = fmaf(wgt, ml.y, l);
-      const float4 po = __ldg(reinterpret_cast<const float4*>(part_o + pi * kC + d));
-      acc.x = fmaf(wgt, po.x, acc.x);
-      acc.y = fmaf(wgt, po.y, acc.y);
-      acc.z = fmaf(wgt, po.z, acc.z);
-      acc.w = fmaf(wgt, po.w, acc.w);
-    }
-  }
-  const float inv = l > 0.f ? 1.f / l : 0.f;
-  acc.x *= inv, acc.y *= inv, acc.z *= inv, acc.w *= inv;
-  *reinterpret_cast<float4*>(o + (bq * n_h + h) * kC + d) = acc;
-  if (threadIdx.x == 0) lse[bq * n_h + h] = l > 0.f ? (M + __log2f(l)) * kLn2 : -INFINITY;
 }
 
 int64_t atc_list_len_max(const AttendJob& j) {
@@ -835,55 +937,30 @@ namespace {
 
 struct AtcPlan {
   int n_split;
-  bool cluster;
 };
 
-// How many clusters of S CTAs of the given mode can be resident at once (queried once per mode and size).
-int clusters_resident(int mode, int S) {
-  static int cache[3][17];  // 0 unknown, else 1 + count
-  if (S < 2 || S > 16) return 0;
-  int& c = cache[mode][S];
-  if (c == 0) {
-    const void* fn = mode == 0 ? (const void*)attend_tc_kernel<0> : (const void*)attend_tc_kernel<1>;
-    bool ok = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) == cudaSuccess;
-    if (ok && S > 8) ok = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
-    int n = 0;
-    if (ok) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3((unsigned)S), cfg.blockDim = dim3(kThreads), cfg.dynamicSmemBytes = kSmemBytes;
-      cudaLaunchAttribute attr;
-      attr.id = cudaLaunchAttributeClusterDimension;
-      attr.val.clusterDim.x = (unsigned)S, attr.val.clusterDim.y = 1, attr.val.clusterDim.z = 1;
-      cfg.attrs = &attr, cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) n = 0;
-    }
-    cudaGetLastError();  // a refused query leaves no sticky error
-    c = 1 + n;
-  }
-  return c - 1;
-}
-
-// Splits of each (query, head group) list.  Either every CTA writes a partial and a
-// combine kernel merges them, or the splits form one cluster (a power of two, so it
-// divides the 512 dims) and merge through DSMEM.  Rough cost model per list: waves of
-// ceil(tiles/S) tiles at ~4 us each, plus ~10 us for partials + combine or ~2 us for the
-// cluster merge; a cluster plan is only taken if all its clusters are resident at once.
+// Splits of each (query, head group) list: every split CTA writes its partial (O, m, l)
+// and the splits of a unit join through L2 inside the kernel.  A launch with splits
+// has at most one CTA per SM, so all its CTAs are resident at once; the split count
+// is the largest that fits, then evened out (the same tiles per CTA, fewer CTAs).
 AtcPlan atc_plan(const AttendJob& j) {
-  if (j.mode == 2) return {1, false};
+  if (j.mode == 2) {
+    // Window merge of one tile whose keys are its values: S CTAs per (query, head group)
+    // each compute the (cheap) softmax and write 512/S of the output dims, merged with
+    // their slice of the compressed branch's output; nothing is exchanged.
+    if (j.k != j.v || atc_list_len_max(j) > kTile) return {1};
+    const int64_t units = j.batch * j.n_q * (j.n_h / kHG);
+    for (int S = 4; S >= 2; S >>= 1)
+      if (units * S <= kNumSMs) return {S};
+    return {1};
+  }
   const int64_t T = (atc_list_len_max(j) + kTile - 1) / kTile;
   const int64_t units = j.batch * j.n_q * (j.n_h / kHG);
   int64_t s = kNumSMs / std::max<int64_t>(units, 1);
-  s = std::min<int64_t>(s, T);
-  if (s <= 1) return {1, false};
-  auto cost = [&](int64_t S, bool cluster) { return (double)((T + S - 1) / S) * 4.0 + (cluster ? 2.0 : 10.0); };
-  AtcPlan best{(int)std::min<int64_t>(s, 64), false};
-  double best_cost = cost(best.n_split, false);
-  for (int S = 2; S <= 16 && S <= T; S *= 2) {
-    if (units * S > kNumSMs || units > clusters_resident(j.mode, S)) continue;
-    const double c = cost(S, true);
-    if (c < best_cost) best_cost = c, best = {S, true};
-  }
-  return best;
+  s = std::min<int64_t>(std::min<int64_t>(s, T), kMaxSplits);
+  if (s <= 1) return {1};
+  const int64_t per = (T + s - 1) / s;  // tiles per split
+  return {(int)((T + per - 1) / per)};
 }
 
 }  // namespace
@@ -892,9 +969,10 @@ int attend_tc_splits(const AttendJob& j) { return atc_plan(j).n_split; }
 
 size_t attend_tc_workspace_bytes(const AttendJob& j) {
   const AtcPlan pl = atc_plan(j);
-  if (pl.n_split <= 1 || pl.cluster) return 0;
+  if (pl.n_split <= 1 || j.mode == 2) return 0;
   const size_t n = (size_t)(j.batch * j.n_q * pl.n_split * j.n_h);
-  return n * (size_t)kC * sizeof(float) + n * sizeof(float2) + 256;
+  const size_t units = (size_t)(j.batch * j.n_q * (j.n_h / kHG));
+  return n * (size_t)kC * sizeof(float) + n * sizeof(float2) + units * sizeof(uint32_t) + 256;
 }
 
 cudaError_t launch_attend_tc(const AttendJob& j, void* ws, cudaStream_t s) {
@@ -909,16 +987,16 @@ cudaError_t launch_attend_tc(const AttendJob& j, void* ws, cudaStream_t s) {
   p.m = j.m, p.q_pos0 = j.q_pos0, p.kv_pos0 = j.kv_pos0, p.n_win = j.n_win;
   const AtcPlan pl = atc_plan(j);
   p.n_split = pl.n_split;
-  p.cluster = pl.cluster ? 1 : 0;
   p.n_hg = (int)(j.n_h / kHG);
   p.alias = j.k == j.v;
   p.scale_log2 = j.scale * kLog2e;
   p.dev_status = j.dev_status;
   const int64_t rows = j.batch * j.n_q;
-  if (p.n_split > 1 && !p.cluster) {
+  if (p.n_split > 1 && j.mode != 2) {
     const size_t n = (size_t)(rows * p.n_split * j.n_h);
     p.part_o = static_cast<float*>(ws);
     p.part_ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + n * (size_t)kC * sizeof(float));
+    p.join_cnt = reinterpret_cast<uint32_t*>(p.part_ml + n);
   }
   const uint64_t kv_rows = (uint64_t)(j.batch * j.kv_stride);
   const uint32_t box_rows = kv_rows < (uint64_t)kTile ? (uint32_t)kv_rows : (uint32_t)kTile;
@@ -933,26 +1011,9 @@ cudaError_t launch_attend_tc(const AttendJob& j, void* ws, cudaStream_t s) {
   const int64_t grid = rows * p.n_split * p.n_hg;
   if (grid >= (int64_t(1) << 31)) return cudaErrorInvalidConfiguration;
   cudaError_t e;
-  if (p.cluster) {
-    const void* fn = j.mode == 0 ? (const void*)attend_tc_kernel<0> : (const void*)attend_tc_kernel<1>;
-    if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)) != cudaSuccess) return e;
-    if (p.n_split > 8 &&
-        (e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
-      return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid), cfg.blockDim = dim3(kThreads), cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = (unsigned)p.n_split, attr.val.clusterDim.y = 1, attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr, cfg.numAttrs = 1;
-    if (j.mode == 0)
-      e = cudaLaunchKernelEx(&cfg, attend_tc_kernel<0>, tm_q, tm_k, tm_v, p);
-    else
-      e = cudaLaunchKernelEx(&cfg, attend_tc_kernel<1>, tm_q, tm_k, tm_v, p);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
-  }
+  if (p.join_cnt != nullptr &&
+      (e = cudaMemsetAsync(p.join_cnt, 0, (size_t)(rows * p.n_hg) * sizeof(uint32_t), s)) != cudaSuccess)
+    return e;
   switch (j.mode) {
     case 0:
       e = cudaFuncSetAttribute(attend_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -968,12 +1029,7 @@ cudaError_t launch_attend_tc(const AttendJob& j, void* ws, cudaStream_t s) {
       break;
   }
   if (e != cudaSuccess) return e;
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (p.n_split > 1 && !p.cluster) {
-    atc_combine_kernel<<<(unsigned)(rows * j.n_h), 128, 0, s>>>(p.part_o, p.part_ml, j.o, j.lse, j.n_h, p.n_split);
-    e = cudaGetLastError();
-  }
-  return e;
+  return cudaGetLastError();
 }
 
 }  // namespace hyb

@@ -183,9 +183,17 @@ hyb_status csa_index_topk(const hyb_index_args* a, void* workspace, size_t ws_by
   uint32_t* ghist = hyb::topk_prepare_hist(a, nv, topk_ws, s, &e);
   if (e != cudaSuccess) return cuda_status(e, "csa_index_topk: histogram reset");
   bool hist_done = false;
+  if (a->ev_scores_begin &&
+      (e = cudaEventRecordWithFlags(static_cast<cudaEvent_t>(a->ev_scores_begin), s, cudaEventRecordExternal)) !=
+          cudaSuccess)
+    return cuda_status(e, "csa_index_topk: ev_scores_begin");
   e = hyb::index_tc_shape_supported(a) ? hyb::launch_index_scores_tc(a, scores, nv, nv, ghist, &hist_done, s)
                                        : hyb::launch_index_scores_cc(a, scores, nv, nv, s);
   if (e != cudaSuccess) return cuda_status(e, "csa_index_topk: index-score launch");
+  if (a->ev_scores_end &&
+      (e = cudaEventRecordWithFlags(static_cast<cudaEvent_t>(a->ev_scores_end), s, cudaEventRecordExternal)) !=
+          cudaSuccess)
+    return cuda_status(e, "csa_index_topk: ev_scores_end");
   return cuda_status(hyb::launch_topk(a, scores, nv, topk_ws, hist_done, s), "csa_index_topk: top-k launch");
 }
 

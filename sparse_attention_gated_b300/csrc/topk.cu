@@ -33,6 +33,24 @@
 //             the last kept candidate; candidates above it are kept, the few
 //             equal to it are selected exactly; the kept candidates are then
 //             merged with the entries above b* (both lists are ascending).
+//   grid (decode: at most one row per SM, up to kGridChunkCap entries per CTA):
+//             one kernel whose CTAs are all resident at once (at most one CTA
+//             per SM, and one fits).  CTA (part, row) stages its chunk of the
+//             row's keys in shared memory once; the CTAs agree on the threshold
+//             through global histograms, with a grid-wide barrier between phases:
+//       1  b1 = the 12-bit bin holding the k-th largest key (row histogram);
+//          the chunk's keys in b1 are histogrammed on their next 12 bits.
+//       2  b2 = the second-level bin holding the last kept key.  Keys whose top
+//          24 bits are above (b1, b2) are kept; the few whose top 24 bits equal
+//          it (sub-candidates) go to the row's list; every CTA publishes how
+//          many of its keys are surely kept.
+//       3  every CTA ranks the row's list by (key desc, entry asc) and keeps the
+//          r2 best, then writes its kept entries in ascending order at the
+//          offset given by the counts of the CTAs before it.
+//          When a row's list overflows (many keys share their top 24 bits), all
+//          CTAs take two more barriers: a histogram of the last 8 bits gives the
+//          exact k-th key T, and the keys equal to T are kept lowest entry first
+//          through a prefix of the tie counts over the CTAs.
 #include "kernels.cuh"
 
 namespace hyb {
@@ -47,6 +65,10 @@ constexpr int kHistBits = kTopkHistBits;
 constexpr int kHistBins = kTopkHistBins;
 constexpr int kMaxChunks = 64;
 constexpr int kPer = 8;  // keys a thread loads before using them (histogram and filter passes)
+constexpr int64_t kGridChunkCap = 32768;  // grid plan: keys per CTA, staged in shared memory
+constexpr int kSubListCap = 1024;         // grid plan: sub-candidates per row ranked directly
+constexpr int kGridSlot = 4;              // grid plan: published counts per CTA (sure, > T, == T, unused)
+constexpr long long kGridWaitCycles = 1LL << 31;  // bound of a grid-barrier wait (about 1 s)
 
 struct TopkParams {
   const float* scores;
@@ -64,6 +86,14 @@ struct TopkParams {
   int32_t* cand_idx;
   int32_t* counts;      // [rows][n_chunks][2]: (#above, #candidates) of each chunk
   uint32_t* done;       // [rows]: filter CTAs finished (the last one selects)
+  // grid plan (ghist, ghist2 and chunk/n_chunks as above)
+  uint32_t* hist3;      // [rows][256]: last 8 bits of the sub-candidates (overflow only)
+  uint32_t* nsub;       // [rows]: sub-candidates appended to the row's list
+  uint32_t* gsync;      // [0]: grid-barrier arrivals, [1]: some row's list overflowed
+  int32_t* slots;       // [rows][n_chunks][kGridSlot]: published per-CTA counts
+  uint2* sub;           // [rows][kSubListCap]: (key, entry) of the sub-candidates
+  int hist_done;        // the row histograms were filled by the indexer
+  int32_t* dev_status;
 };
 
 __device__ __forceinline__ int64_t row_visible(const TopkParams& p, int64_t row) {
@@ -596,23 +626,334 @@ __device__ void filter_chunk(const TopkParams& p, int64_t row, int64_t vis, Bloc
     if (hist2[i]) atomicAdd(gh2 + i, hist2[i]);
 }
 
+
+// ------------------------------------------------------------------ grid plan
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* ptr) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
+// Barrier over all CTAs of the grid.  Arrivals count up in *count (zeroed before
+// the launch), so the i-th barrier waits for i * gridDim.x * gridDim.y of them.
+// Bounded: on expiry HYB_DEV_TIMEOUT (with the site) is raised and false returned.
+__device__ bool grid_barrier(uint32_t* count, uint32_t target, int32_t* dev_status, int site) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(count, 1u);
+    int ok = 1;
+    const long long t0 = clock64();
+    while (ld_acquire_u32(count) < target) {
+      if (clock64() - t0 > kGridWaitCycles) {
+        ok = 0;
+        break;
+      }
+    }
+    if (!ok) flag_status(dev_status, HYB_DEV_TIMEOUT | (site << 8));
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+// Sum over the CTA of one value per thread (every thread gets the total).
+__device__ __forceinline__ uint32_t block_sum(uint32_t v, BlockShared& S) {
+  uint32_t before, z0, tot, z1;
+  block_scan_counts(v, 0u, S, before, z0, tot, z1);
+  return tot;
+}
+
+__global__ void __launch_bounds__(kTopkThreads, 1) topk_grid_kernel(TopkParams p) {
+  extern __shared__ uint32_t dyn[];
+  uint32_t* keys = dyn;                                           // [chunk] keys of this CTA's entries
+  uint32_t* hist = keys + p.chunk;                                // [kHistBins]
+  uint2* list = reinterpret_cast<uint2*>(hist + kHistBins);       // [kSubListCap] the row's sub-candidates
+  uint32_t* selb = reinterpret_cast<uint32_t*>(list + kSubListCap);  // [chunk / 32] selected sub-candidates
+  __shared__ BlockShared S;
+  __shared__ int64_t s_before;
+  const int tid = threadIdx.x;
+  const int part = blockIdx.x, parts = gridDim.x;
+  const int64_t row = blockIdx.y;
+  const uint32_t nblk = gridDim.x * gridDim.y;
+  uint32_t nbar = 0;
+  const int64_t vis = row_visible(p, row);
+  const int64_t s0 = (int64_t)part * p.chunk;
+  const int64_t len = vis - s0 < 0 ? 0 : (vis - s0 < p.chunk ? vis - s0 : p.chunk);
+  const bool active = vis > p.k;  // rows with at most k visible entries keep them all
+  const float* sc = p.scores + row * p.score_stride;
+  int32_t* out = p.idx + row * p.k;
+  float* out_sc = p.out_scores ? p.out_scores + row * p.k : nullptr;
+  int32_t* myslot = p.slots + ((int64_t)row * parts + part) * kGridSlot;
+  // each thread owns a contiguous run of the chunk, so block scans keep entry order
+  const int per = (int)(p.chunk / kTopkThreads);
+  const int e0 = tid * per;
+  const int e1 = (int64_t)(e0 + per) < len ? e0 + per : (int)(len > e0 ? len : e0);
+
+  if (active) {
+    for (int64_t base = 0; base < len; base += (int64_t)kPer * kTopkThreads) {
+      float v[kPer];
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {  // all loads first: one round trip per kPer elements
+        const int64_t e = base + u * kTopkThreads + tid;
+        v[u] = e < len ? __ldcg(sc + s0 + e) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int64_t e = base + u * kTopkThreads + tid;
+        if (e < len) keys[e] = float_order_key(v[u]);
+      }
+    }
+  }
+  for (int i = tid; i < kHistBins; i += kTopkThreads) hist[i] = 0;
+  __syncthreads();
+  if (!p.hist_done) {
+    // first-level histogram of the chunk, added into the row's
+    if (active)
+      for (int u = 0; u < per; ++u) {
+        const int e = e0 + u;
+        hist_add(hist, e < e1, e < e1 ? keys[e] >> (32 - kHistBits) : 0u);
+      }
+    __syncthreads();
+    for (int i = tid; i < kHistBins; i += kTopkThreads)
+      if (hist[i]) atomicAdd(p.ghist + row * kHistBins + i, hist[i]), hist[i] = 0;
+    if (!grid_barrier(p.gsync, ++nbar * nblk, p.dev_status, 40)) return;
+  }
+
+  // phase 1: first-level threshold bin; second-level histogram of the chunk's keys in it
+  uint32_t b1 = 0, above1 = 0;
+  if (active) threshold_bin(p.ghist + row * kHistBins, (uint32_t)p.k, S, b1, above1);
+  const uint32_t r = (uint32_t)p.k - above1;  // keys of bin b1 to keep (>= 1)
+  if (active)
+    for (int u = 0; u < per; ++u) {
+      const int e = e0 + u;
+      const uint32_t key = e < e1 ? keys[e] : 0u;
+      hist_add(hist, e < e1 && (key >> (32 - kHistBits)) == b1, (key >> (32 - 2 * kHistBits)) & (kHistBins - 1));
+    }
+  __syncthreads();
+  for (int i = tid; i < kHistBins; i += kTopkThreads)
+    if (hist[i]) atomicAdd(p.ghist2 + row * kHistBins + i, hist[i]);
+  if (!grid_barrier(p.gsync, ++nbar * nblk, p.dev_status, 41)) return;
+
+  // phase 2: second-level bin; sure keeps counted, sub-candidates listed
+  uint32_t b2 = 0, above2 = 0;
+  if (active) threshold_bin(p.ghist2 + row * kHistBins, r, S, b2, above2);
+  const uint32_t r2 = r - above2;  // sub-candidates to keep (>= 1)
+  const uint32_t pre24 = (b1 << kHistBits) | b2;
+  uint32_t sure = 0;
+  if (active)
+    for (int e = e0; e < e1; ++e) {
+      const uint32_t key = keys[e], t24 = key >> 8;
+      sure += t24 > pre24;
+      if (t24 == pre24) {
+        const uint32_t slot = atomicAdd(p.nsub + row, 1u);
+        if (slot < (uint32_t)kSubListCap)
+          p.sub[row * kSubListCap + slot] = make_uint2(key, (uint32_t)(s0 + e));
+        else
+          atomicOr(p.gsync + 1, 1u);
+      }
+    }
+  sure = block_sum(sure, S);
+  if (active && tid == 0) myslot[0] = (int32_t)sure;
+  if (!grid_barrier(p.gsync, ++nbar * nblk, p.dev_status, 42)) return;
+
+  // phase 3: select among the sub-candidates and write this chunk's kept entries
+  const uint32_t n_sub = active ? __ldcg(p.nsub + row) : 0u;
+  const bool fast = active && n_sub <= (uint32_t)kSubListCap;
+  const bool any_overflow = __ldcg(p.gsync + 1) != 0u;  // the same for every CTA
+  if (fast) {
+    for (int i = tid; i < (int)(p.chunk / 32); i += kTopkThreads) selb[i] = 0u;
+    if (tid < (int)n_sub) list[tid] = __ldcg(p.sub + row * kSubListCap + tid);
+    if (tid < 32) {
+      int64_t acc = 0;
+      for (int i = tid; i < part; i += 32) acc += __ldcg(p.slots + ((int64_t)row * parts + i) * kGridSlot);
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (tid == 0) s_before = acc;
+    }
+    __syncthreads();
+    // rank each sub-candidate by (key desc, entry asc): the r2 best are kept
+    bool sel = false;
+    uint32_t sx = 0;
+    if (tid < (int)n_sub) {
+      const uint2 me = list[tid];
+      sx = me.y;
+      uint32_t rank = 0;
+      for (uint32_t y = 0; y < n_sub; ++y) {
+        const uint2 o = list[y];
+        rank += o.x > me.x || (o.x == me.x && o.y < me.y);
+      }
+      sel = rank < r2;
+      if (sel && sx >= (uint32_t)s0 && sx < (uint32_t)(s0 + len)) {
+        const uint32_t e = sx - (uint32_t)s0;
+        atomicOr(&selb[e >> 5], 1u << (e & 31));
+      }
+    }
+    const int64_t sel_before = __syncthreads_count(sel && sx < (uint32_t)s0);
+    const int64_t before = s_before + sel_before;
+    uint32_t mine = 0;
+    for (int e = e0; e < e1; ++e) {
+      const uint32_t t24 = keys[e] >> 8;
+      mine += t24 > pre24 || (t24 == pre24 && ((selb[e >> 5] >> (e & 31)) & 1u));
+    }
+    uint32_t kb, z0, kt, z1;
+    block_scan_counts(mine, 0u, S, kb, z0, kt, z1);
+    int64_t slot = before + kb;
+    for (int e = e0; e < e1; ++e) {
+      const uint32_t t24 = keys[e] >> 8;
+      if (t24 > pre24 || (t24 == pre24 && ((selb[e >> 5] >> (e & 31)) & 1u))) {
+        const int64_t s = s0 + e;
+        out[slot] = (int32_t)s;
+        if (out_sc) out_sc[slot] = __ldcg(sc + s);
+        ++slot;
+      }
+    }
+  }
+  if (any_overflow) {
+    // exact k-th key from the last 8 bits; ties kept lowest entry first over the CTAs
+    const bool slow = active && !fast;
+    for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
+    __syncthreads();
+    if (slow)
+      for (int u = 0; u < per; ++u) {
+        const int e = e0 + u;
+        const uint32_t key = e < e1 ? keys[e] : 0u;
+        hist_add(hist, e < e1 && (key >> 8) == pre24, key & 255u);
+      }
+    __syncthreads();
+    if (slow && tid < 256 && hist[tid]) atomicAdd(p.hist3 + row * 256 + tid, hist[tid]);
+    if (!grid_barrier(p.gsync, ++nbar * nblk, p.dev_status, 43)) return;
+    uint32_t T = 0, r3 = 0;
+    if (slow) {
+      if (tid < 32) {
+        // lane l covers digits 255-8l .. 248-8l
+        const int hi = 255 - 8 * tid;
+        uint32_t c[8], lsum = 0;
+#pragma unroll
+        for (int d = 0; d < 8; ++d) c[d] = __ldcg(p.hist3 + row * 256 + hi - d), lsum += c[d];
+        uint32_t incl = lsum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+          if (tid >= o) incl += u;
+        }
+        const uint32_t excl = incl - lsum;
+        if (excl < r2 && r2 <= incl) {
+          uint32_t cum = excl;
+          for (int d = 0; d < 8; ++d) {
+            if (cum + c[d] >= r2) {
+              S.prefix = (uint32_t)(hi - d);
+              S.desired = r2 - cum;
+              break;
+            }
+            cum += c[d];
+          }
+        }
+      }
+      __syncthreads();
+      T = (pre24 << 8) | S.prefix;
+      r3 = S.desired;  // keys equal to T to keep (>= 1)
+    }
+    uint32_t gt = 0, eq = 0;
+    if (slow)
+      for (int e = e0; e < e1; ++e) gt += keys[e] > T, eq += keys[e] == T;
+    uint32_t gb, eb, gtot, etot;
+    block_scan_counts(gt, eq, S, gb, eb, gtot, etot);
+    if (slow && tid == 0) myslot[1] = (int32_t)gtot, myslot[2] = (int32_t)etot;
+    if (!grid_barrier(p.gsync, ++nbar * nblk, p.dev_status, 44)) return;
+    if (slow) {
+      if (tid < 32) {
+        int64_t g_acc = 0, e_acc = 0;
+        for (int i = tid; i < part; i += 32) {
+          const int32_t* o = p.slots + ((int64_t)row * parts + i) * kGridSlot;
+          g_acc += __ldcg(o + 1), e_acc += __ldcg(o + 2);
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+          g_acc += __shfl_xor_sync(0xffffffffu, g_acc, o);
+          e_acc += __shfl_xor_sync(0xffffffffu, e_acc, o);
+        }
+        if (tid == 0) S.total = (uint32_t)e_acc, s_before = g_acc;
+      }
+      __syncthreads();
+      const int64_t eq_before = S.total;
+      const int64_t ties = r3 > eq_before ? std::min<int64_t>(r3 - eq_before, etot) : 0;  // ours to keep
+      const int64_t base = s_before + std::min<int64_t>(r3, eq_before);
+      int64_t g = gb, q = eb;
+      for (int e = e0; e < e1; ++e) {
+        const uint32_t key = keys[e];
+        int64_t slot = -1;
+        if (key > T) slot = g + std::min<int64_t>(q, ties), ++g;
+        else if (key == T) slot = q < ties ? g + q : -1, ++q;
+        if (slot >= 0) {
+          const int64_t s = s0 + e;
+          out[base + slot] = (int32_t)s;
+          if (out_sc) out_sc[base + slot] = __ldcg(sc + s);
+        }
+      }
+    }
+  }
+  if (!active) {
+    for (int64_t i = (int64_t)part * kTopkThreads + tid; i < p.k; i += (int64_t)parts * kTopkThreads) {
+      out[i] = i < vis ? (int32_t)i : -1;
+      if (out_sc) out_sc[i] = i < vis ? __ldcg(sc + i) : -INFINITY;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ host
 
 struct TopkPlan {
-  bool three;
+  int kind;  // 0 = one stage, 1 = three kernels, 2 = grid
   int64_t chunk;
   int n_chunks;
 };
 
+static size_t grid_smem_bytes(int64_t chunk) {
+  return (size_t)chunk * 4 + kHistBins * 4 + kSubListCap * 8 + (size_t)chunk / 8;
+}
+
+// One CTA of the grid plan fits an SM of the current device (cached per device).
+static bool grid_plan_fits(int64_t chunk) {
+  static int ok_dev[64] = {};  // 0 unknown, 1 fits, 2 does not
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  if (ok_dev[dev] == 0) {
+    int n = 0, sms = 0;
+    const bool fits =
+        cudaFuncSetAttribute(topk_grid_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)grid_smem_bytes(kGridChunkCap)) == cudaSuccess &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, topk_grid_kernel, kTopkThreads,
+                                                      grid_smem_bytes(kGridChunkCap)) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n >= 1 && sms >= kNumSMs;
+    ok_dev[dev] = fits ? 1 : 2;
+  }
+  return chunk <= kGridChunkCap && ok_dev[dev] == 1;
+}
+
 static TopkPlan plan_topk(const hyb_index_args* a, int64_t n_vis_max) {
-  TopkPlan pl{false, 0, 0};
+  TopkPlan pl{0, 0, 0};
   if (n_vis_max <= kStageCap) return pl;
   const int64_t rows = a->batch * a->n_q;
+  if (rows <= kNumSMs) {
+    // grid plan: up to one CTA per SM, the row's entries split evenly
+    const int64_t P = kNumSMs / rows;
+    int64_t chunk = (n_vis_max + P - 1) / P;
+    chunk = (chunk + kTopkThreads - 1) / kTopkThreads * kTopkThreads;
+    if (chunk <= kGridChunkCap && grid_plan_fits(chunk)) {
+      pl.kind = 2;
+      pl.chunk = chunk;
+      pl.n_chunks = (int)((n_vis_max + chunk - 1) / chunk);
+      return pl;
+    }
+  }
   int64_t P = (2 * kNumSMs + rows - 1) / rows;
   P = std::max<int64_t>(1, std::min<int64_t>(P, kMaxChunks));
   int64_t chunk = (n_vis_max + P - 1) / P;
   chunk = (chunk + 1023) / 1024 * 1024;
-  pl.three = true;
+  pl.kind = 1;
   pl.chunk = chunk;
   pl.n_chunks = (int)((n_vis_max + chunk - 1) / chunk);
   return pl;
@@ -620,10 +961,16 @@ static TopkPlan plan_topk(const hyb_index_args* a, int64_t n_vis_max) {
 
 static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
+// grid plan: the zeroed counters first (histograms, list sizes, barrier), then the rest
+static size_t grid_zeroed_bytes(size_t rows) { return rows * (2 * kHistBins + 256 + 1) * 4 + 2 * 4; }
+
 size_t topk_workspace_bytes(const hyb_index_args* a, int64_t n_vis_max) {
   const TopkPlan pl = plan_topk(a, n_vis_max);
-  if (!pl.three) return 0;
   const size_t rows = (size_t)(a->batch * a->n_q);
+  if (pl.kind == 2)
+    return align256(grid_zeroed_bytes(rows)) + align256(rows * pl.n_chunks * kGridSlot * 4) +
+           align256(rows * kSubListCap * 8);
+  if (pl.kind != 1) return 0;
   const size_t region = rows * (size_t)pl.n_chunks * (size_t)pl.chunk;
   return align256(rows * kHistBins * 8 + rows * 4) + 3 * align256(region * 4) + align256(rows * pl.n_chunks * 8);
 }
@@ -631,10 +978,20 @@ size_t topk_workspace_bytes(const hyb_index_args* a, int64_t n_vis_max) {
 bool topk_shape_supported(const hyb_index_args* a, int64_t) { return a->k >= 1 && a->k <= 2048; }
 
 static void topk_pointers(TopkParams& p, const TopkPlan& pl, int64_t rows, void* ws) {
-  const size_t region = (size_t)rows * pl.n_chunks * pl.chunk;
   char* w = static_cast<char*>(ws);
   p.ghist = reinterpret_cast<uint32_t*>(w);
   p.ghist2 = p.ghist + rows * kHistBins;
+  if (pl.kind == 2) {
+    p.hist3 = p.ghist2 + rows * kHistBins;
+    p.nsub = p.hist3 + rows * 256;
+    p.gsync = p.nsub + rows;
+    w += align256(grid_zeroed_bytes((size_t)rows));
+    p.slots = reinterpret_cast<int32_t*>(w);
+    w += align256((size_t)rows * pl.n_chunks * kGridSlot * 4);
+    p.sub = reinterpret_cast<uint2*>(w);
+    return;
+  }
+  const size_t region = (size_t)rows * pl.n_chunks * pl.chunk;
   p.done = p.ghist2 + rows * kHistBins;
   w += align256((size_t)rows * kHistBins * 8 + (size_t)rows * 4);
   p.def_idx = reinterpret_cast<int32_t*>(w);
@@ -650,10 +1007,11 @@ uint32_t* topk_prepare_hist(const hyb_index_args* a, int64_t n_vis_max, void* ws
   *err = cudaSuccess;
   const int64_t rows = a->batch * a->n_q;
   const TopkPlan pl = plan_topk(a, n_vis_max);
-  if (rows == 0 || !pl.three) return nullptr;
+  if (rows == 0 || pl.kind == 0) return nullptr;
   TopkParams p{};
   topk_pointers(p, pl, rows, ws);
-  *err = cudaMemsetAsync(p.ghist, 0, (size_t)rows * (kHistBins * 8 + 4), s);  // histograms and counters
+  const size_t bytes = pl.kind == 2 ? grid_zeroed_bytes((size_t)rows) : (size_t)rows * (kHistBins * 8 + 4);
+  *err = cudaMemsetAsync(p.ghist, 0, bytes, s);  // histograms and counters
   return p.ghist;
 }
 
@@ -662,12 +1020,13 @@ cudaError_t launch_topk(const hyb_index_args* a, const float* scores, int64_t sc
   TopkParams p{};
   p.scores = scores, p.score_stride = score_stride, p.idx = a->idx, p.out_scores = a->scores;
   p.n_q = a->n_q, p.n_entries = a->n_entries, p.m = a->m, p.k = a->k, p.q_pos0 = a->q_pos0;
+  p.dev_status = a->dev_status;
   const int64_t rows = a->batch * a->n_q;
   if (rows == 0) return cudaSuccess;
   const int64_t n_vis_max = std::min<int64_t>(visible_entries(a->q_pos0 + a->n_q - 1, a->m), a->n_entries);
   const TopkPlan pl = plan_topk(a, n_vis_max);
   cudaError_t e;
-  if (!pl.three) {
+  if (pl.kind == 0) {
     const size_t smem = sizeof(uint32_t) * (size_t)kStageCap;
     e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -675,8 +1034,21 @@ cudaError_t launch_topk(const hyb_index_args* a, const float* scores, int64_t sc
     return cudaGetLastError();
   }
   p.chunk = pl.chunk, p.n_chunks = pl.n_chunks;
+  p.hist_done = hist_done ? 1 : 0;
   topk_pointers(p, pl, rows, ws);
   const dim3 grid((unsigned)pl.n_chunks, (unsigned)rows);
+  if (pl.kind == 2) {
+    const size_t smem = grid_smem_bytes(pl.chunk);
+    e = cudaFuncSetAttribute(topk_grid_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    // The kernel has grid-wide barriers, so every CTA must become resident: at most one
+    // CTA per SM is launched and one CTA fits an SM (checked by the plan), so CTAs that
+    // find their SM busy with other work start as that work drains.  (A cooperative launch
+    // would state the same guarantee, but inside a CUDA graph next to copies it measured
+    // slower.)  A permanent shortage of SMs ends as HYB_DEV_TIMEOUT from the bounded barrier.
+    topk_grid_kernel<<<grid, kTopkThreads, smem, s>>>(p);
+    return cudaGetLastError();
+  }
   if (!hist_done) {  // the histograms were zeroed by topk_prepare_hist
     topk_hist_kernel<<<grid, kTopkThreads, 0, s>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -107,7 +107,7 @@ def hyb_compress(ca, za, bias, m: int, *, cb=None, zb=None, overlap: bool = Fals
 
 
 def index_args(qI, w, kI, m, k, q_pos0, qI_scale=None, kI_scale=None, idx=None, scores=None, n_entries=None,
-               dev_status=None):
+               dev_status=None, scores_events=None):
     B, n_q, n_ih, c_I = qI.shape
     a = _abi.IndexArgs()
     a.qI, a.qI_scale, a.w, a.kI, a.kI_scale = _ptr(qI), _ptr(qI_scale), _ptr(w), _ptr(kI), _ptr(kI_scale)
@@ -117,6 +117,8 @@ def index_args(qI, w, kI, m, k, q_pos0, qI_scale=None, kI_scale=None, idx=None, 
     a.kv_stride = kI.shape[1]
     a.dtype = _dtype(qI)
     a.dev_status = _ptr(dev_status)
+    if scores_events is not None:  # (begin, end) torch.cuda.Event: recorded around the scoring kernel
+        a.ev_scores_begin, a.ev_scores_end = (ctypes.c_void_p(int(e.cuda_event)) for e in scores_events)
     return a
 
 
@@ -125,14 +127,16 @@ def csa_index_topk_workspace_size(a) -> int:
 
 
 def csa_index_topk(qI, w, kI, *, m: int, k: int, q_pos0: int, qI_scale=None, kI_scale=None, n_entries=None,
-                   idx=None, scores=None, want_scores: bool = False, workspace=None, dev_status=None, stream=None):
-    """Lightning-indexer scores + top-k.  Returns idx (and the selected scores when asked)."""
+                   idx=None, scores=None, want_scores: bool = False, workspace=None, dev_status=None, stream=None,
+                   scores_events=None):
+    """Lightning-indexer scores + top-k.  Returns idx (and the selected scores when asked).
+    scores_events: optional (begin, end) torch.cuda.Event, recorded around the scoring kernel."""
     B, n_q = qI.shape[:2]
     if idx is None:
         idx = torch.empty((B, n_q, k), dtype=torch.int32, device=qI.device)
     if scores is None and want_scores:
         scores = torch.empty((B, n_q, k), dtype=torch.float32, device=qI.device)
-    a = index_args(qI, w, kI, m, k, q_pos0, qI_scale, kI_scale, idx, scores, n_entries, dev_status)
+    a = index_args(qI, w, kI, m, k, q_pos0, qI_scale, kI_scale, idx, scores, n_entries, dev_status, scores_events)
     ws, nbytes = _workspace(csa_index_topk_workspace_size(a), workspace, qI.device)
     _abi.check(_abi.load().csa_index_topk(ctypes.byref(a), ws, nbytes, _stream(stream)), "csa_index_topk")
     return (idx, scores) if want_scores else idx

@@ -143,3 +143,25 @@ class HybridStep:
 
     def output_keys(self):
         return [k for k in ("out", "out_h") if k in self.buf]
+
+    def pack_step_io(self):
+        """Re-home the per-step inputs and the outputs into one contiguous device
+        buffer each (256-byte aligned views, current values kept), so that a step's
+        host<->device traffic is one copy each way.  Returns the two uint8 buffers
+        (inputs, outputs); the stages keep reading and writing the same tensors."""
+
+        def pack(names, src):
+            place, total = [], 0
+            for k in names:
+                nbytes = src[k].numel() * src[k].element_size()
+                place.append((k, total, nbytes))
+                total = (total + nbytes + 255) // 256 * 256
+            flat = torch.empty(max(total, 1), dtype=torch.uint8, device=self.device)
+            for k, off, nbytes in place:
+                t = src[k]
+                view = flat[off:off + nbytes].view(t.dtype).view(t.shape)
+                view.copy_(t)
+                src[k] = view
+            return flat
+
+        return pack(self.step_input_keys(), self.x), pack(self.output_keys(), self.buf)

@@ -1,0 +1,40 @@
+"""Run a workload's forward step a few times on one GPU, for a profiler.
+
+    python -m sparse_attention_gated_b300.profile_cases [--workload NAME] [--steps N]
+
+Unlike the benchmark, this keeps one copy of the inputs (about 1.3 GB for the
+1M-context hybrid decode) and launches each stage's kernels once per step with
+no graph, events or clock sampling, so that a profiler given a kernel filter
+and a launch count (e.g. ``-k regex:index_tc -s 2 -c 1``) captures one launch
+of that kernel on inputs larger than the L2 cache.
+"""
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+from . import workloads
+from .pipeline import HybridStep
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="pro_1m_hybrid_decode", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--steps", type=int, default=3)
+    args = ap.parse_args()
+    if not torch.cuda.is_available():
+        raise SystemExit("needs a CUDA device")
+    w = workloads.WORKLOADS[args.workload]
+    st = HybridStep(w, workloads.make_inputs(w, device="cuda"))
+    for _ in range(args.steps):
+        st.run()
+    torch.cuda.synchronize()
+    status = int(st.dev_status.item())
+    if status != 0:
+        raise SystemExit(f"device status {status:#x}")
+    print(f"{args.workload}: {args.steps} steps done")
+
+
+if __name__ == "__main__":
+    main()

@@ -138,3 +138,30 @@ def test_noalloc_indexer_rejects_sizes_beyond_its_scratch(lib):
     assert need > _abi.HYB_NOALLOC_SCRATCH_BYTES
     assert lib.csa_index_topk_noalloc(ctypes.byref(a), None) == 3  # HYB_ERR_WORKSPACE
     assert b"scratch" in lib.hyb_last_error()
+
+
+def test_packed_step_io_keeps_values_and_aliases_one_buffer():
+    """HybridStep.pack_step_io: every per-step input (and output) becomes a view of one
+    contiguous buffer at a 256-byte aligned offset, with its values unchanged."""
+    from sparse_attention_gated_b300 import pipeline, workloads
+
+    import torch
+
+    w = workloads.scaled(workloads.WORKLOADS["tiny_f32"], n_ctx=64)
+    # the buffers only (constructing a step sizes workspaces through the CUDA library)
+    st = pipeline.HybridStep.__new__(pipeline.HybridStep)
+    st.w, st.x, st.device = w, workloads.make_inputs(w, device="cpu"), torch.device("cpu")
+    st.buf = {"out": torch.randn(1, 64, 4, 64), "out_h": torch.randn(1, 64, 4, 64)}
+    before = {k: st.x[k].clone() for k in st.step_input_keys()}
+    outs_before = {k: st.buf[k].clone() for k in st.output_keys()}
+    dev_in, dev_out = st.pack_step_io()
+    base = dev_in.data_ptr()
+    for k, v in before.items():
+        t = st.x[k]
+        assert torch.equal(t, v), k
+        off = t.data_ptr() - base
+        assert 0 <= off and off + t.numel() * t.element_size() <= dev_in.numel() and off % 256 == 0, k
+    for k in st.output_keys():
+        off = st.buf[k].data_ptr() - dev_out.data_ptr()
+        assert 0 <= off < dev_out.numel() and off % 256 == 0, k
+        assert torch.equal(st.buf[k], outs_before[k]), k

@@ -145,6 +145,8 @@ def test_hca_attend_aliased_entries(B, n_q, n_h, N, m, q_pos0):
     (4, 1, 128, 128, 2 ** 20 - 128, 128, 2 ** 20 - 1, torch.bfloat16),  # decode window
     (1, 200, 128, 128, 0, 200, 0, torch.bfloat16),                      # prefill: windows cut by the start
     (2, 3, 64, 100, 40, 300, 250, torch.float32),                       # window not a multiple of 128
+    (2, 1, 128, 128, 0, 5, 4, torch.bfloat16),   # 5-row window, output dims split over 4 CTAs
+    (1, 2, 64, 128, 0, 700, 600, torch.float32),  # float32 output, output dims split over 4 CTAs
 ])
 def test_swa_merge_aliased_window(B, n_q, n_h, n_win, kv_pos0, n_kv, q_pos0, out_dtype):
     g = _gen(8)
@@ -187,6 +189,7 @@ def test_attention_reads_no_row_outside_the_visible_set():
     (1, 3, 40000, 512),   # chunks of 864, a short last chunk
     (2, 2, 16390, 1024),  # just past the one-stage limit: one 6-entry last chunk
     (4, 1, 262144, 1024),  # the 1M-context decode shape
+    (1, 150, 20000, 256),  # more rows than SMs: the three-kernel plan
 ])
 def test_two_stage_topk_is_bit_exact_with_ties(B, n_q, N, k):
     """Small-integer indexer inputs give exactly representable scores with many

@@ -127,6 +127,7 @@ def _run_index(qI, kI, qs, ks, w, m, k, q_pos0, N):
     (False, 1, 256, 64, 4, 32, 4, 16, 0),          # the tiny workload's shape: every position a query
     (True, 2, 40, 3000, 64, 128, 4, 512, 12000 - 40),
     (True, 2, 1, 20000, 64, 128, 4, 512, 80000 - 1),  # decode row longer than the shared-memory stage
+    (True, 4, 1, 262144, 64, 128, 4, 1024, 4 * 262144 - 1),  # 1M-context decode rows
     (True, 1, 6, 700, 64, 128, 4, 1024, 2795),      # fewer visible entries than k
     (False, 3, 17, 333, 16, 64, 4, 100, 1000),
 ])
