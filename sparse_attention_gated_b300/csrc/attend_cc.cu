@@ -30,6 +30,8 @@ constexpr int kUnroll = 4;
 
 template <typename T, int V, int MODE>
 __global__ void __launch_bounds__(256) attend_cc_kernel(AttendParams P) {
+  pdl_wait();
+  pdl_trigger();
   const AttendJob& J = P.j;
   const int lane = threadIdx.x & 31;
   const int hpb = blockDim.x >> 5;
@@ -193,6 +195,8 @@ __global__ void __launch_bounds__(256) attend_cc_kernel(AttendParams P) {
 // Merge the split partials of one (batch, query, head): warp per head.
 template <int V>
 __global__ void __launch_bounds__(256) attend_combine_kernel(AttendParams P) {
+  pdl_wait();
+  pdl_trigger();
   const AttendJob& J = P.j;
   const int lane = threadIdx.x & 31;
   const int64_t gw = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -258,16 +262,18 @@ static cudaError_t launch_tv(const AttendParams& P, cudaStream_t s) {
   const AttendJob& J = P.j;
   const int hpb = (J.n_h % 8 == 0) ? 8 : (J.n_h % 4 == 0) ? 4 : (J.n_h % 2 == 0) ? 2 : 1;
   const dim3 grid((unsigned)(J.n_h / hpb), (unsigned)(J.n_q * P.n_split), (unsigned)J.batch), block(32 * hpb);
+  cudaError_t e;
   if (J.mode == 0)
-    attend_cc_kernel<T, V, 0><<<grid, block, 0, s>>>(P);
+    e = launch_pdl(attend_cc_kernel<T, V, 0>, grid, block, 0, s, P);
   else if (J.mode == 1)
-    attend_cc_kernel<T, V, 1><<<grid, block, 0, s>>>(P);
+    e = launch_pdl(attend_cc_kernel<T, V, 1>, grid, block, 0, s, P);
   else
-    attend_cc_kernel<T, V, 2><<<grid, block, 0, s>>>(P);
-  cudaError_t e = cudaGetLastError();
+    e = launch_pdl(attend_cc_kernel<T, V, 2>, grid, block, 0, s, P);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || P.n_split == 1) return e;
   const int64_t warps = J.batch * J.n_q * J.n_h;
-  attend_combine_kernel<V><<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(P);
+  if ((e = launch_pdl(attend_combine_kernel<V>, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s, P)) != cudaSuccess)
+    return e;
   return cudaGetLastError();
 }
 

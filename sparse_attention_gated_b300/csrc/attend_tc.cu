@@ -263,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(sm_all, kSoftThreads);
     *s_abort = 0;
     tc::fence_barrier_init();
+    pdl_wait();  // the loads below may read what the previous kernel wrote
     if (ntiles > 0) {
       tc::prefetch_tmap(&tm_q);
       tc::mbar_arrive_expect_tx(q_full, kSlabs * kQSlabBytes);
@@ -283,6 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *s_tmem;
+  pdl_wait();  // (before it: shared memory, TMEM and parameters only, except thread 0's loads above)
+  pdl_trigger();
 
   bool sm_ok = false;  // softmax warps: the main loop and epilogue completed
   if (warp < kProdWarps) {
@@ -1014,18 +1017,20 @@ cudaError_t launch_attend_tc(const AttendJob& j, void* ws, cudaStream_t s) {
   if (p.join_cnt != nullptr &&
       (e = cudaMemsetAsync(p.join_cnt, 0, (size_t)(rows * p.n_hg) * sizeof(uint32_t), s)) != cudaSuccess)
     return e;
+  auto run = [&](auto kernel) {
+    cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (r != cudaSuccess) return r;
+    return launch_pdl(kernel, dim3((unsigned)grid), dim3(kThreads), (size_t)kSmemBytes, s, tm_q, tm_k, tm_v, p);
+  };
   switch (j.mode) {
     case 0:
-      e = cudaFuncSetAttribute(attend_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-      if (e == cudaSuccess) attend_tc_kernel<0><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(tm_q, tm_k, tm_v, p);
+      e = run(attend_tc_kernel<0>);
       break;
     case 1:
-      e = cudaFuncSetAttribute(attend_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-      if (e == cudaSuccess) attend_tc_kernel<1><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(tm_q, tm_k, tm_v, p);
+      e = run(attend_tc_kernel<1>);
       break;
     default:
-      e = cudaFuncSetAttribute(attend_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-      if (e == cudaSuccess) attend_tc_kernel<2><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(tm_q, tm_k, tm_v, p);
+      e = run(attend_tc_kernel<2>);
       break;
   }
   if (e != cudaSuccess) return e;

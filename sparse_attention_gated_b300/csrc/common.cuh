@@ -16,6 +16,32 @@ constexpr int kNumSMs = 148;  // B300: two dies x 74 SMs
 
 __device__ __forceinline__ float exp2_approx(float x) { return exp2f(x); }
 
+// ------------------------------------------------- programmatic dependent launch
+// Every kernel of the library is launched with programmatic stream serialization
+// (launch_pdl), so it may be scheduled while the kernel before it in the stream is
+// still finishing.  Each kernel calls pdl_wait() before its first access to global
+// memory (from then on it sees every write of the kernels before it, whoever
+// launched them) and pdl_trigger() once its successor may be scheduled; setup that
+// touches only shared memory, TMEM and kernel parameters runs before the wait.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // ---------------------------------------------------------------- vector loads
 // load_vec<V>(p, x): V consecutive elements starting at p (aligned to their
 // total size, or 16 bytes if smaller) converted to float.

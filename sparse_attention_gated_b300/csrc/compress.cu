@@ -43,6 +43,8 @@ template <typename Tin, int OUT>
 __global__ void __launch_bounds__(kCompressThreads) compress_kernel(CompressParams p) {
   extern __shared__ float sm[];  // [3][R][S]: max, denominator, numerator of each row group
   __shared__ float s_red[kCompressThreads / 32];
+  pdl_wait();
+  pdl_trigger();
   const int64_t c = p.c, m = p.m;
   const int G = p.S / kCv;
   const int g = threadIdx.x % G, rg = threadIdx.x / G;
@@ -176,13 +178,13 @@ static cudaError_t launch_t(CompressParams& p, int out_dtype, cudaStream_t s) {
   cudaError_t e;
   if (out_dtype == HYB_F32) {
     e = cudaFuncSetAttribute(compress_kernel<Tin, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) compress_kernel<Tin, 0><<<grid, block, smem, s>>>(p);
+    if (e == cudaSuccess) e = launch_pdl(compress_kernel<Tin, 0>, grid, block, smem, s, p);
   } else if (out_dtype == HYB_BF16) {
     e = cudaFuncSetAttribute(compress_kernel<Tin, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) compress_kernel<Tin, 1><<<grid, block, smem, s>>>(p);
+    if (e == cudaSuccess) e = launch_pdl(compress_kernel<Tin, 1>, grid, block, smem, s, p);
   } else {
     e = cudaFuncSetAttribute(compress_kernel<Tin, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) compress_kernel<Tin, 2><<<grid, block, smem, s>>>(p);
+    if (e == cudaSuccess) e = launch_pdl(compress_kernel<Tin, 2>, grid, block, smem, s, p);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

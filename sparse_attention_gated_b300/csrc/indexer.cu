@@ -45,6 +45,8 @@ __device__ __forceinline__ void load_key16(const void* base, int64_t off, float 
 
 template <bool FP8, int HG>
 __global__ void __launch_bounds__(256) index_scores_cc_kernel(IndexParams p) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ float4 smem4[];
   float* q_s = reinterpret_cast<float*>(smem4);  // [n_ih][c_I]
   float* w_s = q_s + p.n_ih * p.c_I;            // [n_ih]
@@ -117,19 +119,20 @@ cudaError_t launch_index_scores_cc(const hyb_index_args* a, float* scores, int64
   const size_t smem = sizeof(float) * (size_t)(a->n_ih * a->c_I + a->n_ih) + 16;
   const bool fp8 = a->dtype == HYB_E4M3;
   const bool hg16 = (a->n_ih % 16) == 0;
-  if (fp8 && hg16) {
-    cudaFuncSetAttribute(index_scores_cc_kernel<true, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    index_scores_cc_kernel<true, 16><<<grid, block, smem, s>>>(p);
-  } else if (fp8) {
-    cudaFuncSetAttribute(index_scores_cc_kernel<true, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    index_scores_cc_kernel<true, 4><<<grid, block, smem, s>>>(p);
-  } else if (hg16) {
-    cudaFuncSetAttribute(index_scores_cc_kernel<false, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    index_scores_cc_kernel<false, 16><<<grid, block, smem, s>>>(p);
-  } else {
-    cudaFuncSetAttribute(index_scores_cc_kernel<false, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    index_scores_cc_kernel<false, 4><<<grid, block, smem, s>>>(p);
-  }
+  auto run = [&](auto kernel) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    return launch_pdl(kernel, grid, block, smem, s, p);
+  };
+  cudaError_t e;
+  if (fp8 && hg16)
+    e = run(index_scores_cc_kernel<true, 16>);
+  else if (fp8)
+    e = run(index_scores_cc_kernel<true, 4>);
+  else if (hg16)
+    e = run(index_scores_cc_kernel<false, 16>);
+  else
+    e = run(index_scores_cc_kernel<false, 4>);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -33,7 +33,10 @@ struct IdxTc {
   static constexpr int kStages = NQ == 1 ? 5 : 4;
   static constexpr int kAcc = NQ == 1 ? 4 : 2;
   static constexpr int kTmemCols = kAcc * kN;  // 256 or 512
-  static constexpr int kEpiWarps = NQ == 1 ? 4 : 8;
+  static constexpr int kEpiWarps = 8;
+  // decode: two groups of four epilogue warps take alternate tiles; prefill: the two
+  // groups share each tile (two queries each)
+  static constexpr int kEpiGroups = NQ == 1 ? 2 : 1;
   static constexpr int kThreads = (2 + kEpiWarps) * 32;
   static constexpr int kScaleRing = kStages + kAcc;
   static constexpr int kKeyBytes = kTileE * 128;
@@ -113,8 +116,10 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) tc::mbar_init(&full[i], 1), tc::mbar_init(&empty[i], 1);
     for (int i = 0; i < 2; ++i) tc::mbar_init(&q_full[i], 1), tc::mbar_init(&q_empty[i], 1);
-    for (int i = 0; i < C::kAcc; ++i) tc::mbar_init(&acc_full[i], 1), tc::mbar_init(&acc_empty[i], C::kEpiWarps);
-    for (int i = 0; i < C::kScaleRing; ++i) tc::mbar_init(&sc_full[i], 1), tc::mbar_init(&sc_empty[i], C::kEpiWarps);
+    for (int i = 0; i < C::kAcc; ++i)
+      tc::mbar_init(&acc_full[i], 1), tc::mbar_init(&acc_empty[i], C::kEpiWarps / C::kEpiGroups);
+    for (int i = 0; i < C::kScaleRing; ++i)
+      tc::mbar_init(&sc_full[i], 1), tc::mbar_init(&sc_empty[i], C::kEpiWarps / C::kEpiGroups);
     tc::mbar_init(done_bar, 1);
     tc::mbar_init(epi_bar, C::kEpiWarps * 32);
     *s_abort = 0;
@@ -130,6 +135,8 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
+  pdl_wait();  // (the setup above touched only shared memory, TMEM and the parameters)
+  pdl_trigger();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -206,7 +213,7 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
     // ------------------------------------------------------------ epilogue
     const int et = threadIdx.x - 64;  // 0 .. kEpiWarps*32-1
     const int quad = warp & 3;        // TMEM lane quadrant this warp may access
-    const int half = (warp - 2) / 4;  // which queries this warp handles (NQ = 4: two each)
+    const int half = (warp - 2) / 4;  // NQ = 4: which queries this warp handles (two each); NQ = 1: tile parity
     constexpr int kQPerWarp = NQ == 1 ? 1 : 2;
     constexpr int kEpiThreads = C::kEpiWarps * 32;
     // the epilogue warps meet on an mbarrier (bounded), never on a hardware barrier
@@ -236,8 +243,6 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
         }
       }
     };
-    int acc = 0;
-    uint32_t aphase = 0;
     int64_t seq = 0;
     bool ok = true;
     for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
@@ -266,7 +271,10 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
       if (!(ok = esync())) break;
       const bool allpos = *s_allpos != 0;
       for (int64_t t = U.tile_begin; t < U.tile_end; ++t, ++seq) {
+        if (NQ == 1 && (int)(seq & 1) != half) continue;  // the other group's tile
         const int r = (int)(seq % C::kScaleRing);
+        const int acc = (int)(seq % C::kAcc);
+        const uint32_t aphase = (uint32_t)((seq / C::kAcc) & 1);
         if (!(ok = tc::mbar_wait(&acc_full[acc], aphase, s_abort))) break;
         if (!(ok = tc::mbar_wait(&sc_full[r], (uint32_t)((seq / C::kScaleRing) & 1), s_abort))) break;
         tc::tc_fence_after();
@@ -278,27 +286,26 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
         for (int qi = 0; qi < kQPerWarp; ++qi) {
           const int q = NQ == 1 ? 0 : 2 * half + qi;
           const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * C::kN + q * C::kHeads);
-          float v0[32], v1[32];
-          tc::tmem_ld32(taddr, v0);
-          tc::tmem_ld32(taddr + 32, v1);
-          tc::tmem_ld_wait();
+          // heads 0-31 then 32-63 (one 32-column load live at a time; the same summation order)
           const float* wc = w_c + q * C::kHeads;
+          const float* ww = w_w + q * C::kHeads;
+          const float* wq = w_q + q * C::kHeads;
+          const bool fast = allpos && ks > 0.f;
           float sum = 0.f;
-          if (allpos && ks > 0.f) {
 #pragma unroll
-            for (int h = 0; h < 32; ++h) sum = fmaf(wc[h], fmaxf(v0[h], 0.f), sum);
+          for (int hb = 0; hb < 64; hb += 32) {
+            float v[32];
+            tc::tmem_ld32(taddr + hb, v);
+            tc::tmem_ld_wait();
+            if (fast) {
 #pragma unroll
-            for (int h = 0; h < 32; ++h) sum = fmaf(wc[32 + h], fmaxf(v1[h], 0.f), sum);
-            sum *= ks;
-          } else {
-            const float* ww = w_w + q * C::kHeads;
-            const float* wq = w_q + q * C::kHeads;
+              for (int h = 0; h < 32; ++h) sum = fmaf(wc[hb + h], fmaxf(v[h], 0.f), sum);
+            } else {
 #pragma unroll
-            for (int h = 0; h < 32; ++h) sum = fmaf(ww[h], fmaxf(v0[h] * (wq[h] * ks), 0.f), sum);
-#pragma unroll
-            for (int h = 0; h < 32; ++h) sum = fmaf(ww[32 + h], fmaxf(v1[h] * (wq[32 + h] * ks), 0.f), sum);
+              for (int h = 0; h < 32; ++h) sum = fmaf(ww[hb + h], fmaxf(v[h] * (wq[hb + h] * ks), 0.f), sum);
+            }
           }
-          score[qi] = sum;
+          score[qi] = fast ? sum * ks : sum;
         }
         tc::tc_fence_before();
         __syncwarp();
@@ -319,7 +326,6 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
             atomicAdd(&hist[bin >> 1], 1u << (16 * (bin & 1)));
           }
         }
-        if (++acc == C::kAcc) acc = 0, aphase ^= 1u;
       }
     }
     if (do_hist && ok && hist_row >= 0 && esync()) flush_hist();
@@ -382,7 +388,9 @@ static cudaError_t launch_nq(const hyb_index_args* a, float* scores, int64_t sco
   cudaError_t e = cudaFuncSetAttribute(index_tc_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int64_t grid = p.n_units < slots ? p.n_units : slots;
-  index_tc_kernel<NQ><<<(unsigned)grid, C::kThreads, C::kSmemBytes, s>>>(tm_keys, tm_scales, tm_q, p);
+  e = launch_pdl(index_tc_kernel<NQ>, dim3((unsigned)grid), dim3(C::kThreads), (size_t)C::kSmemBytes, s, tm_keys, tm_scales,
+                 tm_q, p);
+  if (e != cudaSuccess) return e;
   *hist_done = p.ghist != nullptr;
   return cudaGetLastError();
 }

@@ -261,6 +261,8 @@ __device__ __forceinline__ void keep_all(const TopkParams& p, int64_t row, int64
 
 // ------------------------------------------------------------- one stage
 __global__ void __launch_bounds__(kTopkThreads) topk_row_kernel(TopkParams p) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint32_t keys_s[];  // [kStageCap]
   __shared__ BlockShared S;
   const int64_t row = blockIdx.x;
@@ -285,6 +287,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_row_kernel(TopkParams p) {
 
 // ------------------------------------------------ three kernels: hist
 __global__ void __launch_bounds__(kTopkThreads) topk_hist_kernel(TopkParams p) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ uint32_t hist[kHistBins];
   const int64_t row = blockIdx.y;
   const int64_t vis = row_visible(p, row);
@@ -559,6 +563,8 @@ __device__ void filter_chunk(const TopkParams& p, int64_t row, int64_t vis, Bloc
 // Every CTA filters its chunk, then counts itself done; the row's last CTA (no
 // waiting: it is simply the one that finds all others done) runs the final selection.
 __global__ void __launch_bounds__(kTopkThreads) topk_filter_kernel(TopkParams p) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint32_t dyn[];
   __shared__ BlockShared S;
   __shared__ uint32_t s_last;
@@ -667,6 +673,8 @@ __device__ __forceinline__ uint32_t block_sum(uint32_t v, BlockShared& S) {
 }
 
 __global__ void __launch_bounds__(kTopkThreads, 1) topk_grid_kernel(TopkParams p) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint32_t dyn[];
   uint32_t* keys = dyn;                                           // [chunk] keys of this CTA's entries
   uint32_t* hist = keys + p.chunk;                                // [kHistBins]
@@ -1030,7 +1038,8 @@ cudaError_t launch_topk(const hyb_index_args* a, const float* scores, int64_t sc
     const size_t smem = sizeof(uint32_t) * (size_t)kStageCap;
     e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    topk_row_kernel<<<(unsigned)rows, kTopkThreads, smem, s>>>(p);
+    if ((e = launch_pdl(topk_row_kernel, dim3((unsigned)rows), dim3(kTopkThreads), smem, s, p)) != cudaSuccess)
+      return e;
     return cudaGetLastError();
   }
   p.chunk = pl.chunk, p.n_chunks = pl.n_chunks;
@@ -1046,17 +1055,17 @@ cudaError_t launch_topk(const hyb_index_args* a, const float* scores, int64_t sc
     // find their SM busy with other work start as that work drains.  (A cooperative launch
     // would state the same guarantee, but inside a CUDA graph next to copies it measured
     // slower.)  A permanent shortage of SMs ends as HYB_DEV_TIMEOUT from the bounded barrier.
-    topk_grid_kernel<<<grid, kTopkThreads, smem, s>>>(p);
+    if ((e = launch_pdl(topk_grid_kernel, grid, dim3(kTopkThreads), smem, s, p)) != cudaSuccess) return e;
     return cudaGetLastError();
   }
   if (!hist_done) {  // the histograms were zeroed by topk_prepare_hist
-    topk_hist_kernel<<<grid, kTopkThreads, 0, s>>>(p);
+    if ((e = launch_pdl(topk_hist_kernel, grid, dim3(kTopkThreads), 0, s, p)) != cudaSuccess) return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   const size_t smem = (size_t)2 * a->k * 4 + (size_t)kSubCap * 8 + (size_t)kCandCap / 8;
   e = cudaFuncSetAttribute(topk_filter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  topk_filter_kernel<<<grid, kTopkThreads, smem, s>>>(p);
+  if ((e = launch_pdl(topk_filter_kernel, grid, dim3(kTopkThreads), smem, s, p)) != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
