@@ -90,7 +90,7 @@ struct AtcParams {
   const __nv_bfloat16* v;
   float* o;                 // modes 0/1, one split: [rows][n_h][c]
   float* lse;               // [rows][n_h]
-  float* part_o;            // modes 0/1, several splits: [rows][n_split][n_h][c]
+  __nv_bfloat16* part_o;    // modes 0/1, several splits: [rows][n_split][n_hg][4][64][128] (chunk-major)
   uint32_t* join_cnt;       // modes 0/1, several splits: [rows * n_hg] splits done (zeroed per launch)
   float2* part_ml;          // [rows][n_split][n_h] (reference m in log2 units, denominator)
   const float* o_in;        // mode 2
@@ -714,11 +714,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else if (MODE != 2 && ok && p.n_split > 1) {
-      // split partial (unnormalised O): chunk by chunk, this half's [32 heads][128] float32
-      // piece is staged in the free ring and bulk-stored at once into the unit's
-      // chunk-major partial [4 chunks][64 heads][128]
-      float* piece0 = reinterpret_cast<float*>(kv_s) + hh * (4 * 32 * 128);
-      float* dst0 = p.part_o + ((W.bq * p.n_split + W.sp) * p.n_hg + W.hg) * (int64_t)(kHG * kC);
+      // split partial (unnormalised O, rounded to bf16 like the probabilities that made it):
+      // chunk by chunk, this half's [32 heads][128] piece is staged in the free ring and
+      // bulk-stored at once into the unit's chunk-major partial [4 chunks][64 heads][128]
+      __nv_bfloat16* piece0 = reinterpret_cast<__nv_bfloat16*>(kv_s) + hh * (4 * 32 * 128);
+      __nv_bfloat16* dst0 = p.part_o + ((W.bq * p.n_split + W.sp) * p.n_hg + W.hg) * (int64_t)(kHG * kC);
 #pragma unroll 1
       for (int ch = 0; ch < 4 && ok; ++ch) {
         float v[32];
@@ -729,13 +729,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int y = 0; y < 32; ++y) v[y] = 0.f;
         }
-        float* piece = piece0 + ch * (32 * 128);
+        __nv_bfloat16* piece = piece0 + ch * (32 * 128);
 #pragma unroll
-        for (int y = 0; y < 32; ++y) piece[y * 128 + e] = v[y];
+        for (int y = 0; y < 32; ++y) piece[y * 128 + e] = __float2bfloat16_rn(v[y]);
         tc::fence_proxy_async_smem();
         ok = hsync();
         if (ok && q4 == 0 && lane == 0) {
-          tc::bulk_store(dst0 + (int64_t)(ch * kHG + h0) * 128, piece, 32 * 128 * 4);
+          tc::bulk_store(dst0 + (int64_t)(ch * kHG + h0) * 128, piece, 32 * 128 * 2);
           tc::bulk_commit();
         }
       }
@@ -870,7 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) {
           // every thread: up to 4 items (float4 quads) at once, all splits' loads in flight
-          const float* po_b = p.part_o + (W.bq * S * p.n_hg + W.hg) * (int64_t)(kHG * kC);
+          const __nv_bfloat16* po_b = p.part_o + (W.bq * S * p.n_hg + W.hg) * (int64_t)(kHG * kC);
           const int64_t split_stride = (int64_t)p.n_hg * kHG * kC;
           float* o_b = p.o + (W.bq * p.n_h + W.hg * kHG) * kC;
           for (int base = i0 + ts; base < i1; base += 4 * kSoftThreads) {
@@ -889,7 +889,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
                 if (base + k * kSoftThreads < i1) {
-                  const float4 v = __ldcg(reinterpret_cast<const float4*>(po_b + s2 * split_stride + off[k]));
+                  const uint2 raw = __ldcg(reinterpret_cast<const uint2*>(po_b + s2 * split_stride + off[k]));
+                  const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+                  const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+                  const float4 v = make_float4(lo.x, lo.y, hi.x, hi.y);
                   const float w = t_w[wi[k] + s2];
                   acc[k].x = fmaf(w, v.x, acc[k].x), acc[k].y = fmaf(w, v.y, acc[k].y);
                   acc[k].z = fmaf(w, v.z, acc[k].z), acc[k].w = fmaf(w, v.w, acc[k].w);
@@ -975,7 +978,7 @@ size_t attend_tc_workspace_bytes(const AttendJob& j) {
   if (pl.n_split <= 1 || j.mode == 2) return 0;
   const size_t n = (size_t)(j.batch * j.n_q * pl.n_split * j.n_h);
   const size_t units = (size_t)(j.batch * j.n_q * (j.n_h / kHG));
-  return n * (size_t)kC * sizeof(float) + n * sizeof(float2) + units * sizeof(uint32_t) + 256;
+  return n * (size_t)kC * sizeof(__nv_bfloat16) + n * sizeof(float2) + units * sizeof(uint32_t) + 256;
 }
 
 cudaError_t launch_attend_tc(const AttendJob& j, void* ws, cudaStream_t s) {
@@ -997,8 +1000,8 @@ cudaError_t launch_attend_tc(const AttendJob& j, void* ws, cudaStream_t s) {
   const int64_t rows = j.batch * j.n_q;
   if (p.n_split > 1 && j.mode != 2) {
     const size_t n = (size_t)(rows * p.n_split * j.n_h);
-    p.part_o = static_cast<float*>(ws);
-    p.part_ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + n * (size_t)kC * sizeof(float));
+    p.part_o = static_cast<__nv_bfloat16*>(ws);
+    p.part_ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + n * (size_t)kC * sizeof(__nv_bfloat16));
     p.join_cnt = reinterpret_cast<uint32_t*>(p.part_ml + n);
   }
   const uint64_t kv_rows = (uint64_t)(j.batch * j.kv_stride);

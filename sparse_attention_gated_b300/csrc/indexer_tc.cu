@@ -375,7 +375,10 @@ static cudaError_t launch_nq(const hyb_index_args* a, float* scores, int64_t sco
   const int64_t tiles_max = (n_vis_max + 127) / 128;
   const int ctas_per_sm = C::kSmemBytes <= 113 * 1024 ? 2 : 1;
   const int64_t slots = (int64_t)kNumSMs * ctas_per_sm;
-  int64_t tpu = (groups * tiles_max + 2 * slots - 1) / (2 * slots);
+  // decode: one unit per CTA (one query-group setup, one histogram flush); prefill: two
+  // per CTA on average, for balance
+  const int64_t per_slot = NQ == 1 ? 1 : 2;
+  int64_t tpu = (groups * tiles_max + per_slot * slots - 1) / (per_slot * slots);
   tpu = tpu < 1 ? 1 : (tpu > tiles_max ? tiles_max : tpu);
   p.tiles_per_unit = tpu;
   p.units_per_group = (tiles_max + tpu - 1) / tpu;

@@ -66,8 +66,9 @@ constexpr int kHistBins = kTopkHistBins;
 constexpr int kMaxChunks = 64;
 constexpr int kPer = 8;  // keys a thread loads before using them (histogram and filter passes)
 constexpr int64_t kGridChunkCap = 32768;  // grid plan: keys per CTA, staged in shared memory
-constexpr int kSubListCap = 1024;         // grid plan: sub-candidates per row ranked directly
-constexpr int kGridSlot = 4;              // grid plan: published counts per CTA (sure, > T, == T, unused)
+constexpr int kCandListCap = 4096;        // grid plan: candidates per row selected in shared memory
+constexpr int kSubListCap = 1024;         // grid plan, overflow: sub-candidates per row ranked directly
+constexpr int kGridSlot = 8;              // grid plan: published counts per CTA
 constexpr long long kGridWaitCycles = 1LL << 31;  // bound of a grid-barrier wait (about 1 s)
 
 struct TopkParams {
@@ -88,9 +89,11 @@ struct TopkParams {
   uint32_t* done;       // [rows]: filter CTAs finished (the last one selects)
   // grid plan (ghist, ghist2 and chunk/n_chunks as above)
   uint32_t* hist3;      // [rows][256]: last 8 bits of the sub-candidates (overflow only)
-  uint32_t* nsub;       // [rows]: sub-candidates appended to the row's list
-  uint32_t* gsync;      // [0]: grid-barrier arrivals, [1]: some row's list overflowed
-  int32_t* slots;       // [rows][n_chunks][kGridSlot]: published per-CTA counts
+  uint32_t* nsub;       // [rows]: sub-candidates appended to the row's sub-list
+  uint32_t* ncand;      // [rows]: candidates appended to the row's list
+  uint32_t* gsync;      // [0]: grid-barrier arrivals, [1]: a sub-list overflowed
+  int32_t* slots;       // [rows][n_chunks][kGridSlot]: published per-CTA counts (slow path 0-2, list 4-6)
+  uint2* cand;          // [rows][n_chunks][chunk]: (key, entry) of each CTA's first-level candidates
   uint2* sub;           // [rows][kSubListCap]: (key, entry) of the sub-candidates
   int hist_done;        // the row histograms were filled by the indexer
   int32_t* dev_status;
@@ -665,6 +668,11 @@ __device__ bool grid_barrier(uint32_t* count, uint32_t target, int32_t* dev_stat
   return s_ok != 0;
 }
 
+// The float32 whose order-preserving key is k (the inverse of float_order_key; -0 comes back as +0).
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 // Sum over the CTA of one value per thread (every thread gets the total).
 __device__ __forceinline__ uint32_t block_sum(uint32_t v, BlockShared& S) {
   uint32_t before, z0, tot, z1;
@@ -680,6 +688,8 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_grid_kernel(TopkParams p
   uint32_t* hist = keys + p.chunk;                                // [kHistBins]
   uint2* list = reinterpret_cast<uint2*>(hist + kHistBins);       // [kSubListCap] the row's sub-candidates
   uint32_t* selb = reinterpret_cast<uint32_t*>(list + kSubListCap);  // [chunk / 32] selected sub-candidates
+  uint2* sorted = reinterpret_cast<uint2*>(selb + p.chunk / 32);     // [kCandListCap] candidates by entry
+  uint32_t* kbits = reinterpret_cast<uint32_t*>(sorted + kCandListCap);  // [kCandListCap / 32] kept ones
   __shared__ BlockShared S;
   __shared__ int64_t s_before;
   const int tid = threadIdx.x;
@@ -730,28 +740,194 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_grid_kernel(TopkParams p
     if (!grid_barrier(p.gsync, ++nbar * nblk, p.dev_status, 40)) return;
   }
 
-  // phase 1: first-level threshold bin; second-level histogram of the chunk's keys in it
+  // phase 1: first-level threshold bin b1.  The chunk's keys in b1 (candidates) go to the
+  // row's candidate list, one contiguous range per CTA in entry order, and are histogrammed
+  // on their next 12 bits (needed only if some row's list overflows).
   uint32_t b1 = 0, above1 = 0;
   if (active) threshold_bin(p.ghist + row * kHistBins, (uint32_t)p.k, S, b1, above1);
   const uint32_t r = (uint32_t)p.k - above1;  // keys of bin b1 to keep (>= 1)
+  uint32_t n_c = 0, n_s1 = 0;                 // this thread's candidates and keys above b1
   if (active)
     for (int u = 0; u < per; ++u) {
       const int e = e0 + u;
       const uint32_t key = e < e1 ? keys[e] : 0u;
-      hist_add(hist, e < e1 && (key >> (32 - kHistBits)) == b1, (key >> (32 - 2 * kHistBits)) & (kHistBins - 1));
+      const uint32_t bin = key >> (32 - kHistBits);
+      const bool c = e < e1 && bin == b1;
+      n_c += c, n_s1 += (e < e1 && bin > b1);
+      hist_add(hist, c, (key >> (32 - 2 * kHistBits)) & (kHistBins - 1));
     }
-  __syncthreads();
+  uint32_t cb, z0, ctot, s1tot;
+  block_scan_counts(n_c, n_s1, S, cb, z0, ctot, s1tot);  // (its barriers also complete the histogram)
+  if (active) {
+    // this CTA's candidates, in entry order, in its own region of the row's list
+    uint2* mine = p.cand + ((int64_t)row * parts + part) * p.chunk;
+    uint32_t x = cb;
+    for (int e = e0; e < e1; ++e) {
+      const uint32_t key = keys[e];
+      if ((key >> (32 - kHistBits)) == b1) mine[x++] = make_uint2(key, (uint32_t)(s0 + e));
+    }
+    if (tid == 0) {
+      myslot[4] = (int32_t)s1tot, myslot[5] = (int32_t)ctot;
+      if (ctot) atomicAdd(p.ncand + row, ctot);  // the row's total (no return value needed)
+    }
+  }
   for (int i = tid; i < kHistBins; i += kTopkThreads)
     if (hist[i]) atomicAdd(p.ghist2 + row * kHistBins + i, hist[i]);
   if (!grid_barrier(p.gsync, ++nbar * nblk, p.dev_status, 41)) return;
 
-  // phase 2: second-level bin; sure keeps counted, sub-candidates listed
+  // phase 2 (rows with at most kCandListCap candidates): every CTA gathers the row's
+  // candidates in entry order (CTA by CTA, at the prefix of the counts before it), finds
+  // the second-level bin b2 from the row's second histogram, keeps the candidates whose
+  // next 12 bits are above b2 and the r2 best (key desc, entry asc) of the few equal to
+  // it, then writes its own kept entries at the offset given by the CTAs before it.
+  __shared__ uint32_t p_pre[kNumSMs + 1];
+  __shared__ int64_t s_sure;
+  __shared__ uint32_t s_flags;  // bit 0: some row has more candidates than the cap
+  uint32_t n_cand = 0;
+  {
+    // the per-CTA counts of this row (warp 0) and every row's total (warp 1), read
+    // together with the second histogram below
+    uint32_t cnt[5] = {0u, 0u, 0u, 0u, 0u};
+    int64_t sure = 0;
+    if (tid < 32 && active) {
+#pragma unroll
+      for (int k = 0; k < 5; ++k) {
+        const int q = tid * 5 + k;
+        const int32_t* o = p.slots + ((int64_t)row * parts + q) * kGridSlot;
+        if (q < parts) cnt[k] = (uint32_t)__ldcg(o + 5);
+        if (q < part) sure += __ldcg(o + 4);
+      }
+    }
+    if (tid >= 32 && tid < 64) {
+      uint32_t over = 0;
+      for (int rr = tid - 32; rr < (int)gridDim.y; rr += 32) over |= __ldcg(p.ncand + rr) > (uint32_t)kCandListCap;
+      over = __any_sync(0xffffffffu, over != 0);
+      if (tid == 32) s_flags = over;
+    }
+    if (tid < 32 && active) {
+      uint32_t sum = cnt[0] + cnt[1] + cnt[2] + cnt[3] + cnt[4];
+      uint32_t incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (tid >= o) incl += u;
+      }
+      uint32_t run = incl - sum;
+#pragma unroll
+      for (int k = 0; k < 5; ++k) {
+        const int q = tid * 5 + k;
+        if (q < parts) p_pre[q] = run;
+        run += cnt[k];
+      }
+      if (tid == 31) p_pre[parts] = incl;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) sure += __shfl_xor_sync(0xffffffffu, sure, o);
+      if (tid == 0) s_sure = sure;
+    }
+  }
   uint32_t b2 = 0, above2 = 0;
   if (active) threshold_bin(p.ghist2 + row * kHistBins, r, S, b2, above2);
-  const uint32_t r2 = r - above2;  // sub-candidates to keep (>= 1)
+  __syncthreads();  // the tables above are written
+  const bool any_overflow = s_flags != 0u;  // the same for every CTA
+  if (active) n_cand = p_pre[parts];
+  const bool listed = active && n_cand <= (uint32_t)kCandListCap;
+  const uint32_t r2 = r - above2;  // keys with the top 24 bits (b1, b2) to keep (>= 1)
   const uint32_t pre24 = (b1 << kHistBits) | b2;
+  if (listed) {
+    for (int i = tid; i < kCandListCap / 32; i += kTopkThreads) kbits[i] = 0u;
+    for (uint32_t x = tid; x < n_cand; x += kTopkThreads) {
+      int lo = 0, hi = parts - 1;  // the CTA that holds candidate x: the last q with p_pre[q] <= x
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p_pre[mid] <= x) lo = mid; else hi = mid - 1;
+      }
+      sorted[x] = __ldcg(p.cand + ((int64_t)row * parts + lo) * p.chunk + (x - p_pre[lo]));
+    }
+    __syncthreads();
+    // the sub-candidates (top 24 bits = (b1, b2)) in entry order, and their ranks
+    uint32_t sub_base = 0;
+    for (uint32_t base = 0; base < n_cand; base += kTopkThreads) {
+      const uint32_t x = base + tid;
+      const uint32_t key = x < n_cand ? sorted[x].x : 0u;
+      const bool above = x < n_cand && (key >> 8) > pre24, sub = x < n_cand && (key >> 8) == pre24;
+      uint32_t ab, sb, at, st;
+      block_scan2(above, sub, S, ab, sb, at, st);
+      if (above) atomicOr(&kbits[x >> 5], 1u << (x & 31));
+      if (sub && sub_base + sb < (uint32_t)kSubListCap) list[sub_base + sb] = make_uint2(key, x);
+      sub_base += st;
+    }
+    __syncthreads();
+    const uint32_t n_sub = sub_base;  // >= r2
+    if (n_sub <= (uint32_t)kSubListCap) {
+      if (tid < (int)n_sub) {
+        const uint2 me = list[tid];
+        uint32_t rank = 0;
+        for (uint32_t y = 0; y < n_sub; ++y) {
+          const uint2 o = list[y];
+          rank += o.x > me.x || (o.x == me.x && o.y < me.y);
+        }
+        if (rank < r2) atomicOr(&kbits[me.y >> 5], 1u << (me.y & 31));
+      }
+    } else {
+      // many equal 24-bit prefixes: exact selection over the row's candidates
+      uint32_t T, ties;
+      auto sub24 = [&](int64_t x) { return (sorted[x].x >> 8) == pre24 ? sorted[x].x : 0u; };
+      radix_select(sub24, n_cand, r2, S, T, ties);
+      uint32_t eq_base = 0;
+      for (uint32_t base = 0; base < n_cand; base += kTopkThreads) {
+        const uint32_t x = base + tid;
+        const uint32_t key = x < n_cand ? sub24(x) : 0u;
+        const bool gt = x < n_cand && key > T && key != 0u, eq = x < n_cand && key == T && key != 0u;
+        uint32_t gb, eb, gtt, ett;
+        block_scan2(gt, eq, S, gb, eb, gtt, ett);
+        if (gt || (eq && eq_base + eb < ties)) atomicOr(&kbits[x >> 5], 1u << (x & 31));
+        eq_base += ett;
+      }
+    }
+    __syncthreads();
+    // kept candidates of the CTAs before this one
+    const uint32_t mine0 = p_pre[part];
+    uint32_t kc = 0;
+    for (uint32_t w = tid; w * 32 < mine0; w += kTopkThreads) {
+      const uint32_t bits = kbits[w];
+      const uint32_t lim = mine0 - w * 32;
+      kc += __popc(lim >= 32 ? bits : (bits & ((1u << lim) - 1u)));
+    }
+    const int64_t before = s_sure + block_sum(kc, S);
+    // this CTA's kept entries, in entry order
+    auto kept = [&](uint32_t key, uint32_t ci) {
+      const uint32_t bin = key >> (32 - kHistBits);
+      return bin > b1 || (bin == b1 && ((kbits[(mine0 + ci) >> 5] >> ((mine0 + ci) & 31)) & 1u));
+    };
+    uint32_t mine = 0, ci = cb;
+    for (int e = e0; e < e1; ++e) {
+      const uint32_t key = keys[e];
+      mine += kept(key, ci);
+      ci += (key >> (32 - kHistBits)) == b1;
+    }
+    uint32_t kb, zb, kt, zt;
+    block_scan_counts(mine, 0u, S, kb, zb, kt, zt);
+    int64_t slot = before + kb;
+    ci = cb;
+    for (int e = e0; e < e1; ++e) {
+      const uint32_t key = keys[e];
+      if (kept(key, ci)) {
+        out[slot] = (int32_t)(s0 + e);
+        if (out_sc) out_sc[slot] = key_to_float(key);
+        ++slot;
+      }
+      ci += (key >> (32 - kHistBits)) == b1;
+    }
+  }
+
+  // rows whose candidate list overflowed (many keys share their top 12 bits): a
+  // second 12-bit level, then a list of the few sub-candidates or, if that overflows
+  // too, the last 8 bits and the ties through a prefix over the CTAs
+  const bool slow_row = active && !listed;
+  if (any_overflow) {
+  // phase 2s: sure keeps counted, sub-candidates (top 24 bits = (b1, b2)) listed
   uint32_t sure = 0;
-  if (active)
+  if (slow_row)
     for (int e = e0; e < e1; ++e) {
       const uint32_t key = keys[e], t24 = key >> 8;
       sure += t24 > pre24;
@@ -764,13 +940,13 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_grid_kernel(TopkParams p
       }
     }
   sure = block_sum(sure, S);
-  if (active && tid == 0) myslot[0] = (int32_t)sure;
+  if (slow_row && tid == 0) myslot[0] = (int32_t)sure;
   if (!grid_barrier(p.gsync, ++nbar * nblk, p.dev_status, 42)) return;
 
-  // phase 3: select among the sub-candidates and write this chunk's kept entries
-  const uint32_t n_sub = active ? __ldcg(p.nsub + row) : 0u;
-  const bool fast = active && n_sub <= (uint32_t)kSubListCap;
-  const bool any_overflow = __ldcg(p.gsync + 1) != 0u;  // the same for every CTA
+  // phase 3s: select among the sub-candidates and write this chunk's kept entries
+  const uint32_t n_sub = slow_row ? __ldcg(p.nsub + row) : 0u;
+  const bool fast = slow_row && n_sub <= (uint32_t)kSubListCap;
+  const bool sub_overflow = __ldcg(p.gsync + 1) != 0u;  // the same for every CTA
   if (fast) {
     for (int i = tid; i < (int)(p.chunk / 32); i += kTopkThreads) selb[i] = 0u;
     if (tid < (int)n_sub) list[tid] = __ldcg(p.sub + row * kSubListCap + tid);
@@ -819,9 +995,9 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_grid_kernel(TopkParams p
       }
     }
   }
-  if (any_overflow) {
+  if (sub_overflow) {
     // exact k-th key from the last 8 bits; ties kept lowest entry first over the CTAs
-    const bool slow = active && !fast;
+    const bool slow = slow_row && !fast;
     for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
     __syncthreads();
     if (slow)
@@ -903,6 +1079,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_grid_kernel(TopkParams p
       }
     }
   }
+  }  // any_overflow
   if (!active) {
     for (int64_t i = (int64_t)part * kTopkThreads + tid; i < p.k; i += (int64_t)parts * kTopkThreads) {
       out[i] = i < vis ? (int32_t)i : -1;
@@ -920,7 +1097,8 @@ struct TopkPlan {
 };
 
 static size_t grid_smem_bytes(int64_t chunk) {
-  return (size_t)chunk * 4 + kHistBins * 4 + kSubListCap * 8 + (size_t)chunk / 8;
+  return (size_t)chunk * 4 + kHistBins * 4 + kSubListCap * 8 + (size_t)chunk / 8 + kCandListCap * 8 +
+         kCandListCap / 8;
 }
 
 // One CTA of the grid plan fits an SM of the current device (cached per device).
@@ -969,15 +1147,15 @@ static TopkPlan plan_topk(const hyb_index_args* a, int64_t n_vis_max) {
 
 static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-// grid plan: the zeroed counters first (histograms, list sizes, barrier), then the rest
-static size_t grid_zeroed_bytes(size_t rows) { return rows * (2 * kHistBins + 256 + 1) * 4 + 2 * 4; }
+// grid plan: the zeroed counters first (histograms, list sizes, barrier and flags), then the rest
+static size_t grid_zeroed_bytes(size_t rows) { return rows * (2 * kHistBins + 256 + 2) * 4 + 4 * 4; }
 
 size_t topk_workspace_bytes(const hyb_index_args* a, int64_t n_vis_max) {
   const TopkPlan pl = plan_topk(a, n_vis_max);
   const size_t rows = (size_t)(a->batch * a->n_q);
   if (pl.kind == 2)
     return align256(grid_zeroed_bytes(rows)) + align256(rows * pl.n_chunks * kGridSlot * 4) +
-           align256(rows * kSubListCap * 8);
+           align256(rows * kSubListCap * 8) + align256(rows * pl.n_chunks * pl.chunk * 8);
   if (pl.kind != 1) return 0;
   const size_t region = rows * (size_t)pl.n_chunks * (size_t)pl.chunk;
   return align256(rows * kHistBins * 8 + rows * 4) + 3 * align256(region * 4) + align256(rows * pl.n_chunks * 8);
@@ -992,11 +1170,14 @@ static void topk_pointers(TopkParams& p, const TopkPlan& pl, int64_t rows, void*
   if (pl.kind == 2) {
     p.hist3 = p.ghist2 + rows * kHistBins;
     p.nsub = p.hist3 + rows * 256;
-    p.gsync = p.nsub + rows;
+    p.ncand = p.nsub + rows;
+    p.gsync = p.ncand + rows;
     w += align256(grid_zeroed_bytes((size_t)rows));
     p.slots = reinterpret_cast<int32_t*>(w);
     w += align256((size_t)rows * pl.n_chunks * kGridSlot * 4);
     p.sub = reinterpret_cast<uint2*>(w);
+    w += align256((size_t)rows * kSubListCap * 8);
+    p.cand = reinterpret_cast<uint2*>(w);
     return;
   }
   const size_t region = (size_t)rows * pl.n_chunks * pl.chunk;

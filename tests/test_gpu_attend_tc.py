@@ -126,6 +126,8 @@ def test_softmax_reference_moves_late_in_the_list(order):
     (8, 1, 64, 2048, 128, 2048 * 128 - 1),    # Flash HCA decode
     (1, 1, 64, 20000, 128, 20000 * 128 - 1),  # more tiles than SMs: splits of several tiles
     (1, 300, 64, 80, 4, 0),                   # causal prefill: empty, short and ragged lists
+    (2, 1, 128, 3000, 128, 2999 * 128 + 5),    # two head groups, 24 splits of one tile, ragged last tile
+    (3, 2, 128, 700, 16, 700 * 16 - 18),       # two queries with different lengths, ragged tails
 ])
 def test_hca_attend_aliased_entries(B, n_q, n_h, N, m, q_pos0):
     g = _gen(7)
