@@ -66,17 +66,14 @@ def stage_model(w):
         m["csa_compress"] = dict(bytes=B * (4 * 2 * w.m * (c + w.c_I) * bf + c * bf + w.c_I + 4), flops=0)
         m["csa_index_topk"] = dict(bytes=B * (N * (w.c_I + 4) + w.n_ih * (w.c_I + 8) + w.k * 4),
                                    flops=B * N * w.n_ih * w.c_I * 2, flop_dtype="fp8")
-        m["csa_attend"] = dict(bytes=B * (w.k * (c * bf + 4) + H * c * bf + H * (c + 1) * 4),
-                               flops=B * w.k * H * c * 4, flop_dtype="bf16")
-        m["csa_swa_merge"] = dict(bytes=B * (w.n_win * c * bf + H * c * bf + H * (c + 1) * 4 + H * c * bf),
-                                  flops=B * w.n_win * H * c * 4, flop_dtype="bf16")
+        # attention over the selected entries with the window merge fused (one call)
+        m["csa_attend"] = dict(bytes=B * ((w.k + w.n_win) * c * bf + w.k * 4 + H * c * bf + H * c * bf + H * 4),
+                               flops=B * (w.k + w.n_win) * H * c * 4, flop_dtype="bf16")
     if w.kind in ("hybrid_decode", "hca_decode"):
         Nh = w.n_hca
         m["hca_compress"] = dict(bytes=B * (2 * w.m_hca * c * bf + c * bf), flops=0)
-        m["hca_attend"] = dict(bytes=B * (Nh * c * bf + H * c * bf + H * (c + 1) * 4), flops=B * Nh * H * c * 4,
-                               flop_dtype="bf16")
-        m["hca_swa_merge"] = dict(bytes=B * (w.n_win * c * bf + H * c * bf + H * (c + 1) * 4 + H * c * bf),
-                                  flops=B * w.n_win * H * c * 4, flop_dtype="bf16")
+        m["hca_attend"] = dict(bytes=B * ((Nh + w.n_win) * c * bf + H * c * bf + H * c * bf + H * 4),
+                               flops=B * (Nh + w.n_win) * H * c * 4, flop_dtype="bf16")
     if w.kind == "csa_prefill":
         n, N = w.n_ctx, w.n_csa
         pairs = sum(min(N, (t + 1) // w.m) for t in range(n))  # visible (query, entry) pairs
@@ -85,10 +82,8 @@ def stage_model(w):
         m["csa_compress"] = dict(bytes=n * 4 * (c + w.c_I) * bf + N * (c * bf + w.c_I + 4), flops=0)
         m["csa_index_topk"] = dict(bytes=n * w.n_ih * (w.c_I + 8) + N * (w.c_I + 4) + n * w.k * 4,
                                    flops=pairs * w.n_ih * w.c_I * 2, flop_dtype="fp8")
-        m["csa_attend"] = dict(bytes=n * H * c * (bf + 4) + N * c * bf + n * w.k * 4,
-                               flops=sel * H * c * 4, flop_dtype="bf16")
-        m["csa_swa_merge"] = dict(bytes=n * (c * bf + H * c * (bf + 4 + bf)), flops=win * H * c * 4,
-                                  flop_dtype="bf16")
+        m["csa_attend"] = dict(bytes=n * H * c * (bf + bf) + N * c * bf + n * w.k * 4 + n * c * bf,
+                               flops=(sel + win) * H * c * 4, flop_dtype="bf16")
     return m
 
 
@@ -386,13 +381,8 @@ def _csa_parts(st, stream, rec, scoring_events=None):
     rec("csa_index_topk", 1)
     rec("csa_attend", 0)
     ops.csa_attend(x["q"], kc, kc, b["idx"], scale=w.scale, o=b["o"], lse=b["lse"], workspace=st.ws["csa"],
-                   dev_status=s, stream=stream)
+                   dev_status=s, stream=stream, window=st._win_csa(as_dict=True))
     rec("csa_attend", 1)
-    rec("csa_swa_merge", 0)
-    kv_pos0 = w.n_ctx - w.n_win if w.decode else 0
-    ops.swa_merge(x["q"], x["kv"], x["kv"], kv_pos0=kv_pos0, q_pos0=w.q_pos0, n_win=w.n_win, scale=w.scale,
-                  o_in=b["o"], lse_in=b["lse"], out=b["out"], dev_status=s, stream=stream)
-    rec("csa_swa_merge", 1)
 
 
 def _hca_parts(st, stream, rec):
@@ -409,20 +399,18 @@ def _hca_parts(st, stream, rec):
     rec("hca_compress", 1)
     rec("hca_attend", 0)
     ops.hca_attend(q, kc, kc, m=w.m_hca, q_pos0=w.q_pos0, scale=w.scale, o=b["o_h"], lse=b["lse_h"],
-                   workspace=st.ws["hca"], dev_status=s, stream=stream)
+                   workspace=st.ws["hca"], dev_status=s, stream=stream, window=st._win_hca(as_dict=True))
     rec("hca_attend", 1)
-    rec("hca_swa_merge", 0)
-    ops.swa_merge(q, kv, kv, kv_pos0=w.n_ctx - w.n_win, q_pos0=w.q_pos0, n_win=w.n_win, scale=w.scale,
-                  o_in=b["o_h"], lse_in=b["lse_h"], out=b["out_h"], dev_status=s, stream=stream)
-    rec("hca_swa_merge", 1)
 
 
 def _launches_per_step(w):
     n = 0
-    if w.kind in ("hybrid_decode", "csa_decode", "csa_prefill"):
-        n += 2 + 2 + 1 + 1  # compress x2, index scores + top-k, attend (splits join in-kernel), window merge
+    if w.kind in ("hybrid_decode", "csa_decode"):
+        n += 2 + 2 + 1  # compress x2, index scores + top-k, attention with the window merge fused
+    if w.kind == "csa_prefill":
+        n += 2 + 2 + 2  # (32,768 queries: too many to fuse the window, so two attention launches)
     if w.kind in ("hybrid_decode", "hca_decode"):
-        n += 1 + 1 + 1
+        n += 1 + 1
     return n
 
 

@@ -219,6 +219,33 @@ HYB_API hyb_status csa_index_topk(const hyb_index_args* a, void* workspace, size
 HYB_API hyb_status csa_index_topk_noalloc(const hyb_index_args* a, void* stream);
 
 /* ------------------------------------------------------------------------
+ * hyb_window -- the sliding-window branch fused into csa_attend / hca_attend.
+ *
+ * When the `window` member of their argument struct is not NULL, the call
+ * returns what swa_merge returns for the compressed branch's result (swa_merge
+ * with kw = vw = window->kw and o_in, lse_in = that result): `out` receives the
+ * merged output and `lse` the log-sum-exp of the union; `o` is not written and
+ * may be NULL.  Query j is at absolute position q_pos0 + j (for hca_attend it
+ * must equal the call's q_pos0).  kw [batch][n_kv][c] (the call's dtype) holds
+ * raw rows at absolute positions kv_pos0 ..; the window rows are both keys and
+ * values, and every needed row must lie inside the buffer.  out
+ * [batch][n_q][n_h][c] of out_dtype (F32 or BF16).  Where the launch fits the
+ * GPU at once, the window is one more split of the compressed list's softmax
+ * (no second kernel and no float32 o / lse round trip through memory);
+ * otherwise the call runs the two steps in sequence.  (A fusion of two of the
+ * method's steps for deployment; the result is the same.)
+ * ------------------------------------------------------------------------ */
+typedef struct hyb_window {
+  const void* kw;
+  int64_t n_kv;
+  int64_t kv_pos0;
+  int64_t q_pos0;
+  int64_t n_win;
+  void* out;
+  int32_t out_dtype;
+} hyb_window;
+
+/* ------------------------------------------------------------------------
  * csa_attend -- CSA core attention over the selected entries ([HA] V.3, MQA:
  * every head shares one compressed K and V; [KE] section 6 contract).
  *
@@ -248,6 +275,7 @@ typedef struct hyb_csa_attend_args {
   float scale;
   int32_t dtype; /* hyb_dtype */
   int32_t* dev_status;
+  const hyb_window* window; /* optional fused window merge (see hyb_window), or NULL */
 } hyb_csa_attend_args;
 
 HYB_API size_t csa_attend_workspace_size(const hyb_csa_attend_args* a);
@@ -277,6 +305,7 @@ typedef struct hyb_hca_attend_args {
   float scale;
   int32_t dtype;
   int32_t* dev_status;
+  const hyb_window* window; /* optional fused window merge (see hyb_window), or NULL */
 } hyb_hca_attend_args;
 
 HYB_API size_t hca_attend_workspace_size(const hyb_hca_attend_args* a);

@@ -100,6 +100,12 @@ struct AtcParams {
   int out_bf16;
   int64_t n_q, n_h, n_entries, kv_stride, list_len, m, q_pos0, kv_pos0, n_win;
   int n_split, n_hg, alias;
+  // modes 0/1 with a fused window merge: the last split of each (query, head group) attends
+  // the query's window of raw rows kw [batch][w_stride][c] (row 0 = absolute position w_pos0;
+  // the rows are keys and values), and the join writes the merged `out` and the union's lse
+  int win;
+  const __nv_bfloat16* kw;
+  int64_t w_stride, w_pos0, wq_pos0;
   float scale_log2;
   int32_t* dev_status;
 };
@@ -110,6 +116,7 @@ struct AtcWork {
   int64_t row0;  // modes 1/2: global row of list position 0
   const int32_t* list;
   int64_t tb, te;  // this split's tiles
+  bool win;        // this split is the fused window (contiguous rows of kw)
 };
 
 template <int MODE>
@@ -124,6 +131,17 @@ __device__ __forceinline__ AtcWork atc_work(const AtcParams& p) {
   const int64_t t = p.q_pos0 + w.j;
   w.list = nullptr;
   w.row0 = 0;
+  w.win = false;
+  if (MODE != 2 && p.win && w.sp == p.n_split - 1) {
+    // the fused window: raw rows max(0, tw-n_win+1) .. tw of kw
+    const int64_t tw = p.wq_pos0 + w.j;
+    w.win = true;
+    w.L = tw + 1 < p.n_win ? tw + 1 : p.n_win;
+    w.row0 = w.b * p.w_stride + (tw - w.L + 1 - p.w_pos0);
+    w.tb = 0;
+    w.te = (w.L + kTile - 1) / kTile;
+    return w;
+  }
   if constexpr (MODE == 0) {
     w.L = p.list_len;
     w.list = p.idx + w.bq * p.list_len;
@@ -140,8 +158,9 @@ __device__ __forceinline__ AtcWork atc_work(const AtcParams& p) {
     return w;
   }
   const int64_t T = (w.L + kTile - 1) / kTile;
-  w.tb = w.sp * T / p.n_split;
-  w.te = (w.sp + 1) * T / p.n_split;
+  const int64_t S = p.n_split - (MODE != 2 && p.win ? 1 : 0);  // splits of the compressed list
+  w.tb = w.sp * T / S;
+  w.te = (w.sp + 1) * T / S;
   return w;
 }
 
@@ -149,6 +168,7 @@ __device__ __forceinline__ AtcWork atc_work(const AtcParams& p) {
 template <int MODE>
 __device__ __forceinline__ int64_t atc_row(const AtcParams& p, const AtcWork& w, int64_t pos, bool report) {
   if (pos >= w.L) return -1;
+  if (MODE != 2 && w.win) return w.row0 + pos;
   if constexpr (MODE == 0) {
     const int32_t s = __ldg(w.list + pos);
     if (s == -1) return -1;
@@ -184,8 +204,8 @@ __device__ __forceinline__ int64_t atc_group(int64_t G, int64_t ngroups, bool& i
 // issued alone; warp 0 also gathers so that every slot's phases are waited in
 // order by one warp.  A list shorter than a tile has no TMA tile at all.
 template <int MODE>
-__device__ __forceinline__ int atc_gather_warp(int64_t g, int64_t list_len) {
-  return (MODE == 0 || list_len < kTile) ? (int)(g % kProdWarps) : 0;
+__device__ __forceinline__ int atc_gather_warp(int64_t g, int64_t list_len, bool contiguous) {
+  return (!contiguous || list_len < kTile) ? (int)(g % kProdWarps) : 0;
 }
 
 // Reduce 32 per-lane values (one per head) across the 32 lanes of a warp by
@@ -211,7 +231,8 @@ __device__ __forceinline__ float transpose_reduce32(float (&a)[32], int lane) {
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, AtcParams p) {
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_w,
+                     AtcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_s = smem + kOffQ;
@@ -240,7 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t ntiles = W.te - W.tb;
   // K = V and one tile: O^T reads the K slabs still in the ring (no V group);
   // otherwise the V slabs are loaded again after the next tile's K (see above)
-  const bool reuse = p.alias && ntiles == 1;
+  const bool contig = MODE != 0 || W.win;  // rows are consecutive (TMA tiles where whole)
+  const bool reuse = (p.alias || W.win) && ntiles == 1;
   const int64_t ngroups = reuse ? 1 : 2 * ntiles;
   // O^T chunks (128 dims each) this CTA computes: a split window merge takes 4/n_split of them
   const int ch0 = MODE == 2 ? (int)W.sp * (4 / p.n_split) : 0;
@@ -248,7 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // the first group's loads are issued by the thread that initialises the
   // barriers, before the CTA-wide setup sync (overlapping the TMEM allocation)
-  const bool pre_k = MODE != 0 && ntiles > 0 && (W.tb + 1) * kTile <= W.L;
+  const bool pre_k = contig && ntiles > 0 && (W.tb + 1) * kTile <= W.L;
+  const CUtensorMap* tm_k0 = W.win ? &tm_w : &tm_k;  // the key rows' map
   if (threadIdx.x == 0) {
     tc::mbar_init(q_full, 1);
     for (int s = 0; s < kSlabs; ++s) tc::mbar_init(&kv_full[s], 1), tc::mbar_init(&kv_empty[s], 1);
@@ -271,13 +294,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kSlabs; ++s) tc::tma_load_2d(q_s + s * kQSlabBytes, &tm_q, q_full, 64 * s, qrow);
     }
     if (pre_k) {
-      tc::prefetch_tmap(&tm_k);
+      tc::prefetch_tmap(tm_k0);
       for (int s = 0; s < kSlabs; ++s) {
         tc::mbar_arrive_expect_tx(&kv_full[s], kSlabBytes);
-        tc::tma_load_2d(kv_s + s * kSlabBytes, &tm_k, &kv_full[s], 64 * s, (int32_t)(W.row0 + W.tb * kTile));
+        tc::tma_load_2d(kv_s + s * kSlabBytes, tm_k0, &kv_full[s], 64 * s, (int32_t)(W.row0 + W.tb * kTile));
       }
     }
-    if (MODE != 0) tc::prefetch_tmap(&tm_v);
+    if (MODE != 0 && !W.win) tc::prefetch_tmap(&tm_v);
   }
   if (warp == kMmaWarp) tc::tmem_alloc(s_tmem, kTmemCols);
   tc::tc_fence_before();
@@ -298,10 +321,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // loaded, so the loads that later fill the ring pay L2 rather than HBM latency
     auto prefetch_tile = [&](int64_t i) {
       if (i >= W.te) return;
-      if (MODE != 0) {
+      if (contig) {
         if (warp == 0 && lane == 0) {
           const int64_t n = std::min<int64_t>(kTile, W.L - i * kTile);
-          tc::prefetch_l2(p.k + (W.row0 + i * kTile) * kC, (uint32_t)(n * kC * 2));
+          tc::prefetch_l2((W.win ? p.kw : p.k) + (W.row0 + i * kTile) * kC, (uint32_t)(n * kC * 2));
         }
       } else if (warp == 0) {
 #pragma unroll
@@ -318,14 +341,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t li = atc_group(G, ngroups, is_v);
       const int64_t i = W.tb + li;
       if (!is_v && li > 0) prefetch_tile(i + kPrefetchAhead);
-      const bool tma_tile = MODE != 0 && (i + 1) * kTile <= W.L;
+      const bool tma_tile = contig && (i + 1) * kTile <= W.L;
       int64_t rows[4];
       if (!tma_tile) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) rows[r] = atc_row<MODE>(p, W, i * kTile + lane + 32 * r, warp == 0 && !is_v);
       }
-      const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
-      const __nv_bfloat16* src = is_v ? p.v : p.k;
+      const CUtensorMap* tm = W.win ? &tm_w : (is_v ? &tm_v : &tm_k);
+      const __nv_bfloat16* src = W.win ? p.kw : (is_v ? p.v : p.k);
       const uint32_t par = (uint32_t)(G & 1) ^ 1u;  // wait for the release of the slot's previous use
       for (int s = 0; s < kSlabs; ++s, ++g) {
         uint8_t* dst = kv_s + s * kSlabBytes;
@@ -343,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
             if (!ok) break;
           }
-        } else if (atc_gather_warp<MODE>(g, W.L) == warp) {
+        } else if (atc_gather_warp<MODE>(g, W.L, contig) == warp) {
           int okl = 1;
           if (lane == 0) okl = tc::mbar_wait(&kv_empty[s], par, s_abort, 2);
           ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
@@ -872,7 +895,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // every thread: up to 4 items (float4 quads) at once, all splits' loads in flight
           const __nv_bfloat16* po_b = p.part_o + (W.bq * S * p.n_hg + W.hg) * (int64_t)(kHG * kC);
           const int64_t split_stride = (int64_t)p.n_hg * kHG * kC;
-          float* o_b = p.o + (W.bq * p.n_h + W.hg * kHG) * kC;
+          const int64_t o_b = (W.bq * p.n_h + W.hg * kHG) * kC;  // the unit's first output row
           for (int base = i0 + ts; base < i1; base += 4 * kSoftThreads) {
             float4 acc[4];
             int off[4], wi[4];
@@ -904,7 +927,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int it = base + k * kSoftThreads;
               if (it < i1) {
                 const int h = it / kQuads, d = (it - h * kQuads) * 4;
-                *reinterpret_cast<float4*>(o_b + (int64_t)h * kC + d) = acc[k];
+                const int64_t at = o_b + (int64_t)h * kC + d;
+                if (MODE != 2 && p.win && p.out_bf16) {  // fused window merge: the merged output
+                  const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[k].x, acc[k].y);
+                  const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[k].z, acc[k].w);
+                  uint2 pk;
+                  pk.x = *reinterpret_cast<const uint32_t*>(&lo), pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+                  *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + at) = pk;
+                } else {
+                  float* dst = (MODE != 2 && p.win) ? static_cast<float*>(p.out) : p.o;
+                  *reinterpret_cast<float4*>(dst + at) = acc[k];
+                }
               }
             }
           }
@@ -932,6 +965,13 @@ int64_t atc_list_len_max(const AttendJob& j) {
 
 bool attend_tc_supported(const AttendJob& j) {
   if (j.dtype != HYB_BF16 || j.c != kC || j.n_h < kHG || j.n_h % kHG != 0) return false;
+  if (j.win) {
+    // a fused window joins with the list's splits: every CTA of the launch must be
+    // resident at once (at most one per SM), so there must be room for two per unit
+    const int64_t units = j.batch * j.n_q * (j.n_h / kHG);
+    if (j.mode == 2 || units * 2 > kNumSMs || reinterpret_cast<uintptr_t>(j.wk) % 16 != 0) return false;
+    if (j.batch * j.w_stride >= (int64_t(1) << 31)) return false;
+  }
   const uintptr_t al = reinterpret_cast<uintptr_t>(j.q) | reinterpret_cast<uintptr_t>(j.k) |
                        reinterpret_cast<uintptr_t>(j.v);
   if (al % 16 != 0) return false;
@@ -962,11 +1002,12 @@ AtcPlan atc_plan(const AttendJob& j) {
   }
   const int64_t T = (atc_list_len_max(j) + kTile - 1) / kTile;
   const int64_t units = j.batch * j.n_q * (j.n_h / kHG);
-  int64_t s = kNumSMs / std::max<int64_t>(units, 1);
-  s = std::min<int64_t>(std::min<int64_t>(s, T), kMaxSplits);
-  if (s <= 1) return {1};
+  const int w = j.win ? 1 : 0;  // a fused window is one more split, the last
+  int64_t s = kNumSMs / std::max<int64_t>(units, 1) - w;
+  s = std::min<int64_t>(std::min<int64_t>(s, T), kMaxSplits - w);
+  if (s <= 1) return {1 + w};
   const int64_t per = (T + s - 1) / s;  // tiles per split
-  return {(int)((T + per - 1) / per)};
+  return {(int)((T + per - 1) / per) + w};
 }
 
 }  // namespace
@@ -997,6 +1038,9 @@ cudaError_t launch_attend_tc(const AttendJob& j, void* ws, cudaStream_t s) {
   p.alias = j.k == j.v;
   p.scale_log2 = j.scale * kLog2e;
   p.dev_status = j.dev_status;
+  p.win = j.win;
+  p.kw = static_cast<const __nv_bfloat16*>(j.wk);
+  p.w_stride = j.w_stride, p.w_pos0 = j.w_pos0, p.wq_pos0 = j.wq_pos0;
   const int64_t rows = j.batch * j.n_q;
   if (p.n_split > 1 && j.mode != 2) {
     const size_t n = (size_t)(rows * p.n_split * j.n_h);
@@ -1006,7 +1050,7 @@ cudaError_t launch_attend_tc(const AttendJob& j, void* ws, cudaStream_t s) {
   }
   const uint64_t kv_rows = (uint64_t)(j.batch * j.kv_stride);
   const uint32_t box_rows = kv_rows < (uint64_t)kTile ? (uint32_t)kv_rows : (uint32_t)kTile;
-  CUtensorMap tm_q, tm_k, tm_v;
+  CUtensorMap tm_q, tm_k, tm_v, tm_w;
   if (!encode_tmap_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, j.q, kC, (uint64_t)(rows * j.n_h), kC * 2, 64, kHG,
                       CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tmap_2d(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, j.k, kC, kv_rows, kC * 2, 64, box_rows,
@@ -1014,6 +1058,14 @@ cudaError_t launch_attend_tc(const AttendJob& j, void* ws, cudaStream_t s) {
       !encode_tmap_2d(&tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, j.v, kC, kv_rows, kC * 2, 64, box_rows,
                       CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  tm_w = tm_k;  // (unused without a fused window)
+  if (j.win) {
+    const uint64_t w_rows = (uint64_t)(j.batch * j.w_stride);
+    const uint32_t w_box = w_rows < (uint64_t)kTile ? (uint32_t)w_rows : (uint32_t)kTile;
+    if (!encode_tmap_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, j.wk, kC, w_rows, kC * 2, 64, w_box,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   const int64_t grid = rows * p.n_split * p.n_hg;
   if (grid >= (int64_t(1) << 31)) return cudaErrorInvalidConfiguration;
   cudaError_t e;
@@ -1023,7 +1075,8 @@ cudaError_t launch_attend_tc(const AttendJob& j, void* ws, cudaStream_t s) {
   auto run = [&](auto kernel) {
     cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (r != cudaSuccess) return r;
-    return launch_pdl(kernel, dim3((unsigned)grid), dim3(kThreads), (size_t)kSmemBytes, s, tm_q, tm_k, tm_v, p);
+    return launch_pdl(kernel, dim3((unsigned)grid), dim3(kThreads), (size_t)kSmemBytes, s, tm_q, tm_k, tm_v, tm_w,
+                      p);
   };
   switch (j.mode) {
     case 0:

@@ -1,6 +1,7 @@
 // hyb_api.cu -- the C ABI declared in include/hyb.h: host-side argument
 // validation (before any launch), workspace sizing, dispatch to the kernels
 // and error reporting.  No device memory is allocated here.
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -296,8 +297,86 @@ static hyb_status run_attend(const char* name, const hyb::AttendJob& j, void* wo
   return cuda_status(hyb::launch_attend_cc(j, workspace, s), name);
 }
 
+// ------------------------------------------------- fused window merge
+
+static hyb::AttendJob fused_job(hyb::AttendJob j, const hyb_window* w) {
+  j.win = 1, j.wk = w->kw, j.w_stride = w->n_kv, j.w_pos0 = w->kv_pos0, j.wq_pos0 = w->q_pos0, j.n_win = w->n_win;
+  j.out = w->out, j.out_bf16 = w->out_dtype == HYB_BF16, j.o = nullptr;
+  return j;
+}
+
+// the two-step fallback's window merge over the compressed result (o_in, lse_in)
+static hyb::AttendJob window_merge_job(const hyb::AttendJob& c, const hyb_window* w, const float* o_in,
+                                       const float* lse_in, float* lse_out) {
+  hyb::AttendJob j{};
+  j.mode = 2, j.q = c.q, j.k = w->kw, j.v = w->kw, j.o_in = o_in, j.lse_in = lse_in, j.out = w->out;
+  j.out_bf16 = w->out_dtype == HYB_BF16, j.lse = lse_out;
+  j.batch = c.batch, j.n_q = c.n_q, j.n_h = c.n_h, j.c = c.c, j.n_entries = w->n_kv, j.kv_stride = w->n_kv;
+  j.kv_pos0 = w->kv_pos0, j.q_pos0 = w->q_pos0, j.n_win = w->n_win;
+  j.scale = c.scale, j.dtype = c.dtype, j.dev_status = c.dev_status;
+  return j;
+}
+
+static size_t fallback_io_bytes(const hyb::AttendJob& c) {
+  const size_t n = (size_t)(c.batch * c.n_q * c.n_h);
+  return round_up(n * (size_t)c.c * sizeof(float), 256) + round_up(n * sizeof(float), 256);
+}
+
+static size_t attend_window_workspace(const hyb::AttendJob& c, const hyb_window* w) {
+  const hyb::AttendJob f = fused_job(c, w);
+  if (hyb::attend_tc_supported(f)) return hyb::attend_tc_workspace_bytes(f);
+  const hyb::AttendJob m = window_merge_job(c, w, nullptr, nullptr, nullptr);
+  return fallback_io_bytes(c) + std::max(attend_workspace(c), attend_workspace(m));
+}
+
+static hyb_status validate_window(const char* name, const hyb::AttendJob& c, const hyb_window* w) {
+  if (w->n_win < 1 || w->q_pos0 < 0 || w->kv_pos0 < 0 || w->n_kv < 0)
+    return fail(HYB_ERR_INVALID_ARG, "%s: window n_win < 1 or negative position", name);
+  if (w->out_dtype != HYB_F32 && w->out_dtype != HYB_BF16)
+    return fail(HYB_ERR_INVALID_ARG, "%s: window out_dtype must be F32 or BF16", name);
+  if (c.mode == 1 && w->q_pos0 != c.q_pos0)
+    return fail(HYB_ERR_INVALID_ARG, "%s: window q_pos0 %lld differs from q_pos0 %lld", name, (long long)w->q_pos0,
+                (long long)c.q_pos0);
+  if (c.batch == 0 || c.n_q == 0 || c.n_h == 0) return ok();
+  const int64_t lo = w->q_pos0 - w->n_win + 1 > 0 ? w->q_pos0 - w->n_win + 1 : 0;
+  const int64_t hi = w->q_pos0 + c.n_q - 1;
+  if (lo < w->kv_pos0 || hi >= w->kv_pos0 + w->n_kv)
+    return fail(HYB_ERR_INVALID_ARG, "%s: window rows %lld..%lld are not all inside the buffer %lld..%lld", name,
+                (long long)lo, (long long)hi, (long long)w->kv_pos0, (long long)(w->kv_pos0 + w->n_kv - 1));
+  if (!w->kw || !w->out) return fail(HYB_ERR_INVALID_ARG, "%s: NULL window kw/out", name);
+  if (!aligned(w->kw, lane_align(c.c, c.dtype)) || !aligned(w->out, lane_align(c.c, w->out_dtype)))
+    return fail(HYB_ERR_INVALID_ARG, "%s: misaligned window kw/out", name);
+  return ok();
+}
+
+// c: the compressed-branch job (its o unused), lse: the union's lse
+static hyb_status run_attend_window(const char* name, hyb::AttendJob c, const hyb_window* w, void* workspace,
+                                    size_t ws_bytes, void* stream) {
+  const size_t need = attend_window_workspace(c, w);
+  if (need > 0 && (!workspace || ws_bytes < need))
+    return fail(HYB_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", name, need, ws_bytes);
+  if (!aligned(workspace, 256)) return fail(HYB_ERR_WORKSPACE, "%s: workspace must be 256-byte aligned", name);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const hyb::AttendJob f = fused_job(c, w);
+  if (hyb::attend_tc_supported(f)) return cuda_status(hyb::launch_attend_tc(f, workspace, s), name);
+  // two steps: the compressed branch into the workspace, then the window merge
+  const size_t n = (size_t)(c.batch * c.n_q * c.n_h);
+  char* base = static_cast<char*>(workspace);
+  float* o_tmp = reinterpret_cast<float*>(base);
+  float* lse_tmp = reinterpret_cast<float*>(base + round_up(n * (size_t)c.c * sizeof(float), 256));
+  void* rest = base + fallback_io_bytes(c);
+  float* lse_out = c.lse;
+  c.o = o_tmp, c.lse = lse_tmp;
+  cudaError_t e = hyb::attend_tc_supported(c) ? hyb::launch_attend_tc(c, rest, s) : hyb::launch_attend_cc(c, rest, s);
+  if (e != cudaSuccess) return cuda_status(e, name);
+  const hyb::AttendJob m = window_merge_job(c, w, o_tmp, lse_tmp, lse_out);
+  e = hyb::attend_tc_supported(m) ? hyb::launch_attend_tc(m, rest, s) : hyb::launch_attend_cc(m, rest, s);
+  return cuda_status(e, name);
+}
+
 size_t csa_attend_workspace_size(const hyb_csa_attend_args* a) {
   if (!a || a->batch <= 0 || a->n_q <= 0 || a->n_h <= 0) return 0;
+  if (a->window) return attend_window_workspace(csa_job(a), a->window);
   return attend_workspace(csa_job(a));
 }
 
@@ -307,15 +386,19 @@ hyb_status csa_attend(const hyb_csa_attend_args* a, void* workspace, size_t ws_b
   if (st != HYB_OK) return st;
   if (a->k < 0 || a->n_entries < 0 || a->kv_stride < 0) return fail(HYB_ERR_INVALID_ARG, "csa_attend: negative size");
   if (a->kv_stride != 0 && a->kv_stride < a->n_entries) return fail(HYB_ERR_INVALID_ARG, "csa_attend: kv_stride < n_entries");
+  if (a->window && (st = validate_window("csa_attend", csa_job(a), a->window)) != HYB_OK) return st;
   if (a->batch == 0 || a->n_q == 0 || a->n_h == 0) return ok();
-  if (!a->o || !a->lse || (a->k > 0 && !a->idx)) return fail(HYB_ERR_INVALID_ARG, "csa_attend: NULL o/lse/idx");
+  if ((!a->o && !a->window) || !a->lse || (a->k > 0 && !a->idx))
+    return fail(HYB_ERR_INVALID_ARG, "csa_attend: NULL o/lse/idx");
   if (!aligned(a->o, lane_align(a->c, HYB_F32)) || !aligned(a->idx, 4) || !aligned(a->lse, 4))
     return fail(HYB_ERR_INVALID_ARG, "csa_attend: misaligned o/lse/idx");
+  if (a->window) return run_attend_window("csa_attend", csa_job(a), a->window, workspace, ws_bytes, stream);
   return run_attend("csa_attend", csa_job(a), workspace, ws_bytes, stream);
 }
 
 size_t hca_attend_workspace_size(const hyb_hca_attend_args* a) {
   if (!a || a->batch <= 0 || a->n_q <= 0 || a->n_h <= 0 || a->m < 1) return 0;
+  if (a->window) return attend_window_workspace(hca_job(a), a->window);
   return attend_workspace(hca_job(a));
 }
 
@@ -329,10 +412,12 @@ hyb_status hca_attend(const hyb_hca_attend_args* a, void* workspace, size_t ws_b
   if (a->n_q > 0 && hyb::visible_entries(a->q_pos0 + a->n_q - 1, a->m) > a->n_entries)
     return fail(HYB_ERR_INVALID_ARG, "hca_attend: the last query sees %lld entries but only %lld exist",
                 (long long)hyb::visible_entries(a->q_pos0 + a->n_q - 1, a->m), (long long)a->n_entries);
+  if (a->window && (st = validate_window("hca_attend", hca_job(a), a->window)) != HYB_OK) return st;
   if (a->batch == 0 || a->n_q == 0 || a->n_h == 0) return ok();
-  if (!a->o || !a->lse) return fail(HYB_ERR_INVALID_ARG, "hca_attend: NULL o/lse");
+  if ((!a->o && !a->window) || !a->lse) return fail(HYB_ERR_INVALID_ARG, "hca_attend: NULL o/lse");
   if (!aligned(a->o, lane_align(a->c, HYB_F32)) || !aligned(a->lse, 4))
     return fail(HYB_ERR_INVALID_ARG, "hca_attend: misaligned o/lse");
+  if (a->window) return run_attend_window("hca_attend", hca_job(a), a->window, workspace, ws_bytes, stream);
   return run_attend("hca_attend", hca_job(a), workspace, ws_bytes, stream);
 }
 

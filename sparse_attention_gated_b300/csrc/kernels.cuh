@@ -51,6 +51,12 @@ struct AttendJob {
   float scale;
   int dtype;
   int32_t* dev_status;
+  // modes 0/1: fused window merge (see hyb_window): raw rows wk [batch][w_stride][c] at
+  // absolute positions w_pos0.., query 0 at wq_pos0; out / out_bf16 / n_win as in mode 2;
+  // lse then receives the union's lse and o is not written
+  int win;
+  const void* wk;
+  int64_t w_stride, w_pos0, wq_pos0;
 };
 bool attend_cc_shape_supported(int64_t c, int64_t n_h);
 

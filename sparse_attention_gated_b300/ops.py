@@ -145,7 +145,17 @@ def csa_index_topk(qI, w, kI, *, m: int, k: int, q_pos0: int, qI_scale=None, kI_
 # ---------------------------------------------------------------- attention
 
 
-def csa_attend_args(q, kc, vc, idx, scale, o, lse, n_entries=None, dev_status=None):
+def window_args(kw, *, kv_pos0: int, q_pos0: int, n_win: int, out):
+    """The fused window merge of csa_attend / hca_attend (hyb_window): the raw rows kw
+    [B, n_kv, c] (row 0 = absolute position kv_pos0) are the window's keys and values;
+    out [B, n_q, n_h, c] receives the merged output."""
+    w = _abi.Window()
+    w.kw, w.n_kv, w.kv_pos0, w.q_pos0, w.n_win = _ptr(kw), kw.shape[1], kv_pos0, q_pos0, n_win
+    w.out, w.out_dtype = _ptr(out), _dtype(out)
+    return w
+
+
+def csa_attend_args(q, kc, vc, idx, scale, o, lse, n_entries=None, dev_status=None, window=None):
     B, n_q, n_h, c = q.shape
     a = _abi.CsaAttendArgs()
     a.q, a.kc, a.vc, a.idx, a.o, a.lse = _ptr(q), _ptr(kc), _ptr(vc), _ptr(idx), _ptr(o), _ptr(lse)
@@ -156,24 +166,42 @@ def csa_attend_args(q, kc, vc, idx, scale, o, lse, n_entries=None, dev_status=No
     a.scale = scale
     a.dtype = _dtype(q)
     a.dev_status = _ptr(dev_status)
+    a._window = window  # keep the struct alive as long as the arguments
+    a.window = ctypes.cast(ctypes.pointer(window), ctypes.c_void_p) if window is not None else None
     return a
 
 
+def _window(q, window):
+    """window: None or dict(kw=, kv_pos0=, q_pos0=, n_win=, out= (optional), out_dtype= (optional))."""
+    if window is None:
+        return None, None
+    w = dict(window)
+    out = w.pop("out", None)
+    if out is None:
+        B, n_q, n_h, c = q.shape
+        out = torch.empty((B, n_q, n_h, c), dtype=w.pop("out_dtype", None) or q.dtype, device=q.device)
+    w.pop("out_dtype", None)
+    return window_args(w.pop("kw"), out=out, **w), out
+
+
 def csa_attend(q, kc, vc, idx, *, scale: float | None = None, n_entries=None, o=None, lse=None, workspace=None,
-               dev_status=None, stream=None):
-    """CSA core attention over the selected entries.  Returns (o, lse)."""
+               dev_status=None, stream=None, window=None):
+    """CSA core attention over the selected entries.  Returns (o, lse), or (out, lse) of the
+    union with a fused window merge (window=dict(kw, kv_pos0, q_pos0, n_win[, out]))."""
     B, n_q, n_h, c = q.shape
     scale = 1.0 / math.sqrt(c) if scale is None else scale
-    o = torch.empty((B, n_q, n_h, c), dtype=torch.float32, device=q.device) if o is None else o
+    w, out = _window(q, window)
+    if o is None and w is None:
+        o = torch.empty((B, n_q, n_h, c), dtype=torch.float32, device=q.device)
     lse = torch.empty((B, n_q, n_h), dtype=torch.float32, device=q.device) if lse is None else lse
-    a = csa_attend_args(q, kc, vc, idx, scale, o, lse, n_entries, dev_status)
+    a = csa_attend_args(q, kc, vc, idx, scale, o, lse, n_entries, dev_status, w)
     lib = _abi.load()
     ws, nbytes = _workspace(int(lib.csa_attend_workspace_size(ctypes.byref(a))), workspace, q.device)
     _abi.check(lib.csa_attend(ctypes.byref(a), ws, nbytes, _stream(stream)), "csa_attend")
-    return o, lse
+    return (out, lse) if w is not None else (o, lse)
 
 
-def hca_attend_args(q, kc, vc, m, q_pos0, scale, o, lse, n_entries=None, dev_status=None):
+def hca_attend_args(q, kc, vc, m, q_pos0, scale, o, lse, n_entries=None, dev_status=None, window=None):
     B, n_q, n_h, c = q.shape
     a = _abi.HcaAttendArgs()
     a.q, a.kc, a.vc, a.o, a.lse = _ptr(q), _ptr(kc), _ptr(vc), _ptr(o), _ptr(lse)
@@ -183,21 +211,28 @@ def hca_attend_args(q, kc, vc, m, q_pos0, scale, o, lse, n_entries=None, dev_sta
     a.m, a.q_pos0, a.scale = m, q_pos0, scale
     a.dtype = _dtype(q)
     a.dev_status = _ptr(dev_status)
+    a._window = window
+    a.window = ctypes.cast(ctypes.pointer(window), ctypes.c_void_p) if window is not None else None
     return a
 
 
 def hca_attend(q, kc, vc, *, m: int, q_pos0: int, scale: float | None = None, n_entries=None, o=None, lse=None,
-               workspace=None, dev_status=None, stream=None):
-    """HCA core attention over every visible entry.  Returns (o, lse)."""
+               workspace=None, dev_status=None, stream=None, window=None):
+    """HCA core attention over every visible entry.  Returns (o, lse), or (out, lse) of the
+    union with a fused window merge (window=dict(kw, kv_pos0, n_win[, out]); q_pos0 as the call's)."""
     B, n_q, n_h, c = q.shape
     scale = 1.0 / math.sqrt(c) if scale is None else scale
-    o = torch.empty((B, n_q, n_h, c), dtype=torch.float32, device=q.device) if o is None else o
+    if window is not None and "q_pos0" not in window:
+        window = dict(window, q_pos0=q_pos0)
+    w, out = _window(q, window)
+    if o is None and w is None:
+        o = torch.empty((B, n_q, n_h, c), dtype=torch.float32, device=q.device)
     lse = torch.empty((B, n_q, n_h), dtype=torch.float32, device=q.device) if lse is None else lse
-    a = hca_attend_args(q, kc, vc, m, q_pos0, scale, o, lse, n_entries, dev_status)
+    a = hca_attend_args(q, kc, vc, m, q_pos0, scale, o, lse, n_entries, dev_status, w)
     lib = _abi.load()
     ws, nbytes = _workspace(int(lib.hca_attend_workspace_size(ctypes.byref(a))), workspace, q.device)
     _abi.check(lib.hca_attend(ctypes.byref(a), ws, nbytes, _stream(stream)), "hca_attend")
-    return o, lse
+    return (out, lse) if w is not None else (o, lse)
 
 
 def swa_args(q, kw, vw, kv_pos0, q_pos0, n_win, scale, o_in, lse_in, out, lse_out, dev_status=None):

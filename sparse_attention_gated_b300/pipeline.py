@@ -25,8 +25,13 @@ from .workloads import Workload
 
 
 class HybridStep:
-    def __init__(self, w: Workload, inputs: dict):
+    def __init__(self, w: Workload, inputs: dict, fuse_window: bool = True):
+        """fuse_window: the sliding-window merge rides on the attention call (csa_attend /
+        hca_attend with a window: one launch where the whole launch fits the GPU at once;
+        `out` and `lse` then hold the merged result and `o` is not written); False runs
+        swa_merge as its own call after the attention."""
         self.w = w
+        self.fuse_window = fuse_window
         self.x = inputs
         dev = inputs["q" if "q" in inputs else "q_h"].device
         self.device = dev
@@ -76,15 +81,36 @@ class HybridStep:
             a = ops.index_args(x["qI"], x["w"], kI, w.m, w.k, w.q_pos0, x.get("qI_scale"), kIs, b["idx"], None)
             n = ops.csa_index_topk_workspace_size(a)
             self.ws["index"] = torch.empty(max(n, 1), dtype=torch.uint8, device=self.device)
-            a = ops.csa_attend_args(x["q"], kc, kc, b["idx"], w.scale, b["o"], b["lse"])
+            a = ops.csa_attend_args(x["q"], kc, kc, b["idx"], w.scale, b["o"], b["lse"], window=self._win_csa())
             n = int(ops._abi.load().csa_attend_workspace_size(a))
             self.ws["csa"] = torch.empty(max(n, 1), dtype=torch.uint8, device=self.device)
         if self.has_hca:
             kc = self._hca_cache()
             q = x["q_h"] if w.kind == "hybrid_decode" else x["q"]
-            a = ops.hca_attend_args(q, kc, kc, w.m_hca, w.q_pos0, w.scale, b["o_h"], b["lse_h"])
+            a = ops.hca_attend_args(q, kc, kc, w.m_hca, w.q_pos0, w.scale, b["o_h"], b["lse_h"],
+                                    window=self._win_hca())
             n = int(ops._abi.load().hca_attend_workspace_size(a))
             self.ws["hca"] = torch.empty(max(n, 1), dtype=torch.uint8, device=self.device)
+
+    def _kv_pos0(self):
+        return self.w.n_ctx - self.w.n_win if self.w.decode else 0
+
+    def _win_csa(self, as_dict=False):
+        if not self.fuse_window:
+            return None
+        d = dict(kw=self.x["kv"], kv_pos0=self._kv_pos0(), q_pos0=self.w.q_pos0, n_win=self.w.n_win, out=self.buf["out"])
+        if as_dict:
+            return d
+        return ops.window_args(d.pop("kw"), **d)
+
+    def _win_hca(self, as_dict=False):
+        if not self.fuse_window:
+            return None
+        kv = self.x["kv_h"] if self.w.kind == "hybrid_decode" else self.x["kv"]
+        d = dict(kw=kv, kv_pos0=self._kv_pos0(), q_pos0=self.w.q_pos0, n_win=self.w.n_win, out=self.buf["out_h"])
+        if as_dict:
+            return d
+        return ops.window_args(d.pop("kw"), **d)
 
     # ------------------------------------------------------------ stages
     def run_csa(self, stream=None):
@@ -106,10 +132,11 @@ class HybridStep:
         ops.csa_index_topk(x["qI"], x["w"], kI, m=w.m, k=w.k, q_pos0=w.q_pos0, qI_scale=x.get("qI_scale"),
                            kI_scale=kIs, idx=b["idx"], workspace=self.ws["index"], dev_status=st, stream=stream)
         ops.csa_attend(x["q"], kc, kc, b["idx"], scale=w.scale, o=b["o"], lse=b["lse"], workspace=self.ws["csa"],
-                       dev_status=st, stream=stream)
-        kv_pos0 = w.n_ctx - w.n_win if w.decode else 0
-        ops.swa_merge(x["q"], x["kv"], x["kv"], kv_pos0=kv_pos0, q_pos0=w.q_pos0, n_win=w.n_win, scale=w.scale,
-                      o_in=b["o"], lse_in=b["lse"], out=b["out"], dev_status=st, stream=stream)
+                       dev_status=st, stream=stream, window=self._win_csa(as_dict=True))
+        if not self.fuse_window:
+            ops.swa_merge(x["q"], x["kv"], x["kv"], kv_pos0=self._kv_pos0(), q_pos0=w.q_pos0, n_win=w.n_win,
+                          scale=w.scale, o_in=b["o"], lse_in=b["lse"], out=b["out"], dev_status=st,
+                          stream=stream)
 
     def run_hca(self, stream=None):
         w, x, b = self.w, self.x, self.buf
@@ -124,10 +151,10 @@ class HybridStep:
         else:
             ops.hyb_compress(x["ch"], x["zh"], x["bias_h"], w.m_hca, out=kc, dev_status=st, stream=stream)
         ops.hca_attend(q, kc, kc, m=w.m_hca, q_pos0=w.q_pos0, scale=w.scale, o=b["o_h"], lse=b["lse_h"],
-                       workspace=self.ws["hca"], dev_status=st, stream=stream)
-        kv_pos0 = w.n_ctx - w.n_win if w.decode else 0
-        ops.swa_merge(q, kv, kv, kv_pos0=kv_pos0, q_pos0=w.q_pos0, n_win=w.n_win, scale=w.scale, o_in=b["o_h"],
-                      lse_in=b["lse_h"], out=b["out_h"], dev_status=st, stream=stream)
+                       workspace=self.ws["hca"], dev_status=st, stream=stream, window=self._win_hca(as_dict=True))
+        if not self.fuse_window:
+            ops.swa_merge(q, kv, kv, kv_pos0=self._kv_pos0(), q_pos0=w.q_pos0, n_win=w.n_win, scale=w.scale,
+                          o_in=b["o_h"], lse_in=b["lse_h"], out=b["out_h"], dev_status=st, stream=stream)
 
     def run(self, stream=None):
         if self.has_csa:

@@ -212,3 +212,62 @@ def test_two_stage_topk_is_bit_exact_with_ties(B, n_q, N, k):
     for b in range(B):
         for j in range(n_q):
             assert np.array_equal(gs[b, j], ref[b, j, want[b, j]].astype(np.float32))
+
+
+# ------------------------------------------------------- fused window merge
+
+
+def _fused_case(g, B, n_q, n_h, n_kv, c=512):
+    q = _randn(g, (B, n_q, n_h, c))
+    kv = _randn(g, (B, n_kv, c), 1 / math.sqrt(c))
+    return q, kv
+
+
+@pytest.mark.parametrize("B,n_q,n_h,N,k,n_win,q_pos0,n_kv,out_dtype", [
+    (4, 1, 128, 20000, 1024, 128, 80000 - 1, 128, torch.bfloat16),  # decode: the window is one more split
+    (2, 1, 64, 3000, 512, 100, 11999, 300, torch.float32),          # window not a tile, float32 out
+    (2, 1, 128, 500, 256, 128, 40, 41, torch.bfloat16),              # window cut by the sequence start
+    (1, 80, 128, 4000, 256, 128, 15000, 300, torch.bfloat16),        # too many units to fuse: two steps
+])
+def test_csa_attend_with_fused_window(B, n_q, n_h, N, k, n_win, q_pos0, n_kv, out_dtype):
+    g = _gen(11)
+    c = 512
+    q, kv = _fused_case(g, B, n_q, n_h, n_kv)
+    kc = _randn(g, (B, N, c), 1 / math.sqrt(c))
+    idx = torch.sort(torch.randint(0, N, (B, n_q, k), generator=g), dim=-1).values.int()
+    idx[0, 0, -7:] = -1  # some padding
+    kv_pos0 = q_pos0 + n_q - n_kv
+    scale = 1 / math.sqrt(c)
+    st = _status()
+    out, lse = _ops().csa_attend(q.to(DEV), kc.to(DEV), kc.to(DEV), idx.to(DEV), scale=scale, dev_status=st,
+                                 window=dict(kw=kv.to(DEV), kv_pos0=kv_pos0, q_pos0=q_pos0, n_win=n_win,
+                                             out_dtype=out_dtype))
+    torch.cuda.synchronize()
+    assert st.item() == 0, f"device status {st.item()}"
+    o, l = oracle.csa_attend(q, kc, kc, idx.numpy(), scale)
+    ro, rl = oracle.swa_merge(q, kv, kv, kv_pos0, q_pos0, n_win, scale, o, l)
+    assert max_abs(to_np(out), ro) <= TOL_BF16
+    assert max_abs(to_np(lse), rl) <= TOL_BF16
+
+
+@pytest.mark.parametrize("B,n_q,n_h,N,m,q_pos0,n_win,n_kv", [
+    (4, 1, 128, 8192, 128, 8192 * 128 - 1, 128, 128),  # 1M-context HCA decode + window in one launch
+    (2, 1, 64, 300, 16, 300 * 16 - 5, 128, 200),       # ragged list, window at the end of the buffer
+    (1, 1, 128, 3, 128, 400, 128, 401),                # a few entries, window from the sequence start
+])
+def test_hca_attend_with_fused_window(B, n_q, n_h, N, m, q_pos0, n_win, n_kv):
+    g = _gen(12)
+    c = 512
+    q, kv = _fused_case(g, B, n_q, n_h, n_kv)
+    kc = _randn(g, (B, N, c), 1 / math.sqrt(c))
+    kv_pos0 = q_pos0 + n_q - n_kv
+    scale = 1 / math.sqrt(c)
+    st = _status()
+    out, lse = _ops().hca_attend(q.to(DEV), kc.to(DEV), kc.to(DEV), m=m, q_pos0=q_pos0, scale=scale, dev_status=st,
+                                 window=dict(kw=kv.to(DEV), kv_pos0=kv_pos0, n_win=n_win))
+    torch.cuda.synchronize()
+    assert st.item() == 0, f"device status {st.item()}"
+    o, l = oracle.hca_attend(q, kc, kc, m=m, q_pos0=q_pos0, scale=scale)
+    ro, rl = oracle.swa_merge(q, kv, kv, kv_pos0, q_pos0, n_win, scale, o, l)
+    assert max_abs(to_np(out), ro) <= TOL_BF16
+    assert max_abs(to_np(lse), rl) <= TOL_BF16
