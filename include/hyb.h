@@ -278,6 +278,11 @@ typedef struct hyb_csa_attend_args {
   const hyb_window* window; /* optional fused window merge (see hyb_window), or NULL */
 } hyb_csa_attend_args;
 
+/* Workspace of csa_attend and hca_attend: *_workspace_size(a) bytes, 256-byte
+   aligned.  Its first 1024 bytes hold counters that must be zero before the
+   first call that uses the workspace; every call leaves them zero again (the
+   rest is scratch), so a caller zero-fills a workspace once, when it allocates
+   it.  After a call that reported HYB_DEV_TIMEOUT, zero-fill it again. */
 HYB_API size_t csa_attend_workspace_size(const hyb_csa_attend_args* a);
 HYB_API hyb_status csa_attend(const hyb_csa_attend_args* a, void* workspace, size_t ws_bytes, void* stream);
 

@@ -62,6 +62,10 @@ constexpr int kSlabs = kC / 64;         // column slabs of 64 dims (128 bytes) p
 constexpr int kSlabBytes = kTile * 128;  // 16 KiB
 constexpr int kQSlabBytes = kHG * 128;   // 8 KiB
 constexpr int kMaxSplits = 64;         // splits of one (query, head group) list
+// join counters at the start of the workspace: arrivals and departures of up to
+// kMaxJoinUnits (query, head group) units; a launch with splits has at most one CTA
+// per SM and at least two per unit
+constexpr int kMaxJoinUnits = kNumSMs / 2;
 constexpr int kOffQ = 0;
 constexpr int kOffKV = kOffQ + kSlabs * kQSlabBytes;
 constexpr int kOffP = kOffKV + kSlabs * kSlabBytes;
@@ -91,7 +95,7 @@ struct AtcParams {
   float* o;                 // modes 0/1, one split: [rows][n_h][c]
   float* lse;               // [rows][n_h]
   __nv_bfloat16* part_o;    // modes 0/1, several splits: [rows][n_split][n_hg][4][64][128] (chunk-major)
-  uint32_t* join_cnt;       // modes 0/1, several splits: [rows * n_hg] splits done (zeroed per launch)
+  uint32_t* join_cnt;       // modes 0/1, several splits: [2][units] arrivals and departures (start and end at 0)
   float2* part_ml;          // [rows][n_split][n_h] (reference m in log2 units, denominator)
   const float* o_in;        // mode 2
   const float* lse_in;
@@ -846,17 +850,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       ok = ok && all_sync();
       if (ok && ts == 0) {
-        uint32_t* cnt = p.join_cnt + W.bq * p.n_hg + W.hg;
+        const int64_t unit = W.bq * p.n_hg + W.hg;
+        uint32_t* cnt = p.join_cnt + unit;
+        uint32_t* dep = p.join_cnt + kMaxJoinUnits + unit;
         __threadfence();
         atomicAdd(cnt, 1u);
         const long long t0 = clock64();
+        bool joined = true;
         while (tc::ld_acquire_gpu_u32(cnt) < (uint32_t)S) {
           if (clock64() - t0 > tc::kWaitLimitCycles) {
             *s_abort = 18;
+            joined = false;
             break;
           }
         }
         __threadfence();
+        // the last split past the barrier puts both counters back to zero for the next call
+        // (every split has seen all arrivals before it counts its departure)
+        if (joined && atomicAdd(dep, 1u) == (uint32_t)(S - 1)) {
+          atomicExch(cnt, 0u);
+          atomicExch(dep, 0u);
+        }
       }
       ok = ok && all_sync() && *s_abort == 0;
       if (ok) {
@@ -1016,10 +1030,10 @@ int attend_tc_splits(const AttendJob& j) { return atc_plan(j).n_split; }
 
 size_t attend_tc_workspace_bytes(const AttendJob& j) {
   const AtcPlan pl = atc_plan(j);
-  if (pl.n_split <= 1 || j.mode == 2) return 0;
+  if (j.mode == 2) return 0;
+  if (pl.n_split <= 1) return kJoinRegionBytes;
   const size_t n = (size_t)(j.batch * j.n_q * pl.n_split * j.n_h);
-  const size_t units = (size_t)(j.batch * j.n_q * (j.n_h / kHG));
-  return n * (size_t)kC * sizeof(__nv_bfloat16) + n * sizeof(float2) + units * sizeof(uint32_t) + 256;
+  return kJoinRegionBytes + n * (size_t)kC * sizeof(__nv_bfloat16) + n * sizeof(float2) + 256;
 }
 
 cudaError_t launch_attend_tc(const AttendJob& j, void* ws, cudaStream_t s) {
@@ -1043,10 +1057,12 @@ cudaError_t launch_attend_tc(const AttendJob& j, void* ws, cudaStream_t s) {
   p.w_stride = j.w_stride, p.w_pos0 = j.w_pos0, p.wq_pos0 = j.wq_pos0;
   const int64_t rows = j.batch * j.n_q;
   if (p.n_split > 1 && j.mode != 2) {
+    if (rows * p.n_hg > kMaxJoinUnits) return cudaErrorInvalidConfiguration;  // (the plan never does this)
     const size_t n = (size_t)(rows * p.n_split * j.n_h);
-    p.part_o = static_cast<__nv_bfloat16*>(ws);
-    p.part_ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + n * (size_t)kC * sizeof(__nv_bfloat16));
-    p.join_cnt = reinterpret_cast<uint32_t*>(p.part_ml + n);
+    p.join_cnt = static_cast<uint32_t*>(ws);
+    p.part_o = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(ws) + kJoinRegionBytes);
+    p.part_ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + kJoinRegionBytes +
+                                          n * (size_t)kC * sizeof(__nv_bfloat16));
   }
   const uint64_t kv_rows = (uint64_t)(j.batch * j.kv_stride);
   const uint32_t box_rows = kv_rows < (uint64_t)kTile ? (uint32_t)kv_rows : (uint32_t)kTile;
@@ -1069,9 +1085,6 @@ cudaError_t launch_attend_tc(const AttendJob& j, void* ws, cudaStream_t s) {
   const int64_t grid = rows * p.n_split * p.n_hg;
   if (grid >= (int64_t(1) << 31)) return cudaErrorInvalidConfiguration;
   cudaError_t e;
-  if (p.join_cnt != nullptr &&
-      (e = cudaMemsetAsync(p.join_cnt, 0, (size_t)(rows * p.n_hg) * sizeof(uint32_t), s)) != cudaSuccess)
-    return e;
   auto run = [&](auto kernel) {
     cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (r != cudaSuccess) return r;

@@ -282,9 +282,20 @@ static hyb_status validate_attend_common(const char* name, int64_t batch, int64_
 }
 
 // Attention dispatch: the tensor-core kernel for its shapes (bf16, c = 512,
-// heads a multiple of 64), the CUDA-core kernel otherwise.
+// heads a multiple of 64), the CUDA-core kernel otherwise.  The workspace of
+// csa_attend / hca_attend starts with the tensor-core kernel's join counters
+// (kJoinRegionBytes, zero between calls) whichever kernel runs; other scratch
+// follows them.  A standalone window merge has no join.
+static size_t join_region(const hyb::AttendJob& j) { return j.mode == 2 ? 0 : hyb::kJoinRegionBytes; }
+
 static size_t attend_workspace(const hyb::AttendJob& j) {
-  return hyb::attend_tc_supported(j) ? hyb::attend_tc_workspace_bytes(j) : hyb::attend_cc_workspace_bytes(j);
+  return hyb::attend_tc_supported(j) ? hyb::attend_tc_workspace_bytes(j)
+                                     : join_region(j) + hyb::attend_cc_workspace_bytes(j);
+}
+
+static cudaError_t launch_attend(const hyb::AttendJob& j, void* ws, cudaStream_t s) {
+  if (hyb::attend_tc_supported(j)) return hyb::launch_attend_tc(j, ws, s);
+  return hyb::launch_attend_cc(j, static_cast<char*>(ws) + join_region(j), s);
 }
 
 static hyb_status run_attend(const char* name, const hyb::AttendJob& j, void* workspace, size_t ws_bytes, void* stream) {
@@ -292,9 +303,7 @@ static hyb_status run_attend(const char* name, const hyb::AttendJob& j, void* wo
   if (need > 0 && (!workspace || ws_bytes < need))
     return fail(HYB_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", name, need, ws_bytes);
   if (!aligned(workspace, 256)) return fail(HYB_ERR_WORKSPACE, "%s: workspace must be 256-byte aligned", name);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (hyb::attend_tc_supported(j)) return cuda_status(hyb::launch_attend_tc(j, workspace, s), name);
-  return cuda_status(hyb::launch_attend_cc(j, workspace, s), name);
+  return cuda_status(launch_attend(j, workspace, static_cast<cudaStream_t>(stream)), name);
 }
 
 // ------------------------------------------------- fused window merge
@@ -326,7 +335,8 @@ static size_t attend_window_workspace(const hyb::AttendJob& c, const hyb_window*
   const hyb::AttendJob f = fused_job(c, w);
   if (hyb::attend_tc_supported(f)) return hyb::attend_tc_workspace_bytes(f);
   const hyb::AttendJob m = window_merge_job(c, w, nullptr, nullptr, nullptr);
-  return fallback_io_bytes(c) + std::max(attend_workspace(c), attend_workspace(m));
+  return round_up(std::max(attend_workspace(c), hyb::kJoinRegionBytes + attend_workspace(m)), 256) +
+         fallback_io_bytes(c);
 }
 
 static hyb_status validate_window(const char* name, const hyb::AttendJob& c, const hyb_window* w) {
@@ -359,19 +369,20 @@ static hyb_status run_attend_window(const char* name, hyb::AttendJob c, const hy
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const hyb::AttendJob f = fused_job(c, w);
   if (hyb::attend_tc_supported(f)) return cuda_status(hyb::launch_attend_tc(f, workspace, s), name);
-  // two steps: the compressed branch into the workspace, then the window merge
+  // two steps: the compressed branch into the workspace (after the kernels' own
+  // scratch, which keeps the join counters first), then the window merge
   const size_t n = (size_t)(c.batch * c.n_q * c.n_h);
+  const hyb::AttendJob m0 = window_merge_job(c, w, nullptr, nullptr, nullptr);
   char* base = static_cast<char*>(workspace);
-  float* o_tmp = reinterpret_cast<float*>(base);
-  float* lse_tmp = reinterpret_cast<float*>(base + round_up(n * (size_t)c.c * sizeof(float), 256));
-  void* rest = base + fallback_io_bytes(c);
+  char* io = base + round_up(std::max(attend_workspace(c), hyb::kJoinRegionBytes + attend_workspace(m0)), 256);
+  float* o_tmp = reinterpret_cast<float*>(io);
+  float* lse_tmp = reinterpret_cast<float*>(io + round_up(n * (size_t)c.c * sizeof(float), 256));
   float* lse_out = c.lse;
   c.o = o_tmp, c.lse = lse_tmp;
-  cudaError_t e = hyb::attend_tc_supported(c) ? hyb::launch_attend_tc(c, rest, s) : hyb::launch_attend_cc(c, rest, s);
+  cudaError_t e = launch_attend(c, base, s);
   if (e != cudaSuccess) return cuda_status(e, name);
   const hyb::AttendJob m = window_merge_job(c, w, o_tmp, lse_tmp, lse_out);
-  e = hyb::attend_tc_supported(m) ? hyb::launch_attend_tc(m, rest, s) : hyb::launch_attend_cc(m, rest, s);
-  return cuda_status(e, name);
+  return cuda_status(launch_attend(m, base + hyb::kJoinRegionBytes, s), name);  // (the counters stay untouched)
 }
 
 size_t csa_attend_workspace_size(const hyb_csa_attend_args* a) {
@@ -421,7 +432,10 @@ hyb_status hca_attend(const hyb_hca_attend_args* a, void* workspace, size_t ws_b
   return run_attend("hca_attend", hca_job(a), workspace, ws_bytes, stream);
 }
 
-size_t swa_merge_workspace_size(const hyb_swa_args*) { return 0; }
+size_t swa_merge_workspace_size(const hyb_swa_args* a) {
+  if (!a || a->batch <= 0 || a->n_q <= 0 || a->n_h <= 0) return 0;
+  return attend_workspace(swa_job(a));
+}
 
 hyb_status swa_merge(const hyb_swa_args* a, void* workspace, size_t ws_bytes, void* stream) {
   if (!a) return fail(HYB_ERR_INVALID_ARG, "swa_merge: args is NULL");

@@ -7,6 +7,10 @@
 
 namespace hyb {
 
+// Attention workspaces start with this many bytes of join counters, which must be zero
+// before the first call and which every call leaves zero again.
+constexpr size_t kJoinRegionBytes = 1024;
+
 // top-k threshold histogram over the top bits of the order-preserving score keys
 constexpr int kTopkHistBits = 12;
 constexpr int kTopkHistBins = 1 << kTopkHistBits;

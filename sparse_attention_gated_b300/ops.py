@@ -41,11 +41,14 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _workspace(nbytes, workspace, device):
+def _workspace(nbytes, workspace, device, zeroed=False):
+    """zeroed: the call needs the workspace to start zero-filled (csa_attend / hca_attend keep
+    their join counters in its first bytes and leave them zero); a caller's own workspace
+    must then have been zero-filled once."""
     if nbytes == 0:
         return None, 0
     if workspace is None:
-        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        workspace = (torch.zeros if zeroed else torch.empty)(nbytes, dtype=torch.uint8, device=device)
     if workspace.numel() * workspace.element_size() < nbytes:
         raise ValueError(f"workspace holds {workspace.numel() * workspace.element_size()} bytes, {nbytes} needed")
     return _ptr(workspace), workspace.numel() * workspace.element_size()
@@ -196,7 +199,7 @@ def csa_attend(q, kc, vc, idx, *, scale: float | None = None, n_entries=None, o=
     lse = torch.empty((B, n_q, n_h), dtype=torch.float32, device=q.device) if lse is None else lse
     a = csa_attend_args(q, kc, vc, idx, scale, o, lse, n_entries, dev_status, w)
     lib = _abi.load()
-    ws, nbytes = _workspace(int(lib.csa_attend_workspace_size(ctypes.byref(a))), workspace, q.device)
+    ws, nbytes = _workspace(int(lib.csa_attend_workspace_size(ctypes.byref(a))), workspace, q.device, zeroed=True)
     _abi.check(lib.csa_attend(ctypes.byref(a), ws, nbytes, _stream(stream)), "csa_attend")
     return (out, lse) if w is not None else (o, lse)
 
@@ -230,7 +233,7 @@ def hca_attend(q, kc, vc, *, m: int, q_pos0: int, scale: float | None = None, n_
     lse = torch.empty((B, n_q, n_h), dtype=torch.float32, device=q.device) if lse is None else lse
     a = hca_attend_args(q, kc, vc, m, q_pos0, scale, o, lse, n_entries, dev_status, w)
     lib = _abi.load()
-    ws, nbytes = _workspace(int(lib.hca_attend_workspace_size(ctypes.byref(a))), workspace, q.device)
+    ws, nbytes = _workspace(int(lib.hca_attend_workspace_size(ctypes.byref(a))), workspace, q.device, zeroed=True)
     _abi.check(lib.hca_attend(ctypes.byref(a), ws, nbytes, _stream(stream)), "hca_attend")
     return (out, lse) if w is not None else (o, lse)
 

@@ -83,14 +83,14 @@ class HybridStep:
             self.ws["index"] = torch.empty(max(n, 1), dtype=torch.uint8, device=self.device)
             a = ops.csa_attend_args(x["q"], kc, kc, b["idx"], w.scale, b["o"], b["lse"], window=self._win_csa())
             n = int(ops._abi.load().csa_attend_workspace_size(a))
-            self.ws["csa"] = torch.empty(max(n, 1), dtype=torch.uint8, device=self.device)
+            self.ws["csa"] = torch.zeros(max(n, 1), dtype=torch.uint8, device=self.device)  # (join counters)
         if self.has_hca:
             kc = self._hca_cache()
             q = x["q_h"] if w.kind == "hybrid_decode" else x["q"]
             a = ops.hca_attend_args(q, kc, kc, w.m_hca, w.q_pos0, w.scale, b["o_h"], b["lse_h"],
                                     window=self._win_hca())
             n = int(ops._abi.load().hca_attend_workspace_size(a))
-            self.ws["hca"] = torch.empty(max(n, 1), dtype=torch.uint8, device=self.device)
+            self.ws["hca"] = torch.zeros(max(n, 1), dtype=torch.uint8, device=self.device)
 
     def _kv_pos0(self):
         return self.w.n_ctx - self.w.n_win if self.w.decode else 0

@@ -271,3 +271,36 @@ def test_hca_attend_with_fused_window(B, n_q, n_h, N, m, q_pos0, n_win, n_kv):
     ro, rl = oracle.swa_merge(q, kv, kv, kv_pos0, q_pos0, n_win, scale, o, l)
     assert max_abs(to_np(out), ro) <= TOL_BF16
     assert max_abs(to_np(lse), rl) <= TOL_BF16
+
+
+def test_join_counters_reset_across_calls_of_different_shapes():
+    """The splits' join counters live at the start of the workspace and every call
+    leaves them zero: one zero-filled workspace serves consecutive calls of different
+    shapes and split counts (and a standalone window merge in between)."""
+    g = _gen(13)
+    c = 512
+    scale = 1 / math.sqrt(c)
+    ws = torch.zeros(64 << 20, dtype=torch.uint8, device=DEV)
+    q1 = _randn(g, (4, 1, 128, c))
+    kc1 = _randn(g, (4, 3000, c), 1 / math.sqrt(c))
+    idx1 = torch.sort(torch.randint(0, 3000, (4, 1, 512), generator=g), dim=-1).values.int()
+    q2 = _randn(g, (2, 1, 64, c))
+    kc2 = _randn(g, (2, 4000, c), 1 / math.sqrt(c))
+    kv2 = _randn(g, (2, 128, c), 1 / math.sqrt(c))
+    ro1, rl1 = oracle.csa_attend(q1, kc1, kc1, idx1.numpy(), scale)
+    o2, l2 = oracle.hca_attend(q2, kc2, kc2, m=16, q_pos0=4000 * 16 - 1, scale=scale)
+    ro2, rl2 = oracle.swa_merge(q2, kv2, kv2, 4000 * 16 - 128, 4000 * 16 - 1, 128, scale, o2, l2)
+    st = _status()
+    for _ in range(3):
+        o, lse = _ops().csa_attend(q1.to(DEV), kc1.to(DEV), kc1.to(DEV), idx1.to(DEV), scale=scale, workspace=ws,
+                                   dev_status=st)
+        out, lse2 = _ops().hca_attend(q2.to(DEV), kc2.to(DEV), kc2.to(DEV), m=16, q_pos0=4000 * 16 - 1, scale=scale,
+                                      workspace=ws, dev_status=st,
+                                      window=dict(kw=kv2.to(DEV), kv_pos0=4000 * 16 - 128, n_win=128))
+        _ops().swa_merge(q2.to(DEV), kv2.to(DEV), kv2.to(DEV), kv_pos0=4000 * 16 - 128, q_pos0=4000 * 16 - 1,
+                         n_win=128, scale=scale, workspace=ws[4096:], dev_status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0, f"device status {st.item()}"
+        assert max_abs(to_np(o), ro1) <= TOL_BF16 and max_abs(to_np(lse), rl1) <= TOL_BF16
+        assert max_abs(to_np(out), ro2) <= TOL_BF16 and max_abs(to_np(lse2), rl2) <= TOL_BF16
+    assert int(ws[:1024].count_nonzero()) == 0
