@@ -186,6 +186,12 @@ typedef struct hyb_index_args {
   void* ev_scores_end;
 } hyb_index_args;
 
+/* Workspace: csa_index_topk_workspace_size(a) bytes, 256-byte aligned.  Its
+   first bytes hold the top-k plan's counters (histograms, list sizes, a grid
+   barrier), which must be zero before the first call that uses the workspace;
+   every call leaves them zero again (the rest is scratch), so a caller
+   zero-fills a workspace once, when it allocates it.  After a call that
+   reported HYB_DEV_TIMEOUT, zero-fill it again. */
 HYB_API size_t csa_index_topk_workspace_size(const hyb_index_args* a);
 HYB_API hyb_status csa_index_topk(const hyb_index_args* a, void* workspace, size_t ws_bytes, void* stream);
 
@@ -211,9 +217,10 @@ HYB_API hyb_status csa_index_topk(const hyb_index_args* a, void* workspace, size
  *    (csa_index_topk_workspace_size(a) > HYB_NOALLOC_SCRATCH_BYTES) are
  *    rejected with HYB_ERR_WORKSPACE before any launch.
  *  - Every call shares the one array, which keeps the previous call's
- *    contents; the call clears what must start at zero.  Calls whose work
- *    overlaps on the GPU (other streams, other host threads) race on it:
- *    serialise them on one stream.
+ *    contents: it starts zero-filled and every call leaves the counters that
+ *    must start at zero zero again.  Calls whose work overlaps on the GPU
+ *    (other streams, other host threads) race on it: serialise them on one
+ *    stream.
  * ------------------------------------------------------------------------ */
 #define HYB_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 HYB_API hyb_status csa_index_topk_noalloc(const hyb_index_args* a, void* stream);

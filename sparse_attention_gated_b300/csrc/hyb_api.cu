@@ -134,7 +134,7 @@ static size_t index_scores_bytes(const hyb_index_args* a) {
 size_t csa_index_topk_workspace_size(const hyb_index_args* a) {
   if (!a || a->batch <= 0 || a->n_q <= 0 || a->m < 1) return 0;
   const int64_t nv = n_vis_max(a->q_pos0, a->n_q, a->m, a->n_entries);
-  return index_scores_bytes(a) + round_up(hyb::topk_workspace_bytes(a, nv), 256);
+  return hyb::kTopkZeroRegionBytes + index_scores_bytes(a) + round_up(hyb::topk_workspace_bytes(a, nv), 256);
 }
 
 static hyb_status validate_index(const hyb_index_args* a) {
@@ -178,10 +178,12 @@ hyb_status csa_index_topk(const hyb_index_args* a, void* workspace, size_t ws_by
   if (!aligned(workspace, 256)) return fail(HYB_ERR_WORKSPACE, "csa_index_topk: workspace must be 256-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t nv = n_vis_max(a->q_pos0, a->n_q, a->m, a->n_entries);
-  float* scores = static_cast<float*>(workspace);
-  void* topk_ws = static_cast<char*>(workspace) + index_scores_bytes(a);
+  // [counters that stay zero between calls][scores][top-k scratch]
+  void* zr = workspace;
+  float* scores = reinterpret_cast<float*>(static_cast<char*>(workspace) + hyb::kTopkZeroRegionBytes);
+  void* topk_ws = static_cast<char*>(workspace) + hyb::kTopkZeroRegionBytes + index_scores_bytes(a);
   cudaError_t e;
-  uint32_t* ghist = hyb::topk_prepare_hist(a, nv, topk_ws, s, &e);
+  uint32_t* ghist = hyb::topk_prepare_hist(a, nv, topk_ws, zr, s, &e);
   if (e != cudaSuccess) return cuda_status(e, "csa_index_topk: histogram reset");
   bool hist_done = false;
   if (a->ev_scores_begin &&
@@ -195,7 +197,7 @@ hyb_status csa_index_topk(const hyb_index_args* a, void* workspace, size_t ws_by
       (e = cudaEventRecordWithFlags(static_cast<cudaEvent_t>(a->ev_scores_end), s, cudaEventRecordExternal)) !=
           cudaSuccess)
     return cuda_status(e, "csa_index_topk: ev_scores_end");
-  return cuda_status(hyb::launch_topk(a, scores, nv, topk_ws, hist_done, s), "csa_index_topk: top-k launch");
+  return cuda_status(hyb::launch_topk(a, scores, nv, topk_ws, zr, hist_done, s), "csa_index_topk: top-k launch");
 }
 
 // ----------------------------------------------- index + top-k, no allocation

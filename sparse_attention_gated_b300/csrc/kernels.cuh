@@ -14,6 +14,11 @@ constexpr size_t kJoinRegionBytes = 1024;
 // top-k threshold histogram over the top bits of the order-preserving score keys
 constexpr int kTopkHistBits = 12;
 constexpr int kTopkHistBins = 1 << kTopkHistBits;
+// The csa_index_topk workspace starts with the counters of the top-k grid plan (up to one
+// row per SM): two histograms and a 256-bin one per row, three words per row, four for
+// the grid.  They must be zero before the first call and every call leaves them zero.
+constexpr size_t kTopkZeroRegionBytes =
+    ((size_t)kNumSMs * (2 * kTopkHistBins + 256 + 3) * 4 + 4 * 4 + 255) / 256 * 256;
 
 // compress.cu
 bool compress_shape_supported(int64_t c);
@@ -31,12 +36,14 @@ cudaError_t launch_index_scores_tc(const hyb_index_args* a, float* scores, int64
                                    uint32_t* ghist, bool* hist_done, cudaStream_t s);
 
 // topk.cu
+// ws: the plan's scratch; zr: the zeroed counters (kTopkZeroRegionBytes at the workspace start)
 size_t topk_workspace_bytes(const hyb_index_args* a, int64_t n_vis_max);
 bool topk_shape_supported(const hyb_index_args* a, int64_t n_vis_max);
 // the zeroed row histograms when the top-k plan uses them (else nullptr)
-uint32_t* topk_prepare_hist(const hyb_index_args* a, int64_t n_vis_max, void* ws, cudaStream_t s, cudaError_t* err);
-cudaError_t launch_topk(const hyb_index_args* a, const float* scores, int64_t score_stride, void* ws, bool hist_done,
-                        cudaStream_t s);
+uint32_t* topk_prepare_hist(const hyb_index_args* a, int64_t n_vis_max, void* ws, void* zr, cudaStream_t s,
+                            cudaError_t* err);
+cudaError_t launch_topk(const hyb_index_args* a, const float* scores, int64_t score_stride, void* ws, void* zr,
+                        bool hist_done, cudaStream_t s);
 
 // attend_cc.cu (CUDA-core attention for all three entry sources)
 struct AttendJob {

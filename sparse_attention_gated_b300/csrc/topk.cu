@@ -91,7 +91,8 @@ struct TopkParams {
   uint32_t* hist3;      // [rows][256]: last 8 bits of the sub-candidates (overflow only)
   uint32_t* nsub;       // [rows]: sub-candidates appended to the row's sub-list
   uint32_t* ncand;      // [rows]: candidates appended to the row's list
-  uint32_t* gsync;      // [0]: grid-barrier arrivals, [1]: a sub-list overflowed
+  uint32_t* dep;        // [rows]: CTAs of the row that finished
+  uint32_t* gsync;      // [0]: grid-barrier arrivals, [1]: a sub-list overflowed, [2]: CTAs that finished
   int32_t* slots;       // [rows][n_chunks][kGridSlot]: published per-CTA counts (slow path 0-2, list 4-6)
   uint2* cand;          // [rows][n_chunks][chunk]: (key, entry) of each CTA's first-level candidates
   uint2* sub;           // [rows][kSubListCap]: (key, entry) of the sub-candidates
@@ -774,6 +775,12 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_grid_kernel(TopkParams p
   for (int i = tid; i < kHistBins; i += kTopkThreads)
     if (hist[i]) atomicAdd(p.ghist2 + row * kHistBins + i, hist[i]);
   if (!grid_barrier(p.gsync, ++nbar * nblk, p.dev_status, 41)) return;
+  {
+    // every CTA of the row has read the first-level histogram: clear this CTA's slice of it
+    const int slice = (kHistBins + parts - 1) / parts;
+    const int lo = part * slice, hi = lo + slice < kHistBins ? lo + slice : kHistBins;
+    for (int i = lo + tid; i < hi; i += kTopkThreads) p.ghist[row * kHistBins + i] = 0u;
+  }
 
   // phase 2 (rows with at most kCandListCap candidates): every CTA gathers the row's
   // candidates in entry order (CTA by CTA, at the prefix of the counts before it), finds
@@ -1086,6 +1093,30 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_grid_kernel(TopkParams p
       if (out_sc) out_sc[i] = i < vis ? __ldcg(sc + i) : -INFINITY;
     }
   }
+  // Leave the counters zero for the next call: the row's last CTA to finish clears the
+  // row's second-level histograms and list size, the grid's last the grid-wide words
+  // (every CTA counts itself finished only after its last read of them).
+  __shared__ int s_last;
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    s_last = atomicAdd(p.dep + row, 1u) == (uint32_t)(parts - 1);
+  }
+  __syncthreads();
+  if (s_last) {
+    for (int i = tid; i < kHistBins; i += kTopkThreads) p.ghist2[row * kHistBins + i] = 0u;
+    for (int i = tid; i < 256; i += kTopkThreads) p.hist3[row * 256 + i] = 0u;
+    if (tid == 0) p.nsub[row] = 0u, p.dep[row] = 0u;
+  }
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(p.gsync + 2, 1u) == nblk - 1) {
+      for (int rr = 0; rr < (int)gridDim.y; ++rr) p.ncand[rr] = 0u;
+      p.gsync[0] = 0u, p.gsync[1] = 0u;
+      __threadfence();
+      p.gsync[2] = 0u;
+    }
+  }
 }
 
 // ------------------------------------------------------------------ host
@@ -1147,15 +1178,13 @@ static TopkPlan plan_topk(const hyb_index_args* a, int64_t n_vis_max) {
 
 static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-// grid plan: the zeroed counters first (histograms, list sizes, barrier and flags), then the rest
-static size_t grid_zeroed_bytes(size_t rows) { return rows * (2 * kHistBins + 256 + 2) * 4 + 4 * 4; }
 
 size_t topk_workspace_bytes(const hyb_index_args* a, int64_t n_vis_max) {
   const TopkPlan pl = plan_topk(a, n_vis_max);
   const size_t rows = (size_t)(a->batch * a->n_q);
   if (pl.kind == 2)
-    return align256(grid_zeroed_bytes(rows)) + align256(rows * pl.n_chunks * kGridSlot * 4) +
-           align256(rows * kSubListCap * 8) + align256(rows * pl.n_chunks * pl.chunk * 8);
+    return align256(rows * pl.n_chunks * kGridSlot * 4) + align256(rows * kSubListCap * 8) +
+           align256(rows * pl.n_chunks * pl.chunk * 8);
   if (pl.kind != 1) return 0;
   const size_t region = rows * (size_t)pl.n_chunks * (size_t)pl.chunk;
   return align256(rows * kHistBins * 8 + rows * 4) + 3 * align256(region * 4) + align256(rows * pl.n_chunks * 8);
@@ -1163,16 +1192,18 @@ size_t topk_workspace_bytes(const hyb_index_args* a, int64_t n_vis_max) {
 
 bool topk_shape_supported(const hyb_index_args* a, int64_t) { return a->k >= 1 && a->k <= 2048; }
 
-static void topk_pointers(TopkParams& p, const TopkPlan& pl, int64_t rows, void* ws) {
+static void topk_pointers(TopkParams& p, const TopkPlan& pl, int64_t rows, void* ws, void* zr) {
   char* w = static_cast<char*>(ws);
-  p.ghist = reinterpret_cast<uint32_t*>(w);
-  p.ghist2 = p.ghist + rows * kHistBins;
   if (pl.kind == 2) {
-    p.hist3 = p.ghist2 + rows * kHistBins;
-    p.nsub = p.hist3 + rows * 256;
-    p.ncand = p.nsub + rows;
-    p.gsync = p.ncand + rows;
-    w += align256(grid_zeroed_bytes((size_t)rows));
+    // the counters (zero between calls) at fixed places of the workspace's start
+    constexpr int64_t R = kNumSMs;
+    p.ghist = static_cast<uint32_t*>(zr);
+    p.ghist2 = p.ghist + R * kHistBins;
+    p.hist3 = p.ghist2 + R * kHistBins;
+    p.nsub = p.hist3 + R * 256;
+    p.ncand = p.nsub + R;
+    p.dep = p.ncand + R;
+    p.gsync = p.dep + R;
     p.slots = reinterpret_cast<int32_t*>(w);
     w += align256((size_t)rows * pl.n_chunks * kGridSlot * 4);
     p.sub = reinterpret_cast<uint2*>(w);
@@ -1181,6 +1212,8 @@ static void topk_pointers(TopkParams& p, const TopkPlan& pl, int64_t rows, void*
     return;
   }
   const size_t region = (size_t)rows * pl.n_chunks * pl.chunk;
+  p.ghist = reinterpret_cast<uint32_t*>(w);
+  p.ghist2 = p.ghist + rows * kHistBins;
   p.done = p.ghist2 + rows * kHistBins;
   w += align256((size_t)rows * kHistBins * 8 + (size_t)rows * 4);
   p.def_idx = reinterpret_cast<int32_t*>(w);
@@ -1192,20 +1225,22 @@ static void topk_pointers(TopkParams& p, const TopkPlan& pl, int64_t rows, void*
   p.counts = reinterpret_cast<int32_t*>(w);
 }
 
-uint32_t* topk_prepare_hist(const hyb_index_args* a, int64_t n_vis_max, void* ws, cudaStream_t s, cudaError_t* err) {
+uint32_t* topk_prepare_hist(const hyb_index_args* a, int64_t n_vis_max, void* ws, void* zr, cudaStream_t s,
+                            cudaError_t* err) {
   *err = cudaSuccess;
   const int64_t rows = a->batch * a->n_q;
   const TopkPlan pl = plan_topk(a, n_vis_max);
   if (rows == 0 || pl.kind == 0) return nullptr;
   TopkParams p{};
-  topk_pointers(p, pl, rows, ws);
-  const size_t bytes = pl.kind == 2 ? grid_zeroed_bytes((size_t)rows) : (size_t)rows * (kHistBins * 8 + 4);
-  *err = cudaMemsetAsync(p.ghist, 0, bytes, s);  // histograms and counters
+  topk_pointers(p, pl, rows, ws, zr);
+  // the grid plan's counters are already zero (left so by the previous call); the
+  // three-kernel plan clears its own
+  if (pl.kind == 1) *err = cudaMemsetAsync(p.ghist, 0, (size_t)rows * (kHistBins * 8 + 4), s);
   return p.ghist;
 }
 
-cudaError_t launch_topk(const hyb_index_args* a, const float* scores, int64_t score_stride, void* ws, bool hist_done,
-                        cudaStream_t s) {
+cudaError_t launch_topk(const hyb_index_args* a, const float* scores, int64_t score_stride, void* ws, void* zr,
+                        bool hist_done, cudaStream_t s) {
   TopkParams p{};
   p.scores = scores, p.score_stride = score_stride, p.idx = a->idx, p.out_scores = a->scores;
   p.n_q = a->n_q, p.n_entries = a->n_entries, p.m = a->m, p.k = a->k, p.q_pos0 = a->q_pos0;
@@ -1225,7 +1260,7 @@ cudaError_t launch_topk(const hyb_index_args* a, const float* scores, int64_t sc
   }
   p.chunk = pl.chunk, p.n_chunks = pl.n_chunks;
   p.hist_done = hist_done ? 1 : 0;
-  topk_pointers(p, pl, rows, ws);
+  topk_pointers(p, pl, rows, ws, zr);
   const dim3 grid((unsigned)pl.n_chunks, (unsigned)rows);
   if (pl.kind == 2) {
     const size_t smem = grid_smem_bytes(pl.chunk);

@@ -42,9 +42,9 @@ def _stream(stream):
 
 
 def _workspace(nbytes, workspace, device, zeroed=False):
-    """zeroed: the call needs the workspace to start zero-filled (csa_attend / hca_attend keep
-    their join counters in its first bytes and leave them zero); a caller's own workspace
-    must then have been zero-filled once."""
+    """zeroed: the call needs the workspace to start zero-filled (csa_index_topk, csa_attend
+    and hca_attend keep counters in its first bytes and leave them zero); a caller's own
+    workspace must then have been zero-filled once."""
     if nbytes == 0:
         return None, 0
     if workspace is None:
@@ -140,7 +140,7 @@ def csa_index_topk(qI, w, kI, *, m: int, k: int, q_pos0: int, qI_scale=None, kI_
     if scores is None and want_scores:
         scores = torch.empty((B, n_q, k), dtype=torch.float32, device=qI.device)
     a = index_args(qI, w, kI, m, k, q_pos0, qI_scale, kI_scale, idx, scores, n_entries, dev_status, scores_events)
-    ws, nbytes = _workspace(csa_index_topk_workspace_size(a), workspace, qI.device)
+    ws, nbytes = _workspace(csa_index_topk_workspace_size(a), workspace, qI.device, zeroed=True)
     _abi.check(_abi.load().csa_index_topk(ctypes.byref(a), ws, nbytes, _stream(stream)), "csa_index_topk")
     return (idx, scores) if want_scores else idx
 

@@ -80,7 +80,7 @@ class HybridStep:
             kc, kI, kIs = self._csa_tensors()
             a = ops.index_args(x["qI"], x["w"], kI, w.m, w.k, w.q_pos0, x.get("qI_scale"), kIs, b["idx"], None)
             n = ops.csa_index_topk_workspace_size(a)
-            self.ws["index"] = torch.empty(max(n, 1), dtype=torch.uint8, device=self.device)
+            self.ws["index"] = torch.zeros(max(n, 1), dtype=torch.uint8, device=self.device)  # (counters)
             a = ops.csa_attend_args(x["q"], kc, kc, b["idx"], w.scale, b["o"], b["lse"], window=self._win_csa())
             n = int(ops._abi.load().csa_attend_workspace_size(a))
             self.ws["csa"] = torch.zeros(max(n, 1), dtype=torch.uint8, device=self.device)  # (join counters)
