@@ -187,12 +187,14 @@ typedef struct hyb_index_args {
 } hyb_index_args;
 
 /* Workspace: csa_index_topk_workspace_size(a) bytes, 256-byte aligned.  Its
-   first bytes hold the top-k plan's counters (histograms, list sizes, a grid
-   barrier), which must be zero before the first call that uses the workspace;
-   every call leaves them zero again (the rest is scratch), so a caller
-   zero-fills a workspace once, when it allocates it.  After a call that
-   reported HYB_DEV_TIMEOUT, zero-fill it again. */
+   first csa_index_topk_counter_bytes() bytes hold the top-k plan's counters
+   (histograms, list sizes, a grid barrier), which must be zero before the
+   first call that uses the workspace; every call leaves them zero again (the
+   rest is scratch), so a caller zero-fills a workspace once, when it allocates
+   it.  After a call that reported HYB_DEV_TIMEOUT, zero-fill those bytes again.
+   csa_index_topk_counter_bytes() is a constant of the library build. */
 HYB_API size_t csa_index_topk_workspace_size(const hyb_index_args* a);
+HYB_API size_t csa_index_topk_counter_bytes(void);
 HYB_API hyb_status csa_index_topk(const hyb_index_args* a, void* workspace, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------

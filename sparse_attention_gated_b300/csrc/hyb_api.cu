@@ -131,6 +131,8 @@ static size_t index_scores_bytes(const hyb_index_args* a) {
   return round_up((size_t)(a->batch * a->n_q) * (size_t)nv * sizeof(float), 256);
 }
 
+size_t csa_index_topk_counter_bytes(void) { return hyb::kTopkZeroRegionBytes; }
+
 size_t csa_index_topk_workspace_size(const hyb_index_args* a) {
   if (!a || a->batch <= 0 || a->n_q <= 0 || a->m < 1) return 0;
   const int64_t nv = n_vis_max(a->q_pos0, a->n_q, a->m, a->n_entries);

@@ -129,6 +129,12 @@ def csa_index_topk_workspace_size(a) -> int:
     return int(_abi.load().csa_index_topk_workspace_size(ctypes.byref(a)))
 
 
+def csa_index_topk_counter_bytes() -> int:
+    """Leading bytes of a csa_index_topk workspace that must be zero before a call
+    (every call leaves them zero; re-zero them after a device timeout)."""
+    return int(_abi.load().csa_index_topk_counter_bytes())
+
+
 def csa_index_topk(qI, w, kI, *, m: int, k: int, q_pos0: int, qI_scale=None, kI_scale=None, n_entries=None,
                    idx=None, scores=None, want_scores: bool = False, workspace=None, dev_status=None, stream=None,
                    scores_events=None):

@@ -149,6 +149,38 @@ def test_index_topk_matches_oracle(fp8, B, n_q, N, n_ih, c_I, m, k, q_pos0):
             assert np.all(np.isneginf(sel_scores[b, j, take:]))
 
 
+def test_index_topk_counters_reset_across_calls_of_different_shapes():
+    """One zero-filled workspace serves consecutive index + top-k calls of different
+    shapes (two decode batches with different row counts and lengths, and a prefill
+    block), in turn.  Every call must match the oracle and leave the workspace's
+    counters zero."""
+    cases = [
+        (4, 1, 80000, 64, 128, 4, 512, 4 * 80000 - 1),
+        (2, 1, 20000, 64, 128, 4, 512, 80000 - 1),
+        (1, 40, 3000, 64, 128, 4, 256, 12000 - 40),      # prefill kernel
+    ]
+    inputs = [(_index_case(31 + i, B, n_q, N, n_ih, c_I, m, q_pos0, True), (B, n_q, N, m, k, q_pos0))
+              for i, (B, n_q, N, n_ih, c_I, m, k, q_pos0) in enumerate(cases)]
+    refs = [oracle.index_scores(qI, w, kI, m=m, q_pos0=q_pos0, qI_scale=qs, kI_scale=ks)
+            for (qI, kI, qs, ks, w), (B, n_q, N, m, k, q_pos0) in inputs]
+    ws = torch.zeros(64 << 20, dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    n_zero = ops.csa_index_topk_counter_bytes()
+    assert 0 < n_zero < ws.numel()
+    for _ in range(2):
+        for ((qI, kI, qs, ks, w), (B, n_q, N, m, k, q_pos0)), ref in zip(inputs, refs):
+            idx = ops.csa_index_topk(qI.to(DEV), w.to(DEV), kI.to(DEV), m=m, k=k, q_pos0=q_pos0,
+                                     qI_scale=qs.to(DEV), kI_scale=ks.to(DEV), n_entries=N, workspace=ws,
+                                     dev_status=st)
+            torch.cuda.synchronize()
+            assert st.item() == 0, f"device status {st.item()}"
+            idx = idx.cpu().numpy()
+            for b in range(B):
+                for j in range(n_q):
+                    check_topk_row(idx[b, j], ref[b, j], min(oracle.visible(q_pos0 + j, m), N), k)
+            assert int(ws[:n_zero].count_nonzero()) == 0
+
+
 def test_topk_is_bit_exact_with_integer_scores_and_ties():
     """Small-integer indexer inputs make every score exact in float32, so the
     selection (including the lower-index tie rule) must equal the oracle's exactly."""
