@@ -179,9 +179,10 @@ typedef struct hyb_index_args {
   int32_t* dev_status;
   /* Optional profiling events (cudaEvent_t, or NULL): recorded on the stream
      right before and right after the scoring kernel, so that a caller can time
-     the scoring apart from the selection.  Recorded as external events
-     (cudaEventRecordExternal), so they stay in a graph captured from the
-     stream.  The library neither creates nor destroys them. */
+     the scoring apart from the selection.  While the stream is being captured
+     into a graph they are recorded as external events (cudaEventRecordExternal),
+     so they stay in the graph; otherwise they are recorded plainly.  The
+     library neither creates nor destroys them. */
   void* ev_scores_begin;
   void* ev_scores_end;
 } hyb_index_args;

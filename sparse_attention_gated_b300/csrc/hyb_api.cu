@@ -49,6 +49,16 @@ size_t lane_align(int64_t c, int32_t dt) {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// A caller's profiling event: an external event node while the stream is being captured
+// into a graph (so that it stays in the graph), a plain record otherwise.
+cudaError_t record_event(void* ev, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cs);
+  if (e != cudaSuccess) return e;
+  return cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev), s,
+                                  cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault);
+}
+
 int64_t n_vis_max(int64_t q_pos0, int64_t n_q, int64_t m, int64_t n_entries) {
   if (n_q <= 0) return 0;
   int64_t v = hyb::visible_entries(q_pos0 + n_q - 1, m);
@@ -188,16 +198,12 @@ hyb_status csa_index_topk(const hyb_index_args* a, void* workspace, size_t ws_by
   uint32_t* ghist = hyb::topk_prepare_hist(a, nv, topk_ws, zr, s, &e);
   if (e != cudaSuccess) return cuda_status(e, "csa_index_topk: histogram reset");
   bool hist_done = false;
-  if (a->ev_scores_begin &&
-      (e = cudaEventRecordWithFlags(static_cast<cudaEvent_t>(a->ev_scores_begin), s, cudaEventRecordExternal)) !=
-          cudaSuccess)
+  if (a->ev_scores_begin && (e = record_event(a->ev_scores_begin, s)) != cudaSuccess)
     return cuda_status(e, "csa_index_topk: ev_scores_begin");
   e = hyb::index_tc_shape_supported(a) ? hyb::launch_index_scores_tc(a, scores, nv, nv, ghist, &hist_done, s)
                                        : hyb::launch_index_scores_cc(a, scores, nv, nv, s);
   if (e != cudaSuccess) return cuda_status(e, "csa_index_topk: index-score launch");
-  if (a->ev_scores_end &&
-      (e = cudaEventRecordWithFlags(static_cast<cudaEvent_t>(a->ev_scores_end), s, cudaEventRecordExternal)) !=
-          cudaSuccess)
+  if (a->ev_scores_end && (e = record_event(a->ev_scores_end, s)) != cudaSuccess)
     return cuda_status(e, "csa_index_topk: ev_scores_end");
   return cuda_status(hyb::launch_topk(a, scores, nv, topk_ws, zr, hist_done, s), "csa_index_topk: top-k launch");
 }

@@ -135,6 +135,9 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
+  // the CTA's first unit, from the parameters alone (64-bit divisions): computed while
+  // the previous kernel may still be running
+  const IdxUnit U_first = idx_unit<NQ>(p, blockIdx.x);
   pdl_wait();  // (the setup above touched only shared memory, TMEM and the parameters)
   pdl_trigger();
 
@@ -146,24 +149,30 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
       int64_t q_count = 0, seq = 0, issued = 0;
       bool ok = true;
       for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
-        const IdxUnit U = idx_unit<NQ>(p, u);
+        const IdxUnit U = u == blockIdx.x ? U_first : idx_unit<NQ>(p, u);
         if (U.tile_begin >= U.tile_end) continue;
-        const int qb = (int)(q_count & 1);
-        if (!(ok = tc::mbar_wait(&q_empty[qb], (uint32_t)((q_count >> 1) & 1) ^ 1u, s_abort))) break;
-        tc::mbar_arrive_expect_tx(&q_full[qb], C::kQBytes);
-        tc::tma_load_2d(qbuf + qb * C::kQBytes, &tm_q, &q_full[qb], 0, (int32_t)((U.b * p.n_q + U.j0) * C::kHeads));
-        ++q_count;
+        // per tile: the keys first (the long HBM read), then, on a unit's first tile, its
+        // queries, then the tile's scales
+        bool q_todo = true;
         for (int64_t t = U.tile_begin; t < U.tile_end; ++t, ++seq) {
-          const int r = (int)(seq % C::kScaleRing);
-          if (!(ok = tc::mbar_wait(&sc_empty[r], (uint32_t)((seq / C::kScaleRing) & 1) ^ 1u, s_abort))) break;
-          tc::mbar_arrive_expect_tx(&sc_full[r], C::kScaleBytes);
-          tc::tma_load_2d(scales + r * C::kTileE, &tm_scales, &sc_full[r], (int32_t)(t * C::kTileE), (int32_t)U.b);
           if (!(ok = tc::mbar_wait(&empty[stage], sphase ^ 1u, s_abort))) break;
           tc::mbar_arrive_expect_tx(&full[stage], C::kKeyBytes);
           tc::tma_load_2d(keys + stage * C::kKeyBytes, &tm_keys, &full[stage], 0,
                           (int32_t)(U.b * p.kv_stride + t * C::kTileE));
           ++issued;
           if (++stage == C::kStages) stage = 0, sphase ^= 1u;
+          if (q_todo) {
+            const int qb = (int)(q_count & 1);
+            if (!(ok = tc::mbar_wait(&q_empty[qb], (uint32_t)((q_count >> 1) & 1) ^ 1u, s_abort))) break;
+            tc::mbar_arrive_expect_tx(&q_full[qb], C::kQBytes);
+            tc::tma_load_2d(qbuf + qb * C::kQBytes, &tm_q, &q_full[qb], 0, (int32_t)((U.b * p.n_q + U.j0) * C::kHeads));
+            ++q_count;
+            q_todo = false;
+          }
+          const int r = (int)(seq % C::kScaleRing);
+          if (!(ok = tc::mbar_wait(&sc_empty[r], (uint32_t)((seq / C::kScaleRing) & 1) ^ 1u, s_abort))) break;
+          tc::mbar_arrive_expect_tx(&sc_full[r], C::kScaleBytes);
+          tc::tma_load_2d(scales + r * C::kTileE, &tm_scales, &sc_full[r], (int32_t)(t * C::kTileE), (int32_t)U.b);
         }
       }
       if (!ok) {
@@ -181,7 +190,7 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
       int64_t q_count = 0;
       bool ok = true;
       for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
-        const IdxUnit U = idx_unit<NQ>(p, u);
+        const IdxUnit U = u == blockIdx.x ? U_first : idx_unit<NQ>(p, u);
         if (U.tile_begin >= U.tile_end) continue;
         const int qb = (int)(q_count & 1);
         if (!(ok = tc::mbar_wait(&q_full[qb], (uint32_t)((q_count >> 1) & 1), s_abort))) break;
@@ -232,25 +241,28 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
     int64_t hist_row = -1;
     if (do_hist)
       for (int i = et; i < kTopkHistBins / 2; i += kEpiThreads) hist[i] = 0;
-    auto flush_hist = [&]() {
-      for (int i = et; i < kTopkHistBins / 2; i += kEpiThreads) {
-        const uint32_t v = hist[i];
-        if (v) {
-          uint32_t* g = p.ghist + hist_row * kTopkHistBins + 2 * i;
-          if (v & 0xFFFFu) atomicAdd(g, v & 0xFFFFu);
-          if (v >> 16) atomicAdd(g + 1, v >> 16);
-          hist[i] = 0;
-        }
+    // each thread takes 8 consecutive words (16 bins), read as two 16-byte vectors
+    static_assert(kTopkHistBins / 2 == 8 * kEpiThreads, "one 8-word slice of the histogram per epilogue thread");
+    auto flush_hist = [&](bool clear) {
+      uint4* h4 = reinterpret_cast<uint4*>(hist) + 2 * et;
+      const uint4 a = h4[0], b = h4[1];
+      const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      uint32_t* g = p.ghist + hist_row * kTopkHistBins + 16 * et;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (v[i] & 0xFFFFu) atomicAdd(g + 2 * i, v[i] & 0xFFFFu);
+        if (v[i] >> 16) atomicAdd(g + 2 * i + 1, v[i] >> 16);
       }
+      if (clear) h4[0] = h4[1] = make_uint4(0u, 0u, 0u, 0u);
     };
     int64_t seq = 0;
     bool ok = true;
     for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
-      const IdxUnit U = idx_unit<NQ>(p, u);
+      const IdxUnit U = u == blockIdx.x ? U_first : idx_unit<NQ>(p, u);
       if (U.tile_begin >= U.tile_end) continue;
       if (!(ok = esync())) break;  // everyone is done with the previous unit's tables
       if (do_hist && U.b * p.n_q + U.j0 != hist_row) {
-        if (hist_row >= 0) flush_hist();
+        if (hist_row >= 0) flush_hist(true);
         hist_row = U.b * p.n_q + U.j0;
       }
       if (et == 0) *s_allpos = 1;
@@ -270,6 +282,14 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
       }
       if (!(ok = esync())) break;
       const bool allpos = *s_allpos != 0;
+      // entries each of this warp's queries sees (a score past them is not written)
+      int64_t vis_q[kQPerWarp];
+#pragma unroll
+      for (int qi = 0; qi < kQPerWarp; ++qi) {
+        const int q = NQ == 1 ? 0 : 2 * half + qi;
+        int64_t vis = visible_entries(p.q_pos0 + U.j0 + q, p.m);
+        vis_q[qi] = q < U.nq ? (vis < p.n_entries ? vis : p.n_entries) : 0;
+      }
       for (int64_t t = U.tile_begin; t < U.tile_end; ++t, ++seq) {
         if (NQ == 1 && (int)(seq & 1) != half) continue;  // the other group's tile
         const int r = (int)(seq % C::kScaleRing);
@@ -286,12 +306,13 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
         for (int qi = 0; qi < kQPerWarp; ++qi) {
           const int q = NQ == 1 ? 0 : 2 * half + qi;
           const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * C::kN + q * C::kHeads);
-          // heads 0-31 then 32-63 (one 32-column load live at a time; the same summation order)
+          // heads 0-31 then 32-63 (one 32-column load live at a time), summed in four
+          // interleaved partial sums (head h into sum h mod 4) that are then added pairwise
           const float* wc = w_c + q * C::kHeads;
           const float* ww = w_w + q * C::kHeads;
           const float* wq = w_q + q * C::kHeads;
           const bool fast = allpos && ks > 0.f;
-          float sum = 0.f;
+          float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int hb = 0; hb < 64; hb += 32) {
             float v[32];
@@ -299,12 +320,13 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
             tc::tmem_ld_wait();
             if (fast) {
 #pragma unroll
-              for (int h = 0; h < 32; ++h) sum = fmaf(wc[hb + h], fmaxf(v[h], 0.f), sum);
+              for (int h = 0; h < 32; ++h) ps[h & 3] = fmaf(wc[hb + h], fmaxf(v[h], 0.f), ps[h & 3]);
             } else {
 #pragma unroll
-              for (int h = 0; h < 32; ++h) sum = fmaf(ww[hb + h], fmaxf(v[h] * (wq[hb + h] * ks), 0.f), sum);
+              for (int h = 0; h < 32; ++h) ps[h & 3] = fmaf(ww[hb + h], fmaxf(v[h] * (wq[hb + h] * ks), 0.f), ps[h & 3]);
             }
           }
+          const float sum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
           score[qi] = fast ? sum * ks : sum;
         }
         tc::tc_fence_before();
@@ -317,18 +339,19 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
         for (int qi = 0; qi < kQPerWarp; ++qi) {
           const int q = NQ == 1 ? 0 : 2 * half + qi;
           const int64_t j = U.j0 + q;
-          int64_t vis = visible_entries(p.q_pos0 + j, p.m);
-          if (vis > p.n_entries) vis = p.n_entries;
-          const bool keep = q < U.nq && s < vis;
+          const bool keep = s < vis_q[qi];
           if (keep) p.scores[(U.b * p.n_q + j) * p.score_stride + s] = score[qi];
-          if (do_hist && keep) {
-            const uint32_t bin = float_order_key(score[qi]) >> (32 - kTopkHistBits);
-            atomicAdd(&hist[bin >> 1], 1u << (16 * (bin & 1)));
+          if (do_hist) {
+            // lanes with the same bin add their count once (scores crowd into few bins)
+            const uint32_t bin = keep ? float_order_key(score[qi]) >> (32 - kTopkHistBits) : 0xFFFFFFFFu;
+            const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+            if (keep && lane == __ffs(peers) - 1)
+              atomicAdd(&hist[bin >> 1], (uint32_t)__popc(peers) << (16 * (bin & 1)));
           }
         }
       }
     }
-    if (do_hist && ok && hist_row >= 0 && esync()) flush_hist();
+    if (do_hist && ok && hist_row >= 0 && esync()) flush_hist(false);
   }
 
   tc::tc_fence_before();

@@ -181,6 +181,22 @@ def test_index_topk_counters_reset_across_calls_of_different_shapes():
             assert int(ws[:n_zero].count_nonzero()) == 0
 
 
+def test_scoring_events_outside_a_graph():
+    """The scoring-kernel events may be passed on a stream that is not being captured:
+    the call records them plainly, the result is unchanged and they bracket the kernel."""
+    qI, kI, qs, ks, w = _index_case(41, 2, 1, 20000, 64, 128, 4, 80000 - 1, True)
+    args = [t.to(DEV) for t in (qI, w, kI)]
+    kw = dict(m=4, k=512, q_pos0=80000 - 1, qI_scale=qs.to(DEV), kI_scale=ks.to(DEV), n_entries=20000)
+    plain = ops.csa_index_topk(*args, **kw)
+    ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    for e in ev:
+        e.record()  # torch only times events it has seen recorded; the library records them again
+    timed = ops.csa_index_topk(*args, **kw, scores_events=ev)
+    torch.cuda.synchronize()
+    assert torch.equal(plain, timed)
+    assert ev[0].elapsed_time(ev[1]) > 0
+
+
 def test_topk_is_bit_exact_with_integer_scores_and_ties():
     """Small-integer indexer inputs make every score exact in float32, so the
     selection (including the lower-index tie rule) must equal the oracle's exactly."""
