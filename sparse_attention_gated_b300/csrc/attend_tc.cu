@@ -874,86 +874,74 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = ok && all_sync() && *s_abort == 0;
       if (ok) {
-        constexpr int kQuads = kC / 4;
-        const int n_items = kHG * kQuads;
+        // Each thread merges items of 8 output dims of one head: it loads the (m, l) of
+        // every split for that head and the split partials of its 8 dims, up to kJoinBatch
+        // splits at once (all in flight together), and keeps a running maximum across
+        // batches.  No shared table and no further barrier: one L2 round trip per batch.
+        constexpr int kOcts = kC / 8;
+        constexpr int kJoinBatch = 16;
+        const int n_items = kHG * kOcts;
         const int i0 = (int)((int64_t)W.sp * n_items / S), i1 = (int)((int64_t)(W.sp + 1) * n_items / S);
-        const int h_lo = i0 / kQuads, nh = (i1 - 1) / kQuads - h_lo + 1;  // heads of this CTA's items
-        float2* t_ml = reinterpret_cast<float2*>(red);  // [nh][S] (m, l) of every split
-        float* t_w = red + 512;                          // [nh][S] merge weights (1/L included)
         const float2* ml_b = p.part_ml + W.bq * S * p.n_h + W.hg * kHG;
-        for (int t = ts; t < nh * S; t += kSoftThreads) {
-          const int hl = t / S, s2 = t - hl * S;
-          t_ml[t] = __ldcg(&ml_b[(int64_t)s2 * p.n_h + h_lo + hl]);
-        }
-        ok = all_sync();
-        if (ok) {
-          for (int t = ts; t < nh * S; t += kSoftThreads) {
-            const int hl = t / S;
-            float M = -INFINITY;
-            for (int s2 = 0; s2 < S; ++s2) M = fmaxf(M, t_ml[hl * S + s2].x);
-            float L = 0.f;
-            if (M != -INFINITY)
-              for (int s2 = 0; s2 < S; ++s2) {
-                const float2 ml = t_ml[hl * S + s2];
-                if (ml.x != -INFINITY) L = fmaf(ml.y, exp2f(ml.x - M), L);
+        const __nv_bfloat16* po_b = p.part_o + (W.bq * S * p.n_hg + W.hg) * (int64_t)(kHG * kC);
+        const int64_t split_stride = (int64_t)p.n_hg * kHG * kC;
+        const int64_t o_b = (W.bq * p.n_h + W.hg * kHG) * kC;  // the unit's first output row
+        for (int it = i0 + ts; it < i1; it += kSoftThreads) {
+          const int h = it / kOcts, d = (it - h * kOcts) * 8;
+          const int off = ((d >> 7) * kHG + h) * 128 + (d & 127);  // chunk-major partial
+          float M = -INFINITY, L = 0.f, acc[8];
+#pragma unroll
+          for (int x = 0; x < 8; ++x) acc[x] = 0.f;
+          for (int s0 = 0; s0 < S; s0 += kJoinBatch) {
+            float2 ml[kJoinBatch];
+            uint4 raw[kJoinBatch];
+#pragma unroll
+            for (int j = 0; j < kJoinBatch; ++j) {
+              const bool in = s0 + j < S;
+              ml[j] = in ? __ldcg(&ml_b[(int64_t)(s0 + j) * p.n_h + h]) : make_float2(-INFINITY, 0.f);
+              raw[j] = in ? __ldcg(reinterpret_cast<const uint4*>(po_b + (s0 + j) * split_stride + off))
+                          : make_uint4(0u, 0u, 0u, 0u);
+            }
+            float Mb = M;
+#pragma unroll
+            for (int j = 0; j < kJoinBatch; ++j) Mb = fmaxf(Mb, ml[j].x);
+            if (Mb == -INFINITY) continue;
+            const float r = M == -INFINITY ? 0.f : exp2f(M - Mb);  // rescale what earlier batches added
+            L *= r;
+#pragma unroll
+            for (int x = 0; x < 8; ++x) acc[x] *= r;
+#pragma unroll
+            for (int j = 0; j < kJoinBatch; ++j) {
+              if (ml[j].x == -INFINITY) continue;
+              const float e = exp2f(ml[j].x - Mb);
+              L = fmaf(ml[j].y, e, L);
+              const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+              for (int x = 0; x < 4; ++x) {
+                const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[x]));
+                acc[2 * x] = fmaf(e, v.x, acc[2 * x]);
+                acc[2 * x + 1] = fmaf(e, v.y, acc[2 * x + 1]);
               }
-            const float2 mine = t_ml[t];
-            t_w[t] = (L > 0.f && mine.x != -INFINITY) ? exp2f(mine.x - M) / L : 0.f;
-            const int h = h_lo + hl;
-            if (t - hl * S == 0 && h * kQuads >= i0)  // this CTA holds the head's first quad
-              p.lse[W.bq * p.n_h + W.hg * kHG + h] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
+            }
+            M = Mb;
           }
-          ok = all_sync();
-        }
-        if (ok) {
-          // every thread: up to 4 items (float4 quads) at once, all splits' loads in flight
-          const __nv_bfloat16* po_b = p.part_o + (W.bq * S * p.n_hg + W.hg) * (int64_t)(kHG * kC);
-          const int64_t split_stride = (int64_t)p.n_hg * kHG * kC;
-          const int64_t o_b = (W.bq * p.n_h + W.hg * kHG) * kC;  // the unit's first output row
-          for (int base = i0 + ts; base < i1; base += 4 * kSoftThreads) {
-            float4 acc[4];
-            int off[4], wi[4];
+          const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int it = base + k * kSoftThreads;
-              const int h = it / kQuads, d = (it - h * kQuads) * 4;
-              off[k] = ((d >> 7) * kHG + h) * 128 + (d & 127);  // chunk-major partial
-              wi[k] = (h - h_lo) * S;
-              acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll 4
-            for (int s2 = 0; s2 < S; ++s2) {
+          for (int x = 0; x < 8; ++x) acc[x] *= inv;
+          if (d == 0) p.lse[W.bq * p.n_h + W.hg * kHG + h] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
+          const int64_t at = o_b + (int64_t)h * kC + d;
+          if (MODE != 2 && p.win && p.out_bf16) {  // fused window merge: the merged output
+            uint32_t pk[4];
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                if (base + k * kSoftThreads < i1) {
-                  const uint2 raw = __ldcg(reinterpret_cast<const uint2*>(po_b + s2 * split_stride + off[k]));
-                  const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
-                  const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
-                  const float4 v = make_float4(lo.x, lo.y, hi.x, hi.y);
-                  const float w = t_w[wi[k] + s2];
-                  acc[k].x = fmaf(w, v.x, acc[k].x), acc[k].y = fmaf(w, v.y, acc[k].y);
-                  acc[k].z = fmaf(w, v.z, acc[k].z), acc[k].w = fmaf(w, v.w, acc[k].w);
-                }
-              }
+            for (int x = 0; x < 4; ++x) {
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * x], acc[2 * x + 1]);
+              pk[x] = *reinterpret_cast<const uint32_t*>(&b2);
             }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int it = base + k * kSoftThreads;
-              if (it < i1) {
-                const int h = it / kQuads, d = (it - h * kQuads) * 4;
-                const int64_t at = o_b + (int64_t)h * kC + d;
-                if (MODE != 2 && p.win && p.out_bf16) {  // fused window merge: the merged output
-                  const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[k].x, acc[k].y);
-                  const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[k].z, acc[k].w);
-                  uint2 pk;
-                  pk.x = *reinterpret_cast<const uint32_t*>(&lo), pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-                  *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + at) = pk;
-                } else {
-                  float* dst = (MODE != 2 && p.win) ? static_cast<float*>(p.out) : p.o;
-                  *reinterpret_cast<float4*>(dst + at) = acc[k];
-                }
-              }
-            }
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + at) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          } else {
+            float* dst = (MODE != 2 && p.win) ? static_cast<float*>(p.out) : p.o;
+            *reinterpret_cast<float4*>(dst + at) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            *reinterpret_cast<float4*>(dst + at + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
           }
         }
       }
