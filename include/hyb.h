@@ -96,7 +96,9 @@ typedef enum hyb_dtype {
  *   overlap = 0 (HCA): window = the m rows of block i (positions 0..m-1).
  *
  * Inputs ca, za (and cb, zb when overlap) are [batch][n_rows][c] of in_dtype
- * (F32 or BF16); cb/zb must be NULL when overlap = 0.  bias is float32
+ * (F32 or BF16), sequence b starting in_batch_stride rows after sequence b-1
+ * (0 means "= n_rows"; otherwise >= n_rows: the rows may be a window of a
+ * longer per-sequence buffer); cb/zb must be NULL when overlap = 0.  bias is float32
  * [overlap ? 2m : m][c].  Row r of the inputs is absolute token
  * first_block*m + r; n_rows need not be a multiple of m (a trailing partial
  * block is a tail and produces nothing).
@@ -127,6 +129,7 @@ typedef struct hyb_compress_args {
   int64_t m;
   int64_t first_block;
   int64_t out_batch_stride;
+  int64_t in_batch_stride; /* rows from one sequence's inputs to the next; 0 = n_rows */
   int32_t overlap;
   int32_t in_dtype;  /* hyb_dtype */
   int32_t out_dtype; /* hyb_dtype */

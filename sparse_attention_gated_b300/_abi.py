@@ -24,7 +24,8 @@ _f = ctypes.c_float
 class CompressArgs(ctypes.Structure):
     _fields_ = [("ca", _p), ("cb", _p), ("za", _p), ("zb", _p), ("bias", _p), ("out", _p), ("out_scale", _p),
                 ("batch", _i64), ("n_rows", _i64), ("c", _i64), ("m", _i64), ("first_block", _i64),
-                ("out_batch_stride", _i64), ("overlap", _i32), ("in_dtype", _i32), ("out_dtype", _i32),
+                ("out_batch_stride", _i64), ("in_batch_stride", _i64), ("overlap", _i32), ("in_dtype", _i32),
+                ("out_dtype", _i32),
                 ("dev_status", _p)]
 
 

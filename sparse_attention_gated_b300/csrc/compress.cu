@@ -28,7 +28,7 @@ struct CompressParams {
   const float* bias;
   void* out;
   float* out_scale;
-  int64_t batch, n_rows, c, m, first_block, out_batch_stride, n_out, skip;
+  int64_t batch, n_rows, in_batch_stride, c, m, first_block, out_batch_stride, n_out, skip;
   int overlap;
   int S;  // channels per CTA
   int R;  // row groups (power of two)
@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(kCompressThreads) compress_kernel(CompressPara
   const bool has_prev = p.overlap && p.first_block + lb > 0;
   const int64_t ch0 = (int64_t)blockIdx.y * p.S + g * kCv;
   const int W = (int)(p.overlap ? 2 * m : m);
-  const int64_t base = b * p.n_rows;
+  const int64_t base = b * p.in_batch_stride;
   const Tin* ca = static_cast<const Tin*>(p.ca);
   const Tin* za = static_cast<const Tin*>(p.za);
   const Tin* cb = static_cast<const Tin*>(p.cb);
@@ -196,6 +196,7 @@ cudaError_t launch_compress(const hyb_compress_args* a, int64_t n_out, cudaStrea
   CompressParams p;
   p.ca = a->ca, p.cb = a->cb, p.za = a->za, p.zb = a->zb, p.bias = a->bias, p.out = a->out, p.out_scale = a->out_scale;
   p.batch = a->batch, p.n_rows = a->n_rows, p.c = a->c, p.m = a->m, p.first_block = a->first_block;
+  p.in_batch_stride = a->in_batch_stride > 0 ? a->in_batch_stride : a->n_rows;
   p.out_batch_stride = a->out_batch_stride > 0 ? a->out_batch_stride : n_out;
   p.n_out = n_out;
   p.skip = (a->overlap && a->first_block > 0) ? 1 : 0;

@@ -99,8 +99,12 @@ size_t hyb_compress_workspace_size(const hyb_compress_args*) { return 0; }
 
 static hyb_status validate_compress(const hyb_compress_args* a, int64_t* n_out) {
   if (!a) return fail(HYB_ERR_INVALID_ARG, "hyb_compress: args is NULL");
-  if (a->batch < 0 || a->n_rows < 0 || a->m < 1 || a->first_block < 0 || a->out_batch_stride < 0)
+  if (a->batch < 0 || a->n_rows < 0 || a->m < 1 || a->first_block < 0 || a->out_batch_stride < 0 ||
+      a->in_batch_stride < 0)
     return fail(HYB_ERR_INVALID_ARG, "hyb_compress: negative size or m < 1");
+  if (a->in_batch_stride != 0 && a->in_batch_stride < a->n_rows)
+    return fail(HYB_ERR_INVALID_ARG, "hyb_compress: in_batch_stride %lld < n_rows %lld", (long long)a->in_batch_stride,
+                (long long)a->n_rows);
   if (a->overlap != 0 && a->overlap != 1) return fail(HYB_ERR_INVALID_ARG, "hyb_compress: overlap must be 0 or 1");
   if (a->in_dtype != HYB_F32 && a->in_dtype != HYB_BF16)
     return fail(HYB_ERR_INVALID_ARG, "hyb_compress: in_dtype must be F32 or BF16");

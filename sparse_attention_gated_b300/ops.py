@@ -29,6 +29,19 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _rows_ptr(t, batch_rows):
+    """Pointer of a [B][n][c] view whose rows are contiguous within each sequence and
+    whose sequences start batch_rows rows apart (a window of a longer buffer)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to the hybrid-attention library must be CUDA tensors")
+    B, n, c = t.shape
+    if t.stride(2) != 1 or (n > 1 and t.stride(1) != c) or (B > 1 and t.stride(0) != batch_rows * c):
+        raise ValueError("compressor inputs: rows must be contiguous, sequences equally spaced")
+    return ctypes.c_void_p(t.data_ptr())
+
+
 def _dtype(t):
     try:
         return _DT[t.dtype]
@@ -63,16 +76,21 @@ def compress_out_count(n_rows: int, m: int, overlap: bool, first_block: int = 0)
 
 def compress_args(ca, za, bias, m, cb=None, zb=None, overlap=False, first_block=0, out=None, out_scale=None,
                   out_batch_stride=0, out_dtype=None, dev_status=None, out_row0=0):
-    """Argument struct of hyb_compress.  With out_row0 > 0 the entries are written
-    from row out_row0 of out ([B][rows][c]) on, and the batch stride is out's row count."""
+    """Argument struct of hyb_compress.  The entries are written from row out_row0 of
+    out ([B][rows][c]) on; the batch stride is out's row count."""
     B, n, c = ca.shape
+    # the inputs may be windows of longer per-sequence buffers (all with the same spacing)
+    rows = ca.stride(0) // c if B > 1 else n
     a = _abi.CompressArgs()
-    a.ca, a.cb, a.za, a.zb, a.bias = _ptr(ca), _ptr(cb), _ptr(za), _ptr(zb), _ptr(bias)
+    a.ca, a.cb, a.za, a.zb = (_rows_ptr(t, rows) for t in (ca, cb, za, zb))
+    a.bias = _ptr(bias)
+    a.in_batch_stride = 0 if rows == n else rows
     a.out, a.out_scale = _ptr(out), _ptr(out_scale)
-    if out is not None and out_row0:
-        a.out = ctypes.c_void_p(out.data_ptr() + out_row0 * c * out.element_size())
-        if out_scale is not None:
-            a.out_scale = ctypes.c_void_p(out_scale.data_ptr() + out_row0 * out_scale.element_size())
+    if out is not None:
+        if out_row0:
+            a.out = ctypes.c_void_p(out.data_ptr() + out_row0 * c * out.element_size())
+            if out_scale is not None:
+                a.out_scale = ctypes.c_void_p(out_scale.data_ptr() + out_row0 * out_scale.element_size())
         out_batch_stride = out.shape[1]
     a.batch, a.n_rows, a.c, a.m, a.first_block = B, n, c, m, first_block
     a.out_batch_stride = out_batch_stride

@@ -65,7 +65,7 @@ def _compress_args(**kw):
 @pytest.mark.parametrize("change,status", [
     (dict(ca=None), 1), (dict(m=0), 1), (dict(overlap=2), 1), (dict(in_dtype=_abi.HYB_E4M3), 1),
     (dict(c=48), 2), (dict(out_dtype=_abi.HYB_E4M3), 1), (dict(ca=FAKE + 4), 1), (dict(zb=None), 1),
-    (dict(out_batch_stride=2), 1), (dict(batch=-1), 1),
+    (dict(out_batch_stride=2), 1), (dict(batch=-1), 1), (dict(in_batch_stride=8), 1), (dict(in_batch_stride=-1), 1),
 ])
 def test_compress_rejects_invalid_arguments(lib, change, status):
     a = _compress_args(**change)

@@ -1,0 +1,87 @@
+"""Host logic of the incremental decode session: ring slots and views (no GPU).
+
+Every token's rows carry its position as their value, so a view of a ring can be
+read back as the list of positions it holds.
+"""
+import torch
+
+from sparse_attention_gated_b300.session import DecodeSession
+
+B, C, CI, M, MH, W = 2, 8, 4, 4, 16, 8
+
+
+def _session():
+    return DecodeSession(batch=B, n_max=256, n_h=1, c=C, m=M, m_hca=MH, k=4, n_ih=1, c_I=CI, n_win=W,
+                         bias=torch.zeros(2 * M, C), biasI=torch.zeros(2 * M, CI), bias_h=torch.zeros(MH, C),
+                         device="cpu", dtype=torch.float32)
+
+
+def _rows(p):
+    r = {}
+    for s in ("ca", "cb", "za", "zb", "ch", "zh", "kv", "kv_h"):
+        r[s] = torch.full((B, C), float(p))
+    for s in ("kIa", "kIb", "zIa", "zIb"):
+        r[s] = torch.full((B, CI), float(p))
+    return r
+
+
+def _positions(view):
+    """[B, rows, width] view of marker rows -> the positions of sequence 0 (all equal across b)."""
+    assert torch.equal(view[0], view[-1])
+    return [int(v) for v in view[0, :, 0].tolist()]
+
+
+def _check_views(s, t):
+    """What step t reads: the CSA block view when t completes a block, the HCA block,
+    the window rows."""
+    if (t + 1) % M == 0:
+        i = (t + 1) // M - 1
+        start, rows, fb, row0 = DecodeSession.csa_block_view(i, M)
+        for name in ("ca", "zb", "kIa", "zIb"):
+            got = _positions(s.tails[name][:, start:start + rows])
+            assert got == list(range(fb * M, fb * M + rows)), (t, name, got)
+        # the call writes entries row0.. : the first one it produces (its first block
+        # is only the previous block of the next when first_block > 0)
+        assert row0 == (fb if fb == 0 else fb + 1)
+    if (t + 1) % MH == 0:
+        j = (t + 1) // MH - 1
+        assert _positions(s.tails["ch"][:, :MH]) == list(range(j * MH, (j + 1) * MH))
+    kw, pos0 = s._window("kv", t)
+    n = min(W, t + 1)
+    assert pos0 == max(0, t - W + 1)
+    assert _positions(kw[:, :n]) == list(range(pos0, pos0 + n))
+
+
+def test_rings_hold_what_each_step_reads():
+    s = _session()
+    for t in range(120):
+        s.append(_rows(t))
+        _check_views(s, t)
+        s.t += 1
+
+
+def test_prefill_rings_match_appending_token_by_token():
+    for n0 in (0, 1, 3, 4, 5, 15, 16, 17, 31, 37, 64):
+        a, b = _session(), _session()
+        chunk = {k: torch.stack([_rows(p)[k] for p in range(n0)], dim=1) if n0 else torch.zeros(B, 0, v.shape[1])
+                 for k, v in _rows(0).items()}
+        a.fill_rings(chunk)
+        for p in range(n0):
+            b.append(_rows(p), p)
+        b.t = n0
+        assert a.t == n0
+        # both continue the same way and read the same views
+        for t in range(n0, n0 + 40):
+            for s in (a, b):
+                s.append(_rows(t))
+                _check_views(s, t)
+                s.t += 1
+
+
+def test_window_view_stays_inside_its_allocation():
+    s = _session()
+    for t in range(3 * W):
+        kw, _ = s._window("kv", t)
+        base = s.win["kv"].data_ptr()
+        end = base + s.win["kv"].numel() * s.win["kv"].element_size()
+        assert base <= kw.data_ptr() and kw.data_ptr() + kw.numel() * kw.element_size() <= end
