@@ -20,6 +20,10 @@ least 4x the L2 size.  A second graph of the same K steps with CUDA events
 around every stage, and around the indexer's scoring kernel (recorded by the
 library), gives each stage's and that kernel's average duration (the
 roofline); its own step time is reported beside the headline.
+
+`session` (hybrid decode, one GPU): the same layer pair decoded token by token
+through the incremental session (caches, block tails and windows in rings) over
+the 128 positions ending at the workload's query, one CUDA graph per token.
 """
 from __future__ import annotations
 
@@ -353,11 +357,87 @@ def run_ours(args, w):
         "ms_per_step_with_stage_events": ms_step_ev,
         "step_hbm_roofline_frac": step_roof_s / (ms_step / 1e3),
     }
+    if rank == 0 and world == 1 and w.kind == "hybrid_decode" and not args.no_session:
+        out["session"] = run_session(w, stream)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, steps[0])
     if dist is not None:
         dist.destroy_process_group()
     return out if rank == 0 else None
+
+
+def run_session(w, stream, tokens=128, reps=5):
+    """Token-by-token decode through session.DecodeSession at the workload's context:
+    the `tokens` positions ending at the workload's query position (every m-th token
+    completes a CSA block, the last one an HCA block).  The caches before them hold
+    seeded random entries (as the decode workload's), each token's appends and step are
+    captured as one CUDA graph, and the graphs are replayed in order `reps` times
+    between CUDA events.  The appends are torch copies into the rings (a model's
+    projections would write there directly)."""
+    import math
+
+    import torch
+
+    from sparse_attention_gated_b300 import session
+
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed + 7)
+    Bq, c, cI = w.batch, w.c, w.c_I
+    kv_std = 1.0 / math.sqrt(c)
+    rn = lambda *shape, std=1.0: torch.randn(*shape, generator=g, device=dev).mul_(std)
+    t0, t_end = w.n_ctx - tokens, w.n_ctx
+    s = session.DecodeSession(batch=Bq, n_max=w.n_ctx, n_h=w.n_h, c=c, m=w.m, m_hca=w.m_hca, k=w.k, n_ih=w.n_ih,
+                              c_I=cI, n_win=w.n_win, bias=rn(2 * w.m, c), biasI=rn(2 * w.m, cI),
+                              bias_h=rn(w.m_hca, c), device=dev)
+    nv, nvh = t0 // w.m, t0 // w.m_hca
+    for i in range(0, nv, 16384):  # the entries before t0, in slices (bounded temporaries)
+        j = min(nv, i + 16384)
+        s.csa_kc[:, i:j] = rn(Bq, j - i, c, std=kv_std).to(s.dtype)
+        s.csa_kI[:, i:j] = rn(Bq, j - i, cI).to(torch.float8_e4m3fn)
+    s.csa_kIs[:, :nv] = torch.rand(Bq, nv, generator=g, device=dev) + 0.5
+    s.hca_kc[:, :nvh] = rn(Bq, nvh, c, std=kv_std).to(s.dtype)
+    for r in list(s.tails.values()) + list(s.win.values()):
+        r.copy_(rn(*r.shape, std=kv_std))
+    width = {k: v[0].shape[-1] for k, v in s.token_slots(t0).items()}
+    rows = [{k: rn(Bq, wd, std=kv_std).to(s.dtype) for k, wd in width.items()} for _ in range(tokens)]
+    inp = [dict(q=rn(Bq, w.n_h, c).to(s.dtype), q_h=rn(Bq, w.n_h, c).to(s.dtype),
+                qI=rn(Bq, w.n_ih, cI).to(torch.float8_e4m3fn),
+                qI_scale=torch.rand(Bq, w.n_ih, generator=g, device=dev) + 0.5,
+                w=torch.rand(Bq, w.n_ih, generator=g, device=dev)) for _ in range(tokens)]
+    s.t = t0
+    s.reserve(t_end - 1)
+    with torch.cuda.stream(stream):
+        for i in range(tokens):  # one eager pass (first launches, same writes as the replays)
+            s.append(rows[i])
+            s.step(**inp[i], stream=stream)
+    stream.synchronize()
+    if s.dev_status.item() != 0:
+        raise RuntimeError(f"session decode: device status {s.dev_status.item()}")
+    s.t = t0
+    graphs = []
+    for i in range(tokens):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            s.append(rows[i])
+            s.step(**inp[i], stream=stream)
+        graphs.append(gr)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for gr in graphs:
+            gr.replay()
+        stream.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            for gr in graphs:
+                gr.replay()
+        e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1) / (reps * tokens)
+    return {"tokens_per_s": Bq / (ms / 1e3), "ms_per_token_step": ms, "sequences": Bq,
+            "positions": [t0, t_end - 1], "csa_blocks_completed": tokens // w.m,
+            "hca_blocks_completed": tokens // w.m_hca, "reps": reps,
+            "graph": "one CUDA graph per token (appends + step), replayed in order"}
 
 
 def _ridge(peaks, dt):
@@ -638,6 +718,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-session", action="store_true", help="skip the token-by-token session measurement")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

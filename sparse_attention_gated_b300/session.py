@@ -169,6 +169,31 @@ class DecodeSession:
         self.t = n0
 
     # ------------------------------------------------------------ one token
+    def _sizes(self, t):
+        """Workspace bytes the calls of a step at position t need."""
+        m, mh = self.m, self.m_hca
+        dq = lambda *s: torch.empty(s, dtype=self.dtype, device=self.device)
+        q1 = dq(self.B, 1, self.n_h, self.c)
+        qI1 = torch.empty((self.B, 1, self.n_ih, self.c_I), dtype=torch.float8_e4m3fn, device=self.device)
+        f1 = torch.empty((self.B, 1, self.n_ih), dtype=torch.float32, device=self.device)
+        a = ops.index_args(qI1, f1, self.csa_kI, m, self.k, t, f1, self.csa_kIs, self.idx, None, (t + 1) // m)
+        sizes = {"index": ops.csa_index_topk_workspace_size(a)}
+        kw, pos0 = self._window("kv", t)
+        a = ops.csa_attend_args(q1, self.csa_kc, self.csa_kc, self.idx, self.scale, None, self.lse, (t + 1) // m,
+                                window=ops.window_args(kw, kv_pos0=pos0, q_pos0=t, n_win=self.n_win, out=self.out))
+        sizes["csa"] = int(ops._abi.load().csa_attend_workspace_size(a))
+        a = ops.hca_attend_args(q1, self.hca_kc, self.hca_kc, mh, t, self.scale, None, self.lse_h, (t + 1) // mh,
+                                window=ops.window_args(kw, kv_pos0=pos0, q_pos0=t, n_win=self.n_win, out=self.out_h))
+        sizes["hca"] = int(ops._abi.load().hca_attend_workspace_size(a))
+        return sizes
+
+    def reserve(self, t_last: int):
+        """Allocate the workspaces for every position up to t_last now (for example before
+        capturing steps into CUDA graphs, which must not allocate)."""
+        for t in {self.t, t_last}:
+            for key, n in self._sizes(t).items():
+                self._workspace(key, n)
+
     def _workspace(self, key, nbytes):
         buf = self.ws.get(key)
         if buf is None or buf.numel() < nbytes:
