@@ -397,7 +397,7 @@ def run_session(w, stream, tokens=128, reps=5):
         s.csa_kI[:, i:j] = rn(Bq, j - i, cI).to(torch.float8_e4m3fn)
     s.csa_kIs[:, :nv] = torch.rand(Bq, nv, generator=g, device=dev) + 0.5
     s.hca_kc[:, :nvh] = rn(Bq, nvh, c, std=kv_std).to(s.dtype)
-    for r in list(s.tails.values()) + list(s.win.values()):
+    for r in (s.rings, s.rings_I):
         r.copy_(rn(*r.shape, std=kv_std))
     width = {k: v[0].shape[-1] for k, v in s.token_slots(t0).items()}
     rows = [{k: rn(Bq, wd, std=kv_std).to(s.dtype) for k, wd in width.items()} for _ in range(tokens)]

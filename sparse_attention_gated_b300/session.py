@@ -21,16 +21,19 @@ tokens, and runs one token per ``step``, every stage a library call:
 Layout (device, row-major):
   csa_kc [B][N][c], csa_kI [B][N][c_I] e4m3, csa_kIs [B][N] float32, N = n_max / m;
   hca_kc [B][N'][c], N' = n_max / m'.
-  CSA tails (ca, cb, za, zb at width c; kIa, kIb, zIa, zIb at width c_I): per sequence
-    a ring of 4m rows holding the last 2m tokens twice, token p at slots p mod 2m and
-    p mod 2m + 2m.  The 2m rows an overlapping entry pools (blocks i-1 and i) are then
-    always consecutive, and the compressor reads them in place, sequences 4m rows apart.
-  HCA tails (ch, zh): a ring of m' rows per sequence, token p at slot p mod m' (a block
-    starts at slot 0).
-  Windows (kv for the CSA layer, kv_h for the HCA layer): 2 n_win rows per sequence,
-    token p at slots p mod n_win and p mod n_win + n_win, so that the last n_win
-    tokens are consecutive rows; one spare sequence of rows at the end keeps the
-    window's view (which starts inside the ring) within the allocation.
+  Rings, packed by width: rings [9][B][R][c] (ca, cb, za, zb, ch, zh, kv, kv_h and a
+  spare), R = max(4m, m', 2 n_win); rings_I [4][B][4m][c_I] (kIa, kIb, zIa, zIb).
+  CSA tails (ca, cb, za, zb; kIa, kIb, zIa, zIb): the last 2m tokens twice, token p at
+    slots p mod 2m and p mod 2m + 2m.  The 2m rows an overlapping entry pools (blocks
+    i-1 and i) are then always consecutive, and the compressor reads them in place
+    (sequences R rows apart).
+  HCA tails (ch, zh): token p at slot p mod m' (a block starts at slot 0).
+  Windows (kv for the CSA layer, kv_h for the HCA layer): token p at slots p mod n_win
+    and p mod n_win + n_win, so that the last n_win tokens are consecutive rows; the
+    window's view starts inside its ring and may run into the next one (hence the
+    spare ring), never past the allocation.
+  A token's rows land with one gather and one scatter per width (slot table on the
+  device, indexed by the position modulo the rings' common period).
 """
 from __future__ import annotations
 
@@ -42,6 +45,7 @@ from . import ops
 
 _CSA_STREAMS = ("ca", "cb", "za", "zb")
 _IDX_STREAMS = ("kIa", "kIb", "zIa", "zIb")
+_WIDE = _CSA_STREAMS + ("ch", "zh", "kv", "kv_h")  # width c, ring order in `rings`
 
 
 class DecodeSession:
@@ -63,11 +67,25 @@ class DecodeSession:
         self.csa_kI = torch.zeros((B, self.N, c_I), dtype=torch.float8_e4m3fn, device=dev)
         self.csa_kIs = torch.ones((B, self.N), dtype=torch.float32, device=dev)
         self.hca_kc = torch.zeros((B, self.Nh, c), dtype=dtype, device=dev)
-        self.tails = {s: torch.zeros((B, 4 * m, c), dtype=dtype, device=dev) for s in _CSA_STREAMS}
-        self.tails.update({s: torch.zeros((B, 4 * m, c_I), dtype=dtype, device=dev) for s in _IDX_STREAMS})
-        self.tails.update({s: torch.zeros((B, m_hca, c), dtype=dtype, device=dev) for s in ("ch", "zh")})
-        # windows: flat rows, sequence b at rows [2 n_win b, 2 n_win (b+1)), one spare sequence
-        self.win = {s: torch.zeros(((B + 1) * 2 * n_win, c), dtype=dtype, device=dev) for s in ("kv", "kv_h")}
+        self.R = max(4 * m, m_hca, 2 * n_win)
+        self.rings = torch.zeros((len(_WIDE) + 1, B, self.R, c), dtype=dtype, device=dev)
+        self.rings_I = torch.zeros((len(_IDX_STREAMS), B, 4 * m, c_I), dtype=dtype, device=dev)
+        # the writes of one token: (ring, slot) per write, slots tabulated over the period
+        self.period = math.lcm(2 * m, m_hca, n_win)
+        self._writes, self._writes_I = [], []
+        for s in _WIDE:
+            for j in range(1 if s in ("ch", "zh") else 2):
+                self._writes.append((s, j))
+        for s in _IDX_STREAMS:
+            for j in range(2):
+                self._writes_I.append((s, j))
+        ring_ids = lambda ws, order: torch.tensor([order.index(s) for s, _ in ws], dtype=torch.long, device=dev)
+        self._ring_ids = ring_ids(self._writes, _WIDE)
+        self._ring_ids_I = ring_ids(self._writes_I, _IDX_STREAMS)
+        self._slot_tab = torch.tensor([[self._slot(s, j, p) for s, j in self._writes] for p in range(self.period)],
+                                      dtype=torch.long, device=dev)
+        self._slot_tab_I = torch.tensor([[self._slot(s, j, p) for s, j in self._writes_I]
+                                         for p in range(self.period)], dtype=torch.long, device=dev)
         self.idx = torch.empty((B, 1, k), dtype=torch.int32, device=dev)
         self.lse = torch.empty((B, 1, n_h), dtype=torch.float32, device=dev)
         self.lse_h = torch.empty((B, 1, n_h), dtype=torch.float32, device=dev)
@@ -102,25 +120,35 @@ class DecodeSession:
         # with first_block = 0 the call writes entries 0 and 1 (entry 0 again, same values)
         return start, 2 * m, i - 1, (0 if i == 1 else i)
 
+    def _slot(self, name, j, p):
+        """Ring slot of copy j of token p's row of stream `name`."""
+        if name in ("ch", "zh"):
+            return p % self.m_hca
+        if name in ("kv", "kv_h"):
+            return self.window_slots(p, self.n_win)[j]
+        return self.csa_slots(p, self.m)[j]
+
+    def ring(self, name) -> torch.Tensor:
+        """The ring of a stream: [B][R][c] (or [B][4m][c_I] for the indexer-key streams)."""
+        if name in _IDX_STREAMS:
+            return self.rings_I[_IDX_STREAMS.index(name)]
+        return self.rings[_WIDE.index(name)]
+
     def token_slots(self, p: int | None = None) -> dict:
         """Where token p's rows go: name -> list of [B, width] views (write each)."""
         p = self.t if p is None else p
         v = {}
-        for s in _CSA_STREAMS + _IDX_STREAMS:
-            v[s] = [self.tails[s][:, j] for j in self.csa_slots(p, self.m)]
-        for s in ("ch", "zh"):
-            v[s] = [self.tails[s][:, p % self.m_hca]]
-        W = self.n_win
-        for s in ("kv", "kv_h"):
-            rows = self.win[s][: self.B * 2 * W].view(self.B, 2 * W, self.c)
-            v[s] = [rows[:, j] for j in self.window_slots(p, W)]
+        for s, j in self._writes + self._writes_I:
+            v.setdefault(s, []).append(self.ring(s)[:, self._slot(s, j, p)])
         return v
 
     def append(self, rows: dict, p: int | None = None):
-        """Copy token p's rows (name -> [B, width]) into their slots."""
-        for name, views in self.token_slots(p).items():
-            for dst in views:
-                dst.copy_(rows[name])
+        """Put token p's rows (name -> [B, width]) into their slots: per width, one
+        gather of the rows and one scatter into the rings."""
+        p = self.t if p is None else p
+        k = p % self.period
+        self.rings[self._ring_ids, :, self._slot_tab[k]] = torch.stack([rows[s] for s, _ in self._writes])
+        self.rings_I[self._ring_ids_I, :, self._slot_tab_I[k]] = torch.stack([rows[s] for s, _ in self._writes_I])
 
     # ------------------------------------------------------------ state from a prefix
     def prefill(self, chunk: dict, stream=None):
@@ -155,17 +183,16 @@ class DecodeSession:
             pos = torch.arange(p0, n0, device=self.device)
             if len(pos) == 0:
                 continue
-            src = chunk[s][:, p0:n0]
+            src, r = chunk[s][:, p0:n0], self.ring(s)
             if s in ("kv", "kv_h"):
                 W = self.n_win
-                rows = self.win[s][: self.B * 2 * W].view(self.B, 2 * W, self.c)
-                rows.index_copy_(1, pos % W, src)
-                rows.index_copy_(1, pos % W + W, src)
+                r.index_copy_(1, pos % W, src)
+                r.index_copy_(1, pos % W + W, src)
             elif s in ("ch", "zh"):
-                self.tails[s].index_copy_(1, pos % mh, src)
+                r.index_copy_(1, pos % mh, src)
             else:
-                self.tails[s].index_copy_(1, pos % (2 * m), src)
-                self.tails[s].index_copy_(1, pos % (2 * m) + 2 * m, src)
+                r.index_copy_(1, pos % (2 * m), src)
+                r.index_copy_(1, pos % (2 * m) + 2 * m, src)
         self.t = n0
 
     # ------------------------------------------------------------ one token
@@ -202,10 +229,12 @@ class DecodeSession:
         return buf
 
     def _window(self, name, t):
-        W = self.n_win
-        start, pos0 = self.window_start(t, W)
-        rows = self.win[name][start:start + self.B * 2 * W]
-        return rows.view(self.B, 2 * W, self.c), pos0
+        """The window of query t as [B][R][c] rows (row 0 at the returned position), a
+        view that starts inside the stream's ring."""
+        start, pos0 = self.window_start(t, self.n_win)
+        first = _WIDE.index(name) * self.B * self.R + start
+        rows = self.rings.view(-1, self.c)[first:first + self.B * self.R]
+        return rows.view(self.B, self.R, self.c), pos0
 
     def step(self, *, q, qI, qI_scale, w, q_h, stream=None):
         """Run the layer pair for the token at position t (its rows already appended):
@@ -217,7 +246,7 @@ class DecodeSession:
         if (t + 1) % m == 0:
             i = (t + 1) // m - 1
             start, rows, fb, row0 = self.csa_block_view(i, m)
-            tl = {s: self.tails[s][:, start:start + rows] for s in _CSA_STREAMS + _IDX_STREAMS}
+            tl = {s: self.ring(s)[:, start:start + rows] for s in _CSA_STREAMS + _IDX_STREAMS}
             ops.hyb_compress(tl["ca"], tl["za"], self.bias, m, cb=tl["cb"], zb=tl["zb"], overlap=True,
                              first_block=fb, out=self.csa_kc, out_row0=row0, dev_status=st, stream=stream)
             ops.hyb_compress(tl["kIa"], tl["zIa"], self.biasI, m, cb=tl["kIb"], zb=tl["zIb"], overlap=True,
@@ -225,8 +254,8 @@ class DecodeSession:
                              stream=stream)
         if (t + 1) % mh == 0:
             j = (t + 1) // mh - 1
-            ops.hyb_compress(self.tails["ch"], self.tails["zh"], self.bias_h, mh, first_block=j, out=self.hca_kc,
-                             out_row0=j, dev_status=st, stream=stream)
+            ops.hyb_compress(self.ring("ch")[:, :mh], self.ring("zh")[:, :mh], self.bias_h, mh, first_block=j,
+                             out=self.hca_kc, out_row0=j, dev_status=st, stream=stream)
         n_vis = (t + 1) // m
         q1, q1h = q.unsqueeze(1), q_h.unsqueeze(1)
         qI1, qIs1, w1 = qI.unsqueeze(1), qI_scale.unsqueeze(1), w.unsqueeze(1)

@@ -38,18 +38,19 @@ def _check_views(s, t):
         i = (t + 1) // M - 1
         start, rows, fb, row0 = DecodeSession.csa_block_view(i, M)
         for name in ("ca", "zb", "kIa", "zIb"):
-            got = _positions(s.tails[name][:, start:start + rows])
+            got = _positions(s.ring(name)[:, start:start + rows])
             assert got == list(range(fb * M, fb * M + rows)), (t, name, got)
         # the call writes entries row0.. : the first one it produces (its first block
         # is only the previous block of the next when first_block > 0)
         assert row0 == (fb if fb == 0 else fb + 1)
     if (t + 1) % MH == 0:
         j = (t + 1) // MH - 1
-        assert _positions(s.tails["ch"][:, :MH]) == list(range(j * MH, (j + 1) * MH))
-    kw, pos0 = s._window("kv", t)
-    n = min(W, t + 1)
-    assert pos0 == max(0, t - W + 1)
-    assert _positions(kw[:, :n]) == list(range(pos0, pos0 + n))
+        assert _positions(s.ring("ch")[:, :MH]) == list(range(j * MH, (j + 1) * MH))
+    for name in ("kv", "kv_h"):
+        kw, pos0 = s._window(name, t)
+        n = min(W, t + 1)
+        assert pos0 == max(0, t - W + 1)
+        assert _positions(kw[:, :n]) == list(range(pos0, pos0 + n))
 
 
 def test_rings_hold_what_each_step_reads():
@@ -80,8 +81,31 @@ def test_prefill_rings_match_appending_token_by_token():
 
 def test_window_view_stays_inside_its_allocation():
     s = _session()
-    for t in range(3 * W):
-        kw, _ = s._window("kv", t)
-        base = s.win["kv"].data_ptr()
-        end = base + s.win["kv"].numel() * s.win["kv"].element_size()
-        assert base <= kw.data_ptr() and kw.data_ptr() + kw.numel() * kw.element_size() <= end
+    base = s.rings.data_ptr()
+    end = base + s.rings.numel() * s.rings.element_size()
+    for name in ("kv", "kv_h"):
+        for t in range(3 * W):
+            kw, _ = s._window(name, t)
+            assert base <= kw.data_ptr() and kw.data_ptr() + kw.numel() * kw.element_size() <= end
+
+
+def test_append_writes_every_slot_of_the_token_and_nothing_else():
+    s = _session()
+    for p in range(40):
+        before = (s.rings.clone(), s.rings_I.clone())
+        s.append(_rows(p + 1000), p)
+        changed = (s.rings != before[0]).any(dim=-1).any(dim=1)  # [ring, row]
+        changed_I = (s.rings_I != before[1]).any(dim=-1).any(dim=1)
+        want = torch.zeros_like(changed)
+        want_I = torch.zeros_like(changed_I)
+        for name, views in s.token_slots(p).items():
+            for v in views:
+                assert torch.equal(v, torch.full_like(v, float(p + 1000)))
+        for name in ("ca", "cb", "za", "zb", "ch", "zh", "kv", "kv_h"):
+            r = ("ca", "cb", "za", "zb", "ch", "zh", "kv", "kv_h").index(name)
+            for j in range(1 if name in ("ch", "zh") else 2):
+                want[r, s._slot(name, j, p)] = True
+        for r, name in enumerate(("kIa", "kIb", "zIa", "zIb")):
+            for j in range(2):
+                want_I[r, s._slot(name, j, p)] = True
+        assert torch.equal(changed, want) and torch.equal(changed_I, want_I)
