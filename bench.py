@@ -173,6 +173,27 @@ class ClockSampler:
 # -------------------------------------------------------------- our arm
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest of every rank's x: the job's time is its slowest rank's."""
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job throughput: the units every rank processed over the job's time."""
+    return units_per_rank * world / (ms / 1e3)
+
+
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank decodes its own sequences (weak scaling): a distinct seed per rank."""
+    return seed + 7919 * rank
+
+
 def run_ours(args, w):
     import torch
 
@@ -194,7 +215,7 @@ def run_ours(args, w):
     model = stage_model(w)
     step_bytes = sum(v["bytes"] for v in model.values())
     # each rank processes its own sequences (independent decode streams): different seeds
-    wr = workloads.scaled(w, seed=w.seed + 7919 * rank)
+    wr = workloads.scaled(w, seed=rank_seed(w.seed, rank))
     copies = max(1, min(16, math.ceil(4 * l2 / max(step_bytes, 1))))
     if w.kind == "csa_prefill":
         copies = 1  # 17 GB per copy; one step streams >> L2
@@ -278,11 +299,7 @@ def run_ours(args, w):
         dist.barrier()
     t_timed1 = time.time()
     clocks = sampler.stop(t_busy0, t_timed1)
-    ms_total = start.elapsed_time(end)
-    if dist is not None:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(start.elapsed_time(end), dist, dev)
     ms_step = ms_total / args.steps
     # the evented graph, right after: per-stage and scoring-kernel times
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -299,7 +316,7 @@ def run_ours(args, w):
     scoring_ms = stage_ms.pop("index_scores", None)
 
     units = w.batch if w.decode else w.n_ctx
-    value = units * world / (ms_step / 1e3)
+    value = job_rate(units, world, ms_step)
 
     # -------- e2e through the public API: fresh inputs from pinned host memory
     e2e = run_e2e(args, w, steps[0], stream, units, world, dist)
@@ -576,12 +593,8 @@ def run_e2e(args, w, st, stream, units, world, dist):
         g.replay()
         s1.record(stream)
     torch.cuda.synchronize()
-    ms = s0.elapsed_time(s1)
-    if dist is not None:
-        t = torch.tensor([ms], device=stream.device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": units * world / (ms / n / 1e3), "unit": "queries/s" if w.decode else "tokens/s",
+    ms = max_over_ranks(s0.elapsed_time(s1), dist, stream.device)
+    return {"value": job_rate(units, world, ms / n), "unit": "queries/s" if w.decode else "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / n,
             "graph": "copies + step captured as one CUDA graph",
             "copies": "one H2D and one D2H per step (packed buffers), on their own streams, "
