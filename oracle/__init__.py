@@ -97,6 +97,12 @@ def _declare(lib):
     lib.orc_swa_merge.restype = None
     lib.orc_swa_merge.argtypes = [_i, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _d, _p, _p,
                                   _p, _p]
+    lib.orc_rmsnorm.restype = None
+    lib.orc_rmsnorm.argtypes = [_p, _i64, _i64, _p, _d, _p]
+    lib.orc_rope_partial.restype = None
+    lib.orc_rope_partial.argtypes = [_p, _i64, _i64, _i64, _p, _d, _p]
+    lib.orc_sink_merge.restype = None
+    lib.orc_sink_merge.argtypes = [_p, _p, _i64, _i64, _i64, _p, _p, _p]
     return lib
 
 
@@ -317,3 +323,48 @@ def swa_merge(q, kw, vw, kv_pos0: int, q_pos0: int, n_win: int, scale: float, o_
     load().orc_swa_merge(code, _ptr(q_), _ptr(kw_), _ptr(vw_), B, n_q, n_h, c, n_kv, kv_pos0, q_pos0, n_win,
                          float(scale), _ptr(o_in_), _ptr(lse_in_), _ptr(out), _ptr(lse))
     return out, lse
+
+
+# ------------------------------------------------------ in-branch operations
+
+
+def rmsnorm(x, gamma=None, eps: float = 1e-6) -> np.ndarray:
+    """RMSNorm over the last dimension ("DeepSeek-V4 hybrid attention" (trishampatil.com)
+    section IV: queries and compressed KV entries are RMS-normalised inside both branches).
+    Returns float64 of x's shape."""
+    x_ = np.ascontiguousarray(x, dtype=np.float64)
+    c = x_.shape[-1]
+    rows = int(np.prod(x_.shape[:-1])) if x_.ndim > 1 else 1
+    g = None if gamma is None else np.ascontiguousarray(gamma, dtype=np.float64)
+    y = np.zeros_like(x_)
+    load().orc_rmsnorm(_ptr(x_), rows, c, _ptr(g), float(eps), _ptr(y))
+    return y
+
+
+def rope_partial(x, pos, rope_dims: int = 64, theta: float = 10000.0) -> np.ndarray:
+    """Rotary encoding of the last rope_dims dimensions only (same page, section IV:
+    "partial RoPE"), consecutive pairs rotated by pos * theta^(-2i/rope_dims) (the
+    pairing and frequencies of the PyTorch walkthrough on juhe.plus, "The Code: RoPE
+    Helpers").  x [..., c]; pos broadcastable to x.shape[:-1].  Returns float64."""
+    x_ = np.ascontiguousarray(x, dtype=np.float64)
+    c = x_.shape[-1]
+    lead = x_.shape[:-1]
+    p = np.ascontiguousarray(np.broadcast_to(np.asarray(pos, dtype=np.float64), lead)).reshape(-1)
+    y = np.zeros_like(x_)
+    load().orc_rope_partial(_ptr(x_), int(p.size), c, rope_dims, _ptr(p), float(theta), _ptr(y))
+    return y
+
+
+def sink_merge(o, lse, sink):
+    """Per-head attention sink (same page, section IV): one more logit per head in the
+    softmax denominator with no value.  o [..., n_h, c], lse [..., n_h], sink [n_h].
+    Returns (out, lse) float64."""
+    o_ = np.ascontiguousarray(o, dtype=np.float64)
+    l_ = np.ascontiguousarray(lse, dtype=np.float64)
+    s_ = np.ascontiguousarray(sink, dtype=np.float64)
+    n_h, c = o_.shape[-2], o_.shape[-1]
+    rows = int(np.prod(o_.shape[:-2])) if o_.ndim > 2 else 1
+    out = np.zeros_like(o_)
+    lo = np.zeros_like(l_)
+    load().orc_sink_merge(_ptr(o_), _ptr(l_), rows, n_h, c, _ptr(s_), _ptr(out), _ptr(lo))
+    return out, lo

@@ -513,3 +513,64 @@ void orc_swa_merge(int dtype, const void* q, const void* kw, const void* vw, int
   free(q_h);
   free(o_w);
 }
+
+/* ------------------------------------------------- in-branch operations
+ * [HA] section IV (the hybrid attention block): inside both branches the queries
+ * and the compressed KV entries are RMS-normalised, only the last 64 dimensions
+ * carry rotary position encoding, and every head has a learnable attention sink.
+ * The pages name these without formulas; the textbook definitions are written
+ * out below, with the rotary convention of [JH] "The Code: RoPE Helpers"
+ * (consecutive dimension pairs, frequency theta^(-2i/d)).
+ */
+
+/* RMSNorm of each row: y[d] = x[d] / sqrt(mean_d x^2 + eps) * gamma[d].
+ * x, y [rows][c] double; gamma [c] double (NULL = all ones). */
+void orc_rmsnorm(const double* x, int64_t rows, int64_t c, const double* gamma, double eps, double* y) {
+  for (int64_t r = 0; r < rows; ++r) {
+    double ss = 0.0;
+    for (int64_t d = 0; d < c; ++d) ss += x[r * c + d] * x[r * c + d];
+    double inv = 1.0 / sqrt(ss / (double)c + eps);
+    for (int64_t d = 0; d < c; ++d) y[r * c + d] = x[r * c + d] * inv * (gamma ? gamma[d] : 1.0);
+  }
+}
+
+/* Partial rotary encoding: the last rope_dims dimensions of each row, taken as
+ * consecutive pairs (2i, 2i+1) of that slice, are rotated by the angle
+ * pos[r] * theta^(-2i / rope_dims); the first c - rope_dims dimensions are copied.
+ * x, y [rows][c] double; pos [rows] (the row's position, any real value). */
+void orc_rope_partial(const double* x, int64_t rows, int64_t c, int64_t rope_dims, const double* pos,
+                      double theta, double* y) {
+  int64_t d0 = c - rope_dims;
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t d = 0; d < d0; ++d) y[r * c + d] = x[r * c + d];
+    for (int64_t i = 0; i < rope_dims / 2; ++i) {
+      double freq = pow(theta, -(double)(2 * i) / (double)rope_dims);
+      double ang = pos[r] * freq;
+      double re = x[r * c + d0 + 2 * i], im = x[r * c + d0 + 2 * i + 1];
+      y[r * c + d0 + 2 * i] = re * cos(ang) - im * sin(ang);
+      y[r * c + d0 + 2 * i + 1] = re * sin(ang) + im * cos(ang);
+    }
+  }
+}
+
+/* Attention sink: one more logit s_h per head in the softmax denominator, with no
+ * value.  Given the branch's result (o, lse) over its attended multiset,
+ *   out = o * exp(lse - L),   L = log(exp(lse) + exp(s_h)).
+ * o, out [rows][n_h][c], lse, lse_out [rows][n_h] double; sink [n_h] double
+ * (-inf = no sink).  lse_out may be NULL. */
+void orc_sink_merge(const double* o, const double* lse, int64_t rows, int64_t n_h, int64_t c, const double* sink,
+                    double* out, double* lse_out) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t h = 0; h < n_h; ++h) {
+      double a = lse[r * n_h + h], s = sink[h], L;
+      if (a == -INFINITY && s == -INFINITY)
+        L = -INFINITY;
+      else {
+        double mx = a > s ? a : s;
+        L = mx + log(exp(a - mx) + exp(s - mx));
+      }
+      double w = (a == -INFINITY) ? 0.0 : exp(a - L);
+      for (int64_t d = 0; d < c; ++d) out[(r * n_h + h) * c + d] = w * o[(r * n_h + h) * c + d];
+      if (lse_out) lse_out[r * n_h + h] = L;
+    }
+}

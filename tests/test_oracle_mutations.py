@@ -42,6 +42,20 @@ MUTATIONS = [
     ("quantiser_range", "amax / 448.0f", "amax / 240.0f"),
     ("bf16_rounding_width", "int q = e - 8; ", "int q = e - 9; "),
     ("key_value_swapped", "o_h[d] += p * load_elem(kv_dtype, v,", "o_h[d] += p * load_elem(kv_dtype, k,"),
+    ("rmsnorm_sum_not_mean", "double inv = 1.0 / sqrt(ss / (double)c + eps);", "double inv = 1.0 / sqrt(ss + eps);"),
+    ("rmsnorm_eps_outside_root", "double inv = 1.0 / sqrt(ss / (double)c + eps);",
+     "double inv = 1.0 / (sqrt(ss / (double)c) + eps);"),
+    ("rmsnorm_gain_dropped", "y[r * c + d] = x[r * c + d] * inv * (gamma ? gamma[d] : 1.0);",
+     "y[r * c + d] = x[r * c + d] * inv;"),
+    ("rope_frequency_exponent", "double freq = pow(theta, -(double)(2 * i) / (double)rope_dims);",
+     "double freq = pow(theta, -(double)i / (double)rope_dims);"),
+    ("rope_rotation_sign", "y[r * c + d0 + 2 * i + 1] = re * sin(ang) + im * cos(ang);",
+     "y[r * c + d0 + 2 * i + 1] = -re * sin(ang) + im * cos(ang);"),
+    ("rope_whole_row", "int64_t d0 = c - rope_dims;", "int64_t d0 = 0;"),
+    ("sink_weight_inverted", "double w = (a == -INFINITY) ? 0.0 : exp(a - L);",
+     "double w = (a == -INFINITY) ? 0.0 : exp(L - a);"),
+    ("sink_ignored_in_lse", "        L = mx + log(exp(a - mx) + exp(s - mx));\n      }\n      double w",
+     "        L = a;\n      }\n      double w"),
 ]
 
 

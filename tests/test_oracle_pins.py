@@ -555,3 +555,84 @@ def test_pipeline_never_reads_the_future():
         got = forward(*poisoned)
         for g, b in zip(got, base):
             assert np.array_equal(g[:, : t + 1], b[:, : t + 1])
+
+
+# --------------------------------------------- in-branch operations ([HA] IV)
+
+
+def test_rmsnorm_rows_have_unit_rms_and_ignore_scale():
+    x = _rng(61).normal(size=(7, 64)) * _rng(62).uniform(0.1, 10, size=(7, 1))
+    y = oracle.rmsnorm(x, eps=0.0)
+    assert np.allclose(np.mean(y * y, axis=-1), 1.0, atol=1e-12)
+    assert np.allclose(oracle.rmsnorm(3.5 * x, eps=0.0), y, atol=1e-12)
+    assert np.allclose(oracle.rmsnorm(-x, eps=0.0), -y, atol=1e-12)
+
+
+def test_rmsnorm_worked_values_and_gain():
+    # [3, 4]: mean square 12.5, so the row divides by sqrt(12.5) = 3.5355...
+    y = oracle.rmsnorm(np.array([[3.0, 4.0]]), eps=0.0)
+    assert np.allclose(y, [[0.848528137423857, 1.131370849898476]], atol=1e-12)
+    # a constant row v gives sign(v) in every channel; the gain scales channel by channel
+    g = np.array([2.0, -1.0, 0.5, 4.0])
+    assert np.allclose(oracle.rmsnorm(np.full((1, 4), -0.3), g, eps=0.0), -g, atol=1e-12)
+    # eps enters under the root: a zero row stays zero, and x^2 mean 1 with eps 3 halves the row
+    assert np.all(oracle.rmsnorm(np.zeros((1, 8)), eps=1e-6) == 0.0)
+    assert np.allclose(oracle.rmsnorm(np.ones((1, 8)), eps=3.0), 0.5, atol=1e-12)
+
+
+def test_partial_rope_leaves_the_leading_dims_and_pair_norms():
+    x = _rng(63).normal(size=(5, 96))
+    pos = np.array([0.0, 1.0, 17.0, 1000.0, 123456.0])
+    y = oracle.rope_partial(x, pos, rope_dims=64)
+    assert np.array_equal(y[:, :32], x[:, :32])
+    assert np.allclose(y[0], x[0], atol=0)  # position 0: no rotation
+    pn = lambda a: np.hypot(a[:, 32::2], a[:, 33::2])
+    assert np.allclose(pn(y), pn(x), atol=1e-12)
+
+
+def test_partial_rope_composes_and_depends_on_relative_position_only():
+    r = _rng(64)
+    q, k = r.normal(size=(1, 128)), r.normal(size=(1, 128))
+    a, b = 321.0, 77.0
+    rq = lambda v, p: oracle.rope_partial(v, [p], rope_dims=64)
+    assert np.allclose(rq(rq(q, a), b), rq(q, a + b), atol=1e-9)
+    assert np.isclose((rq(q, a) @ rq(k, b).T).item(), (rq(q, a - b) @ k.T).item(), atol=1e-9)
+
+
+def test_partial_rope_frequencies_worked_values():
+    # rope_dims = 4, theta = 10000: pair 0 turns by the position itself, pair 1 by
+    # position * 10000^(-2/4) = position / 100; so at position 100 both turn by 1 radian
+    x = np.array([[9.0, 1.0, 0.0, 1.0, 0.0]])  # one untouched dim, then the two pairs (1, 0), (1, 0)
+    y = oracle.rope_partial(x, [100.0], rope_dims=4)
+    c1, s1 = math.cos(1.0), math.sin(1.0)
+    c100, s100 = math.cos(100.0), math.sin(100.0)
+    assert np.allclose(y, [[9.0, c100, s100, c1, s1]], atol=1e-12)
+
+
+def test_attention_sink_is_a_value_free_logit_in_the_softmax():
+    # brute force over a tiny multiset: scores z with values v, plus the sink logit s
+    # whose value is the zero vector, through numpy's softmax
+    r = _rng(65)
+    z, v = r.normal(size=(3, 2, 6)), r.normal(size=(3, 2, 6, 5))  # [rows][heads][entries](, dims)
+    s = np.array([0.7, -1.2])
+    o = np.einsum("rhe,rhed->rhd", np.exp(z - z.max(-1, keepdims=True)) /
+                  np.exp(z - z.max(-1, keepdims=True)).sum(-1, keepdims=True), v)
+    lse = np.log(np.exp(z).sum(-1))
+    zs = np.concatenate([z, np.broadcast_to(s[None, :, None], (3, 2, 1))], axis=-1)
+    p = np.exp(zs - zs.max(-1, keepdims=True))
+    p /= p.sum(-1, keepdims=True)
+    want = np.einsum("rhe,rhed->rhd", p[..., :6], v)  # the sink's value is zero
+    out, l2 = oracle.sink_merge(o, lse, s)
+    assert np.allclose(out, want, atol=1e-12)
+    assert np.allclose(l2, np.log(np.exp(zs).sum(-1)), atol=1e-12)
+
+
+def test_attention_sink_special_cases():
+    r = _rng(66)
+    o, lse = r.normal(size=(4, 3, 8)), r.normal(size=(4, 3))
+    out, l2 = oracle.sink_merge(o, lse, np.full(3, -np.inf))  # no sink
+    assert np.array_equal(out, o) and np.array_equal(l2, lse)
+    out, l2 = oracle.sink_merge(o, lse, lse[0])  # row 0: the sink weighs as much as the branch
+    assert np.allclose(out[0], o[0] / 2, atol=1e-12) and np.allclose(l2[0], lse[0] + math.log(2), atol=1e-12)
+    out, l2 = oracle.sink_merge(o, np.full((4, 3), -np.inf), np.zeros(3))  # empty branch: zero output
+    assert np.all(out == 0) and np.allclose(l2, 0.0)
