@@ -270,6 +270,14 @@ typedef struct hyb_window {
  * [batch][kv_stride][c] (vc may equal kc: in the method key = value = the
  * compressed entries).  o float32 [batch][n_q][n_h][c], lse float32
  * [batch][n_q][n_h].  dtype F32 or BF16 (q, kc, vc); float32 accumulation.
+ *
+ * Optional attention sink ([HA] section IV: a learnable sink per head inside
+ * both branches): with `sink` non-NULL (float32 [n_h], natural-log units) each
+ * head's softmax denominator gains exp(sink[h]) with no value, once, on the
+ * call's final result: o (or the fused window's out) is scaled by
+ * exp(lse - L) and lse becomes L = log(exp(lse) + exp(sink[h])).  Because the
+ * result is a log-sum-exp union, a later swa_merge of (o, lse) still yields
+ * the sink applied to the whole union.
  * ------------------------------------------------------------------------ */
 typedef struct hyb_csa_attend_args {
   const void* q;
@@ -289,6 +297,7 @@ typedef struct hyb_csa_attend_args {
   int32_t dtype; /* hyb_dtype */
   int32_t* dev_status;
   const hyb_window* window; /* optional fused window merge (see hyb_window), or NULL */
+  const float* sink;        /* optional per-head attention-sink logits [n_h], or NULL */
 } hyb_csa_attend_args;
 
 /* Workspace of csa_attend and hca_attend: *_workspace_size(a) bytes, 256-byte
@@ -324,6 +333,7 @@ typedef struct hyb_hca_attend_args {
   int32_t dtype;
   int32_t* dev_status;
   const hyb_window* window; /* optional fused window merge (see hyb_window), or NULL */
+  const float* sink;        /* optional per-head attention-sink logits [n_h], or NULL (see csa_attend) */
 } hyb_hca_attend_args;
 
 HYB_API size_t hca_attend_workspace_size(const hyb_hca_attend_args* a);

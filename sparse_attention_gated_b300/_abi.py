@@ -44,13 +44,13 @@ class Window(ctypes.Structure):
 class CsaAttendArgs(ctypes.Structure):
     _fields_ = [("q", _p), ("kc", _p), ("vc", _p), ("idx", _p), ("o", _p), ("lse", _p), ("batch", _i64),
                 ("n_q", _i64), ("n_h", _i64), ("c", _i64), ("n_entries", _i64), ("kv_stride", _i64), ("k", _i64),
-                ("scale", _f), ("dtype", _i32), ("dev_status", _p), ("window", _p)]
+                ("scale", _f), ("dtype", _i32), ("dev_status", _p), ("window", _p), ("sink", _p)]
 
 
 class HcaAttendArgs(ctypes.Structure):
     _fields_ = [("q", _p), ("kc", _p), ("vc", _p), ("o", _p), ("lse", _p), ("batch", _i64), ("n_q", _i64),
                 ("n_h", _i64), ("c", _i64), ("n_entries", _i64), ("kv_stride", _i64), ("m", _i64), ("q_pos0", _i64),
-                ("scale", _f), ("dtype", _i32), ("dev_status", _p), ("window", _p)]
+                ("scale", _f), ("dtype", _i32), ("dev_status", _p), ("window", _p), ("sink", _p)]
 
 
 class SwaArgs(ctypes.Structure):

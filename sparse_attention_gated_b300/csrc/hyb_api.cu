@@ -405,6 +405,15 @@ size_t csa_attend_workspace_size(const hyb_csa_attend_args* a) {
   return attend_workspace(csa_job(a));
 }
 
+// The attention sink on a call's final result: the fused window's out where there is
+// one, else o (float32), and lse.
+static hyb_status apply_sink(const char* name, const hyb_window* w, float* o, float* lse, const float* sink,
+                             int64_t rows, int64_t n_h, int64_t c, void* stream) {
+  void* out = w ? w->out : static_cast<void*>(o);
+  const int32_t dt = w ? w->out_dtype : HYB_F32;
+  return cuda_status(hyb::launch_sink(out, dt, lse, sink, rows * n_h, n_h, c, static_cast<cudaStream_t>(stream)), name);
+}
+
 hyb_status csa_attend(const hyb_csa_attend_args* a, void* workspace, size_t ws_bytes, void* stream) {
   if (!a) return fail(HYB_ERR_INVALID_ARG, "csa_attend: args is NULL");
   hyb_status st = validate_attend_common("csa_attend", a->batch, a->n_q, a->n_h, a->c, a->dtype, a->q, a->kc, a->vc);
@@ -415,10 +424,12 @@ hyb_status csa_attend(const hyb_csa_attend_args* a, void* workspace, size_t ws_b
   if (a->batch == 0 || a->n_q == 0 || a->n_h == 0) return ok();
   if ((!a->o && !a->window) || !a->lse || (a->k > 0 && !a->idx))
     return fail(HYB_ERR_INVALID_ARG, "csa_attend: NULL o/lse/idx");
-  if (!aligned(a->o, lane_align(a->c, HYB_F32)) || !aligned(a->idx, 4) || !aligned(a->lse, 4))
-    return fail(HYB_ERR_INVALID_ARG, "csa_attend: misaligned o/lse/idx");
-  if (a->window) return run_attend_window("csa_attend", csa_job(a), a->window, workspace, ws_bytes, stream);
-  return run_attend("csa_attend", csa_job(a), workspace, ws_bytes, stream);
+  if (!aligned(a->o, lane_align(a->c, HYB_F32)) || !aligned(a->idx, 4) || !aligned(a->lse, 4) || !aligned(a->sink, 4))
+    return fail(HYB_ERR_INVALID_ARG, "csa_attend: misaligned o/lse/idx/sink");
+  st = a->window ? run_attend_window("csa_attend", csa_job(a), a->window, workspace, ws_bytes, stream)
+                 : run_attend("csa_attend", csa_job(a), workspace, ws_bytes, stream);
+  if (st != HYB_OK || !a->sink) return st;
+  return apply_sink("csa_attend", a->window, a->o, a->lse, a->sink, a->batch * a->n_q, a->n_h, a->c, stream);
 }
 
 size_t hca_attend_workspace_size(const hyb_hca_attend_args* a) {
@@ -440,10 +451,12 @@ hyb_status hca_attend(const hyb_hca_attend_args* a, void* workspace, size_t ws_b
   if (a->window && (st = validate_window("hca_attend", hca_job(a), a->window)) != HYB_OK) return st;
   if (a->batch == 0 || a->n_q == 0 || a->n_h == 0) return ok();
   if ((!a->o && !a->window) || !a->lse) return fail(HYB_ERR_INVALID_ARG, "hca_attend: NULL o/lse");
-  if (!aligned(a->o, lane_align(a->c, HYB_F32)) || !aligned(a->lse, 4))
-    return fail(HYB_ERR_INVALID_ARG, "hca_attend: misaligned o/lse");
-  if (a->window) return run_attend_window("hca_attend", hca_job(a), a->window, workspace, ws_bytes, stream);
-  return run_attend("hca_attend", hca_job(a), workspace, ws_bytes, stream);
+  if (!aligned(a->o, lane_align(a->c, HYB_F32)) || !aligned(a->lse, 4) || !aligned(a->sink, 4))
+    return fail(HYB_ERR_INVALID_ARG, "hca_attend: misaligned o/lse/sink");
+  st = a->window ? run_attend_window("hca_attend", hca_job(a), a->window, workspace, ws_bytes, stream)
+                 : run_attend("hca_attend", hca_job(a), workspace, ws_bytes, stream);
+  if (st != HYB_OK || !a->sink) return st;
+  return apply_sink("hca_attend", a->window, a->o, a->lse, a->sink, a->batch * a->n_q, a->n_h, a->c, stream);
 }
 
 size_t swa_merge_workspace_size(const hyb_swa_args* a) {

@@ -182,7 +182,7 @@ def window_args(kw, *, kv_pos0: int, q_pos0: int, n_win: int, out):
     return w
 
 
-def csa_attend_args(q, kc, vc, idx, scale, o, lse, n_entries=None, dev_status=None, window=None):
+def csa_attend_args(q, kc, vc, idx, scale, o, lse, n_entries=None, dev_status=None, window=None, sink=None):
     B, n_q, n_h, c = q.shape
     a = _abi.CsaAttendArgs()
     a.q, a.kc, a.vc, a.idx, a.o, a.lse = _ptr(q), _ptr(kc), _ptr(vc), _ptr(idx), _ptr(o), _ptr(lse)
@@ -195,6 +195,7 @@ def csa_attend_args(q, kc, vc, idx, scale, o, lse, n_entries=None, dev_status=No
     a.dev_status = _ptr(dev_status)
     a._window = window  # keep the struct alive as long as the arguments
     a.window = ctypes.cast(ctypes.pointer(window), ctypes.c_void_p) if window is not None else None
+    a.sink = _ptr(sink)
     return a
 
 
@@ -212,23 +213,24 @@ def _window(q, window):
 
 
 def csa_attend(q, kc, vc, idx, *, scale: float | None = None, n_entries=None, o=None, lse=None, workspace=None,
-               dev_status=None, stream=None, window=None):
+               dev_status=None, stream=None, window=None, sink=None):
     """CSA core attention over the selected entries.  Returns (o, lse), or (out, lse) of the
-    union with a fused window merge (window=dict(kw, kv_pos0, q_pos0, n_win[, out]))."""
+    union with a fused window merge (window=dict(kw, kv_pos0, q_pos0, n_win[, out])).
+    sink: optional float32 [n_h] per-head attention-sink logits, applied to the result."""
     B, n_q, n_h, c = q.shape
     scale = 1.0 / math.sqrt(c) if scale is None else scale
     w, out = _window(q, window)
     if o is None and w is None:
         o = torch.empty((B, n_q, n_h, c), dtype=torch.float32, device=q.device)
     lse = torch.empty((B, n_q, n_h), dtype=torch.float32, device=q.device) if lse is None else lse
-    a = csa_attend_args(q, kc, vc, idx, scale, o, lse, n_entries, dev_status, w)
+    a = csa_attend_args(q, kc, vc, idx, scale, o, lse, n_entries, dev_status, w, sink)
     lib = _abi.load()
     ws, nbytes = _workspace(int(lib.csa_attend_workspace_size(ctypes.byref(a))), workspace, q.device, zeroed=True)
     _abi.check(lib.csa_attend(ctypes.byref(a), ws, nbytes, _stream(stream)), "csa_attend")
     return (out, lse) if w is not None else (o, lse)
 
 
-def hca_attend_args(q, kc, vc, m, q_pos0, scale, o, lse, n_entries=None, dev_status=None, window=None):
+def hca_attend_args(q, kc, vc, m, q_pos0, scale, o, lse, n_entries=None, dev_status=None, window=None, sink=None):
     B, n_q, n_h, c = q.shape
     a = _abi.HcaAttendArgs()
     a.q, a.kc, a.vc, a.o, a.lse = _ptr(q), _ptr(kc), _ptr(vc), _ptr(o), _ptr(lse)
@@ -240,13 +242,15 @@ def hca_attend_args(q, kc, vc, m, q_pos0, scale, o, lse, n_entries=None, dev_sta
     a.dev_status = _ptr(dev_status)
     a._window = window
     a.window = ctypes.cast(ctypes.pointer(window), ctypes.c_void_p) if window is not None else None
+    a.sink = _ptr(sink)
     return a
 
 
 def hca_attend(q, kc, vc, *, m: int, q_pos0: int, scale: float | None = None, n_entries=None, o=None, lse=None,
-               workspace=None, dev_status=None, stream=None, window=None):
+               workspace=None, dev_status=None, stream=None, window=None, sink=None):
     """HCA core attention over every visible entry.  Returns (o, lse), or (out, lse) of the
-    union with a fused window merge (window=dict(kw, kv_pos0, n_win[, out]); q_pos0 as the call's)."""
+    union with a fused window merge (window=dict(kw, kv_pos0, n_win[, out]); q_pos0 as the call's).
+    sink: optional float32 [n_h] per-head attention-sink logits, applied to the result."""
     B, n_q, n_h, c = q.shape
     scale = 1.0 / math.sqrt(c) if scale is None else scale
     if window is not None and "q_pos0" not in window:
@@ -255,7 +259,7 @@ def hca_attend(q, kc, vc, *, m: int, q_pos0: int, scale: float | None = None, n_
     if o is None and w is None:
         o = torch.empty((B, n_q, n_h, c), dtype=torch.float32, device=q.device)
     lse = torch.empty((B, n_q, n_h), dtype=torch.float32, device=q.device) if lse is None else lse
-    a = hca_attend_args(q, kc, vc, m, q_pos0, scale, o, lse, n_entries, dev_status, w)
+    a = hca_attend_args(q, kc, vc, m, q_pos0, scale, o, lse, n_entries, dev_status, w, sink)
     lib = _abi.load()
     ws, nbytes = _workspace(int(lib.hca_attend_workspace_size(ctypes.byref(a))), workspace, q.device, zeroed=True)
     _abi.check(lib.hca_attend(ctypes.byref(a), ws, nbytes, _stream(stream)), "hca_attend")

@@ -112,6 +112,11 @@ def test_attend_and_merge_reject_invalid_arguments(lib):
     a.dtype = _abi.HYB_F32
     a.c = 96
     assert lib.csa_attend(ctypes.byref(a), None, 0, None) == 2
+    a.c = 64
+    a.sink = FAKE + 2  # sink logits must be float-aligned
+    assert lib.csa_attend(ctypes.byref(a), None, 0, None) == 1
+    assert "sink" in lib.hyb_last_error().decode()
+    a.sink = None
     h = _abi.HcaAttendArgs()
     h.q = h.kc = h.vc = h.o = h.lse = FAKE
     h.batch, h.n_q, h.n_h, h.c, h.n_entries, h.m, h.q_pos0, h.dtype = 1, 1, 4, 64, 3, 16, 100, _abi.HYB_F32
