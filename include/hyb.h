@@ -380,6 +380,38 @@ typedef struct hyb_swa_args {
 HYB_API size_t swa_merge_workspace_size(const hyb_swa_args* a);
 HYB_API hyb_status swa_merge(const hyb_swa_args* a, void* workspace, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------------
+ * hyb_rmsnorm_rope -- RMSNorm of each row, then rotary encoding of the row's
+ * last rope_dims dimensions ([HA] section IV: queries and compressed KV
+ * entries are RMS-normalised inside both branches, and only their last 64
+ * dimensions carry rotary position; rotary convention of [JH] "The Code: RoPE
+ * Helpers": consecutive pairs, frequencies theta^(-2i/d)).
+ *
+ * In place on x [rows][c] of dtype F32 or BF16 (c even):
+ *   y = x / sqrt(mean over the row of x^2 + eps) * gamma   (gamma float32 [c],
+ *       NULL = ones; eps >= 0),
+ *   then the pairs (2i, 2i+1) of the last rope_dims dimensions (even, <= c;
+ *   0 = none) are rotated by the angle pos * theta^(-2i / rope_dims), pos =
+ *   pos[r / rows_per_pos] (int64 absolute positions, rows_per_pos >= 1, e.g.
+ *   n_h for a query's heads; NULL with rope_dims > 0 is an error).
+ * Float32 arithmetic; the angle is formed and reduced in float64, so that
+ * positions in the millions keep full float32 accuracy.  No workspace.
+ * ------------------------------------------------------------------------ */
+typedef struct hyb_norm_rope_args {
+  void* x;
+  int64_t rows;
+  int64_t c;
+  const float* gamma;
+  float eps;
+  int32_t dtype; /* hyb_dtype: F32 or BF16 */
+  const int64_t* pos;
+  int64_t rows_per_pos;
+  int64_t rope_dims;
+  double theta;
+} hyb_norm_rope_args;
+
+HYB_API hyb_status hyb_rmsnorm_rope(const hyb_norm_rope_args* a, void* stream);
+
 /* ------------------------------------------------------------------------ misc */
 HYB_API const char* hyb_status_string(hyb_status s);
 HYB_API const char* hyb_last_error(void);

@@ -53,6 +53,11 @@ class HcaAttendArgs(ctypes.Structure):
                 ("scale", _f), ("dtype", _i32), ("dev_status", _p), ("window", _p), ("sink", _p)]
 
 
+class NormRopeArgs(ctypes.Structure):
+    _fields_ = [("x", _p), ("rows", _i64), ("c", _i64), ("gamma", _p), ("eps", _f), ("dtype", _i32), ("pos", _p),
+                ("rows_per_pos", _i64), ("rope_dims", _i64), ("theta", ctypes.c_double)]
+
+
 class SwaArgs(ctypes.Structure):
     _fields_ = [("q", _p), ("kw", _p), ("vw", _p), ("o_in", _p), ("lse_in", _p), ("out", _p), ("lse_out", _p),
                 ("batch", _i64), ("n_q", _i64), ("n_h", _i64), ("c", _i64), ("n_kv", _i64), ("kv_pos0", _i64),
@@ -75,6 +80,7 @@ SIGNATURES = {
     "hca_attend": (ctypes.c_int, [ctypes.POINTER(HcaAttendArgs), _p, ctypes.c_size_t, _p]),
     "swa_merge_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(SwaArgs)]),
     "swa_merge": (ctypes.c_int, [ctypes.POINTER(SwaArgs), _p, ctypes.c_size_t, _p]),
+    "hyb_rmsnorm_rope": (ctypes.c_int, [ctypes.POINTER(NormRopeArgs), _p]),
     "hyb_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "hyb_last_error": (ctypes.c_char_p, []),
     "hyb_version": (_i32, []),

@@ -2,6 +2,7 @@
 // validation (before any launch), workspace sizing, dispatch to the kernels
 // and error reporting.  No device memory is allocated here.
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -485,6 +486,26 @@ hyb_status swa_merge(const hyb_swa_args* a, void* workspace, size_t ws_bytes, vo
       !aligned(a->lse_in, 4) || !aligned(a->lse_out, 4))
     return fail(HYB_ERR_INVALID_ARG, "swa_merge: misaligned out/o_in/lse");
   return run_attend("swa_merge", swa_job(a), workspace, ws_bytes, stream);
+}
+
+// ---------------------------------------------------------- RMSNorm + RoPE
+
+hyb_status hyb_rmsnorm_rope(const hyb_norm_rope_args* a, void* stream) {
+  if (!a) return fail(HYB_ERR_INVALID_ARG, "hyb_rmsnorm_rope: args is NULL");
+  if (a->rows < 0 || a->c < 2 || a->c % 2 != 0)
+    return fail(HYB_ERR_INVALID_ARG, "hyb_rmsnorm_rope: rows < 0 or c not even and >= 2");
+  if (a->dtype != HYB_F32 && a->dtype != HYB_BF16)
+    return fail(HYB_ERR_INVALID_ARG, "hyb_rmsnorm_rope: dtype must be F32 or BF16");
+  if (!(a->eps >= 0.f) || !std::isfinite(a->eps)) return fail(HYB_ERR_INVALID_ARG, "hyb_rmsnorm_rope: eps must be >= 0");
+  if (a->rope_dims < 0 || a->rope_dims % 2 != 0 || a->rope_dims > a->c)
+    return fail(HYB_ERR_INVALID_ARG, "hyb_rmsnorm_rope: rope_dims must be even and <= c");
+  if (a->rope_dims > 0 && (!a->pos || a->rows_per_pos < 1 || !(a->theta > 0.0)))
+    return fail(HYB_ERR_INVALID_ARG, "hyb_rmsnorm_rope: rotation needs pos, rows_per_pos >= 1 and theta > 0");
+  if (a->rows == 0) return ok();
+  if (!a->x) return fail(HYB_ERR_INVALID_ARG, "hyb_rmsnorm_rope: x is NULL");
+  if (!aligned(a->x, 2 * elem_size(a->dtype)) || !aligned(a->gamma, 4) || !aligned(a->pos, 8))
+    return fail(HYB_ERR_INVALID_ARG, "hyb_rmsnorm_rope: misaligned x/gamma/pos");
+  return cuda_status(hyb::launch_norm_rope(a, static_cast<cudaStream_t>(stream)), "hyb_rmsnorm_rope");
 }
 
 }  // extern "C"

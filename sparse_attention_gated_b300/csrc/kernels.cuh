@@ -24,6 +24,9 @@ constexpr size_t kTopkZeroRegionBytes =
 bool compress_shape_supported(int64_t c);
 cudaError_t launch_compress(const hyb_compress_args* a, int64_t n_out, cudaStream_t s);
 
+// norm_rope.cu
+cudaError_t launch_norm_rope(const hyb_norm_rope_args* a, cudaStream_t s);
+
 // sink.cu: rows = batch * n_q * n_h rows of c values (out_dtype F32 or BF16) and their lse
 cudaError_t launch_sink(void* out, int32_t out_dtype, float* lse, const float* sink, int64_t rows, int64_t n_h,
                         int64_t c, cudaStream_t s);

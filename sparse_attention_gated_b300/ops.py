@@ -294,3 +294,21 @@ def swa_merge(q, kw, vw, *, kv_pos0: int, q_pos0: int, n_win: int, scale: float 
     ws, nbytes = _workspace(int(lib.swa_merge_workspace_size(ctypes.byref(a))), workspace, q.device)
     _abi.check(lib.swa_merge(ctypes.byref(a), ws, nbytes, _stream(stream)), "swa_merge")
     return (out, lse_out) if want_lse else out
+
+
+# ------------------------------------------------------------ RMSNorm + RoPE
+
+
+def rmsnorm_rope(x, *, gamma=None, eps: float = 1e-6, pos=None, rows_per_pos: int = 1, rope_dims: int = 64,
+                 theta: float = 10000.0, stream=None):
+    """In place: RMSNorm of every row of x [..., c] (float32 or bf16), then rotary
+    encoding of its last rope_dims dimensions at positions pos (int64, one per
+    rows_per_pos consecutive rows; rope_dims=0 or pos=None: no rotation).  Returns x."""
+    c = x.shape[-1]
+    a = _abi.NormRopeArgs()
+    a.x, a.rows, a.c = _ptr(x), x.numel() // c, c
+    a.gamma, a.eps, a.dtype = _ptr(gamma), eps, _dtype(x)
+    a.pos, a.rows_per_pos = _ptr(pos), rows_per_pos
+    a.rope_dims, a.theta = (rope_dims if pos is not None else 0), theta
+    _abi.check(_abi.load().hyb_rmsnorm_rope(ctypes.byref(a), _stream(stream)), "hyb_rmsnorm_rope")
+    return x

@@ -170,3 +170,19 @@ def test_packed_step_io_keeps_values_and_aliases_one_buffer():
         off = st.buf[k].data_ptr() - dev_out.data_ptr()
         assert 0 <= off < dev_out.numel() and off % 256 == 0, k
         assert torch.equal(st.buf[k], outs_before[k]), k
+
+
+def test_rmsnorm_rope_rejects_invalid_arguments(lib):
+    def args(**kw):
+        a = _abi.NormRopeArgs()
+        a.x, a.rows, a.c, a.eps, a.dtype = FAKE, 4, 64, 1e-6, _abi.HYB_F32
+        a.pos, a.rows_per_pos, a.rope_dims, a.theta = FAKE, 1, 16, 10000.0
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return a
+    for bad in (dict(c=63), dict(c=0), dict(dtype=_abi.HYB_E4M3), dict(rope_dims=66), dict(rope_dims=15),
+                dict(pos=None), dict(rows_per_pos=0), dict(theta=0.0), dict(eps=-1.0), dict(x=None), dict(x=FAKE + 4),
+                dict(pos=FAKE + 4), dict(rows=-1)):
+        assert lib.hyb_rmsnorm_rope(ctypes.byref(args(**bad)), None) == 1, bad
+        assert lib.hyb_last_error()
+    assert lib.hyb_rmsnorm_rope(ctypes.byref(args(rows=0)), None) == 0  # nothing to do, nothing launched
