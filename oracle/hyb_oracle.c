@@ -19,7 +19,8 @@
  *
  * Sources (web pages on DeepSeek-V4):
  *   [HA]  "DeepSeek-V4 hybrid attention: CSA, HCA, mHC, MoE" (trishampatil.com),
- *         sections V.1 (compression with overlap), V.2 (lightning indexer),
+ *         sections IV (RMSNorm, partial RoPE and attention sink inside both
+ *         branches), V.1 (compression with overlap), V.2 (lightning indexer),
  *         V.3 (core attention), VI (HCA).
  *   [DV4] "DeepSeek-V4: Anatomy of an Open-Source Frontier Model"
  *         (modernaiengineering.com), "One query in a CSA layer",
@@ -28,6 +29,8 @@
  *         section 9 (heterogeneous KV cache: tails, window).
  *   [MA]  "Mastering DeepSeek-V4 Architecture, Course 1" (mailtotanvir.github.io),
  *         model configurations table.
+ *   [JH]  PyTorch walkthrough re-posted on juhe.plus, "The Code: RoPE Helpers"
+ *         (rotary convention: consecutive pairs, frequencies theta^(-2i/d)).
  *
  * Readings taken where the pages are silent (each also listed in the design
  * notes of the repository):
