@@ -182,8 +182,14 @@ def window_args(kw, *, kv_pos0: int, q_pos0: int, n_win: int, out):
     return w
 
 
+def _check_sink(sink, n_h):
+    if sink is not None and (sink.dtype != torch.float32 or sink.numel() != n_h):
+        raise ValueError("sink must be float32 [n_h]")
+
+
 def csa_attend_args(q, kc, vc, idx, scale, o, lse, n_entries=None, dev_status=None, window=None, sink=None):
     B, n_q, n_h, c = q.shape
+    _check_sink(sink, n_h)
     a = _abi.CsaAttendArgs()
     a.q, a.kc, a.vc, a.idx, a.o, a.lse = _ptr(q), _ptr(kc), _ptr(vc), _ptr(idx), _ptr(o), _ptr(lse)
     a.batch, a.n_q, a.n_h, a.c = B, n_q, n_h, c
@@ -232,6 +238,7 @@ def csa_attend(q, kc, vc, idx, *, scale: float | None = None, n_entries=None, o=
 
 def hca_attend_args(q, kc, vc, m, q_pos0, scale, o, lse, n_entries=None, dev_status=None, window=None, sink=None):
     B, n_q, n_h, c = q.shape
+    _check_sink(sink, n_h)
     a = _abi.HcaAttendArgs()
     a.q, a.kc, a.vc, a.o, a.lse = _ptr(q), _ptr(kc), _ptr(vc), _ptr(o), _ptr(lse)
     a.batch, a.n_q, a.n_h, a.c = B, n_q, n_h, c
@@ -305,8 +312,13 @@ def rmsnorm_rope(x, *, gamma=None, eps: float = 1e-6, pos=None, rows_per_pos: in
     encoding of its last rope_dims dimensions at positions pos (int64, one per
     rows_per_pos consecutive rows; rope_dims=0 or pos=None: no rotation).  Returns x."""
     c = x.shape[-1]
+    rows = x.numel() // c
+    if pos is not None and (pos.dtype != torch.int64 or pos.numel() * rows_per_pos < rows):
+        raise ValueError("pos must be int64 with one position per rows_per_pos rows")
+    if gamma is not None and (gamma.dtype != torch.float32 or gamma.numel() != c):
+        raise ValueError("gamma must be float32 [c]")
     a = _abi.NormRopeArgs()
-    a.x, a.rows, a.c = _ptr(x), x.numel() // c, c
+    a.x, a.rows, a.c = _ptr(x), rows, c
     a.gamma, a.eps, a.dtype = _ptr(gamma), eps, _dtype(x)
     a.pos, a.rows_per_pos = _ptr(pos), rows_per_pos
     a.rope_dims, a.theta = (rope_dims if pos is not None else 0), theta
