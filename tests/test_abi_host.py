@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from sparse_attention_gated_b300 import _abi
 
@@ -186,3 +187,19 @@ def test_rmsnorm_rope_rejects_invalid_arguments(lib):
         assert lib.hyb_rmsnorm_rope(ctypes.byref(args(**bad)), None) == 1, bad
         assert lib.hyb_last_error()
     assert lib.hyb_rmsnorm_rope(ctypes.byref(args(rows=0)), None) == 0  # nothing to do, nothing launched
+
+
+def test_binding_rejects_bad_sink_positions_and_gain_before_any_call():
+    from sparse_attention_gated_b300 import ops
+    q = torch.zeros(1, 1, 4, 64)
+    with pytest.raises(ValueError):
+        ops.csa_attend_args(q, q, q, None, 0.1, None, None, sink=torch.zeros(3))
+    with pytest.raises(ValueError):
+        ops.hca_attend_args(q, q, q, 4, 0, 0.1, None, None, sink=torch.zeros(4, dtype=torch.float64))
+    x = torch.zeros(6, 64)
+    with pytest.raises(ValueError):
+        ops.rmsnorm_rope(x, pos=torch.zeros(5, dtype=torch.int64))  # 6 rows need 6 positions
+    with pytest.raises(ValueError):
+        ops.rmsnorm_rope(x, pos=torch.zeros(6, dtype=torch.int32))
+    with pytest.raises(ValueError):
+        ops.rmsnorm_rope(x, gamma=torch.ones(32), pos=None)
