@@ -103,6 +103,8 @@ def _declare(lib):
     lib.orc_rope_partial.argtypes = [_p, _i64, _i64, _i64, _p, _d, _p]
     lib.orc_sink_merge.restype = None
     lib.orc_sink_merge.argtypes = [_p, _p, _i64, _i64, _i64, _p, _p, _p]
+    lib.orc_grouped_out_proj.restype = None
+    lib.orc_grouped_out_proj.argtypes = [_p, _p, _i64, _i64, _i64, _i64, _i64, _p]
     return lib
 
 
@@ -368,3 +370,24 @@ def sink_merge(o, lse, sink):
     lo = np.zeros_like(l_)
     load().orc_sink_merge(_ptr(o_), _ptr(l_), rows, n_h, c, _ptr(s_), _ptr(out), _ptr(lo))
     return out, lo
+
+
+def grouped_out_proj(o, W, W_out=None) -> np.ndarray:
+    """Grouped output projection ("DeepSeek-V4 hybrid attention" (trishampatil.com)
+    section V.3): o [..., n_h, c] (the heads of each row), W [g, d_g, (n_h/g)*c]: group j
+    of n_h/g consecutive heads projected by W[j]; the g results concatenated
+    ([..., g*d_g]), then, when W_out [d, g*d_g] is given, mapped to d by that matrix (a
+    library matmul).  Returns float64."""
+    o_ = np.ascontiguousarray(o, dtype=np.float64)
+    W_ = np.ascontiguousarray(W, dtype=np.float64)
+    n_h, c = o_.shape[-2], o_.shape[-1]
+    g, d_g, in_g = W_.shape
+    if n_h % g or in_g != (n_h // g) * c:
+        raise ValueError("W must be [g, d_g, (n_h/g)*c] with g dividing n_h")
+    lead = o_.shape[:-2]
+    rows = int(np.prod(lead)) if lead else 1
+    out = np.zeros(lead + (g * d_g,))
+    load().orc_grouped_out_proj(_ptr(o_), _ptr(W_), rows, n_h, c, g, d_g, _ptr(out))
+    if W_out is not None:
+        out = out @ np.asarray(W_out, dtype=np.float64).T
+    return out

@@ -577,3 +577,22 @@ void orc_sink_merge(const double* o, const double* lse, int64_t rows, int64_t n_
       if (lse_out) lse_out[r * n_h + h] = L;
     }
 }
+
+/* ------------------------------------------------ grouped output projection
+ * [HA] section V.3 ("Core attention and grouped output"): the concatenated head
+ * outputs (n_h heads of c values) are split into g groups of n_h/g consecutive
+ * heads; group j's (n_h/g)*c values are projected by its own d_g x (n_h/g)*c
+ * matrix, and the g results are concatenated (g*d_g values per row).
+ * o [rows][n_h*c], W [g][d_g][(n_h/g)*c], out [rows][g*d_g], all double.
+ */
+void orc_grouped_out_proj(const double* o, const double* W, int64_t rows, int64_t n_h, int64_t c, int64_t g,
+                          int64_t d_g, double* out) {
+  int64_t in_g = (n_h / g) * c;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t j = 0; j < g; ++j)
+      for (int64_t e = 0; e < d_g; ++e) {
+        double acc = 0.0;
+        for (int64_t d = 0; d < in_g; ++d) acc += W[(j * d_g + e) * in_g + d] * o[r * n_h * c + j * in_g + d];
+        out[r * g * d_g + j * d_g + e] = acc;
+      }
+}

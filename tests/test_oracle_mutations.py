@@ -56,6 +56,8 @@ MUTATIONS = [
      "double w = (a == -INFINITY) ? 0.0 : exp(L - a);"),
     ("sink_ignored_in_lse", "        L = mx + log(exp(a - mx) + exp(s - mx));\n      }\n      double w",
      "        L = a;\n      }\n      double w"),
+    ("grouped_proj_wrong_group_input", "o[r * n_h * c + j * in_g + d]", "o[r * n_h * c + d]"),
+    ("grouped_proj_transposed_weight", "W[(j * d_g + e) * in_g + d]", "W[(j * in_g + d) * d_g + e]"),
 ]
 
 

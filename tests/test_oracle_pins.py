@@ -636,3 +636,42 @@ def test_attention_sink_special_cases():
     assert np.allclose(out[0], o[0] / 2, atol=1e-12) and np.allclose(l2[0], lse[0] + math.log(2), atol=1e-12)
     out, l2 = oracle.sink_merge(o, np.full((4, 3), -np.inf), np.zeros(3))  # empty branch: zero output
     assert np.all(out == 0) and np.allclose(l2, 0.0)
+
+
+# ------------------------------------------- grouped output projection ([HA] V.3)
+
+
+def test_grouped_projection_is_a_block_diagonal_matmul():
+    import scipy.linalg
+
+    r = _rng(71)
+    n_h, c, g, d_g = 8, 6, 4, 5
+    o = r.normal(size=(3, 2, n_h, c))
+    W = r.normal(size=(g, d_g, (n_h // g) * c))
+    got = oracle.grouped_out_proj(o, W)
+    want = o.reshape(3, 2, n_h * c) @ scipy.linalg.block_diag(*W).T
+    assert got.shape == (3, 2, g * d_g) and np.allclose(got, want, atol=1e-12)
+
+
+def test_grouped_projection_with_one_group_is_a_plain_projection_and_maps_to_d():
+    r = _rng(72)
+    n_h, c, d_g, d = 4, 3, 7, 5
+    o = r.normal(size=(6, n_h, c))
+    W = r.normal(size=(1, d_g, n_h * c))
+    assert np.allclose(oracle.grouped_out_proj(o, W), o.reshape(6, -1) @ W[0].T, atol=1e-12)
+    W_out = r.normal(size=(d, d_g))
+    assert np.allclose(oracle.grouped_out_proj(o, W, W_out), o.reshape(6, -1) @ W[0].T @ W_out.T, atol=1e-12)
+
+
+def test_grouped_projection_keeps_groups_apart():
+    # a change in head h moves only the output block of its group h // (n_h / g)
+    r = _rng(73)
+    n_h, c, g, d_g = 8, 4, 4, 3
+    o = r.normal(size=(1, n_h, c))
+    W = r.normal(size=(g, d_g, (n_h // g) * c))
+    base = oracle.grouped_out_proj(o, W)
+    for h in range(n_h):
+        o2 = o.copy()
+        o2[0, h] += 1.0
+        moved = np.abs(oracle.grouped_out_proj(o2, W) - base).reshape(g, d_g).max(axis=1) > 0
+        assert np.array_equal(moved, np.arange(g) == h // (n_h // g))
