@@ -151,8 +151,6 @@ def test_packed_step_io_keeps_values_and_aliases_one_buffer():
     contiguous buffer at a 256-byte aligned offset, with its values unchanged."""
     from sparse_attention_gated_b300 import pipeline, workloads
 
-    import torch
-
     w = workloads.scaled(workloads.WORKLOADS["tiny_f32"], n_ctx=64)
     # the buffers only (constructing a step sizes workspaces through the CUDA library)
     st = pipeline.HybridStep.__new__(pipeline.HybridStep)
@@ -203,3 +201,31 @@ def test_binding_rejects_bad_sink_positions_and_gain_before_any_call():
         ops.rmsnorm_rope(x, pos=torch.zeros(6, dtype=torch.int32))
     with pytest.raises(ValueError):
         ops.rmsnorm_rope(x, gamma=torch.ones(32), pos=None)
+
+
+def test_fused_window_arguments_are_validated_before_any_launch(lib):
+    def csa(**w):
+        win = _abi.Window()
+        win.kw, win.out, win.out_dtype = FAKE, FAKE, _abi.HYB_BF16
+        win.n_kv, win.kv_pos0, win.q_pos0, win.n_win = 256, 1000, 1127, 128
+        for k, v in w.items():
+            setattr(win, k, v)
+        a = _abi.CsaAttendArgs()
+        a.q = a.kc = a.vc = a.idx = a.lse = FAKE
+        a.batch, a.n_q, a.n_h, a.c, a.n_entries, a.k, a.scale, a.dtype = 1, 1, 64, 512, 100, 16, 0.1, _abi.HYB_BF16
+        a._w = win
+        a.window = ctypes.cast(ctypes.pointer(win), ctypes.c_void_p)
+        return a
+    for bad in (dict(n_win=0), dict(out_dtype=_abi.HYB_E4M3), dict(kv_pos0=1001),  # first window row not held
+                dict(n_kv=127), dict(q_pos0=-1), dict(kw=None), dict(out=None), dict(kw=FAKE + 2)):
+        assert lib.csa_attend(ctypes.byref(csa(**bad)), None, 0, None) == 1, bad
+        assert lib.hyb_last_error()
+    h = _abi.HcaAttendArgs()
+    h.q = h.kc = h.vc = h.lse = FAKE
+    h.batch, h.n_q, h.n_h, h.c, h.n_entries, h.m, h.q_pos0, h.dtype = 1, 1, 64, 512, 100, 16, 1599, _abi.HYB_BF16
+    win = _abi.Window()
+    win.kw, win.out, win.out_dtype, win.n_kv, win.kv_pos0, win.q_pos0, win.n_win = FAKE, FAKE, _abi.HYB_BF16, 128, \
+        1472, 1598, 128
+    h.window = ctypes.cast(ctypes.pointer(win), ctypes.c_void_p)
+    assert lib.hca_attend(ctypes.byref(h), None, 0, None) == 1  # the window's query is not the call's
+    assert "q_pos0" in lib.hyb_last_error().decode()
