@@ -103,6 +103,14 @@ def _declare(lib):
     lib.orc_rope_partial.argtypes = [_p, _i64, _i64, _i64, _p, _d, _p]
     lib.orc_sink_merge.restype = None
     lib.orc_sink_merge.argtypes = [_p, _p, _i64, _i64, _i64, _p, _p, _p]
+    lib.orc_e2m1_decode.restype = _d
+    lib.orc_e2m1_decode.argtypes = [ctypes.c_uint8]
+    lib.orc_e8m0_decode.restype = _d
+    lib.orc_e8m0_decode.argtypes = [ctypes.c_uint8]
+    lib.orc_e2m1_encode.restype = ctypes.c_uint8
+    lib.orc_e2m1_encode.argtypes = [ctypes.c_float]
+    lib.orc_quantise_mxfp4_rows.restype = None
+    lib.orc_quantise_mxfp4_rows.argtypes = [_p, _i64, _i64, _p, _p]
     lib.orc_grouped_out_proj.restype = None
     lib.orc_grouped_out_proj.argtypes = [_p, _p, _i64, _i64, _i64, _i64, _i64, _p]
     return lib
@@ -391,3 +399,46 @@ def grouped_out_proj(o, W, W_out=None) -> np.ndarray:
     if W_out is not None:
         out = out @ np.asarray(W_out, dtype=np.float64).T
     return out
+
+
+# ------------------------------------------------------------------ MXFP4
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    lib = load()
+    c = np.asarray(codes, dtype=np.uint8).ravel()
+    return np.array([lib.orc_e2m1_decode(int(v)) for v in c]).reshape(np.shape(codes))
+
+
+def e8m0_decode(codes) -> np.ndarray:
+    lib = load()
+    c = np.asarray(codes, dtype=np.uint8).ravel()
+    return np.array([lib.orc_e8m0_decode(int(v)) for v in c]).reshape(np.shape(codes))
+
+
+def e2m1_encode(x) -> np.ndarray:
+    lib = load()
+    a = np.asarray(x, dtype=np.float32).ravel()
+    return np.array([lib.orc_e2m1_encode(float(v)) for v in a], dtype=np.uint8).reshape(np.shape(x))
+
+
+def quantise_mxfp4_rows(x) -> tuple[np.ndarray, np.ndarray]:
+    """MXFP4 rows (reading R23): e2m1 codes [..., c] (one per byte) and e8m0 block
+    scales [..., c/32]; decisions in float32."""
+    x_ = np.ascontiguousarray(x, dtype=np.float32)
+    shp = x_.shape
+    c = shp[-1]
+    if c % 32:
+        raise ValueError("MXFP4 rows need a multiple of 32 values")
+    rows = int(np.prod(shp[:-1])) if x_.ndim > 1 else 1
+    codes = np.zeros(shp, dtype=np.uint8)
+    scales = np.zeros(shp[:-1] + (c // 32,), dtype=np.uint8)
+    load().orc_quantise_mxfp4_rows(_ptr(x_), rows, c, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def mxfp4_decode(codes, scales) -> np.ndarray:
+    """Values of MXFP4 rows: e2m1(code) * e8m0(scale of its block of 32)."""
+    v = e2m1_decode(codes)
+    s = e8m0_decode(scales)
+    return v * np.repeat(s, 32, axis=-1)

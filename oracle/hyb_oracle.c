@@ -278,6 +278,69 @@ void orc_quantise_fp8_rows(const float* x, int64_t rows, int64_t c, uint8_t* cod
   }
 }
 
+/* -------------------------------------------------------------- MXFP4
+ * FP4 for the indexer's query-key path ("DeepSeek-V4: Anatomy..." (modernaiengineering.com),
+ * "FP4 quantization-aware training": V4 applies FP4 to the indexer's query-key path).
+ * The pages name no format; the OCP microscaling one is taken (reading R23): e2m1
+ * elements in blocks of 32 sharing one e8m0 power-of-two scale.
+ */
+
+/* e2m1: sign(1) exponent(2, bias 1) mantissa(1); exponent field 0 is subnormal
+ * (0.m * 2^0); no infinities or NaN; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+double orc_e2m1_decode(uint8_t v) {
+  int sign = (v >> 3) & 1;
+  int e = (v >> 1) & 3;
+  int mant = v & 1;
+  double mag = (e == 0) ? 0.5 * (double)mant : ldexp(1.0 + 0.5 * (double)mant, e - 1);
+  return sign ? -mag : mag;
+}
+
+/* e8m0: 2^(e - 127); e = 255 is NaN. */
+double orc_e8m0_decode(uint8_t e) { return e == 255 ? NAN : ldexp(1.0, (int)e - 127); }
+
+/* Nearest e2m1 code, ties to the even code, saturating to +-6 (brute force over
+ * the 8 non-negative codes). */
+uint8_t orc_e2m1_encode(float x) {
+  double ax = fabs((double)x);
+  int best = 0;
+  double best_err = INFINITY;
+  for (int code = 0; code <= 7; ++code) {
+    double err = fabs(orc_e2m1_decode((uint8_t)code) - ax);
+    if (err < best_err || (err == best_err && (code & 1) == 0)) {
+      best = code;
+      best_err = err;
+    }
+  }
+  if (ax > 6.0) best = 7;
+  return (uint8_t)((x < 0 || (x == 0 && signbit(x))) ? (best | 8) : best);
+}
+
+/* Rows of c values (c a multiple of 32) to MXFP4: per block of 32, the shared
+ * exponent E = floor(log2(amax)) - 2 (2 = the exponent of e2m1's largest
+ * magnitude, 6 = 1.5 * 2^2), clamped to [-127, 127] (E = -127 when amax = 0);
+ * scale code E + 127; element code = e2m1 of x / 2^E (exact: a power of two).
+ * codes [rows][c] (one code per byte), scales [rows][c/32]. */
+void orc_quantise_mxfp4_rows(const float* x, int64_t rows, int64_t c, uint8_t* codes, uint8_t* scales) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t b0 = 0; b0 < c; b0 += 32) {
+      float amax = 0.0f;
+      for (int64_t i = b0; i < b0 + 32; ++i) {
+        float a = fabsf(x[r * c + i]);
+        if (a > amax) amax = a;
+      }
+      int E = -127;
+      if (amax > 0.0f) {
+        int e;
+        frexp((double)amax, &e); /* amax = f * 2^e, f in [0.5, 1): floor(log2 amax) = e - 1 */
+        E = (e - 1) - 2;
+        if (E < -127) E = -127;
+        if (E > 127) E = 127;
+      }
+      scales[r * (c / 32) + b0 / 32] = (uint8_t)(E + 127);
+      for (int64_t i = b0; i < b0 + 32; ++i) codes[r * c + i] = orc_e2m1_encode((float)ldexp((double)x[r * c + i], -E));
+    }
+}
+
 /* ------------------------------------------------------- lightning indexer */
 
 /*

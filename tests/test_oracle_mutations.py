@@ -58,6 +58,10 @@ MUTATIONS = [
      "        L = a;\n      }\n      double w"),
     ("grouped_proj_wrong_group_input", "o[r * n_h * c + j * in_g + d]", "o[r * n_h * c + d]"),
     ("grouped_proj_transposed_weight", "W[(j * d_g + e) * in_g + d]", "W[(j * in_g + d) * d_g + e]"),
+    ("e2m1_exponent_bias", "ldexp(1.0 + 0.5 * (double)mant, e - 1)", "ldexp(1.0 + 0.5 * (double)mant, e - 2)"),
+    ("mxfp4_shared_exponent_offset", "E = (e - 1) - 2;", "E = (e - 1) - 1;"),
+    ("e2m1_ties_to_odd", "if (err < best_err || (err == best_err && (code & 1) == 0)) {\n      best = code;\n      best_err = err;\n    }\n  }\n  if (ax > 6.0)",
+     "if (err < best_err || (err == best_err && (code & 1) == 1)) {\n      best = code;\n      best_err = err;\n    }\n  }\n  if (ax > 6.0)"),
 ]
 
 

@@ -675,3 +675,54 @@ def test_grouped_projection_keeps_groups_apart():
         o2[0, h] += 1.0
         moved = np.abs(oracle.grouped_out_proj(o2, W) - base).reshape(g, d_g).max(axis=1) > 0
         assert np.array_equal(moved, np.arange(g) == h // (n_h // g))
+
+
+# --------------------------------------------------- MXFP4 (indexer's FP4 path)
+
+
+def test_e2m1_values_are_the_microscaling_grid():
+    v = oracle.e2m1_decode(np.arange(16))
+    # the eight magnitudes of e2m1 and their negatives (sign bit = bit 3)
+    assert list(v[:8]) == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert np.array_equal(v[8:], -v[:8]) and math.copysign(1.0, v[8]) == -1.0
+
+
+def test_e8m0_scales_are_powers_of_two():
+    s = oracle.e8m0_decode(np.array([0, 1, 126, 127, 128, 254, 255]))
+    assert list(s[:6]) == [2.0 ** -127, 2.0 ** -126, 0.5, 1.0, 2.0, 2.0 ** 127] and np.isnan(s[6])
+
+
+def test_e2m1_encode_rounds_to_nearest_ties_to_even_and_saturates():
+    grid = oracle.e2m1_decode(np.arange(8))
+    assert np.array_equal(oracle.e2m1_encode(grid), np.arange(8))
+    # midpoints: 0.25 -> 0 (code 0), 1.25 -> 1 (code 2), 2.5 -> 2 (code 4), 3.5 -> 4 (code 6), 5 -> 4 (code 6)
+    assert list(oracle.e2m1_encode([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])) == [0, 2, 2, 4, 4, 6, 6]
+    assert list(oracle.e2m1_encode([6.5, 100.0, -7.0])) == [7, 7, 15]
+    assert list(oracle.e2m1_encode([-0.5, -0.0])) == [9, 8]
+
+
+def test_mxfp4_worked_blocks():
+    # amax 12: floor(log2 12) = 3, shared exponent 3 - 2 = 1, scale 2: 1, 2, 3, 12 land on the grid
+    x = np.zeros((1, 64), dtype=np.float32)
+    x[0, :4] = [1, 2, 3, 12]
+    # second block: amax 7, shared exponent 0: 7 saturates to 6 (the format's clipping), 2.6 -> 3
+    x[0, 32:35] = [7, 2.6, -0.2]
+    codes, scales = oracle.quantise_mxfp4_rows(x)
+    assert list(scales[0]) == [128, 127]
+    y = oracle.mxfp4_decode(codes, scales)
+    assert list(y[0, :4]) == [1.0, 2.0, 3.0, 12.0] and np.all(y[0, 4:32] == 0)
+    assert list(y[0, 32:35]) == [6.0, 3.0, 0.0]
+    z = oracle.quantise_mxfp4_rows(np.zeros((2, 32), dtype=np.float32))
+    assert np.all(z[0] == 0) and np.all(z[1] == 0)  # all-zero block: smallest scale, zero codes
+
+
+def test_mxfp4_error_is_within_half_a_grid_step():
+    x = (_rng(74).normal(size=(50, 128)) * _rng(75).uniform(1e-3, 1e3, size=(50, 1))).astype(np.float32)
+    codes, scales = oracle.quantise_mxfp4_rows(x)
+    y = oracle.mxfp4_decode(codes, scales)
+    s = np.repeat(oracle.e8m0_decode(scales), 32, axis=-1)
+    u = np.abs(x) / s  # in units of the block's scale
+    assert np.all(u.reshape(50, 4, 32).max(axis=-1) >= 4) and np.all(u < 8)  # normalisation of each block
+    step = np.where(u < 2, 0.5, np.where(u < 4, 1.0, 2.0))  # grid spacing around |x| / scale
+    bound = np.where(u <= 6, step / 2, u - 6) * s
+    assert np.all(np.abs(y - x) <= bound + 1e-12)
