@@ -40,6 +40,10 @@ class Workload:
     n_win: int = 128
     dtype: torch.dtype = torch.bfloat16
     seed: int = 0
+    # value scales: None = the recipe (cache / raw rows N(0,1)/sqrt(c), N(0,1) in float32);
+    # parity cases also draw unit-scale rows and larger queries so that outputs are O(1)
+    kv_std: float | None = None
+    q_std: float = 1.0
 
     @property
     def n_csa(self) -> int:
@@ -133,7 +137,7 @@ def make_inputs(w: Workload, device="cpu") -> dict:
     """
     d = _Draw(w.seed, device)
     B, n, c, dt = w.batch, w.n_ctx, w.c, w.dtype
-    kv_std = 1.0 if dt == torch.float32 else 1.0 / math.sqrt(c)
+    kv_std = w.kv_std if w.kv_std is not None else (1.0 if dt == torch.float32 else 1.0 / math.sqrt(c))
     out = {}
 
     def csa_raw(rows):
@@ -149,7 +153,7 @@ def make_inputs(w: Workload, device="cpu") -> dict:
         out["biasI"] = d.normal((2 * w.m, w.c_I))
 
     def queries(n_q, suffix=""):
-        out["q" + suffix] = d.normal((B, n_q, w.n_h, c), 1.0, dt)
+        out["q" + suffix] = d.normal((B, n_q, w.n_h, c), w.q_std, dt)
 
     def indexer_queries(n_q):
         qI, qs = _indexer_values(d, (B, n_q, w.n_ih, w.c_I), w.idx_dtype)

@@ -7,6 +7,10 @@ import torch
 # tolerances on attention outputs (max-abs), per the parity bar of the build
 TOL_F32 = 1e-4
 TOL_BF16 = 2e-2
+# Outputs are also held to a bound relative to the reference's largest magnitude: with
+# the method's input recipe (cache rows N(0,1)/sqrt(c)) attention outputs are ~1e-3, so
+# the absolute bound alone would pass an all-zero or mis-accumulated output.
+REL_OUT = 1e-2
 TOPK_GAP = 1e-3  # relative oracle score gap below which several top-k sets count as correct
 
 
@@ -18,11 +22,37 @@ def to_np(t: torch.Tensor) -> np.ndarray:
 
 
 def max_abs(a, b) -> float:
+    """Largest |a - b|; equal infinities count as equal, and a NaN on either side
+    where the other side has none (or any NaN difference) counts as infinite."""
     a = np.asarray(a, dtype=np.float64)
     b = np.asarray(b, dtype=np.float64)
+    if a.shape != b.shape:
+        raise AssertionError(f"shape {a.shape} vs {b.shape}")
+    if a.size == 0:
+        return 0.0
+    nan_a, nan_b = np.isnan(a), np.isnan(b)
+    if np.any(nan_a != nan_b):
+        return float("inf")
     both_inf = np.isinf(a) & np.isinf(b) & (np.sign(a) == np.sign(b))
-    d = np.abs(np.where(both_inf, 0.0, a - b))
-    return float(np.nanmax(d)) if d.size else 0.0
+    with np.errstate(invalid="ignore"):
+        d = np.abs(np.where(both_inf | (nan_a & nan_b), 0.0, a - b))
+    return float(np.max(d))
+
+
+def out_close(got, ref, tol: float = TOL_BF16, rel: float = REL_OUT) -> bool:
+    """An attention output is close to the reference when its max-abs error is within
+    `tol` AND within `rel` of the reference's largest magnitude (a reference that is
+    zero everywhere must be matched exactly)."""
+    err = max_abs(got, ref)
+    scale = float(np.max(np.abs(np.nan_to_num(np.asarray(ref, dtype=np.float64))))) if np.size(ref) else 0.0
+    return err <= tol and err <= rel * scale
+
+
+def assert_out_close(got, ref, tol: float = TOL_BF16, rel: float = REL_OUT, what: str = "output"):
+    err = max_abs(got, ref)
+    scale = float(np.max(np.abs(np.nan_to_num(np.asarray(ref, dtype=np.float64))))) if np.size(ref) else 0.0
+    assert err <= tol, f"{what}: max-abs error {err:.3e} > {tol:.1e}"
+    assert err <= rel * scale, f"{what}: max-abs error {err:.3e} > {rel:.0e} x max|ref| = {rel * scale:.3e}"
 
 
 def check_topk_row(gpu_idx: np.ndarray, ref_scores: np.ndarray, visible: int, k: int, gap: float = TOPK_GAP):

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import TOL_BF16, max_abs, to_np
+from helpers import TOL_BF16, assert_out_close, max_abs, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -72,7 +72,7 @@ def test_csa_attend_aliased_entries(B, n_q, n_h, N, k, seed):
     scale = 1 / math.sqrt(c)
     o, lse = _csa(q, kc, kc, idx, scale)
     ro, rl = oracle.csa_attend(q, kc, kc, idx, scale)
-    assert max_abs(o, ro) <= TOL_BF16
+    assert_out_close(o, ro)
     assert max_abs(lse, rl) <= TOL_BF16
 
 
@@ -91,7 +91,7 @@ def test_csa_attend_padding_runs_duplicates_and_empty_lists():
     scale = 1 / math.sqrt(c)
     o, lse = _csa(q, kc, kc, idx, scale)
     ro, rl = oracle.csa_attend(q, kc, kc, idx, scale)
-    assert max_abs(o, ro) <= TOL_BF16
+    assert_out_close(o, ro)
     assert max_abs(lse, rl) <= TOL_BF16
     assert np.all(o[1, 2] == 0) and np.all(np.isneginf(lse[1, 2]))
 
@@ -117,7 +117,7 @@ def test_softmax_reference_moves_late_in_the_list(order):
     scale = 1 / math.sqrt(c) * 8
     o, lse = _csa(q, kc, vc, idx, scale)
     ro, rl = oracle.csa_attend(q, kc, vc, idx, scale)
-    assert max_abs(o, ro) <= TOL_BF16
+    assert_out_close(o, ro)
     assert np.max(np.abs(lse - rl) / np.maximum(1.0, np.abs(rl))) <= 2e-3
 
 
@@ -139,7 +139,7 @@ def test_hca_attend_aliased_entries(B, n_q, n_h, N, m, q_pos0):
     o, lse = _ops().hca_attend(q.to(DEV), kc.to(DEV), kc.to(DEV), m=m, q_pos0=q_pos0, scale=scale, dev_status=st)
     assert st.item() == 0, f"device status {st.item()}"
     ro, rl = oracle.hca_attend(q, kc, kc, m=m, q_pos0=q_pos0, scale=scale)
-    assert max_abs(to_np(o), ro) <= TOL_BF16
+    assert_out_close(to_np(o), ro)
     assert max_abs(to_np(lse), rl) <= TOL_BF16
 
 
@@ -165,7 +165,7 @@ def test_swa_merge_aliased_window(B, n_q, n_h, n_win, kv_pos0, n_kv, q_pos0, out
     assert st.item() == 0, f"device status {st.item()}"
     ro, _ = oracle.swa_merge(q, kv, kv, kv_pos0, q_pos0, n_win, scale, o_in.double().numpy(),
                              lse_in.double().numpy())
-    assert max_abs(to_np(out), ro) <= TOL_BF16
+    assert_out_close(to_np(out), ro)
 
 
 def test_attention_reads_no_row_outside_the_visible_set():
@@ -246,7 +246,7 @@ def test_csa_attend_with_fused_window(B, n_q, n_h, N, k, n_win, q_pos0, n_kv, ou
     assert st.item() == 0, f"device status {st.item()}"
     o, l = oracle.csa_attend(q, kc, kc, idx.numpy(), scale)
     ro, rl = oracle.swa_merge(q, kv, kv, kv_pos0, q_pos0, n_win, scale, o, l)
-    assert max_abs(to_np(out), ro) <= TOL_BF16
+    assert_out_close(to_np(out), ro)
     assert max_abs(to_np(lse), rl) <= TOL_BF16
 
 
@@ -269,7 +269,7 @@ def test_hca_attend_with_fused_window(B, n_q, n_h, N, m, q_pos0, n_win, n_kv):
     assert st.item() == 0, f"device status {st.item()}"
     o, l = oracle.hca_attend(q, kc, kc, m=m, q_pos0=q_pos0, scale=scale)
     ro, rl = oracle.swa_merge(q, kv, kv, kv_pos0, q_pos0, n_win, scale, o, l)
-    assert max_abs(to_np(out), ro) <= TOL_BF16
+    assert_out_close(to_np(out), ro)
     assert max_abs(to_np(lse), rl) <= TOL_BF16
 
 
@@ -301,6 +301,8 @@ def test_join_counters_reset_across_calls_of_different_shapes():
                          n_win=128, scale=scale, workspace=ws[4096:], dev_status=st)
         torch.cuda.synchronize()
         assert st.item() == 0, f"device status {st.item()}"
-        assert max_abs(to_np(o), ro1) <= TOL_BF16 and max_abs(to_np(lse), rl1) <= TOL_BF16
-        assert max_abs(to_np(out), ro2) <= TOL_BF16 and max_abs(to_np(lse2), rl2) <= TOL_BF16
+        assert_out_close(to_np(o), ro1)
+        assert max_abs(to_np(lse), rl1) <= TOL_BF16
+        assert_out_close(to_np(out), ro2)
+        assert max_abs(to_np(lse2), rl2) <= TOL_BF16
     assert int(ws[:1024].count_nonzero()) == 0

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from tests.helpers import TOL_BF16, check_topk_row, max_abs, to_np
+from tests.helpers import TOL_BF16, assert_out_close, check_topk_row, max_abs, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -20,8 +20,10 @@ if torch.cuda.is_available():
 DEV = "cuda"
 
 
-def _run(name):
+def _run(name, **changes):
     w = workloads.WORKLOADS[name]
+    if changes:
+        w = workloads.scaled(w, **changes)
     x = workloads.make_inputs(w, DEV)
     cache_before = {k: x[k].clone() for k in ("kc", "kI", "kI_scale", "kc_h") if k in x}
     step = pipeline.HybridStep(w, x)
@@ -58,7 +60,7 @@ def _check_decode_csa(w, x, step, before, b):
     kc = cpu("kc")
     o, l = oracle.csa_attend(cpu("q"), kc, kc, gidx, w.scale)
     out, lu = oracle.swa_merge(cpu("q"), cpu("kv"), cpu("kv"), w.n_ctx - w.n_win, t, w.n_win, w.scale, o, l)
-    assert max_abs(to_np(step.buf["out"][sl]), out) <= TOL_BF16
+    assert_out_close(to_np(step.buf["out"][sl]), out)
     # the fused window merge leaves the union's lse (and no compressed-only o)
     assert max_abs(to_np(step.buf["lse"][sl]), lu) <= TOL_BF16
 
@@ -76,7 +78,7 @@ def _check_decode_hca(w, x, step, before, b, sfx):
     q = cpu("q" + sfx)
     o, l = oracle.hca_attend(q, kc, kc, m=w.m_hca, q_pos0=t, scale=w.scale)
     out, lu = oracle.swa_merge(q, cpu("kv" + sfx), cpu("kv" + sfx), w.n_ctx - w.n_win, t, w.n_win, w.scale, o, l)
-    assert max_abs(to_np(step.buf["out_h"][sl]), out) <= TOL_BF16
+    assert_out_close(to_np(step.buf["out_h"][sl]), out)
     assert max_abs(to_np(step.buf["lse_h"][sl]), lu) <= TOL_BF16
 
 
@@ -99,8 +101,39 @@ def test_pro_1m_hybrid_decode_full_size():
         _check_decode_hca(w, x, step, before, b, "_h")
 
 
+def test_pro_1m_hybrid_decode_full_size_unit_scale_values():
+    """The 1M decode with cache and window rows N(0,1) and queries N(0,2): outputs of
+    order 0.1-1, so that the split join (16 splits + the window at 1M context) and
+    the gathered CSA path are checked well above any rounding floor."""
+    w, x, step, before = _run("pro_1m_hybrid_decode", kv_std=1.0, q_std=2.0)
+    assert float(step.buf["out_h"].abs().max()) > 0.1 and float(step.buf["out"].abs().max()) > 0.1
+    for b in (0, w.batch - 1):
+        _check_decode_csa(w, x, step, before, b)
+        _check_decode_hca(w, x, step, before, b, "_h")
+
+
+def test_flash_decodes_full_size_unit_scale_values():
+    for name, check in (("flash_csa_decode", _check_decode_csa), ("flash_hca_decode", _check_decode_hca)):
+        w, x, step, before = _run(name, kv_std=1.0, q_std=2.0)
+        for b in (0, w.batch - 1):
+            if check is _check_decode_hca:
+                check(w, x, step, before, b, "")
+            else:
+                check(w, x, step, before, b)
+
+
+def test_csa_prefill_unit_scale_values_sampled_rows():
+    """A prefill chunk of 8,192 tokens (Pro shapes) with unit-scale rows: query tiles,
+    the causal edge and the two-launch window merge with O(1) outputs."""
+    _check_prefill(*_run("pro_csa_prefill", n_ctx=8192, kv_std=1.0, q_std=2.0)[:3],
+                   rows=(0, 3, 4, 127, 128, 1000, 4095, 4096, 8191))
+
+
 def test_pro_csa_prefill_full_size_sampled_rows():
-    w, x, step, _ = _run("pro_csa_prefill")
+    _check_prefill(*_run("pro_csa_prefill")[:3], rows=(0, 2, 3, 4, 127, 128, 4095, 4096, 16383, 32767))
+
+
+def _check_prefill(w, x, step, rows):
     cpu = {k: v.cpu() for k, v in x.items()}
     ent = oracle.compress(cpu["ca"], cpu["za"], cpu["bias"], w.m, cb=cpu["cb"], zb=cpu["zb"], overlap=True)
     assert _bf16_close(to_np(step.buf["entries"]), ent)
@@ -111,12 +144,12 @@ def test_pro_csa_prefill_full_size_sampled_rows():
     kI, kIs = step.buf["kI"].cpu(), step.buf["kI_scale"].cpu()
     e = step.buf["entries"].cpu()
     gidx = step.buf["idx"].cpu().numpy()
-    for j in (0, 2, 3, 4, 127, 128, 4095, 4096, 16383, 32767):
+    for j in rows:
         js = slice(j, j + 1)
         s = oracle.index_scores(cpu["qI"][:, js], cpu["w"][:, js], kI, m=w.m, q_pos0=j,
                                 qI_scale=cpu["qI_scale"][:, js], kI_scale=kIs)
         check_topk_row(gidx[0, j], s[0, 0], oracle.visible(j, w.m), w.k)
         o, l = oracle.csa_attend(cpu["q"][:, js], e, e, gidx[:, js], w.scale)
         out, lu = oracle.swa_merge(cpu["q"][:, js], cpu["kv"], cpu["kv"], 0, j, w.n_win, w.scale, o, l)
-        assert max_abs(to_np(step.buf["out"][:, js]), out) <= TOL_BF16
+        assert_out_close(to_np(step.buf["out"][:, js]), out)
         assert max_abs(to_np(step.buf["lse"][:, js]), lu) <= TOL_BF16

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle
-from tests.helpers import TOL_BF16, TOL_F32, check_topk_row, max_abs, to_np
+from tests.helpers import TOL_BF16, TOL_F32, assert_out_close, check_topk_row, max_abs, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -243,7 +243,7 @@ def test_csa_attend_matches_oracle(dtype, B, n_q, n_h, c, N, k):
     o, lse = ops.csa_attend(q.to(DEV), kc.to(DEV), vc.to(DEV), idx.to(DEV), scale=scale)
     ro, rl = oracle.csa_attend(q, kc, vc, idx, scale)
     tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
-    assert max_abs(to_np(o), ro) <= tol
+    assert_out_close(to_np(o), ro, tol)
     assert max_abs(to_np(lse), rl) <= tol
     if n_q > 1:
         assert np.all(to_np(o)[-1, 1] == 0) and np.all(np.isneginf(to_np(lse)[-1, 1]))
@@ -261,7 +261,7 @@ def test_hca_attend_matches_oracle(dtype, B, n_q, n_h, c, N, m, q_pos0):
     o, lse = ops.hca_attend(q.to(DEV), kc.to(DEV), vc.to(DEV), m=m, q_pos0=q_pos0, scale=scale)
     ro, rl = oracle.hca_attend(q, kc, vc, m=m, q_pos0=q_pos0, scale=scale)
     tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
-    assert max_abs(to_np(o), ro) <= tol
+    assert_out_close(to_np(o), ro, tol)
     assert max_abs(to_np(lse), rl) <= tol
 
 
@@ -288,7 +288,7 @@ def test_swa_merge_matches_oracle(dtype, B, n_q, n_h, c, n_win, kv_pos0, n_kv, q
     zl = np.full((B, n_q, n_h), -np.inf) if lse_in is None else lse_in.double().numpy()
     ro, rl = oracle.swa_merge(q, kw, vw, kv_pos0, q_pos0, n_win, scale, zo, zl)
     tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
-    assert max_abs(to_np(out), ro) <= tol
+    assert_out_close(to_np(out), ro, tol)
     assert max_abs(to_np(lse), rl) <= tol
 
 
@@ -300,7 +300,7 @@ def test_bad_index_is_skipped_and_reported():
     assert status.item() & 0x1
     clean = torch.tensor([[[1, 5, -1, -1], [2, 3, 9, -1]]], dtype=torch.int32)
     ro, _ = oracle.csa_attend(q, kc, vc, clean, 0.2)
-    assert max_abs(to_np(o), ro) <= TOL_F32
+    assert_out_close(to_np(o), ro, TOL_F32)
 
 
 # ------------------------------------------------------------- end to end
@@ -329,9 +329,9 @@ def test_tiny_forward_end_to_end_matches_the_oracle_chain():
     e32 = ent.astype(np.float32)
     o, l = oracle.csa_attend(x["q"], e32, e32, gidx, w.scale)
     out, _ = oracle.swa_merge(x["q"], x["kv"], x["kv"], 0, 0, w.n_win, w.scale, o, l)
-    assert max_abs(to_np(step.buf["out"]), out) <= TOL_F32
+    assert_out_close(to_np(step.buf["out"]), out, TOL_F32)
     # HCA layer
     eh = oracle.compress(x["ch"], x["zh"], x["bias_h"], w.m_hca).astype(np.float32)
     o, l = oracle.hca_attend(x["q"], eh, eh, m=w.m_hca, q_pos0=0, scale=w.scale)
     out, _ = oracle.swa_merge(x["q"], x["kv"], x["kv"], 0, 0, w.n_win, w.scale, o, l)
-    assert max_abs(to_np(step.buf["out_h"]), out) <= TOL_F32
+    assert_out_close(to_np(step.buf["out_h"]), out, TOL_F32)
