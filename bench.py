@@ -91,10 +91,12 @@ def stage_model(w):
     return m
 
 
-# DRAM bytes (read + write) of one launch of the scoring kernel, counted by ncu
-# (dram__bytes_read.sum + dram__bytes_write.sum) on this workload with the current
-# kernel; None where no capture of the current kernel exists
-SCORING_KERNEL_NCU_TRAFFIC = {"pro_1m_hybrid_decode": 138_501_376 + 5_097_984}
+# DRAM bytes (read + write) of one launch of a kernel, counted by ncu
+# (dram__bytes_read.sum + dram__bytes_write.sum) on a workload with the current
+# build of that kernel; absent where no capture of the current kernel exists
+KERNEL_NCU_TRAFFIC = {
+    ("pro_1m_hybrid_decode", "index_scores"): 138_501_376 + 5_097_984,
+}
 
 
 def scoring_kernel_model(w):
@@ -111,6 +113,85 @@ def scoring_kernel_model(w):
         pairs = sum(min(N, (t + 1) // w.m) for t in range(w.n_ctx))
     return dict(bytes=w.batch * (N * (w.c_I + 4) + n_q * qb), flops=w.batch * pairs * w.n_ih * w.c_I * 2,
                 flop_dtype="fp8")
+
+
+def topk_kernel_model(w):
+    """Algorithmic bytes of the selection on its own: the float32 scores of the visible
+    entries read once, the k indices written."""
+    if w.decode:
+        return dict(bytes=w.batch * (w.n_csa * 4 + w.k * 4), flops=0)
+    pairs = sum(min(w.n_csa, (t + 1) // w.m) for t in range(w.n_ctx))
+    return dict(bytes=w.batch * (pairs * 4 + w.n_ctx * w.k * 4), flops=0)
+
+
+# the kernels of each timed stage, for the per-kernel roofline table
+STAGE_KERNELS = {
+    "csa_compress": "compress_kernel x2 (CSA entry bf16 + indexer key e4m3)",
+    "csa_attend": "attend_tc_kernel<0> (csa_attend, window fused)",
+    "hca_compress": "compress_kernel (HCA entry)",
+    "hca_attend": "attend_tc_kernel<1> (hca_attend, window fused)",
+}
+
+
+def kernel_roofline(name, model, ms, peaks, peak_kind, traffic=None):
+    """Roofline entry of one kernel: algorithmic bytes (or flops, above the ridge) of one
+    launch over its measured duration, against the measured peak."""
+    if model["flops"] > 0 and model.get("flop_dtype") in ("bf16", "fp8") and \
+            model["flops"] / max(model["bytes"], 1) > _ridge(peaks, model.get("flop_dtype")):
+        peak = _tensor_peak(peaks, model["flop_dtype"])
+        achieved = model["flops"] / (ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s"}
+    else:
+        peak = peaks["hbm_gbs"]
+        achieved = model["bytes"] / (ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s"}
+    roof["frac"] = achieved / peak
+    roof["traffic"] = traffic
+    roof["kernel"] = name
+    roof["ms_per_launch"] = ms
+    roof["algorithmic_bytes"] = model["bytes"]
+    roof["algorithmic_flops"] = model["flops"]
+    if roof["bound"] == "tensor" and model["flop_dtype"] == "fp8":
+        roof["peak_source"] = peaks.get("fp8_source", "2 x the bf16 burst peak")
+    else:
+        roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
+    return roof
+
+
+def _tensor_peak(peaks, dt):
+    """Dense tensor peak (TFLOP/s) for a contraction of type dt.  The kernels here run
+    at the maximum SM clock inside the step (no power cap seen), so the burst figures
+    apply: bf16 from MEASURED_PEAKS.json, FP8 measured by this run (fp8_peak_probe)
+    where it could be, else twice the bf16 figure."""
+    if dt == "fp8":
+        return peaks.get("fp8_tflops") or 2 * peaks["bf16_tflops"]
+    return peaks["bf16_tflops"]
+
+
+def fp8_peak_probe(device, n=8192, reps=10):
+    """Dense FP8 (e4m3 x e4m3 -> bf16, cuBLASLt through torch._scaled_mm) n^3 GEMM: best of
+    `reps` after warm-up, timed with CUDA events; 2 n^3 flops.  Timing only: no GPU setting
+    is touched.  Returns TFLOP/s or None where the call is unavailable."""
+    import torch
+
+    try:
+        a = torch.randn(n, n, device=device).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=device).to(torch.float8_e4m3fn).t()
+        one = torch.ones((), device=device)
+        for _ in range(3):
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        del a, b
+        return 2 * n ** 3 / (best / 1e3) / 1e12
+    except Exception:  # noqa: BLE001 - the probe is optional
+        return None
 
 
 # ------------------------------------------------------------------ clocks
@@ -321,34 +402,31 @@ def run_ours(args, w):
     # -------- e2e through the public API: fresh inputs from pinned host memory
     e2e = run_e2e(args, w, steps[0], stream, units, world, dist)
 
-    # -------- roofline of the dominant kernel: the indexer's scoring kernel (timed by
-    # the events the library records around it) where the workload has a CSA layer,
-    # else the dominant stage (one kernel per stage)
+    # -------- roofline of every kernel (stage events; the indexer's scoring kernel by the
+    # events the library records around it, the selection as the rest of its stage);
+    # the dominant kernel is the one with the longest measured time
     peaks, peak_kind = measured_peaks()
+    fp8 = fp8_peak_probe(dev) if rank == 0 else None
+    if fp8:
+        peaks = dict(peaks, fp8_tflops=fp8, fp8_source="measured by this run: dense e4m3 8192^3 GEMM (cuBLASLt)")
+    kern = {}
     if has_scoring:
-        dom, dm, dom_ms = "index_tc_kernel (csa_index_topk scoring)", scoring_kernel_model(w), scoring_ms
-    else:
-        dom = max(stage_ms, key=lambda s: stage_ms[s])
-        dm, dom_ms = model[dom], stage_ms[dom]
-    if dm["flops"] > 0 and dm.get("flop_dtype") in ("bf16", "fp8") and \
-            dm["flops"] / max(dm["bytes"], 1) > _ridge(peaks, dm.get("flop_dtype")):
-        peak = peaks["bf16_tflops_sustained"] * (2 if dm["flop_dtype"] == "fp8" else 1)
-        achieved = dm["flops"] / (dom_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": None}
-    else:
-        peak = peaks["hbm_gbs"]
-        achieved = dm["bytes"] / (dom_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": None}
-    roof["kernel"] = dom
-    if has_scoring:
-        roof["traffic"] = SCORING_KERNEL_NCU_TRAFFIC.get(w.name)
-    roof["ms_per_launch"] = dom_ms
-    roof["algorithmic_bytes"] = dm["bytes"]
-    roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
+        kern["index_scores"] = ("index_tc_kernel (csa_index_topk scoring)", scoring_kernel_model(w), scoring_ms)
+        kern["topk"] = ("topk_grid_kernel (csa_index_topk selection)", topk_kernel_model(w),
+                        stage_ms["csa_index_topk"] - scoring_ms)
+    for s_name, label in STAGE_KERNELS.items():
+        if s_name in stage_ms:
+            kern[s_name] = (label, model[s_name], stage_ms[s_name])
+    kernels = {k: kernel_roofline(lbl, m_, ms_, peaks, peak_kind, KERNEL_NCU_TRAFFIC.get((w.name, k)))
+               for k, (lbl, m_, ms_) in kern.items()}
+    dom = max(kernels, key=lambda k: kernels[k]["ms_per_launch"])
+    roof = dict(kernels[dom])
 
     step_roof_s = max(step_bytes / (peaks["hbm_gbs"] * 1e9), 0.0)
+    # each stage at its own bound (bytes at the HBM peak or flops at the tensor peak)
+    step_roof_any_s = sum(max(v["bytes"] / (peaks["hbm_gbs"] * 1e9),
+                              v["flops"] / (_tensor_peak(peaks, v["flop_dtype"]) * 1e12) if v["flops"] else 0.0)
+                          for v in model.values())
     out = {
         "metric": METRIC,
         "value": value,
@@ -370,9 +448,12 @@ def run_ours(args, w):
         "e2e": e2e,
         "gpu_launches": _launches_per_step(w) * args.steps,
         "roofline": roof,
+        "kernels": kernels,
+        "fp8_tflops_measured": fp8,
         "stages_ms": stage_ms,
         "ms_per_step_with_stage_events": ms_step_ev,
         "step_hbm_roofline_frac": step_roof_s / (ms_step / 1e3),
+        "step_roofline_frac": step_roof_any_s / (ms_step / 1e3),
     }
     if rank == 0 and world == 1 and w.kind == "hybrid_decode" and not args.no_session:
         out["session"] = run_session(w, stream)
@@ -458,8 +539,7 @@ def run_session(w, stream, tokens=128, reps=5):
 
 
 def _ridge(peaks, dt):
-    tf = peaks["bf16_tflops_sustained"] * (2 if dt == "fp8" else 1)
-    return tf * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    return _tensor_peak(peaks, dt) * 1e12 / (peaks["hbm_gbs"] * 1e9)
 
 
 def _csa_parts(st, stream, rec, scoring_events=None):
