@@ -27,7 +27,13 @@
  *    bytes (256-byte aligned device memory), or may be NULL when that size is
  *    0.  The workspace's contents need not be initialised.
  *  - Query positions: query j of every batch element sits at absolute token
- *    position t = q_pos0 + j (queries are consecutive positions).
+ *    position t = q_pos0 + j (queries are consecutive positions), unless the
+ *    call is given per-query positions: an optional `q_pos` array, int64
+ *    [batch][n_q] in device memory, holding each query's own absolute position
+ *    (a batch of sequences at different lengths, [KE] section 9's per-request
+ *    cache).  The host cannot read those: a position that is negative, or that
+ *    would see more compressed entries than exist or window rows outside the
+ *    buffer, is clipped to what exists and reported as HYB_DEV_BAD_INDEX.
  *  - Visibility ([HA] V.2: only earlier blocks are scored; [KE] section 9): a compressed
  *    entry s built with compression factor m is visible to position t iff its
  *    last token is <= t, i.e. s < floor((t+1)/m).  Unfinished tails are covered
@@ -188,6 +194,10 @@ typedef struct hyb_index_args {
      library neither creates nor destroys them. */
   void* ev_scores_begin;
   void* ev_scores_end;
+  /* Optional per-query absolute positions, int64 [batch][n_q] in device memory
+     (NULL: query j is at q_pos0 + j, and q_pos0 is ignored otherwise).  With them
+     the workspace is sized for every row seeing all n_entries entries. */
+  const int64_t* q_pos;
 } hyb_index_args;
 
 /* Workspace: csa_index_topk_workspace_size(a) bytes, 256-byte aligned.  Its
@@ -231,6 +241,16 @@ HYB_API hyb_status csa_index_topk(const hyb_index_args* a, void* workspace, size
 #define HYB_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 HYB_API hyb_status csa_index_topk_noalloc(const hyb_index_args* a, void* stream);
 
+/* csa_index_topk_noalloc_reset -- zero the counters at the start of the
+ * library's scratch array on the current device, asynchronously on `stream`
+ * (a memset of memory the library already holds: nothing is allocated).  A
+ * call of csa_index_topk_noalloc that reported HYB_DEV_TIMEOUT can leave those
+ * counters non-zero, and every later call on that device would then start
+ * from them; call this once after such a call, before the next one (ordered
+ * with it on the same stream).  Like csa_index_topk_noalloc, the first use on
+ * a device looks up the array's address: make it before any stream capture. */
+HYB_API hyb_status csa_index_topk_noalloc_reset(void* stream);
+
 /* ------------------------------------------------------------------------
  * hyb_window -- the sliding-window branch fused into csa_attend / hca_attend.
  *
@@ -256,6 +276,12 @@ typedef struct hyb_window {
   int64_t n_win;
   void* out;
   int32_t out_dtype;
+  /* Optional, device memory: q_pos int64 [batch][n_q] per-query positions (NULL:
+     q_pos0 + j; for hca_attend they must be the call's own q_pos), kv_pos0s int64
+     [batch] the absolute position of row 0 of each sequence's rows of kw (NULL:
+     kv_pos0 for all), e.g. a per-sequence ring of raw rows. */
+  const int64_t* q_pos;
+  const int64_t* kv_pos0s;
 } hyb_window;
 
 /* ------------------------------------------------------------------------
@@ -334,6 +360,7 @@ typedef struct hyb_hca_attend_args {
   int32_t* dev_status;
   const hyb_window* window; /* optional fused window merge (see hyb_window), or NULL */
   const float* sink;        /* optional per-head attention-sink logits [n_h], or NULL (see csa_attend) */
+  const int64_t* q_pos;     /* optional per-query positions int64 [batch][n_q], device memory, or NULL */
 } hyb_hca_attend_args;
 
 HYB_API size_t hca_attend_workspace_size(const hyb_hca_attend_args* a);
@@ -375,6 +402,8 @@ typedef struct hyb_swa_args {
   int32_t dtype;
   int32_t out_dtype;
   int32_t* dev_status;
+  const int64_t* q_pos;    /* optional per-query positions int64 [batch][n_q], device memory, or NULL */
+  const int64_t* kv_pos0s; /* optional int64 [batch]: absolute position of row 0 of each sequence's kw / vw rows */
 } hyb_swa_args;
 
 HYB_API size_t swa_merge_workspace_size(const hyb_swa_args* a);
@@ -411,6 +440,27 @@ typedef struct hyb_norm_rope_args {
 } hyb_norm_rope_args;
 
 HYB_API hyb_status hyb_rmsnorm_rope(const hyb_norm_rope_args* a, void* stream);
+
+/* ------------------------------------------------------------------------
+ * hyb_set_grid_wait_limit -- bound of the device-side waits that span CTAs.
+ *
+ * Two kernels wait on other CTAs of their grid: the top-k grid plan of
+ * csa_index_topk (grid barriers between its phases) and the split join of the
+ * tensor-core csa_attend / hca_attend (the splits of one query meet before
+ * they merge).  Each such wait gives up after this many SM clock cycles; the
+ * kernel then ORs HYB_DEV_TIMEOUT (and the wait's site in bits 8-15) into
+ * dev_status and returns without hanging.  The default, about 1 s
+ * (2^31 cycles), is reached only when CTAs of the launch cannot all become
+ * resident (another context holding SMs).  A small limit makes such waits
+ * expire on purpose, which is how failure detection is tested.  cycles < 0
+ * restores the default.  Process-wide; applies to launches issued after the
+ * call.  Returns the previous limit.  After a call that reported
+ * HYB_DEV_TIMEOUT, the counters of its workspace must be zero-filled again
+ * (see the workspace notes of csa_index_topk and csa_attend, and
+ * csa_index_topk_noalloc_reset).  (Waits inside one CTA -- mbarriers of the
+ * copy / tensor-core pipelines -- keep their fixed bound of about 1 s.)
+ * ------------------------------------------------------------------------ */
+HYB_API int64_t hyb_set_grid_wait_limit(int64_t cycles);
 
 /* ------------------------------------------------------------------------ misc */
 HYB_API const char* hyb_status_string(hyb_status s);

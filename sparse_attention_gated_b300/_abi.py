@@ -33,12 +33,12 @@ class IndexArgs(ctypes.Structure):
     _fields_ = [("qI", _p), ("qI_scale", _p), ("w", _p), ("kI", _p), ("kI_scale", _p), ("idx", _p), ("scores", _p),
                 ("batch", _i64), ("n_q", _i64), ("n_entries", _i64), ("kv_stride", _i64), ("n_ih", _i64),
                 ("c_I", _i64), ("m", _i64), ("k", _i64), ("q_pos0", _i64), ("dtype", _i32), ("dev_status", _p),
-                ("ev_scores_begin", _p), ("ev_scores_end", _p)]
+                ("ev_scores_begin", _p), ("ev_scores_end", _p), ("q_pos", _p)]
 
 
 class Window(ctypes.Structure):
     _fields_ = [("kw", _p), ("n_kv", _i64), ("kv_pos0", _i64), ("q_pos0", _i64), ("n_win", _i64), ("out", _p),
-                ("out_dtype", _i32)]
+                ("out_dtype", _i32), ("q_pos", _p), ("kv_pos0s", _p)]
 
 
 class CsaAttendArgs(ctypes.Structure):
@@ -50,7 +50,7 @@ class CsaAttendArgs(ctypes.Structure):
 class HcaAttendArgs(ctypes.Structure):
     _fields_ = [("q", _p), ("kc", _p), ("vc", _p), ("o", _p), ("lse", _p), ("batch", _i64), ("n_q", _i64),
                 ("n_h", _i64), ("c", _i64), ("n_entries", _i64), ("kv_stride", _i64), ("m", _i64), ("q_pos0", _i64),
-                ("scale", _f), ("dtype", _i32), ("dev_status", _p), ("window", _p), ("sink", _p)]
+                ("scale", _f), ("dtype", _i32), ("dev_status", _p), ("window", _p), ("sink", _p), ("q_pos", _p)]
 
 
 class NormRopeArgs(ctypes.Structure):
@@ -62,7 +62,7 @@ class SwaArgs(ctypes.Structure):
     _fields_ = [("q", _p), ("kw", _p), ("vw", _p), ("o_in", _p), ("lse_in", _p), ("out", _p), ("lse_out", _p),
                 ("batch", _i64), ("n_q", _i64), ("n_h", _i64), ("c", _i64), ("n_kv", _i64), ("kv_pos0", _i64),
                 ("q_pos0", _i64), ("n_win", _i64), ("scale", _f), ("dtype", _i32), ("out_dtype", _i32),
-                ("dev_status", _p)]
+                ("dev_status", _p), ("q_pos", _p), ("kv_pos0s", _p)]
 
 
 # every symbol include/hyb.h declares, with (restype, argtypes)
@@ -74,6 +74,8 @@ SIGNATURES = {
     "csa_index_topk_counter_bytes": (ctypes.c_size_t, []),
     "csa_index_topk": (ctypes.c_int, [ctypes.POINTER(IndexArgs), _p, ctypes.c_size_t, _p]),
     "csa_index_topk_noalloc": (ctypes.c_int, [ctypes.POINTER(IndexArgs), _p]),
+    "csa_index_topk_noalloc_reset": (ctypes.c_int, [_p]),
+    "hyb_set_grid_wait_limit": (_i64, [_i64]),
     "csa_attend_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(CsaAttendArgs)]),
     "csa_attend": (ctypes.c_int, [ctypes.POINTER(CsaAttendArgs), _p, ctypes.c_size_t, _p]),
     "hca_attend_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(HcaAttendArgs)]),

@@ -40,7 +40,8 @@ __global__ void __launch_bounds__(256) attend_cc_kernel(AttendParams P) {
   const int sp = blockIdx.y % P.n_split;
   const int64_t b = blockIdx.z;
   if (h >= J.n_h) return;
-  const int64_t t = J.q_pos0 + jq;
+  const int64_t t = query_pos(J.q_pos, J.q_pos0, b * J.n_q + jq, jq);
+  const bool report = lane == 0 && sp == 0 && (threadIdx.x >> 5) == 0 && blockIdx.x == 0;
   const int64_t c = J.c;
 
   // the entry list of this query
@@ -51,11 +52,10 @@ __global__ void __launch_bounds__(256) attend_cc_kernel(AttendParams P) {
     L = J.list_len;
     list = J.idx + (b * J.n_q + jq) * J.list_len;
   } else if constexpr (MODE == 1) {
-    L = visible_entries(t, J.m);
-    if (L > J.n_entries) L = J.n_entries;
+    L = visible_checked(t, J.m, J.n_entries, J.dev_status, report);
   } else {
-    L = t + 1 < J.n_win ? t + 1 : J.n_win;
-    first_row = t - L + 1 - J.kv_pos0;
+    const int64_t kvp = J.kv_pos0s ? __ldg(J.kv_pos0s + b) : J.kv_pos0;
+    L = window_rows(t, J.n_win, kvp, J.n_entries, &first_row, J.dev_status, report);
   }
   const int64_t chunk = (L + P.n_split - 1) / P.n_split;
   const int64_t e_begin = (int64_t)sp * chunk;
@@ -235,7 +235,8 @@ bool attend_cc_shape_supported(int64_t c, int64_t n_h) {
 
 static int64_t list_len_max(const AttendJob& j) {
   if (j.mode == 0) return j.list_len;
-  if (j.mode == 1) return std::min<int64_t>(visible_entries(j.q_pos0 + j.n_q - 1, j.m), j.n_entries);
+  if (j.mode == 1)
+    return j.q_pos ? j.n_entries : std::min<int64_t>(visible_entries(j.q_pos0 + j.n_q - 1, j.m), j.n_entries);
   return j.n_win;
 }
 

@@ -110,8 +110,16 @@ struct AtcParams {
   int win;
   const __nv_bfloat16* kw;
   int64_t w_stride, w_pos0, wq_pos0;
+  // optional positions in device memory (read after the grid-dependency wait): per-query
+  // positions of the call (modes 1/2) and of the fused window, per-sequence kv_pos0 of the
+  // window rows (mode 2) and of the fused window's
+  const int64_t* q_pos;
+  const int64_t* kv_pos0s;
+  const int64_t* wq_pos;
+  const int64_t* w_pos0s;
   float scale_log2;
   int32_t* dev_status;
+  long long wait_cycles;  // bound of the split join's wait (SM clock cycles)
 };
 
 struct AtcWork {
@@ -132,30 +140,34 @@ __device__ __forceinline__ AtcWork atc_work(const AtcParams& p) {
   w.bq = id / ((int64_t)p.n_hg * p.n_split);
   w.b = w.bq / p.n_q;
   w.j = w.bq % p.n_q;
-  const int64_t t = p.q_pos0 + w.j;
+  const bool report = w.hg == 0 && threadIdx.x == 0;
   w.list = nullptr;
   w.row0 = 0;
   w.win = false;
   if (MODE != 2 && p.win && w.sp == p.n_split - 1) {
     // the fused window: raw rows max(0, tw-n_win+1) .. tw of kw
-    const int64_t tw = p.wq_pos0 + w.j;
+    const int64_t tw = query_pos(p.wq_pos, p.wq_pos0, w.bq, w.j);
+    const int64_t kvp = p.w_pos0s ? __ldg(p.w_pos0s + w.b) : p.w_pos0;
+    int64_t first;
     w.win = true;
-    w.L = tw + 1 < p.n_win ? tw + 1 : p.n_win;
-    w.row0 = w.b * p.w_stride + (tw - w.L + 1 - p.w_pos0);
+    w.L = window_rows(tw, p.n_win, kvp, p.w_stride, &first, p.dev_status, report);
+    w.row0 = w.b * p.w_stride + first;
     w.tb = 0;
     w.te = (w.L + kTile - 1) / kTile;
     return w;
   }
+  const int64_t t = MODE == 0 ? 0 : query_pos(p.q_pos, p.q_pos0, w.bq, w.j);
   if constexpr (MODE == 0) {
     w.L = p.list_len;
     w.list = p.idx + w.bq * p.list_len;
   } else if constexpr (MODE == 1) {
-    const int64_t v = visible_entries(t, p.m);
-    w.L = v < p.n_entries ? v : p.n_entries;
+    w.L = visible_checked(t, p.m, p.n_entries, p.dev_status, report && w.sp == 0);
     w.row0 = w.b * p.kv_stride;
   } else {
-    w.L = t + 1 < p.n_win ? t + 1 : p.n_win;
-    w.row0 = w.b * p.kv_stride + (t - w.L + 1 - p.kv_pos0);
+    const int64_t kvp = p.kv_pos0s ? __ldg(p.kv_pos0s + w.b) : p.kv_pos0;
+    int64_t first;
+    w.L = window_rows(t, p.n_win, kvp, p.kv_stride, &first, p.dev_status, report && w.sp == 0);
+    w.row0 = w.b * p.kv_stride + first;
     // (split window merges divide the output dims, not the rows: every split sees the window)
     w.tb = 0;
     w.te = (w.L + kTile - 1) / kTile;
@@ -261,6 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc) + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // positions in device memory may have been written by the previous kernel: read them after the wait
+  if (p.q_pos != nullptr || p.kv_pos0s != nullptr || p.wq_pos != nullptr || p.w_pos0s != nullptr) pdl_wait();
   const AtcWork W = atc_work<MODE>(p);
   const int64_t ntiles = W.te - W.tb;
   // K = V and one tile: O^T reads the K slabs still in the ring (no V group);
@@ -858,7 +872,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const long long t0 = clock64();
         bool joined = true;
         while (tc::ld_acquire_gpu_u32(cnt) < (uint32_t)S) {
-          if (clock64() - t0 > tc::kWaitLimitCycles) {
+          if (clock64() - t0 > p.wait_cycles) {
             *s_abort = 18;
             joined = false;
             break;
@@ -959,7 +973,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int64_t atc_list_len_max(const AttendJob& j) {
   if (j.mode == 0) return j.list_len;
-  if (j.mode == 1) return std::min<int64_t>(visible_entries(j.q_pos0 + j.n_q - 1, j.m), j.n_entries);
+  if (j.mode == 1)
+    return j.q_pos ? j.n_entries : std::min<int64_t>(visible_entries(j.q_pos0 + j.n_q - 1, j.m), j.n_entries);
   return j.n_win;
 }
 
@@ -1040,9 +1055,11 @@ cudaError_t launch_attend_tc(const AttendJob& j, void* ws, cudaStream_t s) {
   p.alias = j.k == j.v;
   p.scale_log2 = j.scale * kLog2e;
   p.dev_status = j.dev_status;
+  p.wait_cycles = grid_wait_cycles();
   p.win = j.win;
   p.kw = static_cast<const __nv_bfloat16*>(j.wk);
   p.w_stride = j.w_stride, p.w_pos0 = j.w_pos0, p.wq_pos0 = j.wq_pos0;
+  p.q_pos = j.q_pos, p.kv_pos0s = j.kv_pos0s, p.wq_pos = j.wq_pos, p.w_pos0s = j.w_pos0s;
   const int64_t rows = j.batch * j.n_q;
   if (p.n_split > 1 && j.mode != 2) {
     if (rows * p.n_hg > kMaxJoinUnits) return cudaErrorInvalidConfiguration;  // (the plan never does this)

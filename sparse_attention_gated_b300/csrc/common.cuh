@@ -167,4 +167,49 @@ __device__ __forceinline__ void flag_status(int32_t* dev_status, int bits) {
 // Entries visible to absolute position t with compression factor m.
 __host__ __device__ __forceinline__ int64_t visible_entries(int64_t t, int64_t m) { return (t + 1) / m; }
 
+// Absolute position of query j of row `row` (row = b * n_q + j): the caller's per-query
+// position where an array of them is given (device memory), else q_pos0 + j.
+__device__ __forceinline__ int64_t query_pos(const int64_t* q_pos, int64_t q_pos0, int64_t row, int64_t j) {
+  return q_pos != nullptr ? __ldg(q_pos + row) : q_pos0 + j;
+}
+
+// Entries visible to position t, at most the n_entries that exist.  The host checks
+// every position it is given as a number; a position read from device memory that is
+// negative or would see more entries than exist is reported as HYB_DEV_BAD_INDEX and
+// clipped (a negative one sees nothing).
+__device__ __forceinline__ int64_t visible_checked(int64_t t, int64_t m, int64_t n_entries, int32_t* dev_status,
+                                                   bool report) {
+  if (t < 0) {
+    if (report) flag_status(dev_status, HYB_DEV_BAD_INDEX);
+    return 0;
+  }
+  const int64_t v = visible_entries(t, m);
+  if (v > n_entries) {
+    if (report) flag_status(dev_status, HYB_DEV_BAD_INDEX);
+    return n_entries;
+  }
+  return v;
+}
+
+// The sliding window of position t: absolute rows max(0, t-n_win+1) .. t of a buffer
+// whose row 0 is absolute position kv_pos0 and which holds n_kv rows.  Returns the row
+// count and sets *first to the buffer row of the first one.  Rows outside the buffer
+// (possible only with positions read from device memory: the host checks its own) are
+// left out and reported as HYB_DEV_BAD_INDEX.
+__device__ __forceinline__ int64_t window_rows(int64_t t, int64_t n_win, int64_t kv_pos0, int64_t n_kv,
+                                               int64_t* first, int32_t* dev_status, bool report) {
+  int64_t lo = t - n_win + 1 > 0 ? t - n_win + 1 : 0;
+  int64_t hi = t;
+  bool bad = t < 0;
+  if (lo < kv_pos0) lo = kv_pos0, bad = true;
+  if (hi > kv_pos0 + n_kv - 1) hi = kv_pos0 + n_kv - 1, bad = true;
+  if (bad && report) flag_status(dev_status, HYB_DEV_BAD_INDEX);
+  if (hi < lo) {
+    *first = 0;
+    return 0;
+  }
+  *first = lo - kv_pos0;
+  return hi - lo + 1;
+}
+
 }  // namespace hyb

@@ -2,6 +2,7 @@
 // validation (before any launch), workspace sizing, dispatch to the kernels
 // and error reporting.  No device memory is allocated here.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -66,11 +67,26 @@ int64_t n_vis_max(int64_t q_pos0, int64_t n_q, int64_t m, int64_t n_entries) {
   return v < n_entries ? v : n_entries;
 }
 
+// the most entries any query of an index call sees: with per-query positions in device
+// memory the host cannot tell, so every row is sized for all of them
+int64_t index_vis_max(const hyb_index_args* a) {
+  if (a->n_q <= 0) return 0;
+  return a->q_pos ? a->n_entries : n_vis_max(a->q_pos0, a->n_q, a->m, a->n_entries);
+}
+
+std::atomic<long long> g_grid_wait_cycles{hyb::kDefaultGridWaitCycles};
+
 }  // namespace
+
+long long hyb::grid_wait_cycles() { return g_grid_wait_cycles.load(std::memory_order_relaxed); }
 
 extern "C" {
 
 int32_t hyb_version(void) { return 1; }
+
+int64_t hyb_set_grid_wait_limit(int64_t cycles) {
+  return g_grid_wait_cycles.exchange(cycles < 0 ? hyb::kDefaultGridWaitCycles : (long long)cycles);
+}
 int32_t hyb_built_arch(void) { return HYB_BUILT_ARCH; }
 
 const char* hyb_status_string(hyb_status s) {
@@ -142,7 +158,7 @@ hyb_status hyb_compress(const hyb_compress_args* a, void*, size_t, void* stream)
 // ---------------------------------------------------------------- index + top-k
 
 static size_t index_scores_bytes(const hyb_index_args* a) {
-  const int64_t nv = n_vis_max(a->q_pos0, a->n_q, a->m, a->n_entries);
+  const int64_t nv = index_vis_max(a);
   return round_up((size_t)(a->batch * a->n_q) * (size_t)nv * sizeof(float), 256);
 }
 
@@ -150,7 +166,7 @@ size_t csa_index_topk_counter_bytes(void) { return hyb::kTopkZeroRegionBytes; }
 
 size_t csa_index_topk_workspace_size(const hyb_index_args* a) {
   if (!a || a->batch <= 0 || a->n_q <= 0 || a->m < 1) return 0;
-  const int64_t nv = n_vis_max(a->q_pos0, a->n_q, a->m, a->n_entries);
+  const int64_t nv = index_vis_max(a);
   return hyb::kTopkZeroRegionBytes + index_scores_bytes(a) + round_up(hyb::topk_workspace_bytes(a, nv), 256);
 }
 
@@ -167,13 +183,13 @@ static hyb_status validate_index(const hyb_index_args* a) {
                 (long long)a->c_I);
   if (a->kv_stride != 0 && a->kv_stride < a->n_entries)
     return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: kv_stride < n_entries");
-  if (a->n_q > 0 && hyb::visible_entries(a->q_pos0 + a->n_q - 1, a->m) > a->n_entries)
+  if (!a->q_pos && a->n_q > 0 && hyb::visible_entries(a->q_pos0 + a->n_q - 1, a->m) > a->n_entries)
     return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: the last query sees %lld entries but only %lld exist",
                 (long long)hyb::visible_entries(a->q_pos0 + a->n_q - 1, a->m), (long long)a->n_entries);
   if (a->batch == 0 || a->n_q == 0) return ok();
-  if (!hyb::topk_shape_supported(a, n_vis_max(a->q_pos0, a->n_q, a->m, a->n_entries)))
+  if (!hyb::topk_shape_supported(a, index_vis_max(a)))
     return fail(HYB_ERR_UNSUPPORTED, "csa_index_topk: %lld visible entries with k = %lld exceed the top-k plan",
-                (long long)n_vis_max(a->q_pos0, a->n_q, a->m, a->n_entries), (long long)a->k);
+                (long long)index_vis_max(a), (long long)a->k);
   if (!a->qI || !a->w || !a->idx) return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: NULL qI/w/idx");
   if (a->n_entries > 0 && !a->kI) return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: NULL kI");
   const bool fp8 = a->dtype == HYB_E4M3;
@@ -181,8 +197,9 @@ static hyb_status validate_index(const hyb_index_args* a) {
     return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: E4M3 needs qI_scale and kI_scale");
   if (!fp8 && (a->qI_scale || a->kI_scale))
     return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: scales must be NULL for F32");
-  if (!aligned(a->kI, 16) || !aligned(a->qI, 4) || !aligned(a->w, 4) || !aligned(a->idx, 4) || !aligned(a->scores, 4))
-    return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: misaligned pointer (kI needs 16 bytes)");
+  if (!aligned(a->kI, 16) || !aligned(a->qI, 4) || !aligned(a->w, 4) || !aligned(a->idx, 4) || !aligned(a->scores, 4) ||
+      !aligned(a->q_pos, 8))
+    return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: misaligned pointer (kI needs 16 bytes, q_pos 8)");
   return ok();
 }
 
@@ -194,7 +211,7 @@ hyb_status csa_index_topk(const hyb_index_args* a, void* workspace, size_t ws_by
     return fail(HYB_ERR_WORKSPACE, "csa_index_topk: workspace of %zu bytes needed, %zu given", need, ws_bytes);
   if (!aligned(workspace, 256)) return fail(HYB_ERR_WORKSPACE, "csa_index_topk: workspace must be 256-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int64_t nv = n_vis_max(a->q_pos0, a->n_q, a->m, a->n_entries);
+  const int64_t nv = index_vis_max(a);
   // [counters that stay zero between calls][scores][top-k scratch]
   void* zr = workspace;
   float* scores = reinterpret_cast<float*>(static_cast<char*>(workspace) + hyb::kTopkZeroRegionBytes);
@@ -228,6 +245,24 @@ void* g_noalloc_ptr[kMaxDevices] = {};
 
 }  // namespace
 
+// The device address of the scratch array on the current device, looked up once per
+// device (with that device current) and remembered.
+static hyb_status noalloc_scratch(const char* name, void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e, name);
+  if (dev < 0 || dev >= kMaxDevices) return fail(HYB_ERR_UNSUPPORTED, "%s: device %d", name, dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_status(e, name);
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return HYB_OK;
+}
+
 hyb_status csa_index_topk_noalloc(const hyb_index_args* a, void* stream) {
   hyb_status st = validate_index(a);
   if (st != HYB_OK || a->batch == 0 || a->n_q == 0) return st;
@@ -235,22 +270,18 @@ hyb_status csa_index_topk_noalloc(const hyb_index_args* a, void* stream) {
   if (need > HYB_NOALLOC_SCRATCH_BYTES)
     return fail(HYB_ERR_WORKSPACE, "csa_index_topk_noalloc: these sizes need %zu bytes of scratch, more than the %zu "
                 "bytes the library holds", need, (size_t)HYB_NOALLOC_SCRATCH_BYTES);
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_status(e, "csa_index_topk_noalloc: cudaGetDevice");
-  if (dev < 0 || dev >= kMaxDevices) return fail(HYB_ERR_UNSUPPORTED, "csa_index_topk_noalloc: device %d", dev);
-  void* scratch;
-  {
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
-      void* p = nullptr;
-      e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // with device `dev` current
-      if (e != cudaSuccess) return cuda_status(e, "csa_index_topk_noalloc: cudaGetSymbolAddress");
-      g_noalloc_ptr[dev] = p;
-    }
-    scratch = g_noalloc_ptr[dev];
-  }
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch("csa_index_topk_noalloc", &scratch)) != HYB_OK) return st;
   return csa_index_topk(a, scratch, HYB_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+hyb_status csa_index_topk_noalloc_reset(void* stream) {
+  void* scratch = nullptr;
+  hyb_status st = noalloc_scratch("csa_index_topk_noalloc_reset", &scratch);
+  if (st != HYB_OK) return st;
+  // a memset of memory the library already holds: nothing is allocated
+  return cuda_status(cudaMemsetAsync(scratch, 0, hyb::kTopkZeroRegionBytes, static_cast<cudaStream_t>(stream)),
+                     "csa_index_topk_noalloc_reset");
 }
 
 // ---------------------------------------------------------------- attention
@@ -270,6 +301,7 @@ static hyb::AttendJob hca_job(const hyb_hca_attend_args* a) {
   j.batch = a->batch, j.n_q = a->n_q, j.n_h = a->n_h, j.c = a->c, j.n_entries = a->n_entries;
   j.kv_stride = a->kv_stride > 0 ? a->kv_stride : a->n_entries;
   j.m = a->m, j.q_pos0 = a->q_pos0, j.scale = a->scale, j.dtype = a->dtype, j.dev_status = a->dev_status;
+  j.q_pos = a->q_pos;
   return j;
 }
 
@@ -280,6 +312,7 @@ static hyb::AttendJob swa_job(const hyb_swa_args* a) {
   j.batch = a->batch, j.n_q = a->n_q, j.n_h = a->n_h, j.c = a->c, j.n_entries = a->n_kv, j.kv_stride = a->n_kv;
   j.kv_pos0 = a->kv_pos0, j.q_pos0 = a->q_pos0, j.n_win = a->n_win;
   j.scale = a->scale, j.dtype = a->dtype, j.dev_status = a->dev_status;
+  j.q_pos = a->q_pos, j.kv_pos0s = a->kv_pos0s;
   return j;
 }
 
@@ -325,6 +358,7 @@ static hyb_status run_attend(const char* name, const hyb::AttendJob& j, void* wo
 
 static hyb::AttendJob fused_job(hyb::AttendJob j, const hyb_window* w) {
   j.win = 1, j.wk = w->kw, j.w_stride = w->n_kv, j.w_pos0 = w->kv_pos0, j.wq_pos0 = w->q_pos0, j.n_win = w->n_win;
+  j.wq_pos = w->q_pos, j.w_pos0s = w->kv_pos0s;
   j.out = w->out, j.out_bf16 = w->out_dtype == HYB_BF16, j.o = nullptr;
   return j;
 }
@@ -338,6 +372,7 @@ static hyb::AttendJob window_merge_job(const hyb::AttendJob& c, const hyb_window
   j.batch = c.batch, j.n_q = c.n_q, j.n_h = c.n_h, j.c = c.c, j.n_entries = w->n_kv, j.kv_stride = w->n_kv;
   j.kv_pos0 = w->kv_pos0, j.q_pos0 = w->q_pos0, j.n_win = w->n_win;
   j.scale = c.scale, j.dtype = c.dtype, j.dev_status = c.dev_status;
+  j.q_pos = w->q_pos, j.kv_pos0s = w->kv_pos0s;
   return j;
 }
 
@@ -359,13 +394,17 @@ static hyb_status validate_window(const char* name, const hyb::AttendJob& c, con
     return fail(HYB_ERR_INVALID_ARG, "%s: window n_win < 1 or negative position", name);
   if (w->out_dtype != HYB_F32 && w->out_dtype != HYB_BF16)
     return fail(HYB_ERR_INVALID_ARG, "%s: window out_dtype must be F32 or BF16", name);
-  if (c.mode == 1 && w->q_pos0 != c.q_pos0)
-    return fail(HYB_ERR_INVALID_ARG, "%s: window q_pos0 %lld differs from q_pos0 %lld", name, (long long)w->q_pos0,
-                (long long)c.q_pos0);
+  if (c.mode == 1 && (w->q_pos != c.q_pos || (!c.q_pos && w->q_pos0 != c.q_pos0)))
+    return fail(HYB_ERR_INVALID_ARG, "%s: the window's query positions (q_pos0 %lld, q_pos %p) differ from the call's "
+                "(q_pos0 %lld, q_pos %p)", name, (long long)w->q_pos0, (const void*)w->q_pos, (long long)c.q_pos0,
+                (const void*)c.q_pos);
+  if (!aligned(w->q_pos, 8) || !aligned(w->kv_pos0s, 8))
+    return fail(HYB_ERR_INVALID_ARG, "%s: misaligned window q_pos/kv_pos0s", name);
   if (c.batch == 0 || c.n_q == 0 || c.n_h == 0) return ok();
   const int64_t lo = w->q_pos0 - w->n_win + 1 > 0 ? w->q_pos0 - w->n_win + 1 : 0;
   const int64_t hi = w->q_pos0 + c.n_q - 1;
-  if (lo < w->kv_pos0 || hi >= w->kv_pos0 + w->n_kv)
+  // (positions in device memory are checked by the kernels)
+  if (!w->q_pos && !w->kv_pos0s && (lo < w->kv_pos0 || hi >= w->kv_pos0 + w->n_kv))
     return fail(HYB_ERR_INVALID_ARG, "%s: window rows %lld..%lld are not all inside the buffer %lld..%lld", name,
                 (long long)lo, (long long)hi, (long long)w->kv_pos0, (long long)(w->kv_pos0 + w->n_kv - 1));
   if (!w->kw || !w->out) return fail(HYB_ERR_INVALID_ARG, "%s: NULL window kw/out", name);
@@ -446,7 +485,8 @@ hyb_status hca_attend(const hyb_hca_attend_args* a, void* workspace, size_t ws_b
   if (a->m < 1 || a->q_pos0 < 0 || a->n_entries < 0 || a->kv_stride < 0)
     return fail(HYB_ERR_INVALID_ARG, "hca_attend: m < 1 or negative size");
   if (a->kv_stride != 0 && a->kv_stride < a->n_entries) return fail(HYB_ERR_INVALID_ARG, "hca_attend: kv_stride < n_entries");
-  if (a->n_q > 0 && hyb::visible_entries(a->q_pos0 + a->n_q - 1, a->m) > a->n_entries)
+  if (!aligned(a->q_pos, 8)) return fail(HYB_ERR_INVALID_ARG, "hca_attend: misaligned q_pos");
+  if (!a->q_pos && a->n_q > 0 && hyb::visible_entries(a->q_pos0 + a->n_q - 1, a->m) > a->n_entries)
     return fail(HYB_ERR_INVALID_ARG, "hca_attend: the last query sees %lld entries but only %lld exist",
                 (long long)hyb::visible_entries(a->q_pos0 + a->n_q - 1, a->m), (long long)a->n_entries);
   if (a->window && (st = validate_window("hca_attend", hca_job(a), a->window)) != HYB_OK) return st;
@@ -476,9 +516,12 @@ hyb_status swa_merge(const hyb_swa_args* a, void* workspace, size_t ws_bytes, vo
   if ((a->o_in == nullptr) != (a->lse_in == nullptr))
     return fail(HYB_ERR_INVALID_ARG, "swa_merge: o_in and lse_in must both be given or both be NULL");
   if (a->batch == 0 || a->n_q == 0 || a->n_h == 0) return ok();
+  if (!aligned(a->q_pos, 8) || !aligned(a->kv_pos0s, 8))
+    return fail(HYB_ERR_INVALID_ARG, "swa_merge: misaligned q_pos/kv_pos0s");
   const int64_t lo = a->q_pos0 - a->n_win + 1 > 0 ? a->q_pos0 - a->n_win + 1 : 0;
   const int64_t hi = a->q_pos0 + a->n_q - 1;
-  if (lo < a->kv_pos0 || hi >= a->kv_pos0 + a->n_kv)
+  // (positions in device memory are checked by the kernels)
+  if (!a->q_pos && !a->kv_pos0s && (lo < a->kv_pos0 || hi >= a->kv_pos0 + a->n_kv))
     return fail(HYB_ERR_INVALID_ARG, "swa_merge: window rows %lld..%lld are not all inside the buffer %lld..%lld",
                 (long long)lo, (long long)hi, (long long)a->kv_pos0, (long long)(a->kv_pos0 + a->n_kv - 1));
   if (!a->out) return fail(HYB_ERR_INVALID_ARG, "swa_merge: NULL out");

@@ -20,6 +20,8 @@ struct IndexParams {
   const float* kI_scale;
   float* scores;
   int64_t score_stride, n_q, n_entries, kv_stride, n_ih, c_I, m, q_pos0;
+  const int64_t* q_pos;  // optional per-query positions [batch * n_q]
+  int32_t* dev_status;
 };
 
 __device__ __forceinline__ void e4m3x2_to_f32(uint32_t two, float& a, float& b) {
@@ -51,9 +53,8 @@ __global__ void __launch_bounds__(256) index_scores_cc_kernel(IndexParams p) {
   float* q_s = reinterpret_cast<float*>(smem4);  // [n_ih][c_I]
   float* w_s = q_s + p.n_ih * p.c_I;            // [n_ih]
   const int64_t b = blockIdx.z, j = blockIdx.y;
-  const int64_t t = p.q_pos0 + j;
-  int64_t vis = visible_entries(t, p.m);
-  if (vis > p.n_entries) vis = p.n_entries;
+  const int64_t t = query_pos(p.q_pos, p.q_pos0, b * p.n_q + j, j);
+  const int64_t vis = visible_checked(t, p.m, p.n_entries, p.dev_status, blockIdx.x == 0 && threadIdx.x == 0);
   const int64_t s0 = (int64_t)blockIdx.x * blockDim.x;
   if (s0 >= vis) return;
 
@@ -114,6 +115,7 @@ cudaError_t launch_index_scores_cc(const hyb_index_args* a, float* scores, int64
   p.score_stride = score_stride, p.n_q = a->n_q, p.n_entries = a->n_entries;
   p.kv_stride = a->kv_stride > 0 ? a->kv_stride : a->n_entries;
   p.n_ih = a->n_ih, p.c_I = a->c_I, p.m = a->m, p.q_pos0 = a->q_pos0;
+  p.q_pos = a->q_pos, p.dev_status = a->dev_status;
   if (n_vis_max == 0 || a->n_q == 0 || a->batch == 0) return cudaSuccess;
   const dim3 grid((unsigned)((n_vis_max + 255) / 256), (unsigned)a->n_q, (unsigned)a->batch), block(256);
   const size_t smem = sizeof(float) * (size_t)(a->n_ih * a->c_I + a->n_ih) + 16;

@@ -60,6 +60,7 @@ struct IdxTcParams {
   uint32_t* ghist;  // optional (one query per unit): [rows][kTopkHistBins] histogram of the score keys' top bits
   int64_t score_stride;
   int64_t n_q, n_entries, kv_stride, m, q_pos0;
+  const int64_t* q_pos;  // optional per-query positions [batch * n_q] (read after the grid-dependency wait)
   int64_t groups_per_b, tiles_per_unit, units_per_group, n_units;
   int32_t* dev_status;
 };
@@ -75,8 +76,17 @@ __device__ __forceinline__ IdxUnit idx_unit(const IdxTcParams& p, int64_t u) {
   U.b = g / p.groups_per_b;
   U.j0 = (g % p.groups_per_b) * NQ;
   U.nq = p.n_q - U.j0 < NQ ? p.n_q - U.j0 : NQ;
-  int64_t vis = visible_entries(p.q_pos0 + U.j0 + U.nq - 1, p.m);
-  if (vis > p.n_entries) vis = p.n_entries;
+  // entries the unit's queries see: the last one's with consecutive positions, the
+  // largest over them with per-query positions
+  int64_t vis = 0;
+  if (p.q_pos == nullptr) {
+    vis = visible_checked(p.q_pos0 + U.j0 + U.nq - 1, p.m, p.n_entries, nullptr, false);
+  } else {
+    for (int64_t q = 0; q < U.nq; ++q) {
+      const int64_t v = visible_checked(__ldg(p.q_pos + U.b * p.n_q + U.j0 + q), p.m, p.n_entries, nullptr, false);
+      vis = v > vis ? v : vis;
+    }
+  }
   const int64_t tiles = (vis + 127) / 128;
   U.tile_begin = chunk * p.tiles_per_unit;
   U.tile_end = U.tile_begin + p.tiles_per_unit < tiles ? U.tile_begin + p.tiles_per_unit : tiles;
@@ -136,10 +146,13 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
   tc::tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
   // the CTA's first unit, from the parameters alone (64-bit divisions): computed while
-  // the previous kernel may still be running
-  const IdxUnit U_first = idx_unit<NQ>(p, blockIdx.x);
+  // the previous kernel may still be running (with positions in device memory, after
+  // the wait: the previous kernel may have written them)
+  IdxUnit U_first;
+  if (p.q_pos == nullptr) U_first = idx_unit<NQ>(p, blockIdx.x);
   pdl_wait();  // (the setup above touched only shared memory, TMEM and the parameters)
   pdl_trigger();
+  if (p.q_pos != nullptr) U_first = idx_unit<NQ>(p, blockIdx.x);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -287,8 +300,10 @@ __global__ void __launch_bounds__(IdxTc<NQ>::kThreads, NQ == 1 ? 2 : 1)
 #pragma unroll
       for (int qi = 0; qi < kQPerWarp; ++qi) {
         const int q = NQ == 1 ? 0 : 2 * half + qi;
-        int64_t vis = visible_entries(p.q_pos0 + U.j0 + q, p.m);
-        vis_q[qi] = q < U.nq ? (vis < p.n_entries ? vis : p.n_entries) : 0;
+        const int64_t row = U.b * p.n_q + U.j0 + q;
+        vis_q[qi] = q < U.nq ? visible_checked(query_pos(p.q_pos, p.q_pos0, row, U.j0 + q), p.m, p.n_entries,
+                                               p.dev_status, lane == 0 && U.tile_begin == 0)
+                             : 0;
       }
       for (int64_t t = U.tile_begin; t < U.tile_end; ++t, ++seq) {
         if (NQ == 1 && (int)(seq & 1) != half) continue;  // the other group's tile
@@ -393,6 +408,7 @@ static cudaError_t launch_nq(const hyb_index_args* a, float* scores, int64_t sco
   p.w = a->w, p.qI_scale = a->qI_scale, p.scores = scores, p.score_stride = score_stride;
   p.ghist = nullptr;  // set below once the units are known
   p.n_q = a->n_q, p.n_entries = a->n_entries, p.kv_stride = kvs, p.m = a->m, p.q_pos0 = a->q_pos0;
+  p.q_pos = a->q_pos;
   p.groups_per_b = (a->n_q + NQ - 1) / NQ;
   const int64_t groups = p.groups_per_b * a->batch;
   const int64_t tiles_max = (n_vis_max + 127) / 128;

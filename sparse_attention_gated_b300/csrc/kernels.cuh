@@ -20,6 +20,12 @@ constexpr int kTopkHistBins = 1 << kTopkHistBits;
 constexpr size_t kTopkZeroRegionBytes =
     ((size_t)kNumSMs * (2 * kTopkHistBins + 256 + 3) * 4 + 4 * 4 + 255) / 256 * 256;
 
+// Bound, in SM clock cycles, of the device-side waits that span CTAs (the top-k grid
+// plan's grid barriers, the split joins of the attention kernel): the value set by
+// hyb_set_grid_wait_limit, about 1 s by default.
+constexpr long long kDefaultGridWaitCycles = 1LL << 31;
+long long grid_wait_cycles();
+
 // compress.cu
 bool compress_shape_supported(int64_t c);
 cudaError_t launch_compress(const hyb_compress_args* a, int64_t n_out, cudaStream_t s);
@@ -75,6 +81,13 @@ struct AttendJob {
   int win;
   const void* wk;
   int64_t w_stride, w_pos0, wq_pos0;
+  // optional device-side positions: q_pos [batch * n_q] absolute query positions (modes 1
+  // and 2; NULL = q_pos0 + j), kv_pos0s [batch] per-sequence kv_pos0 of the window rows
+  // (mode 2; NULL = kv_pos0); the fused window's own: wq_pos, w_pos0s
+  const int64_t* q_pos;
+  const int64_t* kv_pos0s;
+  const int64_t* wq_pos;
+  const int64_t* w_pos0s;
 };
 bool attend_cc_shape_supported(int64_t c, int64_t n_h);
 

@@ -69,7 +69,6 @@ constexpr int64_t kGridChunkCap = 32768;  // grid plan: keys per CTA, staged in 
 constexpr int kCandListCap = 4096;        // grid plan: candidates per row selected in shared memory
 constexpr int kSubListCap = 1024;         // grid plan, overflow: sub-candidates per row ranked directly
 constexpr int kGridSlot = 8;              // grid plan: published counts per CTA
-constexpr long long kGridWaitCycles = 1LL << 31;  // bound of a grid-barrier wait (about 1 s)
 
 struct TopkParams {
   const float* scores;
@@ -77,6 +76,7 @@ struct TopkParams {
   int32_t* idx;
   float* out_scores;
   int64_t n_q, n_entries, m, k, q_pos0;
+  const int64_t* q_pos;  // optional per-query positions [rows]
   // three-kernel plan
   int64_t chunk;
   int n_chunks;
@@ -98,12 +98,13 @@ struct TopkParams {
   uint2* sub;           // [rows][kSubListCap]: (key, entry) of the sub-candidates
   int hist_done;        // the row histograms were filled by the indexer
   int32_t* dev_status;
+  long long wait_cycles;  // bound of a grid-barrier wait (SM clock cycles)
 };
 
+// (a bad device-side position was reported by the scoring kernel of the same call)
 __device__ __forceinline__ int64_t row_visible(const TopkParams& p, int64_t row) {
   const int64_t j = row % p.n_q;
-  const int64_t v = visible_entries(p.q_pos0 + j, p.m);
-  return v < p.n_entries ? v : p.n_entries;
+  return visible_checked(query_pos(p.q_pos, p.q_pos0, row, j), p.m, p.n_entries, nullptr, false);
 }
 
 struct BlockShared {
@@ -647,7 +648,7 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* ptr) {
 // Barrier over all CTAs of the grid.  Arrivals count up in *count (zeroed before
 // the launch), so the i-th barrier waits for i * gridDim.x * gridDim.y of them.
 // Bounded: on expiry HYB_DEV_TIMEOUT (with the site) is raised and false returned.
-__device__ bool grid_barrier(uint32_t* count, uint32_t target, int32_t* dev_status, int site) {
+__device__ bool grid_barrier(uint32_t* count, uint32_t target, int32_t* dev_status, int site, long long limit) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -656,7 +657,7 @@ __device__ bool grid_barrier(uint32_t* count, uint32_t target, int32_t* dev_stat
     int ok = 1;
     const long long t0 = clock64();
     while (ld_acquire_u32(count) < target) {
-      if (clock64() - t0 > kGridWaitCycles) {
+      if (clock64() - t0 > limit) {
         ok = 0;
         break;
       }
@@ -738,7 +739,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_grid_kernel(TopkParams p
     __syncthreads();
     for (int i = tid; i < kHistBins; i += kTopkThreads)
       if (hist[i]) atomicAdd(p.ghist + row * kHistBins + i, hist[i]), hist[i] = 0;
-    if (!grid_barrier(p.gsync, ++nbar * nblk, p.dev_status, 40)) return;
+    if (!grid_barrier(p.gsync, ++nbar * nblk, p.dev_status, 40, p.wait_cycles)) return;
   }
 
   // phase 1: first-level threshold bin b1.  The chunk's keys in b1 (candidates) go to the
@@ -774,7 +775,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_grid_kernel(TopkParams p
   }
   for (int i = tid; i < kHistBins; i += kTopkThreads)
     if (hist[i]) atomicAdd(p.ghist2 + row * kHistBins + i, hist[i]);
-  if (!grid_barrier(p.gsync, ++nbar * nblk, p.dev_status, 41)) return;
+  if (!grid_barrier(p.gsync, ++nbar * nblk, p.dev_status, 41, p.wait_cycles)) return;
   {
     // every CTA of the row has read the first-level histogram: clear this CTA's slice of it
     const int slice = (kHistBins + parts - 1) / parts;
@@ -948,7 +949,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_grid_kernel(TopkParams p
     }
   sure = block_sum(sure, S);
   if (slow_row && tid == 0) myslot[0] = (int32_t)sure;
-  if (!grid_barrier(p.gsync, ++nbar * nblk, p.dev_status, 42)) return;
+  if (!grid_barrier(p.gsync, ++nbar * nblk, p.dev_status, 42, p.wait_cycles)) return;
 
   // phase 3s: select among the sub-candidates and write this chunk's kept entries
   const uint32_t n_sub = slow_row ? __ldcg(p.nsub + row) : 0u;
@@ -1015,7 +1016,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_grid_kernel(TopkParams p
       }
     __syncthreads();
     if (slow && tid < 256 && hist[tid]) atomicAdd(p.hist3 + row * 256 + tid, hist[tid]);
-    if (!grid_barrier(p.gsync, ++nbar * nblk, p.dev_status, 43)) return;
+    if (!grid_barrier(p.gsync, ++nbar * nblk, p.dev_status, 43, p.wait_cycles)) return;
     uint32_t T = 0, r3 = 0;
     if (slow) {
       if (tid < 32) {
@@ -1053,7 +1054,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_grid_kernel(TopkParams p
     uint32_t gb, eb, gtot, etot;
     block_scan_counts(gt, eq, S, gb, eb, gtot, etot);
     if (slow && tid == 0) myslot[1] = (int32_t)gtot, myslot[2] = (int32_t)etot;
-    if (!grid_barrier(p.gsync, ++nbar * nblk, p.dev_status, 44)) return;
+    if (!grid_barrier(p.gsync, ++nbar * nblk, p.dev_status, 44, p.wait_cycles)) return;
     if (slow) {
       if (tid < 32) {
         int64_t g_acc = 0, e_acc = 0;
@@ -1243,11 +1244,13 @@ cudaError_t launch_topk(const hyb_index_args* a, const float* scores, int64_t sc
                         bool hist_done, cudaStream_t s) {
   TopkParams p{};
   p.scores = scores, p.score_stride = score_stride, p.idx = a->idx, p.out_scores = a->scores;
-  p.n_q = a->n_q, p.n_entries = a->n_entries, p.m = a->m, p.k = a->k, p.q_pos0 = a->q_pos0;
+  p.n_q = a->n_q, p.n_entries = a->n_entries, p.m = a->m, p.k = a->k, p.q_pos0 = a->q_pos0, p.q_pos = a->q_pos;
   p.dev_status = a->dev_status;
+  p.wait_cycles = grid_wait_cycles();
   const int64_t rows = a->batch * a->n_q;
   if (rows == 0) return cudaSuccess;
-  const int64_t n_vis_max = std::min<int64_t>(visible_entries(a->q_pos0 + a->n_q - 1, a->m), a->n_entries);
+  const int64_t n_vis_max = a->q_pos ? a->n_entries
+                                     : std::min<int64_t>(visible_entries(a->q_pos0 + a->n_q - 1, a->m), a->n_entries);
   const TopkPlan pl = plan_topk(a, n_vis_max);
   cudaError_t e;
   if (pl.kind == 0) {

@@ -42,6 +42,15 @@ def _rows_ptr(t, batch_rows):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _pos_ptr(t, n, what):
+    """Pointer of an int64 device array of n positions (or None)."""
+    if t is None:
+        return None
+    if t.dtype != torch.int64 or t.numel() != n:
+        raise ValueError(f"{what} must be int64 with {n} elements")
+    return _ptr(t)
+
+
 def _dtype(t):
     try:
         return _DT[t.dtype]
@@ -128,7 +137,8 @@ def hyb_compress(ca, za, bias, m: int, *, cb=None, zb=None, overlap: bool = Fals
 
 
 def index_args(qI, w, kI, m, k, q_pos0, qI_scale=None, kI_scale=None, idx=None, scores=None, n_entries=None,
-               dev_status=None, scores_events=None):
+               dev_status=None, scores_events=None, q_pos=None):
+    """q_pos: optional int64 [B, n_q] per-query absolute positions (then q_pos0 is unused)."""
     B, n_q, n_ih, c_I = qI.shape
     a = _abi.IndexArgs()
     a.qI, a.qI_scale, a.w, a.kI, a.kI_scale = _ptr(qI), _ptr(qI_scale), _ptr(w), _ptr(kI), _ptr(kI_scale)
@@ -140,6 +150,7 @@ def index_args(qI, w, kI, m, k, q_pos0, qI_scale=None, kI_scale=None, idx=None, 
     a.dev_status = _ptr(dev_status)
     if scores_events is not None:  # (begin, end) torch.cuda.Event: recorded around the scoring kernel
         a.ev_scores_begin, a.ev_scores_end = (ctypes.c_void_p(int(e.cuda_event)) for e in scores_events)
+    a.q_pos = _pos_ptr(q_pos, B * n_q, "q_pos")
     return a
 
 
@@ -153,17 +164,19 @@ def csa_index_topk_counter_bytes() -> int:
     return int(_abi.load().csa_index_topk_counter_bytes())
 
 
-def csa_index_topk(qI, w, kI, *, m: int, k: int, q_pos0: int, qI_scale=None, kI_scale=None, n_entries=None,
+def csa_index_topk(qI, w, kI, *, m: int, k: int, q_pos0: int = 0, qI_scale=None, kI_scale=None, n_entries=None,
                    idx=None, scores=None, want_scores: bool = False, workspace=None, dev_status=None, stream=None,
-                   scores_events=None):
+                   scores_events=None, q_pos=None):
     """Lightning-indexer scores + top-k.  Returns idx (and the selected scores when asked).
-    scores_events: optional (begin, end) torch.cuda.Event, recorded around the scoring kernel."""
+    scores_events: optional (begin, end) torch.cuda.Event, recorded around the scoring kernel.
+    q_pos: optional int64 [B, n_q] per-query positions (instead of q_pos0 + j)."""
     B, n_q = qI.shape[:2]
     if idx is None:
         idx = torch.empty((B, n_q, k), dtype=torch.int32, device=qI.device)
     if scores is None and want_scores:
         scores = torch.empty((B, n_q, k), dtype=torch.float32, device=qI.device)
-    a = index_args(qI, w, kI, m, k, q_pos0, qI_scale, kI_scale, idx, scores, n_entries, dev_status, scores_events)
+    a = index_args(qI, w, kI, m, k, q_pos0, qI_scale, kI_scale, idx, scores, n_entries, dev_status, scores_events,
+                   q_pos)
     ws, nbytes = _workspace(csa_index_topk_workspace_size(a), workspace, qI.device, zeroed=True)
     _abi.check(_abi.load().csa_index_topk(ctypes.byref(a), ws, nbytes, _stream(stream)), "csa_index_topk")
     return (idx, scores) if want_scores else idx
@@ -172,13 +185,17 @@ def csa_index_topk(qI, w, kI, *, m: int, k: int, q_pos0: int, qI_scale=None, kI_
 # ---------------------------------------------------------------- attention
 
 
-def window_args(kw, *, kv_pos0: int, q_pos0: int, n_win: int, out):
+def window_args(kw, *, kv_pos0: int = 0, q_pos0: int = 0, n_win: int, out, q_pos=None, kv_pos0s=None):
     """The fused window merge of csa_attend / hca_attend (hyb_window): the raw rows kw
-    [B, n_kv, c] (row 0 = absolute position kv_pos0) are the window's keys and values;
-    out [B, n_q, n_h, c] receives the merged output."""
+    [B, n_kv, c] (row 0 = absolute position kv_pos0, or kv_pos0s[b] per sequence) are the
+    window's keys and values; out [B, n_q, n_h, c] receives the merged output.  q_pos:
+    optional int64 [B, n_q] per-query positions; kv_pos0s: optional int64 [B]."""
     w = _abi.Window()
     w.kw, w.n_kv, w.kv_pos0, w.q_pos0, w.n_win = _ptr(kw), kw.shape[1], kv_pos0, q_pos0, n_win
     w.out, w.out_dtype = _ptr(out), _dtype(out)
+    B, n_q = out.shape[:2]
+    w.q_pos = _pos_ptr(q_pos, B * n_q, "window q_pos")
+    w.kv_pos0s = _pos_ptr(kv_pos0s, B, "window kv_pos0s")
     return w
 
 
@@ -236,7 +253,8 @@ def csa_attend(q, kc, vc, idx, *, scale: float | None = None, n_entries=None, o=
     return (out, lse) if w is not None else (o, lse)
 
 
-def hca_attend_args(q, kc, vc, m, q_pos0, scale, o, lse, n_entries=None, dev_status=None, window=None, sink=None):
+def hca_attend_args(q, kc, vc, m, q_pos0, scale, o, lse, n_entries=None, dev_status=None, window=None, sink=None,
+                    q_pos=None):
     B, n_q, n_h, c = q.shape
     _check_sink(sink, n_h)
     a = _abi.HcaAttendArgs()
@@ -250,30 +268,34 @@ def hca_attend_args(q, kc, vc, m, q_pos0, scale, o, lse, n_entries=None, dev_sta
     a._window = window
     a.window = ctypes.cast(ctypes.pointer(window), ctypes.c_void_p) if window is not None else None
     a.sink = _ptr(sink)
+    a.q_pos = _pos_ptr(q_pos, B * n_q, "q_pos")
     return a
 
 
-def hca_attend(q, kc, vc, *, m: int, q_pos0: int, scale: float | None = None, n_entries=None, o=None, lse=None,
-               workspace=None, dev_status=None, stream=None, window=None, sink=None):
+def hca_attend(q, kc, vc, *, m: int, q_pos0: int = 0, scale: float | None = None, n_entries=None, o=None,
+               lse=None, workspace=None, dev_status=None, stream=None, window=None, sink=None, q_pos=None):
     """HCA core attention over every visible entry.  Returns (o, lse), or (out, lse) of the
-    union with a fused window merge (window=dict(kw, kv_pos0, n_win[, out]); q_pos0 as the call's).
-    sink: optional float32 [n_h] per-head attention-sink logits, applied to the result."""
+    union with a fused window merge (window=dict(kw, kv_pos0 or kv_pos0s, n_win[, out]); the
+    window's query positions are the call's).  sink: optional float32 [n_h] per-head
+    attention-sink logits, applied to the result.  q_pos: optional int64 [B, n_q] per-query
+    positions (instead of q_pos0 + j)."""
     B, n_q, n_h, c = q.shape
     scale = 1.0 / math.sqrt(c) if scale is None else scale
-    if window is not None and "q_pos0" not in window:
-        window = dict(window, q_pos0=q_pos0)
+    if window is not None:
+        window = dict(window, q_pos0=q_pos0, q_pos=q_pos)
     w, out = _window(q, window)
     if o is None and w is None:
         o = torch.empty((B, n_q, n_h, c), dtype=torch.float32, device=q.device)
     lse = torch.empty((B, n_q, n_h), dtype=torch.float32, device=q.device) if lse is None else lse
-    a = hca_attend_args(q, kc, vc, m, q_pos0, scale, o, lse, n_entries, dev_status, w, sink)
+    a = hca_attend_args(q, kc, vc, m, q_pos0, scale, o, lse, n_entries, dev_status, w, sink, q_pos)
     lib = _abi.load()
     ws, nbytes = _workspace(int(lib.hca_attend_workspace_size(ctypes.byref(a))), workspace, q.device, zeroed=True)
     _abi.check(lib.hca_attend(ctypes.byref(a), ws, nbytes, _stream(stream)), "hca_attend")
     return (out, lse) if w is not None else (o, lse)
 
 
-def swa_args(q, kw, vw, kv_pos0, q_pos0, n_win, scale, o_in, lse_in, out, lse_out, dev_status=None):
+def swa_args(q, kw, vw, kv_pos0, q_pos0, n_win, scale, o_in, lse_in, out, lse_out, dev_status=None, q_pos=None,
+             kv_pos0s=None):
     B, n_q, n_h, c = q.shape
     a = _abi.SwaArgs()
     a.q, a.kw, a.vw, a.o_in, a.lse_in, a.out, a.lse_out = (_ptr(q), _ptr(kw), _ptr(vw), _ptr(o_in), _ptr(lse_in),
@@ -283,20 +305,24 @@ def swa_args(q, kw, vw, kv_pos0, q_pos0, n_win, scale, o_in, lse_in, out, lse_ou
     a.dtype = _dtype(q)
     a.out_dtype = _dtype(out)
     a.dev_status = _ptr(dev_status)
+    a.q_pos = _pos_ptr(q_pos, B * n_q, "q_pos")
+    a.kv_pos0s = _pos_ptr(kv_pos0s, B, "kv_pos0s")
     return a
 
 
-def swa_merge(q, kw, vw, *, kv_pos0: int, q_pos0: int, n_win: int, scale: float | None = None, o_in=None,
+def swa_merge(q, kw, vw, *, kv_pos0: int = 0, q_pos0: int = 0, n_win: int, scale: float | None = None, o_in=None,
               lse_in=None, out=None, out_dtype=None, lse_out=None, want_lse: bool = False, workspace=None,
-              dev_status=None, stream=None):
-    """Sliding-window branch merged with (o_in, lse_in) by log-sum-exp.  Returns out (and lse when asked)."""
+              dev_status=None, stream=None, q_pos=None, kv_pos0s=None):
+    """Sliding-window branch merged with (o_in, lse_in) by log-sum-exp.  Returns out (and lse when asked).
+    q_pos: optional int64 [B, n_q] per-query positions; kv_pos0s: optional int64 [B] per-sequence
+    absolute position of row 0 of kw / vw."""
     B, n_q, n_h, c = q.shape
     scale = 1.0 / math.sqrt(c) if scale is None else scale
     if out is None:
         out = torch.empty((B, n_q, n_h, c), dtype=out_dtype or q.dtype, device=q.device)
     if lse_out is None and want_lse:
         lse_out = torch.empty((B, n_q, n_h), dtype=torch.float32, device=q.device)
-    a = swa_args(q, kw, vw, kv_pos0, q_pos0, n_win, scale, o_in, lse_in, out, lse_out, dev_status)
+    a = swa_args(q, kw, vw, kv_pos0, q_pos0, n_win, scale, o_in, lse_in, out, lse_out, dev_status, q_pos, kv_pos0s)
     lib = _abi.load()
     ws, nbytes = _workspace(int(lib.swa_merge_workspace_size(ctypes.byref(a))), workspace, q.device)
     _abi.check(lib.swa_merge(ctypes.byref(a), ws, nbytes, _stream(stream)), "swa_merge")

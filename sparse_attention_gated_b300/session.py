@@ -3,9 +3,12 @@
 The cache of "DeepSeek-V4 Architecture From Kernels" (shivasnotes.com), section 9:
 compressed CSA entries with their FP8 indexer keys, compressed HCA entries, the raw
 rows of the blocks not yet complete (the tails), and the exact recent window.
-``DecodeSession`` owns that state for one CSA layer and one HCA layer of B sequences
-that advance together, allocated once on one device for a capacity of ``n_max``
-tokens, and runs one token per ``step``, every stage a library call:
+``DecodeSession`` owns that state for one CSA layer and one HCA layer of B sequences,
+allocated once on one device for a capacity of ``n_max`` tokens, and runs one token
+per sequence per ``step``, every stage a library call.  The sequences may sit at
+different lengths (a prefix of its own length each): they then carry per-sequence
+positions, which the calls take as device arrays (``q_pos``, and ``kv_pos0s`` for
+the windows read in place from each sequence's ring).
 
   1. the token's rows go to their ring slots (``token_slots``: a model's projections
      write there directly; ``append`` copies given rows);
@@ -93,7 +96,24 @@ class DecodeSession:
         self.out_h = torch.empty((B, 1, n_h, c), dtype=dtype, device=dev)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.ws = {}
-        self.t = 0  # position of the next token
+        self.tb = [0] * B  # position of each sequence's next token
+        self.pos = torch.zeros(B, dtype=torch.int64, device=dev)  # the same, on the device (ragged steps)
+
+    @property
+    def t(self) -> int:
+        """Position of the next token when every sequence is at the same one."""
+        if any(x != self.tb[0] for x in self.tb):
+            raise ValueError("the sequences sit at different positions: see tb")
+        return self.tb[0]
+
+    @t.setter
+    def t(self, value: int):
+        # (the device copy `pos` is used only by ragged steps, which keep it themselves)
+        self.tb = [int(value)] * self.B
+
+    @property
+    def ragged(self) -> bool:
+        return any(x != self.tb[0] for x in self.tb)
 
     # ------------------------------------------------------------ slots
     @staticmethod
@@ -143,17 +163,30 @@ class DecodeSession:
         return v
 
     def append(self, rows: dict, p: int | None = None):
-        """Put token p's rows (name -> [B, width]) into their slots: per width, one
-        gather of the rows and one scatter into the rings."""
+        """Put the next token's rows (name -> [B, width]) into their slots: per width, one
+        gather of the rows and one scatter into the rings.  p: the position, when every
+        sequence is at the same one (default: each sequence's own next position)."""
+        if p is None and self.ragged:
+            # per-sequence slots, looked up on the device from the sequences' positions
+            k = self.pos % self.period
+            bi = torch.arange(self.B, device=self.device).view(1, -1)
+            self.rings[self._ring_ids.view(-1, 1), bi, self._slot_tab[k].T] = \
+                torch.stack([rows[s] for s, _ in self._writes])
+            self.rings_I[self._ring_ids_I.view(-1, 1), bi, self._slot_tab_I[k].T] = \
+                torch.stack([rows[s] for s, _ in self._writes_I])
+            return
         p = self.t if p is None else p
         k = p % self.period
         self.rings[self._ring_ids, :, self._slot_tab[k]] = torch.stack([rows[s] for s, _ in self._writes])
         self.rings_I[self._ring_ids_I, :, self._slot_tab_I[k]] = torch.stack([rows[s] for s, _ in self._writes_I])
 
     # ------------------------------------------------------------ state from a prefix
-    def prefill(self, chunk: dict, stream=None):
+    def prefill(self, chunk: dict, stream=None, lengths=None):
         """Ingest tokens 0..n0-1 (chunk: name -> [B, n0, width]) without computing their
-        outputs: compress every complete block into the caches and fill the rings."""
+        outputs: compress every complete block into the caches and fill the rings.
+        lengths: optional per-sequence prefix lengths (<= n0): sequence b keeps only its
+        first lengths[b] tokens (entries of blocks past them are never visible to it
+        and are rewritten when its own tokens complete them)."""
         n0 = chunk["ca"].shape[1]
         if n0 > self.n_max:
             raise ValueError("prefix longer than the session's capacity")
@@ -167,11 +200,24 @@ class DecodeSession:
         if n0 >= mh:
             ops.hyb_compress(chunk["ch"], chunk["zh"], self.bias_h, mh, out=self.hca_kc, out_row0=0, dev_status=st,
                              stream=stream)
-        self.fill_rings(chunk)
+        if lengths is None:
+            self.fill_rings(chunk)
+            return
+        for b, n in enumerate(lengths):
+            if not 0 <= n <= n0:
+                raise ValueError("each prefix length must be within the chunk")
+            self._fill_rings_of(b, {k: v[b:b + 1, :n] for k, v in chunk.items()})
+        self.tb = [int(n) for n in lengths]
+        self.pos.copy_(torch.tensor(self.tb, dtype=torch.int64))
 
     def fill_rings(self, chunk: dict):
         """The ring part of prefill (no library call): after it the rings hold what
         appending tokens 0..n0-1 one by one leaves in them, and t = n0."""
+        self._fill_rings_of(None, chunk)
+        self.t = chunk["ca"].shape[1]
+
+    def _fill_rings_of(self, b, chunk: dict):
+        """Rings of sequence b (every sequence when b is None) from its tokens 0..n0-1."""
         n0 = chunk["ca"].shape[1]
         m, mh = self.m, self.m_hca
         # the rings keep what later steps read: the CSA block before the open one and the
@@ -184,6 +230,8 @@ class DecodeSession:
             if len(pos) == 0:
                 continue
             src, r = chunk[s][:, p0:n0], self.ring(s)
+            if b is not None:
+                r = r[b:b + 1]
             if s in ("kv", "kv_h"):
                 W = self.n_win
                 r.index_copy_(1, pos % W, src)
@@ -193,7 +241,6 @@ class DecodeSession:
             else:
                 r.index_copy_(1, pos % (2 * m), src)
                 r.index_copy_(1, pos % (2 * m) + 2 * m, src)
-        self.t = n0
 
     # ------------------------------------------------------------ one token
     def _sizes(self, t):
@@ -237,9 +284,11 @@ class DecodeSession:
         return rows.view(self.B, self.R, self.c), pos0
 
     def step(self, *, q, qI, qI_scale, w, q_h, stream=None):
-        """Run the layer pair for the token at position t (its rows already appended):
-        q, q_h [B, n_h, c]; qI [B, n_ih, c_I] e4m3 with qI_scale [B, n_ih]; w [B, n_ih].
-        Returns (out, out_h), [B, 1, n_h, c] each, and advances t."""
+        """Run the layer pair for each sequence's token at its position (its rows already
+        appended): q, q_h [B, n_h, c]; qI [B, n_ih, c_I] e4m3 with qI_scale [B, n_ih];
+        w [B, n_ih].  Returns (out, out_h), [B, 1, n_h, c] each, and advances the positions."""
+        if self.ragged:
+            return self._step_ragged(q=q, qI=qI, qI_scale=qI_scale, w=w, q_h=q_h, stream=stream)
         t, m, mh, st = self.t, self.m, self.m_hca, self.dev_status
         if t >= self.n_max:
             raise ValueError("session is full")
@@ -279,4 +328,53 @@ class DecodeSession:
         ops.hca_attend(q1h, self.hca_kc, self.hca_kc, m=mh, q_pos0=t, scale=self.scale, n_entries=n_vis_h,
                        lse=self.lse_h, workspace=ws, dev_status=st, stream=stream, window=win)
         self.t = t + 1
+        return self.out, self.out_h
+
+    def _step_ragged(self, *, q, qI, qI_scale, w, q_h, stream=None):
+        """step() for sequences at different positions: each sequence that completes a
+        block compresses its own entry (a call on that sequence's rows alone); the
+        indexer and both attentions run once over the batch with per-sequence positions
+        (q_pos), the windows read in place from each sequence's ring (kv_pos0s)."""
+        m, mh, st, W = self.m, self.m_hca, self.dev_status, self.n_win
+        if max(self.tb) >= self.n_max:
+            raise ValueError("session is full")
+        for b, t in enumerate(self.tb):
+            sl = slice(b, b + 1)
+            if (t + 1) % m == 0:
+                start, rows, fb, row0 = self.csa_block_view((t + 1) // m - 1, m)
+                tl = {s: self.ring(s)[sl, start:start + rows] for s in _CSA_STREAMS + _IDX_STREAMS}
+                ops.hyb_compress(tl["ca"], tl["za"], self.bias, m, cb=tl["cb"], zb=tl["zb"], overlap=True,
+                                 first_block=fb, out=self.csa_kc[sl], out_row0=row0, dev_status=st, stream=stream)
+                ops.hyb_compress(tl["kIa"], tl["zIa"], self.biasI, m, cb=tl["kIb"], zb=tl["zIb"], overlap=True,
+                                 first_block=fb, out=self.csa_kI[sl], out_scale=self.csa_kIs[sl], out_row0=row0,
+                                 dev_status=st, stream=stream)
+            if (t + 1) % mh == 0:
+                j = (t + 1) // mh - 1
+                ops.hyb_compress(self.ring("ch")[sl, :mh], self.ring("zh")[sl, :mh], self.bias_h, mh, first_block=j,
+                                 out=self.hca_kc[sl], out_row0=j, dev_status=st, stream=stream)
+        q_pos = self.pos.view(self.B, 1)
+        # row 0 of each sequence's window ring holds the first position of the period the
+        # window starts in (token p sits at rows p mod W and p mod W + W)
+        kv_pos0s = (self.pos - (W - 1)).clamp_(min=0).div_(W, rounding_mode="floor").mul_(W)
+        q1, q1h = q.unsqueeze(1), q_h.unsqueeze(1)
+        qI1, qIs1, w1 = qI.unsqueeze(1), qI_scale.unsqueeze(1), w.unsqueeze(1)
+        a = ops.index_args(qI1, w1, self.csa_kI, m, self.k, 0, qIs1, self.csa_kIs, self.idx, None, q_pos=q_pos)
+        ws = self._workspace("index_r", ops.csa_index_topk_workspace_size(a))
+        ops.csa_index_topk(qI1, w1, self.csa_kI, m=m, k=self.k, q_pos=q_pos, qI_scale=qIs1, kI_scale=self.csa_kIs,
+                           idx=self.idx, workspace=ws, dev_status=st, stream=stream)
+        kw = self.ring("kv")
+        win = dict(kw=kw, q_pos=q_pos, kv_pos0s=kv_pos0s, n_win=W, out=self.out)
+        a = ops.csa_attend_args(q1, self.csa_kc, self.csa_kc, self.idx, self.scale, None, self.lse,
+                                window=ops.window_args(**win))
+        ws = self._workspace("csa_r", int(ops._abi.load().csa_attend_workspace_size(a)))
+        ops.csa_attend(q1, self.csa_kc, self.csa_kc, self.idx, scale=self.scale, lse=self.lse, workspace=ws,
+                       dev_status=st, stream=stream, window=win)
+        win = dict(kw=self.ring("kv_h"), kv_pos0s=kv_pos0s, n_win=W, out=self.out_h)
+        a = ops.hca_attend_args(q1h, self.hca_kc, self.hca_kc, mh, 0, self.scale, None, self.lse_h,
+                                window=ops.window_args(**win, q_pos=q_pos), q_pos=q_pos)
+        ws = self._workspace("hca_r", int(ops._abi.load().hca_attend_workspace_size(a)))
+        ops.hca_attend(q1h, self.hca_kc, self.hca_kc, m=mh, q_pos=q_pos, scale=self.scale, lse=self.lse_h,
+                       workspace=ws, dev_status=st, stream=stream, window=win)
+        self.tb = [t + 1 for t in self.tb]
+        self.pos.add_(1)
         return self.out, self.out_h

@@ -229,3 +229,41 @@ def test_fused_window_arguments_are_validated_before_any_launch(lib):
     h.window = ctypes.cast(ctypes.pointer(win), ctypes.c_void_p)
     assert lib.hca_attend(ctypes.byref(h), None, 0, None) == 1  # the window's query is not the call's
     assert "q_pos0" in lib.hyb_last_error().decode()
+
+
+def test_per_query_positions_are_checked_where_the_host_can(lib):
+    """Per-query positions live in device memory: the host checks their pointers
+    (8-byte alignment) and that a fused HCA window uses the call's own positions;
+    the positions themselves are range-checked by the kernels."""
+    a = _abi.IndexArgs()
+    a.qI = a.w = a.kI = a.idx = FAKE
+    a.batch, a.n_q, a.n_entries, a.n_ih, a.c_I, a.m, a.k, a.dtype = 2, 1, 1000, 8, 64, 4, 16, _abi.HYB_F32
+    a.q_pos0 = 10 ** 9  # ignored with per-query positions (would see more entries than exist)
+    a.q_pos = FAKE + 4
+    assert lib.csa_index_topk(ctypes.byref(a), None, 0, None) == 1
+    assert "q_pos" in lib.hyb_last_error().decode()
+    a.q_pos = FAKE
+    # sized for every row seeing all 1000 entries
+    assert lib.csa_index_topk_workspace_size(ctypes.byref(a)) >= 2 * 1000 * 4
+    assert lib.csa_index_topk(ctypes.byref(a), None, 0, None) == 3  # HYB_ERR_WORKSPACE: it got past validation
+    h = _abi.HcaAttendArgs()
+    h.q = h.kc = h.vc = h.lse = FAKE
+    h.batch, h.n_q, h.n_h, h.c, h.n_entries, h.m, h.q_pos0, h.dtype = 1, 1, 64, 512, 100, 16, 0, _abi.HYB_BF16
+    h.q_pos = FAKE + 8
+    win = _abi.Window()
+    win.kw, win.out, win.out_dtype, win.n_kv, win.kv_pos0, win.n_win = FAKE, FAKE, _abi.HYB_BF16, 128, 0, 128
+    h.window = ctypes.cast(ctypes.pointer(win), ctypes.c_void_p)
+    assert lib.hca_attend(ctypes.byref(h), None, 0, None) == 1  # the window has no per-query positions
+    win.q_pos = FAKE + 8
+    win.kv_pos0s = FAKE + 4
+    assert lib.hca_attend(ctypes.byref(h), None, 0, None) == 1  # misaligned kv_pos0s
+    win.kv_pos0s = FAKE
+    assert lib.hca_attend(ctypes.byref(h), None, 0, None) == 3  # past validation: the workspace is missing
+    s = _abi.SwaArgs()
+    s.q = s.kw = s.vw = s.out = FAKE
+    s.batch, s.n_q, s.n_h, s.c, s.n_kv, s.n_win, s.dtype, s.out_dtype = 1, 1, 64, 512, 10, 128, 1, 1
+    s.q_pos0, s.kv_pos0 = 5000, 0  # rows outside the buffer: rejected as numbers ...
+    assert lib.swa_merge(ctypes.byref(s), None, 0, None) == 1
+    s.q_pos = FAKE  # ... not checkable as device-side positions (the kernel clips and reports)
+    s.kv_pos0s = FAKE + 2
+    assert lib.swa_merge(ctypes.byref(s), None, 0, None) == 1

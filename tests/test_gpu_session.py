@@ -95,3 +95,51 @@ def test_decode_session_matches_the_oracle_token_by_token():
         o, l = oracle.hca_attend(q1(h["q_h"]), hkc, hkc, m=MH, q_pos0=t, scale=scale)
         ref_out, _ = oracle.swa_merge(q1(h["q_h"]), hist["kv_h"], hist["kv_h"], 0, t, W, scale, o, l)
         assert _close(to_np(out_h), ref_out), f"t={t}: HCA layer output"
+
+
+def test_decode_session_with_sequences_at_different_lengths():
+    """Three sequences with prefixes of 301, 250 and 2 tokens (the last one before its
+    first complete block) decode 40 tokens each: blocks complete at different steps,
+    the calls take per-sequence positions, and every sequence must match the oracle
+    over its own history after every token."""
+    h, bias, biasI, bias_h = _history(72)
+    lengths = [301, 250, 2]
+    Bq = len(lengths)
+    h3, _, _, _ = _history(73)  # the history has B = 2 sequences: a third from another seed
+    hh = {k: torch.cat([h[k], h3[k][:1]]) for k in h}
+    s = DecodeSession(batch=Bq, n_max=512, n_h=NH, c=C, m=M, m_hca=MH, k=K, n_ih=NIH, c_I=CI, n_win=W, bias=bias,
+                      biasI=biasI, bias_h=bias_h, device=DEV)
+    n0 = max(lengths)
+    s.prefill({k: hh[k][:, :n0].contiguous().to(DEV) for k in ROW_STREAMS}, lengths=lengths)
+    scale = 1.0 / math.sqrt(C)
+    for step in range(40):
+        tb = list(s.tb)
+        rows = {k: torch.stack([hh[k][b, tb[b]] for b in range(Bq)]).to(DEV) for k in ROW_STREAMS}
+        s.append(rows)
+        at = lambda k: torch.stack([hh[k][b, tb[b]] for b in range(Bq)]).to(DEV)
+        out, out_h = s.step(q=at("q"), qI=at("qI"), qI_scale=at("qI_scale"), w=at("w"), q_h=at("q_h"))
+        torch.cuda.synchronize()
+        assert s.dev_status.item() == 0, f"step {step}: device status {s.dev_status.item()}"
+        assert s.tb == [t + 1 for t in tb]
+        for b, t in enumerate(tb):
+            sl = slice(b, b + 1)
+            nv, nvh = (t + 1) // M, (t + 1) // MH
+            hist = {k: hh[k][sl, :t + 1] for k in ROW_STREAMS}
+            kc = s.csa_kc[sl, :nv].cpu()
+            if nv:
+                ref = oracle.compress(hist["ca"], hist["za"], bias, M, cb=hist["cb"], zb=hist["zb"], overlap=True)
+                assert _close(to_np(kc), ref), f"step {step}, sequence {b}: CSA entries"
+            kI, kIs = s.csa_kI[sl, :nv].cpu(), s.csa_kIs[sl, :nv].cpu()
+            q1 = lambda x: x[sl, t:t + 1]
+            if nv:
+                sc = oracle.index_scores(q1(hh["qI"]), q1(hh["w"]), kI, m=M, q_pos0=t, qI_scale=q1(hh["qI_scale"]),
+                                         kI_scale=kIs)
+                check_topk_row(s.idx[b, 0].cpu().numpy(), sc[0, 0], nv, K)
+            idx = s.idx[sl].cpu().numpy()
+            o, l = oracle.csa_attend(q1(hh["q"]), kc, kc, idx, scale)
+            ref_out, _ = oracle.swa_merge(q1(hh["q"]), hist["kv"], hist["kv"], 0, t, W, scale, o, l)
+            assert _close(to_np(out[sl]), ref_out), f"step {step}, sequence {b}: CSA layer output"
+            hkc = s.hca_kc[sl, :nvh].cpu()
+            o, l = oracle.hca_attend(q1(hh["q_h"]), hkc, hkc, m=MH, q_pos0=t, scale=scale)
+            ref_out, _ = oracle.swa_merge(q1(hh["q_h"]), hist["kv_h"], hist["kv_h"], 0, t, W, scale, o, l)
+            assert _close(to_np(out_h[sl]), ref_out), f"step {step}, sequence {b}: HCA layer output"

@@ -69,3 +69,43 @@ def test_noalloc_indexer_matches_the_ordinary_entry_point_on_two_calls_in_a_row(
         assert torch.equal(got_idx, want_idx)
         assert torch.equal(got_sc, want_sc)
         assert (got_idx >= 0).all() and (got_idx < N).all()
+
+
+def test_noalloc_indexer_recovers_after_a_timeout_through_its_reset():
+    """A call whose cross-CTA waits ran out (made to, by a zero wait limit) leaves the
+    counters in the library's scratch non-zero; csa_index_topk_noalloc_reset clears
+    them, after which the entry point again matches the ordinary one exactly."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from sparse_attention_gated_b300 import _abi, ops
+
+    lib = _abi.load()
+    g = torch.Generator()
+    g.manual_seed(63)
+    m, k, B, N = 4, 512, 2, 60000
+    qI = torch.randn((B, 1, 8, 64), generator=g).to(DEV)
+    kI = torch.randn((B, N, 64), generator=g).to(DEV)
+    w = torch.rand((B, 1, 8), generator=g).to(DEV)
+    q_pos0 = m * N - 1
+    want = ops.csa_index_topk(qI, w, kI, m=m, k=k, q_pos0=q_pos0)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+    def call():
+        idx = torch.full((B, 1, k), -7, dtype=torch.int32, device=DEV)
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        a = ops.index_args(qI, w, kI, m, k, q_pos0, idx=idx, dev_status=st)
+        _abi.check(lib.csa_index_topk_noalloc(ctypes.byref(a), stream), "csa_index_topk_noalloc")
+        torch.cuda.synchronize()
+        return idx, st.item()
+
+    prev = int(lib.hyb_set_grid_wait_limit(0))
+    try:
+        _, status = call()
+    finally:
+        lib.hyb_set_grid_wait_limit(prev)
+    assert status & 0x2, f"status {status:#x}"
+    _abi.check(lib.csa_index_topk_noalloc_reset(stream), "csa_index_topk_noalloc_reset")
+    for _ in range(2):
+        got, status = call()
+        assert status == 0
+        assert torch.equal(got, want)
