@@ -124,13 +124,16 @@ def topk_kernel_model(w):
     return dict(bytes=w.batch * (pairs * 4 + w.n_ctx * w.k * 4), flops=0)
 
 
-# the kernels of each timed stage, for the per-kernel roofline table
-STAGE_KERNELS = {
-    "csa_compress": "compress_kernel x2 (CSA entry bf16 + indexer key e4m3)",
-    "csa_attend": "attend_tc_kernel<0> (csa_attend, window fused)",
-    "hca_compress": "compress_kernel (HCA entry)",
-    "hca_attend": "attend_tc_kernel<1> (hca_attend, window fused)",
-}
+def stage_kernels(w):
+    """The kernel of each timed stage, for the per-kernel roofline table (decode launches with
+    128 heads run the 128-heads-per-CTA attention kernel, the others the 64-head one)."""
+    att = "attend_h128_kernel" if (w.decode and w.n_h % 128 == 0) else "attend_tc_kernel"
+    return {
+        "csa_compress": "compress_kernel x2 (CSA entry bf16 + indexer key e4m3)",
+        "csa_attend": f"{att}<0> (csa_attend, window fused)",
+        "hca_compress": "compress_kernel (HCA entry)",
+        "hca_attend": f"{att}<1> (hca_attend, window fused)",
+    }
 
 
 def kernel_roofline(name, model, ms, peaks, peak_kind, traffic=None):
@@ -414,7 +417,7 @@ def run_ours(args, w):
         kern["index_scores"] = ("index_tc_kernel (csa_index_topk scoring)", scoring_kernel_model(w), scoring_ms)
         kern["topk"] = ("topk_grid_kernel (csa_index_topk selection)", topk_kernel_model(w),
                         stage_ms["csa_index_topk"] - scoring_ms)
-    for s_name, label in STAGE_KERNELS.items():
+    for s_name, label in stage_kernels(w).items():
         if s_name in stage_ms:
             kern[s_name] = (label, model[s_name], stage_ms[s_name])
     kernels = {k: kernel_roofline(lbl, m_, ms_, peaks, peak_kind, KERNEL_NCU_TRAFFIC.get((w.name, k)))

@@ -336,12 +336,17 @@ static hyb_status validate_attend_common(const char* name, int64_t batch, int64_
 // follows them.  A standalone window merge has no join.
 static size_t join_region(const hyb::AttendJob& j) { return j.mode == 2 ? 0 : hyb::kJoinRegionBytes; }
 
+// The 128-head kernel serves its shapes when it is enabled (HYB_ATTEND_H128, on by default).
+static bool use_h128(const hyb::AttendJob& j) { return hyb::attend_h128_enabled() && hyb::attend_h128_supported(j); }
+
 static size_t attend_workspace(const hyb::AttendJob& j) {
+  if (use_h128(j)) return hyb::attend_h128_workspace_bytes(j);
   return hyb::attend_tc_supported(j) ? hyb::attend_tc_workspace_bytes(j)
                                      : join_region(j) + hyb::attend_cc_workspace_bytes(j);
 }
 
 static cudaError_t launch_attend(const hyb::AttendJob& j, void* ws, cudaStream_t s) {
+  if (use_h128(j)) return hyb::launch_attend_h128(j, ws, s);
   if (hyb::attend_tc_supported(j)) return hyb::launch_attend_tc(j, ws, s);
   return hyb::launch_attend_cc(j, static_cast<char*>(ws) + join_region(j), s);
 }
@@ -383,6 +388,7 @@ static size_t fallback_io_bytes(const hyb::AttendJob& c) {
 
 static size_t attend_window_workspace(const hyb::AttendJob& c, const hyb_window* w) {
   const hyb::AttendJob f = fused_job(c, w);
+  if (use_h128(f)) return hyb::attend_h128_workspace_bytes(f);
   if (hyb::attend_tc_supported(f)) return hyb::attend_tc_workspace_bytes(f);
   const hyb::AttendJob m = window_merge_job(c, w, nullptr, nullptr, nullptr);
   return round_up(std::max(attend_workspace(c), hyb::kJoinRegionBytes + attend_workspace(m)), 256) +
@@ -422,6 +428,7 @@ static hyb_status run_attend_window(const char* name, hyb::AttendJob c, const hy
   if (!aligned(workspace, 256)) return fail(HYB_ERR_WORKSPACE, "%s: workspace must be 256-byte aligned", name);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const hyb::AttendJob f = fused_job(c, w);
+  if (use_h128(f)) return cuda_status(hyb::launch_attend_h128(f, workspace, s), name);
   if (hyb::attend_tc_supported(f)) return cuda_status(hyb::launch_attend_tc(f, workspace, s), name);
   // two steps: the compressed branch into the workspace (after the kernels' own
   // scratch, which keeps the join counters first), then the window merge

@@ -96,6 +96,13 @@ bool attend_tc_supported(const AttendJob& j);
 int attend_tc_splits(const AttendJob& j);
 size_t attend_tc_workspace_bytes(const AttendJob& j);
 cudaError_t launch_attend_tc(const AttendJob& j, void* ws, cudaStream_t s);
+// attend_h128.cu (tcgen05 MQA attention with 128 heads per CTA: bf16, c = 512, key = value,
+// lists and visible ranges of decode-shaped launches, window fused)
+bool attend_h128_enabled();
+bool attend_h128_supported(const AttendJob& j);
+int attend_h128_splits(const AttendJob& j);
+size_t attend_h128_workspace_bytes(const AttendJob& j);
+cudaError_t launch_attend_h128(const AttendJob& j, void* ws, cudaStream_t s);
 int attend_cc_splits(const AttendJob& j);
 size_t attend_cc_workspace_bytes(const AttendJob& j);
 cudaError_t launch_attend_cc(const AttendJob& j, void* ws, cudaStream_t s);

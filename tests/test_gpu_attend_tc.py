@@ -306,3 +306,106 @@ def test_join_counters_reset_across_calls_of_different_shapes():
         assert_out_close(to_np(out), ro2)
         assert max_abs(to_np(lse2), rl2) <= TOL_BF16
     assert int(ws[:1024].count_nonzero()) == 0
+
+
+# ---------------------------------------------------------------- 128 heads per CTA
+# Decode-shaped launches with 128 heads and key = value run the kernel that keeps all 128
+# heads of a query in one CTA (each CTA one half of the output dims).  Its own cases: the
+# lazy softmax reference moving mid-list (O rescaled in tensor memory), gathered lists with
+# padding runs, repeats and empty lists, splits with fewer tiles than splits, a ragged last
+# tile read by gather, and a fused window shorter than a tile.
+
+
+@pytest.mark.parametrize("order", ["rising", "spike", "falling"])
+@pytest.mark.parametrize("mode", ["csa", "hca"])
+def test_h128_softmax_reference_moves_late(order, mode):
+    g = _gen(16)
+    B, n_h, N, c = 2, 128, 1500, 512
+    q = _randn(g, (B, 1, n_h, c))
+    base = torch.randn((B, N, c), generator=g) / math.sqrt(c)
+    if order == "rising":
+        gain = torch.linspace(0.2, 12.0, N)
+    elif order == "falling":
+        gain = torch.linspace(12.0, 0.2, N)
+    else:
+        gain = torch.full((N,), 1.0)
+        gain[900:905] = 14.0
+    kc = (base * gain[None, :, None]).to(torch.bfloat16)
+    scale = 1 / math.sqrt(c) * 8
+    st = _status()
+    if mode == "csa":
+        idx = torch.arange(N, dtype=torch.int32).expand(B, 1, N).contiguous()
+        o, lse = _ops().csa_attend(q.to(DEV), kc.to(DEV), kc.to(DEV), idx.to(DEV), scale=scale, dev_status=st)
+        ro, rl = oracle.csa_attend(q, kc, kc, idx, scale)
+    else:
+        o, lse = _ops().hca_attend(q.to(DEV), kc.to(DEV), kc.to(DEV), m=4, q_pos0=4 * N - 1, scale=scale,
+                                   dev_status=st)
+        ro, rl = oracle.hca_attend(q, kc, kc, m=4, q_pos0=4 * N - 1, scale=scale)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert_out_close(to_np(o), ro)
+    assert np.max(np.abs(to_np(lse) - rl) / np.maximum(1.0, np.abs(rl))) <= 2e-3
+
+
+def test_h128_csa_padding_runs_duplicates_and_empty_lists():
+    g = _gen(17)
+    B, n_h, N, k, c = 3, 128, 5000, 700, 512
+    q = _randn(g, (B, 1, n_h, c))
+    kc = _randn(g, (B, N, c), 2 / math.sqrt(c))
+    idx = torch.randint(0, N, (B, 1, k), generator=g).int()
+    idx[0, 0, :300] = -1          # the first tiles and more: nothing
+    idx[1, 0, 128:512] = -1       # whole tiles in the middle
+    idx[1, 0, 10:20] = idx[1, 0, 5]  # repeats
+    idx[2, 0, :] = -1             # empty list
+    scale = 1 / math.sqrt(c)
+    o, lse = _csa(q, kc, kc, idx, scale)
+    ro, rl = oracle.csa_attend(q, kc, kc, idx, scale)
+    assert_out_close(o, ro)
+    assert max_abs(lse, rl) <= TOL_BF16
+    assert np.all(o[2, 0] == 0) and np.all(np.isneginf(lse[2, 0]))
+
+
+@pytest.mark.parametrize("N,q_pos0,m", [
+    (100, 4 * 70 - 1, 4),    # 70 visible: two tiles, the second ragged (gathered), many empty splits
+    (100, 2, 4),             # nothing visible
+    (64, 4 * 64 - 1, 4),     # exactly one whole tile
+    (9000, 9000 * 4 - 1, 4), # long list: several tiles per split
+])
+def test_h128_hca_split_edges(N, q_pos0, m):
+    g = _gen(18)
+    B, n_h, c = 2, 128, 512
+    q = _randn(g, (B, 1, n_h, c))
+    kc = _randn(g, (B, N, c))  # unit-scale rows: outputs of order 0.1
+    vis = min(N, (q_pos0 + 1) // m)
+    kc[:, vis:] = float("nan")  # rows that must not be read
+    scale = 1 / math.sqrt(c)
+    st = _status()
+    o, lse = _ops().hca_attend(q.to(DEV), kc.to(DEV), kc.to(DEV), m=m, q_pos0=q_pos0, scale=scale, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    ro, rl = oracle.hca_attend(q, kc[:, :max(vis, 1)], kc[:, :max(vis, 1)], m=m, q_pos0=q_pos0, scale=scale)
+    if vis == 0:
+        assert np.all(to_np(o) == 0) and np.all(np.isneginf(to_np(lse)))
+    else:
+        assert_out_close(to_np(o), ro)
+        assert max_abs(to_np(lse), rl) <= TOL_BF16
+
+
+@pytest.mark.parametrize("q_pos0,n_win", [(30, 128), (5000, 100), (200, 128)])
+def test_h128_fused_window_shorter_than_a_tile_or_ragged(q_pos0, n_win):
+    g = _gen(19)
+    B, n_h, N, m, c = 2, 128, 2000, 4, 512
+    q = _randn(g, (B, 1, n_h, c), 2.0)
+    kc = _randn(g, (B, N, c))
+    n_kv = q_pos0 + 1
+    kw = _randn(g, (B, n_kv, c))
+    scale = 1 / math.sqrt(c)
+    st = _status()
+    out, lu = _ops().hca_attend(q.to(DEV), kc.to(DEV), kc.to(DEV), m=m, q_pos0=q_pos0, scale=scale, dev_status=st,
+                                window=dict(kw=kw.to(DEV), kv_pos0=0, n_win=n_win))
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    ro, rl = oracle.hca_attend(q, kc, kc, m=m, q_pos0=q_pos0, scale=scale)
+    rw, rwl = oracle.swa_merge(q, kw, kw, 0, q_pos0, n_win, scale, ro, rl)
+    assert_out_close(to_np(out), rw)
+    assert max_abs(to_np(lu), rwl) <= TOL_BF16
