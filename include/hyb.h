@@ -442,6 +442,43 @@ typedef struct hyb_norm_rope_args {
 HYB_API hyb_status hyb_rmsnorm_rope(const hyb_norm_rope_args* a, void* stream);
 
 /* ------------------------------------------------------------------------
+ * hyb_grouped_out_proj -- grouped output projection ([HA] section V.3, core
+ * attention and grouped output: the n_h heads are split into g groups of
+ * n_h/g consecutive heads, each group's (n_h/g)*c values are projected by a
+ * matrix of its own, and the g results are concatenated; [MA] model
+ * configurations table: g / d_g = 16 / 1024 (Pro), 8 / 1024 (Flash)).
+ *
+ *   out[r][j*d_g + e] = sum_k w[j][e][k] * o[r][j*(n_h/g)*c + k]
+ *
+ * o [rows][n_h][c] and w [g][d_g][(n_h/g)*c] are bf16 (dtype HYB_BF16); out
+ * [rows][g*d_g] is F32 or BF16 (out_dtype); float32 accumulation on the
+ * tensor cores.  g must divide n_h, d_g must be a multiple of 128 and
+ * (n_h/g)*c a multiple of 64.  With g = 1 the call is a plain projection of
+ * all n_h*c values (e.g. the concatenated g*d_g features mapped to the model
+ * dimension: pass them as o [rows][1][g*d_g]).  out_row_stride: elements from
+ * one output row to the next (0 = g*d_g; otherwise >= g*d_g), so that two
+ * calls can fill the two halves of one output row (the projection of a
+ * concatenation whose groups do not straddle it).  No workspace.  Pointers
+ * 16-byte aligned.
+ * ------------------------------------------------------------------------ */
+typedef struct hyb_gproj_args {
+  const void* o;
+  const void* w;
+  void* out;
+  int64_t rows;
+  int64_t n_h;
+  int64_t c;
+  int64_t g;
+  int64_t d_g;
+  int32_t dtype;     /* hyb_dtype of o and w: HYB_BF16 */
+  int32_t out_dtype; /* hyb_dtype: HYB_F32 or HYB_BF16 */
+  int32_t* dev_status;
+  int64_t out_row_stride; /* 0 = g*d_g */
+} hyb_gproj_args;
+
+HYB_API hyb_status hyb_grouped_out_proj(const hyb_gproj_args* a, void* stream);
+
+/* ------------------------------------------------------------------------
  * hyb_set_grid_wait_limit -- bound of the device-side waits that span CTAs.
  *
  * Two kernels wait on other CTAs of their grid: the top-k grid plan of

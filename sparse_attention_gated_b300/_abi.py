@@ -58,6 +58,11 @@ class NormRopeArgs(ctypes.Structure):
                 ("rows_per_pos", _i64), ("rope_dims", _i64), ("theta", ctypes.c_double)]
 
 
+class GprojArgs(ctypes.Structure):
+    _fields_ = [("o", _p), ("w", _p), ("out", _p), ("rows", _i64), ("n_h", _i64), ("c", _i64), ("g", _i64),
+                ("d_g", _i64), ("dtype", _i32), ("out_dtype", _i32), ("dev_status", _p), ("out_row_stride", _i64)]
+
+
 class SwaArgs(ctypes.Structure):
     _fields_ = [("q", _p), ("kw", _p), ("vw", _p), ("o_in", _p), ("lse_in", _p), ("out", _p), ("lse_out", _p),
                 ("batch", _i64), ("n_q", _i64), ("n_h", _i64), ("c", _i64), ("n_kv", _i64), ("kv_pos0", _i64),
@@ -83,6 +88,7 @@ SIGNATURES = {
     "swa_merge_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(SwaArgs)]),
     "swa_merge": (ctypes.c_int, [ctypes.POINTER(SwaArgs), _p, ctypes.c_size_t, _p]),
     "hyb_rmsnorm_rope": (ctypes.c_int, [ctypes.POINTER(NormRopeArgs), _p]),
+    "hyb_grouped_out_proj": (ctypes.c_int, [ctypes.POINTER(GprojArgs), _p]),
     "hyb_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "hyb_last_error": (ctypes.c_char_p, []),
     "hyb_version": (_i32, []),

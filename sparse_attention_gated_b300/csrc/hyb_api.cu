@@ -538,6 +538,34 @@ hyb_status swa_merge(const hyb_swa_args* a, void* workspace, size_t ws_bytes, vo
   return run_attend("swa_merge", swa_job(a), workspace, ws_bytes, stream);
 }
 
+// ------------------------------------------------- grouped output projection
+
+hyb_status hyb_grouped_out_proj(const hyb_gproj_args* a, void* stream) {
+  if (!a) return fail(HYB_ERR_INVALID_ARG, "hyb_grouped_out_proj: args is NULL");
+  if (a->rows < 0 || a->n_h < 1 || a->c < 1 || a->g < 1 || a->d_g < 1 || a->out_row_stride < 0)
+    return fail(HYB_ERR_INVALID_ARG, "hyb_grouped_out_proj: negative size or n_h, c, g, d_g < 1");
+  if (a->n_h % a->g != 0) return fail(HYB_ERR_INVALID_ARG, "hyb_grouped_out_proj: g must divide n_h");
+  if (a->dtype != HYB_BF16) return fail(HYB_ERR_UNSUPPORTED, "hyb_grouped_out_proj: o and w must be BF16");
+  if (a->out_dtype != HYB_F32 && a->out_dtype != HYB_BF16)
+    return fail(HYB_ERR_INVALID_ARG, "hyb_grouped_out_proj: out_dtype must be F32 or BF16");
+  if (!hyb::out_proj_shape_supported(a->n_h, a->c, a->g, a->d_g))
+    return fail(HYB_ERR_UNSUPPORTED, "hyb_grouped_out_proj: d_g = %lld (a multiple of 128 needed) / group inputs %lld "
+                "(a multiple of 64 needed)", (long long)a->d_g, (long long)(a->n_h / a->g * a->c));
+  if (a->rows == 0) return ok();
+  if (!a->o || !a->w || !a->out) return fail(HYB_ERR_INVALID_ARG, "hyb_grouped_out_proj: NULL o/w/out");
+  if (!aligned(a->o, 16) || !aligned(a->w, 16) || !aligned(a->out, 16))
+    return fail(HYB_ERR_INVALID_ARG, "hyb_grouped_out_proj: pointers must be 16-byte aligned");
+  if (a->rows >= (int64_t(1) << 31) || a->g * a->d_g >= (int64_t(1) << 31))
+    return fail(HYB_ERR_UNSUPPORTED, "hyb_grouped_out_proj: too many rows or features");
+  if (a->out_row_stride != 0 && a->out_row_stride < a->g * a->d_g)
+    return fail(HYB_ERR_INVALID_ARG, "hyb_grouped_out_proj: out_row_stride %lld < g*d_g = %lld",
+                (long long)a->out_row_stride, (long long)(a->g * a->d_g));
+  const int64_t stride = a->out_row_stride ? a->out_row_stride : a->g * a->d_g;
+  return cuda_status(hyb::launch_out_proj(a->o, a->w, a->out, a->out_dtype == HYB_BF16, a->rows, a->n_h, a->c, a->g,
+                                          a->d_g, stride, a->dev_status, static_cast<cudaStream_t>(stream)),
+                     "hyb_grouped_out_proj");
+}
+
 // ---------------------------------------------------------- RMSNorm + RoPE
 
 hyb_status hyb_rmsnorm_rope(const hyb_norm_rope_args* a, void* stream) {

@@ -33,6 +33,11 @@ cudaError_t launch_compress(const hyb_compress_args* a, int64_t n_out, cudaStrea
 // norm_rope.cu
 cudaError_t launch_norm_rope(const hyb_norm_rope_args* a, cudaStream_t s);
 
+// out_proj.cu (tcgen05 grouped output projection: bf16 in, F32 or BF16 out)
+bool out_proj_shape_supported(int64_t n_h, int64_t c, int64_t g, int64_t d_g);
+cudaError_t launch_out_proj(const void* o, const void* w, void* out, int out_bf16, int64_t rows, int64_t n_h, int64_t c,
+                            int64_t g, int64_t d_g, int64_t out_stride, int32_t* dev_status, cudaStream_t s);
+
 // sink.cu: rows = batch * n_q * n_h rows of c values (out_dtype F32 or BF16) and their lse
 cudaError_t launch_sink(void* out, int32_t out_dtype, float* lse, const float* sink, int64_t rows, int64_t n_h,
                         int64_t c, cudaStream_t s);

@@ -350,3 +350,37 @@ def rmsnorm_rope(x, *, gamma=None, eps: float = 1e-6, pos=None, rows_per_pos: in
     a.rope_dims, a.theta = (rope_dims if pos is not None else 0), theta
     _abi.check(_abi.load().hyb_rmsnorm_rope(ctypes.byref(a), _stream(stream)), "hyb_rmsnorm_rope")
     return x
+
+
+# ---------------------------------------------------- grouped output projection
+
+
+def grouped_out_proj(o, w, *, out=None, out_dtype=torch.float32, dev_status=None, stream=None):
+    """Grouped output projection: o [..., n_h, c] bf16 (the heads of each row), w [g, d_g,
+    (n_h/g)*c] bf16.  Returns out [..., g*d_g] (out_dtype float32 or bf16): group j of n_h/g
+    consecutive heads projected by w[j], the g results concatenated.  out may be a column
+    slice of a wider [rows, F] buffer (rows contiguous, row stride F): the call then fills
+    its g*d_g columns."""
+    n_h, c = o.shape[-2], o.shape[-1]
+    g, d_g, k = w.shape
+    if k * g != n_h * c:
+        raise ValueError("w must be [g, d_g, (n_h/g)*c]")
+    lead = o.shape[:-2]
+    rows = math.prod(lead) if lead else 1
+    if out is None:
+        out = torch.empty(tuple(lead) + (g * d_g,), dtype=out_dtype, device=o.device)
+    if out.shape[-1] != g * d_g or out.stride(-1) != 1:
+        raise ValueError("out must end in g*d_g contiguous features")
+    a = _abi.GprojArgs()
+    a.o, a.w = _ptr(o), _ptr(w)
+    if not out.is_cuda:
+        raise ValueError("tensors passed to the hybrid-attention library must be CUDA tensors")
+    a.out = ctypes.c_void_p(out.data_ptr())
+    a.out_row_stride = out.stride(-2) if out.dim() >= 2 and rows > 1 else 0
+    a.rows, a.n_h, a.c, a.g, a.d_g = rows, n_h, c, g, d_g
+    a.dtype, a.out_dtype = _dtype(o), _dtype(out)
+    if _dtype(w) != a.dtype:
+        raise ValueError("o and w must have the same dtype")
+    a.dev_status = _ptr(dev_status)
+    _abi.check(_abi.load().hyb_grouped_out_proj(ctypes.byref(a), _stream(stream)), "hyb_grouped_out_proj")
+    return out

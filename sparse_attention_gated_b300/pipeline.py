@@ -11,10 +11,25 @@ once, with torch) and runs the stages of the forward in order on one stream:
              compress the completed block(s), attend every visible entry,
              merge the sliding window.
 
+  Parallel    ("DeepSeek-V4 hybrid attention" (trishampatil.com) section IV: the
+             attention sublayer runs the two compressed mechanisms side by side
+             and concatenates their outputs): CSA and HCA on the same queries
+             and window; the concatenation is the 2 n_h heads [CSA | HCA].
+  SWA        (the Flash configuration's first layers, "Mastering DeepSeek-V4
+             Architecture" model configurations table): the sliding window
+             alone (swa_merge with no compressed branch).
+
 Decode workloads keep the compressed caches resident (state) and write the
 entry of the block that completes at this step into its cache slot; the
 query is the last context token.  Prefill / forward workloads compress the
 whole chunk and treat every position as a query.
+
+Optional grouped output projection (same page, section V.3): proj = dict(w=...)
+for a single attention output ([g][d_g][(n_h/g)*c] bf16, applied to `out`; a
+hybrid step also takes w_h for `out_h`), or, for the parallel step, one matrix set
+over the 2 n_h concatenated heads, whose first g/2 groups read the CSA heads and
+the rest the HCA heads: the two halves of each projected row are written by one
+grouped call each, so the concatenation is never copied.
 """
 from __future__ import annotations
 
@@ -25,7 +40,9 @@ from .workloads import Workload
 
 
 class HybridStep:
-    def __init__(self, w: Workload, inputs: dict, fuse_window: bool = True):
+    proj = None  # the optional grouped output projection's matrices
+
+    def __init__(self, w: Workload, inputs: dict, fuse_window: bool = True, proj: dict | None = None):
         """fuse_window: the sliding-window merge rides on the attention call (csa_attend /
         hca_attend with a window: one launch where the whole launch fits the GPU at once;
         `out` and `lse` then hold the merged result and `o` is not written); False runs
@@ -38,9 +55,12 @@ class HybridStep:
         B, c, n_h = w.batch, w.c, w.n_h
         n_q = w.n_q
         self.buf = {}
-        kinds_csa = w.kind in ("forward", "csa_prefill", "csa_decode", "hybrid_decode")
-        kinds_hca = w.kind in ("forward", "hca_decode", "hybrid_decode")
+        kinds_csa = w.kind in ("forward", "csa_prefill", "csa_decode", "hybrid_decode", "parallel_decode")
+        kinds_hca = w.kind in ("forward", "hca_decode", "hybrid_decode", "parallel_decode")
         self.has_csa, self.has_hca = kinds_csa, kinds_hca
+        self.swa_only = w.kind == "swa_decode"
+        if self.swa_only:
+            self.buf["out"] = torch.empty((B, n_q, n_h, c), dtype=w.dtype, device=dev)
         f32 = torch.float32
         if kinds_csa:
             if not w.decode:
@@ -59,6 +79,15 @@ class HybridStep:
             self.buf["o_h"] = torch.empty((B, n_q, n_h, c), dtype=f32, device=dev)
             self.buf["lse_h"] = torch.empty((B, n_q, n_h), dtype=f32, device=dev)
             self.buf["out_h"] = torch.empty((B, n_q, n_h, c), dtype=w.dtype, device=dev)
+        self.proj = proj
+        if proj is not None:
+            g, d_g = proj["w"].shape[:2]
+            if w.kind == "parallel_decode" and (g % 2 or proj["w"].shape[2] * g != 2 * n_h * c):
+                raise ValueError("the parallel step's projection spans the 2 n_h concatenated heads")
+            self.buf["proj"] = torch.empty((B, n_q, g * d_g), dtype=torch.float32, device=dev)
+            if "w_h" in proj:
+                g_h, d_h = proj["w_h"].shape[:2]
+                self.buf["proj_h"] = torch.empty((B, n_q, g_h * d_h), dtype=torch.float32, device=dev)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.ws = {}
         self._size_workspaces()
@@ -71,8 +100,15 @@ class HybridStep:
         return b["entries"], b["kI"], b.get("kI_scale")
 
     def _hca_cache(self):
-        return self.x["kc_h"] if self.w.kind == "hybrid_decode" else (
-            self.x["kc"] if self.w.kind == "hca_decode" else self.buf["entries_h"])
+        if self.w.kind in ("hybrid_decode", "parallel_decode"):
+            return self.x["kc_h"]
+        return self.x["kc"] if self.w.kind == "hca_decode" else self.buf["entries_h"]
+
+    def _hca_q_kv(self):
+        """The HCA branch's queries and window rows (its own in a hybrid step's HCA layer)."""
+        if self.w.kind == "hybrid_decode":
+            return self.x["q_h"], self.x["kv_h"]
+        return self.x["q"], self.x["kv"]
 
     def _size_workspaces(self):
         w, x, b = self.w, self.x, self.buf
@@ -86,7 +122,7 @@ class HybridStep:
             self.ws["csa"] = torch.zeros(max(n, 1), dtype=torch.uint8, device=self.device)  # (join counters)
         if self.has_hca:
             kc = self._hca_cache()
-            q = x["q_h"] if w.kind == "hybrid_decode" else x["q"]
+            q = self._hca_q_kv()[0]
             a = ops.hca_attend_args(q, kc, kc, w.m_hca, w.q_pos0, w.scale, b["o_h"], b["lse_h"],
                                     window=self._win_hca())
             n = int(ops._abi.load().hca_attend_workspace_size(a))
@@ -106,7 +142,7 @@ class HybridStep:
     def _win_hca(self, as_dict=False):
         if not self.fuse_window:
             return None
-        kv = self.x["kv_h"] if self.w.kind == "hybrid_decode" else self.x["kv"]
+        kv = self._hca_q_kv()[1]
         d = dict(kw=kv, kv_pos0=self._kv_pos0(), q_pos0=self.w.q_pos0, n_win=self.w.n_win, out=self.buf["out_h"])
         if as_dict:
             return d
@@ -142,8 +178,7 @@ class HybridStep:
         w, x, b = self.w, self.x, self.buf
         st = self.dev_status
         kc = self._hca_cache()
-        q = x["q_h"] if w.kind == "hybrid_decode" else x["q"]
-        kv = x["kv_h"] if w.kind == "hybrid_decode" else x["kv"]
+        q, kv = self._hca_q_kv()
         if w.decode:
             Nh = w.n_hca
             ops.hyb_compress(x["ch"], x["zh"], x["bias_h"], w.m_hca, first_block=Nh - 1, out=kc, out_row0=Nh - 1,
@@ -156,11 +191,35 @@ class HybridStep:
             ops.swa_merge(q, kv, kv, kv_pos0=self._kv_pos0(), q_pos0=w.q_pos0, n_win=w.n_win, scale=w.scale,
                           o_in=b["o_h"], lse_in=b["lse_h"], out=b["out_h"], dev_status=st, stream=stream)
 
+    def run_swa(self, stream=None):
+        """A pure sliding-window layer: the window of each query, no compressed branch."""
+        w, x, b = self.w, self.x, self.buf
+        ops.swa_merge(x["q"], x["kv"], x["kv"], kv_pos0=self._kv_pos0(), q_pos0=w.q_pos0, n_win=w.n_win, scale=w.scale,
+                      out=b["out"], dev_status=self.dev_status, stream=stream)
+
+    def run_proj(self, stream=None):
+        """The grouped output projection of the step's attention outputs (see the module notes)."""
+        if self.proj is None:
+            return
+        b, st, W = self.buf, self.dev_status, self.proj["w"]
+        if self.w.kind == "parallel_decode":
+            g, d_g = W.shape[:2]
+            half = (g // 2) * d_g
+            ops.grouped_out_proj(b["out"], W[: g // 2], out=b["proj"][..., :half], dev_status=st, stream=stream)
+            ops.grouped_out_proj(b["out_h"], W[g // 2:], out=b["proj"][..., half:], dev_status=st, stream=stream)
+            return
+        ops.grouped_out_proj(b["out"], W, out=b["proj"], dev_status=st, stream=stream)
+        if "w_h" in self.proj:
+            ops.grouped_out_proj(b["out_h"], self.proj["w_h"], out=b["proj_h"], dev_status=st, stream=stream)
+
     def run(self, stream=None):
+        if self.swa_only:
+            self.run_swa(stream)
         if self.has_csa:
             self.run_csa(stream)
         if self.has_hca:
             self.run_hca(stream)
+        self.run_proj(stream)
 
     # ------------------------------------------------------------ e2e view
     def step_input_keys(self):
@@ -169,6 +228,8 @@ class HybridStep:
         return keys
 
     def output_keys(self):
+        if self.proj is not None:
+            return [k for k in ("proj", "proj_h") if k in self.buf]
         return [k for k in ("out", "out_h") if k in self.buf]
 
     def pack_step_io(self):

@@ -27,7 +27,10 @@ import torch
 @dataclasses.dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str  # "forward" | "csa_decode" | "hca_decode" | "csa_prefill" | "hybrid_decode"
+    # "forward" | "csa_decode" | "hca_decode" | "csa_prefill" | "hybrid_decode" (a CSA layer and an
+    # HCA layer) | "parallel_decode" (CSA and HCA side by side on the same queries and window, their
+    # outputs concatenated) | "swa_decode" (a pure sliding-window layer)
+    kind: str
     batch: int
     n_ctx: int  # decode: tokens in context (the query is the last one); prefill/forward: chunk length
     n_h: int
@@ -85,6 +88,11 @@ WORKLOADS = {
                                 n_ih=64, c_I=128, seed=1004),
     "pro_1m_hybrid_decode": Workload("pro_1m_hybrid_decode", "hybrid_decode", batch=4, n_ctx=1048576, n_h=128, c=512,
                                      m=4, k=1024, n_ih=64, c_I=128, m_hca=128, seed=1005),
+    # the same caches with the two branches side by side in one sublayer
+    "pro_1m_parallel_decode": Workload("pro_1m_parallel_decode", "parallel_decode", batch=4, n_ctx=1048576, n_h=128,
+                                       c=512, m=4, k=1024, n_ih=64, c_I=128, m_hca=128, seed=1006),
+    # Flash's first layers: sliding window only
+    "flash_swa_decode": Workload("flash_swa_decode", "swa_decode", batch=8, n_ctx=65536, n_h=64, c=512, seed=1007),
 }
 
 
@@ -173,7 +181,12 @@ def make_inputs(w: Workload, device="cpu") -> dict:
             out["bias_h"] = d.normal((w.m_hca, c))
         return out
 
-    if w.kind in ("csa_decode", "hybrid_decode"):
+    if w.kind == "swa_decode":
+        queries(1)
+        out["kv"] = d.normal((B, w.n_win, c), kv_std, dt)
+        return out
+
+    if w.kind in ("csa_decode", "hybrid_decode", "parallel_decode"):
         N = w.n_csa
         out["kc"] = d.normal((B, N, c), kv_std, dt)
         kI, ks = _indexer_values(d, (B, N, w.c_I), w.idx_dtype)
@@ -184,6 +197,12 @@ def make_inputs(w: Workload, device="cpu") -> dict:
         indexer_queries(1)
         queries(1)
         out["kv"] = d.normal((B, w.n_win, c), kv_std, dt)
+    if w.kind == "parallel_decode":
+        # the HCA cache and its raw block; the queries and the window are the CSA branch's
+        out["kc_h"] = d.normal((B, w.n_hca, c), kv_std, dt)
+        out["ch"] = d.normal((B, w.m_hca, c), kv_std, dt)
+        out["zh"] = d.normal((B, w.m_hca, c), 1.0, dt)
+        out["bias_h"] = d.normal((w.m_hca, c))
     if w.kind in ("hca_decode", "hybrid_decode"):
         sfx = "_h" if w.kind == "hybrid_decode" else ""
         out["kc" + ("_h" if sfx else "")] = d.normal((B, w.n_hca, c), kv_std, dt)

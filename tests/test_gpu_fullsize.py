@@ -20,13 +20,13 @@ if torch.cuda.is_available():
 DEV = "cuda"
 
 
-def _run(name, **changes):
+def _run(name, proj=None, **changes):
     w = workloads.WORKLOADS[name]
     if changes:
         w = workloads.scaled(w, **changes)
     x = workloads.make_inputs(w, DEV)
     cache_before = {k: x[k].clone() for k in ("kc", "kI", "kI_scale", "kc_h") if k in x}
-    step = pipeline.HybridStep(w, x)
+    step = pipeline.HybridStep(w, x, proj=proj)
     step.run()
     torch.cuda.synchronize()
     assert step.dev_status.item() == 0
@@ -65,7 +65,10 @@ def _check_decode_csa(w, x, step, before, b):
     assert max_abs(to_np(step.buf["lse"][sl]), lu) <= TOL_BF16
 
 
-def _check_decode_hca(w, x, step, before, b, sfx):
+def _check_decode_hca(w, x, step, before, b, sfx, qkv_sfx=None):
+    """qkv_sfx: suffix of the branch's queries and window rows (the cache's suffix unless
+    the branch shares the CSA branch's queries, as in the parallel composition)."""
+    qkv_sfx = sfx if qkv_sfx is None else qkv_sfx
     sl = slice(b, b + 1)
     cpu = lambda k: x[k][sl].cpu()
     Nh = w.n_hca
@@ -75,9 +78,10 @@ def _check_decode_hca(w, x, step, before, b, sfx):
     assert _bf16_close(to_np(x[kc_key][b, Nh - 1]), ref[0, 0])
     assert torch.equal(x[kc_key][b, : Nh - 1], before[kc_key][b, : Nh - 1])
     kc = cpu(kc_key)
-    q = cpu("q" + sfx)
+    q = cpu("q" + qkv_sfx)
     o, l = oracle.hca_attend(q, kc, kc, m=w.m_hca, q_pos0=t, scale=w.scale)
-    out, lu = oracle.swa_merge(q, cpu("kv" + sfx), cpu("kv" + sfx), w.n_ctx - w.n_win, t, w.n_win, w.scale, o, l)
+    kv = cpu("kv" + qkv_sfx)
+    out, lu = oracle.swa_merge(q, kv, kv, w.n_ctx - w.n_win, t, w.n_win, w.scale, o, l)
     assert_out_close(to_np(step.buf["out_h"][sl]), out)
     assert max_abs(to_np(step.buf["lse_h"][sl]), lu) <= TOL_BF16
 
@@ -110,6 +114,43 @@ def test_pro_1m_hybrid_decode_full_size_unit_scale_values():
     for b in (0, w.batch - 1):
         _check_decode_csa(w, x, step, before, b)
         _check_decode_hca(w, x, step, before, b, "_h")
+
+
+def _proj_weights(seed, g, d_g, k):
+    gen = torch.Generator()
+    gen.manual_seed(seed)
+    return (torch.randn((g, d_g, k), generator=gen) / math.sqrt(k)).to(torch.bfloat16).to(DEV)
+
+
+@pytest.mark.parametrize("kv_std,q_std", [(None, 1.0), (1.0, 2.0)])
+def test_pro_1m_parallel_decode_full_size_with_grouped_projection(kv_std, q_std):
+    """CSA and HCA side by side on the same queries and window, at 1M context: each branch
+    against the oracle chain, then the grouped projection of the 2 n_h concatenated heads
+    (16 groups of 16 heads; the first 8 groups read the CSA heads) fed the GPU's outputs."""
+    w0 = workloads.WORKLOADS["pro_1m_parallel_decode"]
+    g, d_g = 16, 256
+    W = _proj_weights(83, g, d_g, 2 * w0.n_h * w0.c // g)
+    w, x, step, before = _run("pro_1m_parallel_decode", proj=dict(w=W), kv_std=kv_std, q_std=q_std)
+    for b in (0, w.batch - 1):
+        _check_decode_csa(w, x, step, before, b)
+        _check_decode_hca(w, x, step, before, b, "_h", qkv_sfx="")
+    cat = torch.cat([step.buf["out"], step.buf["out_h"]], dim=-2)
+    ref = oracle.grouped_out_proj(to_np(cat), W.double().cpu().numpy())
+    assert_out_close(to_np(step.buf["proj"]), ref, tol=1e-3, rel=1e-3, what="projection")
+
+
+@pytest.mark.parametrize("kv_std,q_std", [(None, 1.0), (1.0, 2.0)])
+def test_flash_swa_decode_full_size(kv_std, q_std):
+    """A pure sliding-window layer (Flash shapes): softmax attention over the window alone."""
+    w, x, step, _ = _run("flash_swa_decode", kv_std=kv_std, q_std=q_std)
+    t = w.n_ctx - 1
+    for b in (0, w.batch - 1):
+        sl = slice(b, b + 1)
+        q, kv = x["q"][sl].cpu(), x["kv"][sl].cpu()
+        shape = q.shape[:3]
+        out, _ = oracle.swa_merge(q, kv, kv, w.n_ctx - w.n_win, t, w.n_win, w.scale, np.zeros(q.shape),
+                                  np.full(shape, -np.inf))
+        assert_out_close(to_np(step.buf["out"][sl]), out)
 
 
 def test_flash_decodes_full_size_unit_scale_values():
