@@ -59,13 +59,17 @@ def measured_peaks():
 # -------------------------------------------------------- algorithmic bytes
 
 
-def stage_model(w):
+def stage_model(w, proj=None):
     """Algorithmic bytes / flops per stage per step (the minimum traffic the
-    stage's definition needs: each input read once, each output written once)."""
+    stage's definition needs: each input read once, each output written once).
+    proj: the step's grouped output projection, {"g", "d_g", "in_heads", "calls"} (None: none)."""
     B, c, H = w.batch, w.c, w.n_h
     bf = 2 if w.dtype.itemsize == 2 else 4
     m = {}
-    if w.kind in ("hybrid_decode", "csa_decode"):
+    if w.kind == "swa_decode":
+        m["swa"] = dict(bytes=B * (w.n_win * c * bf + H * c * bf * 2), flops=B * w.n_win * H * c * 4,
+                        flop_dtype="bf16")
+    if w.kind in ("hybrid_decode", "csa_decode", "parallel_decode"):
         N = w.n_csa
         m["csa_compress"] = dict(bytes=B * (4 * 2 * w.m * (c + w.c_I) * bf + c * bf + w.c_I + 4), flops=0)
         m["csa_index_topk"] = dict(bytes=B * (N * (w.c_I + 4) + w.n_ih * (w.c_I + 8) + w.k * 4),
@@ -73,7 +77,7 @@ def stage_model(w):
         # attention over the selected entries with the window merge fused (one call)
         m["csa_attend"] = dict(bytes=B * ((w.k + w.n_win) * c * bf + w.k * 4 + H * c * bf + H * c * bf + H * 4),
                                flops=B * (w.k + w.n_win) * H * c * 4, flop_dtype="bf16")
-    if w.kind in ("hybrid_decode", "hca_decode"):
+    if w.kind in ("hybrid_decode", "hca_decode", "parallel_decode"):
         Nh = w.n_hca
         m["hca_compress"] = dict(bytes=B * (2 * w.m_hca * c * bf + c * bf), flops=0)
         m["hca_attend"] = dict(bytes=B * ((Nh + w.n_win) * c * bf + H * c * bf + H * c * bf + H * 4),
@@ -88,6 +92,12 @@ def stage_model(w):
                                    flops=pairs * w.n_ih * w.c_I * 2, flop_dtype="fp8")
         m["csa_attend"] = dict(bytes=n * H * c * (bf + bf) + N * c * bf + n * w.k * 4 + n * c * bf,
                                flops=(sel + win) * H * c * 4, flop_dtype="bf16")
+    if proj is not None:
+        rows = B * w.n_q
+        K = proj["in_heads"] * c // proj["g"]
+        m["proj"] = dict(bytes=proj["g"] * proj["d_g"] * K * 2 + rows * proj["in_heads"] * c * 2
+                         + rows * proj["g"] * proj["d_g"] * 4,
+                         flops=2 * rows * proj["g"] * proj["d_g"] * K, flop_dtype="bf16")
     return m
 
 
@@ -102,7 +112,7 @@ KERNEL_NCU_TRAFFIC = {
 def scoring_kernel_model(w):
     """Algorithmic bytes / flops of one launch of the indexer's scoring kernel (its
     inputs read once: the FP8 keys and scales, the queries, scales and head weights)."""
-    if w.kind not in ("hybrid_decode", "csa_decode", "csa_prefill"):
+    if w.kind not in ("hybrid_decode", "csa_decode", "csa_prefill", "parallel_decode"):
         return None
     n_q = 1 if w.decode else w.n_ctx
     N = w.n_csa
@@ -129,6 +139,8 @@ def stage_kernels(w):
     128 heads run the 128-heads-per-CTA attention kernel, the others the 64-head one)."""
     att = "attend_h128_kernel" if (w.decode and w.n_h % 128 == 0) else "attend_tc_kernel"
     return {
+        "swa": f"{att}<2> (swa_merge, window only)",
+        "proj": "out_proj_kernel (grouped output projection)",
         "csa_compress": "compress_kernel x2 (CSA entry bf16 + indexer key e4m3)",
         "csa_attend": f"{att}<0> (csa_attend, window fused)",
         "hca_compress": "compress_kernel (HCA entry)",
@@ -278,25 +290,44 @@ def rank_seed(seed: int, rank: int) -> int:
     return seed + 7919 * rank
 
 
-def run_ours(args, w):
+def make_proj(w, spec, dev):
+    """Seeded bf16 projection matrices for a step (HybridStep's proj argument) and the
+    stage model's description of them.  spec: "per_layer" (each attention output of the
+    step projected by its own [g][d_g][(n_h/g) c] set) or "concat" (one set over the 2 n_h
+    concatenated heads of the parallel composition)."""
+    import torch
+
+    g_, d_g = w.out_groups, w.out_dim
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w.seed + 31)
+    heads = 2 * w.n_h if spec == "concat" else w.n_h
+    K = heads * w.c // g_
+    mk = lambda: (torch.randn((g_, d_g, K), generator=gen, device=dev) / math.sqrt(K)).to(torch.bfloat16)
+    mats = {"w": mk()}
+    calls = 2 if spec == "concat" else 1
+    if spec == "per_layer" and w.kind == "hybrid_decode":
+        mats["w_h"] = mk()
+        calls = 2
+    model = {"g": g_ * (2 if "w_h" in mats else 1), "d_g": d_g, "in_heads": heads * (2 if "w_h" in mats else 1),
+             "calls": calls}
+    return mats, model
+
+
+def measure_workload(args, w, dev, dist=None, rank=0, world=1, steps_k=None, proj_spec=None, sample_clocks=True):
+    """Time one workload: K steps captured as one CUDA graph of the library's launches
+    (the step time), and the same K steps as a second graph with CUDA events around
+    every stage and around the indexer's scoring kernel (stage and kernel times).
+    Inputs rotate over enough copies that one pass streams at least 4x the L2 size.
+    Returns (result dict, the step objects, the stream)."""
     import torch
 
     from sparse_attention_gated_b300 import pipeline, workloads
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl")
-    dev = torch.device("cuda", local)
+    K = steps_k or args.steps
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20
-
-    model = stage_model(w)
+    mats, pmodel = make_proj(w, proj_spec, dev) if proj_spec else (None, None)
+    model = stage_model(w, pmodel)
     step_bytes = sum(v["bytes"] for v in model.values())
     # each rank processes its own sequences (independent decode streams): different seeds
     wr = workloads.scaled(w, seed=rank_seed(w.seed, rank))
@@ -306,7 +337,7 @@ def run_ours(args, w):
     steps = []
     for r in range(copies):
         x = workloads.make_inputs(workloads.scaled(wr, seed=wr.seed + 104729 * r), dev)
-        steps.append(pipeline.HybridStep(w, x))
+        steps.append(pipeline.HybridStep(w, x, proj=mats))
     torch.cuda.synchronize()
 
     stream = torch.cuda.Stream(device=dev)
@@ -322,25 +353,31 @@ def run_ours(args, w):
         if ev is None:  # the headline graph: the library's launches, as HybridStep.run issues them
             st.run(stream)
             return
+        if st.swa_only:
+            rec("swa", 0)
+            st.run_swa(stream)
+            rec("swa", 1)
         if st.has_csa:
             rec("csa_compress", 0)
             _csa_parts(st, stream, rec, ev["index_scores"])
         if st.has_hca:
             rec("hca_compress", 0)
             _hca_parts(st, stream, rec)
+        if st.proj is not None:
+            rec("proj", 0)
+            st.run_proj(stream)
+            rec("proj", 1)
 
     # warm-up (eager), also the first-call setup of every kernel
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
             run_step(steps[i % copies])
     stream.synchronize()
+    if int(steps[0].dev_status.item()) != 0:
+        raise RuntimeError(f"{w.name}: device status {int(steps[0].dev_status.item())}")
 
-    # The K timed steps as one graph of the library's launches only (the headline
-    # time), and the same K steps as a second graph with CUDA events around every
-    # stage and around the indexer's scoring kernel (stage and kernel times).
-    # External event records: real timestamps taken by each replay of the graph.
     ev = lambda: torch.cuda.Event(enable_timing=True, external=True)
-    events = [{s: (ev(), ev()) for s in stages + ["index_scores"]} for _ in range(args.steps)]
+    events = [{s_: (ev(), ev()) for s_ in stages + ["index_scores"]} for _ in range(K)]
     with torch.cuda.stream(stream):
         for e in events:  # create the events (the library records two of them itself)
             for pair in e.values():
@@ -350,22 +387,23 @@ def run_ours(args, w):
     g_ev = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(g, stream=stream):
-            for i in range(args.steps):
+            for i in range(K):
                 run_step(steps[i % copies])
         with torch.cuda.graph(g_ev, stream=stream):
-            for i in range(args.steps):
+            for i in range(K):
                 run_step(steps[i % copies], events[i])
     # warm the graphs (and the clocks) for about a second
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(dev.index or 0) if sample_clocks else None
     t_busy0 = time.time()
     with torch.cuda.stream(stream):
         g.replay()
     stream.synchronize()
-    t_graph = time.time() - t_busy0
-    reps = max(1, int(1.0 / max(t_graph, 1e-3)))
+    # (replays until a second has passed, so that the clock samples cover the busy GPU)
     with torch.cuda.stream(stream):
-        for _ in range(min(reps, 200)):
-            g.replay()
+        while time.time() - t_busy0 < 1.0:
+            for _ in range(8):
+                g.replay()
+            stream.synchronize()
         g_ev.replay()
     stream.synchronize()
 
@@ -373,7 +411,6 @@ def run_ours(args, w):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    t_timed0 = time.time()
     with torch.cuda.stream(stream):
         start.record(stream)
         g.replay()
@@ -382,9 +419,8 @@ def run_ours(args, w):
     if dist is not None:
         dist.barrier()
     t_timed1 = time.time()
-    clocks = sampler.stop(t_busy0, t_timed1)
-    ms_total = max_over_ranks(start.elapsed_time(end), dist, dev)
-    ms_step = ms_total / args.steps
+    clocks = sampler.stop(t_busy0, t_timed1) if sampler else None
+    ms_step = max_over_ranks(start.elapsed_time(end), dist, dev) / K
     # the evented graph, right after: per-stage and scoring-kernel times
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
@@ -392,26 +428,20 @@ def run_ours(args, w):
         g_ev.replay()
         s1.record(stream)
     torch.cuda.synchronize()
-    ms_step_ev = s0.elapsed_time(s1) / args.steps
+    if int(steps[0].dev_status.item()) != 0:
+        raise RuntimeError(f"{w.name}: device status {int(steps[0].dev_status.item())}")
+    ms_step_ev = s0.elapsed_time(s1) / K
     has_scoring = "csa_index_topk" in stages
     timed = stages + (["index_scores"] if has_scoring else [])
-    stage_ms = {s: statistics.mean(events[i][s][0].elapsed_time(events[i][s][1]) for i in range(args.steps))
-                for s in timed}
+    stage_ms = {s_: statistics.mean(events[i][s_][0].elapsed_time(events[i][s_][1]) for i in range(K))
+                for s_ in timed}
     scoring_ms = stage_ms.pop("index_scores", None)
-
     units = w.batch if w.decode else w.n_ctx
-    value = job_rate(units, world, ms_step)
 
-    # -------- e2e through the public API: fresh inputs from pinned host memory
-    e2e = run_e2e(args, w, steps[0], stream, units, world, dist)
-
-    # -------- roofline of every kernel (stage events; the indexer's scoring kernel by the
-    # events the library records around it, the selection as the rest of its stage);
-    # the dominant kernel is the one with the longest measured time
-    peaks, peak_kind = measured_peaks()
-    fp8 = fp8_peak_probe(dev) if rank == 0 else None
-    if fp8:
-        peaks = dict(peaks, fp8_tflops=fp8, fp8_source="measured by this run: dense e4m3 8192^3 GEMM (cuBLASLt)")
+    # roofline of every kernel (stage events; the indexer's scoring kernel by the events the
+    # library records around it, the selection as the rest of its stage); the dominant kernel
+    # is the one with the longest measured time
+    peaks, peak_kind = args.peaks
     kern = {}
     if has_scoring:
         kern["index_scores"] = ("index_tc_kernel (csa_index_topk scoring)", scoring_kernel_model(w), scoring_ms)
@@ -423,45 +453,118 @@ def run_ours(args, w):
     kernels = {k: kernel_roofline(lbl, m_, ms_, peaks, peak_kind, KERNEL_NCU_TRAFFIC.get((w.name, k)))
                for k, (lbl, m_, ms_) in kern.items()}
     dom = max(kernels, key=lambda k: kernels[k]["ms_per_launch"])
-    roof = dict(kernels[dom])
-
-    step_roof_s = max(step_bytes / (peaks["hbm_gbs"] * 1e9), 0.0)
+    step_roof_s = step_bytes / (peaks["hbm_gbs"] * 1e9)
     # each stage at its own bound (bytes at the HBM peak or flops at the tensor peak)
     step_roof_any_s = sum(max(v["bytes"] / (peaks["hbm_gbs"] * 1e9),
                               v["flops"] / (_tensor_peak(peaks, v["flop_dtype"]) * 1e12) if v["flops"] else 0.0)
                           for v in model.values())
-    out = {
-        "metric": METRIC,
-        "value": value,
+    config = {"workload": w.name, "batch": w.batch, "context": w.n_ctx, "n_h": w.n_h, "c": w.c, "m": w.m,
+              "m_hca": w.m_hca, "top_k": w.k, "n_ih": w.n_ih, "c_I": w.c_I, "n_win": w.n_win,
+              "l2_defeat": f"inputs rotate over {copies} copies (>= 4x L2 per pass)" if copies > 1 else
+              "one step streams several times the L2 size", "graph": "K steps captured as one CUDA graph"}
+    if pmodel:
+        config["out_proj"] = {"spec": proj_spec, "groups": pmodel["g"], "d_g": pmodel["d_g"],
+                              "weights": "seeded random bf16, resident"}
+    res = {
+        "value": job_rate(units, world, ms_step),
         "unit": "queries/s" if w.decode else "tokens/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
         "ms_per_step": ms_step,
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16+fp8" if w.dtype != __import__("torch").float32 else "f32",
-        "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch, "context": w.n_ctx, "n_h": w.n_h, "c": w.c,
-                   "m": w.m, "m_hca": w.m_hca, "top_k": w.k, "n_ih": w.n_ih, "c_I": w.c_I, "n_win": w.n_win,
-                   "l2_defeat": f"inputs rotate over {copies} copies (>= 4x L2 per pass)" if copies > 1 else
-                   "one step streams several times the L2 size", "graph": "K steps captured as one CUDA graph"},
+        "steps": K,
+        "config": config,
         "clocks": clocks,
-        "e2e": e2e,
-        "gpu_launches": _launches_per_step(w) * args.steps,
-        "roofline": roof,
+        "gpu_launches": _launches_per_step(w, pmodel) * K,
+        "roofline": dict(kernels[dom]),
         "kernels": kernels,
-        "fp8_tflops_measured": fp8,
         "stages_ms": stage_ms,
         "ms_per_step_with_stage_events": ms_step_ev,
         "step_hbm_roofline_frac": step_roof_s / (ms_step / 1e3),
         "step_roofline_frac": step_roof_any_s / (ms_step / 1e3),
     }
+    return res, steps, stream
+
+
+# the other workloads of the method's configurations, measured after the headline at N = 1:
+# (workload, output projection, steps)
+EXTRA_CONFIGS = (
+    ("flash_csa_decode", None, 20),
+    ("flash_hca_decode", None, 20),
+    ("flash_swa_decode", None, 20),
+    ("pro_1m_parallel_decode", "concat", 20),
+    ("pro_1m_hybrid_decode", "per_layer", 20),
+    ("pro_csa_prefill", None, 3),
+)
+
+
+def run_ours(args, w):
+    import torch
+
+    from sparse_attention_gated_b300 import workloads
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    peaks, peak_kind = measured_peaks()
+    fp8 = fp8_peak_probe(dev) if rank == 0 else None
+    if fp8:
+        peaks = dict(peaks, fp8_tflops=fp8, fp8_source="measured by this run: dense e4m3 8192^3 GEMM (cuBLASLt)")
+    args.peaks = (peaks, peak_kind)
+
+    res, steps, stream = measure_workload(args, w, dev, dist, rank, world)
+    units = w.batch if w.decode else w.n_ctx
+    # -------- e2e through the public API: fresh inputs from pinned host memory
+    e2e = run_e2e(args, w, steps[0], stream, units, world, dist)
+    out = {
+        "metric": METRIC,
+        "value": res["value"],
+        "unit": res["unit"],
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": res["ms_per_step"],
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16+fp8" if w.dtype != torch.float32 else "f32",
+        "data": "synthetic",
+        "config": res["config"],
+        "clocks": res["clocks"],
+        "e2e": e2e,
+        "gpu_launches": res["gpu_launches"],
+        "roofline": res["roofline"],
+        "kernels": res["kernels"],
+        "fp8_tflops_measured": fp8,
+        "stages_ms": res["stages_ms"],
+        "ms_per_step_with_stage_events": res["ms_per_step_with_stage_events"],
+        "step_hbm_roofline_frac": res["step_hbm_roofline_frac"],
+        "step_roofline_frac": res["step_roofline_frac"],
+    }
     if rank == 0 and world == 1 and w.kind == "hybrid_decode" and not args.no_session:
         out["session"] = run_session(w, stream)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, steps[0])
+    del steps
+    if world == 1 and not args.no_configs:
+        # the method's other configurations (context for the headline, same timing rules)
+        out["configs"] = {}
+        for name, spec, k in EXTRA_CONFIGS:
+            torch.cuda.empty_cache()
+            wx = workloads.WORKLOADS[name]
+            key = name + ("+out_proj" if spec else "")
+            try:
+                r, st_x, _ = measure_workload(args, wx, dev, steps_k=min(args.steps, k), proj_spec=spec)
+                if not args.no_cpu_baseline:
+                    r["cpu_baseline"] = cpu_baseline(wx, st_x[0], budget_s=3.0, prefill_rows=4)
+                del st_x
+            except Exception as e:  # noqa: BLE001 - one failed extra config must not lose the headline
+                r = {"error": f"{type(e).__name__}: {e}"}
+            out["configs"][key] = r
     if dist is not None:
         dist.destroy_process_group()
     return out if rank == 0 else None
@@ -582,8 +685,7 @@ def _hca_parts(st, stream, rec):
     w, x, b = st.w, st.x, st.buf
     s = st.dev_status
     kc = st._hca_cache()
-    q = x["q_h"] if w.kind == "hybrid_decode" else x["q"]
-    kv = x["kv_h"] if w.kind == "hybrid_decode" else x["kv"]
+    q = st._hca_q_kv()[0]
     Nh = w.n_hca
     ops.hyb_compress(x["ch"], x["zh"], x["bias_h"], w.m_hca, first_block=Nh - 1, out=kc, out_row0=Nh - 1,
                      dev_status=s, stream=stream)
@@ -594,14 +696,18 @@ def _hca_parts(st, stream, rec):
     rec("hca_attend", 1)
 
 
-def _launches_per_step(w):
+def _launches_per_step(w, proj=None):
     n = 0
-    if w.kind in ("hybrid_decode", "csa_decode"):
+    if w.kind == "swa_decode":
+        n += 1
+    if w.kind in ("hybrid_decode", "csa_decode", "parallel_decode"):
         n += 2 + 2 + 1  # compress x2, index scores + top-k, attention with the window merge fused
     if w.kind == "csa_prefill":
-        n += 2 + 2 + 2  # (32,768 queries: too many to fuse the window, so two attention launches)
-    if w.kind in ("hybrid_decode", "hca_decode"):
+        n += 2 + 2 + 1  # compress x2, index scores + top-k, attention with the window merge fused
+    if w.kind in ("hybrid_decode", "hca_decode", "parallel_decode"):
         n += 1 + 1
+    if proj is not None:
+        n += proj["calls"]
     return n
 
 
@@ -687,14 +793,23 @@ def run_e2e(args, w, st, stream, units, world, dist):
 # ------------------------------------------------------------ CPU oracle
 
 
-def oracle_query(w, x, b):
+def oracle_query(w, x, b, proj=None):
     """The float64 oracle's chain for query b of a decode workload (the
-    CPU-baseline unit of work).  x holds CPU tensors."""
+    CPU-baseline unit of work), with the step's grouped output projection when
+    proj (the step's matrices, CPU) is given.  x holds CPU tensors."""
+    import numpy as np
+
     import oracle
 
     t = w.n_ctx - 1
     sl = slice(b, b + 1)
-    if w.kind in ("hybrid_decode", "csa_decode"):
+    outs = []
+    if w.kind == "swa_decode":
+        q = x["q"][sl]
+        o, _ = oracle.swa_merge(q, x["kv"][sl], x["kv"][sl], w.n_ctx - w.n_win, t, w.n_win, w.scale,
+                                np.zeros(q.shape), np.full(q.shape[:3], -np.inf))
+        outs.append(o)
+    if w.kind in ("hybrid_decode", "csa_decode", "parallel_decode"):
         N = w.n_csa
         oracle.compress(x["ca"][sl], x["za"][sl], x["bias"], w.m, cb=x["cb"][sl], zb=x["zb"][sl], overlap=True,
                         first_block=N - 2)
@@ -705,14 +820,22 @@ def oracle_query(w, x, b):
                                 kI_scale=x["kI_scale"][sl])
         idx = oracle.topk(s, [[N]], w.k)
         o, l = oracle.csa_attend(x["q"][sl], x["kc"][sl], x["kc"][sl], idx, w.scale)
-        oracle.swa_merge(x["q"][sl], x["kv"][sl], x["kv"][sl], w.n_ctx - w.n_win, t, w.n_win, w.scale, o, l)
-    if w.kind in ("hybrid_decode", "hca_decode"):
-        sfx = "_h" if w.kind == "hybrid_decode" else ""
+        outs.append(oracle.swa_merge(x["q"][sl], x["kv"][sl], x["kv"][sl], w.n_ctx - w.n_win, t, w.n_win, w.scale,
+                                     o, l)[0])
+    if w.kind in ("hybrid_decode", "hca_decode", "parallel_decode"):
+        sfx = "_h" if w.kind in ("hybrid_decode", "parallel_decode") else ""
+        qsfx = "_h" if w.kind == "hybrid_decode" else ""
         kc = x["kc" + sfx][sl]
         oracle.compress(x["ch"][sl], x["zh"][sl], x["bias_h"], w.m_hca, first_block=w.n_hca - 1)
-        o, l = oracle.hca_attend(x["q" + sfx][sl], kc, kc, m=w.m_hca, q_pos0=t, scale=w.scale)
-        oracle.swa_merge(x["q" + sfx][sl], x["kv" + sfx][sl], x["kv" + sfx][sl], w.n_ctx - w.n_win, t, w.n_win,
-                         w.scale, o, l)
+        o, l = oracle.hca_attend(x["q" + qsfx][sl], kc, kc, m=w.m_hca, q_pos0=t, scale=w.scale)
+        outs.append(oracle.swa_merge(x["q" + qsfx][sl], x["kv" + qsfx][sl], x["kv" + qsfx][sl], w.n_ctx - w.n_win, t,
+                                     w.n_win, w.scale, o, l)[0])
+    if proj is not None:
+        if w.kind == "parallel_decode":  # one projection of the concatenated heads
+            oracle.grouped_out_proj(np.concatenate(outs, axis=-2), proj["w"])
+        else:
+            for o_, key in zip(outs, ("w", "w_h")):
+                oracle.grouped_out_proj(o_, proj[key])
 
 
 def oracle_prefill_rows(w, x, rows):
@@ -737,7 +860,7 @@ def oracle_prefill_rows(w, x, rows):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(w, st=None, budget_s=25.0):
+def cpu_baseline(w, st=None, budget_s=25.0, prefill_rows=16):
     """The oracle, as it stands, on one host core, on a bounded sample."""
     import torch
 
@@ -747,16 +870,19 @@ def cpu_baseline(w, st=None, budget_s=25.0):
         x = {k: v.detach().cpu() for k, v in st.x.items()}
     else:
         x = workloads.make_inputs(w, "cpu")
+    proj = None
+    if st is not None and st.proj is not None:
+        proj = {k: v.float().cpu().numpy() for k, v in st.proj.items()}
     if w.decode:
         done, t0 = 0, time.perf_counter()
         while done < w.batch and (done == 0 or time.perf_counter() - t0 < budget_s):
-            oracle_query(w, x, done)
+            oracle_query(w, x, done, proj)
             done += 1
         dt = time.perf_counter() - t0
         return {"value": done / dt, "unit": "queries/s", "cores": 1, "kind": "oracle",
                 "sample": f"{done} of the {w.batch} decode queries of one step, whole (float64, one thread)",
                 "host_nproc": os.cpu_count()}
-    rows = sorted(set([w.n_ctx - 1] + [int(r) for r in torch.linspace(0, w.n_ctx - 1, 16).tolist()]))
+    rows = sorted(set([w.n_ctx - 1] + [int(r) for r in torch.linspace(0, w.n_ctx - 1, prefill_rows).tolist()]))
     dt = oracle_prefill_rows(w, x, rows)
     # extrapolate per-token time linearly in the attended work of each row
     def cost(j):
@@ -815,6 +941,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-session", action="store_true", help="skip the token-by-token session measurement")
+    ap.add_argument("--no-configs", action="store_true", help="measure the headline workload only")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

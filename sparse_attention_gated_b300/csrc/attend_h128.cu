@@ -5,9 +5,10 @@
 //           (trishampatil.com) section V.3: every query head attends the same selected
 //           entries, key = value = the entry);
 //   mode 1, HCA: every visible entry, s < floor((t+1)/m') (same page, section VI);
-// each optionally with the query's sliding window fused in as one more split of the same
-// softmax ("DeepSeek-V4: Anatomy..." (modernaiengineering.com), "One query in a CSA
-// layer", steps 4-5: one softmax over the union of entries and window rows).
+// each optionally with the query's sliding window fused into the same softmax ("DeepSeek-V4:
+// Anatomy..." (modernaiengineering.com), "One query in a CSA layer", steps 4-5: one softmax
+// over the union of entries and window rows): as one more split of a decode-shaped launch,
+// or as the tiles that follow the list's in a launch with one split.
 //
 // One CTA owns (query, 128 heads, one half of the 512 output dims, split of the list).
 // With the heads on the MMA's 128 rows:
@@ -23,21 +24,29 @@
 // A tile of 64 entries is 8 slabs of [64 rows x 64 dims] bf16 in the 128-byte swizzle.
 // The 4 slabs of this CTA's output half go to ring A (freed once O of the tile is done),
 // the other 4 to ring B (freed once S is done), so that the next tiles' loads start early.
-// Whole tiles of consecutive rows come by TMA tile loads; index lists, a ragged last tile
-// and short windows by TMA gather4 (a row past the list reads as zeros).
+// Whole tiles of consecutive rows come by TMA tile loads; a ragged last tile and short
+// windows by TMA gather4 (a row past the list reads as zeros); index lists by 16-byte
+// cp.async copies of two warps, one per ring, written in the swizzled layout (a TMA gather
+// moves 4 rows of 128 bytes per instruction, several times slower than the L2 can deliver
+// a tile of 64 scattered rows).
 //
-// Warp roles (256 threads, one CTA per SM):
-//   warp 0      producer: one lane issues the TMA loads, the lanes compute gathered rows;
+// Warp roles (320 threads, one CTA per SM):
+//   warp 0      producer: one lane issues the TMA loads (the query rows; the tiles of
+//               contiguous sources), the lanes compute the rows of gather4 copies;
 //   warp 1      TMEM owner and MMA issuer (one elected lane);
-//   warps 2-3   the split join only;
+//   warps 2-3, 8-9  in a CTA with an index list, every tile (the list's, then a fused
+//               window's) by cp.async: the other half's slabs (2: rows 0-31, 8: rows 32-63)
+//               and this half's (3, 9); warps 2-3 also take part in the split join;
 //   warps 4-7   softmax and epilogue: thread h of the four owns TMEM lane h = head h, so a
 //               head's scores are one row and its maximum, exponentials and sum stay in
 //               one thread.
 // Online softmax in base 2 with a lazy reference per head: it moves only when a tile's
 // maximum exceeds it by more than 2^8 (then that head's O row is rescaled in TMEM).
-// Splits of one (query, half) write an unnormalised bf16 partial and (m, l) per head and
-// join through L2 inside the kernel (a launch with splits has at most one CTA per SM, so
-// all are resident); each split then merges 1/S of the outputs.  Every wait is bounded:
+// Decode-shaped launches (few queries) split each (query, half) over several CTAs: the splits
+// write an unnormalised bf16 partial and (m, l) per head and join through L2 inside the
+// kernel (a launch with splits has at most one CTA per SM, so all are resident); each split
+// then merges 1/S of the outputs.  Launches with many queries (prefill) run one CTA per
+// (query, head group, half) over the whole list and window, with no join.  Every wait is bounded:
 // on expiry HYB_DEV_TIMEOUT is raised, the CTA's own copies and products in flight land,
 // TMEM is freed and the kernel returns.
 #include <cstdlib>
@@ -77,8 +86,9 @@ enum {
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + abort flag, TMEM address; + alignment slack
 constexpr uint32_t kColO = 0, kColQ = 256, kColS = 384;
-constexpr int kThreads = 256;
+constexpr int kThreads = 320;
 constexpr int kSoftWarp0 = 4;
+constexpr int kWarps8 = 8;  // warps 8-9: the second pair of copy warps
 constexpr float kTau = 8.0f;          // lazy-reference threshold (log2 units)
 constexpr int kOcts = kC / 2 / 8;     // 32 groups of 8 output dims per half
 
@@ -87,6 +97,8 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 struct H128Params {
   const int32_t* idx;  // mode 0: [rows][list_len]
   const __nv_bfloat16* q;
+  const __nv_bfloat16* kv;  // the entries [batch][kv_stride][c] (key = value)
+  const __nv_bfloat16* wkv; // the window rows [batch][w_stride][c]
   float* o;            // no window: [rows][n_h][c] float32
   float* lse;          // [rows][n_h]: the list's lse, or the union's with a window
   void* out;           // with a window: merged output [rows][n_h][c]
@@ -113,6 +125,8 @@ struct H128Work {
   const int32_t* list;
   int64_t tb, te;  // this split's tiles
   bool win;        // the split attends the window (contiguous rows of the window map)
+  // one split with a window: the window's tiles follow the list's (rows wrow0 .. wrow0 + wL - 1)
+  int64_t nw, wL, wrow0;
 };
 
 // 2^x by the SFU's approximate exponential (relative error far below the bf16 rounding
@@ -138,7 +152,8 @@ __device__ __forceinline__ H128Work h128_work(const H128Params& p) {
   w.list = nullptr;
   w.row0 = 0;
   w.win = false;
-  if (p.win && w.sp == p.n_split - 1) {
+  w.nw = 0, w.wL = 0, w.wrow0 = 0;
+  if (p.win && p.n_split > 1 && w.sp == p.n_split - 1) {
     const int64_t tw = query_pos(p.wq_pos, p.wq_pos0, w.bq, w.j);
     const int64_t kvp = p.w_pos0s ? __ldg(p.w_pos0s + w.b) : p.w_pos0;
     int64_t first;
@@ -158,9 +173,17 @@ __device__ __forceinline__ H128Work h128_work(const H128Params& p) {
     w.row0 = w.b * p.kv_stride;
   }
   const int64_t T = (w.L + kT - 1) / kT;
-  const int64_t S = p.n_split - (p.win ? 1 : 0);
+  const int64_t S = p.n_split - (p.win && p.n_split > 1 ? 1 : 0);
   w.tb = w.sp * T / S;
   w.te = (w.sp + 1) * T / S;
+  if (p.win && p.n_split == 1) {
+    const int64_t tw = query_pos(p.wq_pos, p.wq_pos0, w.bq, w.j);
+    const int64_t kvp = p.w_pos0s ? __ldg(p.w_pos0s + w.b) : p.w_pos0;
+    int64_t first;
+    w.wL = window_rows(tw, p.n_win, kvp, p.w_stride, &first, p.dev_status, report);
+    w.wrow0 = w.b * p.w_stride + first;
+    w.nw = (w.wL + kT - 1) / kT;
+  }
   return w;
 }
 
@@ -209,13 +232,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   // positions in device memory may have been written by the previous kernel: read them after the wait
   if (p.q_pos != nullptr || p.wq_pos != nullptr || p.w_pos0s != nullptr) pdl_wait();
   const H128Work W = h128_work<MODE>(p);
-  const int64_t ntiles = W.te - W.tb;
+  const int64_t nl = W.te - W.tb;  // tiles of the list (or of the window split's window)
+  const int64_t ntiles = nl + W.nw;  // + the window's, after them, with one split
   const bool contig = MODE != 0 || W.win;
+  // index-list tiles are copied by warps 2-3, and then every tile of the CTA is (so that one
+  // role fills the rings in tile order: a parity wait on a slot's barrier is only exact for
+  // the next phase)
+  const bool gathered = !contig;
 
   if (threadIdx.x == 0) {
+    // a tile's slabs in a ring: one TMA transaction count, or two copy warps' signals
+    const uint32_t nfull = gathered ? 2 : 1;
     tc::mbar_init(q_full, 1);
-    for (int s = 0; s < kDA; ++s) tc::mbar_init(&full_a[s], 1), tc::mbar_init(&empty_a[s], 1);
-    for (int s = 0; s < kDB; ++s) tc::mbar_init(&full_b[s], 1), tc::mbar_init(&empty_b[s], 1);
+    for (int s = 0; s < kDA; ++s) tc::mbar_init(&full_a[s], nfull), tc::mbar_init(&empty_a[s], 1);
+    for (int s = 0; s < kDB; ++s) tc::mbar_init(&full_b[s], nfull), tc::mbar_init(&empty_b[s], 1);
     for (int i = 0; i < 2; ++i) tc::mbar_init(&s_full[i], 1), tc::mbar_init(&p_full[i], 4);
     tc::mbar_init(o_done, 1);
     tc::mbar_init(qlo_ready, 4);
@@ -240,9 +270,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kDA; ++s) last_a[s] = -1;
 #pragma unroll
     for (int s = 0; s < kDB; ++s) last_b[s] = -1;
-    const CUtensorMap* tmt = W.win ? &tm_w : &tm_k;
-    const CUtensorMap* tmg = W.win ? &tm_wg : &tm_kg;
-    const int32_t oob = W.win ? p.w_rows : p.k_rows;
+    const CUtensorMap* tmt_l = W.win ? &tm_w : &tm_k;
+    const CUtensorMap* tmg_l = W.win ? &tm_wg : &tm_kg;
+    const int32_t oob_l = W.win ? p.w_rows : p.k_rows;
     // the query rows: dims 256..511 into their own region, dims 0..255 staged in ring A's
     // slots 1 and 2 until the softmax warps have moved them into TMEM
     if (ntiles > 0 && lane == 0) {
@@ -252,21 +282,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tma_load_2d(q_s + s * kQSlab, &tm_q, q_full, 256 + 64 * s, (int32_t)qrow);
         tc::tma_load_2d(ring_a + 4 * kSlab + s * kQSlab, &tm_q, q_full, 64 * s, (int32_t)qrow);
       }
-      tc::prefetch_tmap(tmt);
-      tc::prefetch_tmap(tmg);
+      tc::prefetch_tmap(tmt_l);
+      tc::prefetch_tmap(tmg_l);
+      if (W.nw > 0) tc::prefetch_tmap(&tm_w), tc::prefetch_tmap(&tm_wg);
     }
-    for (int64_t li = 0; li < ntiles && ok; ++li) {
-      const int64_t i = W.tb + li;
-      if (li == 1) {
+    bool qlo_seen = false;
+    for (int64_t li = 0; li < (gathered ? 0 : ntiles) && ok; ++li) {
+      const bool wt = li >= nl;  // a window tile after the list's
+      const int64_t i = wt ? li - nl : W.tb + li;
+      const CUtensorMap* tmt = wt ? &tm_w : tmt_l;
+      const CUtensorMap* tmg = wt ? &tm_wg : tmg_l;
+      const int32_t oob = wt ? p.w_rows : oob_l;
+      if (li >= 1 && !qlo_seen) {
         // ring A's slots 1 and 2 hold the staged query rows until they are in TMEM
         int okq = 1;
         if (lane == 0) okq = tc::mbar_wait(qlo_ready, 0, s_abort, 12);
         if (!(ok = __shfl_sync(0xffffffffu, okq, 0) != 0)) break;
+        qlo_seen = true;
       }
       const int sa = (int)(li % kDA), sb = (int)(li % kDB);
-      const bool whole = contig && (i + 1) * kT <= W.L;
+      const bool whole = wt ? (i + 1) * kT <= W.wL : contig && (i + 1) * kT <= W.L;
       int32_t r0 = oob, r1 = oob;  // map rows of positions 64i + lane and 64i + 32 + lane
-      if (!whole) {
+      if (!whole && wt) {
+        const int64_t p0 = i * kT + lane, p1 = p0 + 32;
+        r0 = p0 < W.wL ? (int32_t)(W.wrow0 + p0) : oob;
+        r1 = p1 < W.wL ? (int32_t)(W.wrow0 + p1) : oob;
+      } else if (!whole) {
         r0 = h128_row<MODE>(p, W, i * kT + lane, oob, true);
         r1 = h128_row<MODE>(p, W, i * kT + 32 + lane, oob, true);
       }
@@ -284,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       if (whole) {
         if (lane == 0) {
-          const int32_t y = (int32_t)(W.row0 + i * kT);
+          const int32_t y = (int32_t)((wt ? W.wrow0 : W.row0) + i * kT);
           for (int j = 0; j < 4; ++j) {
             const int own = 4 * (int)W.dh + j, other = 4 * (1 - (int)W.dh) + j;
             tc::tma_load_2d(ring_b + (sb * 4 + j) * kSlab, tmt, &full_b[sb], 64 * other, y);
@@ -405,7 +446,92 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_wait_drain(fin, 0);
     }
     __syncwarp();
-  } else if (warp >= kSoftWarp0) {
+  } else if (gathered && (warp == 2 || warp == 3 || warp >= kWarps8)) {
+    // ================================================================ tiles by cp.async
+    // Warps 2 and 8 copy the other half's 4 slabs of each tile (the list's, then the
+    // window's) into ring B, warps 3 and 9 this half's into ring A; warps 2-3 take the
+    // tile's rows 0-31, warps 8-9 rows 32-63 (a warp issues one 512-byte cp.async in some 30
+    // cycles, so a tile needs four warps to keep up with the L2).  Lane l copies 16-byte
+    // chunk l % 8 of rows 4u + l / 8 of the warp's 32 rows in every slab: one instruction
+    // moves four 128-byte row pieces.  A tile's copies are one group; the warp signals the
+    // tile's full barrier (two signals complete it) once the group has landed (checked
+    // while the next tile's copies are in flight), after a proxy fence that hands the writes
+    // to the tensor cores.  Positions without an entry are written as zeros.
+    const bool own = (warp & 1) != 0;
+    const int part = warp >= kWarps8 ? 1 : 0;  // rows 32 part .. 32 part + 31
+    const int c16 = lane & 7;
+    const int half = own ? (int)W.dh : 1 - (int)W.dh;
+    const char* kbase = reinterpret_cast<const char*>(p.kv);
+    const char* wbase = reinterpret_cast<const char*>(p.wkv);
+    uint8_t* ring = own ? ring_a : ring_b;
+    const int depth = own ? kDA : kDB;
+    int32_t nx0 = -1, nx1 = -1;  // list values at positions lane and 32 + lane of the next tile
+    auto fetch = [&](int64_t li_) {
+      const int64_t pos = (W.tb + li_) * kT + lane;
+      nx0 = pos < W.L ? __ldg(W.list + pos) : -1;
+      nx1 = pos + 32 < W.L ? __ldg(W.list + pos + 32) : -1;
+    };
+    // map row of a list value; -1 when it holds no entry (an index outside [-1, n_entries)
+    // is reported and left out)
+    auto map_row = [&](int32_t v, bool report) -> int32_t {
+      if (v < 0 || v >= p.n_entries) {
+        if (v != -1 && report) flag_status(p.dev_status, HYB_DEV_BAD_INDEX);
+        return -1;
+      }
+      return (int32_t)(W.b * p.kv_stride + v);
+    };
+    auto signal = [&](int64_t lt) {
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(own ? &full_a[lt % kDA] : &full_b[lt % kDB]);
+    };
+    if (nl > 0) fetch(0);
+    int64_t pend = -1;  // the tile whose copies are in flight and not yet signalled
+    bool ok = true;
+    for (int64_t li = 0; li < ntiles && ok; ++li) {
+      const bool wt = li >= nl;  // a window tile (rows wrow0 + position)
+      int32_t mr_l;  // map row of position 32 part + lane of the tile (-1: none)
+      if (wt) {
+        const int64_t pw = (li - nl) * kT + 32 * part + lane;
+        mr_l = pw < W.wL ? (int32_t)(W.wrow0 + pw) : -1;
+      } else {
+        mr_l = map_row(part ? nx1 : nx0, !own);
+        if (li + 1 < nl) fetch(li + 1);
+      }
+      const char* base = wt ? wbase : kbase;
+      int32_t rows[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) rows[u] = __shfl_sync(0xffffffffu, mr_l, 4 * u + (lane >> 3));
+      const int slot = (int)(li % depth);
+      int okw = 1;
+      if (lane == 0) {
+        okw = tc::mbar_wait(own ? &empty_a[slot] : &empty_b[slot], (uint32_t)((li / depth) & 1) ^ 1u, s_abort, 20);
+        // ring A's slots 1 and 2 hold the staged query rows until they are in TMEM
+        if (okw && own && li == 1) okw = tc::mbar_wait(qlo_ready, 0, s_abort, 21);
+      }
+      if (!(ok = __shfl_sync(0xffffffffu, okw, 0) != 0)) break;
+      const uint32_t dst0 = tc::smem_u32(ring + slot * 4 * kSlab);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int sd = 4 * half + j;  // the slab's 64 dims of the row
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int r = 32 * part + 4 * u + (lane >> 3);
+          const int32_t mr = rows[u];
+          const char* src = base + (int64_t)(mr < 0 ? 0 : mr) * (kC * 2) + sd * 128 + c16 * 16;
+          tc::cp_async16(dst0 + (uint32_t)(j * kSlab + r * 128 + ((c16 ^ (r & 7)) << 4)), src, mr < 0 ? 0u : 16u);
+        }
+      }
+      tc::cp_async_commit();
+      if (pend >= 0) {
+        tc::cp_async_wait_group<1>();
+        signal(pend);
+      }
+      pend = li;
+    }
+    tc::cp_async_wait_group<0>();  // (after an abort too: the copies land before the CTA exits)
+    if (ok && pend >= 0) signal(pend);
+  } else if (warp >= kSoftWarp0 && warp < kWarps8) {
     // ================================================================ softmax + epilogue
     const int q4 = warp & 3;
     const int h = q4 * 32 + lane;  // head (TMEM lane) of this thread
@@ -434,18 +560,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     float m = -INFINITY, l = 0.f;  // reference (log2 units) and denominator of head h
+    // list values of the next list tile at positions lane and 32 + lane (loaded a tile ahead)
+    int32_t nx0 = -1, nx1 = -1;
+    auto fetch = [&](int64_t li_) {
+      const int64_t pos = (W.tb + li_) * kT + lane;
+      nx0 = pos < W.L ? __ldg(W.list + pos) : -1;
+      nx1 = pos + 32 < W.L ? __ldg(W.list + pos + 32) : -1;
+    };
+    if (gathered && nl > 0) fetch(0);
     for (int64_t li = 0; li < ntiles && ok; ++li) {
-      const int64_t i = W.tb + li;
+      const bool wt = li >= nl;
+      const int64_t i = wt ? li - nl : W.tb + li;
       const int b = (int)(li & 1);
       // which of the tile's 64 entries exist
       uint64_t valid;
-      if (contig) {
-        const int64_t n = W.L - i * kT;
+      if (wt || contig) {
+        const int64_t n = (wt ? W.wL : W.L) - i * kT;
         valid = n >= kT ? ~0ull : ((1ull << n) - 1ull);
       } else {
-        const int32_t oob = -1;
-        const bool v0 = h128_row<MODE>(p, W, i * kT + lane, oob, false) != oob;
-        const bool v1 = h128_row<MODE>(p, W, i * kT + 32 + lane, oob, false) != oob;
+        const bool v0 = nx0 >= 0 && nx0 < p.n_entries, v1 = nx1 >= 0 && nx1 < p.n_entries;
+        if (li + 1 < nl) fetch(li + 1);
         valid = (uint64_t)__ballot_sync(0xffffffffu, v0) | ((uint64_t)__ballot_sync(0xffffffffu, v1) << 32);
       }
       if (!(ok = tc::mbar_wait(&s_full[b], (uint32_t)((li >> 1) & 1), s_abort, 8))) break;
@@ -526,9 +660,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // split partial: (m, l) of head h; its O row is written below by all eight warps
       p.part_ml[(W.unit * p.n_split + W.sp) * kH + h] = make_float2(l > 0.f ? m : -INFINITY, l);
     } else if (ok) {
-      // one split (no window): normalised float32 output of this half and the lse
+      // one split: the normalised output of this half (float32 o, or with a window the
+      // merged out in its own type) and the lse
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      float* dst = p.o + (qrow + h) * kC + 256 * W.dh;
+      const int64_t at = (qrow + h) * kC + 256 * W.dh;
+      const bool to_bf16 = p.win && p.out_bf16;
+      float* dst = p.win ? static_cast<float*>(p.out) + at : p.o + at;
+      __nv_bfloat16* dst16 = static_cast<__nv_bfloat16*>(p.out) + at;
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         float v[32];
@@ -539,10 +677,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int y = 0; y < 32; ++y) v[y] = 0.f;
         }
+        if (to_bf16) {
 #pragma unroll
-        for (int x = 0; x < 8; ++x)
-          *reinterpret_cast<float4*>(dst + 32 * c + 4 * x) =
-              make_float4(v[4 * x] * inv, v[4 * x + 1] * inv, v[4 * x + 2] * inv, v[4 * x + 3] * inv);
+          for (int x = 0; x < 4; ++x)
+            *reinterpret_cast<uint4*>(dst16 + 32 * c + 8 * x) =
+                make_uint4(pack_bf16x2(v[8 * x] * inv, v[8 * x + 1] * inv), pack_bf16x2(v[8 * x + 2] * inv, v[8 * x + 3] * inv),
+                           pack_bf16x2(v[8 * x + 4] * inv, v[8 * x + 5] * inv), pack_bf16x2(v[8 * x + 6] * inv, v[8 * x + 7] * inv));
+        } else {
+#pragma unroll
+          for (int x = 0; x < 8; ++x)
+            *reinterpret_cast<float4*>(dst + 32 * c + 4 * x) =
+                make_float4(v[4 * x] * inv, v[4 * x + 1] * inv, v[4 * x + 2] * inv, v[4 * x + 3] * inv);
+        }
       }
       if (W.dh == 0) p.lse[qrow + h] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
     }
@@ -554,11 +700,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (p.n_split > 1) {
     // this split's unnormalised O, bf16, [oct][head][8 dims]: warp w reads TMEM lane quadrant
     // w % 4 (heads 32(w%4) ..) and columns 128 (w / 4) .. 128 (w / 4) + 127
-    if (ntiles > 0 && *s_abort == 0) {
+    if (ntiles > 0 && *s_abort == 0 && warp < kWarps8) {
       bool fine = tc::mbar_wait(fin, 0, s_abort, 10);
       if (fine) {
         tc::tc_fence_after();
-        const int q4 = warp & 3, hh = q4 * 32 + lane, c0 = (warp >> 2) * 4;
+        const int q4 = warp & 3, hh = q4 * 32 + lane, c0 = (warp >> 2) * 4;  // (warps 0-7)
         const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
         __nv_bfloat16* dst = p.part_o + (W.unit * p.n_split + W.sp) * (int64_t)(kOcts * kH * 8);
         float v[2][32];
@@ -696,9 +842,11 @@ struct H128Plan {
 };
 
 // Splits per (query, head group, half): as many as fit one CTA per SM, evened out (the
-// same tiles per split, fewer CTAs); a fused window is one more split, the last.
+// same tiles per split, fewer CTAs); a fused window is one more split, the last.  Launches
+// with more units than that (every unit at least two CTAs, all resident) have one split.
 H128Plan h128_plan(const AttendJob& j) {
   const int64_t units = j.batch * j.n_q * (j.n_h / kH) * 2;
+  if (units * 2 > kNumSMs || units > kMaxJoinUnits) return {1};
   const int w = j.win ? 1 : 0;
   const int64_t T = (h128_list_len_max(j) + kT - 1) / kT;
   int64_t s = kNumSMs / std::max<int64_t>(units, 1) - w;
@@ -724,9 +872,6 @@ bool attend_h128_enabled() {
 bool attend_h128_supported(const AttendJob& j) {
   if (j.mode != 0 && j.mode != 1) return false;
   if (j.dtype != HYB_BF16 || j.c != kC || j.n_h < kH || j.n_h % kH != 0 || j.k != j.v) return false;
-  const int64_t units = j.batch * j.n_q * (j.n_h / kH) * 2;
-  // decode-shaped launches: every unit gets at least two CTAs (and all of them fit the GPU at once)
-  if (units * 2 > kNumSMs || units > kMaxJoinUnits) return false;
   const uintptr_t al = reinterpret_cast<uintptr_t>(j.q) | reinterpret_cast<uintptr_t>(j.k);
   if (al % 16 != 0) return false;
   if (j.batch * j.kv_stride >= (int64_t(1) << 31) - 1 || j.batch * j.n_q * j.n_h >= (int64_t(1) << 31)) return false;
@@ -751,6 +896,8 @@ cudaError_t launch_attend_h128(const AttendJob& j, void* ws, cudaStream_t s) {
   const H128Plan pl = h128_plan(j);
   p.idx = j.idx;
   p.q = static_cast<const __nv_bfloat16*>(j.q);
+  p.kv = static_cast<const __nv_bfloat16*>(j.k);
+  p.wkv = static_cast<const __nv_bfloat16*>(j.wk);
   p.o = j.o, p.lse = j.lse, p.out = j.out, p.out_bf16 = j.out_bf16;
   p.n_q = j.n_q, p.n_h = j.n_h, p.n_entries = j.n_entries, p.kv_stride = j.kv_stride, p.list_len = j.list_len;
   p.m = j.m, p.q_pos0 = j.q_pos0, p.q_pos = j.q_pos;
@@ -765,7 +912,7 @@ cudaError_t launch_attend_h128(const AttendJob& j, void* ws, cudaStream_t s) {
   const int64_t rows = j.batch * j.n_q;
   const int64_t units = rows * p.n_hg * 2;
   if (p.n_split > 1) {
-    if (units > kMaxJoinUnits) return cudaErrorInvalidConfiguration;  // (the support check never allows it)
+    if (units > kMaxJoinUnits) return cudaErrorInvalidConfiguration;  // (the plan never splits those)
     const size_t n = (size_t)units * p.n_split;
     p.join_cnt = static_cast<uint32_t*>(ws);
     p.part_o = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(ws) + kJoinRegionBytes);

@@ -47,6 +47,10 @@ class Workload:
     # parity cases also draw unit-scale rows and larger queries so that outputs are O(1)
     kv_std: float | None = None
     q_std: float = 1.0
+    # grouped output projection: g groups of n_h/g heads, each mapped to d_g features
+    # (16 / 1024 in the Pro configuration, 8 / 1024 in Flash)
+    out_groups: int = 16
+    out_dim: int = 1024
 
     @property
     def n_csa(self) -> int:
@@ -81,9 +85,9 @@ WORKLOADS = {
     "tiny_f32": Workload("tiny_f32", "forward", batch=1, n_ctx=256, n_h=4, c=64, m=4, k=16, n_ih=4, c_I=32, m_hca=16,
                          n_win=16, dtype=torch.float32, seed=1001),
     "flash_csa_decode": Workload("flash_csa_decode", "csa_decode", batch=8, n_ctx=65536, n_h=64, c=512, m=4, k=512,
-                                 n_ih=64, c_I=128, seed=1002),
+                                 n_ih=64, c_I=128, seed=1002, out_groups=8),
     "flash_hca_decode": Workload("flash_hca_decode", "hca_decode", batch=8, n_ctx=262144, n_h=64, c=512, m_hca=128,
-                                 seed=1003),
+                                 seed=1003, out_groups=8),
     "pro_csa_prefill": Workload("pro_csa_prefill", "csa_prefill", batch=1, n_ctx=32768, n_h=128, c=512, m=4, k=1024,
                                 n_ih=64, c_I=128, seed=1004),
     "pro_1m_hybrid_decode": Workload("pro_1m_hybrid_decode", "hybrid_decode", batch=4, n_ctx=1048576, n_h=128, c=512,
@@ -92,7 +96,7 @@ WORKLOADS = {
     "pro_1m_parallel_decode": Workload("pro_1m_parallel_decode", "parallel_decode", batch=4, n_ctx=1048576, n_h=128,
                                        c=512, m=4, k=1024, n_ih=64, c_I=128, m_hca=128, seed=1006),
     # Flash's first layers: sliding window only
-    "flash_swa_decode": Workload("flash_swa_decode", "swa_decode", batch=8, n_ctx=65536, n_h=64, c=512, seed=1007),
+    "flash_swa_decode": Workload("flash_swa_decode", "swa_decode", batch=8, n_ctx=65536, n_h=64, c=512, seed=1007, out_groups=8),
 }
 
 

@@ -227,7 +227,7 @@ def _fused_case(g, B, n_q, n_h, n_kv, c=512):
     (4, 1, 128, 20000, 1024, 128, 80000 - 1, 128, torch.bfloat16),  # decode: the window is one more split
     (2, 1, 64, 3000, 512, 100, 11999, 300, torch.float32),          # window not a tile, float32 out
     (2, 1, 128, 500, 256, 128, 40, 41, torch.bfloat16),              # window cut by the sequence start
-    (1, 80, 128, 4000, 256, 128, 15000, 300, torch.bfloat16),        # too many units to fuse: two steps
+    (1, 80, 128, 4000, 256, 128, 15000, 300, torch.bfloat16),        # many queries: one split, window after the list
 ])
 def test_csa_attend_with_fused_window(B, n_q, n_h, N, k, n_win, q_pos0, n_kv, out_dtype):
     g = _gen(11)
@@ -409,3 +409,60 @@ def test_h128_fused_window_shorter_than_a_tile_or_ragged(q_pos0, n_win):
     rw, rwl = oracle.swa_merge(q, kw, kw, 0, q_pos0, n_win, scale, ro, rl)
     assert_out_close(to_np(out), rw)
     assert max_abs(to_np(lu), rwl) <= TOL_BF16
+
+
+# Launches with many queries (prefill): one CTA per (query, head group, half) over its whole
+# list, the window's tiles after the list's in the same softmax, no join.
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("window", [True, False])
+def test_h128_many_queries_csa_lists_and_window(out_dtype, window):
+    g = _gen(20)
+    B, n_q, n_h, N, k, c, n_win = 2, 40, 128, 3000, 300, 512, 128
+    q0 = 50  # the first queries' windows are cut by the sequence start
+    q = _randn(g, (B, n_q, n_h, c), 2.0)
+    kc = _randn(g, (B, N, c))
+    kv = _randn(g, (B, q0 + n_q, c))
+    idx = torch.sort(torch.randint(0, N, (B, n_q, k), generator=g), dim=-1).values.int()
+    idx[0, 3, -100:] = -1   # ragged list ends
+    idx[1, 7, :] = -1       # an empty list
+    idx[1, 9, 64:192] = -1  # whole tiles of padding
+    scale = 1 / math.sqrt(c)
+    st = _status()
+    o_ref, l_ref = oracle.csa_attend(q, kc, kc, idx.numpy(), scale)
+    if window:
+        out, lse = _ops().csa_attend(q.to(DEV), kc.to(DEV), kc.to(DEV), idx.to(DEV), scale=scale, dev_status=st,
+                                     window=dict(kw=kv.to(DEV), kv_pos0=0, q_pos0=q0, n_win=n_win,
+                                                 out_dtype=out_dtype))
+        o_ref, l_ref = oracle.swa_merge(q, kv, kv, 0, q0, n_win, scale, o_ref, l_ref)
+    else:
+        out, lse = _ops().csa_attend(q.to(DEV), kc.to(DEV), kc.to(DEV), idx.to(DEV), scale=scale, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0, f"device status {st.item()}"
+    assert_out_close(to_np(out), o_ref)
+    assert max_abs(to_np(lse), l_ref) <= TOL_BF16
+    if not window:
+        assert np.all(to_np(out)[1, 7] == 0) and np.all(np.isneginf(to_np(lse)[1, 7]))
+
+
+@pytest.mark.parametrize("m,n_win", [(4, 128), (16, 100)])
+def test_h128_many_queries_hca_prefill_chunk(m, n_win):
+    """A prefill chunk from position 0: every query sees its own number of entries (none for
+    the first m - 1, ragged last tiles) and a window cut by the chunk start."""
+    g = _gen(21)
+    B, n_q, n_h, c = 1, 300, 128, 512
+    N = n_q // m
+    q = _randn(g, (B, n_q, n_h, c), 2.0)
+    kc = _randn(g, (B, N, c))
+    kv = _randn(g, (B, n_q, c))
+    scale = 1 / math.sqrt(c)
+    st = _status()
+    out, lse = _ops().hca_attend(q.to(DEV), kc.to(DEV), kc.to(DEV), m=m, q_pos0=0, scale=scale, dev_status=st,
+                                 window=dict(kw=kv.to(DEV), kv_pos0=0, n_win=n_win))
+    torch.cuda.synchronize()
+    assert st.item() == 0, f"device status {st.item()}"
+    o, l = oracle.hca_attend(q, kc, kc, m=m, q_pos0=0, scale=scale)
+    ro, rl = oracle.swa_merge(q, kv, kv, 0, 0, n_win, scale, o, l)
+    assert_out_close(to_np(out), ro)
+    assert max_abs(to_np(lse), rl) <= TOL_BF16
