@@ -105,7 +105,13 @@ def stage_model(w, proj=None):
 # (dram__bytes_read.sum + dram__bytes_write.sum) on a workload with the current
 # build of that kernel; absent where no capture of the current kernel exists
 KERNEL_NCU_TRAFFIC = {
-    ("pro_1m_hybrid_decode", "index_scores"): 138_501_376 + 5_097_984,
+    ("pro_1m_hybrid_decode", "csa_attend"): 5_348_096,
+    ("pro_1m_hybrid_decode", "hca_attend"): 34_682_624 + 52_736,
+    ("pro_1m_hybrid_decode", "topk"): 4_410_368,
+    ("pro_1m_hybrid_decode", "csa_compress"): 101_632 + 42_752,
+    ("pro_1m_hybrid_decode", "hca_compress"): 1_330_432,
+    # the stage's two projections (one per layer), 137.9 MB each
+    ("pro_1m_hybrid_decode", "proj"): 2 * (134_834_176 + 3_063_552),
 }
 
 
