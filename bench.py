@@ -524,8 +524,13 @@ def run_ours(args, w):
 
     res, steps, stream = measure_workload(args, w, dev, dist, rank, world)
     units = w.batch if w.decode else w.n_ctx
-    # -------- e2e through the public API: fresh inputs from pinned host memory
-    e2e = run_e2e(args, w, steps[0], stream, units, world, dist)
+    # -------- e2e through the public API: fresh inputs from pinned host memory.  For the
+    # hybrid decode: the session, one token per sequence per step (the serving loop); the
+    # snapshot step with its whole block tails and windows re-sent is reported beside it.
+    e2e_snap = run_e2e(args, w, steps[0], stream, units, world, dist)
+    e2e = e2e_snap
+    if w.kind == "hybrid_decode":
+        e2e = run_e2e_session(args, w, stream, world, dist)
     out = {
         "metric": METRIC,
         "value": res["value"],
@@ -542,6 +547,7 @@ def run_ours(args, w):
         "config": res["config"],
         "clocks": res["clocks"],
         "e2e": e2e,
+        "e2e_snapshot_step": e2e_snap if e2e is not e2e_snap else None,
         "gpu_launches": res["gpu_launches"],
         "roofline": res["roofline"],
         "kernels": res["kernels"],
@@ -576,21 +582,16 @@ def run_ours(args, w):
     return out if rank == 0 else None
 
 
-def run_session(w, stream, tokens=128, reps=5):
-    """Token-by-token decode through session.DecodeSession at the workload's context:
-    the `tokens` positions ending at the workload's query position (every m-th token
-    completes a CSA block, the last one an HCA block).  The caches before them hold
-    seeded random entries (as the decode workload's), each token's appends and step are
-    captured as one CUDA graph, and the graphs are replayed in order `reps` times
-    between CUDA events.  The appends are torch copies into the rings (a model's
-    projections would write there directly)."""
+def _make_session(w, tokens, dev):
+    """A DecodeSession at the workload's context, with the caches before the `tokens`
+    positions ending at the workload's query position holding seeded random entries (as
+    the decode workload's), and each of those tokens' rows and queries (device tensors)."""
     import math
 
     import torch
 
     from sparse_attention_gated_b300 import session
 
-    dev = torch.device("cuda")
     g = torch.Generator(device=dev)
     g.manual_seed(w.seed + 7)
     Bq, c, cI = w.batch, w.c, w.c_I
@@ -617,6 +618,23 @@ def run_session(w, stream, tokens=128, reps=5):
                 w=torch.rand(Bq, w.n_ih, generator=g, device=dev)) for _ in range(tokens)]
     s.t = t0
     s.reserve(t_end - 1)
+    return s, rows, inp, t0
+
+
+def run_session(w, stream, tokens=128, reps=5):
+    """Token-by-token decode through session.DecodeSession at the workload's context:
+    the `tokens` positions ending at the workload's query position (every m-th token
+    completes a CSA block, the last one an HCA block).  The caches before them hold
+    seeded random entries (as the decode workload's), each token's appends and step are
+    captured as one CUDA graph, and the graphs are replayed in order `reps` times
+    between CUDA events.  The appends are torch copies into the rings (a model's
+    projections would write there directly)."""
+    import torch
+
+    dev = torch.device("cuda")
+    s, rows, inp, t0 = _make_session(w, tokens, dev)
+    t_end = t0 + tokens
+    Bq = w.batch
     with torch.cuda.stream(stream):
         for i in range(tokens):  # one eager pass (first launches, same writes as the replays)
             s.append(rows[i])
@@ -648,6 +666,109 @@ def run_session(w, stream, tokens=128, reps=5):
             "positions": [t0, t_end - 1], "csa_blocks_completed": tokens // w.m,
             "hca_blocks_completed": tokens // w.m_hca, "reps": reps,
             "graph": "one CUDA graph per token (appends + step), replayed in order"}
+
+
+def run_e2e_session(args, w, stream, world, dist, tokens=128):
+    """The decode metric end to end through the public API as a serving loop runs it:
+    DecodeSession token by token at the workload's context (4 sequences, positions
+    n_ctx - tokens .. n_ctx - 1), every step copying in from pinned host memory only what
+    one token brings (each sequence's raw rows of the token for every stream, its queries,
+    indexer queries, scales and head weights: one packed buffer) and copying both layers'
+    outputs back.  Host-to-device copies on one stream, device-to-host on another, two
+    sets of step buffers, so that a token's copies overlap the neighbouring tokens'
+    compute; the `tokens` steps are captured as one CUDA graph and replayed between CUDA
+    events."""
+    import torch
+
+    dev = stream.device
+    s, rows, inp, t0 = _make_session(w, tokens, dev)
+    B = w.batch
+    # the packed layout of one token's inputs (256-byte aligned fields)
+    fields = [(k, v) for k, v in rows[0].items()] + [(k, inp[0][k]) for k in ("q", "q_h", "qI", "qI_scale", "w")]
+    layout, off = [], 0
+    for k, v in fields:
+        n = v.numel() * v.element_size()
+        layout.append((k, off, n, v.dtype, tuple(v.shape)))
+        off = (off + n + 255) // 256 * 256
+    nbytes = off
+    host_in = torch.empty((tokens, nbytes), dtype=torch.uint8, pin_memory=True)
+    for i in range(tokens):
+        src = dict(rows[i], **inp[i])
+        for k, o, n, dt, shp in layout:
+            host_in[i, o:o + n].view(dt).copy_(src[k].reshape(-1).cpu())
+    dev_in = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    view = [{k: d[o:o + n].view(dt).view(shp) for k, o, n, dt, shp in layout} for d in dev_in]
+    out_shape = (2, B, 1, w.n_h, w.c)
+    dev_out = [torch.empty(out_shape, dtype=s.dtype, device=dev) for _ in range(2)]
+    host_out = [torch.empty(out_shape, dtype=s.dtype, pin_memory=True) for _ in range(2)]
+    d2h = dev_out[0].numel() * dev_out[0].element_size()
+    row_names = list(rows[0].keys())
+    s_h2d, s_d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def steps(n):
+        s.t = t0
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        s_h2d.wait_event(fork)
+        s_d2h.wait_event(fork)
+        freed = [None, None]
+        for i in range(n):
+            b = i % 2
+            if freed[b] is not None:
+                s_h2d.wait_event(freed[b])
+                stream.wait_event(freed[b])
+            with torch.cuda.stream(s_h2d):
+                dev_in[b].copy_(host_in[i], non_blocking=True)
+            e_in = torch.cuda.Event()
+            e_in.record(s_h2d)
+            stream.wait_event(e_in)
+            f = view[b]
+            with torch.cuda.stream(stream):
+                s.out, s.out_h = dev_out[b][0], dev_out[b][1]
+                s.append({k: f[k] for k in row_names})
+                s.step(q=f["q"], qI=f["qI"], qI_scale=f["qI_scale"], w=f["w"], q_h=f["q_h"], stream=stream)
+            e_done = torch.cuda.Event()
+            e_done.record(stream)
+            s_d2h.wait_event(e_done)
+            with torch.cuda.stream(s_d2h):
+                host_out[b].copy_(dev_out[b], non_blocking=True)
+            freed[b] = torch.cuda.Event()
+            freed[b].record(s_d2h)
+        for sx in (s_h2d, s_d2h):  # join
+            j = torch.cuda.Event()
+            j.record(sx)
+            stream.wait_event(j)
+
+    with torch.cuda.stream(stream):
+        steps(tokens)  # eager pass: first launches and workspaces
+    torch.cuda.synchronize()
+    if s.dev_status.item() != 0:
+        raise RuntimeError(f"session e2e: device status {s.dev_status.item()}")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            steps(tokens)
+        g.replay()
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(1, args.steps // tokens) if args.steps > tokens else 1
+    with torch.cuda.stream(stream):
+        s0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        s1.record(stream)
+    torch.cuda.synchronize()
+    if s.dev_status.item() != 0:
+        raise RuntimeError(f"session e2e: device status {s.dev_status.item()}")
+    ms = max_over_ranks(s0.elapsed_time(s1), dist, dev) / (reps * tokens)
+    return {"value": job_rate(B, world, ms), "unit": "queries/s", "h2d_bytes_per_step": nbytes,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "path": "DecodeSession token by token (public API): per step one token's rows and queries per "
+                    f"sequence in, both layers' outputs out; positions {t0}..{t0 + tokens - 1} "
+                    f"({tokens // w.m} CSA and {tokens // w.m_hca} HCA blocks completed)",
+            "graph": f"{tokens} token steps with their copies captured as one CUDA graph",
+            "copies": "one H2D (packed token inputs) and one D2H (out, out_h) per step, on their own streams, "
+                      "double-buffered so copies overlap the neighbouring steps' compute"}
 
 
 def _ridge(peaks, dt):
