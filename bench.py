@@ -92,6 +92,10 @@ def stage_model(w, proj=None):
                                    flops=pairs * w.n_ih * w.c_I * 2, flop_dtype="fp8")
         m["csa_attend"] = dict(bytes=n * H * c * (bf + bf) + N * c * bf + n * w.k * 4 + n * c * bf,
                                flops=(sel + win) * H * c * 4, flop_dtype="bf16")
+    if w.decode and "csa_compress" in m and "hca_compress" in m:
+        # decode steps with both layers compress in one launch (hyb_compress_batch)
+        cm = [m.pop(k) for k in ("csa_compress", "hca_compress") if k in m]
+        m = dict(compress=dict(bytes=sum(v["bytes"] for v in cm), flops=0), **m)
     if proj is not None:
         rows = B * w.n_q
         K = proj["in_heads"] * c // proj["g"]
@@ -108,8 +112,6 @@ KERNEL_NCU_TRAFFIC = {
     ("pro_1m_hybrid_decode", "csa_attend"): 5_348_096,
     ("pro_1m_hybrid_decode", "hca_attend"): 34_682_624 + 52_736,
     ("pro_1m_hybrid_decode", "topk"): 4_410_368,
-    ("pro_1m_hybrid_decode", "csa_compress"): 101_632 + 42_752,
-    ("pro_1m_hybrid_decode", "hca_compress"): 1_330_432,
     # the stage's two projections (one per layer), 137.9 MB each
     ("pro_1m_hybrid_decode", "proj"): 2 * (134_834_176 + 3_063_552),
 }
@@ -146,6 +148,7 @@ def stage_kernels(w):
     att = "attend_h128_kernel" if (w.decode and w.n_h % 128 == 0) else "attend_tc_kernel"
     return {
         "swa": f"{att}<2> (swa_merge, window only)",
+        "compress": "compress_batch_kernel (the step's compressions in one launch)",
         "proj": "out_proj_kernel (grouped output projection)",
         "csa_compress": "compress_kernel x2 (CSA entry bf16 + indexer key e4m3)",
         "csa_attend": f"{att}<0> (csa_attend, window fused)",
@@ -353,7 +356,7 @@ def measure_workload(args, w, dev, dist=None, rank=0, world=1, steps_k=None, pro
         # one forward step; ev: dict stage -> (start, end) events recorded around each stage
         # (and "index_scores" -> the events the library records around its scoring kernel)
         def rec(name, which):
-            if ev is not None:
+            if ev is not None and name in ev:
                 ev[name][which].record(stream)
 
         if ev is None:  # the headline graph: the library's launches, as HybridStep.run issues them
@@ -363,6 +366,10 @@ def measure_workload(args, w, dev, dist=None, rank=0, world=1, steps_k=None, pro
             rec("swa", 0)
             st.run_swa(stream)
             rec("swa", 1)
+        if "compress" in ev:
+            rec("compress", 0)
+            st.run_compress(stream)
+            rec("compress", 1)
         if st.has_csa:
             rec("csa_compress", 0)
             _csa_parts(st, stream, rec, ev["index_scores"])
@@ -776,14 +783,17 @@ def _ridge(peaks, dt):
 
 
 def _csa_parts(st, stream, rec, scoring_events=None):
-    """The CSA layer's ABI calls with stage events between them (same calls as HybridStep.run_csa);
-    scoring_events: (begin, end) events the library records around its scoring kernel."""
+    """The CSA layer's ABI calls with stage events between them (same calls as HybridStep.run
+    issues; decode steps compressed before, in one launch); scoring_events: (begin, end)
+    events the library records around its scoring kernel."""
     from sparse_attention_gated_b300 import ops
 
     w, x, b = st.w, st.x, st.buf
     kc, kI, kIs = st._csa_tensors()
     s = st.dev_status
-    if w.decode:
+    if w.decode and st.has_hca:
+        pass  # compressed before, in one launch with the HCA entry
+    elif w.decode:
         N = w.n_csa
         ops.hyb_compress(x["ca"], x["za"], x["bias"], w.m, cb=x["cb"], zb=x["zb"], overlap=True, first_block=N - 2,
                          out=kc, out_row0=N - 1, dev_status=s, stream=stream)
@@ -813,9 +823,10 @@ def _hca_parts(st, stream, rec):
     s = st.dev_status
     kc = st._hca_cache()
     q = st._hca_q_kv()[0]
-    Nh = w.n_hca
-    ops.hyb_compress(x["ch"], x["zh"], x["bias_h"], w.m_hca, first_block=Nh - 1, out=kc, out_row0=Nh - 1,
-                     dev_status=s, stream=stream)
+    if not st.has_csa:  # (with a CSA layer too, compressed before in one launch)
+        Nh = w.n_hca
+        ops.hyb_compress(x["ch"], x["zh"], x["bias_h"], w.m_hca, first_block=Nh - 1, out=kc, out_row0=Nh - 1,
+                         dev_status=s, stream=stream)
     rec("hca_compress", 1)
     rec("hca_attend", 0)
     ops.hca_attend(q, kc, kc, m=w.m_hca, q_pos0=w.q_pos0, scale=w.scale, o=b["o_h"], lse=b["lse_h"],
@@ -827,12 +838,18 @@ def _launches_per_step(w, proj=None):
     n = 0
     if w.kind == "swa_decode":
         n += 1
+    if w.kind in ("hybrid_decode", "parallel_decode"):
+        n += 1  # the step's three compressions, one launch
+    if w.kind == "csa_decode":
+        n += 2  # the entry and its indexer key
+    if w.kind == "hca_decode":
+        n += 1
     if w.kind in ("hybrid_decode", "csa_decode", "parallel_decode"):
-        n += 2 + 2 + 1  # compress x2, index scores + top-k, attention with the window merge fused
+        n += 2 + 1  # index scores + top-k, attention with the window merge fused
     if w.kind == "csa_prefill":
         n += 2 + 2 + 1  # compress x2, index scores + top-k, attention with the window merge fused
     if w.kind in ("hybrid_decode", "hca_decode", "parallel_decode"):
-        n += 1 + 1
+        n += 1
     if proj is not None:
         n += proj["calls"]
     return n

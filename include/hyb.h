@@ -146,6 +146,15 @@ HYB_API int64_t hyb_compress_out_count(int64_t n_rows, int64_t m, int32_t overla
 HYB_API size_t hyb_compress_workspace_size(const hyb_compress_args* a);
 HYB_API hyb_status hyb_compress(const hyb_compress_args* a, void* workspace, size_t ws_bytes, void* stream);
 
+/* hyb_compress_batch -- up to HYB_COMPRESS_BATCH_MAX independent compressions in one launch:
+ * each calls[i] computes exactly what hyb_compress(&calls[i], ...) computes (the entries
+ * that complete at one decode step: the CSA entry, its indexer key and the HCA entry).
+ * calls: host array of n_calls argument structs (read during the call only), all with the
+ * same in_dtype; each is validated as hyb_compress validates it and nothing is launched if
+ * one fails.  The calls must not write what another call reads.  No workspace. */
+#define HYB_COMPRESS_BATCH_MAX 4
+HYB_API hyb_status hyb_compress_batch(const hyb_compress_args* calls, int32_t n_calls, void* stream);
+
 /* ------------------------------------------------------------------------
  * csa_index_topk -- lightning indexer scores and top-k selection
  * ([HA] V.2: I[t,s] = sum_h w[t,h] * ReLU(q_I[t,h] . K_I[s]); keep the top-k;

@@ -75,6 +75,7 @@ SIGNATURES = {
     "hyb_compress_out_count": (_i64, [_i64, _i64, _i32, _i64]),
     "hyb_compress_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(CompressArgs)]),
     "hyb_compress": (ctypes.c_int, [ctypes.POINTER(CompressArgs), _p, ctypes.c_size_t, _p]),
+    "hyb_compress_batch": (ctypes.c_int, [ctypes.POINTER(CompressArgs), ctypes.c_int32, _p]),
     "csa_index_topk_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(IndexArgs)]),
     "csa_index_topk_counter_bytes": (ctypes.c_size_t, []),
     "csa_index_topk": (ctypes.c_int, [ctypes.POINTER(IndexArgs), _p, ctypes.c_size_t, _p]),

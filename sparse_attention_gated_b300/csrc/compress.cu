@@ -16,6 +16,10 @@
 // The R partial states (max, denominator, numerator) are merged by a tree in
 // shared memory.  E4M3 output needs the whole entry for its scale (amax/448),
 // so it keeps S = c.
+//
+// A batch of up to kCompressBatchMax compressions (the entries that complete at one decode
+// step in the CSA layer, its indexer keys and the HCA layer) runs as one launch: CTA
+// ranges per call, 256 threads, each call with its own S and R.
 #include "kernels.cuh"
 
 namespace hyb {
@@ -38,21 +42,20 @@ constexpr int kCv = 4;           // channels per thread
 constexpr int kRowBatch = 4;     // rows loaded at once per thread
 constexpr int kCompressThreads = 256;
 
-// OUT: 0 = float32, 1 = bf16, 2 = e4m3 + per-entry scale
+// One CTA's work: entry bj of the call (b * n_out + j), channel slab `slab`.  OUT: 0 =
+// float32, 1 = bf16, 2 = e4m3 + per-entry scale.  Threads past the call's G x R (a batch
+// launch sizes its CTAs for the largest call) accumulate nothing.
 template <typename Tin, int OUT>
-__global__ void __launch_bounds__(kCompressThreads) compress_kernel(CompressParams p) {
-  extern __shared__ float sm[];  // [3][R][S]: max, denominator, numerator of each row group
-  __shared__ float s_red[kCompressThreads / 32];
-  pdl_wait();
-  pdl_trigger();
+__device__ __forceinline__ void compress_cta(const CompressParams& p, int64_t bj, int64_t slab, float* sm,
+                                             float* s_red) {
   const int64_t c = p.c, m = p.m;
   const int G = p.S / kCv;
   const int g = threadIdx.x % G, rg = threadIdx.x / G;
-  const int64_t bj = blockIdx.x;
+  const bool live = rg < p.R;
   const int64_t b = bj / p.n_out, j = bj % p.n_out;
   const int64_t lb = j + p.skip;  // block index within the rows passed in
   const bool has_prev = p.overlap && p.first_block + lb > 0;
-  const int64_t ch0 = (int64_t)blockIdx.y * p.S + g * kCv;
+  const int64_t ch0 = slab * p.S + g * kCv;
   const int W = (int)(p.overlap ? 2 * m : m);
   const int64_t base = b * p.in_batch_stride;
   const Tin* ca = static_cast<const Tin*>(p.ca);
@@ -64,7 +67,7 @@ __global__ void __launch_bounds__(kCompressThreads) compress_kernel(CompressPara
 #pragma unroll
   for (int i = 0; i < kCv; ++i) mx[i] = -INFINITY, den[i] = 0.f, num[i] = 0.f;
 
-  for (int pos0 = rg; pos0 < W; pos0 += kRowBatch * p.R) {
+  for (int pos0 = rg; live && pos0 < W; pos0 += kRowBatch * p.R) {
     float lg[kRowBatch][kCv], cv[kRowBatch][kCv];
     bool have[kRowBatch];
 #pragma unroll
@@ -163,8 +166,43 @@ __global__ void __launch_bounds__(kCompressThreads) compress_kernel(CompressPara
   }
 }
 
+template <typename Tin, int OUT>
+__global__ void __launch_bounds__(kCompressThreads) compress_kernel(CompressParams p) {
+  extern __shared__ float sm[];  // [3][R][S]: max, denominator, numerator of each row group
+  __shared__ float s_red[kCompressThreads / 32];
+  pdl_wait();
+  pdl_trigger();
+  compress_cta<Tin, OUT>(p, blockIdx.x, blockIdx.y, sm, s_red);
+}
+
+struct CompressBatch {
+  CompressParams call[kCompressBatchMax];
+  int out[kCompressBatchMax];        // OUT of each call
+  int64_t cta_end[kCompressBatchMax];  // CTAs of calls 0..i
+  int64_t slabs[kCompressBatchMax];    // c / S of each call
+  int n;
+};
+
 template <typename Tin>
-static cudaError_t launch_t(CompressParams& p, int out_dtype, cudaStream_t s) {
+__global__ void __launch_bounds__(kCompressThreads) compress_batch_kernel(const __grid_constant__ CompressBatch B) {
+  extern __shared__ float sm[];
+  __shared__ float s_red[kCompressThreads / 32];
+  pdl_wait();
+  pdl_trigger();
+  int i = 0;
+  while (i + 1 < B.n && (int64_t)blockIdx.x >= B.cta_end[i]) ++i;
+  const int64_t local = (int64_t)blockIdx.x - (i ? B.cta_end[i - 1] : 0);
+  const int64_t bj = local / B.slabs[i], slab = local % B.slabs[i];
+  switch (B.out[i]) {  // (the same for every thread of the CTA)
+    case 0: compress_cta<Tin, 0>(B.call[i], bj, slab, sm, s_red); break;
+    case 1: compress_cta<Tin, 1>(B.call[i], bj, slab, sm, s_red); break;
+    default: compress_cta<Tin, 2>(B.call[i], bj, slab, sm, s_red); break;
+  }
+}
+
+// S and R of one call: S halves (from c, down to 16) until the call has at least two CTAs
+// per SM (e4m3 output keeps the whole entry in one CTA); R doubles while it fits.
+static void shape_call(CompressParams& p, int out_dtype) {
   const int W = (int)(p.overlap ? 2 * p.m : p.m);
   int S = (int)p.c;
   if (out_dtype != HYB_E4M3)
@@ -173,6 +211,12 @@ static cudaError_t launch_t(CompressParams& p, int out_dtype, cudaStream_t s) {
   int R = 1;
   while (2 * R <= W && 2 * R * G <= kCompressThreads) R <<= 1;
   p.S = S, p.R = R;
+}
+
+template <typename Tin>
+static cudaError_t launch_t(CompressParams& p, int out_dtype, cudaStream_t s) {
+  shape_call(p, out_dtype);
+  const int S = p.S, R = p.R, G = S / kCv;
   const size_t smem = (size_t)3 * R * S * sizeof(float);
   const dim3 grid((unsigned)(p.batch * p.n_out), (unsigned)(p.c / S)), block((unsigned)(G * R));
   cudaError_t e;
@@ -192,7 +236,7 @@ static cudaError_t launch_t(CompressParams& p, int out_dtype, cudaStream_t s) {
 
 bool compress_shape_supported(int64_t c) { return c == 32 || c == 64 || c == 128 || c == 256 || c == 512; }
 
-cudaError_t launch_compress(const hyb_compress_args* a, int64_t n_out, cudaStream_t s) {
+static CompressParams make_params(const hyb_compress_args* a, int64_t n_out) {
   CompressParams p;
   p.ca = a->ca, p.cb = a->cb, p.za = a->za, p.zb = a->zb, p.bias = a->bias, p.out = a->out, p.out_scale = a->out_scale;
   p.batch = a->batch, p.n_rows = a->n_rows, p.c = a->c, p.m = a->m, p.first_block = a->first_block;
@@ -202,10 +246,46 @@ cudaError_t launch_compress(const hyb_compress_args* a, int64_t n_out, cudaStrea
   p.skip = (a->overlap && a->first_block > 0) ? 1 : 0;
   p.overlap = a->overlap;
   p.S = (int)a->c, p.R = 1;
+  return p;
+}
+
+cudaError_t launch_compress(const hyb_compress_args* a, int64_t n_out, cudaStream_t s) {
+  CompressParams p = make_params(a, n_out);
   if (n_out == 0 || p.batch == 0) return cudaSuccess;
   if (p.batch * n_out >= (int64_t(1) << 31) - 1) return cudaErrorInvalidConfiguration;
   if (a->in_dtype == HYB_F32) return launch_t<float>(p, a->out_dtype, s);
   return launch_t<__nv_bfloat16>(p, a->out_dtype, s);
+}
+
+// calls with no output are left out; all calls have the same input type (checked by the caller)
+cudaError_t launch_compress_batch(const hyb_compress_args* const* a, const int64_t* n_out, int n, cudaStream_t s) {
+  CompressBatch B{};
+  size_t smem = 0;
+  int64_t ctas = 0;
+  for (int i = 0; i < n; ++i) {
+    if (n_out[i] == 0 || a[i]->batch == 0) continue;
+    CompressParams p = make_params(a[i], n_out[i]);
+    if (p.batch * n_out[i] >= (int64_t(1) << 31) - 1) return cudaErrorInvalidConfiguration;
+    shape_call(p, a[i]->out_dtype);
+    const int k = B.n++;
+    B.call[k] = p;
+    B.out[k] = a[i]->out_dtype == HYB_F32 ? 0 : a[i]->out_dtype == HYB_BF16 ? 1 : 2;
+    B.slabs[k] = p.c / p.S;
+    ctas += p.batch * n_out[i] * B.slabs[k];
+    B.cta_end[k] = ctas;
+    smem = std::max(smem, (size_t)3 * p.R * p.S * sizeof(float));
+  }
+  if (B.n == 0) return cudaSuccess;
+  if (ctas >= (int64_t(1) << 31)) return cudaErrorInvalidConfiguration;
+  const bool f32 = a[0]->in_dtype == HYB_F32;
+  cudaError_t e = f32 ? cudaFuncSetAttribute(compress_batch_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
+                      : cudaFuncSetAttribute(compress_batch_kernel<__nv_bfloat16>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  e = f32 ? launch_pdl(compress_batch_kernel<float>, dim3((unsigned)ctas), dim3(kCompressThreads), smem, s, B)
+          : launch_pdl(compress_batch_kernel<__nv_bfloat16>, dim3((unsigned)ctas), dim3(kCompressThreads), smem, s, B);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 }  // namespace hyb

@@ -155,6 +155,25 @@ hyb_status hyb_compress(const hyb_compress_args* a, void*, size_t, void* stream)
   return cuda_status(hyb::launch_compress(a, n_out, static_cast<cudaStream_t>(stream)), "hyb_compress launch");
 }
 
+hyb_status hyb_compress_batch(const hyb_compress_args* calls, int32_t n_calls, void* stream) {
+  static_assert(HYB_COMPRESS_BATCH_MAX == hyb::kCompressBatchMax, "batch size");
+  if (n_calls < 0 || n_calls > HYB_COMPRESS_BATCH_MAX)
+    return fail(HYB_ERR_INVALID_ARG, "hyb_compress_batch: n_calls = %d outside 0..%d", n_calls, HYB_COMPRESS_BATCH_MAX);
+  if (n_calls > 0 && !calls) return fail(HYB_ERR_INVALID_ARG, "hyb_compress_batch: calls is NULL");
+  const hyb_compress_args* ptr[HYB_COMPRESS_BATCH_MAX];
+  int64_t n_out[HYB_COMPRESS_BATCH_MAX];
+  for (int i = 0; i < n_calls; ++i) {
+    hyb_status st = validate_compress(&calls[i], &n_out[i]);
+    if (st != HYB_OK) return st;
+    if (calls[i].in_dtype != calls[0].in_dtype)
+      return fail(HYB_ERR_INVALID_ARG, "hyb_compress_batch: calls %d and 0 have different in_dtype", i);
+    ptr[i] = &calls[i];
+  }
+  if (n_calls == 0) return ok();
+  return cuda_status(hyb::launch_compress_batch(ptr, n_out, n_calls, static_cast<cudaStream_t>(stream)),
+                     "hyb_compress_batch launch");
+}
+
 // ---------------------------------------------------------------- index + top-k
 
 static size_t index_scores_bytes(const hyb_index_args* a) {

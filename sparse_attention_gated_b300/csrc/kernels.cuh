@@ -29,6 +29,9 @@ long long grid_wait_cycles();
 // compress.cu
 bool compress_shape_supported(int64_t c);
 cudaError_t launch_compress(const hyb_compress_args* a, int64_t n_out, cudaStream_t s);
+constexpr int kCompressBatchMax = 4;
+// Several compressions in one launch (n <= kCompressBatchMax, one input type).
+cudaError_t launch_compress_batch(const hyb_compress_args* const* a, const int64_t* n_out, int n, cudaStream_t s);
 
 // norm_rope.cu
 cudaError_t launch_norm_rope(const hyb_norm_rope_args* a, cudaStream_t s);

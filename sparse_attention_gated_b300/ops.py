@@ -133,6 +133,18 @@ def hyb_compress(ca, za, bias, m: int, *, cb=None, zb=None, overlap: bool = Fals
     return out, out_scale
 
 
+def compress_call(a, stream=None):
+    """hyb_compress on an argument struct from compress_args."""
+    _abi.check(_abi.load().hyb_compress(ctypes.byref(a), None, 0, _stream(stream)), "hyb_compress")
+
+
+def hyb_compress_batch(calls, stream=None):
+    """Several compressions in one launch (hyb_compress_batch): calls is a list of argument
+    structs from compress_args (each with its out given), at most HYB_COMPRESS_BATCH_MAX."""
+    arr = (_abi.CompressArgs * max(1, len(calls)))(*calls)
+    _abi.check(_abi.load().hyb_compress_batch(arr, len(calls), _stream(stream)), "hyb_compress_batch")
+
+
 # ------------------------------------------------------------- index + top-k
 
 

@@ -292,19 +292,24 @@ class DecodeSession:
         t, m, mh, st = self.t, self.m, self.m_hca, self.dev_status
         if t >= self.n_max:
             raise ValueError("session is full")
+        calls = []  # the entries this token completes, compressed in one launch
         if (t + 1) % m == 0:
             i = (t + 1) // m - 1
             start, rows, fb, row0 = self.csa_block_view(i, m)
             tl = {s: self.ring(s)[:, start:start + rows] for s in _CSA_STREAMS + _IDX_STREAMS}
-            ops.hyb_compress(tl["ca"], tl["za"], self.bias, m, cb=tl["cb"], zb=tl["zb"], overlap=True,
-                             first_block=fb, out=self.csa_kc, out_row0=row0, dev_status=st, stream=stream)
-            ops.hyb_compress(tl["kIa"], tl["zIa"], self.biasI, m, cb=tl["kIb"], zb=tl["zIb"], overlap=True,
-                             first_block=fb, out=self.csa_kI, out_scale=self.csa_kIs, out_row0=row0, dev_status=st,
-                             stream=stream)
+            calls.append(ops.compress_args(tl["ca"], tl["za"], self.bias, m, tl["cb"], tl["zb"], True, fb, self.csa_kc,
+                                           None, dev_status=st, out_row0=row0))
+            calls.append(ops.compress_args(tl["kIa"], tl["zIa"], self.biasI, m, tl["kIb"], tl["zIb"], True, fb,
+                                           self.csa_kI, self.csa_kIs, dev_status=st, out_row0=row0))
         if (t + 1) % mh == 0:
             j = (t + 1) // mh - 1
-            ops.hyb_compress(self.ring("ch")[:, :mh], self.ring("zh")[:, :mh], self.bias_h, mh, first_block=j,
-                             out=self.hca_kc, out_row0=j, dev_status=st, stream=stream)
+            calls.append(ops.compress_args(self.ring("ch")[:, :mh], self.ring("zh")[:, :mh], self.bias_h, mh,
+                                           first_block=j, out=self.hca_kc, dev_status=st, out_row0=j))
+        if len(calls) == 3:  # both layers: one launch (slower than two launches for the CSA pair alone)
+            ops.hyb_compress_batch(calls, stream=stream)
+        else:
+            for a in calls:
+                ops.compress_call(a, stream=stream)
         n_vis = (t + 1) // m
         q1, q1h = q.unsqueeze(1), q_h.unsqueeze(1)
         qI1, qIs1, w1 = qI.unsqueeze(1), qI_scale.unsqueeze(1), w.unsqueeze(1)

@@ -79,6 +79,20 @@ def test_compress_with_nothing_to_do_launches_nothing(lib):
     assert lib.hyb_compress(ctypes.byref(a), None, 0, None) == 0
 
 
+def test_compress_batch_validates_every_call_before_any_launch(lib):
+    arr = (_abi.CompressArgs * 5)(*[_compress_args(n_rows=3) for _ in range(5)])  # nothing to compute
+    assert lib.hyb_compress_batch(arr, 0, None) == 0
+    assert lib.hyb_compress_batch(arr, 4, None) == 0
+    assert lib.hyb_compress_batch(arr, 5, None) == 1  # more than HYB_COMPRESS_BATCH_MAX calls
+    assert lib.hyb_compress_batch(arr, -1, None) == 1
+    assert lib.hyb_compress_batch(None, 2, None) == 1
+    bad = (_abi.CompressArgs * 3)(_compress_args(n_rows=3), _compress_args(n_rows=3, m=0), _compress_args(n_rows=3))
+    assert lib.hyb_compress_batch(bad, 3, None) == 1  # the second call is invalid
+    mixed = (_abi.CompressArgs * 2)(_compress_args(n_rows=3), _compress_args(n_rows=3, in_dtype=_abi.HYB_BF16))
+    assert lib.hyb_compress_batch(mixed, 2, None) == 1
+    assert "in_dtype" in lib.hyb_last_error().decode()
+
+
 def _index_args(**kw):
     a = _abi.IndexArgs()
     a.qI = a.w = a.kI = a.idx = FAKE

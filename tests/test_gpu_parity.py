@@ -4,6 +4,7 @@ Sizes span several tiles and ragged tails; the full-size workloads are
 checked in test_gpu_fullsize.py on sampled rows.  All calls go through the
 C ABI (sparse_attention_gated_b300.ops -> libhyb.so).
 """
+import ctypes
 import math
 
 import numpy as np
@@ -82,6 +83,44 @@ def test_compress_fp8_output_is_the_oracle_quantiser_of_the_float_result(c, B, n
     x = np.abs(ref) / scales[..., None]  # magnitude in code units
     step_code = np.where(x >= 2.0 ** -6, 2.0 ** (np.floor(np.log2(np.maximum(x, 1e-30))) - 3), 2.0 ** -9)
     assert np.all(np.abs(dec - ref) <= step_code * scales[..., None] * 1.0001)
+
+
+def test_compress_batch_equals_the_separate_calls():
+    """The decode step's three compressions in one launch (CSA entry with overlap, its FP8
+    indexer key, HCA entry, written into cache slots) are bit-identical to three
+    hyb_compress calls, and the CSA entry also matches the oracle."""
+    g = _gen(31)
+    B, c, cI, m, mh, N, Nh = 3, 512, 128, 4, 128, 20, 6
+    bf = torch.bfloat16
+    ca, cb, za, zb = (_randn(g, (B, 2 * m, c), std=0.3).to(bf) for _ in range(4))
+    kIa, kIb, zIa, zIb = (_randn(g, (B, 2 * m, cI)).to(bf) for _ in range(4))
+    ch, zh = (_randn(g, (B, mh, c)).to(bf) for _ in range(2))
+    bias, biasI, bias_h = _randn(g, (2 * m, c)), _randn(g, (2 * m, cI)), _randn(g, (mh, c))
+    d = {k: v.to(DEV) for k, v in dict(ca=ca, cb=cb, za=za, zb=zb, kIa=kIa, kIb=kIb, zIa=zIa, zIb=zIb, ch=ch, zh=zh,
+                                        bias=bias, biasI=biasI, bias_h=bias_h).items()}
+    outs = []
+    for batched in (False, True):
+        kc = torch.zeros((B, N, c), dtype=bf, device=DEV)
+        kI = torch.zeros((B, N, cI), dtype=torch.float8_e4m3fn, device=DEV)
+        kIs = torch.zeros((B, N), device=DEV)
+        kh = torch.zeros((B, Nh, c), dtype=bf, device=DEV)
+        calls = [ops.compress_args(d["ca"], d["za"], d["bias"], m, d["cb"], d["zb"], True, N - 2, kc, None,
+                                   out_row0=N - 1),
+                 ops.compress_args(d["kIa"], d["zIa"], d["biasI"], m, d["kIb"], d["zIb"], True, N - 2, kI, kIs,
+                                   out_row0=N - 1),
+                 ops.compress_args(d["ch"], d["zh"], d["bias_h"], mh, first_block=Nh - 1, out=kh, out_row0=Nh - 1)]
+        if batched:
+            ops.hyb_compress_batch(calls)
+        else:
+            lib = ops._abi.load()
+            for a in calls:
+                ops._abi.check(lib.hyb_compress(ctypes.byref(a), None, 0, None), "hyb_compress")
+        torch.cuda.synchronize()
+        outs.append((kc, kI.view(torch.uint8), kIs, kh))
+    for x, y in zip(*outs):
+        assert torch.equal(x, y)
+    ref = oracle.compress(ca, za, bias, m, cb=cb, zb=zb, overlap=True, first_block=N - 2)
+    assert max_abs(to_np(outs[1][0][:, N - 1:]), ref) <= 2.0 ** -7 * max(np.abs(ref).max(), 1e-3)
 
 
 def test_compress_writes_into_a_cache_slot():
