@@ -65,14 +65,15 @@ def stage_model(w, proj=None):
     proj: the step's grouped output projection, {"g", "d_g", "in_heads", "calls"} (None: none)."""
     B, c, H = w.batch, w.c, w.n_h
     bf = 2 if w.dtype.itemsize == 2 else 4
+    kb, qb = _index_row_bytes(w)
     m = {}
     if w.kind == "swa_decode":
         m["swa"] = dict(bytes=B * (w.n_win * c * bf + H * c * bf * 2), flops=B * w.n_win * H * c * 4,
                         flop_dtype="bf16")
     if w.kind in ("hybrid_decode", "csa_decode", "parallel_decode"):
         N = w.n_csa
-        m["csa_compress"] = dict(bytes=B * (4 * 2 * w.m * (c + w.c_I) * bf + c * bf + w.c_I + 4), flops=0)
-        m["csa_index_topk"] = dict(bytes=B * (N * (w.c_I + 4) + w.n_ih * (w.c_I + 8) + w.k * 4),
+        m["csa_compress"] = dict(bytes=B * (4 * 2 * w.m * (c + w.c_I) * bf + c * bf + kb), flops=0)
+        m["csa_index_topk"] = dict(bytes=B * (N * kb + w.n_ih * (qb + 4) + w.k * 4),
                                    flops=B * N * w.n_ih * w.c_I * 2, flop_dtype="fp8")
         # attention over the selected entries with the window merge fused (one call)
         m["csa_attend"] = dict(bytes=B * ((w.k + w.n_win) * c * bf + w.k * 4 + H * c * bf + H * c * bf + H * 4),
@@ -117,6 +118,14 @@ KERNEL_NCU_TRAFFIC = {
 }
 
 
+def _index_row_bytes(w):
+    """Bytes of one indexer key row (with its scales) and of one query head row (with its
+    scales): FP8 c_I + 4 and c_I + 4; MXFP4 c_I/2 + c_I/32 for both."""
+    if w.idx_fmt == "mxfp4":
+        return w.c_I // 2 + w.c_I // 32, w.c_I // 2 + w.c_I // 32
+    return w.c_I + 4, w.c_I + 4
+
+
 def scoring_kernel_model(w):
     """Algorithmic bytes / flops of one launch of the indexer's scoring kernel (its
     inputs read once: the FP8 keys and scales, the queries, scales and head weights)."""
@@ -124,12 +133,13 @@ def scoring_kernel_model(w):
         return None
     n_q = 1 if w.decode else w.n_ctx
     N = w.n_csa
-    qb = w.n_ih * (w.c_I + 8)
+    kb, qrow = _index_row_bytes(w)
+    qb = w.n_ih * (qrow + 4)
     if w.decode:
         pairs = N
     else:
         pairs = sum(min(N, (t + 1) // w.m) for t in range(w.n_ctx))
-    return dict(bytes=w.batch * (N * (w.c_I + 4) + n_q * qb), flops=w.batch * pairs * w.n_ih * w.c_I * 2,
+    return dict(bytes=w.batch * (N * kb + n_q * qb), flops=w.batch * pairs * w.n_ih * w.c_I * 2,
                 flop_dtype="fp8")
 
 
@@ -457,7 +467,9 @@ def measure_workload(args, w, dev, dist=None, rank=0, world=1, steps_k=None, pro
     peaks, peak_kind = args.peaks
     kern = {}
     if has_scoring:
-        kern["index_scores"] = ("index_tc_kernel (csa_index_topk scoring)", scoring_kernel_model(w), scoring_ms)
+        label = ("index_fp4_kernel (csa_index_topk scoring, MXFP4)" if w.idx_fmt == "mxfp4"
+                 else "index_tc_kernel (csa_index_topk scoring)")
+        kern["index_scores"] = (label, scoring_kernel_model(w), scoring_ms)
         kern["topk"] = ("topk_grid_kernel (csa_index_topk selection)", topk_kernel_model(w),
                         stage_ms["csa_index_topk"] - scoring_ms)
     for s_name, label in stage_kernels(w).items():
@@ -504,6 +516,7 @@ EXTRA_CONFIGS = (
     ("flash_swa_decode", None, 20),
     ("pro_1m_parallel_decode", "concat", 20),
     ("pro_1m_hybrid_decode", "per_layer", 20),
+    ("pro_1m_hybrid_decode_fp4", None, 20),
     ("pro_csa_prefill", None, 3),
 )
 
@@ -536,7 +549,7 @@ def run_ours(args, w):
     # snapshot step with its whole block tails and windows re-sent is reported beside it.
     e2e_snap = run_e2e(args, w, steps[0], stream, units, world, dist)
     e2e = e2e_snap
-    if w.kind == "hybrid_decode":
+    if w.kind == "hybrid_decode" and w.idx_fmt == "e4m3":
         e2e = run_e2e_session(args, w, stream, world, dist)
     out = {
         "metric": METRIC,
@@ -564,7 +577,7 @@ def run_ours(args, w):
         "step_hbm_roofline_frac": res["step_hbm_roofline_frac"],
         "step_roofline_frac": res["step_roofline_frac"],
     }
-    if rank == 0 and world == 1 and w.kind == "hybrid_decode" and not args.no_session:
+    if rank == 0 and world == 1 and w.kind == "hybrid_decode" and w.idx_fmt == "e4m3" and not args.no_session:
         out["session"] = run_session(w, stream)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, steps[0])
@@ -942,6 +955,7 @@ def oracle_query(w, x, b, proj=None):
     CPU-baseline unit of work), with the step's grouped output projection when
     proj (the step's matrices, CPU) is given.  x holds CPU tensors."""
     import numpy as np
+    import torch
 
     import oracle
 
@@ -959,9 +973,20 @@ def oracle_query(w, x, b, proj=None):
                         first_block=N - 2)
         kIn = oracle.compress(x["kIa"][sl], x["zIa"][sl], x["biasI"], w.m, cb=x["kIb"][sl], zb=x["zIb"][sl],
                               overlap=True, first_block=N - 2)
-        oracle.quantise_fp8_rows(kIn.astype("float32"))
-        s = oracle.index_scores(x["qI"][sl], x["w"][sl], x["kI"][sl], m=w.m, q_pos0=t, qI_scale=x["qI_scale"][sl],
-                                kI_scale=x["kI_scale"][sl])
+        if w.idx_fmt == "mxfp4":
+            def dec(codes, scales):  # MXFP4 rows decoded by the oracle (element 2i in the low nibble)
+                bts = codes.view(torch.uint8).numpy()
+                un = np.empty(bts.shape[:-1] + (2 * bts.shape[-1],), dtype=np.uint8)
+                un[..., 0::2], un[..., 1::2] = bts & 15, bts >> 4
+                return oracle.mxfp4_decode(un, scales.view(torch.uint8).numpy()).astype(np.float32)
+
+            oracle.quantise_mxfp4_rows(kIn.astype("float32"))
+            s = oracle.index_scores(dec(x["qI"][sl], x["qI_scale"][sl]), x["w"][sl],
+                                    dec(x["kI"][sl], x["kI_scale"][sl]), m=w.m, q_pos0=t)
+        else:
+            oracle.quantise_fp8_rows(kIn.astype("float32"))
+            s = oracle.index_scores(x["qI"][sl], x["w"][sl], x["kI"][sl], m=w.m, q_pos0=t,
+                                    qI_scale=x["qI_scale"][sl], kI_scale=x["kI_scale"][sl])
         idx = oracle.topk(s, [[N]], w.k)
         o, l = oracle.csa_attend(x["q"][sl], x["kc"][sl], x["kc"][sl], idx, w.scale)
         outs.append(oracle.swa_merge(x["q"][sl], x["kv"][sl], x["kv"][sl], w.n_ctx - w.n_win, t, w.n_win, w.scale,

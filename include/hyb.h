@@ -77,7 +77,10 @@ typedef enum hyb_status {
 typedef enum hyb_dtype {
   HYB_F32 = 0,   /* IEEE binary32 */
   HYB_BF16 = 1,  /* bfloat16 (upper half of binary32) */
-  HYB_E4M3 = 2   /* OCP FP8 e4m3 (bias 7, max 448, no inf), one float32 scale per row */
+  HYB_E4M3 = 2,  /* OCP FP8 e4m3 (bias 7, max 448, no inf), one float32 scale per row */
+  HYB_MXFP4 = 3  /* OCP microscaling FP4: e2m1 codes packed two per byte (element 2i in the
+                    low nibble of byte i), one e8m0 scale byte (2^(e-127)) per block of 32
+                    consecutive elements of a row */
 } hyb_dtype;
 
 /* bits OR-ed into *dev_status by the kernels */
@@ -118,7 +121,12 @@ typedef enum hyb_dtype {
  * out_dtype: F32, BF16 (round to nearest even) or E4M3 (per-entry scale
  * written to out_scale[b*out_batch_stride + j]: scale = amax/448 over the
  * entry's c channels, or 1 when amax = 0; code = nearest-even e4m3 of
- * value/scale, saturated to +-448; both divisions IEEE-rounded float32).
+ * value/scale, saturated to +-448; both divisions IEEE-rounded float32), or
+ * MXFP4 (out: c/2 bytes per entry; out_scale, read as uint8*: c/32 e8m0 bytes
+ * per entry at out_scale + (b*out_batch_stride + j)*(c/32); per block of 32
+ * channels E = floor(log2(amax)) - 2 clamped to [-127, 127] (-127 when amax
+ * = 0), scale byte E + 127, code = nearest e2m1 of value * 2^-E, ties to the
+ * even code, saturated to +-6; the decisions taken on the float32 result).
  * Arithmetic: float32 softmax and accumulation.
  * ------------------------------------------------------------------------ */
 typedef struct hyb_compress_args {
@@ -160,9 +168,14 @@ HYB_API hyb_status hyb_compress_batch(const hyb_compress_args* calls, int32_t n_
  * ([HA] V.2: I[t,s] = sum_h w[t,h] * ReLU(q_I[t,h] . K_I[s]); keep the top-k;
  * [DV4] steps 2-3; the indexer runs at reduced precision).
  *
- * qI [batch][n_q][n_ih][c_I] and kI [batch][kv_stride][c_I] are both F32 or
- * both E4M3 (dtype).  With E4M3 the decoded codes are multiplied by
- * qI_scale [batch][n_q][n_ih] and kI_scale [batch][kv_stride] (float32);
+ * qI [batch][n_q][n_ih][c_I] and kI [batch][kv_stride][c_I] are both F32,
+ * both E4M3 or both MXFP4 (dtype).  With E4M3 the decoded codes are
+ * multiplied by qI_scale [batch][n_q][n_ih] and kI_scale [batch][kv_stride]
+ * (float32); with MXFP4 qI and kI hold c_I/2 bytes per row and the scale
+ * pointers, read as uint8*, hold c_I/32 e8m0 bytes per row (qI_scale
+ * [batch][n_q][n_ih][c_I/32], kI_scale [batch][kv_stride][c_I/32]): each
+ * element decodes to its e2m1 value times its block's 2^(e-127) (MXFP4 runs
+ * on the tensor cores only: n_ih = 64, c_I = 128, kv_stride a multiple of 4);
  * with F32 both scale pointers must be NULL.  w [batch][n_q][n_ih] float32.
  * Entries 0..n_entries-1 exist; query j (position t = q_pos0 + j) scores only
  * the visible ones, s < floor((t+1)/m), and floor((q_pos0+n_q)/m) must not
@@ -193,7 +206,7 @@ typedef struct hyb_index_args {
   int64_t m;
   int64_t k;
   int64_t q_pos0;
-  int32_t dtype; /* hyb_dtype: HYB_F32 or HYB_E4M3 */
+  int32_t dtype; /* hyb_dtype: HYB_F32, HYB_E4M3 or HYB_MXFP4 */
   int32_t* dev_status;
   /* Optional profiling events (cudaEvent_t, or NULL): recorded on the stream
      right before and right after the scoring kernel, so that a caller can time

@@ -405,15 +405,18 @@ def grouped_out_proj(o, W, W_out=None) -> np.ndarray:
 
 
 def e2m1_decode(codes) -> np.ndarray:
+    """Values of e2m1 codes (one per byte), each decoded by the C decoder (a table of its 16
+    results, indexed by code)."""
     lib = load()
-    c = np.asarray(codes, dtype=np.uint8).ravel()
-    return np.array([lib.orc_e2m1_decode(int(v)) for v in c]).reshape(np.shape(codes))
+    table = np.array([lib.orc_e2m1_decode(v) for v in range(16)])
+    return table[np.asarray(codes, dtype=np.uint8) & 15]
 
 
 def e8m0_decode(codes) -> np.ndarray:
+    """Values of e8m0 scale bytes, each decoded by the C decoder (a table of its 256 results)."""
     lib = load()
-    c = np.asarray(codes, dtype=np.uint8).ravel()
-    return np.array([lib.orc_e8m0_decode(int(v)) for v in c]).reshape(np.shape(codes))
+    table = np.array([lib.orc_e8m0_decode(v) for v in range(256)])
+    return table[np.asarray(codes, dtype=np.uint8)]
 
 
 def e2m1_encode(x) -> np.ndarray:

@@ -11,7 +11,7 @@ import os
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libhyb.so")
 
-HYB_F32, HYB_BF16, HYB_E4M3 = 0, 1, 2
+HYB_F32, HYB_BF16, HYB_E4M3, HYB_MXFP4 = 0, 1, 2, 3
 HYB_DEV_BAD_INDEX, HYB_DEV_TIMEOUT = 0x1, 0x2
 HYB_NOALLOC_SCRATCH_BYTES = 32 << 20  # include/hyb.h
 

@@ -15,7 +15,7 @@
 // and the weighted numerator relative to its running maximum (base 2, float32).
 // The R partial states (max, denominator, numerator) are merged by a tree in
 // shared memory.  E4M3 output needs the whole entry for its scale (amax/448),
-// so it keeps S = c.
+// so it keeps S = c; so does MXFP4 output (a scale per block of 32 channels).
 //
 // A batch of up to kCompressBatchMax compressions (the entries that complete at one decode
 // step in the CSA layer, its indexer keys and the HCA layer) runs as one launch: CTA
@@ -42,8 +42,18 @@ constexpr int kCv = 4;           // channels per thread
 constexpr int kRowBatch = 4;     // rows loaded at once per thread
 constexpr int kCompressThreads = 256;
 
+// e2m1 code of a float32 (OCP microscaling FP4): the nearest of 0, 0.5, 1, 1.5, 2, 3, 4, 6,
+// a tie going to the code with an even last bit, above 6 saturated; bit 3 the sign.
+__device__ __forceinline__ uint32_t e2m1_code(float y) {
+  const float a = fabsf(y);
+  const uint32_t m = a <= 0.25f ? 0u : a < 0.75f ? 1u : a <= 1.25f ? 2u : a < 1.75f ? 3u
+                   : a <= 2.5f ? 4u : a < 3.5f ? 5u : a <= 5.0f ? 6u : 7u;
+  return m | ((__float_as_uint(y) >> 31) << 3);
+}
+
 // One CTA's work: entry bj of the call (b * n_out + j), channel slab `slab`.  OUT: 0 =
-// float32, 1 = bf16, 2 = e4m3 + per-entry scale.  Threads past the call's G x R (a batch
+// float32, 1 = bf16, 2 = e4m3 + per-entry scale, 3 = MXFP4 (e2m1 codes two per byte +
+// an e8m0 scale byte per 32 channels).  Threads past the call's G x R (a batch
 // launch sizes its CTAs for the largest call) accumulate nothing.
 template <typename Tin, int OUT>
 __device__ __forceinline__ void compress_cta(const CompressParams& p, int64_t bj, int64_t slab, float* sm,
@@ -143,6 +153,30 @@ __device__ __forceinline__ void compress_cta(const CompressParams& p, int64_t bj
     if (rg == 0) store_vec<kCv>(static_cast<float*>(p.out) + orow * c + ch0, r);
   } else if constexpr (OUT == 1) {
     if (rg == 0) store_vec<kCv>(static_cast<__nv_bfloat16*>(p.out) + orow * c + ch0, r);
+  } else if constexpr (OUT == 3) {
+    // per block of 32 channels (8 consecutive channel threads of one warp): E = floor(log2
+    // amax) - 2 clamped to [-127, 127] (-127 for amax = 0; floor(log2) of a float32 is its
+    // unbiased exponent field, which already lies below -127 for subnormals), scale byte
+    // E + 127, codes of value * 2^-E (exact scaling by a power of two)
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < kCv; ++i) amax = fmaxf(amax, fabsf(r[i]));
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    int E = -127;
+    if (amax > 0.f) E = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 2;
+    E = E < -127 ? -127 : (E > 127 ? 127 : E);
+    if (rg == 0) {
+      // 2^-E as a float32: E in [-127, 127] gives exponents 0..254; 2^127 (E = -127) is
+      // 0x7F000000, and every factor is a normal power of two
+      const float inv = __uint_as_float((uint32_t)(127 - E) << 23);
+      uint32_t packed = 0;
+#pragma unroll
+      for (int i = 0; i < kCv; ++i) packed |= e2m1_code(r[i] * inv) << (4 * i);
+      *reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(p.out) + orow * (c / 2) + ch0 / 2) = (uint16_t)packed;
+      if ((ch0 & 31) == 0)
+        reinterpret_cast<uint8_t*>(p.out_scale)[orow * (c / 32) + ch0 / 32] = (uint8_t)(E + 127);
+    }
   } else {
     // per-entry scale = amax / 448 over all c channels (this CTA holds the whole entry)
     float amax = 0.f;
@@ -196,7 +230,8 @@ __global__ void __launch_bounds__(kCompressThreads) compress_batch_kernel(const 
   switch (B.out[i]) {  // (the same for every thread of the CTA)
     case 0: compress_cta<Tin, 0>(B.call[i], bj, slab, sm, s_red); break;
     case 1: compress_cta<Tin, 1>(B.call[i], bj, slab, sm, s_red); break;
-    default: compress_cta<Tin, 2>(B.call[i], bj, slab, sm, s_red); break;
+    case 2: compress_cta<Tin, 2>(B.call[i], bj, slab, sm, s_red); break;
+    default: compress_cta<Tin, 3>(B.call[i], bj, slab, sm, s_red); break;
   }
 }
 
@@ -205,7 +240,7 @@ __global__ void __launch_bounds__(kCompressThreads) compress_batch_kernel(const 
 static void shape_call(CompressParams& p, int out_dtype) {
   const int W = (int)(p.overlap ? 2 * p.m : p.m);
   int S = (int)p.c;
-  if (out_dtype != HYB_E4M3)
+  if (out_dtype != HYB_E4M3 && out_dtype != HYB_MXFP4)
     while (S > 16 && p.batch * p.n_out * (p.c / S) < 2 * kNumSMs) S >>= 1;
   const int G = S / kCv;
   int R = 1;
@@ -226,9 +261,12 @@ static cudaError_t launch_t(CompressParams& p, int out_dtype, cudaStream_t s) {
   } else if (out_dtype == HYB_BF16) {
     e = cudaFuncSetAttribute(compress_kernel<Tin, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess) e = launch_pdl(compress_kernel<Tin, 1>, grid, block, smem, s, p);
-  } else {
+  } else if (out_dtype == HYB_E4M3) {
     e = cudaFuncSetAttribute(compress_kernel<Tin, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess) e = launch_pdl(compress_kernel<Tin, 2>, grid, block, smem, s, p);
+  } else {
+    e = cudaFuncSetAttribute(compress_kernel<Tin, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) e = launch_pdl(compress_kernel<Tin, 3>, grid, block, smem, s, p);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -269,7 +307,7 @@ cudaError_t launch_compress_batch(const hyb_compress_args* const* a, const int64
     shape_call(p, a[i]->out_dtype);
     const int k = B.n++;
     B.call[k] = p;
-    B.out[k] = a[i]->out_dtype == HYB_F32 ? 0 : a[i]->out_dtype == HYB_BF16 ? 1 : 2;
+    B.out[k] = a[i]->out_dtype == HYB_F32 ? 0 : a[i]->out_dtype == HYB_BF16 ? 1 : a[i]->out_dtype == HYB_E4M3 ? 2 : 3;
     B.slabs[k] = p.c / p.S;
     ctas += p.batch * n_out[i] * B.slabs[k];
     B.cta_end[k] = ctas;

@@ -125,7 +125,7 @@ static hyb_status validate_compress(const hyb_compress_args* a, int64_t* n_out) 
   if (a->overlap != 0 && a->overlap != 1) return fail(HYB_ERR_INVALID_ARG, "hyb_compress: overlap must be 0 or 1");
   if (a->in_dtype != HYB_F32 && a->in_dtype != HYB_BF16)
     return fail(HYB_ERR_INVALID_ARG, "hyb_compress: in_dtype must be F32 or BF16");
-  if (a->out_dtype != HYB_F32 && a->out_dtype != HYB_BF16 && a->out_dtype != HYB_E4M3)
+  if (a->out_dtype != HYB_F32 && a->out_dtype != HYB_BF16 && a->out_dtype != HYB_E4M3 && a->out_dtype != HYB_MXFP4)
     return fail(HYB_ERR_INVALID_ARG, "hyb_compress: bad out_dtype");
   if (a->c < 1) return fail(HYB_ERR_INVALID_ARG, "hyb_compress: c < 1");
   if (!hyb::compress_shape_supported(a->c))
@@ -138,12 +138,14 @@ static hyb_status validate_compress(const hyb_compress_args* a, int64_t* n_out) 
   if (*n_out == 0 || a->batch == 0) return ok();
   if (!a->ca || !a->za || !a->bias || !a->out) return fail(HYB_ERR_INVALID_ARG, "hyb_compress: NULL ca/za/bias/out");
   if (a->overlap && (!a->cb || !a->zb)) return fail(HYB_ERR_INVALID_ARG, "hyb_compress: overlap needs cb and zb");
-  if ((a->out_dtype == HYB_E4M3) != (a->out_scale != nullptr))
-    return fail(HYB_ERR_INVALID_ARG, "hyb_compress: out_scale is required for E4M3 output and only then");
+  const bool scaled = a->out_dtype == HYB_E4M3 || a->out_dtype == HYB_MXFP4;
+  if (scaled != (a->out_scale != nullptr))
+    return fail(HYB_ERR_INVALID_ARG, "hyb_compress: out_scale is required for E4M3 and MXFP4 output and only then");
   // the kernel moves 4 consecutive channels per access
   const size_t ai = 4 * elem_size(a->in_dtype);
   if (!aligned(a->ca, ai) || !aligned(a->za, ai) || (a->overlap && (!aligned(a->cb, ai) || !aligned(a->zb, ai))) ||
-      !aligned(a->bias, 16) || !aligned(a->out, 4 * elem_size(a->out_dtype)) || !aligned(a->out_scale, 4))
+      !aligned(a->bias, 16) || !aligned(a->out, a->out_dtype == HYB_MXFP4 ? 2 : 4 * elem_size(a->out_dtype)) ||
+      !aligned(a->out_scale, a->out_dtype == HYB_MXFP4 ? 1 : 4))
     return fail(HYB_ERR_INVALID_ARG, "hyb_compress: misaligned pointer");
   return ok();
 }
@@ -193,8 +195,8 @@ static hyb_status validate_index(const hyb_index_args* a) {
   if (!a) return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: args is NULL");
   if (a->batch < 0 || a->n_q < 0 || a->n_entries < 0 || a->kv_stride < 0 || a->q_pos0 < 0 || a->m < 1)
     return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: negative size or m < 1");
-  if (a->dtype != HYB_F32 && a->dtype != HYB_E4M3)
-    return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: dtype must be F32 or E4M3");
+  if (a->dtype != HYB_F32 && a->dtype != HYB_E4M3 && a->dtype != HYB_MXFP4)
+    return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: dtype must be F32, E4M3 or MXFP4");
   if (a->k < 1 || a->n_ih < 1 || a->c_I < 1) return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: k, n_ih, c_I must be >= 1");
   if (a->k > 2048) return fail(HYB_ERR_UNSUPPORTED, "csa_index_topk: k = %lld > 2048", (long long)a->k);
   if (!hyb::index_cc_shape_supported(a->n_ih, a->c_I))
@@ -211,9 +213,12 @@ static hyb_status validate_index(const hyb_index_args* a) {
                 (long long)index_vis_max(a), (long long)a->k);
   if (!a->qI || !a->w || !a->idx) return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: NULL qI/w/idx");
   if (a->n_entries > 0 && !a->kI) return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: NULL kI");
-  const bool fp8 = a->dtype == HYB_E4M3;
+  const bool fp8 = a->dtype == HYB_E4M3 || a->dtype == HYB_MXFP4;
   if (fp8 && (!a->qI_scale || (a->n_entries > 0 && !a->kI_scale)))
-    return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: E4M3 needs qI_scale and kI_scale");
+    return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: E4M3 and MXFP4 need qI_scale and kI_scale");
+  if (a->dtype == HYB_MXFP4 && !hyb::index_fp4_shape_supported(a))
+    return fail(HYB_ERR_UNSUPPORTED, "csa_index_topk: MXFP4 runs with n_ih = 64, c_I = 128, kv_stride a multiple of 4 "
+                "and 16-byte aligned qI, kI and scales only");
   if (!fp8 && (a->qI_scale || a->kI_scale))
     return fail(HYB_ERR_INVALID_ARG, "csa_index_topk: scales must be NULL for F32");
   if (!aligned(a->kI, 16) || !aligned(a->qI, 4) || !aligned(a->w, 4) || !aligned(a->idx, 4) || !aligned(a->scores, 4) ||
@@ -241,8 +246,9 @@ hyb_status csa_index_topk(const hyb_index_args* a, void* workspace, size_t ws_by
   bool hist_done = false;
   if (a->ev_scores_begin && (e = record_event(a->ev_scores_begin, s)) != cudaSuccess)
     return cuda_status(e, "csa_index_topk: ev_scores_begin");
-  e = hyb::index_tc_shape_supported(a) ? hyb::launch_index_scores_tc(a, scores, nv, nv, ghist, &hist_done, s)
-                                       : hyb::launch_index_scores_cc(a, scores, nv, nv, s);
+  e = a->dtype == HYB_MXFP4             ? hyb::launch_index_scores_fp4(a, scores, nv, nv, ghist, &hist_done, s)
+      : hyb::index_tc_shape_supported(a) ? hyb::launch_index_scores_tc(a, scores, nv, nv, ghist, &hist_done, s)
+                                         : hyb::launch_index_scores_cc(a, scores, nv, nv, s);
   if (e != cudaSuccess) return cuda_status(e, "csa_index_topk: index-score launch");
   if (a->ev_scores_end && (e = record_event(a->ev_scores_end, s)) != cudaSuccess)
     return cuda_status(e, "csa_index_topk: ev_scores_end");

@@ -1,0 +1,468 @@
+// indexer_fp4.cu -- lightning-indexer scores with MXFP4 queries and keys on the tensor cores
+// ("DeepSeek-V4 hybrid attention" (trishampatil.com) section V.2 for the score; "DeepSeek-V4:
+// Anatomy of an Open-Source Frontier Model" (modernaiengineering.com), "FP4 quantization-aware
+// training": V4 runs the indexer's query-key path in FP4).
+//
+//   I[t,s] = sum_h w[t,h] * ReLU( sum_blk 2^(eq[t,h,blk] + ek[s,blk] - 254) * sum_{i in blk} q_i k_i )
+//
+// where q_i, k_i are e2m1 values and eq, ek the e8m0 scale bytes of their block of 32 dims.
+// The keys stay packed in HBM (64 bytes + 4 scale bytes per entry, against 132 for FP8).  On
+// chip every e2m1 value is written as the e4m3 byte of the same value (exact: e2m1's eight
+// magnitudes are all e4m3 numbers), and each 32-dim block is one tcgen05.mma kind::f8f6f4
+// (M = 128 entries, N = 64 heads, K = 32) into its own TMEM accumulator, so that the block's
+// exact integer-valued product (in units of 1/4) meets its two scales in the epilogue.
+//
+// Roles (one CTA of 384 threads per SM, persistent over units = (query row, run of tiles)):
+//   warp 0      TMA producer: the unit's packed query rows, then per tile of 128 entries the
+//               packed keys (8 KiB) and their scale words (512 B) into a ring;
+//   warps 2-3   expand packed tiles into e4m3 tiles (128-byte swizzle) for the MMA, and hand
+//               the scale words to the epilogue;
+//   warp 1      TMEM owner and MMA issuer (four K = 32 products per tile, one per block);
+//   warps 4-11  epilogue in two groups taking alternate tiles: the four block accumulators
+//               of an entry row, the scales, ReLU and the head weights, one float32 score
+//               per (query, entry), and (decode) the row's 12-bit score-key histogram.
+// Every wait is bounded (about 1 s): on expiry HYB_DEV_TIMEOUT is raised, the CTA's own copies
+// and products in flight land, TMEM is freed and the kernel returns.
+#include "kernels.cuh"
+#include "tc_common.cuh"
+
+namespace hyb {
+
+namespace {
+
+constexpr int kTileE = 128;                 // entries per tile (MMA M)
+constexpr int kHeads = 64;                  // indexer heads (MMA N)
+constexpr int kRowRaw = 64;                 // packed bytes per 128-dim row
+constexpr int kRawKeyBytes = kTileE * kRowRaw;    // 8 KiB
+constexpr int kRawScaleBytes = kTileE * 4;        // one 4-byte word (4 e8m0 bytes) per entry
+constexpr int kF8Bytes = kTileE * 128;            // 16 KiB: e4m3, 128-byte swizzle
+constexpr int kRawQBytes = kHeads * kRowRaw;      // 4 KiB
+constexpr int kQ8Bytes = kHeads * 128;            // 8 KiB
+constexpr int kSR = 8;                      // packed-tile ring
+constexpr int kS8 = 4;                      // e4m3 tile ring
+constexpr int kAcc = 2;                     // accumulator sets (4 blocks x 64 columns each)
+constexpr int kScaleRing = kS8 + kAcc;      // scale words on their way to the epilogue
+constexpr int kThreads = 384;
+constexpr int kEpiWarp0 = 4, kEpiWarps = 8, kEpiGroups = 2;
+constexpr int kEpiThreads = kEpiWarps * 32;
+
+constexpr int kOffF8 = 0;
+constexpr int kOffQ8 = kOffF8 + kS8 * kF8Bytes;
+constexpr int kOffRaw = kOffQ8 + 2 * kQ8Bytes;
+constexpr int kOffRawS = kOffRaw + kSR * kRawKeyBytes;
+constexpr int kOffRawQ = kOffRawS + kSR * kRawScaleBytes;
+constexpr int kOffKS = kOffRawQ + 2 * kRawQBytes;
+constexpr int kOffQS = kOffKS + kScaleRing * kRawScaleBytes;  // float [64][4] query block scales, then w [64]
+constexpr int kOffLut = kOffQS + kHeads * 5 * 4;              // uint16 [256]: packed byte -> two e4m3 bytes
+constexpr int kOffHist = kOffLut + 256 * 2;                   // 16-bit counters, two per word
+constexpr int kOffBar = kOffHist + kTopkHistBins * 2;
+enum {
+  kBarRawFull = 0,
+  kBarRawEmpty = kBarRawFull + kSR,
+  kBarF8Full = kBarRawEmpty + kSR,
+  kBarF8Empty = kBarF8Full + kS8,
+  kBarRqFull = kBarF8Empty + kS8,
+  kBarRqEmpty = kBarRqFull + 2,
+  kBarQ8Full = kBarRqEmpty + 2,
+  kBarQ8Empty = kBarQ8Full + 2,
+  kBarAccFull = kBarQ8Empty + 2,
+  kBarAccEmpty = kBarAccFull + kAcc,
+  kBarKsFull = kBarAccEmpty + kAcc,
+  kBarKsEmpty = kBarKsFull + kScaleRing,
+  kBarDone = kBarKsEmpty + kScaleRing,
+  kBarEpi = kBarDone + 1,
+  kNumBars = kBarEpi + 1
+};
+constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 64 + 1024;  // + flags + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kTopkHistBins / 2 == 8 * kEpiThreads, "one 8-word slice of the histogram per epilogue thread");
+
+struct Fp4Params {
+  const float* w;
+  const uint8_t* qI_scale;  // [rows][64][4] e8m0
+  float* scores;
+  uint32_t* ghist;
+  int64_t score_stride;
+  int64_t n_q, n_entries, kv_stride, m, q_pos0;
+  const int64_t* q_pos;
+  int64_t tiles_per_unit, units_per_group, n_units;
+  int32_t* dev_status;
+};
+
+struct Fp4Unit {
+  int64_t b, j, row, tile_begin, tile_end;
+};
+
+__device__ __forceinline__ Fp4Unit fp4_unit(const Fp4Params& p, int64_t u) {
+  Fp4Unit U;
+  const int64_t g = u / p.units_per_group, chunk = u % p.units_per_group;
+  U.row = g, U.b = g / p.n_q, U.j = g % p.n_q;
+  const int64_t vis = visible_checked(query_pos(p.q_pos, p.q_pos0, U.row, U.j), p.m, p.n_entries, nullptr, false);
+  const int64_t tiles = (vis + kTileE - 1) / kTileE;
+  U.tile_begin = chunk * p.tiles_per_unit;
+  U.tile_end = U.tile_begin + p.tiles_per_unit < tiles ? U.tile_begin + p.tiles_per_unit : tiles;
+  return U;
+}
+
+// 2^(e - 127) for an e8m0 byte (255 is NaN), as a float32
+__device__ __forceinline__ float e8m0_value(uint32_t e) {
+  return e == 255u ? __uint_as_float(0x7FC00000u) : e == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23);
+}
+
+// e4m3 byte of the e2m1 code v (bit 3 the sign): 0, 0.5, 1, 1.5, 2, 3, 4, 6 exactly
+__host__ __device__ constexpr uint32_t e2m1_to_e4m3(uint32_t v) {
+  constexpr uint8_t mag[8] = {0x00, 0x30, 0x38, 0x3C, 0x40, 0x44, 0x48, 0x4C};
+  return (uint32_t)mag[v & 7u] | ((v & 8u) << 4);
+}
+
+// Expand one 8-byte piece (16 packed e2m1 values, element 2i in the low nibble of byte i)
+// into the 16 e4m3 bytes of the same values.
+__device__ __forceinline__ uint4 expand16(uint2 raw, const uint16_t* lut) {
+  const uint32_t w[2] = {raw.x, raw.y};
+  uint32_t o[4];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t b0 = lut[w[h] & 0xFFu], b1 = lut[(w[h] >> 8) & 0xFFu], b2 = lut[(w[h] >> 16) & 0xFFu],
+                   b3 = lut[w[h] >> 24];
+    o[2 * h] = b0 | (b1 << 16);
+    o[2 * h + 1] = b2 | (b3 << 16);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    index_fp4_kernel(const __grid_constant__ CUtensorMap tm_keys, const __grid_constant__ CUtensorMap tm_ks,
+                     const __grid_constant__ CUtensorMap tm_q, Fp4Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* f8 = smem + kOffF8;
+  uint8_t* q8 = smem + kOffQ8;
+  uint8_t* raw = smem + kOffRaw;
+  uint32_t* raw_s = reinterpret_cast<uint32_t*>(smem + kOffRawS);
+  uint8_t* raw_q = smem + kOffRawQ;
+  uint32_t* ks_ring = reinterpret_cast<uint32_t*>(smem + kOffKS);
+  float* qs_t = reinterpret_cast<float*>(smem + kOffQS);  // [64][4]
+  float* w_t = qs_t + kHeads * 4;                          // [64]
+  uint16_t* lut = reinterpret_cast<uint16_t*>(smem + kOffLut);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kOffHist);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(bars + kNumBars);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + kNumBars) + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kSR; ++i) tc::mbar_init(&bars[kBarRawFull + i], 1), tc::mbar_init(&bars[kBarRawEmpty + i], 2);
+    for (int i = 0; i < kS8; ++i) tc::mbar_init(&bars[kBarF8Full + i], 2), tc::mbar_init(&bars[kBarF8Empty + i], 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&bars[kBarRqFull + i], 1), tc::mbar_init(&bars[kBarRqEmpty + i], 2);
+      tc::mbar_init(&bars[kBarQ8Full + i], 2), tc::mbar_init(&bars[kBarQ8Empty + i], 1);
+    }
+    for (int i = 0; i < kAcc; ++i)
+      tc::mbar_init(&bars[kBarAccFull + i], 1), tc::mbar_init(&bars[kBarAccEmpty + i], kEpiWarps / kEpiGroups);
+    for (int i = 0; i < kScaleRing; ++i)
+      tc::mbar_init(&bars[kBarKsFull + i], 2), tc::mbar_init(&bars[kBarKsEmpty + i], kEpiWarps / kEpiGroups);
+    tc::mbar_init(&bars[kBarDone], 1);
+    tc::mbar_init(&bars[kBarEpi], kEpiThreads);
+    *s_abort = 0;
+    tc::fence_barrier_init();
+  }
+  for (int i = threadIdx.x; i < 256; i += kThreads)
+    lut[i] = (uint16_t)(e2m1_to_e4m3((uint32_t)i & 15u) | (e2m1_to_e4m3((uint32_t)i >> 4) << 8));
+  if (warp == 1) tc::tmem_alloc(s_tmem, 512);
+  if (warp == 0 && lane == 0) {
+    tc::prefetch_tmap(&tm_keys);
+    tc::prefetch_tmap(&tm_ks);
+    tc::prefetch_tmap(&tm_q);
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  pdl_wait();  // (the setup above touched only shared memory, TMEM and the parameters)
+  pdl_trigger();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int64_t seq = 0, qc = 0, issued = 0;
+      bool ok = true;
+      int64_t q_last[2] = {-1, -1};  // last query load issued into each buffer (drained on abort)
+      for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+        const Fp4Unit U = fp4_unit(p, u);
+        if (U.tile_begin >= U.tile_end) continue;
+        const int qb = (int)(qc & 1);
+        if (!(ok = tc::mbar_wait(&bars[kBarRqEmpty + qb], (uint32_t)((qc >> 1) & 1) ^ 1u, s_abort, 1))) break;
+        tc::mbar_arrive_expect_tx(&bars[kBarRqFull + qb], kRawQBytes);
+        tc::tma_load_2d(raw_q + qb * kRawQBytes, &tm_q, &bars[kBarRqFull + qb], 0, (int32_t)(U.row * kHeads));
+        q_last[qb] = qc;
+        ++qc;
+        for (int64_t t = U.tile_begin; t < U.tile_end; ++t, ++seq) {
+          const int rs = (int)(seq % kSR);
+          if (!(ok = tc::mbar_wait(&bars[kBarRawEmpty + rs], (uint32_t)((seq / kSR) & 1) ^ 1u, s_abort, 2))) break;
+          tc::mbar_arrive_expect_tx(&bars[kBarRawFull + rs], kRawKeyBytes + kRawScaleBytes);
+          tc::tma_load_2d(raw + rs * kRawKeyBytes, &tm_keys, &bars[kBarRawFull + rs], 0,
+                          (int32_t)(U.b * p.kv_stride + t * kTileE));
+          tc::tma_load_2d(raw_s + rs * kTileE, &tm_ks, &bars[kBarRawFull + rs], (int32_t)(t * kTileE), (int32_t)U.b);
+          ++issued;
+        }
+      }
+      if (!ok) {
+        // let this thread's copies in flight land before the CTA can exit
+        for (int64_t i = issued > kSR ? issued - kSR : 0; i < issued; ++i)
+          tc::mbar_wait_drain(&bars[kBarRawFull + i % kSR], (uint32_t)((i / kSR) & 1));
+        for (int b = 0; b < 2; ++b)
+          if (q_last[b] >= 0) tc::mbar_wait_drain(&bars[kBarRqFull + b], (uint32_t)((q_last[b] >> 1) & 1));
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------------------------------ expand packed -> e4m3
+    // 64 threads; thread x takes 16-byte output chunks x, x + 64, ... of a tile (row = chunk
+    // / 8, chunk c = chunk % 8 of the row, written at chunk c ^ (row & 7): 128-byte swizzle)
+    const int x = (warp - 2) * 32 + lane;
+    int64_t seq = 0, qc = 0;
+    bool ok = true;
+    auto done = [&](uint64_t* bar) {
+      tc::fence_proxy_async_smem();  // the e4m3 tiles are read by the tensor cores
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(bar);
+    };
+    for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+      const Fp4Unit U = fp4_unit(p, u);
+      if (U.tile_begin >= U.tile_end) continue;
+      const int qb = (int)(qc & 1);
+      const uint32_t qpar = (uint32_t)((qc >> 1) & 1);
+      int okw = 1;
+      if (lane == 0)
+        okw = tc::mbar_wait(&bars[kBarRqFull + qb], qpar, s_abort, 3) &&
+              tc::mbar_wait(&bars[kBarQ8Empty + qb], qpar ^ 1u, s_abort, 4);
+      if (!(ok = __shfl_sync(0xffffffffu, okw, 0) != 0)) break;
+      {
+        const uint8_t* src = raw_q + qb * kRawQBytes;
+        uint8_t* dst = q8 + qb * kQ8Bytes;
+#pragma unroll 2
+        for (int ch = x; ch < kHeads * 8; ch += 64) {
+          const int r = ch >> 3, c = ch & 7;
+          const uint2 v = *reinterpret_cast<const uint2*>(src + r * kRowRaw + c * 8);
+          *reinterpret_cast<uint4*>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = expand16(v, lut);
+        }
+      }
+      done(&bars[kBarQ8Full + qb]);
+      if (lane == 0) tc::mbar_arrive(&bars[kBarRqEmpty + qb]);
+      ++qc;
+      for (int64_t t = U.tile_begin; t < U.tile_end && ok; ++t, ++seq) {
+        const int rs = (int)(seq % kSR), s8 = (int)(seq % kS8), r = (int)(seq % kScaleRing);
+        okw = 1;
+        if (lane == 0)
+          okw = tc::mbar_wait(&bars[kBarRawFull + rs], (uint32_t)((seq / kSR) & 1), s_abort, 5) &&
+                tc::mbar_wait(&bars[kBarF8Empty + s8], (uint32_t)((seq / kS8) & 1) ^ 1u, s_abort, 6) &&
+                tc::mbar_wait(&bars[kBarKsEmpty + r], (uint32_t)((seq / kScaleRing) & 1) ^ 1u, s_abort, 7);
+        if (!(ok = __shfl_sync(0xffffffffu, okw, 0) != 0)) break;
+        const uint8_t* src = raw + rs * kRawKeyBytes;
+        uint8_t* dst = f8 + s8 * kF8Bytes;
+#pragma unroll 4
+        for (int ch = x; ch < kTileE * 8; ch += 64) {
+          const int rr = ch >> 3, c = ch & 7;
+          const uint2 v = *reinterpret_cast<const uint2*>(src + rr * kRowRaw + c * 8);
+          *reinterpret_cast<uint4*>(dst + rr * 128 + ((c ^ (rr & 7)) << 4)) = expand16(v, lut);
+        }
+        ks_ring[r * kTileE + x] = raw_s[rs * kTileE + x];
+        ks_ring[r * kTileE + 64 + x] = raw_s[rs * kTileE + 64 + x];
+        done(&bars[kBarF8Full + s8]);
+        if (lane == 0) {
+          tc::mbar_arrive(&bars[kBarKsFull + r]);
+          tc::mbar_arrive(&bars[kBarRawEmpty + rs]);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (tc::elect_one()) {
+      constexpr uint32_t idesc = tc::make_idesc(0, 0, 0, 0, kTileE, kHeads);  // e4m3 x e4m3, both K-major
+      int64_t seq = 0, qc = 0;
+      bool ok = true;
+      for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+        const Fp4Unit U = fp4_unit(p, u);
+        if (U.tile_begin >= U.tile_end) continue;
+        const int qb = (int)(qc & 1);
+        if (!(ok = tc::mbar_wait(&bars[kBarQ8Full + qb], (uint32_t)((qc >> 1) & 1), s_abort, 8))) break;
+        const uint32_t b_base = tc::smem_u32(q8 + qb * kQ8Bytes);
+        for (int64_t t = U.tile_begin; t < U.tile_end; ++t, ++seq) {
+          const int s8 = (int)(seq % kS8), acc = (int)(seq % kAcc);
+          if (!(ok = tc::mbar_wait(&bars[kBarAccEmpty + acc], (uint32_t)((seq / kAcc) & 1) ^ 1u, s_abort, 9))) break;
+          if (!(ok = tc::mbar_wait(&bars[kBarF8Full + s8], (uint32_t)((seq / kS8) & 1), s_abort, 10))) break;
+          tc::tc_fence_after();
+          const uint32_t a_base = tc::smem_u32(f8 + s8 * kF8Bytes);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)  // block k (dims 32k .. 32k+31): its own accumulator
+            tc::mma_f8f6f4(tmem + (uint32_t)(acc * 4 * kHeads + k * kHeads), tc::desc_kmajor_sw128(a_base + 32 * k),
+                           tc::desc_kmajor_sw128(b_base + 32 * k), idesc, 0u);
+          tc::mma_commit(&bars[kBarF8Empty + s8]);
+          tc::mma_commit(&bars[kBarAccFull + acc]);
+        }
+        if (!ok) break;
+        tc::mma_commit(&bars[kBarQ8Empty + qb]);
+        ++qc;
+      }
+      tc::mma_commit(&bars[kBarDone]);  // completes once, after every product above
+      tc::mbar_wait_drain(&bars[kBarDone], 0);
+    }
+    __syncwarp();
+  } else if (warp >= kEpiWarp0) {
+    // ------------------------------------------------------------ epilogue
+    const int et = threadIdx.x - kEpiWarp0 * 32;
+    const int quad = warp & 3;
+    const int grp = (warp - kEpiWarp0) / 4;  // tiles with seq % 2 == grp
+    uint32_t ephase = 0;
+    auto esync = [&]() -> bool {
+      tc::mbar_arrive(&bars[kBarEpi]);
+      const bool r = tc::mbar_wait(&bars[kBarEpi], ephase, s_abort, 11);
+      ephase ^= 1u;
+      return r;
+    };
+    const bool do_hist = p.ghist != nullptr;
+    int64_t hist_row = -1;
+    if (do_hist)
+      for (int i = et; i < kTopkHistBins / 2; i += kEpiThreads) hist[i] = 0;
+    auto flush_hist = [&](bool clear) {
+      uint4* h4 = reinterpret_cast<uint4*>(hist) + 2 * et;
+      const uint4 a = h4[0], b = h4[1];
+      const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      uint32_t* g = p.ghist + hist_row * kTopkHistBins + 16 * et;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (v[i] & 0xFFFFu) atomicAdd(g + 2 * i, v[i] & 0xFFFFu);
+        if (v[i] >> 16) atomicAdd(g + 2 * i + 1, v[i] >> 16);
+      }
+      if (clear) h4[0] = h4[1] = make_uint4(0u, 0u, 0u, 0u);
+    };
+    int64_t seq = 0;
+    bool ok = true;
+    for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+      const Fp4Unit U = fp4_unit(p, u);
+      if (U.tile_begin >= U.tile_end) continue;
+      if (!(ok = esync())) break;  // everyone is done with the previous unit's tables
+      if (do_hist && U.row != hist_row) {
+        if (hist_row >= 0) flush_hist(true);
+        hist_row = U.row;
+      }
+      // the unit's query block scales (as floats) and head weights
+      {
+        const uint8_t* qsb = p.qI_scale + U.row * (kHeads * 4);
+        for (int i = et; i < kHeads * 4; i += kEpiThreads) qs_t[i] = e8m0_value(__ldg(qsb + i));
+        for (int i = et; i < kHeads; i += kEpiThreads) w_t[i] = __ldg(p.w + U.row * kHeads + i);
+      }
+      if (!(ok = esync())) break;
+      const int64_t vis = visible_checked(query_pos(p.q_pos, p.q_pos0, U.row, U.j), p.m, p.n_entries, p.dev_status,
+                                          lane == 0 && U.tile_begin == 0);
+      for (int64_t t = U.tile_begin; t < U.tile_end; ++t, ++seq) {
+        if ((int)(seq & 1) != grp) continue;  // the other group's tile
+        const int acc = (int)(seq % kAcc), r = (int)(seq % kScaleRing);
+        if (!(ok = tc::mbar_wait(&bars[kBarAccFull + acc], (uint32_t)((seq / kAcc) & 1), s_abort, 12))) break;
+        if (!(ok = tc::mbar_wait(&bars[kBarKsFull + r], (uint32_t)((seq / kScaleRing) & 1), s_abort, 13))) break;
+        tc::tc_fence_after();
+        const int row = quad * 32 + lane;
+        const int64_t s = t * kTileE + row;
+        const uint32_t kw = ks_ring[r * kTileE + row];
+        float ksf[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) ksf[k] = e8m0_value((kw >> (8 * k)) & 0xFFu);
+        const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 4 * kHeads);
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int hb = 0; hb < kHeads; hb += 32) {
+          float dot[32];
+#pragma unroll
+          for (int h = 0; h < 32; ++h) dot[h] = 0.f;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            float v[32];
+            tc::tmem_ld32(taddr + (uint32_t)(k * kHeads + hb), v);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int h = 0; h < 32; ++h) dot[h] = fmaf(v[h] * ksf[k], qs_t[(hb + h) * 4 + k], dot[h]);
+          }
+#pragma unroll
+          for (int h = 0; h < 32; ++h) ps[h & 3] = fmaf(w_t[hb + h], fmaxf(dot[h], 0.f), ps[h & 3]);
+        }
+        const float score = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          tc::mbar_arrive(&bars[kBarAccEmpty + acc]);
+          tc::mbar_arrive(&bars[kBarKsEmpty + r]);
+        }
+        const bool keep = s < vis;
+        if (keep) p.scores[U.row * p.score_stride + s] = score;
+        if (do_hist) {
+          // lanes with the same bin add their count once (scores crowd into few bins)
+          const uint32_t bin = keep ? float_order_key(score) >> (32 - kTopkHistBits) : 0xFFFFFFFFu;
+          const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+          if (keep && lane == __ffs(peers) - 1) atomicAdd(&hist[bin >> 1], (uint32_t)__popc(peers) << (16 * (bin & 1)));
+        }
+      }
+    }
+    if (do_hist && ok && hist_row >= 0 && esync()) flush_hist(false);
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *s_abort) flag_status(p.dev_status, HYB_DEV_TIMEOUT | ((*s_abort & 0xFF) << 8));
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+bool index_fp4_shape_supported(const hyb_index_args* a) {
+  if (a->dtype != HYB_MXFP4 || a->c_I != 128 || a->n_ih != kHeads) return false;
+  const int64_t kvs = a->kv_stride > 0 ? a->kv_stride : a->n_entries;
+  if (kvs % 4 != 0) return false;  // rows of scale words start on 16-byte boundaries
+  const uintptr_t al = reinterpret_cast<uintptr_t>(a->kI) | reinterpret_cast<uintptr_t>(a->kI_scale) |
+                       reinterpret_cast<uintptr_t>(a->qI) | reinterpret_cast<uintptr_t>(a->qI_scale);
+  if (al % 16 != 0) return false;
+  if (a->batch * kvs >= (int64_t(1) << 31) || a->batch * a->n_q * kHeads >= (int64_t(1) << 31)) return false;
+  return true;
+}
+
+cudaError_t launch_index_scores_fp4(const hyb_index_args* a, float* scores, int64_t score_stride, int64_t n_vis_max,
+                                    uint32_t* ghist, bool* hist_done, cudaStream_t s) {
+  *hist_done = false;
+  if (n_vis_max == 0 || a->n_q == 0 || a->batch == 0) return cudaSuccess;
+  const int64_t kvs = a->kv_stride > 0 ? a->kv_stride : a->n_entries;
+  CUtensorMap tm_keys, tm_ks, tm_q;
+  if (!encode_tmap_2d(&tm_keys, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->kI, kRowRaw, (uint64_t)(a->batch * kvs), kRowRaw,
+                      kRowRaw, kTileE, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_tmap_2d(&tm_ks, CU_TENSOR_MAP_DATA_TYPE_UINT32, a->kI_scale, (uint64_t)kvs, (uint64_t)a->batch,
+                      (uint64_t)kvs * 4, kTileE, 1, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_tmap_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->qI, kRowRaw, (uint64_t)(a->batch * a->n_q * kHeads),
+                      kRowRaw, kRowRaw, kHeads, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  Fp4Params p{};
+  p.w = a->w, p.qI_scale = reinterpret_cast<const uint8_t*>(a->qI_scale), p.scores = scores;
+  p.score_stride = score_stride;
+  p.n_q = a->n_q, p.n_entries = a->n_entries, p.kv_stride = kvs, p.m = a->m, p.q_pos0 = a->q_pos0;
+  p.q_pos = a->q_pos;
+  p.dev_status = a->dev_status;
+  const int64_t rows = a->batch * a->n_q;
+  const int64_t tiles_max = (n_vis_max + kTileE - 1) / kTileE;
+  // one unit per CTA where the rows are few (decode), the runs evened out over the SMs
+  int64_t tpu = (rows * tiles_max + kNumSMs - 1) / kNumSMs;
+  tpu = tpu < 1 ? 1 : (tpu > tiles_max ? tiles_max : tpu);
+  p.tiles_per_unit = tpu;
+  p.units_per_group = (tiles_max + tpu - 1) / tpu;
+  p.n_units = rows * p.units_per_group;
+  // fused histogram: fewer than 2^16 entries per unit (16-bit counters)
+  p.ghist = (ghist != nullptr && tpu * kTileE < 65536) ? ghist : nullptr;
+  cudaError_t e = cudaFuncSetAttribute(index_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = p.n_units < kNumSMs ? p.n_units : kNumSMs;
+  e = launch_pdl(index_fp4_kernel, dim3((unsigned)grid), dim3(kThreads), (size_t)kSmemBytes, s, tm_keys, tm_ks, tm_q, p);
+  if (e != cudaSuccess) return e;
+  *hist_done = p.ghist != nullptr;
+  return cudaGetLastError();
+}
+
+}  // namespace hyb

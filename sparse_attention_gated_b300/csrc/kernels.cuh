@@ -55,6 +55,10 @@ bool index_tc_shape_supported(const hyb_index_args* a);
 // ghist (optional): the row histograms of the top-k plan; *hist_done tells whether this launch filled them
 cudaError_t launch_index_scores_tc(const hyb_index_args* a, float* scores, int64_t score_stride, int64_t n_vis_max,
                                    uint32_t* ghist, bool* hist_done, cudaStream_t s);
+// MXFP4 scores (packed e2m1 keys and queries with e8m0 block scales) on the tensor cores
+bool index_fp4_shape_supported(const hyb_index_args* a);
+cudaError_t launch_index_scores_fp4(const hyb_index_args* a, float* scores, int64_t score_stride, int64_t n_vis_max,
+                                    uint32_t* ghist, bool* hist_done, cudaStream_t s);
 
 // topk.cu
 // ws: the plan's scratch; zr: the zeroed counters (kTopkZeroRegionBytes at the workspace start)

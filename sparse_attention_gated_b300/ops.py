@@ -15,7 +15,10 @@ import torch
 
 from . import _abi
 
-_DT = {torch.float32: _abi.HYB_F32, torch.bfloat16: _abi.HYB_BF16, torch.float8_e4m3fn: _abi.HYB_E4M3}
+# MXFP4 tensors are torch.float4_e2m1fn_x2 (two e2m1 codes per byte: the last dimension counts
+# pairs), their scales torch.float8_e8m0fnu (one byte per block of 32 elements)
+_DT = {torch.float32: _abi.HYB_F32, torch.bfloat16: _abi.HYB_BF16, torch.float8_e4m3fn: _abi.HYB_E4M3,
+       torch.float4_e2m1fn_x2: _abi.HYB_MXFP4}
 _TORCH_OF = {v: k for k, v in _DT.items()}
 
 
@@ -96,10 +99,11 @@ def compress_args(ca, za, bias, m, cb=None, zb=None, overlap=False, first_block=
     a.in_batch_stride = 0 if rows == n else rows
     a.out, a.out_scale = _ptr(out), _ptr(out_scale)
     if out is not None:
-        if out_row0:
-            a.out = ctypes.c_void_p(out.data_ptr() + out_row0 * c * out.element_size())
+        if out_row0:  # (row strides of out and out_scale: c values or c/2 pairs; one scale or c/32)
+            a.out = ctypes.c_void_p(out.data_ptr() + out_row0 * out.stride(1) * out.element_size())
             if out_scale is not None:
-                a.out_scale = ctypes.c_void_p(out_scale.data_ptr() + out_row0 * out_scale.element_size())
+                rs = out_scale.stride(1) if out_scale.dim() == 3 else 1
+                a.out_scale = ctypes.c_void_p(out_scale.data_ptr() + out_row0 * rs * out_scale.element_size())
         out_batch_stride = out.shape[1]
     a.batch, a.n_rows, a.c, a.m, a.first_block = B, n, c, m, first_block
     a.out_batch_stride = out_batch_stride
@@ -121,7 +125,12 @@ def hyb_compress(ca, za, bias, m: int, *, cb=None, zb=None, overlap: bool = Fals
     n_out = compress_out_count(n, m, overlap, first_block)
     if out is None:
         dt = out_dtype if out_dtype is not None else ca.dtype
-        out = torch.empty((B, n_out, c), dtype=dt, device=ca.device)
+        if dt == torch.float4_e2m1fn_x2:
+            out = torch.empty((B, n_out, c // 2), dtype=dt, device=ca.device)
+            if out_scale is None:
+                out_scale = torch.empty((B, n_out, c // 32), dtype=torch.float8_e8m0fnu, device=ca.device)
+        else:
+            out = torch.empty((B, n_out, c), dtype=dt, device=ca.device)
         if dt == torch.float8_e4m3fn and out_scale is None:
             out_scale = torch.empty((B, n_out), dtype=torch.float32, device=ca.device)
     if out_row0 and (out_row0 + n_out > out.shape[1]):
@@ -150,8 +159,11 @@ def hyb_compress_batch(calls, stream=None):
 
 def index_args(qI, w, kI, m, k, q_pos0, qI_scale=None, kI_scale=None, idx=None, scores=None, n_entries=None,
                dev_status=None, scores_events=None, q_pos=None):
-    """q_pos: optional int64 [B, n_q] per-query absolute positions (then q_pos0 is unused)."""
+    """q_pos: optional int64 [B, n_q] per-query absolute positions (then q_pos0 is unused).
+    MXFP4 (qI, kI float4_e2m1fn_x2, last dimension c_I/2; scales float8_e8m0fnu [..., c_I/32])."""
     B, n_q, n_ih, c_I = qI.shape
+    if qI.dtype == torch.float4_e2m1fn_x2:
+        c_I *= 2
     a = _abi.IndexArgs()
     a.qI, a.qI_scale, a.w, a.kI, a.kI_scale = _ptr(qI), _ptr(qI_scale), _ptr(w), _ptr(kI), _ptr(kI_scale)
     a.idx, a.scores = _ptr(idx), _ptr(scores)

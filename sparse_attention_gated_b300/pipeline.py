@@ -36,6 +36,7 @@ from __future__ import annotations
 import torch
 
 from . import ops
+from . import workloads
 from .workloads import Workload
 
 
@@ -66,9 +67,10 @@ class HybridStep:
             if not w.decode:
                 N = w.n_csa
                 self.buf["entries"] = torch.empty((B, N, c), dtype=w.dtype, device=dev)
-                self.buf["kI"] = torch.empty((B, N, w.c_I), dtype=w.idx_dtype, device=dev)
-                if w.idx_dtype != f32:
-                    self.buf["kI_scale"] = torch.empty((B, N), dtype=f32, device=dev)
+                kI, kIs = workloads.index_key_buffers(w, B, N, dev)
+                self.buf["kI"] = kI
+                if kIs is not None:
+                    self.buf["kI_scale"] = kIs
             self.buf["idx"] = torch.empty((B, n_q, w.k), dtype=torch.int32, device=dev)
             self.buf["o"] = torch.empty((B, n_q, n_h, c), dtype=f32, device=dev)
             self.buf["lse"] = torch.empty((B, n_q, n_h), dtype=f32, device=dev)

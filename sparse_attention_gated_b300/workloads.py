@@ -51,6 +51,9 @@ class Workload:
     # (16 / 1024 in the Pro configuration, 8 / 1024 in Flash)
     out_groups: int = 16
     out_dim: int = 1024
+    # indexer query/key format: "e4m3" (one float32 scale per row) or "mxfp4" (e2m1 pairs,
+    # one e8m0 scale per 32 dims)
+    idx_fmt: str = "e4m3"
 
     @property
     def n_csa(self) -> int:
@@ -62,7 +65,9 @@ class Workload:
 
     @property
     def idx_dtype(self) -> torch.dtype:
-        return torch.float32 if self.dtype == torch.float32 else torch.float8_e4m3fn
+        if self.dtype == torch.float32:
+            return torch.float32
+        return torch.float4_e2m1fn_x2 if self.idx_fmt == "mxfp4" else torch.float8_e4m3fn
 
     @property
     def decode(self) -> bool:
@@ -97,6 +102,9 @@ WORKLOADS = {
                                        c=512, m=4, k=1024, n_ih=64, c_I=128, m_hca=128, seed=1006),
     # Flash's first layers: sliding window only
     "flash_swa_decode": Workload("flash_swa_decode", "swa_decode", batch=8, n_ctx=65536, n_h=64, c=512, seed=1007, out_groups=8),
+    # the 1M decode with the indexer's queries and keys in MXFP4
+    "pro_1m_hybrid_decode_fp4": Workload("pro_1m_hybrid_decode_fp4", "hybrid_decode", batch=4, n_ctx=1048576, n_h=128,
+                                         c=512, m=4, k=1024, n_ih=64, c_I=128, m_hca=128, seed=1008, idx_fmt="mxfp4"),
 }
 
 
@@ -123,11 +131,27 @@ class _Draw:
 
 
 def _indexer_values(d: _Draw, shape, dtype):
-    """Indexer queries/keys: N(0,1), cast to e4m3 by torch, plus per-row scales U(0.5, 1.5)."""
+    """Indexer queries/keys: N(0,1), cast to e4m3 by torch, plus per-row scales U(0.5, 1.5);
+    for MXFP4, uniformly random e2m1 codes (two per byte) and e8m0 block scales 2^-7 .. 2^6."""
+    if dtype == torch.float4_e2m1fn_x2:
+        codes = torch.randint(0, 256, shape[:-1] + (shape[-1] // 2,), generator=d.g, device=d.device, dtype=torch.uint8)
+        scales = torch.randint(120, 134, shape[:-1] + (shape[-1] // 32,), generator=d.g, device=d.device,
+                               dtype=torch.uint8)
+        return codes.view(torch.float4_e2m1fn_x2), scales.view(torch.float8_e8m0fnu)
     x = d.normal(shape)
     if dtype == torch.float32:
         return x, None
     return x.to(torch.float8_e4m3fn), d.uniform(shape[:-1], 0.5, 1.5)
+
+
+def index_key_buffers(w: Workload, B: int, N: int, device):
+    """Empty indexer-key buffers of N entries per sequence in w's format: (keys, scales or None)."""
+    dt = w.idx_dtype
+    if dt == torch.float4_e2m1fn_x2:
+        return (torch.empty((B, N, w.c_I // 2), dtype=dt, device=device),
+                torch.empty((B, N, w.c_I // 32), dtype=torch.float8_e8m0fnu, device=device))
+    kI = torch.empty((B, N, w.c_I), dtype=dt, device=device)
+    return kI, (None if dt == torch.float32 else torch.empty((B, N), dtype=torch.float32, device=device))
 
 
 def make_inputs(w: Workload, device="cpu") -> dict:

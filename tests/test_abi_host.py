@@ -93,6 +93,25 @@ def test_compress_batch_validates_every_call_before_any_launch(lib):
     assert "in_dtype" in lib.hyb_last_error().decode()
 
 
+def test_mxfp4_arguments_are_validated_before_any_launch(lib):
+    # compression to MXFP4 needs the scale bytes (and only scaled outputs take them)
+    assert lib.hyb_compress(ctypes.byref(_compress_args(c=128, out_dtype=_abi.HYB_MXFP4)), None, 0, None) == 1
+    assert lib.hyb_compress(ctypes.byref(_compress_args(c=48, out_dtype=_abi.HYB_MXFP4, out_scale=FAKE)), None, 0,
+                            None) == 2  # (c not compiled)
+    # the MXFP4 indexer runs on the tensor cores only: 64 heads x 128 dims
+    a = _index_args(dtype=_abi.HYB_MXFP4, qI_scale=FAKE, kI_scale=FAKE)  # 4 heads x 32 dims
+    assert lib.csa_index_topk(ctypes.byref(a), None, 0, None) == 2
+    assert "MXFP4" in lib.hyb_last_error().decode()
+    a = _index_args(dtype=_abi.HYB_MXFP4)  # no scales
+    assert lib.csa_index_topk(ctypes.byref(a), None, 0, None) == 1
+
+
+def test_binding_maps_the_fp4_formats():
+    from sparse_attention_gated_b300 import ops
+
+    assert ops._DT[torch.float4_e2m1fn_x2] == _abi.HYB_MXFP4
+
+
 def _index_args(**kw):
     a = _abi.IndexArgs()
     a.qI = a.w = a.kI = a.idx = FAKE
