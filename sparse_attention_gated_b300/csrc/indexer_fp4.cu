@@ -7,10 +7,16 @@
 //
 // where q_i, k_i are e2m1 values and eq, ek the e8m0 scale bytes of their block of 32 dims.
 // The keys stay packed in HBM (64 bytes + 4 scale bytes per entry, against 132 for FP8).  On
-// chip every e2m1 value is written as the e4m3 byte of the same value (exact: e2m1's eight
-// magnitudes are all e4m3 numbers), and each 32-dim block is one tcgen05.mma kind::f8f6f4
-// (M = 128 entries, N = 64 heads, K = 32) into its own TMEM accumulator, so that the block's
-// exact integer-valued product (in units of 1/4) meets its two scales in the epilogue.
+// chip every e2m1 value is written as an e4m3 byte, and the products run as tcgen05.mma
+// kind::f8f6f4 (M = 128 entries, N = 64 heads, K = 32 per block), in one of two ways per tile:
+//   folded  (every key row of the tile and every head of the query has block exponents within
+//           8 of its largest, R): each value is written as the e4m3 byte of value * 2^(e - R),
+//           exact (e2m1's magnitudes 0.5 .. 6 times 2^0 .. 2^-8 are all e4m3 numbers), the four
+//           blocks accumulate into one TMEM accumulator, and the epilogue applies 2^(Rk + Rq
+//           - 254) per (entry, head), as the FP8 path applies its row scales;
+//   blocked (otherwise): each value is written as the e4m3 byte of the same value, each block
+//           is one product into its own accumulator, and the epilogue combines the four with
+//           their two scales.
 //
 // Roles (one CTA of 384 threads per SM, persistent over units = (query row, run of tiles)):
 //   warp 0      TMA producer: the unit's packed query rows, then per tile of 128 entries the
@@ -51,10 +57,12 @@ constexpr int kOffQ8 = kOffF8 + kS8 * kF8Bytes;
 constexpr int kOffRaw = kOffQ8 + 2 * kQ8Bytes;
 constexpr int kOffRawS = kOffRaw + kSR * kRawKeyBytes;
 constexpr int kOffRawQ = kOffRawS + kSR * kRawScaleBytes;
-constexpr int kOffKS = kOffRawQ + 2 * kRawQBytes;
-constexpr int kOffQS = kOffKS + kScaleRing * kRawScaleBytes;  // float [64][4] query block scales, then w [64]
-constexpr int kOffLut = kOffQS + kHeads * 5 * 4;              // uint16 [256]: packed byte -> two e4m3 bytes
-constexpr int kOffHist = kOffLut + 256 * 2;                   // 16-bit counters, two per word
+constexpr int kOffQ8f = kOffRawQ + 2 * kRawQBytes;            // the folded query tiles
+constexpr int kOffKS = kOffQ8f + 2 * kQ8Bytes;
+constexpr int kOffQS = kOffKS + kScaleRing * kRawScaleBytes;  // float [64][4] query block scales, [64] 2^(Rq-127), w [64]
+constexpr int kOffFlag = kOffQS + kHeads * 6 * 4;             // per scale slot: 1 = the tile is folded
+constexpr int kOffTab = kOffFlag + kScaleRing * 4;            // uint32 [9][2]: e4m3 bytes of e2m1 magnitudes * 2^-d
+constexpr int kOffHist = kOffTab + 9 * 2 * 4;                 // 16-bit counters, two per word
 constexpr int kOffBar = kOffHist + kTopkHistBins * 2;
 enum {
   kBarRawFull = 0,
@@ -115,19 +123,36 @@ __host__ __device__ constexpr uint32_t e2m1_to_e4m3(uint32_t v) {
   return (uint32_t)mag[v & 7u] | ((v & 8u) << 4);
 }
 
-// Expand one 8-byte piece (16 packed e2m1 values, element 2i in the low nibble of byte i)
-// into the 16 e4m3 bytes of the same values.
-__device__ __forceinline__ uint4 expand16(uint2 raw, const uint16_t* lut) {
-  const uint32_t w[2] = {raw.x, raw.y};
-  uint32_t o[4];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const uint32_t b0 = lut[w[h] & 0xFFu], b1 = lut[(w[h] >> 8) & 0xFFu], b2 = lut[(w[h] >> 16) & 0xFFu],
-                   b3 = lut[w[h] >> 24];
-    o[2 * h] = b0 | (b1 << 16);
-    o[2 * h + 1] = b2 | (b3 << 16);
-  }
-  return make_uint4(o[0], o[1], o[2], o[3]);
+// e4m3 byte of the e2m1 magnitude m (0..7) times 2^-d, d in 0..8: exact.  The magnitudes
+// are 1.0 or 1.5 times 2^-1 .. 2^2; scaled, a normal e4m3 number has exponent field E + 7 >= 1,
+// below that the subnormal (field 0) holds (2 + half) * 2^(E + 8) units of 2^-9.
+__host__ __device__ constexpr uint32_t e4m3_of_e2m1(uint32_t m, int d) {
+  constexpr int em[8] = {0, -1, 0, 0, 1, 1, 2, 2};
+  constexpr int hf[8] = {0, 0, 0, 1, 0, 1, 0, 1};
+  if (m == 0) return 0u;
+  const int E = em[m] - d, h = hf[m];
+  if (E >= -6) return (uint32_t)(((E + 7) << 3) | (h << 2));
+  return E == -9 ? 1u : (uint32_t)((2 + h) << (E + 8));
+}
+__host__ __device__ constexpr uint32_t mag_table(int d, int half) {
+  return e4m3_of_e2m1(4 * half, d) | (e4m3_of_e2m1(4 * half + 1, d) << 8) | (e4m3_of_e2m1(4 * half + 2, d) << 16) |
+         (e4m3_of_e2m1(4 * half + 3, d) << 24);
+}
+static_assert(mag_table(0, 0) == (e2m1_to_e4m3(0) | (e2m1_to_e4m3(1) << 8) | (e2m1_to_e4m3(2) << 16) |
+                                  (e2m1_to_e4m3(3) << 24)), "unscaled table");
+
+// e4m3 bytes of four packed e2m1 codes (the 16 low bits of v, element i in nibble i): the
+// nibbles' magnitudes select from the byte tables lo/hi (one byte permute), their signs
+// select 0x00 or 0x80 (another).
+__device__ __forceinline__ uint32_t expand4(uint32_t v, uint32_t lo, uint32_t hi) {
+  return __byte_perm(lo, hi, v & 0x7777u) | __byte_perm(0x00008000u, 0u, (v >> 3) & 0x1111u);
+}
+
+// Largest and smallest of a word's four e8m0 bytes
+__device__ __forceinline__ void exp_range(uint32_t w4, uint32_t& mx, uint32_t& mn) {
+  const uint32_t b0 = w4 & 0xFFu, b1 = (w4 >> 8) & 0xFFu, b2 = (w4 >> 16) & 0xFFu, b3 = w4 >> 24;
+  mx = max(max(b0, b1), max(b2, b3));
+  mn = min(min(b0, b1), min(b2, b3));
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -140,10 +165,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* raw = smem + kOffRaw;
   uint32_t* raw_s = reinterpret_cast<uint32_t*>(smem + kOffRawS);
   uint8_t* raw_q = smem + kOffRawQ;
+  uint8_t* q8f = smem + kOffQ8f;
   uint32_t* ks_ring = reinterpret_cast<uint32_t*>(smem + kOffKS);
   float* qs_t = reinterpret_cast<float*>(smem + kOffQS);  // [64][4]
-  float* w_t = qs_t + kHeads * 4;                          // [64]
-  uint16_t* lut = reinterpret_cast<uint16_t*>(smem + kOffLut);
+  float* qr_t = qs_t + kHeads * 4;                         // [64]: 2^(Rq[h] - 127)
+  float* w_t = qr_t + kHeads;                              // [64]
+  volatile int* tile_fast = reinterpret_cast<volatile int*>(smem + kOffFlag);
+  uint32_t* tab = reinterpret_cast<uint32_t*>(smem + kOffTab);
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kOffHist);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   volatile int* s_abort = reinterpret_cast<volatile int*>(bars + kNumBars);
@@ -166,8 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *s_abort = 0;
     tc::fence_barrier_init();
   }
-  for (int i = threadIdx.x; i < 256; i += kThreads)
-    lut[i] = (uint16_t)(e2m1_to_e4m3((uint32_t)i & 15u) | (e2m1_to_e4m3((uint32_t)i >> 4) << 8));
+  if (threadIdx.x < 18) tab[threadIdx.x] = mag_table(threadIdx.x >> 1, threadIdx.x & 1);
   if (warp == 1) tc::tmem_alloc(s_tmem, 512);
   if (warp == 0 && lane == 0) {
     tc::prefetch_tmap(&tm_keys);
@@ -217,9 +244,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 2 || warp == 3) {
     // ------------------------------------------------------------ expand packed -> e4m3
-    // 64 threads; thread x takes 16-byte output chunks x, x + 64, ... of a tile (row = chunk
-    // / 8, chunk c = chunk % 8 of the row, written at chunk c ^ (row & 7): 128-byte swizzle)
+    // 64 threads; thread x takes rows x and x + 64 of a key tile (row x of a query tile):
+    // the row's 64 packed bytes become its 128 e4m3 bytes, 16-byte chunk c of the row
+    // written at chunk c ^ (row & 7) (128-byte swizzle), each 32-dim block with its table.
     const int x = (warp - 2) * 32 + lane;
+    // one row: tables lo/hi per block (d = the block's distance below the row's largest
+    // exponent when folded, 0 otherwise)
+    auto convert_row = [&](const uint8_t* src, uint8_t* dst, int row, uint32_t w4, bool fold) {
+      uint32_t lo[4], hi[4];
+      uint32_t mx = 0, mn = 0;
+      if (fold) exp_range(w4, mx, mn);
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int d = fold ? (int)(mx - ((w4 >> (8 * b)) & 0xFFu)) : 0;
+        lo[b] = tab[2 * d], hi[b] = tab[2 * d + 1];
+      }
+      const uint4* s4 = reinterpret_cast<const uint4*>(src + row * kRowRaw);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {  // 16 packed bytes = 32 values = block q = output chunks 2q, 2q + 1
+        const uint4 v = s4[q];
+        const uint4 o0 = make_uint4(expand4(v.x, lo[q], hi[q]), expand4(v.x >> 16, lo[q], hi[q]),
+                                    expand4(v.y, lo[q], hi[q]), expand4(v.y >> 16, lo[q], hi[q]));
+        const uint4 o1 = make_uint4(expand4(v.z, lo[q], hi[q]), expand4(v.z >> 16, lo[q], hi[q]),
+                                    expand4(v.w, lo[q], hi[q]), expand4(v.w >> 16, lo[q], hi[q]));
+        *reinterpret_cast<uint4*>(dst + row * 128 + (((2 * q) ^ (row & 7)) << 4)) = o0;
+        *reinterpret_cast<uint4*>(dst + row * 128 + (((2 * q + 1) ^ (row & 7)) << 4)) = o1;
+      }
+    };
     int64_t seq = 0, qc = 0;
     bool ok = true;
     auto done = [&](uint64_t* bar) {
@@ -237,15 +288,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         okw = tc::mbar_wait(&bars[kBarRqFull + qb], qpar, s_abort, 3) &&
               tc::mbar_wait(&bars[kBarQ8Empty + qb], qpar ^ 1u, s_abort, 4);
       if (!(ok = __shfl_sync(0xffffffffu, okw, 0) != 0)) break;
+      // the query heads' block exponents (each warp reads all 64 heads: both decide alike)
+      const uint32_t* qsw = reinterpret_cast<const uint32_t*>(p.qI_scale) + U.row * kHeads;
+      const uint32_t qw0 = __ldg(qsw + lane), qw1 = __ldg(qsw + 32 + lane);
+      uint32_t qmx0, qmn0, qmx1, qmn1;
+      exp_range(qw0, qmx0, qmn0);
+      exp_range(qw1, qmx1, qmn1);
+      const bool unit_fold = __all_sync(0xffffffffu, qmx0 - qmn0 <= 8u && qmx1 - qmn1 <= 8u);
       {
-        const uint8_t* src = raw_q + qb * kRawQBytes;
-        uint8_t* dst = q8 + qb * kQ8Bytes;
-#pragma unroll 2
-        for (int ch = x; ch < kHeads * 8; ch += 64) {
-          const int r = ch >> 3, c = ch & 7;
-          const uint2 v = *reinterpret_cast<const uint2*>(src + r * kRowRaw + c * 8);
-          *reinterpret_cast<uint4*>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = expand16(v, lut);
-        }
+        // head x: its scale word is lane x's qw0 in warp 2 and lane x - 32's qw1 in warp 3
+        const uint32_t w4 = warp == 2 ? qw0 : qw1;
+        convert_row(raw_q + qb * kRawQBytes, q8 + qb * kQ8Bytes, x, w4, false);
+        if (unit_fold) convert_row(raw_q + qb * kRawQBytes, q8f + qb * kQ8Bytes, x, w4, true);
       }
       done(&bars[kBarQ8Full + qb]);
       if (lane == 0) tc::mbar_arrive(&bars[kBarRqEmpty + qb]);
@@ -259,13 +313,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::mbar_wait(&bars[kBarKsEmpty + r], (uint32_t)((seq / kScaleRing) & 1) ^ 1u, s_abort, 7);
         if (!(ok = __shfl_sync(0xffffffffu, okw, 0) != 0)) break;
         const uint8_t* src = raw + rs * kRawKeyBytes;
+        const uint32_t* sw = raw_s + rs * kTileE;
         uint8_t* dst = f8 + s8 * kF8Bytes;
-#pragma unroll 4
-        for (int ch = x; ch < kTileE * 8; ch += 64) {
-          const int rr = ch >> 3, c = ch & 7;
-          const uint2 v = *reinterpret_cast<const uint2*>(src + rr * kRowRaw + c * 8);
-          *reinterpret_cast<uint4*>(dst + rr * 128 + ((c ^ (rr & 7)) << 4)) = expand16(v, lut);
+        // folded when every key row of the tile (each warp checks all 128) and the query allow it
+        bool fold = unit_fold;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t mx, mn;
+          exp_range(sw[32 * i + lane], mx, mn);
+          fold = fold && mx - mn <= 8u;
         }
+        fold = __all_sync(0xffffffffu, fold);
+        convert_row(src, dst, x, sw[x], fold);
+        convert_row(src, dst, x + 64, sw[x + 64], fold);
+        if (x == 0) tile_fast[r] = fold ? 1 : 0;
         ks_ring[r * kTileE + x] = raw_s[rs * kTileE + x];
         ks_ring[r * kTileE + 64 + x] = raw_s[rs * kTileE + 64 + x];
         done(&bars[kBarF8Full + s8]);
@@ -286,17 +347,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (U.tile_begin >= U.tile_end) continue;
         const int qb = (int)(qc & 1);
         if (!(ok = tc::mbar_wait(&bars[kBarQ8Full + qb], (uint32_t)((qc >> 1) & 1), s_abort, 8))) break;
-        const uint32_t b_base = tc::smem_u32(q8 + qb * kQ8Bytes);
+        const uint32_t b_plain = tc::smem_u32(q8 + qb * kQ8Bytes), b_fold = tc::smem_u32(q8f + qb * kQ8Bytes);
         for (int64_t t = U.tile_begin; t < U.tile_end; ++t, ++seq) {
           const int s8 = (int)(seq % kS8), acc = (int)(seq % kAcc);
           if (!(ok = tc::mbar_wait(&bars[kBarAccEmpty + acc], (uint32_t)((seq / kAcc) & 1) ^ 1u, s_abort, 9))) break;
           if (!(ok = tc::mbar_wait(&bars[kBarF8Full + s8], (uint32_t)((seq / kS8) & 1), s_abort, 10))) break;
           tc::tc_fence_after();
           const uint32_t a_base = tc::smem_u32(f8 + s8 * kF8Bytes);
+          if (tile_fast[seq % kScaleRing]) {
+            // folded: the four blocks into one accumulator
 #pragma unroll
-          for (int k = 0; k < 4; ++k)  // block k (dims 32k .. 32k+31): its own accumulator
-            tc::mma_f8f6f4(tmem + (uint32_t)(acc * 4 * kHeads + k * kHeads), tc::desc_kmajor_sw128(a_base + 32 * k),
-                           tc::desc_kmajor_sw128(b_base + 32 * k), idesc, 0u);
+            for (int k = 0; k < 4; ++k)
+              tc::mma_f8f6f4(tmem + (uint32_t)(acc * 4 * kHeads), tc::desc_kmajor_sw128(a_base + 32 * k),
+                             tc::desc_kmajor_sw128(b_fold + 32 * k), idesc, k > 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)  // block k (dims 32k .. 32k+31): its own accumulator
+              tc::mma_f8f6f4(tmem + (uint32_t)(acc * 4 * kHeads + k * kHeads), tc::desc_kmajor_sw128(a_base + 32 * k),
+                             tc::desc_kmajor_sw128(b_plain + 32 * k), idesc, 0u);
+          }
           tc::mma_commit(&bars[kBarF8Empty + s8]);
           tc::mma_commit(&bars[kBarAccFull + acc]);
         }
@@ -350,7 +419,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const uint8_t* qsb = p.qI_scale + U.row * (kHeads * 4);
         for (int i = et; i < kHeads * 4; i += kEpiThreads) qs_t[i] = e8m0_value(__ldg(qsb + i));
-        for (int i = et; i < kHeads; i += kEpiThreads) w_t[i] = __ldg(p.w + U.row * kHeads + i);
+        for (int i = et; i < kHeads; i += kEpiThreads) {
+          uint32_t mx, mn;
+          exp_range(__ldg(reinterpret_cast<const uint32_t*>(qsb) + i), mx, mn);
+          qr_t[i] = e8m0_value(mx);
+          w_t[i] = __ldg(p.w + U.row * kHeads + i);
+        }
       }
       if (!(ok = esync())) break;
       const int64_t vis = visible_checked(query_pos(p.q_pos, p.q_pos0, U.row, U.j), p.m, p.n_entries, p.dev_status,
@@ -364,11 +438,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = quad * 32 + lane;
         const int64_t s = t * kTileE + row;
         const uint32_t kw = ks_ring[r * kTileE + row];
-        float ksf[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) ksf[k] = e8m0_value((kw >> (8 * k)) & 0xFFu);
         const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 4 * kHeads);
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        float ksf[4];
+        if (tile_fast[r]) {
+          // folded tile: S[e,h] * 2^(Rk[e] - 127) * 2^(Rq[h] - 127)
+          uint32_t mx, mn;
+          exp_range(kw, mx, mn);
+          const float kr = e8m0_value(mx);
+#pragma unroll
+          for (int hb = 0; hb < kHeads; hb += 32) {
+            float v[32];
+            tc::tmem_ld32(taddr + (uint32_t)hb, v);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int h = 0; h < 32; ++h) ps[h & 3] = fmaf(w_t[hb + h], fmaxf(v[h] * (kr * qr_t[hb + h]), 0.f), ps[h & 3]);
+          }
+        } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) ksf[k] = e8m0_value((kw >> (8 * k)) & 0xFFu);
 #pragma unroll
         for (int hb = 0; hb < kHeads; hb += 32) {
           float dot[32];
@@ -384,6 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int h = 0; h < 32; ++h) ps[h & 3] = fmaf(w_t[hb + h], fmaxf(dot[h], 0.f), ps[h & 3]);
+        }
         }
         const float score = (ps[0] + ps[1]) + (ps[2] + ps[3]);
         tc::tc_fence_before();

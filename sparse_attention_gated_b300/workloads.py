@@ -132,10 +132,11 @@ class _Draw:
 
 def _indexer_values(d: _Draw, shape, dtype):
     """Indexer queries/keys: N(0,1), cast to e4m3 by torch, plus per-row scales U(0.5, 1.5);
-    for MXFP4, uniformly random e2m1 codes (two per byte) and e8m0 block scales 2^-7 .. 2^6."""
+    for MXFP4, uniformly random e2m1 codes (two per byte) and e8m0 block scales 2^-5 .. 2^3
+    (a row's blocks within 8 binades of each other, as for rows of similar-sized values)."""
     if dtype == torch.float4_e2m1fn_x2:
         codes = torch.randint(0, 256, shape[:-1] + (shape[-1] // 2,), generator=d.g, device=d.device, dtype=torch.uint8)
-        scales = torch.randint(120, 134, shape[:-1] + (shape[-1] // 32,), generator=d.g, device=d.device,
+        scales = torch.randint(122, 131, shape[:-1] + (shape[-1] // 32,), generator=d.g, device=d.device,
                                dtype=torch.uint8)
         return codes.view(torch.float4_e2m1fn_x2), scales.view(torch.float8_e8m0fnu)
     x = d.normal(shape)

@@ -67,14 +67,17 @@ def test_compress_mxfp4_output_is_the_oracle_quantiser_of_the_float_result(c, m,
     assert np.all(np.abs(dec - to_np(ref32)) <= 2.0 * step + 1e-12)  # (half a step; up to 2 steps where saturated)
 
 
-def _fp4_case(seed, B, n_q, N):
+def _fp4_case(seed, B, n_q, N, lo=120, hi=134):
+    """Random codes; scale bytes in [lo, hi): a row's block exponents within 8 of each other
+    for hi - lo <= 9 (the kernel folds them into the values), wider otherwise (it keeps the
+    blocks apart)."""
     g = torch.Generator(device=DEV)
     g.manual_seed(seed)
-    r = lambda shape, lo, hi: torch.randint(lo, hi, shape, generator=g, device=DEV, dtype=torch.uint8)
+    r = lambda shape, a, b: torch.randint(a, b, shape, generator=g, device=DEV, dtype=torch.uint8)
     qI = r((B, n_q, 64, 64), 0, 256).view(torch.float4_e2m1fn_x2)
-    qs = r((B, n_q, 64, 4), 120, 134).view(torch.float8_e8m0fnu)
+    qs = r((B, n_q, 64, 4), lo, hi).view(torch.float8_e8m0fnu)
     kI = r((B, N, 64), 0, 256).view(torch.float4_e2m1fn_x2)
-    ks = r((B, N, 4), 120, 134).view(torch.float8_e8m0fnu)
+    ks = r((B, N, 4), lo, hi).view(torch.float8_e8m0fnu)
     w = torch.rand((B, n_q, 64), generator=g, device=DEV)
     return qI, qs, kI, ks, w
 
@@ -84,15 +87,16 @@ def _decoded(codes_t, scales_t):
     return oracle.mxfp4_decode(_unpack(codes_t), scales_t.view(torch.uint8).cpu().numpy()).astype(np.float32)
 
 
+@pytest.mark.parametrize("lo,hi", [(120, 134), (121, 130), (112, 121)])
 @pytest.mark.parametrize("B,n_q,N,m,k,q_pos0", [
     (3, 1, 5000, 4, 512, 4 * 5000 - 1),      # decode rows: 40 tiles, the last ragged
     (2, 1, 20000, 4, 1024, 4 * 20000 - 1),   # longer rows, two runs per row
     (1, 10, 700, 4, 256, 4 * 690 - 1),       # several queries, each its own visible count
     (2, 1, 300, 4, 512, 4 * 300 - 1),        # fewer entries than k: all kept
 ])
-def test_index_topk_mxfp4_matches_oracle(B, n_q, N, m, k, q_pos0):
+def test_index_topk_mxfp4_matches_oracle(B, n_q, N, m, k, q_pos0, lo, hi):
     ops = _ops()
-    qI, qs, kI, ks, w = _fp4_case(61 + N, B, n_q, N)
+    qI, qs, kI, ks, w = _fp4_case(61 + N, B, n_q, N, lo, hi)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     idx, sc = ops.csa_index_topk(qI, w, kI, m=m, k=k, q_pos0=q_pos0, qI_scale=qs, kI_scale=ks, want_scores=True,
                                  dev_status=st)
@@ -108,6 +112,30 @@ def test_index_topk_mxfp4_matches_oracle(B, n_q, N, m, k, q_pos0):
             # the kernel's scores of the selected entries: exact block products, float32 sums
             r_ = ref[b, j][sel]
             assert np.all(np.abs(gsc[b, j][: len(sel)] - r_) <= 1e-4 * np.maximum(np.abs(r_), 1.0))
+
+
+def test_mxfp4_tiles_folded_and_blocked_in_one_row():
+    """Scale spreads within 8 binades everywhere except a few key rows, which put their tiles
+    on the blocked path while the neighbouring tiles stay folded, and one query head out of
+    range in the second sequence, which keeps all of that query's tiles blocked."""
+    ops = _ops()
+    B, N, m, k = 2, 3000, 4, 256
+    qI, qs, kI, ks, w = _fp4_case(71, B, 1, N, 122, 130)
+    ksb = ks.view(torch.uint8)
+    ksb[0, 300, 2] = 135                # tile 2 of sequence 0: one row spread 13
+    ksb[0, 2047, 0] = 110               # tile 15
+    qs.view(torch.uint8)[1, 0, 17, 3] = 140  # sequence 1: a head spread 18
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    idx, sc = ops.csa_index_topk(qI, w, kI, m=m, k=k, q_pos0=m * N - 1, qI_scale=qs, kI_scale=ks, want_scores=True,
+                                 dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    ref = oracle.index_scores(_decoded(qI, qs), to_np(w), _decoded(kI, ks), m=m, q_pos0=m * N - 1)
+    for b in range(B):
+        g = to_np(idx)[b, 0]
+        check_topk_row(g, ref[b, 0], N, k)
+        r_ = ref[b, 0][g]
+        assert np.all(np.abs(to_np(sc)[b, 0] - r_) <= 1e-4 * np.maximum(np.abs(r_), 1.0))
 
 
 def test_pro_1m_decode_with_mxfp4_indexer_keys_full_size():
