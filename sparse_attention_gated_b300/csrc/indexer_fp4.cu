@@ -18,15 +18,18 @@
 //           is one product into its own accumulator, and the epilogue combines the four with
 //           their two scales.
 //
-// Roles (one CTA of 384 threads per SM, persistent over units = (query row, run of tiles)):
+// Roles (one CTA of 448 threads per SM, persistent over units = (query row, run of tiles)):
 //   warp 0      TMA producer: the unit's packed query rows, then per tile of 128 entries the
 //               packed keys (8 KiB) and their scale words (512 B) into a ring;
-//   warps 2-3   expand packed tiles into e4m3 tiles (128-byte swizzle) for the MMA, and hand
-//               the scale words to the epilogue;
-//   warp 1      TMEM owner and MMA issuer (four K = 32 products per tile, one per block);
-//   warps 4-11  epilogue in two groups taking alternate tiles: the four block accumulators
-//               of an entry row, the scales, ReLU and the head weights, one float32 score
-//               per (query, entry), and (decode) the row's 12-bit score-key histogram.
+//   warps 2, 3, 12, 13  expand packed tiles into e4m3 tiles (128-byte swizzle) for the MMA,
+//               32 rows each, and hand the scale words to the epilogue;
+//   warp 1      TMEM owner and MMA issuer;
+//   warps 4-11  epilogue in two groups taking alternate tiles: an entry row's products, the
+//               scales, ReLU and the head weights, one float32 score per (query, entry), and
+//               (decode) the row's 12-bit score-key histogram.
+// Accumulators: 8 slots of 64 TMEM columns (tile i in slot i % 8), so that the MMA runs up to
+// 8 tiles ahead of the epilogue; a folded tile takes one turn of its slot, a blocked tile four
+// (block k's product, read and released by the epilogue before block k + 1's is issued).
 // Every wait is bounded (about 1 s): on expiry HYB_DEV_TIMEOUT is raised, the CTA's own copies
 // and products in flight land, TMEM is freed and the kernel returns.
 #include "kernels.cuh"
@@ -46,9 +49,10 @@ constexpr int kRawQBytes = kHeads * kRowRaw;      // 4 KiB
 constexpr int kQ8Bytes = kHeads * 128;            // 8 KiB
 constexpr int kSR = 8;                      // packed-tile ring
 constexpr int kS8 = 4;                      // e4m3 tile ring
-constexpr int kAcc = 2;                     // accumulator sets (4 blocks x 64 columns each)
+constexpr int kAcc = 8;                     // accumulator slots of 64 columns
 constexpr int kScaleRing = kS8 + kAcc;      // scale words on their way to the epilogue
-constexpr int kThreads = 384;
+constexpr int kThreads = 448;               // 14 warps: 4 on the busiest scheduler, so <= 128 registers each
+constexpr int kConv = 4;                    // converter warps
 constexpr int kEpiWarp0 = 4, kEpiWarps = 8, kEpiGroups = 2;
 constexpr int kEpiThreads = kEpiWarps * 32;
 
@@ -62,8 +66,11 @@ constexpr int kOffKS = kOffQ8f + 2 * kQ8Bytes;
 constexpr int kOffQS = kOffKS + kScaleRing * kRawScaleBytes;  // float [64][4] query block scales, [64] 2^(Rq-127), w [64]
 constexpr int kOffFlag = kOffQS + kHeads * 6 * 4;             // per scale slot: 1 = the tile is folded
 constexpr int kOffTab = kOffFlag + kScaleRing * 4;            // uint32 [9][2]: e4m3 bytes of e2m1 magnitudes * 2^-d
-constexpr int kOffHist = kOffTab + 9 * 2 * 4;                 // 16-bit counters, two per word
+constexpr int kOffHist = (kOffTab + 9 * 2 * 4 + 15) / 16 * 16;  // 16-bit counters, two per word (read as uint4)
 constexpr int kOffBar = kOffHist + kTopkHistBins * 2;
+static_assert(kOffF8 % 1024 == 0 && kOffQ8 % 1024 == 0 && kOffQ8f % 1024 == 0, "128-byte swizzled tiles");
+static_assert(kOffRaw % 128 == 0 && kOffRawS % 128 == 0 && kOffRawQ % 128 == 0, "TMA destinations");
+static_assert(kOffKS % 16 == 0 && kOffQS % 16 == 0 && kOffHist % 16 == 0 && kOffBar % 8 == 0, "vector and mbarrier alignment");
 enum {
   kBarRawFull = 0,
   kBarRawEmpty = kBarRawFull + kSR,
@@ -179,16 +186,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kSR; ++i) tc::mbar_init(&bars[kBarRawFull + i], 1), tc::mbar_init(&bars[kBarRawEmpty + i], 2);
-    for (int i = 0; i < kS8; ++i) tc::mbar_init(&bars[kBarF8Full + i], 2), tc::mbar_init(&bars[kBarF8Empty + i], 1);
+    for (int i = 0; i < kSR; ++i) tc::mbar_init(&bars[kBarRawFull + i], 1), tc::mbar_init(&bars[kBarRawEmpty + i], kConv);
+    for (int i = 0; i < kS8; ++i) tc::mbar_init(&bars[kBarF8Full + i], kConv), tc::mbar_init(&bars[kBarF8Empty + i], 1);
     for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&bars[kBarRqFull + i], 1), tc::mbar_init(&bars[kBarRqEmpty + i], 2);
-      tc::mbar_init(&bars[kBarQ8Full + i], 2), tc::mbar_init(&bars[kBarQ8Empty + i], 1);
+      tc::mbar_init(&bars[kBarRqFull + i], 1), tc::mbar_init(&bars[kBarRqEmpty + i], kConv);
+      tc::mbar_init(&bars[kBarQ8Full + i], kConv), tc::mbar_init(&bars[kBarQ8Empty + i], 1);
     }
     for (int i = 0; i < kAcc; ++i)
       tc::mbar_init(&bars[kBarAccFull + i], 1), tc::mbar_init(&bars[kBarAccEmpty + i], kEpiWarps / kEpiGroups);
     for (int i = 0; i < kScaleRing; ++i)
-      tc::mbar_init(&bars[kBarKsFull + i], 2), tc::mbar_init(&bars[kBarKsEmpty + i], kEpiWarps / kEpiGroups);
+      tc::mbar_init(&bars[kBarKsFull + i], kConv), tc::mbar_init(&bars[kBarKsEmpty + i], kEpiWarps / kEpiGroups);
     tc::mbar_init(&bars[kBarDone], 1);
     tc::mbar_init(&bars[kBarEpi], kEpiThreads);
     *s_abort = 0;
@@ -242,12 +249,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 2 || warp == 3) {
+  } else if (warp == 2 || warp == 3 || warp >= kEpiWarp0 + kEpiWarps) {
     // ------------------------------------------------------------ expand packed -> e4m3
-    // 64 threads; thread x takes rows x and x + 64 of a key tile (row x of a query tile):
-    // the row's 64 packed bytes become its 128 e4m3 bytes, 16-byte chunk c of the row
-    // written at chunk c ^ (row & 7) (128-byte swizzle), each 32-dim block with its table.
-    const int x = (warp - 2) * 32 + lane;
+    // 128 threads; thread x takes row x of a key tile (of a query tile: rows x of the plain
+    // copy for x < 64, rows x - 64 of the folded copy otherwise): the row's 64 packed bytes
+    // become its 128 e4m3 bytes, 16-byte chunk c of the row written at chunk c ^ (row & 7)
+    // (128-byte swizzle), each 32-dim block with its table.
+    const int cw = warp < kEpiWarp0 ? warp - 2 : warp - (kEpiWarp0 + kEpiWarps) + 2;  // 0..3
+    const int x = cw * 32 + lane;
     // one row: tables lo/hi per block (d = the block's distance below the row's largest
     // exponent when folded, 0 otherwise)
     auto convert_row = [&](const uint8_t* src, uint8_t* dst, int row, uint32_t w4, bool fold) {
@@ -296,10 +305,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       exp_range(qw1, qmx1, qmn1);
       const bool unit_fold = __all_sync(0xffffffffu, qmx0 - qmn0 <= 8u && qmx1 - qmn1 <= 8u);
       {
-        // head x: its scale word is lane x's qw0 in warp 2 and lane x - 32's qw1 in warp 3
-        const uint32_t w4 = warp == 2 ? qw0 : qw1;
-        convert_row(raw_q + qb * kRawQBytes, q8 + qb * kQ8Bytes, x, w4, false);
-        if (unit_fold) convert_row(raw_q + qb * kRawQBytes, q8f + qb * kQ8Bytes, x, w4, true);
+        // head x & 63: its scale word is this lane's qw0 (heads 0-31) or qw1 (heads 32-63)
+        const uint32_t w4 = (cw & 1) ? qw1 : qw0;
+        if (cw < 2)
+          convert_row(raw_q + qb * kRawQBytes, q8 + qb * kQ8Bytes, x, w4, false);
+        else if (unit_fold)
+          convert_row(raw_q + qb * kRawQBytes, q8f + qb * kQ8Bytes, x - 64, w4, true);
       }
       done(&bars[kBarQ8Full + qb]);
       if (lane == 0) tc::mbar_arrive(&bars[kBarRqEmpty + qb]);
@@ -325,10 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fold = __all_sync(0xffffffffu, fold);
         convert_row(src, dst, x, sw[x], fold);
-        convert_row(src, dst, x + 64, sw[x + 64], fold);
         if (x == 0) tile_fast[r] = fold ? 1 : 0;
-        ks_ring[r * kTileE + x] = raw_s[rs * kTileE + x];
-        ks_ring[r * kTileE + 64 + x] = raw_s[rs * kTileE + 64 + x];
+        ks_ring[r * kTileE + x] = sw[x];
         done(&bars[kBarF8Full + s8]);
         if (lane == 0) {
           tc::mbar_arrive(&bars[kBarKsFull + r]);
@@ -341,6 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tc::elect_one()) {
       constexpr uint32_t idesc = tc::make_idesc(0, 0, 0, 0, kTileE, kHeads);  // e4m3 x e4m3, both K-major
       int64_t seq = 0, qc = 0;
+      uint32_t turns[kAcc] = {0, 0, 0, 0, 0, 0, 0, 0};  // completed turns of each slot
       bool ok = true;
       for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
         const Fp4Unit U = fp4_unit(p, u);
@@ -348,26 +358,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qb = (int)(qc & 1);
         if (!(ok = tc::mbar_wait(&bars[kBarQ8Full + qb], (uint32_t)((qc >> 1) & 1), s_abort, 8))) break;
         const uint32_t b_plain = tc::smem_u32(q8 + qb * kQ8Bytes), b_fold = tc::smem_u32(q8f + qb * kQ8Bytes);
-        for (int64_t t = U.tile_begin; t < U.tile_end; ++t, ++seq) {
-          const int s8 = (int)(seq % kS8), acc = (int)(seq % kAcc);
-          if (!(ok = tc::mbar_wait(&bars[kBarAccEmpty + acc], (uint32_t)((seq / kAcc) & 1) ^ 1u, s_abort, 9))) break;
+        for (int64_t t = U.tile_begin; t < U.tile_end && ok; ++t, ++seq) {
+          const int s8 = (int)(seq % kS8), a = (int)(seq % kAcc);
+          const uint32_t d = tmem + (uint32_t)(a * kHeads);
           if (!(ok = tc::mbar_wait(&bars[kBarF8Full + s8], (uint32_t)((seq / kS8) & 1), s_abort, 10))) break;
-          tc::tc_fence_after();
           const uint32_t a_base = tc::smem_u32(f8 + s8 * kF8Bytes);
           if (tile_fast[seq % kScaleRing]) {
-            // folded: the four blocks into one accumulator
+            // folded: the four blocks into one accumulator, one turn of the slot
+            if (!(ok = tc::mbar_wait(&bars[kBarAccEmpty + a], (turns[a] & 1u) ^ 1u, s_abort, 9))) break;
+            tc::tc_fence_after();
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              tc::mma_f8f6f4(tmem + (uint32_t)(acc * 4 * kHeads), tc::desc_kmajor_sw128(a_base + 32 * k),
-                             tc::desc_kmajor_sw128(b_fold + 32 * k), idesc, k > 0 ? 1u : 0u);
+              tc::mma_f8f6f4(d, tc::desc_kmajor_sw128(a_base + 32 * k), tc::desc_kmajor_sw128(b_fold + 32 * k), idesc,
+                             k > 0 ? 1u : 0u);
+            tc::mma_commit(&bars[kBarAccFull + a]);
+            ++turns[a];
           } else {
-#pragma unroll
-            for (int k = 0; k < 4; ++k)  // block k (dims 32k .. 32k+31): its own accumulator
-              tc::mma_f8f6f4(tmem + (uint32_t)(acc * 4 * kHeads + k * kHeads), tc::desc_kmajor_sw128(a_base + 32 * k),
-                             tc::desc_kmajor_sw128(b_plain + 32 * k), idesc, 0u);
+            // blocked: block k (dims 32k .. 32k+31) alone, one turn of the slot each
+            for (int k = 0; k < 4 && ok; ++k) {
+              if (!(ok = tc::mbar_wait(&bars[kBarAccEmpty + a], (turns[a] & 1u) ^ 1u, s_abort, 9))) break;
+              tc::tc_fence_after();
+              tc::mma_f8f6f4(d, tc::desc_kmajor_sw128(a_base + 32 * k), tc::desc_kmajor_sw128(b_plain + 32 * k), idesc,
+                             0u);
+              tc::mma_commit(&bars[kBarAccFull + a]);
+              ++turns[a];
+            }
+            if (!ok) break;
           }
           tc::mma_commit(&bars[kBarF8Empty + s8]);
-          tc::mma_commit(&bars[kBarAccFull + acc]);
         }
         if (!ok) break;
         tc::mma_commit(&bars[kBarQ8Empty + qb]);
@@ -377,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_wait_drain(&bars[kBarDone], 0);
     }
     __syncwarp();
-  } else if (warp >= kEpiWarp0) {
+  } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const int et = threadIdx.x - kEpiWarp0 * 32;
     const int quad = warp & 3;
@@ -406,6 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (clear) h4[0] = h4[1] = make_uint4(0u, 0u, 0u, 0u);
     };
     int64_t seq = 0;
+    uint32_t turns[kAcc / kEpiGroups] = {0, 0, 0, 0};  // completed turns of this group's slots (grp, grp + 2, ..)
     bool ok = true;
     for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
       const Fp4Unit U = fp4_unit(p, u);
@@ -431,56 +450,62 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           lane == 0 && U.tile_begin == 0);
       for (int64_t t = U.tile_begin; t < U.tile_end; ++t, ++seq) {
         if ((int)(seq & 1) != grp) continue;  // the other group's tile
-        const int acc = (int)(seq % kAcc), r = (int)(seq % kScaleRing);
-        if (!(ok = tc::mbar_wait(&bars[kBarAccFull + acc], (uint32_t)((seq / kAcc) & 1), s_abort, 12))) break;
+        const int a = (int)(seq % kAcc), r = (int)(seq % kScaleRing);
+        uint32_t& turn = turns[a >> 1];
         if (!(ok = tc::mbar_wait(&bars[kBarKsFull + r], (uint32_t)((seq / kScaleRing) & 1), s_abort, 13))) break;
-        tc::tc_fence_after();
         const int row = quad * 32 + lane;
         const int64_t s = t * kTileE + row;
         const uint32_t kw = ks_ring[r * kTileE + row];
-        const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 4 * kHeads);
+        const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(a * kHeads);
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
-        float ksf[4];
-        if (tile_fast[r]) {
-          // folded tile: S[e,h] * 2^(Rk[e] - 127) * 2^(Rq[h] - 127)
-          uint32_t mx, mn;
-          exp_range(kw, mx, mn);
-          const float kr = e8m0_value(mx);
+        // one turn of the slot: wait for the product, hand this row's heads to use(hb, v) 32 at
+        // a time, release the slot
+        auto take = [&](auto&& use) -> bool {
+          if (!tc::mbar_wait(&bars[kBarAccFull + a], turn & 1u, s_abort, 12)) return false;
+          tc::tc_fence_after();
 #pragma unroll
           for (int hb = 0; hb < kHeads; hb += 32) {
             float v[32];
             tc::tmem_ld32(taddr + (uint32_t)hb, v);
             tc::tmem_ld_wait();
-#pragma unroll
-            for (int h = 0; h < 32; ++h) ps[h & 3] = fmaf(w_t[hb + h], fmaxf(v[h] * (kr * qr_t[hb + h]), 0.f), ps[h & 3]);
+            use(hb, v);
           }
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&bars[kBarAccEmpty + a]);
+          ++turn;
+          return true;
+        };
+        if (tile_fast[r]) {
+          // folded tile: S[e,h] * 2^(Rk[e] - 127) * 2^(Rq[h] - 127)
+          uint32_t mx, mn;
+          exp_range(kw, mx, mn);
+          const float kr = e8m0_value(mx);
+          ok = take([&](int hb, const float (&v)[32]) {
+#pragma unroll
+            for (int h = 0; h < 32; ++h)
+              ps[h & 3] = fmaf(w_t[hb + h], fmaxf(v[h] * (kr * qr_t[hb + h]), 0.f), ps[h & 3]);
+          });
+          if (!ok) break;
         } else {
+          // blocked tile: the four blocks' products, each with its two scales
+          float dot[kHeads];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) ksf[k] = e8m0_value((kw >> (8 * k)) & 0xFFu);
+          for (int h = 0; h < kHeads; ++h) dot[h] = 0.f;
+          for (int k = 0; k < 4 && ok; ++k) {
+            const float ksk = e8m0_value((kw >> (8 * k)) & 0xFFu);
+            ok = take([&](int hb, const float (&v)[32]) {
 #pragma unroll
-        for (int hb = 0; hb < kHeads; hb += 32) {
-          float dot[32];
-#pragma unroll
-          for (int h = 0; h < 32; ++h) dot[h] = 0.f;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            float v[32];
-            tc::tmem_ld32(taddr + (uint32_t)(k * kHeads + hb), v);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int h = 0; h < 32; ++h) dot[h] = fmaf(v[h] * ksf[k], qs_t[(hb + h) * 4 + k], dot[h]);
+              for (int h = 0; h < 32; ++h) dot[hb + h] = fmaf(v[h] * ksk, qs_t[(hb + h) * 4 + k], dot[hb + h]);
+            });
           }
+          if (!ok) break;
 #pragma unroll
-          for (int h = 0; h < 32; ++h) ps[h & 3] = fmaf(w_t[hb + h], fmaxf(dot[h], 0.f), ps[h & 3]);
-        }
+          for (int h = 0; h < kHeads; ++h) ps[h & 3] = fmaf(w_t[h], fmaxf(dot[h], 0.f), ps[h & 3]);
         }
         const float score = (ps[0] + ps[1]) + (ps[2] + ps[3]);
-        tc::tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          tc::mbar_arrive(&bars[kBarAccEmpty + acc]);
-          tc::mbar_arrive(&bars[kBarKsEmpty + r]);
-        }
+        if (lane == 0) tc::mbar_arrive(&bars[kBarKsEmpty + r]);
         const bool keep = s < vis;
         if (keep) p.scores[U.row * p.score_stride + s] = score;
         if (do_hist) {
