@@ -21,17 +21,19 @@
 // Roles (one CTA of 448 threads per SM, persistent over units = (query row, run of tiles)):
 //   warp 0      TMA producer: the unit's packed query rows, then per tile of 128 entries the
 //               packed keys (8 KiB) and their scale words (512 B) into a ring;
-//   warps 2, 3, 12, 13  expand packed tiles into e4m3 tiles (128-byte swizzle) for the MMA,
-//               32 rows each, and hand the scale words to the epilogue;
 //   warp 1      TMEM owner and MMA issuer;
-//   warps 4-11  epilogue in two groups taking alternate tiles: an entry row's products, the
-//               scales, ReLU and the head weights, one float32 score per (query, entry), and
-//               (decode) the row's 12-bit score-key histogram.
+//   warps 2-5   expand packed tiles into e4m3 tiles (128-byte swizzle) for the MMA, 32 rows
+//               per warp, and the unit's query rows, and hand the scale words to the epilogue;
+//   warps 6-13  epilogue in two groups of four taking alternate tiles: an entry row's
+//               products, the scales, ReLU and the head weights, one float32 score per
+//               (query, entry), and (decode) the row's 12-bit score-key histogram.
 // Accumulators: 8 slots of 64 TMEM columns (tile i in slot i % 8), so that the MMA runs up to
 // 8 tiles ahead of the epilogue; a folded tile takes one turn of its slot, a blocked tile four
 // (block k's product, read and released by the epilogue before block k + 1's is issued).
 // Every wait is bounded (about 1 s): on expiry HYB_DEV_TIMEOUT is raised, the CTA's own copies
 // and products in flight land, TMEM is freed and the kernel returns.
+#include <type_traits>
+
 #include "kernels.cuh"
 #include "tc_common.cuh"
 
@@ -52,8 +54,10 @@ constexpr int kS8 = 4;                      // e4m3 tile ring
 constexpr int kAcc = 8;                     // accumulator slots of 64 columns
 constexpr int kScaleRing = kS8 + kAcc;      // scale words on their way to the epilogue
 constexpr int kThreads = 448;               // 14 warps: 4 on the busiest scheduler, so <= 128 registers each
-constexpr int kConv = 4;                    // converter warps
-constexpr int kEpiWarp0 = 4, kEpiWarps = 8, kEpiGroups = 2;
+constexpr int kConvWarp0 = 2, kConvGroups = 1;
+constexpr int kConv = 4;                    // converter warps per group (one tile's arrivals)
+constexpr int kEpiWarp0 = kConvWarp0 + kConvGroups * kConv, kEpiWarps = 8, kEpiGroups = 2;
+static_assert((kEpiWarp0 + kEpiWarps) * 32 == kThreads, "warp roles");
 constexpr int kEpiThreads = kEpiWarps * 32;
 
 constexpr int kOffF8 = 0;
@@ -90,7 +94,7 @@ enum {
 };
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 64 + 1024;  // + flags + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kTopkHistBins / 2 == 8 * kEpiThreads, "one 8-word slice of the histogram per epilogue thread");
+static_assert(kTopkHistBins % 16 == 0, "the histogram in 8-word slices");
 
 struct Fp4Params {
   const float* w;
@@ -175,8 +179,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* q8f = smem + kOffQ8f;
   uint32_t* ks_ring = reinterpret_cast<uint32_t*>(smem + kOffKS);
   float* qs_t = reinterpret_cast<float*>(smem + kOffQS);  // [64][4]
-  float* qr_t = qs_t + kHeads * 4;                         // [64]: 2^(Rq[h] - 127)
-  float* w_t = qr_t + kHeads;                              // [64]
+  float* wq_t = qs_t + kHeads * 4;                         // [64]: w[h] * 2^(Rq[h] - 127)
+  float* w_t = wq_t + kHeads;                              // [64]
   volatile int* tile_fast = reinterpret_cast<volatile int*>(smem + kOffFlag);
   uint32_t* tab = reinterpret_cast<uint32_t*>(smem + kOffTab);
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kOffHist);
@@ -249,13 +253,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 2 || warp == 3 || warp >= kEpiWarp0 + kEpiWarps) {
+  } else if (warp >= kConvWarp0 && warp < kEpiWarp0) {
     // ------------------------------------------------------------ expand packed -> e4m3
-    // 128 threads; thread x takes row x of a key tile (of a query tile: rows x of the plain
+    // kConvGroups groups of 128 threads, group g taking the tiles with seq % kConvGroups == g;
+    // thread x of a group takes row x of a key tile (group 0, of the unit's query tile: rows x of the plain
     // copy for x < 64, rows x - 64 of the folded copy otherwise): the row's 64 packed bytes
     // become its 128 e4m3 bytes, 16-byte chunk c of the row written at chunk c ^ (row & 7)
     // (128-byte swizzle), each 32-dim block with its table.
-    const int cw = warp < kEpiWarp0 ? warp - 2 : warp - (kEpiWarp0 + kEpiWarps) + 2;  // 0..3
+    const int cgrp = (warp - kConvWarp0) / kConv, cw = (warp - kConvWarp0) % kConv;
     const int x = cw * 32 + lane;
     // one row: tables lo/hi per block (d = the block's distance below the row's largest
     // exponent when folded, 0 otherwise)
@@ -293,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qb = (int)(qc & 1);
       const uint32_t qpar = (uint32_t)((qc >> 1) & 1);
       int okw = 1;
-      if (lane == 0)
+      if (lane == 0 && cgrp == 0)
         okw = tc::mbar_wait(&bars[kBarRqFull + qb], qpar, s_abort, 3) &&
               tc::mbar_wait(&bars[kBarQ8Empty + qb], qpar ^ 1u, s_abort, 4);
       if (!(ok = __shfl_sync(0xffffffffu, okw, 0) != 0)) break;
@@ -304,18 +309,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       exp_range(qw0, qmx0, qmn0);
       exp_range(qw1, qmx1, qmn1);
       const bool unit_fold = __all_sync(0xffffffffu, qmx0 - qmn0 <= 8u && qmx1 - qmn1 <= 8u);
-      {
+      if (cgrp == 0) {
         // head x & 63: its scale word is this lane's qw0 (heads 0-31) or qw1 (heads 32-63)
         const uint32_t w4 = (cw & 1) ? qw1 : qw0;
         if (cw < 2)
           convert_row(raw_q + qb * kRawQBytes, q8 + qb * kQ8Bytes, x, w4, false);
         else if (unit_fold)
           convert_row(raw_q + qb * kRawQBytes, q8f + qb * kQ8Bytes, x - 64, w4, true);
+        done(&bars[kBarQ8Full + qb]);
+        if (lane == 0) tc::mbar_arrive(&bars[kBarRqEmpty + qb]);
       }
-      done(&bars[kBarQ8Full + qb]);
-      if (lane == 0) tc::mbar_arrive(&bars[kBarRqEmpty + qb]);
       ++qc;
       for (int64_t t = U.tile_begin; t < U.tile_end && ok; ++t, ++seq) {
+        if ((int)(seq % kConvGroups) != cgrp) continue;  // the other group's tile
         const int rs = (int)(seq % kSR), s8 = (int)(seq % kS8), r = (int)(seq % kScaleRing);
         okw = 1;
         if (lane == 0)
@@ -399,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int et = threadIdx.x - kEpiWarp0 * 32;
     const int quad = warp & 3;
-    const int grp = (warp - kEpiWarp0) / 4;  // tiles with seq % 2 == grp
+    const int grp = (warp - kEpiWarp0) / 4;  // tiles with seq % kEpiGroups == grp
     uint32_t ephase = 0;
     auto esync = [&]() -> bool {
       tc::mbar_arrive(&bars[kBarEpi]);
@@ -412,19 +418,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (do_hist)
       for (int i = et; i < kTopkHistBins / 2; i += kEpiThreads) hist[i] = 0;
     auto flush_hist = [&](bool clear) {
-      uint4* h4 = reinterpret_cast<uint4*>(hist) + 2 * et;
-      const uint4 a = h4[0], b = h4[1];
-      const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-      uint32_t* g = p.ghist + hist_row * kTopkHistBins + 16 * et;
+      for (int sl = et; sl < kTopkHistBins / 16; sl += kEpiThreads) {  // slice sl: bins 16 sl .. 16 sl + 15
+        uint4* h4 = reinterpret_cast<uint4*>(hist) + 2 * sl;
+        const uint4 a = h4[0], b = h4[1];
+        const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        uint32_t* g = p.ghist + hist_row * kTopkHistBins + 16 * sl;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (v[i] & 0xFFFFu) atomicAdd(g + 2 * i, v[i] & 0xFFFFu);
-        if (v[i] >> 16) atomicAdd(g + 2 * i + 1, v[i] >> 16);
+        for (int i = 0; i < 8; ++i) {
+          if (v[i] & 0xFFFFu) atomicAdd(g + 2 * i, v[i] & 0xFFFFu);
+          if (v[i] >> 16) atomicAdd(g + 2 * i + 1, v[i] >> 16);
+        }
+        if (clear) h4[0] = h4[1] = make_uint4(0u, 0u, 0u, 0u);
       }
-      if (clear) h4[0] = h4[1] = make_uint4(0u, 0u, 0u, 0u);
     };
     int64_t seq = 0;
-    uint32_t turns[kAcc / kEpiGroups] = {0, 0, 0, 0};  // completed turns of this group's slots (grp, grp + 2, ..)
+    uint32_t turns[kAcc / kEpiGroups] = {};  // completed turns of this group's slots (grp, grp + kEpiGroups, ..)
     bool ok = true;
     for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
       const Fp4Unit U = fp4_unit(p, u);
@@ -441,17 +449,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = et; i < kHeads; i += kEpiThreads) {
           uint32_t mx, mn;
           exp_range(__ldg(reinterpret_cast<const uint32_t*>(qsb) + i), mx, mn);
-          qr_t[i] = e8m0_value(mx);
           w_t[i] = __ldg(p.w + U.row * kHeads + i);
+          wq_t[i] = w_t[i] * e8m0_value(mx);
         }
       }
       if (!(ok = esync())) break;
       const int64_t vis = visible_checked(query_pos(p.q_pos, p.q_pos0, U.row, U.j), p.m, p.n_entries, p.dev_status,
                                           lane == 0 && U.tile_begin == 0);
       for (int64_t t = U.tile_begin; t < U.tile_end; ++t, ++seq) {
-        if ((int)(seq & 1) != grp) continue;  // the other group's tile
+        if ((int)(seq % kEpiGroups) != grp) continue;  // another group's tile
         const int a = (int)(seq % kAcc), r = (int)(seq % kScaleRing);
-        uint32_t& turn = turns[a >> 1];
+        uint32_t& turn = turns[a / kEpiGroups];
         if (!(ok = tc::mbar_wait(&bars[kBarKsFull + r], (uint32_t)((seq / kScaleRing) & 1), s_abort, 13))) break;
         const int row = quad * 32 + lane;
         const int64_t s = t * kTileE + row;
@@ -459,16 +467,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(a * kHeads);
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
         // one turn of the slot: wait for the product, hand this row's heads to use(hb, v) 32 at
-        // a time, release the slot
-        auto take = [&](auto&& use) -> bool {
+        // a time (both loads in flight at once when kBoth), release the slot
+        auto take = [&](auto both, auto&& use) -> bool {
           if (!tc::mbar_wait(&bars[kBarAccFull + a], turn & 1u, s_abort, 12)) return false;
           tc::tc_fence_after();
-#pragma unroll
-          for (int hb = 0; hb < kHeads; hb += 32) {
-            float v[32];
-            tc::tmem_ld32(taddr + (uint32_t)hb, v);
+          if constexpr (decltype(both)::value) {
+            float v0[32], v1[32];
+            tc::tmem_ld32(taddr, v0);
+            tc::tmem_ld32(taddr + 32u, v1);
             tc::tmem_ld_wait();
-            use(hb, v);
+            use(0, v0);
+            use(32, v1);
+          } else {
+#pragma unroll
+            for (int hb = 0; hb < kHeads; hb += 32) {
+              float v[32];
+              tc::tmem_ld32(taddr + (uint32_t)hb, v);
+              tc::tmem_ld_wait();
+              use(hb, v);
+            }
           }
           tc::tc_fence_before();
           __syncwarp();
@@ -477,16 +494,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           return true;
         };
         if (tile_fast[r]) {
-          // folded tile: S[e,h] * 2^(Rk[e] - 127) * 2^(Rq[h] - 127)
+          // folded tile: S[e,h] * 2^(Rk[e] - 127) * 2^(Rq[h] - 127); the two powers of two
+          // are positive and exact, so 2^(Rk[e] - 127) * sum_h (w[h] 2^(Rq[h] - 127)) ReLU(S[e,h])
+          ok = take(std::true_type{}, [&](int hb, const float (&v)[32]) {
+            const float4* wq4 = reinterpret_cast<const float4*>(wq_t + hb);
+#pragma unroll
+            for (int h4 = 0; h4 < 8; ++h4) {
+              const float4 c = wq4[h4];
+              ps[0] = fmaf(c.x, fmaxf(v[4 * h4 + 0], 0.f), ps[0]);
+              ps[1] = fmaf(c.y, fmaxf(v[4 * h4 + 1], 0.f), ps[1]);
+              ps[2] = fmaf(c.z, fmaxf(v[4 * h4 + 2], 0.f), ps[2]);
+              ps[3] = fmaf(c.w, fmaxf(v[4 * h4 + 3], 0.f), ps[3]);
+            }
+          });
+          if (!ok) break;
           uint32_t mx, mn;
           exp_range(kw, mx, mn);
           const float kr = e8m0_value(mx);
-          ok = take([&](int hb, const float (&v)[32]) {
 #pragma unroll
-            for (int h = 0; h < 32; ++h)
-              ps[h & 3] = fmaf(w_t[hb + h], fmaxf(v[h] * (kr * qr_t[hb + h]), 0.f), ps[h & 3]);
-          });
-          if (!ok) break;
+          for (int i = 0; i < 4; ++i) ps[i] *= kr;
         } else {
           // blocked tile: the four blocks' products, each with its two scales
           float dot[kHeads];
@@ -494,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int h = 0; h < kHeads; ++h) dot[h] = 0.f;
           for (int k = 0; k < 4 && ok; ++k) {
             const float ksk = e8m0_value((kw >> (8 * k)) & 0xFFu);
-            ok = take([&](int hb, const float (&v)[32]) {
+            ok = take(std::false_type{}, [&](int hb, const float (&v)[32]) {
 #pragma unroll
               for (int h = 0; h < 32; ++h) dot[hb + h] = fmaf(v[h] * ksk, qs_t[(hb + h) * 4 + k], dot[hb + h]);
             });
