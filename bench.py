@@ -110,6 +110,8 @@ def stage_model(w, proj=None):
 # (dram__bytes_read.sum + dram__bytes_write.sum) on a workload with the current
 # build of that kernel; absent where no capture of the current kernel exists
 KERNEL_NCU_TRAFFIC = {
+    # index_tc_kernel<1>: 138.52 MB read (keys, scales, queries) + 6.60 MB written (scores, histograms)
+    ("pro_1m_hybrid_decode", "index_scores"): 138_524_672 + 6_600_960,
     ("pro_1m_hybrid_decode", "csa_attend"): 5_348_096,
     ("pro_1m_hybrid_decode", "hca_attend"): 34_682_624 + 52_736,
     ("pro_1m_hybrid_decode", "topk"): 4_410_368,
