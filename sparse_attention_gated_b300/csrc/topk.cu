@@ -18,8 +18,9 @@
 //                    (key > T, key == T) flags gives each kept element's slot,
 //                    so no sort is needed.
 // Plans:
-//   one stage   (rows of at most kStageCap visible entries): one CTA per row
-//               stages the keys in shared memory, selects and collects.
+//   one stage   (rows of at most kStageCap visible entries, unless few rows of more
+//               than kGridMinEntries take the grid plan): one CTA per row stages the
+//               keys in shared memory, selects and collects.
 //   three kernels (longer rows, e.g. 262,144 entries at 1M context):
 //     hist    CTA (chunk, row): 12-bit histogram of its chunk, added into the
 //             row's global histogram (the tensor-core indexer builds it in its
@@ -66,6 +67,7 @@ constexpr int kHistBins = kTopkHistBins;
 constexpr int kMaxChunks = 64;
 constexpr int kPer = 8;  // keys a thread loads before using them (histogram and filter passes)
 constexpr int64_t kGridChunkCap = 32768;  // grid plan: keys per CTA, staged in shared memory
+constexpr int64_t kGridMinEntries = 4096; // shorter rows always take the one-stage plan
 constexpr int kCandListCap = 4096;        // grid plan: candidates per row selected in shared memory
 constexpr int kSubListCap = 1024;         // grid plan, overflow: sub-candidates per row ranked directly
 constexpr int kGridSlot = 8;              // grid plan: published counts per CTA
@@ -1153,8 +1155,10 @@ static bool grid_plan_fits(int64_t chunk) {
 
 static TopkPlan plan_topk(const hyb_index_args* a, int64_t n_vis_max) {
   TopkPlan pl{0, 0, 0};
-  if (n_vis_max <= kStageCap) return pl;
   const int64_t rows = a->batch * a->n_q;
+  // a short row stays on one CTA unless the rows are too few to fill the GPU (decode of a
+  // few sequences): then the grid plan spreads each row over at least 8 SMs
+  if (n_vis_max <= kStageCap && !(n_vis_max > kGridMinEntries && rows * 8 <= kNumSMs)) return pl;
   if (rows <= kNumSMs) {
     // grid plan: up to one CTA per SM, the row's entries split evenly
     const int64_t P = kNumSMs / rows;
