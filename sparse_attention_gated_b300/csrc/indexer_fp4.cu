@@ -32,8 +32,6 @@
 // (block k's product, read and released by the epilogue before block k + 1's is issued).
 // Every wait is bounded (about 1 s): on expiry HYB_DEV_TIMEOUT is raised, the CTA's own copies
 // and products in flight land, TMEM is freed and the kernel returns.
-#include <type_traits>
-
 #include "kernels.cuh"
 #include "tc_common.cuh"
 
@@ -356,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tc::elect_one()) {
       constexpr uint32_t idesc = tc::make_idesc(0, 0, 0, 0, kTileE, kHeads);  // e4m3 x e4m3, both K-major
       int64_t seq = 0, qc = 0;
-      uint32_t turns[kAcc] = {0, 0, 0, 0, 0, 0, 0, 0};  // completed turns of each slot
+      uint32_t tpar = 0;  // bit a: parity of slot a's completed turns (a register, not an indexed array)
       bool ok = true;
       for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
         const Fp4Unit U = fp4_unit(p, u);
@@ -371,23 +369,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a_base = tc::smem_u32(f8 + s8 * kF8Bytes);
           if (tile_fast[seq % kScaleRing]) {
             // folded: the four blocks into one accumulator, one turn of the slot
-            if (!(ok = tc::mbar_wait(&bars[kBarAccEmpty + a], (turns[a] & 1u) ^ 1u, s_abort, 9))) break;
+            if (!(ok = tc::mbar_wait(&bars[kBarAccEmpty + a], ((tpar >> a) & 1u) ^ 1u, s_abort, 9))) break;
             tc::tc_fence_after();
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               tc::mma_f8f6f4(d, tc::desc_kmajor_sw128(a_base + 32 * k), tc::desc_kmajor_sw128(b_fold + 32 * k), idesc,
                              k > 0 ? 1u : 0u);
             tc::mma_commit(&bars[kBarAccFull + a]);
-            ++turns[a];
+            tpar ^= 1u << a;
           } else {
             // blocked: block k (dims 32k .. 32k+31) alone, one turn of the slot each
             for (int k = 0; k < 4 && ok; ++k) {
-              if (!(ok = tc::mbar_wait(&bars[kBarAccEmpty + a], (turns[a] & 1u) ^ 1u, s_abort, 9))) break;
+              if (!(ok = tc::mbar_wait(&bars[kBarAccEmpty + a], ((tpar >> a) & 1u) ^ 1u, s_abort, 9))) break;
               tc::tc_fence_after();
               tc::mma_f8f6f4(d, tc::desc_kmajor_sw128(a_base + 32 * k), tc::desc_kmajor_sw128(b_plain + 32 * k), idesc,
                              0u);
               tc::mma_commit(&bars[kBarAccFull + a]);
-              ++turns[a];
+              tpar ^= 1u << a;
             }
             if (!ok) break;
           }
@@ -432,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     int64_t seq = 0;
-    uint32_t turns[kAcc / kEpiGroups] = {};  // completed turns of this group's slots (grp, grp + kEpiGroups, ..)
+    uint32_t tpar = 0;  // bit a: parity of slot a's completed turns (this group's slots only)
     bool ok = true;
     for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
       const Fp4Unit U = fp4_unit(p, u);
@@ -459,71 +457,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t t = U.tile_begin; t < U.tile_end; ++t, ++seq) {
         if ((int)(seq % kEpiGroups) != grp) continue;  // another group's tile
         const int a = (int)(seq % kAcc), r = (int)(seq % kScaleRing);
-        uint32_t& turn = turns[a / kEpiGroups];
         if (!(ok = tc::mbar_wait(&bars[kBarKsFull + r], (uint32_t)((seq / kScaleRing) & 1), s_abort, 13))) break;
         const int row = quad * 32 + lane;
         const int64_t s = t * kTileE + row;
         const uint32_t kw = ks_ring[r * kTileE + row];
         const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(a * kHeads);
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
-        // one turn of the slot: wait for the product, hand this row's heads to use(hb, v) 32 at
-        // a time (both loads in flight at once when kBoth), release the slot
-        auto take = [&](auto both, auto&& use) -> bool {
-          if (!tc::mbar_wait(&bars[kBarAccFull + a], turn & 1u, s_abort, 12)) return false;
+        // one turn of the slot: wait for its product; once it is read, release the slot
+        auto turn_wait = [&]() -> bool {
+          if (!tc::mbar_wait(&bars[kBarAccFull + a], (tpar >> a) & 1u, s_abort, 12)) return false;
           tc::tc_fence_after();
-          if constexpr (decltype(both)::value) {
-            float v0[32], v1[32];
-            tc::tmem_ld32(taddr, v0);
-            tc::tmem_ld32(taddr + 32u, v1);
-            tc::tmem_ld_wait();
-            use(0, v0);
-            use(32, v1);
-          } else {
-#pragma unroll
-            for (int hb = 0; hb < kHeads; hb += 32) {
-              float v[32];
-              tc::tmem_ld32(taddr + (uint32_t)hb, v);
-              tc::tmem_ld_wait();
-              use(hb, v);
-            }
-          }
+          return true;
+        };
+        auto turn_release = [&]() {
           tc::tc_fence_before();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&bars[kBarAccEmpty + a]);
-          ++turn;
-          return true;
+          tpar ^= 1u << a;
         };
         if (tile_fast[r]) {
           // folded tile: S[e,h] * 2^(Rk[e] - 127) * 2^(Rq[h] - 127); the two powers of two
           // are positive and exact, so 2^(Rk[e] - 127) * sum_h (w[h] 2^(Rq[h] - 127)) ReLU(S[e,h])
-          ok = take(std::true_type{}, [&](int hb, const float (&v)[32]) {
-            const float4* wq4 = reinterpret_cast<const float4*>(wq_t + hb);
+          if (!(ok = turn_wait())) break;
+          float v0[32], v1[32];
+          tc::tmem_ld32(taddr, v0);
+          tc::tmem_ld32(taddr + 32u, v1);
+          tc::tmem_ld_wait();
+          turn_release();
+          const float4* wq4 = reinterpret_cast<const float4*>(wq_t);
 #pragma unroll
-            for (int h4 = 0; h4 < 8; ++h4) {
-              const float4 c = wq4[h4];
-              ps[0] = fmaf(c.x, fmaxf(v[4 * h4 + 0], 0.f), ps[0]);
-              ps[1] = fmaf(c.y, fmaxf(v[4 * h4 + 1], 0.f), ps[1]);
-              ps[2] = fmaf(c.z, fmaxf(v[4 * h4 + 2], 0.f), ps[2]);
-              ps[3] = fmaf(c.w, fmaxf(v[4 * h4 + 3], 0.f), ps[3]);
-            }
-          });
-          if (!ok) break;
+          for (int h4 = 0; h4 < 8; ++h4) {
+            const float4 c = wq4[h4];
+            ps[0] = fmaf(c.x, fmaxf(v0[4 * h4 + 0], 0.f), ps[0]);
+            ps[1] = fmaf(c.y, fmaxf(v0[4 * h4 + 1], 0.f), ps[1]);
+            ps[2] = fmaf(c.z, fmaxf(v0[4 * h4 + 2], 0.f), ps[2]);
+            ps[3] = fmaf(c.w, fmaxf(v0[4 * h4 + 3], 0.f), ps[3]);
+          }
+#pragma unroll
+          for (int h4 = 0; h4 < 8; ++h4) {
+            const float4 c = wq4[8 + h4];
+            ps[0] = fmaf(c.x, fmaxf(v1[4 * h4 + 0], 0.f), ps[0]);
+            ps[1] = fmaf(c.y, fmaxf(v1[4 * h4 + 1], 0.f), ps[1]);
+            ps[2] = fmaf(c.z, fmaxf(v1[4 * h4 + 2], 0.f), ps[2]);
+            ps[3] = fmaf(c.w, fmaxf(v1[4 * h4 + 3], 0.f), ps[3]);
+          }
           uint32_t mx, mn;
           exp_range(kw, mx, mn);
           const float kr = e8m0_value(mx);
 #pragma unroll
           for (int i = 0; i < 4; ++i) ps[i] *= kr;
         } else {
-          // blocked tile: the four blocks' products, each with its two scales
+          // blocked tile: the four blocks' products (one turn each), each with its two scales
           float dot[kHeads];
 #pragma unroll
           for (int h = 0; h < kHeads; ++h) dot[h] = 0.f;
           for (int k = 0; k < 4 && ok; ++k) {
+            if (!(ok = turn_wait())) break;
             const float ksk = e8m0_value((kw >> (8 * k)) & 0xFFu);
-            ok = take(std::false_type{}, [&](int hb, const float (&v)[32]) {
+#pragma unroll
+            for (int hb = 0; hb < kHeads; hb += 32) {
+              float v[32];
+              tc::tmem_ld32(taddr + (uint32_t)hb, v);
+              tc::tmem_ld_wait();
 #pragma unroll
               for (int h = 0; h < 32; ++h) dot[hb + h] = fmaf(v[h] * ksk, qs_t[(hb + h) * 4 + k], dot[hb + h]);
-            });
+            }
+            turn_release();
           }
           if (!ok) break;
 #pragma unroll
