@@ -519,6 +519,7 @@ EXTRA_CONFIGS = (
     ("pro_1m_parallel_decode", "concat", 20),
     ("pro_1m_hybrid_decode", "per_layer", 20),
     ("pro_1m_hybrid_decode_fp4", None, 20),
+    ("pro_1m_hybrid_decode_in_branch", None, 20),
     ("pro_csa_prefill", None, 3),
 )
 
@@ -551,7 +552,7 @@ def run_ours(args, w):
     # snapshot step with its whole block tails and windows re-sent is reported beside it.
     e2e_snap = run_e2e(args, w, steps[0], stream, units, world, dist)
     e2e = e2e_snap
-    if w.kind == "hybrid_decode" and w.idx_fmt == "e4m3":
+    if w.kind == "hybrid_decode" and w.idx_fmt == "e4m3" and not w.in_branch:
         e2e = run_e2e_session(args, w, stream, world, dist)
     out = {
         "metric": METRIC,
@@ -826,8 +827,9 @@ def _csa_parts(st, stream, rec, scoring_events=None):
                        scores_events=scoring_events)
     rec("csa_index_topk", 1)
     rec("csa_attend", 0)
+    st.in_branch_csa(stream)
     ops.csa_attend(x["q"], kc, kc, b["idx"], scale=w.scale, o=b["o"], lse=b["lse"], workspace=st.ws["csa"],
-                   dev_status=s, stream=stream, window=st._win_csa(as_dict=True))
+                   dev_status=s, stream=stream, window=st._win_csa(as_dict=True), sink=st.sink("csa"))
     rec("csa_attend", 1)
 
 
@@ -844,8 +846,10 @@ def _hca_parts(st, stream, rec):
                          dev_status=s, stream=stream)
     rec("hca_compress", 1)
     rec("hca_attend", 0)
+    st.in_branch_hca(stream)
     ops.hca_attend(q, kc, kc, m=w.m_hca, q_pos0=w.q_pos0, scale=w.scale, o=b["o_h"], lse=b["lse_h"],
-                   workspace=st.ws["hca"], dev_status=s, stream=stream, window=st._win_hca(as_dict=True))
+                   workspace=st.ws["hca"], dev_status=s, stream=stream, window=st._win_hca(as_dict=True),
+                   sink=st.sink("hca"))
     rec("hca_attend", 1)
 
 
@@ -865,6 +869,9 @@ def _launches_per_step(w, proj=None):
         n += 2 + 2 + 1  # compress x2, index scores + top-k, attention with the window merge fused
     if w.kind in ("hybrid_decode", "hca_decode", "parallel_decode"):
         n += 1
+    if w.in_branch:
+        # per branch: RMSNorm + RoPE of the queries and of the completed entry, the sink
+        n += 3 * ((w.kind in ("hybrid_decode", "csa_decode")) + (w.kind in ("hybrid_decode", "hca_decode")))
     if proj is not None:
         n += proj["calls"]
     return n
@@ -964,6 +971,17 @@ def oracle_query(w, x, b, proj=None):
     t = w.n_ctx - 1
     sl = slice(b, b + 1)
     outs = []
+
+    def in_branch(q, entry):
+        # RMSNorm + partial RoPE of the queries and of the completed entry, at the query's position
+        if not w.in_branch:
+            return q
+        oracle.rope_partial(oracle.rmsnorm(entry), t)
+        return oracle.rope_partial(oracle.rmsnorm(q.float().numpy()), t).astype(np.float32)
+
+    def sink(out_lse, key):
+        return oracle.sink_merge(out_lse[0], out_lse[1], x[key])[0] if w.in_branch else out_lse[0]
+
     if w.kind == "swa_decode":
         q = x["q"][sl]
         o, _ = oracle.swa_merge(q, x["kv"][sl], x["kv"][sl], w.n_ctx - w.n_win, t, w.n_win, w.scale,
@@ -971,8 +989,8 @@ def oracle_query(w, x, b, proj=None):
         outs.append(o)
     if w.kind in ("hybrid_decode", "csa_decode", "parallel_decode"):
         N = w.n_csa
-        oracle.compress(x["ca"][sl], x["za"][sl], x["bias"], w.m, cb=x["cb"][sl], zb=x["zb"][sl], overlap=True,
-                        first_block=N - 2)
+        entry = oracle.compress(x["ca"][sl], x["za"][sl], x["bias"], w.m, cb=x["cb"][sl], zb=x["zb"][sl], overlap=True,
+                                first_block=N - 2)
         kIn = oracle.compress(x["kIa"][sl], x["zIa"][sl], x["biasI"], w.m, cb=x["kIb"][sl], zb=x["zIb"][sl],
                               overlap=True, first_block=N - 2)
         if w.idx_fmt == "mxfp4":
@@ -990,17 +1008,19 @@ def oracle_query(w, x, b, proj=None):
             s = oracle.index_scores(x["qI"][sl], x["w"][sl], x["kI"][sl], m=w.m, q_pos0=t,
                                     qI_scale=x["qI_scale"][sl], kI_scale=x["kI_scale"][sl])
         idx = oracle.topk(s, [[N]], w.k)
-        o, l = oracle.csa_attend(x["q"][sl], x["kc"][sl], x["kc"][sl], idx, w.scale)
-        outs.append(oracle.swa_merge(x["q"][sl], x["kv"][sl], x["kv"][sl], w.n_ctx - w.n_win, t, w.n_win, w.scale,
-                                     o, l)[0])
+        q = in_branch(x["q"][sl], entry)
+        o, l = oracle.csa_attend(q, x["kc"][sl], x["kc"][sl], idx, w.scale)
+        outs.append(sink(oracle.swa_merge(q, x["kv"][sl], x["kv"][sl], w.n_ctx - w.n_win, t, w.n_win, w.scale, o, l),
+                         "sink"))
     if w.kind in ("hybrid_decode", "hca_decode", "parallel_decode"):
         sfx = "_h" if w.kind in ("hybrid_decode", "parallel_decode") else ""
         qsfx = "_h" if w.kind == "hybrid_decode" else ""
         kc = x["kc" + sfx][sl]
-        oracle.compress(x["ch"][sl], x["zh"][sl], x["bias_h"], w.m_hca, first_block=w.n_hca - 1)
-        o, l = oracle.hca_attend(x["q" + qsfx][sl], kc, kc, m=w.m_hca, q_pos0=t, scale=w.scale)
-        outs.append(oracle.swa_merge(x["q" + qsfx][sl], x["kv" + qsfx][sl], x["kv" + qsfx][sl], w.n_ctx - w.n_win, t,
-                                     w.n_win, w.scale, o, l)[0])
+        entry = oracle.compress(x["ch"][sl], x["zh"][sl], x["bias_h"], w.m_hca, first_block=w.n_hca - 1)
+        q = in_branch(x["q" + qsfx][sl], entry)
+        o, l = oracle.hca_attend(q, kc, kc, m=w.m_hca, q_pos0=t, scale=w.scale)
+        outs.append(sink(oracle.swa_merge(q, x["kv" + qsfx][sl], x["kv" + qsfx][sl], w.n_ctx - w.n_win, t, w.n_win,
+                                          w.scale, o, l), "sink_h" if w.kind == "hybrid_decode" else "sink"))
     if proj is not None:
         if w.kind == "parallel_decode":  # one projection of the concatenated heads
             oracle.grouped_out_proj(np.concatenate(outs, axis=-2), proj["w"])

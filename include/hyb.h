@@ -446,7 +446,10 @@ HYB_API hyb_status swa_merge(const hyb_swa_args* a, void* workspace, size_t ws_b
  *   pos[r / rows_per_pos] (int64 absolute positions, rows_per_pos >= 1, e.g.
  *   n_h for a query's heads; NULL with rope_dims > 0 is an error).
  * Float32 arithmetic; the angle is formed and reduced in float64, so that
- * positions in the millions keep full float32 accuracy.  No workspace.
+ * positions in the millions keep full float32 accuracy.  row_stride: elements
+ * from one row to the next (0 = c; otherwise an even number >= c), so that one
+ * call reaches strided rows such as one cache slot of every sequence.  No
+ * workspace.
  * ------------------------------------------------------------------------ */
 typedef struct hyb_norm_rope_args {
   void* x;
@@ -459,6 +462,7 @@ typedef struct hyb_norm_rope_args {
   int64_t rows_per_pos;
   int64_t rope_dims;
   double theta;
+  int64_t row_stride;
 } hyb_norm_rope_args;
 
 HYB_API hyb_status hyb_rmsnorm_rope(const hyb_norm_rope_args* a, void* stream);

@@ -55,7 +55,7 @@ class HcaAttendArgs(ctypes.Structure):
 
 class NormRopeArgs(ctypes.Structure):
     _fields_ = [("x", _p), ("rows", _i64), ("c", _i64), ("gamma", _p), ("eps", _f), ("dtype", _i32), ("pos", _p),
-                ("rows_per_pos", _i64), ("rope_dims", _i64), ("theta", ctypes.c_double)]
+                ("rows_per_pos", _i64), ("rope_dims", _i64), ("theta", ctypes.c_double), ("row_stride", _i64)]
 
 
 class GprojArgs(ctypes.Structure):

@@ -604,6 +604,8 @@ hyb_status hyb_rmsnorm_rope(const hyb_norm_rope_args* a, void* stream) {
     return fail(HYB_ERR_INVALID_ARG, "hyb_rmsnorm_rope: rope_dims must be even and <= c");
   if (a->rope_dims > 0 && (!a->pos || a->rows_per_pos < 1 || !(a->theta > 0.0)))
     return fail(HYB_ERR_INVALID_ARG, "hyb_rmsnorm_rope: rotation needs pos, rows_per_pos >= 1 and theta > 0");
+  if (a->row_stride != 0 && (a->row_stride < a->c || a->row_stride % 2 != 0))
+    return fail(HYB_ERR_INVALID_ARG, "hyb_rmsnorm_rope: row_stride must be 0 or an even number >= c");
   if (a->rows == 0) return ok();
   if (!a->x) return fail(HYB_ERR_INVALID_ARG, "hyb_rmsnorm_rope: x is NULL");
   if (!aligned(a->x, 2 * elem_size(a->dtype)) || !aligned(a->gamma, 4) || !aligned(a->pos, 8))

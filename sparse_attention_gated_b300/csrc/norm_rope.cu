@@ -20,6 +20,7 @@ struct NormRopeParams {
   const int64_t* pos;
   int64_t rows_per_pos, rope_dims;
   double theta;
+  int64_t row_stride;  // elements from one row to the next
 };
 
 template <typename T>
@@ -44,7 +45,7 @@ __global__ void __launch_bounds__(256) norm_rope_kernel(NormRopeParams p) {
   const int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (r >= p.rows) return;
-  T* x = static_cast<T*>(p.x) + r * p.c;
+  T* x = static_cast<T*>(p.x) + r * p.row_stride;
   const int64_t n_pairs = p.c / 2;
   float ss = 0.f;
   for (int64_t i = lane; i < n_pairs; i += 32) {
@@ -77,6 +78,7 @@ cudaError_t launch_norm_rope(const hyb_norm_rope_args* a, cudaStream_t s) {
   NormRopeParams p;
   p.x = a->x, p.rows = a->rows, p.c = a->c, p.gamma = a->gamma, p.eps = a->eps, p.pos = a->pos;
   p.rows_per_pos = a->rows_per_pos, p.rope_dims = a->rope_dims, p.theta = a->theta;
+  p.row_stride = a->row_stride > 0 ? a->row_stride : a->c;
   if (p.rows == 0) return cudaSuccess;
   const int64_t blocks = (p.rows + 7) / 8;
   if (blocks >= (int64_t(1) << 31)) return cudaErrorInvalidConfiguration;

@@ -360,18 +360,28 @@ def rmsnorm_rope(x, *, gamma=None, eps: float = 1e-6, pos=None, rows_per_pos: in
                  theta: float = 10000.0, stream=None):
     """In place: RMSNorm of every row of x [..., c] (float32 or bf16), then rotary
     encoding of its last rope_dims dimensions at positions pos (int64, one per
-    rows_per_pos consecutive rows; rope_dims=0 or pos=None: no rotation).  Returns x."""
+    rows_per_pos consecutive rows; rope_dims=0 or pos=None: no rotation).  x is
+    contiguous, or a 2-D view [rows, c] of unit column stride whose rows are evenly
+    spaced (e.g. one cache slot of every sequence).  Returns x."""
     c = x.shape[-1]
     rows = x.numel() // c
+    row_stride = 0
+    if not x.is_contiguous():
+        if x.dim() != 2 or x.stride(1) != 1 or x.stride(0) < c:
+            raise ValueError("x must be contiguous or a [rows, c] view with unit column stride")
+        row_stride = x.stride(0)
     if pos is not None and (pos.dtype != torch.int64 or pos.numel() * rows_per_pos < rows):
         raise ValueError("pos must be int64 with one position per rows_per_pos rows")
     if gamma is not None and (gamma.dtype != torch.float32 or gamma.numel() != c):
         raise ValueError("gamma must be float32 [c]")
     a = _abi.NormRopeArgs()
-    a.x, a.rows, a.c = _ptr(x), rows, c
+    if not x.is_cuda:
+        raise ValueError("tensors passed to the hybrid-attention library must be CUDA tensors")
+    a.x, a.rows, a.c = ctypes.c_void_p(x.data_ptr()), rows, c
     a.gamma, a.eps, a.dtype = _ptr(gamma), eps, _dtype(x)
     a.pos, a.rows_per_pos = _ptr(pos), rows_per_pos
     a.rope_dims, a.theta = (rope_dims if pos is not None else 0), theta
+    a.row_stride = row_stride
     _abi.check(_abi.load().hyb_rmsnorm_rope(ctypes.byref(a), _stream(stream)), "hyb_rmsnorm_rope")
     return x
 

@@ -91,6 +91,11 @@ class HybridStep:
                 g_h, d_h = proj["w_h"].shape[:2]
                 self.buf["proj_h"] = torch.empty((B, n_q, g_h * d_h), dtype=torch.float32, device=dev)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+        if w.in_branch:
+            if not w.decode or w.kind in ("parallel_decode", "swa_decode"):
+                raise ValueError("the in-branch operations are built for CSA / HCA / hybrid decode steps")
+            # the query's position: its RoPE, and that of the entries its token completes
+            self._pos = torch.full((B,), w.n_ctx - 1, dtype=torch.int64, device=dev)
         self.ws = {}
         self._size_workspaces()
 
@@ -105,6 +110,30 @@ class HybridStep:
         if self.w.kind in ("hybrid_decode", "parallel_decode"):
             return self.x["kc_h"]
         return self.x["kc"] if self.w.kind == "hca_decode" else self.buf["entries_h"]
+
+    def in_branch_csa(self, stream=None):
+        """RMSNorm + partial RoPE, in place, of the CSA branch's queries and of the entry this
+        step completed, both at the query's position (when the workload has the in-branch
+        operations; the block's entry takes the position of its last token, which is the
+        query's)."""
+        if not self.w.in_branch:
+            return
+        kc = self._csa_tensors()[0]
+        ops.rmsnorm_rope(self.x["q"], pos=self._pos, rows_per_pos=self.w.n_h, stream=stream)
+        ops.rmsnorm_rope(kc[:, self.w.n_csa - 1], pos=self._pos, stream=stream)
+
+    def in_branch_hca(self, stream=None):
+        """The same for the HCA branch's queries and its completed entry."""
+        if not self.w.in_branch:
+            return
+        ops.rmsnorm_rope(self._hca_q_kv()[0], pos=self._pos, rows_per_pos=self.w.n_h, stream=stream)
+        ops.rmsnorm_rope(self._hca_cache()[:, self.w.n_hca - 1], pos=self._pos, stream=stream)
+
+    def sink(self, branch: str):
+        """The branch's per-head attention-sink logits (None without the in-branch operations)."""
+        if not self.w.in_branch:
+            return None
+        return self.x["sink_h"] if branch == "hca" and self.w.kind == "hybrid_decode" else self.x["sink"]
 
     def _hca_q_kv(self):
         """The HCA branch's queries and window rows (its own in a hybrid step's HCA layer)."""
@@ -196,8 +225,9 @@ class HybridStep:
                              out_scale=kIs, dev_status=st, stream=stream)
         ops.csa_index_topk(x["qI"], x["w"], kI, m=w.m, k=w.k, q_pos0=w.q_pos0, qI_scale=x.get("qI_scale"),
                            kI_scale=kIs, idx=b["idx"], workspace=self.ws["index"], dev_status=st, stream=stream)
+        self.in_branch_csa(stream)
         ops.csa_attend(x["q"], kc, kc, b["idx"], scale=w.scale, o=b["o"], lse=b["lse"], workspace=self.ws["csa"],
-                       dev_status=st, stream=stream, window=self._win_csa(as_dict=True))
+                       dev_status=st, stream=stream, window=self._win_csa(as_dict=True), sink=self.sink("csa"))
         if not self.fuse_window:
             ops.swa_merge(x["q"], x["kv"], x["kv"], kv_pos0=self._kv_pos0(), q_pos0=w.q_pos0, n_win=w.n_win,
                           scale=w.scale, o_in=b["o"], lse_in=b["lse"], out=b["out"], dev_status=st,
@@ -216,8 +246,10 @@ class HybridStep:
                              dev_status=st, stream=stream)
         else:
             ops.hyb_compress(x["ch"], x["zh"], x["bias_h"], w.m_hca, out=kc, dev_status=st, stream=stream)
+        self.in_branch_hca(stream)
         ops.hca_attend(q, kc, kc, m=w.m_hca, q_pos0=w.q_pos0, scale=w.scale, o=b["o_h"], lse=b["lse_h"],
-                       workspace=self.ws["hca"], dev_status=st, stream=stream, window=self._win_hca(as_dict=True))
+                       workspace=self.ws["hca"], dev_status=st, stream=stream, window=self._win_hca(as_dict=True),
+                       sink=self.sink("hca"))
         if not self.fuse_window:
             ops.swa_merge(q, kv, kv, kv_pos0=self._kv_pos0(), q_pos0=w.q_pos0, n_win=w.n_win, scale=w.scale,
                           o_in=b["o_h"], lse_in=b["lse_h"], out=b["out_h"], dev_status=st, stream=stream)

@@ -14,7 +14,8 @@ Value recipe (every draw from a torch generator seeded with the workload's
 seed): compressed / raw KV values N(0,1)/sqrt(c) (N(0,1) in the float32 tiny
 workload); queries N(0,1); gating logits N(0,1); positional biases N(0,1);
 indexer queries and keys N(0,1) cast to e4m3 by torch (float32 in the tiny
-workload) with per-row scales U(0.5, 1.5); indexer head weights w U(0,1).
+workload) with per-row scales U(0.5, 1.5); indexer head weights w U(0,1);
+attention-sink logits N(0,1) (workloads with the in-branch operations).
 """
 from __future__ import annotations
 
@@ -54,6 +55,9 @@ class Workload:
     # indexer query/key format: "e4m3" (one float32 scale per row) or "mxfp4" (e2m1 pairs,
     # one e8m0 scale per 32 dims)
     idx_fmt: str = "e4m3"
+    # the in-branch operations in the step: RMSNorm + partial RoPE of the queries and of the
+    # entries the step completes, and a per-head attention sink on each branch's result
+    in_branch: bool = False
 
     @property
     def n_csa(self) -> int:
@@ -102,6 +106,10 @@ WORKLOADS = {
                                        c=512, m=4, k=1024, n_ih=64, c_I=128, m_hca=128, seed=1006),
     # Flash's first layers: sliding window only
     "flash_swa_decode": Workload("flash_swa_decode", "swa_decode", batch=8, n_ctx=65536, n_h=64, c=512, seed=1007, out_groups=8),
+    # the 1M decode with the in-branch operations (RMSNorm + partial RoPE, attention sinks)
+    "pro_1m_hybrid_decode_in_branch": Workload("pro_1m_hybrid_decode_in_branch", "hybrid_decode", batch=4,
+                                               n_ctx=1048576, n_h=128, c=512, m=4, k=1024, n_ih=64, c_I=128,
+                                               m_hca=128, seed=1009, in_branch=True),
     # the 1M decode with the indexer's queries and keys in MXFP4
     "pro_1m_hybrid_decode_fp4": Workload("pro_1m_hybrid_decode_fp4", "hybrid_decode", batch=4, n_ctx=1048576, n_h=128,
                                          c=512, m=4, k=1024, n_ih=64, c_I=128, m_hca=128, seed=1008, idx_fmt="mxfp4"),
@@ -171,6 +179,8 @@ def make_inputs(w: Workload, device="cpu") -> dict:
       hca_decode / hybrid_decode (HCA part, suffix _h in hybrid): cache kc_h
         [B,N',c]; raw rows ch, zh [B,m',c]; bias_h [m',c]; q_h [B,1,n_h,c];
         kv_h [B,n_win,c].
+      in-branch workloads, also: sink [n_h] float32 (sink_h for the HCA layer of a
+        hybrid step).
     """
     d = _Draw(w.seed, device)
     B, n, c, dt = w.batch, w.n_ctx, w.c, w.dtype
@@ -240,4 +250,9 @@ def make_inputs(w: Workload, device="cpu") -> dict:
         out["bias_h"] = d.normal((w.m_hca, c))
         queries(1, "_h" if sfx else "")
         out["kv" + sfx] = d.normal((B, w.n_win, c), kv_std, dt)
+    if w.in_branch:
+        # per-head attention-sink logits N(0,1), one set per layer
+        out["sink"] = d.normal((w.n_h,))
+        if w.kind == "hybrid_decode":
+            out["sink_h"] = d.normal((w.n_h,))
     return out

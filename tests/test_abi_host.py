@@ -214,7 +214,7 @@ def test_rmsnorm_rope_rejects_invalid_arguments(lib):
         return a
     for bad in (dict(c=63), dict(c=0), dict(dtype=_abi.HYB_E4M3), dict(rope_dims=66), dict(rope_dims=15),
                 dict(pos=None), dict(rows_per_pos=0), dict(theta=0.0), dict(eps=-1.0), dict(x=None), dict(x=FAKE + 4),
-                dict(pos=FAKE + 4), dict(rows=-1)):
+                dict(pos=FAKE + 4), dict(rows=-1), dict(row_stride=62), dict(row_stride=65)):
         assert lib.hyb_rmsnorm_rope(ctypes.byref(args(**bad)), None) == 1, bad
         assert lib.hyb_last_error()
     assert lib.hyb_rmsnorm_rope(ctypes.byref(args(rows=0)), None) == 0  # nothing to do, nothing launched
@@ -230,6 +230,10 @@ def test_binding_rejects_bad_sink_positions_and_gain_before_any_call():
     x = torch.zeros(6, 64)
     with pytest.raises(ValueError):
         ops.rmsnorm_rope(x, pos=torch.zeros(5, dtype=torch.int64))  # 6 rows need 6 positions
+    with pytest.raises(ValueError):
+        ops.rmsnorm_rope(torch.zeros(2, 6, 64)[:, 1:4])  # neither contiguous nor 2-D rows
+    with pytest.raises(ValueError):
+        ops.rmsnorm_rope(torch.zeros(64, 6).t())  # columns not unit-stride
     with pytest.raises(ValueError):
         ops.rmsnorm_rope(x, pos=torch.zeros(6, dtype=torch.int32))
     with pytest.raises(ValueError):

@@ -116,6 +116,56 @@ def test_pro_1m_hybrid_decode_full_size_unit_scale_values():
         _check_decode_hca(w, x, step, before, b, "_h")
 
 
+def _check_in_branch(w, x, step, q0, b, layer):
+    """One branch of the in-branch step for sequence b: the completed entry and the queries
+    RMS-normalised and rotated at the query's position, then the attention (with the window
+    merged) and the branch's sink, each stage fed the tensors the GPU stored before it."""
+    sl = slice(b, b + 1)
+    cpu = lambda k: x[k][sl].cpu()
+    t = w.n_ctx - 1
+    sfx = "" if layer == "csa" else "_h"
+    if layer == "csa":
+        N, kc_key = w.n_csa, "kc"
+        ent = oracle.compress(cpu("ca"), cpu("za"), x["bias"].cpu(), w.m, cb=cpu("cb"), zb=cpu("zb"), overlap=True,
+                              first_block=N - 2)[0, 0]
+    else:
+        N, kc_key = w.n_hca, "kc_h"
+        ent = oracle.compress(cpu("ch"), cpu("zh"), x["bias_h"].cpu(), w.m_hca, first_block=N - 1)[0, 0]
+    ent = oracle.rope_partial(oracle.rmsnorm(ent), t)
+    assert _bf16_close(to_np(x[kc_key][b, N - 1]), ent)
+    qn = oracle.rope_partial(oracle.rmsnorm(to_np(q0[sl])), t)
+    assert _bf16_close(to_np(x["q" + sfx][sl]), qn)
+    q, kc, kv = cpu("q" + sfx), cpu(kc_key), cpu("kv" + sfx)
+    if layer == "csa":
+        gidx = step.buf["idx"][sl].cpu().numpy()
+        s = oracle.index_scores(cpu("qI"), cpu("w"), cpu("kI"), m=w.m, q_pos0=t, qI_scale=cpu("qI_scale"),
+                                kI_scale=cpu("kI_scale"))
+        check_topk_row(gidx[0, 0], s[0, 0], N, w.k)
+        o, l = oracle.csa_attend(q, kc, kc, gidx, w.scale)
+    else:
+        o, l = oracle.hca_attend(q, kc, kc, m=w.m_hca, q_pos0=t, scale=w.scale)
+    out, lu = oracle.swa_merge(q, kv, kv, w.n_ctx - w.n_win, t, w.n_win, w.scale, o, l)
+    out, lu = oracle.sink_merge(out, lu, x["sink" + sfx].cpu())
+    assert_out_close(to_np(step.buf["out" + sfx][sl]), out)
+    assert max_abs(to_np(step.buf["lse" + sfx][sl]), lu) <= TOL_BF16
+
+
+def test_pro_1m_hybrid_decode_in_branch_full_size():
+    """The 1M hybrid decode with the in-branch operations as the benchmark times them:
+    RMSNorm + partial RoPE of both layers' queries and completed entries, and each
+    layer's per-head attention sink on its merged result."""
+    w = workloads.WORKLOADS["pro_1m_hybrid_decode_in_branch"]
+    x = workloads.make_inputs(w, DEV)
+    q0, q0_h = x["q"].clone(), x["q_h"].clone()
+    step = pipeline.HybridStep(w, x)
+    step.run()
+    torch.cuda.synchronize()
+    assert step.dev_status.item() == 0
+    for b in (0, w.batch - 1):
+        _check_in_branch(w, x, step, q0, b, "csa")
+        _check_in_branch(w, x, step, q0_h, b, "hca")
+
+
 def _proj_weights(seed, g, d_g, k):
     gen = torch.Generator()
     gen.manual_seed(seed)
