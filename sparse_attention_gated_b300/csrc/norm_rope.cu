@@ -8,6 +8,14 @@
 // then rotate the pairs of the last rope_dims dimensions.  The angle
 // pos * theta^(-2i/d) can reach 10^6 rad: it is formed in float64 and reduced
 // modulo 2 pi there, and only the reduced angle goes to float32 sin / cos.
+// Float64 is slow on this part, so the frequency theta^(-2i/d) is the host's
+// float64 base theta^(-2/d) raised to the integer i by repeated squaring (at
+// most 8 squarings), and the reduction subtracts k = rint(angle / 2 pi) times
+// 2 pi split into two float64 parts (Cody and Waite's additive reduction): a
+// few float64 operations per rotated pair instead of a general power and a
+// remainder.
+#include <cmath>
+
 #include "kernels.cuh"
 
 namespace hyb {
@@ -19,7 +27,7 @@ struct NormRopeParams {
   float eps;
   const int64_t* pos;
   int64_t rows_per_pos, rope_dims;
-  double theta;
+  double rope_base;    // theta^(-2 / rope_dims)
   int64_t row_stride;  // elements from one row to the next
 };
 
@@ -57,15 +65,23 @@ __global__ void __launch_bounds__(256) norm_rope_kernel(NormRopeParams p) {
   const float inv = rsqrtf(ss / (float)p.c + p.eps);
   const int64_t first_rot = (p.c - p.rope_dims) / 2;  // first rotated pair
   const double pos = p.rope_dims > 0 ? (double)p.pos[r / p.rows_per_pos] : 0.0;
-  const double two_pi = 6.283185307179586476925286766559;
+  // 2 pi = kTwoPiHi + kTwoPiLo (the float64 nearest 2 pi and the remainder)
+  constexpr double kTwoPiHi = 6.283185307179586232, kTwoPiLo = 2.4492935982947064e-16;
+  constexpr double kInvTwoPi = 0.15915494309189535;
   for (int64_t i = lane; i < n_pairs; i += 32) {
     float2 v = ld_pair<T>(x + 2 * i);
     const float g0 = p.gamma ? p.gamma[2 * i] : 1.f, g1 = p.gamma ? p.gamma[2 * i + 1] : 1.f;
     v.x = v.x * inv * g0;
     v.y = v.y * inv * g1;
     if (i >= first_rot) {
-      const double freq = pow(p.theta, -(double)(2 * (i - first_rot)) / (double)p.rope_dims);
-      const float ang = (float)fmod(pos * freq, two_pi);
+      double freq = 1.0, b = p.rope_base;
+      for (int64_t e = i - first_rot; e > 0; e >>= 1) {  // rope_base^(i - first_rot)
+        if (e & 1) freq *= b;
+        b *= b;
+      }
+      const double a = pos * freq;
+      const double k = rint(a * kInvTwoPi);
+      const float ang = (float)fma(-k, kTwoPiLo, fma(-k, kTwoPiHi, a));
       float sn, cs;
       sincosf(ang, &sn, &cs);
       v = make_float2(v.x * cs - v.y * sn, v.x * sn + v.y * cs);
@@ -77,7 +93,8 @@ __global__ void __launch_bounds__(256) norm_rope_kernel(NormRopeParams p) {
 cudaError_t launch_norm_rope(const hyb_norm_rope_args* a, cudaStream_t s) {
   NormRopeParams p;
   p.x = a->x, p.rows = a->rows, p.c = a->c, p.gamma = a->gamma, p.eps = a->eps, p.pos = a->pos;
-  p.rows_per_pos = a->rows_per_pos, p.rope_dims = a->rope_dims, p.theta = a->theta;
+  p.rows_per_pos = a->rows_per_pos, p.rope_dims = a->rope_dims;
+  p.rope_base = a->rope_dims > 0 ? std::pow(a->theta, -2.0 / (double)a->rope_dims) : 1.0;
   p.row_stride = a->row_stride > 0 ? a->row_stride : a->c;
   if (p.rows == 0) return cudaSuccess;
   const int64_t blocks = (p.rows + 7) / 8;
