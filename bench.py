@@ -827,7 +827,8 @@ def _csa_parts(st, stream, rec, scoring_events=None):
                        scores_events=scoring_events)
     rec("csa_index_topk", 1)
     rec("csa_attend", 0)
-    st.in_branch_csa(stream)
+    # the in-branch RMSNorm + RoPE: both layers' in one launch when the step has both
+    st.run_in_branch(stream, ("csa", "hca") if w.decode and st.has_hca else ("csa",))
     ops.csa_attend(x["q"], kc, kc, b["idx"], scale=w.scale, o=b["o"], lse=b["lse"], workspace=st.ws["csa"],
                    dev_status=s, stream=stream, window=st._win_csa(as_dict=True), sink=st.sink("csa"))
     rec("csa_attend", 1)
@@ -846,7 +847,8 @@ def _hca_parts(st, stream, rec):
                          dev_status=s, stream=stream)
     rec("hca_compress", 1)
     rec("hca_attend", 0)
-    st.in_branch_hca(stream)
+    if not st.has_csa:
+        st.run_in_branch(stream, ("hca",))
     ops.hca_attend(q, kc, kc, m=w.m_hca, q_pos0=w.q_pos0, scale=w.scale, o=b["o_h"], lse=b["lse_h"],
                    workspace=st.ws["hca"], dev_status=s, stream=stream, window=st._win_hca(as_dict=True),
                    sink=st.sink("hca"))
@@ -870,8 +872,8 @@ def _launches_per_step(w, proj=None):
     if w.kind in ("hybrid_decode", "hca_decode", "parallel_decode"):
         n += 1
     if w.in_branch:
-        # per branch: RMSNorm + RoPE of the queries and of the completed entry, the sink
-        n += 3 * ((w.kind in ("hybrid_decode", "csa_decode")) + (w.kind in ("hybrid_decode", "hca_decode")))
+        # RMSNorm + RoPE of the queries and the completed entries (one launch), a sink per layer
+        n += 1 + (w.kind in ("hybrid_decode", "csa_decode")) + (w.kind in ("hybrid_decode", "hca_decode"))
     if proj is not None:
         n += proj["calls"]
     return n

@@ -467,6 +467,13 @@ typedef struct hyb_norm_rope_args {
 
 HYB_API hyb_status hyb_rmsnorm_rope(const hyb_norm_rope_args* a, void* stream);
 
+/* Up to HYB_NORM_ROPE_BATCH_MAX calls of one dtype in one launch (the queries and the
+ * completed entries of a decode step's two layers, say): each call is validated as
+ * hyb_rmsnorm_rope validates it, before anything is launched; the calls' rows must not
+ * overlap.  n_calls 0 does nothing; calls are read on the host only. */
+#define HYB_NORM_ROPE_BATCH_MAX 4
+HYB_API hyb_status hyb_rmsnorm_rope_batch(const hyb_norm_rope_args* calls, int32_t n_calls, void* stream);
+
 /* ------------------------------------------------------------------------
  * hyb_grouped_out_proj -- grouped output projection ([HA] section V.3, core
  * attention and grouped output: the n_h heads are split into g groups of

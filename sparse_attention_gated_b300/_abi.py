@@ -89,6 +89,7 @@ SIGNATURES = {
     "swa_merge_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(SwaArgs)]),
     "swa_merge": (ctypes.c_int, [ctypes.POINTER(SwaArgs), _p, ctypes.c_size_t, _p]),
     "hyb_rmsnorm_rope": (ctypes.c_int, [ctypes.POINTER(NormRopeArgs), _p]),
+    "hyb_rmsnorm_rope_batch": (ctypes.c_int, [ctypes.POINTER(NormRopeArgs), ctypes.c_int32, _p]),
     "hyb_grouped_out_proj": (ctypes.c_int, [ctypes.POINTER(GprojArgs), _p]),
     "hyb_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "hyb_last_error": (ctypes.c_char_p, []),

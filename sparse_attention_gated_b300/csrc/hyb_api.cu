@@ -593,7 +593,7 @@ hyb_status hyb_grouped_out_proj(const hyb_gproj_args* a, void* stream) {
 
 // ---------------------------------------------------------- RMSNorm + RoPE
 
-hyb_status hyb_rmsnorm_rope(const hyb_norm_rope_args* a, void* stream) {
+static hyb_status check_norm_rope(const hyb_norm_rope_args* a) {
   if (!a) return fail(HYB_ERR_INVALID_ARG, "hyb_rmsnorm_rope: args is NULL");
   if (a->rows < 0 || a->c < 2 || a->c % 2 != 0)
     return fail(HYB_ERR_INVALID_ARG, "hyb_rmsnorm_rope: rows < 0 or c not even and >= 2");
@@ -610,7 +610,29 @@ hyb_status hyb_rmsnorm_rope(const hyb_norm_rope_args* a, void* stream) {
   if (!a->x) return fail(HYB_ERR_INVALID_ARG, "hyb_rmsnorm_rope: x is NULL");
   if (!aligned(a->x, 2 * elem_size(a->dtype)) || !aligned(a->gamma, 4) || !aligned(a->pos, 8))
     return fail(HYB_ERR_INVALID_ARG, "hyb_rmsnorm_rope: misaligned x/gamma/pos");
+  return ok();
+}
+
+hyb_status hyb_rmsnorm_rope(const hyb_norm_rope_args* a, void* stream) {
+  const hyb_status st = check_norm_rope(a);
+  if (st != HYB_OK || a->rows == 0) return st;
   return cuda_status(hyb::launch_norm_rope(a, static_cast<cudaStream_t>(stream)), "hyb_rmsnorm_rope");
+}
+
+hyb_status hyb_rmsnorm_rope_batch(const hyb_norm_rope_args* calls, int32_t n_calls, void* stream) {
+  static_assert(HYB_NORM_ROPE_BATCH_MAX == hyb::kNormRopeBatchMax, "batch size");
+  if (n_calls < 0 || n_calls > HYB_NORM_ROPE_BATCH_MAX)
+    return fail(HYB_ERR_INVALID_ARG, "hyb_rmsnorm_rope_batch: n_calls must be 0 .. HYB_NORM_ROPE_BATCH_MAX");
+  if (n_calls == 0) return ok();
+  if (!calls) return fail(HYB_ERR_INVALID_ARG, "hyb_rmsnorm_rope_batch: calls is NULL");
+  for (int32_t i = 0; i < n_calls; ++i) {
+    const hyb_status st = check_norm_rope(&calls[i]);
+    if (st != HYB_OK) return st;
+    if (calls[i].dtype != calls[0].dtype)
+      return fail(HYB_ERR_INVALID_ARG, "hyb_rmsnorm_rope_batch: the calls must share one dtype");
+  }
+  return cuda_status(hyb::launch_norm_rope_batch(calls, n_calls, static_cast<cudaStream_t>(stream)),
+                     "hyb_rmsnorm_rope_batch");
 }
 
 }  // extern "C"

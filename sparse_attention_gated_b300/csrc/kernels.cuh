@@ -35,6 +35,8 @@ cudaError_t launch_compress_batch(const hyb_compress_args* const* a, const int64
 
 // norm_rope.cu
 cudaError_t launch_norm_rope(const hyb_norm_rope_args* a, cudaStream_t s);
+constexpr int kNormRopeBatchMax = 4;
+cudaError_t launch_norm_rope_batch(const hyb_norm_rope_args* calls, int n, cudaStream_t s);
 
 // out_proj.cu (tcgen05 grouped output projection: bf16 in, F32 or BF16 out)
 bool out_proj_shape_supported(int64_t n_h, int64_t c, int64_t g, int64_t d_g);

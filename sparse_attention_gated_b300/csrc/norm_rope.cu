@@ -46,13 +46,9 @@ __device__ __forceinline__ void st_pair(__nv_bfloat16* p, float2 v) {
   *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(v.x, v.y);
 }
 
+// Row r of a call (one warp).
 template <typename T>
-__global__ void __launch_bounds__(256) norm_rope_kernel(NormRopeParams p) {
-  pdl_wait();
-  pdl_trigger();
-  const int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (r >= p.rows) return;
+__device__ __forceinline__ void norm_rope_row(const NormRopeParams& p, int64_t r, int lane) {
   T* x = static_cast<T*>(p.x) + r * p.row_stride;
   const int64_t n_pairs = p.c / 2;
   float ss = 0.f;
@@ -90,12 +86,66 @@ __global__ void __launch_bounds__(256) norm_rope_kernel(NormRopeParams p) {
   }
 }
 
-cudaError_t launch_norm_rope(const hyb_norm_rope_args* a, cudaStream_t s) {
+template <typename T>
+__global__ void __launch_bounds__(256) norm_rope_kernel(NormRopeParams p) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (r >= p.rows) return;
+  norm_rope_row<T>(p, r, threadIdx.x & 31);
+}
+
+// Several calls of one dtype in one launch: call i takes blocks [block_end[i-1], block_end[i]).
+struct NormRopeBatch {
+  NormRopeParams call[kNormRopeBatchMax];
+  int64_t block_end[kNormRopeBatchMax];
+  int n;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256) norm_rope_batch_kernel(NormRopeBatch b) {
+  pdl_wait();
+  pdl_trigger();
+  int i = 0;
+  while (i + 1 < b.n && (int64_t)blockIdx.x >= b.block_end[i]) ++i;
+  const int64_t blk = (int64_t)blockIdx.x - (i > 0 ? b.block_end[i - 1] : 0);
+  const NormRopeParams& p = b.call[i];
+  const int64_t r = (blk * blockDim.x + threadIdx.x) >> 5;
+  if (r >= p.rows) return;
+  norm_rope_row<T>(p, r, threadIdx.x & 31);
+}
+
+static NormRopeParams norm_rope_params(const hyb_norm_rope_args* a) {
   NormRopeParams p;
   p.x = a->x, p.rows = a->rows, p.c = a->c, p.gamma = a->gamma, p.eps = a->eps, p.pos = a->pos;
   p.rows_per_pos = a->rows_per_pos, p.rope_dims = a->rope_dims;
   p.rope_base = a->rope_dims > 0 ? std::pow(a->theta, -2.0 / (double)a->rope_dims) : 1.0;
   p.row_stride = a->row_stride > 0 ? a->row_stride : a->c;
+  return p;
+}
+
+cudaError_t launch_norm_rope_batch(const hyb_norm_rope_args* calls, int n, cudaStream_t s) {
+  NormRopeBatch b{};
+  int64_t blocks = 0;
+  b.n = 0;
+  for (int i = 0; i < n; ++i) {
+    if (calls[i].rows == 0) continue;
+    b.call[b.n] = norm_rope_params(&calls[i]);
+    blocks += (calls[i].rows + 7) / 8;
+    b.block_end[b.n] = blocks;
+    ++b.n;
+  }
+  if (b.n == 0) return cudaSuccess;
+  if (blocks >= (int64_t(1) << 31)) return cudaErrorInvalidConfiguration;
+  cudaError_t e = calls[0].dtype == HYB_F32
+                      ? launch_pdl(norm_rope_batch_kernel<float>, dim3((unsigned)blocks), dim3(256), 0, s, b)
+                      : launch_pdl(norm_rope_batch_kernel<__nv_bfloat16>, dim3((unsigned)blocks), dim3(256), 0, s, b);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_norm_rope(const hyb_norm_rope_args* a, cudaStream_t s) {
+  const NormRopeParams p = norm_rope_params(a);
   if (p.rows == 0) return cudaSuccess;
   const int64_t blocks = (p.rows + 7) / 8;
   if (blocks >= (int64_t(1) << 31)) return cudaErrorInvalidConfiguration;

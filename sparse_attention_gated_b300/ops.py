@@ -356,13 +356,9 @@ def swa_merge(q, kw, vw, *, kv_pos0: int = 0, q_pos0: int = 0, n_win: int, scale
 # ------------------------------------------------------------ RMSNorm + RoPE
 
 
-def rmsnorm_rope(x, *, gamma=None, eps: float = 1e-6, pos=None, rows_per_pos: int = 1, rope_dims: int = 64,
-                 theta: float = 10000.0, stream=None):
-    """In place: RMSNorm of every row of x [..., c] (float32 or bf16), then rotary
-    encoding of its last rope_dims dimensions at positions pos (int64, one per
-    rows_per_pos consecutive rows; rope_dims=0 or pos=None: no rotation).  x is
-    contiguous, or a 2-D view [rows, c] of unit column stride whose rows are evenly
-    spaced (e.g. one cache slot of every sequence).  Returns x."""
+def rmsnorm_rope_args(x, *, gamma=None, eps: float = 1e-6, pos=None, rows_per_pos: int = 1, rope_dims: int = 64,
+                      theta: float = 10000.0):
+    """Argument struct of hyb_rmsnorm_rope for x (see rmsnorm_rope)."""
     c = x.shape[-1]
     rows = x.numel() // c
     row_stride = 0
@@ -382,8 +378,28 @@ def rmsnorm_rope(x, *, gamma=None, eps: float = 1e-6, pos=None, rows_per_pos: in
     a.pos, a.rows_per_pos = _ptr(pos), rows_per_pos
     a.rope_dims, a.theta = (rope_dims if pos is not None else 0), theta
     a.row_stride = row_stride
+    return a
+
+
+def rmsnorm_rope(x, *, gamma=None, eps: float = 1e-6, pos=None, rows_per_pos: int = 1, rope_dims: int = 64,
+                 theta: float = 10000.0, stream=None):
+    """In place: RMSNorm of every row of x [..., c] (float32 or bf16), then rotary
+    encoding of its last rope_dims dimensions at positions pos (int64, one per
+    rows_per_pos consecutive rows; rope_dims=0 or pos=None: no rotation).  x is
+    contiguous, or a 2-D view [rows, c] of unit column stride whose rows are evenly
+    spaced (e.g. one cache slot of every sequence).  Returns x."""
+    a = rmsnorm_rope_args(x, gamma=gamma, eps=eps, pos=pos, rows_per_pos=rows_per_pos, rope_dims=rope_dims,
+                          theta=theta)
     _abi.check(_abi.load().hyb_rmsnorm_rope(ctypes.byref(a), _stream(stream)), "hyb_rmsnorm_rope")
     return x
+
+
+def rmsnorm_rope_batch(calls, stream=None):
+    """Several RMSNorm + RoPE calls of one dtype in one launch (hyb_rmsnorm_rope_batch):
+    calls is a list of argument structs from rmsnorm_rope_args, at most
+    HYB_NORM_ROPE_BATCH_MAX."""
+    arr = (_abi.NormRopeArgs * max(1, len(calls)))(*calls)
+    _abi.check(_abi.load().hyb_rmsnorm_rope_batch(arr, len(calls), _stream(stream)), "hyb_rmsnorm_rope_batch")
 
 
 # ---------------------------------------------------- grouped output projection

@@ -111,23 +111,28 @@ class HybridStep:
             return self.x["kc_h"]
         return self.x["kc"] if self.w.kind == "hca_decode" else self.buf["entries_h"]
 
-    def in_branch_csa(self, stream=None):
-        """RMSNorm + partial RoPE, in place, of the CSA branch's queries and of the entry this
-        step completed, both at the query's position (when the workload has the in-branch
-        operations; the block's entry takes the position of its last token, which is the
-        query's)."""
-        if not self.w.in_branch:
-            return
-        kc = self._csa_tensors()[0]
-        ops.rmsnorm_rope(self.x["q"], pos=self._pos, rows_per_pos=self.w.n_h, stream=stream)
-        ops.rmsnorm_rope(kc[:, self.w.n_csa - 1], pos=self._pos, stream=stream)
+    def in_branch_args(self, branch: str):
+        """RMSNorm + partial RoPE calls of a branch ("csa" or "hca"): its queries and the entry
+        this step completed, both at the query's position (the block's entry takes the
+        position of its last token, which is the query's)."""
+        w = self.w
+        if branch == "csa":
+            q, entry = self.x["q"], self._csa_tensors()[0][:, w.n_csa - 1]
+        else:
+            q, entry = self._hca_q_kv()[0], self._hca_cache()[:, w.n_hca - 1]
+        return [ops.rmsnorm_rope_args(q, pos=self._pos, rows_per_pos=w.n_h),
+                ops.rmsnorm_rope_args(entry, pos=self._pos)]
 
-    def in_branch_hca(self, stream=None):
-        """The same for the HCA branch's queries and its completed entry."""
+    def run_in_branch(self, stream=None, branches=("csa", "hca")):
+        """The in-branch RMSNorm + RoPE of the given branches, in place, as one launch (when
+        the workload has the in-branch operations)."""
         if not self.w.in_branch:
             return
-        ops.rmsnorm_rope(self._hca_q_kv()[0], pos=self._pos, rows_per_pos=self.w.n_h, stream=stream)
-        ops.rmsnorm_rope(self._hca_cache()[:, self.w.n_hca - 1], pos=self._pos, stream=stream)
+        calls = []
+        for br in branches:
+            if (br == "csa" and self.has_csa) or (br == "hca" and self.has_hca):
+                calls += self.in_branch_args(br)
+        ops.rmsnorm_rope_batch(calls, stream=stream)
 
     def sink(self, branch: str):
         """The branch's per-head attention-sink logits (None without the in-branch operations)."""
@@ -205,7 +210,7 @@ class HybridStep:
         if calls:
             ops.hyb_compress_batch(calls, stream=stream)
 
-    def run_csa(self, stream=None, compress=True):
+    def run_csa(self, stream=None, compress=True, in_branch=True):
         w, x, b = self.w, self.x, self.buf
         kc, kI, kIs = self._csa_tensors()
         st = self.dev_status
@@ -225,7 +230,8 @@ class HybridStep:
                              out_scale=kIs, dev_status=st, stream=stream)
         ops.csa_index_topk(x["qI"], x["w"], kI, m=w.m, k=w.k, q_pos0=w.q_pos0, qI_scale=x.get("qI_scale"),
                            kI_scale=kIs, idx=b["idx"], workspace=self.ws["index"], dev_status=st, stream=stream)
-        self.in_branch_csa(stream)
+        if in_branch:
+            self.run_in_branch(stream, ("csa",))
         ops.csa_attend(x["q"], kc, kc, b["idx"], scale=w.scale, o=b["o"], lse=b["lse"], workspace=self.ws["csa"],
                        dev_status=st, stream=stream, window=self._win_csa(as_dict=True), sink=self.sink("csa"))
         if not self.fuse_window:
@@ -233,7 +239,7 @@ class HybridStep:
                           scale=w.scale, o_in=b["o"], lse_in=b["lse"], out=b["out"], dev_status=st,
                           stream=stream)
 
-    def run_hca(self, stream=None, compress=True):
+    def run_hca(self, stream=None, compress=True, in_branch=True):
         w, x, b = self.w, self.x, self.buf
         st = self.dev_status
         kc = self._hca_cache()
@@ -246,7 +252,8 @@ class HybridStep:
                              dev_status=st, stream=stream)
         else:
             ops.hyb_compress(x["ch"], x["zh"], x["bias_h"], w.m_hca, out=kc, dev_status=st, stream=stream)
-        self.in_branch_hca(stream)
+        if in_branch:
+            self.run_in_branch(stream, ("hca",))
         ops.hca_attend(q, kc, kc, m=w.m_hca, q_pos0=w.q_pos0, scale=w.scale, o=b["o_h"], lse=b["lse_h"],
                        workspace=self.ws["hca"], dev_status=st, stream=stream, window=self._win_hca(as_dict=True),
                        sink=self.sink("hca"))
@@ -285,10 +292,11 @@ class HybridStep:
         batched = self.w.decode and self.has_csa and self.has_hca
         if batched:
             self.run_compress(stream)
+            self.run_in_branch(stream)  # both layers' queries and entries, one launch
         if self.has_csa:
-            self.run_csa(stream, compress=not batched)
+            self.run_csa(stream, compress=not batched, in_branch=not batched)
         if self.has_hca:
-            self.run_hca(stream, compress=not batched)
+            self.run_hca(stream, compress=not batched, in_branch=not batched)
         self.run_proj(stream)
 
     # ------------------------------------------------------------ e2e view

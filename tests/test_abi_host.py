@@ -220,6 +220,25 @@ def test_rmsnorm_rope_rejects_invalid_arguments(lib):
     assert lib.hyb_rmsnorm_rope(ctypes.byref(args(rows=0)), None) == 0  # nothing to do, nothing launched
 
 
+def test_rmsnorm_rope_batch_validates_every_call_before_any_launch(lib):
+    def args(**kw):
+        a = _abi.NormRopeArgs()
+        a.x, a.rows, a.c, a.eps, a.dtype = FAKE, 4, 64, 1e-6, _abi.HYB_F32
+        a.pos, a.rows_per_pos, a.rope_dims, a.theta = FAKE, 1, 16, 10000.0
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return a
+    def call(*calls, n=None):
+        arr = (_abi.NormRopeArgs * max(1, len(calls)))(*calls)
+        return lib.hyb_rmsnorm_rope_batch(arr, len(calls) if n is None else n, None)
+    assert call(n=0) == 0  # nothing to do
+    assert call(args(), n=5) == 1 and call(args(), n=-1) == 1
+    assert call(args(), args(c=63)) == 1  # an invalid member
+    assert call(args(), args(dtype=_abi.HYB_BF16)) == 1  # mixed dtypes
+    assert call(args(rows=0), args(rows=0)) == 0  # nothing launched
+    assert lib.hyb_rmsnorm_rope_batch(None, 1, None) == 1
+
+
 def test_binding_rejects_bad_sink_positions_and_gain_before_any_call():
     from sparse_attention_gated_b300 import ops
     q = torch.zeros(1, 1, 4, 64)

@@ -47,3 +47,29 @@ def test_rmsnorm_only_without_positions():
     y = ops.rmsnorm_rope(x.to(DEV), eps=0.0, pos=None)
     torch.cuda.synchronize()
     assert max_abs(to_np(y), oracle.rmsnorm(x.double().numpy(), eps=0.0)) <= 2e-5
+
+
+def test_strided_rows_and_the_batched_call_match_the_oracle():
+    """One cache slot of every sequence (rows N*c apart) and a query block, normalised and
+    rotated as one batched launch: each against the oracle, the rows around the slot
+    untouched, and bit for bit the same as the two calls made separately."""
+    g = torch.Generator().manual_seed(93)
+    B, N, n_h, c, slot = 4, 50, 16, 512, 37
+    cache = (torch.randn(B, N, c, generator=g) * 0.05).to(torch.bfloat16).to(DEV)
+    q = (torch.randn(B, 1, n_h, c, generator=g) * 2.0).to(torch.bfloat16).to(DEV)
+    pos = torch.randint(0, 1 << 20, (B,), generator=g, dtype=torch.int64).to(DEV)
+    cache0, q0 = cache.clone(), q.clone()
+    ops.rmsnorm_rope_batch([ops.rmsnorm_rope_args(q, pos=pos, rows_per_pos=n_h),
+                            ops.rmsnorm_rope_args(cache[:, slot], pos=pos)])
+    c2, q2 = cache0.clone(), q0.clone()
+    ops.rmsnorm_rope(q2, pos=pos, rows_per_pos=n_h)
+    ops.rmsnorm_rope(c2[:, slot], pos=pos)
+    torch.cuda.synchronize()
+    assert torch.equal(cache, c2) and torch.equal(q, q2)
+    keep = [s for s in range(N) if s != slot]
+    assert torch.equal(cache[:, keep], cache0[:, keep])
+    p = pos.cpu().double().numpy()
+    ref_e = oracle.rope_partial(oracle.rmsnorm(to_np(cache0[:, slot])), p)
+    assert max_abs(to_np(cache[:, slot]), ref_e) <= 2e-2 * max(1.0, float(np.abs(ref_e).max()))
+    ref_q = oracle.rope_partial(oracle.rmsnorm(to_np(q0).reshape(B * n_h, c)), np.repeat(p, n_h))
+    assert max_abs(to_np(q).reshape(B * n_h, c), ref_q) <= 2e-2 * max(1.0, float(np.abs(ref_q).max()))
