@@ -116,6 +116,7 @@ struct H128Params {
   float scale_log2;
   int32_t* dev_status;
   long long wait_cycles;
+  const float* sink;  // optional per-head sink logits [n_h] (natural log), joined to the final result
 };
 
 struct H128Work {
@@ -135,6 +136,22 @@ __device__ __forceinline__ float ex2_sfu(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// The final normaliser of a head whose softmax has base-2 maximum m and sum l (l = 0: no
+// entry), with the head's sink logit s (natural log; -inf = none) as one more term of the
+// denominator with no value: returns the factor that replaces 1 / l on the accumulated
+// output and writes the union's natural-log lse (no entry: output 0, lse = s).
+__device__ __forceinline__ float sink_normaliser(float m, float l, float s, float& lse) {
+  if (!(l > 0.f)) {
+    lse = s;
+    return 0.f;
+  }
+  const float s2 = s * kLog2e;
+  const float M = fmaxf(m, s2);
+  const float a = ex2_sfu(m - M), den = fmaf(l, a, ex2_sfu(s2 - M));
+  lse = (M + __log2f(den)) * kLn2;
+  return a / den;
 }
 
 template <int MODE>
@@ -662,7 +679,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (ok) {
       // one split: the normalised output of this half (float32 o, or with a window the
       // merged out in its own type) and the lse
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      float lse_h = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+      const float inv = p.sink ? sink_normaliser(m, l, p.sink[W.hg * kH + h], lse_h) : (l > 0.f ? 1.f / l : 0.f);
       const int64_t at = (qrow + h) * kC + 256 * W.dh;
       const bool to_bf16 = p.win && p.out_bf16;
       float* dst = p.win ? static_cast<float*>(p.out) + at : p.o + at;
@@ -690,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 make_float4(v[4 * x] * inv, v[4 * x + 1] * inv, v[4 * x + 2] * inv, v[4 * x + 3] * inv);
         }
       }
-      if (W.dh == 0) p.lse[qrow + h] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+      if (W.dh == 0) p.lse[qrow + h] = lse_h;
     }
     if (!ok && *s_abort == 0) *s_abort = 11;
   }
@@ -805,10 +823,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
+        float lse_h = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
+        const float inv = p.sink ? sink_normaliser(M, L, p.sink[W.hg * kH + hh], lse_h) : (L > 0.f ? 1.f / L : 0.f);
 #pragma unroll
         for (int x = 0; x < 8; ++x) acc[x] *= inv;
-        if (W.dh == 0 && oct == 0) p.lse[qrow + hh] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
+        if (W.dh == 0 && oct == 0) p.lse[qrow + hh] = lse_h;
         const int64_t at = (qrow + hh) * kC + 256 * W.dh + 8 * oct;
         if (p.win && p.out_bf16) {
           *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + at) =
@@ -908,6 +927,7 @@ cudaError_t launch_attend_h128(const AttendJob& j, void* ws, cudaStream_t s) {
   p.wq_pos = j.wq_pos, p.w_pos0s = j.w_pos0s;
   p.scale_log2 = j.scale * kLog2e;
   p.dev_status = j.dev_status;
+  p.sink = j.sink;
   p.wait_cycles = grid_wait_cycles();
   const int64_t rows = j.batch * j.n_q;
   const int64_t units = rows * p.n_hg * 2;

@@ -376,11 +376,18 @@ static cudaError_t launch_attend(const hyb::AttendJob& j, void* ws, cudaStream_t
   return hyb::launch_attend_cc(j, static_cast<char*>(ws) + join_region(j), s);
 }
 
-static hyb_status run_attend(const char* name, const hyb::AttendJob& j, void* workspace, size_t ws_bytes, void* stream) {
+// sink / sink_done: a per-head sink that the launched kernel joins to its final result
+// where it can (the 128-head kernel); *sink_done says whether it did.
+static hyb_status run_attend(const char* name, hyb::AttendJob j, void* workspace, size_t ws_bytes, void* stream,
+                             const float* sink = nullptr, bool* sink_done = nullptr) {
   const size_t need = attend_workspace(j);
   if (need > 0 && (!workspace || ws_bytes < need))
     return fail(HYB_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", name, need, ws_bytes);
   if (!aligned(workspace, 256)) return fail(HYB_ERR_WORKSPACE, "%s: workspace must be 256-byte aligned", name);
+  if (sink && use_h128(j)) {
+    j.sink = sink;
+    *sink_done = true;
+  }
   return cuda_status(launch_attend(j, workspace, static_cast<cudaStream_t>(stream)), name);
 }
 
@@ -446,14 +453,18 @@ static hyb_status validate_window(const char* name, const hyb::AttendJob& c, con
 
 // c: the compressed-branch job (its o unused), lse: the union's lse
 static hyb_status run_attend_window(const char* name, hyb::AttendJob c, const hyb_window* w, void* workspace,
-                                    size_t ws_bytes, void* stream) {
+                                    size_t ws_bytes, void* stream, const float* sink = nullptr,
+                                    bool* sink_done = nullptr) {
   const size_t need = attend_window_workspace(c, w);
   if (need > 0 && (!workspace || ws_bytes < need))
     return fail(HYB_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", name, need, ws_bytes);
   if (!aligned(workspace, 256)) return fail(HYB_ERR_WORKSPACE, "%s: workspace must be 256-byte aligned", name);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const hyb::AttendJob f = fused_job(c, w);
-  if (use_h128(f)) return cuda_status(hyb::launch_attend_h128(f, workspace, s), name);
+  hyb::AttendJob f = fused_job(c, w);
+  if (use_h128(f)) {
+    if (sink) f.sink = sink, *sink_done = true;
+    return cuda_status(hyb::launch_attend_h128(f, workspace, s), name);
+  }
   if (hyb::attend_tc_supported(f)) return cuda_status(hyb::launch_attend_tc(f, workspace, s), name);
   // two steps: the compressed branch into the workspace (after the kernels' own
   // scratch, which keeps the join counters first), then the window merge
@@ -498,9 +509,10 @@ hyb_status csa_attend(const hyb_csa_attend_args* a, void* workspace, size_t ws_b
     return fail(HYB_ERR_INVALID_ARG, "csa_attend: NULL o/lse/idx");
   if (!aligned(a->o, lane_align(a->c, HYB_F32)) || !aligned(a->idx, 4) || !aligned(a->lse, 4) || !aligned(a->sink, 4))
     return fail(HYB_ERR_INVALID_ARG, "csa_attend: misaligned o/lse/idx/sink");
-  st = a->window ? run_attend_window("csa_attend", csa_job(a), a->window, workspace, ws_bytes, stream)
-                 : run_attend("csa_attend", csa_job(a), workspace, ws_bytes, stream);
-  if (st != HYB_OK || !a->sink) return st;
+  bool sink_done = false;
+  st = a->window ? run_attend_window("csa_attend", csa_job(a), a->window, workspace, ws_bytes, stream, a->sink, &sink_done)
+                 : run_attend("csa_attend", csa_job(a), workspace, ws_bytes, stream, a->sink, &sink_done);
+  if (st != HYB_OK || !a->sink || sink_done) return st;
   return apply_sink("csa_attend", a->window, a->o, a->lse, a->sink, a->batch * a->n_q, a->n_h, a->c, stream);
 }
 
@@ -526,9 +538,10 @@ hyb_status hca_attend(const hyb_hca_attend_args* a, void* workspace, size_t ws_b
   if ((!a->o && !a->window) || !a->lse) return fail(HYB_ERR_INVALID_ARG, "hca_attend: NULL o/lse");
   if (!aligned(a->o, lane_align(a->c, HYB_F32)) || !aligned(a->lse, 4) || !aligned(a->sink, 4))
     return fail(HYB_ERR_INVALID_ARG, "hca_attend: misaligned o/lse/sink");
-  st = a->window ? run_attend_window("hca_attend", hca_job(a), a->window, workspace, ws_bytes, stream)
-                 : run_attend("hca_attend", hca_job(a), workspace, ws_bytes, stream);
-  if (st != HYB_OK || !a->sink) return st;
+  bool sink_done = false;
+  st = a->window ? run_attend_window("hca_attend", hca_job(a), a->window, workspace, ws_bytes, stream, a->sink, &sink_done)
+                 : run_attend("hca_attend", hca_job(a), workspace, ws_bytes, stream, a->sink, &sink_done);
+  if (st != HYB_OK || !a->sink || sink_done) return st;
   return apply_sink("hca_attend", a->window, a->o, a->lse, a->sink, a->batch * a->n_q, a->n_h, a->c, stream);
 }
 

@@ -102,6 +102,9 @@ struct AttendJob {
   const int64_t* kv_pos0s;
   const int64_t* wq_pos;
   const int64_t* w_pos0s;
+  // optional per-head sink logits [n_h] joined to the final result by the kernels that
+  // write it (the 128-head kernel); NULL = none
+  const float* sink;
 };
 bool attend_cc_shape_supported(int64_t c, int64_t n_h);
 

@@ -104,3 +104,33 @@ def test_sink_of_minus_infinity_changes_nothing():
     o1, l1 = ops.csa_attend(*args, sink=torch.full((n_h,), -math.inf, device=DEV))
     torch.cuda.synchronize()
     assert torch.equal(o0, o1) and torch.equal(l0, l1)
+
+
+@pytest.mark.parametrize("n_q,window", [(80, False), (80, True), (1, False), (1, True)])
+def test_sink_joined_by_the_128_head_kernel(n_q, window):
+    """128 heads: the sink is joined where the kernel writes its final result, in one split
+    per (query, half) when the queries fill the GPU (80 queries x 2 halves) and in the split
+    join otherwise (one query, a long list); with and without the fused window, and a query
+    with an empty list (no window: output 0, lse = the sink)."""
+    B, n_h, c, N, k, n_win, q0 = 1, 128, 512, 4000, 1024, 128, 50
+    g = torch.Generator().manual_seed(87)
+    q = torch.randn(B, n_q, n_h, c, generator=g).to(torch.bfloat16)
+    kc = torch.randn(B, N, c, generator=g).to(torch.bfloat16)  # unit scale: outputs of order 0.1-1
+    kv = torch.randn(B, q0 + n_q, c, generator=g).to(torch.bfloat16)
+    sink = torch.randn(n_h, generator=g) * 2.0 + 3.0
+    idx = torch.stack([torch.sort(torch.randperm(N, generator=g)[:k]).values for _ in range(n_q)])[None].int()
+    if n_q > 7:
+        idx[0, 7, :] = -1
+    scale = 1.0 / math.sqrt(c)
+    win = dict(kw=kv.to(DEV), kv_pos0=0, q_pos0=q0, n_win=n_win) if window else None
+    o, lse = ops.csa_attend(q.to(DEV), kc.to(DEV), kc.to(DEV), idx.to(DEV), scale=scale, sink=sink.to(DEV),
+                            window=win)
+    torch.cuda.synchronize()
+    ro, rl = oracle.csa_attend(q, kc, kc, idx.numpy(), scale)
+    if window:
+        ro, rl = oracle.swa_merge(q, kv, kv, 0, q0, n_win, scale, ro, rl)
+    ref, ref_l = oracle.sink_merge(ro, rl, sink.double().numpy())
+    assert _close(to_np(o), ref, TOL_BF16)
+    assert max_abs(to_np(lse), ref_l) <= TOL_BF16
+    if n_q > 7 and not window:
+        assert np.all(to_np(o)[0, 7] == 0) and np.allclose(to_np(lse)[0, 7], sink.numpy(), atol=1e-6)
