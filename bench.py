@@ -872,8 +872,11 @@ def _launches_per_step(w, proj=None):
     if w.kind in ("hybrid_decode", "hca_decode", "parallel_decode"):
         n += 1
     if w.in_branch:
-        # RMSNorm + RoPE of the queries and the completed entries (one launch), a sink per layer
-        n += 1 + (w.kind in ("hybrid_decode", "csa_decode")) + (w.kind in ("hybrid_decode", "hca_decode"))
+        # RMSNorm + RoPE of the queries and the completed entries (one launch); the sinks ride in
+        # the 128-head attention launches, other head counts add a sink launch per layer
+        n += 1
+        if w.n_h % 128 != 0:
+            n += (w.kind in ("hybrid_decode", "csa_decode")) + (w.kind in ("hybrid_decode", "hca_decode"))
     if proj is not None:
         n += proj["calls"]
     return n
